@@ -1,0 +1,430 @@
+"""W12 GEMM benchmark on GB300.
+
+Metric: W12 GEMM weight-GB/s (bytes of packed W12 weights streamed per second)
+and the fraction of the HBM roofline, on the four GEMMs of a 27B-class dense
+decoder layer (QKV 5120->7168, O 5120->5120, gate/up 5120->34816,
+down 17408->5120).
+
+One step = the four layer GEMMs at each of M = 1, 2, 4, 8 (16 launches of
+w12_gemm), weights resident in HBM as W12, synthetic BF16 activations.  The
+per-step working set (4 x 496 MB of W12) is larger than the 129 MB L2 and the
+layers are visited round-robin, so every weight tensor is re-read only after
+at least 228 MB of other weights have passed through L2.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_VALUES = (1, 2, 4, 8)
+SWEEP_M = (16,)
+METRIC = "W12 GEMM weight-GB/s & % HBM roofline at M=1/16/64 (27B-class layers)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1940.8)), "measured"
+    return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lossless_bit_weight_02_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.startswith("w12_gemm_mma") or fn == "w12_device.cuh":
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(shape_bytes):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemm_mma_dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    ratio = d.get("traffic_over_algorithmic")
+    return None if ratio is None else ratio * shape_bytes
+
+
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic_bytes(t, M: int) -> int:
+    """W12 bytes + activations read + outputs written."""
+    return t.nbytes() + 2 * M * t.K + 2 * M * t.N
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import lossless_bit_weight_02_gb300 as w12
+    from lossless_bit_weight_02_gb300 import synth
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, peak_src = peaks()
+
+    # ---- resident W12 layer (encoded and verified on the GPU) ----
+    layers = []
+    for i, (name, N, K) in enumerate(synth.LAYER_SHAPES):
+        Wd = synth.dense_weights_device(N, K, seed=1000 + i, device=dev)
+        t = w12.w12_encode(Wd)
+        st, nm = w12.w12_verify_roundtrip(Wd, t)
+        assert st == w12.W12_OK, (name, st, nm)
+        del Wd
+        layers.append((name, t))
+    torch.cuda.empty_cache()
+    Ms = sorted(set(M_VALUES) | set(SWEEP_M))
+    acts = {(M, name): synth.activations_device(M, t.K, seed=2000 + 10 * M + i, device=dev)
+            for M in Ms for i, (name, t) in enumerate(layers)}
+    outs = {(M, name): torch.empty(M, t.N, dtype=torch.bfloat16, device=dev)
+            for M in Ms for name, t in layers}
+    wsp = w12.Workspace(dev, max(w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in Ms for _, t in layers))
+    stream = torch.cuda.current_stream(dev)
+    wsp.ensure(max(w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in Ms for _, t in layers))
+    calls = {(M, name): w12.GemmCall(acts[(M, name)], t, outs[(M, name)], wsp, stream=stream)
+             for M in Ms for name, t in layers}
+
+    def one_step(ev=None, m_values=M_VALUES):
+        j = 0
+        for M in m_values:
+            for name, t in layers:
+                if ev is not None:
+                    ev[j][0].record(stream)
+                calls[(M, name)]()
+                if ev is not None:
+                    ev[j][1].record(stream)
+                j += 1
+
+    launches_per_step = len(M_VALUES) * len(layers)
+    step_bytes = sum(t.nbytes() for _, t in layers) * len(M_VALUES)
+    alg_bytes = {(M, name): algorithmic_bytes(t, M) for M in Ms for name, t in layers}
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    # per-launch events for (up to) the first 400 timed steps
+    n_ev = min(args.steps, 400)
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(launches_per_step)] for _ in range(n_ev)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws_n > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        one_step(evs[k] if k < n_ev else None)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if ws_n > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(stop)
+    if ws_n > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # per-launch kernel durations -> per (M, layer) and overall
+    dur = {}
+    j = 0
+    for M in M_VALUES:
+        for name, _ in layers:
+            dur[(M, name)] = [evs[k][j][0].elapsed_time(evs[k][j][1]) for k in range(n_ev)]
+            j += 1
+    kern_ms = sum(sum(v) for v in dur.values())
+    kern_bytes = sum(alg_bytes[key] * len(v) for key, v in dur.items())
+    achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
+    per_m = {}
+    for M in M_VALUES:
+        b = sum(layers_t.nbytes() for _, layers_t in layers)
+        ms = sum(statistics.median(dur[(M, name)]) for name, _ in layers)
+        per_m[str(M)] = {"weight_gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                         "roofline_frac": round(sum(alg_bytes[(M, n)] for n, _ in layers) / (ms * 1e-3) / 1e9
+                                                / hbm_peak, 4)}
+    per_layer = {name: round(statistics.median(dur[(1, name)]) * 1e3, 2) for name, _ in layers}
+
+    # ---- M = 16 (tree / batch verification), timed the same way ----
+    sweep = {}
+    for M in SWEEP_M:
+        ev2 = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in range(len(layers))]
+        ts = []
+        for _ in range(max(3, args.warmup)):
+            one_step(None, (M,))
+        for _ in range(50):
+            one_step(ev2, (M,))
+            torch.cuda.synchronize()
+            ts.append(sum(e[0].elapsed_time(e[1]) for e in ev2))
+        ms = statistics.median(ts)
+        b = sum(t.nbytes() for _, t in layers)
+        ab = sum(alg_bytes[(M, n)] for n, _ in layers)
+        sweep[str(M)] = {"weight_gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                         "roofline_frac": round(ab / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
+
+    # ---- end to end through the public API with host buffers ----
+    h_in = {key: a.cpu().pin_memory() for key, a in acts.items() if key[0] in M_VALUES}
+    h_out = {key: torch.empty(o.shape, dtype=o.dtype).pin_memory() for key, o in outs.items()
+             if key[0] in M_VALUES}
+    d_in = {key: torch.empty_like(a) for key, a in acts.items() if key[0] in M_VALUES}
+    e2e_calls = {key: w12.GemmCall(d_in[key], t, outs[key], wsp, stream=stream)
+                 for key in d_in for name, t in layers if name == key[1]}
+    h2d = sum(a.numel() * 2 for a in h_in.values())
+    d2h = sum(o.numel() * 2 for o in h_out.values())
+
+    def e2e_step():
+        for M in M_VALUES:
+            for name, t in layers:
+                d_in[(M, name)].copy_(h_in[(M, name)], non_blocking=True)
+                e2e_calls[(M, name)]()
+                h_out[(M, name)].copy_(outs[(M, name)], non_blocking=True)
+
+    e2e_steps = max(10, min(args.steps, 500))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    value = step_bytes * args.steps * ws_n / (total_ms * 1e-3) / 1e9
+    e2e_val = step_bytes * e2e_steps * ws_n / (e2e_ms * 1e-3) / 1e9
+    top_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers) / launches_per_step
+    traffic = ncu_traffic(top_bytes)
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian weights with LogNormal(0,0.5) channel scale, 0.1% zeros, "
+                "0.05% x2^9 outliers; N(0,1) activations)",
+        "config": {"workload": "27B-class decoder layer GEMMs (QKV 7168x5120, O 5120x5120, gate/up "
+                               "34816x5120, down 5120x17408), M in {1,2,4,8}, W12 weights resident",
+                   "global_batch": list(M_VALUES), "parallelism": f"replica x{ws_n} (N-sharding not needed)",
+                   "l2": "inputs larger than L2 (496 MB W12 per layer pass, layers round-robin)",
+                   "bits_per_weight": round(sum(t.nbytes() for _, t in layers) * 8 /
+                                            sum(t.N * t.K for _, t in layers), 4)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)"},
+        "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep,
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(layers, budget_s=args.cpu_seconds)
+    if ws_n > 1:
+        dist.destroy_process_group()
+    return rank, result
+
+
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """The oracle (decode + FP64 dot products, OpenMP over rows) on a bounded
+    sample of the same workload: the first `rows` rows of each layer shape at
+    M = 1, 2, 4, 8.  Encoding is done once per sample size, outside timing."""
+
+    def __init__(self):
+        import oracle
+        from lossless_bit_weight_02_gb300 import synth
+        oracle.build()
+        self.oracle, self.synth = oracle, synth
+        self.cache = {}
+
+    def _prepared(self, rows):
+        if rows not in self.cache:
+            items = []
+            for i, (name, N, K) in enumerate(self.synth.LAYER_SHAPES):
+                st, ref = self.oracle.encode(self.synth.dense_weights(rows, K, seed=1000 + i))
+                nb = ref.hi.size + ref.lo.size + rows + 4 * (rows + 1) + 6 * ref.n_esc
+                for M in M_VALUES:
+                    items.append((self.synth.activations(M, K, seed=2000 + 10 * M + i), ref, nb))
+            self.cache[rows] = items
+        return self.cache[rows]
+
+    def run(self, rows):
+        """One pass over the sample: (weight bytes, seconds)."""
+        b, sec = 0.0, 0.0
+        for A, ref, nb in self._prepared(rows):
+            t0 = time.perf_counter()
+            self.oracle.gemm(A, ref)
+            sec += time.perf_counter() - t0
+            b += nb
+        return b, sec
+
+    def rows_for(self, seconds):
+        rows = 16
+        while rows < 4096:
+            b, s = self.run(rows)
+            if s * 2 > seconds:
+                break
+            rows *= 2
+        return rows
+
+
+def cpu_baseline(layers=None, budget_s=10.0):
+    smp = OracleSample()
+    rows = smp.rows_for(budget_s / 4)
+    b = s = 0.0
+    passes = 0
+    while s < budget_s and passes < 64:
+        db, ds = smp.run(rows)
+        b += db
+        s += ds
+        passes += 1
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": smp.oracle.num_threads(), "kind": "oracle",
+            "sample": f"oracle decode+FP64 GEMM on the first {rows} rows of each of the 4 layer shapes at "
+                      f"M=1,2,4,8, {passes} passes, {s:.1f} s of CPU time"}
+
+
+def run_reference(args):
+    """The oracle timed as the reference arm, on the host cores."""
+    ws_n, rank, local = dist_env()
+    if rank != 0:
+        return rank, None
+    smp = OracleSample()
+    step_s = min(args.ref_step_seconds, 150.0 / max(1, args.steps + args.warmup))
+    rows = smp.rows_for(step_s)
+    for _ in range(args.warmup):
+        smp.run(rows)
+    total_b = total_s = 0.0
+    for _ in range(args.steps):
+        b, s = smp.run(rows)
+        total_b += b
+        total_s += s
+    v = total_b / total_s / 1e9
+    threads = smp.oracle.num_threads()
+    cb = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+          "sample": f"per step: oracle decode+FP64 GEMM on the first {rows} rows of each layer shape at "
+                    f"M=1,2,4,8"}
+    return 0, {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "27B-class decoder layer GEMMs (QKV 7168x5120, O 5120x5120, "
+                                                     "gate/up 34816x5120, down 5120x17408), M in {1,2,4,8}, "
+                                                     "row sample on the CPU oracle"},
+        "cpu_baseline": cb,
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        rank, res = run_reference(args)
+    else:
+        rank, res = run_gpu(args)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

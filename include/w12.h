@@ -1,0 +1,170 @@
+/*
+ * w12.h - C ABI of the W12 library (GB300 / sm_103a).
+ *
+ * W12 is the lossless 12-bit BF16 weight format of "SpecPilot: Autonomous
+ * Algorithm Discovery and Systems Optimization for Speculative Decoding"
+ * (arXiv 2611.02501), section 4.1: every weight is a sign bit, a 4-bit
+ * exponent offset inside a window of 16 binades chosen per output channel,
+ * and the 7 BF16 mantissa bits; weights outside the window, zeros and
+ * denormals (and, in this library, Inf/NaN) go to an exact escape list.  The
+ * same section describes a GEMM that decodes the records in registers and
+ * splits its reduction in a fixed order, so that its result is deterministic,
+ * and a bit-for-bit check of every decoded tensor at load time.
+ *
+ * Conventions shared by every call:
+ *   - BF16 values travel as uint16_t bit patterns (no CUDA header needed).
+ *   - Pointers marked "device" are CUDA device memory owned by the caller;
+ *     the library never allocates or frees device memory.
+ *   - Calls validate their arguments on the host before any launch and
+ *     return a w12_status; on an error nothing has been launched, except
+ *     where a call says otherwise.
+ *   - Calls are asynchronous on `stream` unless documented as synchronous.
+ *     `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - The library holds no state between calls and is thread-safe; two calls
+ *     that share a workspace must not run concurrently.
+ *
+ * Tensor layout (the "packed-record layout"; the paper does not fix one):
+ *   Np = N rounded up to 16, Kp = K rounded up to 64.  The 12-bit record of
+ *   weight (n,k) is s<<11 | off<<7 | m (off = exponent - base[n]); escaped
+ *   and padding slots hold record 0.  The records live in two planes, stored
+ *   as tiles of 16 rows x 64 columns, tile (t,c) = (n/16, k/64) at index
+ *   t*(Kp/64)+c:
+ *     hi plane, 1024 bytes per tile: the top 8 record bits (s|off|m[6:4]).
+ *       Row i (0..15), column j (0..63) of a tile is byte
+ *       (i/8)*512 + (4*(i%8) + j/16)*16 + j%16.  This plane alone is the
+ *       8-bit view nested in W12 (section "(3) two-level verification" of
+ *       the paper's news-article page).
+ *     lo plane, 512 bytes per tile: the low record nibble (m[3:0]).
+ *       Slot L = 4*(i%8) + j/16 owns bytes L*16 .. L*16+15: the first 8 for
+ *       row i%8, the next 8 for row i%8+8.  Each group of 8 bytes is two
+ *       32-bit little-endian words for columns j%16 = 0..7 and 8..15; inside
+ *       a word, column u is the high nibble of byte u (u < 4) or the low
+ *       nibble of byte u-4 (u >= 4).
+ *   This order hands each lane of a warp exactly the operand fragment of a
+ *   16x16 BF16 tensor-core tile with 128-bit loads.
+ *   base[n] is the window base exponent of row n (1..239).
+ *   Escapes are a row CSR: esc_row_ptr[n] .. esc_row_ptr[n+1]-1 index the
+ *   escapes of row n, esc_col[] ascending inside a row, esc_val[] the raw
+ *   BF16 bits.
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *w12_stream_t;
+
+typedef enum {
+    W12_OK = 0,
+    W12_ERR_INVALID = -1,     /* bad shape, null pointer, bad stride or option */
+    W12_ERR_ALIGN = -2,       /* a buffer or stride breaks the alignment rules */
+    W12_ERR_CAPACITY = -3,    /* escape arrays or workspace too small */
+    W12_ERR_CUDA = -4,        /* a CUDA runtime call failed */
+    W12_ERR_MISMATCH = -5,    /* verify found decoded bits != original bits */
+    W12_ERR_TIMEOUT = -6,     /* a bounded device-side wait gave up */
+    W12_ERR_CORRUPT = -7,     /* the escape list is malformed */
+    W12_ERR_UNSUPPORTED = -8  /* requested path not available for this shape/device */
+} w12_status;
+
+/* A W12 tensor.  All pointers are device memory owned by the caller. */
+typedef struct {
+    int64_t N, K;           /* logical shape of the BF16 tensor [N,K] */
+    uint8_t *hi;            /* [w12_hi_bytes(N,K)], 16-byte aligned */
+    uint8_t *lo;            /* [w12_lo_bytes(N,K)], 16-byte aligned */
+    uint8_t *base;          /* [N] */
+    int32_t *esc_row_ptr;   /* [N+1] */
+    int32_t *esc_col;       /* [esc_cap] */
+    uint16_t *esc_val;      /* [esc_cap], raw BF16 bits */
+    int64_t esc_cap;        /* capacity of esc_col / esc_val */
+    int64_t n_esc;          /* number of escapes (set by w12_encode) */
+} w12_tensor;
+
+/* GEMM kernel paths. */
+#define W12_PATH_AUTO 0     /* chosen from M alone */
+#define W12_PATH_MMA 1      /* decode in registers + mma.sync, 1 <= M <= 16 */
+#define W12_PATH_TC 2       /* tcgen05 / TMEM path, 16 <= M <= 256 */
+
+/* Options of w12_gemm (NULL = all defaults).  Results are bitwise identical
+ * for any max_ctas; they depend only on (M, N, K, path, split_k). */
+typedef struct {
+    int32_t max_ctas;       /* 0 = as many as fit; >0 caps the grid (tests) */
+    int32_t split_k;        /* 0 = chosen from (M,N,K); >0 forces the split */
+    int32_t path;           /* W12_PATH_* */
+    int32_t reserved;       /* must be 0 */
+} w12_gemm_opts;
+
+/* ---- size queries (host only, no CUDA call) ---- */
+int64_t w12_rows_padded(int64_t N);          /* Np */
+int64_t w12_cols_padded(int64_t K);          /* Kp */
+int64_t w12_hi_bytes(int64_t N, int64_t K);  /* Np*Kp */
+int64_t w12_lo_bytes(int64_t N, int64_t K);  /* Np*Kp/2 */
+
+/* ---- w12_encode ----  BF16 [N,K] -> W12 (paper section 4.1: window per
+ * output channel, records, exact escape list).
+ * W: device [N rows, stride ldw elements], ldw >= K.  out: N, K, all
+ * pointers and esc_cap filled in by the caller; n_esc is written.
+ * Synchronous: waits on `stream` once to read the escape count.
+ * If the tensor needs more than esc_cap escapes the call returns
+ * W12_ERR_CAPACITY with out->n_esc = the number needed; the planes, base and
+ * esc_row_ptr are complete and the first esc_cap escapes are written, so the
+ * caller can grow the escape arrays and call again.  Returns W12_ERR_INVALID
+ * if the count would not fit an int32 row offset. */
+w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_stream_t stream);
+
+/* ---- w12_decode ----  W12 -> BF16 [N,K] (paper section 4.1: decode is bit
+ * for bit).  W_out: device, stride ldw >= K.  Asynchronous.  For a tensor
+ * whose escape list is malformed the output is unspecified (but no access
+ * leaves the buffers); use w12_verify_roundtrip to detect that. */
+w12_status w12_decode(const w12_tensor *w, uint16_t *W_out, int64_t ldw, w12_stream_t stream);
+
+/* ---- w12_verify_roundtrip ----  load-time check (paper section 4.1: every
+ * decoded tensor is checked bit for bit).  Counts the (n,k) whose decoded
+ * bits differ from W into *n_mismatch (host pointer).  workspace: device,
+ * at least w12_verify_workspace_bytes() bytes, any contents.
+ * Synchronous.  Returns W12_OK (0 mismatches), W12_ERR_MISMATCH (>0), or
+ * W12_ERR_CORRUPT with *n_mismatch = -1 when the escape list is malformed
+ * (row offsets not monotone or not ending at n_esc, a column outside [0,K),
+ * columns not strictly ascending inside a row). */
+size_t w12_verify_workspace_bytes(void);
+w12_status w12_verify_roundtrip(const uint16_t *W, int64_t ldw, const w12_tensor *w,
+                                int64_t *n_mismatch, void *workspace, size_t ws_bytes,
+                                w12_stream_t stream);
+
+/* ---- w12_gemm ----  Y[M,N] = A[M,K] * W^T (paper section 4.1: the GEMM
+ * decodes records in registers and splits the reduction in a fixed order).
+ * A: device BF16, row stride lda (elements), 16-byte aligned, lda % 8 == 0.
+ * Y: device BF16, row stride ldy >= N.  FP32 accumulation; each output is
+ * rounded once to BF16 (nearest even).  The summation order depends only on
+ * (M, N, K, path, split_k), never on the grid, so results are bitwise
+ * reproducible.  workspace: device, at least
+ * w12_gemm_workspace_bytes(M,N,K,opts) bytes, ZERO-FILLED before its first
+ * use; every successful call leaves its counters at zero again, so it can be
+ * reused by later calls on the same stream.  Asynchronous.
+ * M = 0 or N = 0 is a no-op.  K = 0 writes zeros. */
+size_t w12_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *opts);
+w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_t *Y,
+                    int64_t ldy, int64_t M, void *workspace, size_t ws_bytes,
+                    const w12_gemm_opts *opts, w12_stream_t stream);
+
+/* Reads (and clears) the device-side error word that bounded waits inside
+ * w12_gemm set when they give up.  Synchronous on `stream`.  Returns W12_OK
+ * or W12_ERR_TIMEOUT. */
+w12_status w12_gemm_workspace_status(void *workspace, size_t ws_bytes, w12_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *w12_status_string(w12_status status);
+
+/* Library version, (major << 16) | minor. */
+int32_t w12_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_H */

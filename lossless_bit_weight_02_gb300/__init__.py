@@ -1,0 +1,330 @@
+"""W12 for GB300: Python binding of the C-ABI library libw12.so.
+
+W12 is the lossless 12-bit BF16 weight format of "SpecPilot" (arXiv
+2611.02501), section 4.1.  Every step of encode, decode, verify and GEMM runs
+in the library's CUDA kernels; this module only marshals arguments (torch
+tensors -> device pointers, the current CUDA stream) and allocates device
+memory through torch.  There is no CPU fallback: if the library cannot be
+loaded, every call raises.
+
+Entry points (same names as the C ABI in include/w12.h):
+    w12_encode(W)                      -> W12Tensor
+    w12_decode(t, out=None)            -> torch.bfloat16 [N,K]
+    w12_verify_roundtrip(W, t)         -> (status, n_mismatch)
+    w12_gemm(A, t, Y=None, ...)        -> torch.bfloat16 [M,N]
+    w12_gemm_workspace_bytes(M, N, K)  -> int
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libw12.so")
+
+W12_OK = 0
+W12_ERR_INVALID = -1
+W12_ERR_ALIGN = -2
+W12_ERR_CAPACITY = -3
+W12_ERR_CUDA = -4
+W12_ERR_MISMATCH = -5
+W12_ERR_TIMEOUT = -6
+W12_ERR_CORRUPT = -7
+W12_ERR_UNSUPPORTED = -8
+
+W12_PATH_AUTO, W12_PATH_MMA, W12_PATH_TC = 0, 1, 2
+
+# Every symbol include/w12.h declares.
+EXPORTS = (
+    "w12_rows_padded", "w12_cols_padded", "w12_hi_bytes", "w12_lo_bytes", "w12_encode",
+    "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
+    "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_workspace_status", "w12_status_string",
+    "w12_version",
+)
+
+
+class W12Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("hi", ctypes.c_void_p), ("lo", ctypes.c_void_p), ("base", ctypes.c_void_p),
+        ("esc_row_ptr", ctypes.c_void_p), ("esc_col", ctypes.c_void_p), ("esc_val", ctypes.c_void_p),
+        ("esc_cap", ctypes.c_int64), ("n_esc", ctypes.c_int64),
+    ]
+
+
+class GemmOpts(ctypes.Structure):
+    _fields_ = [("max_ctas", ctypes.c_int32), ("split_k", ctypes.c_int32),
+                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libw12.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libw12.so not built ({p}); run __graft_entry__.build() or "
+                               "python lossless_bit_weight_02_gb300/_build.py")
+        lib = ctypes.CDLL(p)
+        i64, vp, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+        st = ctypes.c_int
+        sig = {
+            "w12_rows_padded": (i64, [i64]),
+            "w12_cols_padded": (i64, [i64]),
+            "w12_hi_bytes": (i64, [i64, i64]),
+            "w12_lo_bytes": (i64, [i64, i64]),
+            "w12_encode": (st, [vp, i64, ctypes.POINTER(_Tensor), vp]),
+            "w12_decode": (st, [ctypes.POINTER(_Tensor), vp, i64, vp]),
+            "w12_verify_workspace_bytes": (sz, []),
+            "w12_verify_roundtrip": (st, [vp, i64, ctypes.POINTER(_Tensor), ctypes.POINTER(i64), vp, sz, vp]),
+            "w12_gemm_workspace_bytes": (sz, [i64, i64, i64, ctypes.POINTER(GemmOpts)]),
+            "w12_gemm": (st, [vp, i64, ctypes.POINTER(_Tensor), vp, i64, i64, vp, sz,
+                              ctypes.POINTER(GemmOpts), vp]),
+            "w12_gemm_workspace_status": (st, [vp, sz, vp]),
+            "w12_status_string": (ctypes.c_char_p, [st]),
+            "w12_version": (ctypes.c_int32, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().w12_status_string(status).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != W12_OK:
+        raise W12Error(status, what)
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+@dataclass
+class W12Tensor:
+    """A W12 tensor in device memory (all arrays are torch CUDA tensors)."""
+    N: int
+    K: int
+    hi: torch.Tensor       # uint8 [Np*Kp]
+    lo: torch.Tensor       # uint8 [Np*Kp/2]
+    base: torch.Tensor     # uint8 [N]
+    row_ptr: torch.Tensor  # int32 [N+1]
+    esc_col: torch.Tensor  # int32 [esc_cap]
+    esc_val: torch.Tensor  # int16 [esc_cap] (raw BF16 bits)
+    n_esc: int
+
+    @property
+    def esc_cap(self) -> int:
+        return self.esc_col.numel()
+
+    def struct(self) -> _Tensor:
+        return _Tensor(self.N, self.K, self.hi.data_ptr(), self.lo.data_ptr(), self.base.data_ptr(),
+                       self.row_ptr.data_ptr(), self.esc_col.data_ptr(), self.esc_val.data_ptr(),
+                       self.esc_cap, self.n_esc)
+
+    def nbytes(self) -> int:
+        """Bytes the GEMM reads: both planes, bases, row offsets, escapes."""
+        return self.hi.numel() + self.lo.numel() + self.N + 4 * (self.N + 1) + 6 * self.n_esc
+
+    def bits_per_weight(self) -> float:
+        return 8.0 * self.nbytes() / max(1, self.N * self.K)
+
+    def rows(self, n0: int, n1: int) -> "W12Tensor":
+        """Rows [n0, n1) as a W12 tensor of their own (n0 a multiple of 16):
+        plane tiles and bases are sliced; the escape offsets are rebased on
+        the device (the new row offsets are a fresh tensor)."""
+        assert 0 <= n0 <= n1 <= self.N and n0 % 16 == 0
+        KT = self.hi.numel() // max(1, rows_padded(self.N)) // 64
+        t0, t1 = n0 // 16, (n1 + 15) // 16
+        rp = self.row_ptr[n0:n1 + 1]
+        e0 = int(rp[0].item())
+        e1 = int(rp[-1].item())
+        return W12Tensor(n1 - n0, self.K, self.hi[t0 * KT * 1024:t1 * KT * 1024],
+                         self.lo[t0 * KT * 512:t1 * KT * 512], self.base[n0:n1], (rp - e0).contiguous(),
+                         self.esc_col[e0:e1], self.esc_val[e0:e1], e1 - e0)
+
+
+def rows_padded(N: int) -> int:
+    return int(load().w12_rows_padded(N))
+
+
+def cols_padded(K: int) -> int:
+    return int(load().w12_cols_padded(K))
+
+
+def empty_tensor(N: int, K: int, esc_cap: int, device) -> W12Tensor:
+    lib = load()
+    hi = torch.empty(max(1, lib.w12_hi_bytes(N, K)), dtype=torch.uint8, device=device)
+    lo = torch.empty(max(1, lib.w12_lo_bytes(N, K)), dtype=torch.uint8, device=device)
+    base = torch.empty(max(1, N), dtype=torch.uint8, device=device)
+    row_ptr = torch.empty(N + 1, dtype=torch.int32, device=device)
+    esc_col = torch.empty(max(1, esc_cap), dtype=torch.int32, device=device)
+    esc_val = torch.empty(max(1, esc_cap), dtype=torch.int16, device=device)
+    return W12Tensor(N, K, hi[:lib.w12_hi_bytes(N, K)], lo[:lib.w12_lo_bytes(N, K)], base[:N], row_ptr,
+                     esc_col[:esc_cap], esc_val[:esc_cap], 0)
+
+
+def w12_encode(W: torch.Tensor, esc_cap: int | None = None, stream=None) -> W12Tensor:
+    """BF16 [N,K] (CUDA) -> W12Tensor.  Grows the escape arrays if needed."""
+    _need_cuda(W, "W", torch.bfloat16)
+    assert W.dim() == 2 and W.stride(1) == 1
+    N, K = W.shape
+    if esc_cap is None:
+        esc_cap = max(1024, (N * K) // 256)
+    lib = load()
+    for _ in range(2):
+        t = empty_tensor(N, K, esc_cap, W.device)
+        s = t.struct()
+        st = lib.w12_encode(ctypes.c_void_p(W.data_ptr()), W.stride(0), ctypes.byref(s), _stream(stream))
+        t.n_esc = s.n_esc
+        if st == W12_ERR_CAPACITY:
+            esc_cap = s.n_esc
+            continue
+        _check(st, "w12_encode")
+        t.esc_col = t.esc_col[:t.n_esc]
+        t.esc_val = t.esc_val[:t.n_esc]
+        return t
+    raise W12Error(W12_ERR_CAPACITY, "w12_encode")
+
+
+def w12_decode(t: W12Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(t.N, t.K, dtype=torch.bfloat16, device=t.hi.device)
+    _need_cuda(out, "out", torch.bfloat16)
+    s = t.struct()
+    _check(load().w12_decode(ctypes.byref(s), ctypes.c_void_p(out.data_ptr()), out.stride(0) if t.K else t.K,
+                             _stream(stream)), "w12_decode")
+    return out
+
+
+_ws_cache: dict = {}
+
+
+def verify_workspace(device) -> torch.Tensor:
+    key = ("verify", torch.device(device))
+    if key not in _ws_cache:
+        _ws_cache[key] = torch.zeros(int(load().w12_verify_workspace_bytes()), dtype=torch.uint8, device=device)
+    return _ws_cache[key]
+
+
+def w12_verify_roundtrip(W: torch.Tensor, t: W12Tensor, workspace: torch.Tensor | None = None, stream=None):
+    """Bitwise load-time check.  Returns (status, n_mismatch); status is
+    W12_OK, W12_ERR_MISMATCH or W12_ERR_CORRUPT (other errors raise)."""
+    _need_cuda(W, "W", torch.bfloat16)
+    ws = workspace if workspace is not None else verify_workspace(W.device)
+    s = t.struct()
+    nm = ctypes.c_int64(0)
+    st = load().w12_verify_roundtrip(ctypes.c_void_p(W.data_ptr()), W.stride(0) if t.K else t.K, ctypes.byref(s),
+                                     ctypes.byref(nm), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                     _stream(stream))
+    if st not in (W12_OK, W12_ERR_MISMATCH, W12_ERR_CORRUPT):
+        _check(st, "w12_verify_roundtrip")
+    return st, nm.value
+
+
+def make_opts(max_ctas=0, split_k=0, path=W12_PATH_AUTO) -> GemmOpts:
+    return GemmOpts(max_ctas, split_k, path, 0)
+
+
+def w12_gemm_workspace_bytes(M: int, N: int, K: int, opts: GemmOpts | None = None) -> int:
+    o = opts if opts is not None else make_opts()
+    return int(load().w12_gemm_workspace_bytes(M, N, K, ctypes.byref(o)))
+
+
+class Workspace:
+    """A zero-filled device workspace that grows on demand (torch-allocated)."""
+
+    def __init__(self, device, nbytes: int = 0):
+        self.device = torch.device(device)
+        self.buf = torch.zeros(max(256, nbytes), dtype=torch.uint8, device=self.device)
+
+    def ensure(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def default_workspace(device) -> Workspace:
+    key = ("gemm", torch.device(device))
+    if key not in _ws_cache:
+        _ws_cache[key] = Workspace(device)
+    return _ws_cache[key]
+
+
+def w12_gemm(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor | None = None, workspace: Workspace | None = None,
+             opts: GemmOpts | None = None, stream=None) -> torch.Tensor:
+    """Y[M,N] = A[M,K] * W^T with W in W12 (BF16 out, FP32 accumulation)."""
+    _need_cuda(A, "A", torch.bfloat16)
+    M = A.shape[0]
+    if Y is None:
+        Y = torch.empty(M, t.N, dtype=torch.bfloat16, device=A.device)
+    o = opts if opts is not None else make_opts()
+    need = w12_gemm_workspace_bytes(M, t.N, t.K, o)
+    ws = (workspace or default_workspace(A.device)).ensure(max(need, 256))
+    s = t.struct()
+    _check(load().w12_gemm(ctypes.c_void_p(A.data_ptr()), A.stride(0), ctypes.byref(s),
+                           ctypes.c_void_p(Y.data_ptr()), Y.stride(0), M, ctypes.c_void_p(ws.data_ptr()),
+                           ws.numel(), ctypes.byref(o), _stream(stream)), "w12_gemm")
+    return Y
+
+
+class GemmCall:
+    """w12_gemm with every argument marshalled once (for launch loops and
+    benchmarks): calling the object only invokes the C entry point."""
+
+    def __init__(self, A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, workspace: Workspace,
+                 opts: GemmOpts | None = None, stream=None):
+        _need_cuda(A, "A", torch.bfloat16)
+        _need_cuda(Y, "Y", torch.bfloat16)
+        self._keep = (A, t, Y, workspace)
+        self._opts = opts if opts is not None else make_opts()
+        need = w12_gemm_workspace_bytes(A.shape[0], t.N, t.K, self._opts)
+        ws = workspace.ensure(max(need, 256))
+        self._struct = t.struct()
+        self._fn = load().w12_gemm
+        self._args = (ctypes.c_void_p(A.data_ptr()), A.stride(0), ctypes.byref(self._struct),
+                      ctypes.c_void_p(Y.data_ptr()), Y.stride(0), A.shape[0], ctypes.c_void_p(ws.data_ptr()),
+                      ws.numel(), ctypes.byref(self._opts), _stream(stream))
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != W12_OK:
+            raise W12Error(st, "w12_gemm")
+
+
+def w12_gemm_workspace_status(workspace: Workspace, stream=None) -> int:
+    return load().w12_gemm_workspace_status(ctypes.c_void_p(workspace.buf.data_ptr()), workspace.buf.numel(),
+                                            _stream(stream))

@@ -1,0 +1,233 @@
+// C-ABI layer of the W12 library: argument validation, workspace layout and
+// kernel launches.  Every public entry point is declared in include/w12.h.
+#include <cstdint>
+#include <cstring>
+
+#include "w12.h"
+#include "w12_device.cuh"
+#include "w12_internal.h"
+
+namespace {
+
+using namespace w12;
+
+constexpr int64_t kMaxK = (1LL << 31) - 128;  // columns are int32 in the escape list
+constexpr int64_t kMaxN = 1LL << 30;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+w12_status check_tensor(const w12_tensor *w) {
+    if (!w) return W12_ERR_INVALID;
+    if (w->N < 0 || w->K < 0 || w->N > kMaxN || w->K > kMaxK) return W12_ERR_INVALID;
+    if (w->esc_cap < 0 || w->n_esc < 0) return W12_ERR_INVALID;
+    if (w->N > 0 && (!w->base || !w->esc_row_ptr)) return W12_ERR_INVALID;
+    if (w->N > 0 && w->K > 0) {
+        if (!w->hi || !w->lo) return W12_ERR_INVALID;
+        if (!aligned16(w->hi) || !aligned16(w->lo)) return W12_ERR_ALIGN;
+    }
+    if (w->esc_cap > 0 && (!w->esc_col || !w->esc_val)) return W12_ERR_INVALID;
+    return W12_OK;
+}
+
+TensorView view_of(const w12_tensor *w) {
+    TensorView t;
+    t.N = w->N;
+    t.K = w->K;
+    t.Np = rows_padded(w->N);
+    t.Kp = cols_padded(w->K);
+    t.KT = t.Kp / 64;
+    t.hi = w->hi;
+    t.lo = w->lo;
+    t.base = w->base;
+    t.row_ptr = w->esc_row_ptr;
+    t.esc_col = w->esc_col;
+    t.esc_val = w->esc_val;
+    t.n_esc = w->n_esc < w->esc_cap ? w->n_esc : w->esc_cap;
+    return t;
+}
+
+struct GemmPlan {
+    int path;
+    int split;
+    int64_t mp;  // partial columns
+    size_t counters_off, partials_off, bytes;
+};
+
+int choose_path(int64_t M, const w12_gemm_opts *o) {
+    const int p = o ? o->path : W12_PATH_AUTO;
+    if (p != W12_PATH_AUTO) return p;
+    return W12_PATH_MMA;
+}
+
+w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, GemmPlan &pl) {
+    if (M < 0 || N < 0 || K < 0 || N > kMaxN || K > kMaxK) return W12_ERR_INVALID;
+    if (o && (o->reserved != 0 || o->max_ctas < 0 || o->split_k < 0 || o->split_k > 256))
+        return W12_ERR_INVALID;
+    pl.path = choose_path(M, o);
+    if (pl.path != W12_PATH_MMA && pl.path != W12_PATH_TC) return W12_ERR_INVALID;
+    if (pl.path == W12_PATH_MMA && M > 16) return W12_ERR_UNSUPPORTED;
+    if (pl.path == W12_PATH_TC) return W12_ERR_UNSUPPORTED;
+    int split = (o && o->split_k > 0) ? o->split_k : gemm_mma_split(M, N, K);
+    const int64_t KT = cols_padded(K) / 64;
+    if (KT == 0) split = 1;
+    if (split > KT && KT > 0) split = (int)KT;
+    pl.split = split;
+    pl.mp = gemm_mma_partial_cols(M);
+    const int64_t Np = rows_padded(N);
+    pl.counters_off = 256;
+    pl.partials_off = 256 + round256((Np / 16) * 4);
+    pl.bytes = pl.partials_off + (split > 1 ? (size_t)split * Np * pl.mp * 4 : 0);
+    return W12_OK;
+}
+
+w12_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W12_OK : W12_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int64_t w12_rows_padded(int64_t N) { return N < 0 ? -1 : rows_padded(N); }
+int64_t w12_cols_padded(int64_t K) { return K < 0 ? -1 : cols_padded(K); }
+int64_t w12_hi_bytes(int64_t N, int64_t K) { return (N < 0 || K < 0) ? -1 : rows_padded(N) * cols_padded(K); }
+int64_t w12_lo_bytes(int64_t N, int64_t K) {
+    return (N < 0 || K < 0) ? -1 : rows_padded(N) * cols_padded(K) / 2;
+}
+
+int32_t w12_version(void) { return (1 << 16) | 0; }
+
+const char *w12_status_string(w12_status s) {
+    switch (s) {
+        case W12_OK: return "W12_OK";
+        case W12_ERR_INVALID: return "W12_ERR_INVALID";
+        case W12_ERR_ALIGN: return "W12_ERR_ALIGN";
+        case W12_ERR_CAPACITY: return "W12_ERR_CAPACITY";
+        case W12_ERR_CUDA: return "W12_ERR_CUDA";
+        case W12_ERR_MISMATCH: return "W12_ERR_MISMATCH";
+        case W12_ERR_TIMEOUT: return "W12_ERR_TIMEOUT";
+        case W12_ERR_CORRUPT: return "W12_ERR_CORRUPT";
+        case W12_ERR_UNSUPPORTED: return "W12_ERR_UNSUPPORTED";
+    }
+    return "W12_ERR_UNKNOWN";
+}
+
+w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_stream_t stream) {
+    w12_status st = check_tensor(out);
+    if (st != W12_OK) return st;
+    if (ldw < out->K) return W12_ERR_INVALID;
+    if (out->N > 0 && out->K > 0 && !W) return W12_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t N = out->N, K = out->K;
+    if (N == 0) {
+        int32_t zero = 0;
+        if (cudaMemcpyAsync(out->esc_row_ptr, &zero, 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return W12_ERR_CUDA;
+        out->n_esc = 0;
+        return W12_OK;
+    }
+    if (launch_window_count(W, ldw, N, K, out->base, out->esc_row_ptr, s) != cudaSuccess) return W12_ERR_CUDA;
+    if (launch_row_scan(out->esc_row_ptr, N, s) != cudaSuccess) return W12_ERR_CUDA;
+    int32_t total = 0;
+    if (cudaMemcpyAsync(&total, out->esc_row_ptr + N, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (total < 0) return W12_ERR_INVALID;  // more escapes than an int32 offset can index
+    out->n_esc = total;
+    if (launch_pack(W, ldw, N, K, out->base, out->esc_row_ptr, out->hi, out->lo, out->esc_col, out->esc_val,
+                    out->esc_cap, s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    return total > out->esc_cap ? W12_ERR_CAPACITY : W12_OK;
+}
+
+w12_status w12_decode(const w12_tensor *w, uint16_t *W_out, int64_t ldw, w12_stream_t stream) {
+    w12_status st = check_tensor(w);
+    if (st != W12_OK) return st;
+    if (ldw < w->K) return W12_ERR_INVALID;
+    if (w->N > 0 && w->K > 0 && !W_out) return W12_ERR_INVALID;
+    if (w->N == 0 || w->K == 0) return W12_OK;
+    return cuda_status(launch_decode(view_of(w), W_out, ldw, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w12_verify_workspace_bytes(void) { return 16; }
+
+w12_status w12_verify_roundtrip(const uint16_t *W, int64_t ldw, const w12_tensor *w, int64_t *n_mismatch,
+                                void *workspace, size_t ws_bytes, w12_stream_t stream) {
+    w12_status st = check_tensor(w);
+    if (st != W12_OK) return st;
+    if (!n_mismatch || ldw < w->K) return W12_ERR_INVALID;
+    if (!workspace || ws_bytes < w12_verify_workspace_bytes()) return W12_ERR_CAPACITY;
+    if (reinterpret_cast<uintptr_t>(workspace) & 7) return W12_ERR_ALIGN;
+    if (w->N > 0 && w->K > 0 && !W) return W12_ERR_INVALID;
+    *n_mismatch = -1;
+    if (w->n_esc > w->esc_cap) return W12_ERR_CORRUPT;
+    if (w->N == 0) {
+        *n_mismatch = 0;
+        return w->n_esc == 0 ? W12_OK : W12_ERR_CORRUPT;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned long long *cnt = static_cast<unsigned long long *>(workspace);
+    const TensorView t = view_of(w);
+    if (cudaMemsetAsync(cnt, 0, 16, s) != cudaSuccess) return W12_ERR_CUDA;
+    if (launch_check_structure(t, w->esc_cap, cnt, s) != cudaSuccess) return W12_ERR_CUDA;
+    if (w->K > 0 && launch_verify(t, W, ldw, cnt + 1, s) != cudaSuccess) return W12_ERR_CUDA;
+    unsigned long long host[2] = {0, 0};
+    if (cudaMemcpyAsync(host, cnt, 16, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (host[0] != 0) return W12_ERR_CORRUPT;
+    *n_mismatch = (int64_t)host[1];
+    return host[1] ? W12_ERR_MISMATCH : W12_OK;
+}
+
+size_t w12_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *opts) {
+    GemmPlan pl;
+    if (plan_gemm(M, N, K, opts, pl) != W12_OK) return 0;
+    return pl.bytes;
+}
+
+w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_t *Y, int64_t ldy, int64_t M,
+                    void *workspace, size_t ws_bytes, const w12_gemm_opts *opts, w12_stream_t stream) {
+    w12_status st = check_tensor(w);
+    if (st != W12_OK) return st;
+    if (M < 0) return W12_ERR_INVALID;
+    if (M == 0 || w->N == 0) return W12_OK;
+    if (!Y || ldy < w->N) return W12_ERR_INVALID;
+    if (w->K > 0) {
+        if (!A || lda < w->K) return W12_ERR_INVALID;
+        if (!aligned16(A) || (lda % 8) != 0) return W12_ERR_ALIGN;
+    }
+    GemmPlan pl;
+    st = plan_gemm(M, w->N, w->K, opts, pl);
+    if (st != W12_OK) return st;
+    if (!workspace || ws_bytes < pl.bytes) return W12_ERR_CAPACITY;
+    if (!aligned16(workspace)) return W12_ERR_ALIGN;
+    char *ws = static_cast<char *>(workspace);
+    GemmArgs g;
+    g.A = A;
+    g.lda = lda;
+    g.Y = Y;
+    g.ldy = ldy;
+    g.M = M;
+    g.split = pl.split;
+    g.max_ctas = opts ? opts->max_ctas : 0;
+    g.error = reinterpret_cast<int32_t *>(ws);
+    g.counters = reinterpret_cast<int32_t *>(ws + pl.counters_off);
+    g.partials = reinterpret_cast<float *>(ws + pl.partials_off);
+    return cuda_status(launch_gemm_mma(view_of(w), g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w12_status w12_gemm_workspace_status(void *workspace, size_t ws_bytes, w12_stream_t stream) {
+    if (!workspace || ws_bytes < 256) return W12_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t err = 0;
+    if (cudaMemcpyAsync(&err, workspace, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (err == 0) return W12_OK;
+    if (cudaMemsetAsync(workspace, 0, 4, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    return W12_ERR_TIMEOUT;
+}
+
+}  // extern "C"

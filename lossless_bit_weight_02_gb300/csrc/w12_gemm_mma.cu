@@ -1,0 +1,320 @@
+// Small-M W12 GEMM (1 <= M <= 16): Y = A * W^T with the weights decoded in
+// registers (SpecPilot, arXiv 2611.02501, section 4.1: "decodes records in
+// registers", "splits the reduction in a fixed order so the GEMM is
+// deterministic").
+//
+// Design (HBM-bound: ~1.33*M flop per weight byte):
+//   * Work item = (row stripe of 16 weight rows, K-chunk s of S).  Each warp
+//     streams its item's tiles: per 16x64 tile every lane issues two 128-bit
+//     loads of the hi plane and one of the lo plane - the tile layout puts
+//     exactly the lane's tensor-core A fragment (rows g and g+8, 16 columns
+//     each) behind those loads, so a warp reads 1.5 KB contiguous per tile.
+//   * Records are decoded to BF16 pairs with ~2.6 integer ops per weight
+//     (prmt / shift / and / add / select), escapes of the tile are patched in
+//     (through a 2 KB per-warp shared-memory copy of the fragment, only for
+//     tiles that hold an escape), then four mma.sync.m16n8k16 per 8 tokens
+//     accumulate in FP32.  The 64 columns of a tile are fed to the four MMAs
+//     in a fixed permuted order; activations use the same permutation.
+//   * Fixed-order reduction: chunk partials start from zero; when S > 1 they
+//     go to an FP32 workspace and the last warp to finish a stripe sums them
+//     in the order s = 0..S-1 and writes BF16.  S depends on (M, N, K) only,
+//     so the result is identical for any grid.
+#include <climits>
+#include <cstdint>
+
+#include "w12_device.cuh"
+#include "w12_internal.h"
+
+namespace w12 {
+namespace {
+
+constexpr int kWarps = 4;     // warps per block
+constexpr int kPrefetch = 4;  // tiles in flight per warp
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16 activations A[m, k .. k+15] as 8 BF16 pairs, zero past K.
+__device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int64_t k, int64_t K,
+                                           uint32_t w[8]) {
+    if (k + 16 <= K) {
+        const uint4 x0 = __ldg(reinterpret_cast<const uint4 *>(row + k));
+        const uint4 x1 = __ldg(reinterpret_cast<const uint4 *>(row + k + 8));
+        w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
+        w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t lo = (k + 2 * j < K) ? row[k + 2 * j] : 0u;
+            const uint32_t hi = (k + 2 * j + 1 < K) ? row[k + 2 * j + 1] : 0u;
+            w[j] = lo | (hi << 16);
+        }
+    }
+}
+
+template <int NB>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16)
+__global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs g) {
+    __shared__ __align__(16) uint4 patch[kWarps][4][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, q = lane & 3;
+    const int S = g.split;
+    const int64_t T = t.Np / 16;
+    const int64_t items = T * S;
+    constexpr int MP = 8 * NB;
+
+    for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < items;
+         item += (int64_t)gridDim.x * kWarps) {
+        const int64_t st = item / S;
+        const int s = (int)(item % S);
+        const int64_t c_beg = (s * t.KT) / S, c_end = ((s + 1) * t.KT) / S;
+        const int64_t n0 = st * 16;
+        const int64_t rowA = n0 + gid, rowB = n0 + gid + 8;
+        const uint32_t base2A = (rowA < t.N ? (uint32_t)t.base[rowA] : 0u) * 0x00800080u;
+        const uint32_t base2B = (rowB < t.N ? (uint32_t)t.base[rowB] : 0u) * 0x00800080u;
+
+        // Escape cursor: lane r < 16 walks the escapes of row n0 + r.
+        int64_t e_cur = 0, e_end = 0;
+        int64_t e_col = LLONG_MAX;
+        uint16_t e_val = 0;
+        if (lane < 16 && n0 + lane < t.N) {
+            escape_range(t.row_ptr, n0 + lane, t.n_esc, e_cur, e_end);
+            if (c_beg > 0) e_cur = lower_bound_col(t.esc_col, e_cur, e_end, c_beg * 64);
+            if (e_cur < e_end) {
+                e_col = t.esc_col[e_cur];
+                e_val = t.esc_val[e_cur];
+            }
+        }
+
+        // Activation rows of this lane (token m = 8*b + gid).
+        const uint16_t *arow[NB];
+        bool mval[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int m = 8 * b + gid;
+            mval[b] = m < g.M;
+            arow[b] = g.A + (mval[b] ? (int64_t)m * g.lda : 0);
+        }
+
+        float acc[NB][4];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
+
+        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + st * t.KT * 64 + lane;
+        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + st * t.KT * 32 + lane;
+        uint4 bh0[kPrefetch], bh1[kPrefetch], bl[kPrefetch];
+#pragma unroll
+        for (int p = 0; p < kPrefetch; ++p) {
+            const int64_t c = c_beg + p;
+            if (c < c_end) {
+                bh0[p] = ld_stream(hp + c * 64);
+                bh1[p] = ld_stream(hp + c * 64 + 32);
+                bl[p] = ld_stream(lp + c * 32);
+            }
+        }
+
+        for (int64_t cc = c_beg; cc < c_end; cc += kPrefetch) {
+#pragma unroll
+            for (int p = 0; p < kPrefetch; ++p) {
+                const int64_t c = cc + p;
+                if (c < c_end) {
+                    uint32_t dA[8], dB[8];
+                    decode16(bh0[p], bl[p].x, bl[p].y, base2A, dA);
+                    decode16(bh1[p], bl[p].z, bl[p].w, base2B, dB);
+                    const int64_t cn = c + kPrefetch;
+                    if (cn < c_end) {
+                        bh0[p] = ld_stream(hp + cn * 64);
+                        bh1[p] = ld_stream(hp + cn * 64 + 32);
+                        bl[p] = ld_stream(lp + cn * 32);
+                    }
+
+                    // Escapes of this tile replace the decoded placeholders.
+                    const int64_t k_lo = c * 64, k_hi = k_lo + 64;
+                    bool pend = e_col < k_hi;
+                    if (__any_sync(kFull, pend)) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            patch[warp][i][lane] = make_uint4(dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1]);
+                        __syncwarp();
+                        while (pend) {
+                            const int64_t kl = e_col - k_lo;
+                            if (kl >= 0) {
+                                const int r = lane;
+                                const int slot = (r & 7) * 4 + (int)(kl >> 4);
+                                const int j16 = (int)(kl & 15), pr = j16 >> 1;
+                                const int comp = (pr & 1) * 2 + (r >> 3);
+                                reinterpret_cast<uint16_t *>(&patch[warp][pr >> 1][slot])[comp * 2 + (j16 & 1)] = e_val;
+                            }
+                            ++e_cur;
+                            if (e_cur < e_end) {
+                                e_col = t.esc_col[e_cur];
+                                e_val = t.esc_val[e_cur];
+                            } else {
+                                e_col = LLONG_MAX;
+                            }
+                            pend = e_col < k_hi;
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 v = patch[warp][i][lane];
+                            dA[2 * i] = v.x;
+                            dB[2 * i] = v.y;
+                            dA[2 * i + 1] = v.z;
+                            dB[2 * i + 1] = v.w;
+                        }
+                        __syncwarp();
+                    }
+
+                    // B fragments: lane (gid, q) holds A[m, 64c + 16q .. +15].
+                    uint32_t bw[NB][8];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        if (mval[b]) {
+                            load_act16(arow[b], k_lo + 16 * q, t.K, bw[b]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) bw[b][j] = 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                        for (int b = 0; b < NB; ++b)
+                            mma16816(acc[b], dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1], bw[b][2 * i],
+                                     bw[b][2 * i + 1]);
+                    }
+                }
+            }
+        }
+
+        // Epilogue.  acc[b] = {(rowA, m0), (rowA, m0+1), (rowB, m0), (rowB, m0+1)}, m0 = 8b + 2q.
+        if (S == 1) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int m = 8 * b + 2 * q + h;
+                    if (m < g.M) {
+                        if (rowA < t.N) g.Y[(int64_t)m * g.ldy + rowA] = f32_to_bf16_rn(acc[b][h]);
+                        if (rowB < t.N) g.Y[(int64_t)m * g.ldy + rowB] = f32_to_bf16_rn(acc[b][2 + h]);
+                    }
+                }
+            }
+        } else {
+            float *P = g.partials;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                *reinterpret_cast<float2 *>(P + ((int64_t)s * t.Np + rowA) * MP + 8 * b + 2 * q) =
+                    make_float2(acc[b][0], acc[b][1]);
+                *reinterpret_cast<float2 *>(P + ((int64_t)s * t.Np + rowB) * MP + 8 * b + 2 * q) =
+                    make_float2(acc[b][2], acc[b][3]);
+            }
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = (atomicAdd(&g.counters[st], 1) == S - 1);
+            last = __shfl_sync(kFull, last, 0);
+            if (last) {
+                __threadfence();
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int64_t row = rr ? rowB : rowA;
+                        float2 v = __ldcg(reinterpret_cast<const float2 *>(P + row * MP + 8 * b + 2 * q));
+                        for (int ss = 1; ss < S; ++ss) {
+                            const float2 w =
+                                __ldcg(reinterpret_cast<const float2 *>(P + ((int64_t)ss * t.Np + row) * MP + 8 * b + 2 * q));
+                            v.x += w.x;
+                            v.y += w.y;
+                        }
+                        if (row < t.N) {
+                            const int m = 8 * b + 2 * q;
+                            if (m < g.M) g.Y[(int64_t)m * g.ldy + row] = f32_to_bf16_rn(v.x);
+                            if (m + 1 < g.M) g.Y[(int64_t)(m + 1) * g.ldy + row] = f32_to_bf16_rn(v.y);
+                        }
+                    }
+                }
+                if (lane == 0) g.counters[st] = 0;
+            }
+        }
+    }
+}
+
+struct LaunchCache {
+    int sms = 0;
+    int occ[3] = {0, 0, 0};
+};
+
+LaunchCache &cache_for_device(int dev) {
+    static LaunchCache caches[64];
+    return caches[dev & 63];
+}
+
+template <int NB>
+cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    LaunchCache &lc = cache_for_device(dev);
+    if (lc.sms == 0) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        lc.sms = sms;
+    }
+    if (lc.occ[NB] == 0) {
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_gemm_mma<NB>, kWarps * 32, 0);
+        if (e != cudaSuccess) return e;
+        lc.occ[NB] = occ > 0 ? occ : 1;
+    }
+    const int64_t items = (t.Np / 16) * (int64_t)g.split;
+    int64_t blocks = (items + kWarps - 1) / kWarps;
+    const int64_t resident = (int64_t)lc.sms * lc.occ[NB];
+    if (blocks > resident) blocks = resident;
+    if (g.max_ctas > 0 && blocks > g.max_ctas) blocks = g.max_ctas;
+    if (blocks < 1) blocks = 1;
+    k_gemm_mma<NB><<<(unsigned)blocks, kWarps * 32, 0, s>>>(t, g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t gemm_mma_partial_cols(int64_t M) { return M <= 8 ? 8 : 16; }
+
+// Split factor from (M, N, K) only: enough (stripe, chunk) items to keep
+// about 16 warps on each of 152 SMs streaming, at least 4 tiles per chunk.
+int gemm_mma_split(int64_t M, int64_t N, int64_t K) {
+    (void)M;
+    const int64_t T = (N + 15) / 16, KT = (K + 63) / 64;
+    if (T == 0 || KT == 0) return 1;
+    const int64_t target = 152 * 16;
+    int64_t S = (target + T / 2) / T;
+    const int64_t smax = KT / 4 > 1 ? KT / 4 : 1;
+    if (S > smax) S = smax;
+    if (S > 32) S = 32;
+    if (S < 1) S = 1;
+    return (int)S;
+}
+
+cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
+    if (g.M <= 8) return launch_nb<1>(t, g, s);
+    return launch_nb<2>(t, g, s);
+}
+
+}  // namespace w12

@@ -1,0 +1,63 @@
+// Internal launch interface between the C-ABI layer (w12_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "w12.h"
+
+namespace w12 {
+
+// Device view of a W12 tensor (plain pointers, sizes precomputed).
+struct TensorView {
+    int64_t N, K, Np, Kp, KT;  // KT = Kp / 64 tiles per row stripe
+    const uint8_t *hi;
+    const uint8_t *lo;
+    const uint8_t *base;
+    const int32_t *row_ptr;
+    const int32_t *esc_col;
+    const uint16_t *esc_val;
+    int64_t n_esc;
+};
+
+// ---- codec (w12_codec.cu) ----
+// a1 + a2: base[n] and the escape count of row n into row_ptr[n+1].
+cudaError_t launch_window_count(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base,
+                                int32_t *row_ptr, cudaStream_t s);
+// a2: in-place scan of row_ptr[1..N] and row_ptr[0] = 0; row_ptr[N] = -1 on
+// int32 overflow.
+cudaError_t launch_row_scan(int32_t *row_ptr, int64_t N, cudaStream_t s);
+// a3: planes + escapes (escape writes limited to esc_cap).
+cudaError_t launch_pack(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const uint8_t *base,
+                        const int32_t *row_ptr, uint8_t *hi, uint8_t *lo, int32_t *esc_col,
+                        uint16_t *esc_val, int64_t esc_cap, cudaStream_t s);
+// a4
+cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s);
+// escape-list structure violations added to *bad (device counter).
+cudaError_t launch_check_structure(const TensorView &t, int64_t esc_cap,
+                                   unsigned long long *bad, cudaStream_t s);
+// a5: mismatches added to *count (device counter).
+cudaError_t launch_verify(const TensorView &t, const uint16_t *W, int64_t ldw,
+                          unsigned long long *count, cudaStream_t s);
+
+// ---- GEMM ----
+struct GemmArgs {
+    const uint16_t *A;
+    int64_t lda;
+    uint16_t *Y;
+    int64_t ldy;
+    int64_t M;
+    int split;           // S >= 1
+    int max_ctas;        // 0 = occupancy-limited persistent grid
+    float *partials;     // [S][Np][MP] fp32 (S > 1)
+    int32_t *counters;   // [Np/16] arrival counters (S > 1)
+    int32_t *error;      // device error word
+};
+
+// Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).
+cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s);
+int gemm_mma_split(int64_t M, int64_t N, int64_t K);
+int64_t gemm_mma_partial_cols(int64_t M);  // MP
+
+}  // namespace w12

@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every symbol include/w12.h declares, and
+its host-side argument checks reject bad calls before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"\b(w12_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("w12_encode", "w12_decode", "w12_gemm", "w12_verify_roundtrip"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(w12lib):
+    lib = ctypes.CDLL(w12lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(w12lib.EXPORTS)
+
+
+def test_size_queries(w12lib):
+    lib = w12lib.load()
+    assert lib.w12_rows_padded(5121) == 5136
+    assert lib.w12_cols_padded(17400) == 17408
+    assert lib.w12_hi_bytes(5121, 17400) == 5136 * 17408
+    assert lib.w12_lo_bytes(5121, 17400) == 5136 * 17408 // 2
+    assert lib.w12_rows_padded(-1) == -1
+    assert lib.w12_verify_workspace_bytes() == 16
+    assert (lib.w12_version() >> 16) == 1
+
+
+def test_oracle_and_library_agree_on_sizes(w12lib, oracle):
+    for N, K in ((1, 1), (16, 64), (17, 65), (5121, 17400), (34816, 5120)):
+        assert w12lib.rows_padded(N) == oracle.rows_padded(N)
+        assert w12lib.cols_padded(K) == oracle.cols_padded(K)
+
+
+def test_gemm_workspace_query(w12lib):
+    o = w12lib.make_opts()
+    # one stripe count of counters + S partial slabs of [Np, 8] floats
+    nb = w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, o)
+    assert nb >= 256 + 5120 // 16 * 4
+    assert w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, w12lib.make_opts(split_k=1)) <= 256 + 2048
+    assert w12lib.w12_gemm_workspace_bytes(17, 64, 64, w12lib.make_opts(path=w12lib.W12_PATH_MMA)) == 0
+    bad = w12lib.GemmOpts(0, 0, 0, 1)  # reserved must be 0
+    assert w12lib.w12_gemm_workspace_bytes(1, 64, 64, bad) == 0
+
+
+def test_status_strings(w12lib):
+    for code, name in ((0, "W12_OK"), (-3, "W12_ERR_CAPACITY"), (-7, "W12_ERR_CORRUPT")):
+        assert w12lib.status_string(code) == name
+
+
+def test_invalid_arguments_rejected_on_host(w12lib):
+    """These calls fail validation before any CUDA call is made."""
+    lib = w12lib.load()
+    T = w12lib._Tensor
+    t = T(4, 64, None, None, None, None, None, None, 0, 0)
+    assert lib.w12_decode(ctypes.byref(t), None, 64, None) == w12lib.W12_ERR_INVALID
+    assert lib.w12_encode(None, 64, None, None) == w12lib.W12_ERR_INVALID
+    neg = T(-1, 64, None, None, None, None, None, None, 0, 0)
+    assert lib.w12_decode(ctypes.byref(neg), None, 64, None) == w12lib.W12_ERR_INVALID
+    # misaligned planes
+    good = T(4, 64, 16, 17, 32, 48, 64, 80, 1, 0)
+    assert lib.w12_decode(ctypes.byref(good), ctypes.c_void_p(4096), 64, None) == w12lib.W12_ERR_ALIGN
+    # M > 16 on the mma path
+    t2 = T(16, 64, 256, 512, 768, 1024, 1280, 1536, 1, 0)
+    o = w12lib.make_opts(path=w12lib.W12_PATH_MMA)
+    st = lib.w12_gemm(ctypes.c_void_p(4096), 64, ctypes.byref(t2), ctypes.c_void_p(8192), 16, 17,
+                      ctypes.c_void_p(16384), 1 << 20, ctypes.byref(o), None)
+    assert st == w12lib.W12_ERR_UNSUPPORTED
+    # lda not a multiple of 8
+    st = lib.w12_gemm(ctypes.c_void_p(4096), 65, ctypes.byref(t2), ctypes.c_void_p(8192), 16, 1,
+                      ctypes.c_void_p(16384), 1 << 20, None, None)
+    assert st == w12lib.W12_ERR_ALIGN
+    # workspace too small
+    st = lib.w12_gemm(ctypes.c_void_p(4096), 64, ctypes.byref(t2), ctypes.c_void_p(8192), 16, 1,
+                      ctypes.c_void_p(16384), 8, None, None)
+    assert st == w12lib.W12_ERR_CAPACITY
+    nm = ctypes.c_int64()
+    st = lib.w12_verify_roundtrip(ctypes.c_void_p(4096), 64, ctypes.byref(t2), ctypes.byref(nm),
+                                  ctypes.c_void_p(16384), 4, None)
+    assert st == w12lib.W12_ERR_CAPACITY
