@@ -143,9 +143,12 @@ w12_status w12_verify_roundtrip(const uint16_t *W, int64_t ldw, const w12_tensor
  * rounded once to BF16 (nearest even).  The summation order depends only on
  * (M, N, K, path, split_k), never on the grid, so results are bitwise
  * reproducible.  workspace: device, at least
- * w12_gemm_workspace_bytes(M,N,K,opts) bytes, ZERO-FILLED before its first
- * use; every successful call leaves its counters at zero again, so it can be
- * reused by later calls on the same stream.  Asynchronous.
+ * w12_gemm_workspace_bytes(M,N,K,opts) bytes (256 bytes when no split is
+ * needed, else 256 KiB of arrival counters plus the FP32 partials),
+ * ZERO-FILLED before its first use.  The counters sit at the same offset for
+ * every shape and every successful call leaves them at zero, so one
+ * workspace serves any sequence of calls on one stream; after a failed call,
+ * zero it again.  Asynchronous.
  * M = 0 or N = 0 is a no-op.  K = 0 writes zeros. */
 size_t w12_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *opts);
 w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_t *Y,

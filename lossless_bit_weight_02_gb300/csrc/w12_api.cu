@@ -13,6 +13,7 @@ using namespace w12;
 
 constexpr int64_t kMaxK = (1LL << 31) - 128;  // columns are int32 in the escape list
 constexpr int64_t kMaxN = 1LL << 30;
+constexpr int64_t kMaxCounters = 1LL << 16;  // split-K stripes with an arrival counter
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -70,14 +71,18 @@ w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, Ge
     if (pl.path == W12_PATH_TC) return W12_ERR_UNSUPPORTED;
     int split = (o && o->split_k > 0) ? o->split_k : gemm_mma_split(M, N, K);
     const int64_t KT = cols_padded(K) / 64;
+    const int64_t Np = rows_padded(N);
     if (KT == 0) split = 1;
     if (split > KT && KT > 0) split = (int)KT;
+    if (Np / 16 > kMaxCounters) split = 1;  // arrival counters exist for at most kMaxCounters stripes
     pl.split = split;
     pl.mp = gemm_mma_partial_cols(M);
-    const int64_t Np = rows_padded(N);
+    // Fixed layout, the same for every shape, so that the counter region is
+    // never reused for partials: [0,256) error word | [256, 256+4*kMaxCounters)
+    // arrival counters (zero between calls) | FP32 partials.
     pl.counters_off = 256;
-    pl.partials_off = 256 + round256((Np / 16) * 4);
-    pl.bytes = pl.partials_off + (split > 1 ? (size_t)split * Np * pl.mp * 4 : 0);
+    pl.partials_off = 256 + 4 * kMaxCounters;
+    pl.bytes = split > 1 ? pl.partials_off + (size_t)split * Np * pl.mp * 4 : 256;
     return W12_OK;
 }
 

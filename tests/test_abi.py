@@ -54,8 +54,10 @@ def test_gemm_workspace_query(w12lib):
     o = w12lib.make_opts()
     # one stripe count of counters + S partial slabs of [Np, 8] floats
     nb = w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, o)
-    assert nb >= 256 + 5120 // 16 * 4
-    assert w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, w12lib.make_opts(split_k=1)) <= 256 + 2048
+    S = 8  # about 16 warps on each of 152 SMs over 320 stripes
+    assert nb == 256 + 4 * 65536 + S * 5120 * 8 * 4
+    assert w12lib.w12_gemm_workspace_bytes(16, 5120, 5120, o) == 256 + 4 * 65536 + S * 5120 * 16 * 4
+    assert w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, w12lib.make_opts(split_k=1)) == 256
     assert w12lib.w12_gemm_workspace_bytes(17, 64, 64, w12lib.make_opts(path=w12lib.W12_PATH_MMA)) == 0
     bad = w12lib.GemmOpts(0, 0, 0, 1)  # reserved must be 0
     assert w12lib.w12_gemm_workspace_bytes(1, 64, 64, bad) == 0

@@ -135,7 +135,8 @@ def test_workspace_left_clean_and_reusable(w12lib, oracle):
     """Counters return to zero after each call, so one workspace serves a
     sequence of different shapes."""
     ws = w12lib.Workspace("cuda", 1 << 22)
-    for N, K, M in ((512, 2048, 1), (96, 640, 16), (512, 2048, 3), (1024, 1024, 8)):
+    for N, K, M in ((512, 2048, 1), (96, 640, 16), (512, 2048, 3), (1024, 1024, 8), (160, 4096, 16),
+                    (8192, 1024, 1), (64, 2048, 2), (6144, 512, 9)):
         W = synth.dense_weights(N, K, seed=N + K)
         A = synth.activations(M, K, seed=M)
         st, ref = oracle.encode(W)

@@ -20,11 +20,12 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def ulp_bf16(v: np.ndarray) -> np.ndarray:
-    a = np.abs(v)
+    """BF16 ulp of each value (non-finite values get an infinite ulp)."""
+    a = np.where(np.isfinite(v), np.abs(v), 0.0)
     with np.errstate(divide="ignore"):
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     e = np.maximum(np.where(a > 0, e, -126.0), -126.0)
-    return np.ldexp(1.0, (e - 7).astype(np.int64))
+    return np.where(np.isfinite(v), np.ldexp(1.0, (e - 7).astype(np.int64)), np.inf)
 
 
 def gemm_tolerance_failures(y_bits, ref_bits, y64, absdot):
