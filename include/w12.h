@@ -43,9 +43,13 @@
  *   This order hands each lane of a warp exactly the operand fragment of a
  *   16x16 BF16 tensor-core tile with 128-bit loads.
  *   base[n] is the window base exponent of row n (1..239).
- *   Escapes are a row CSR: esc_row_ptr[n] .. esc_row_ptr[n+1]-1 index the
- *   escapes of row n, esc_col[] ascending inside a row, esc_val[] the raw
- *   BF16 bits.
+ *   Escapes: one 32-bit entry each, key<<16 | raw BF16 bits, grouped by
+ *   (row stripe t = n/16, column group g = k/256).  With G = w12_groups(K)
+ *   groups per stripe, the entries of (t,g) are esc[esc_ptr[t*G+g] ..
+ *   esc_ptr[t*G+g+1]-1], sorted by key; the key of weight (n,k) is
+ *   (k%256/64)<<10 | (n%16)<<6 | k%64 (tile, row, column inside the group).
+ *   esc_ptr has w12_esc_ptr_len(N,K) = Np/16*G + 1 entries, the last = n_esc.
+ *   One coalesced 4-byte load per lane fetches the escapes of a group.
  */
 #ifndef W12_H
 #define W12_H
@@ -78,10 +82,9 @@ typedef struct {
     uint8_t *hi;            /* [w12_hi_bytes(N,K)], 16-byte aligned */
     uint8_t *lo;            /* [w12_lo_bytes(N,K)], 16-byte aligned */
     uint8_t *base;          /* [N] */
-    int32_t *esc_row_ptr;   /* [N+1] */
-    int32_t *esc_col;       /* [esc_cap] */
-    uint16_t *esc_val;      /* [esc_cap], raw BF16 bits */
-    int64_t esc_cap;        /* capacity of esc_col / esc_val */
+    int32_t *esc_ptr;       /* [w12_esc_ptr_len(N,K)] */
+    uint32_t *esc;          /* [esc_cap] entries key<<16 | BF16 bits */
+    int64_t esc_cap;        /* capacity of esc */
     int64_t n_esc;          /* number of escapes (set by w12_encode) */
 } w12_tensor;
 
@@ -104,6 +107,8 @@ int64_t w12_rows_padded(int64_t N);          /* Np */
 int64_t w12_cols_padded(int64_t K);          /* Kp */
 int64_t w12_hi_bytes(int64_t N, int64_t K);  /* Np*Kp */
 int64_t w12_lo_bytes(int64_t N, int64_t K);  /* Np*Kp/2 */
+int64_t w12_groups(int64_t K);               /* 256-column groups per stripe: ceil(Kp/256) */
+int64_t w12_esc_ptr_len(int64_t N, int64_t K);  /* Np/16 * w12_groups(K) + 1 */
 
 /* ---- w12_encode ----  BF16 [N,K] -> W12 (paper section 4.1: window per
  * output channel, records, exact escape list).
@@ -112,9 +117,9 @@ int64_t w12_lo_bytes(int64_t N, int64_t K);  /* Np*Kp/2 */
  * Synchronous: waits on `stream` once to read the escape count.
  * If the tensor needs more than esc_cap escapes the call returns
  * W12_ERR_CAPACITY with out->n_esc = the number needed; the planes, base and
- * esc_row_ptr are complete and the first esc_cap escapes are written, so the
- * caller can grow the escape arrays and call again.  Returns W12_ERR_INVALID
- * if the count would not fit an int32 row offset. */
+ * esc_ptr are complete and the first esc_cap escapes are written, so the
+ * caller can grow the escape array and call again.  Returns W12_ERR_INVALID
+ * if the count would not fit an int32 offset. */
 w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_stream_t stream);
 
 /* ---- w12_decode ----  W12 -> BF16 [N,K] (paper section 4.1: decode is bit
@@ -129,8 +134,9 @@ w12_status w12_decode(const w12_tensor *w, uint16_t *W_out, int64_t ldw, w12_str
  * at least w12_verify_workspace_bytes() bytes, any contents.
  * Synchronous.  Returns W12_OK (0 mismatches), W12_ERR_MISMATCH (>0), or
  * W12_ERR_CORRUPT with *n_mismatch = -1 when the escape list is malformed
- * (row offsets not monotone or not ending at n_esc, a column outside [0,K),
- * columns not strictly ascending inside a row). */
+ * (offsets not starting at 0, not monotone or not ending at n_esc; a key
+ * that is >= 4096 or names a weight outside [N,K]; keys not strictly
+ * ascending inside a group). */
 size_t w12_verify_workspace_bytes(void);
 w12_status w12_verify_roundtrip(const uint16_t *W, int64_t ldw, const w12_tensor *w,
                                 int64_t *n_mismatch, void *workspace, size_t ws_bytes,

@@ -40,7 +40,8 @@ W12_PATH_AUTO, W12_PATH_MMA, W12_PATH_TC = 0, 1, 2
 
 # Every symbol include/w12.h declares.
 EXPORTS = (
-    "w12_rows_padded", "w12_cols_padded", "w12_hi_bytes", "w12_lo_bytes", "w12_encode",
+    "w12_rows_padded", "w12_cols_padded", "w12_hi_bytes", "w12_lo_bytes", "w12_groups",
+    "w12_esc_ptr_len", "w12_encode",
     "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
     "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_workspace_status", "w12_status_string",
     "w12_version",
@@ -57,7 +58,7 @@ class _Tensor(ctypes.Structure):
     _fields_ = [
         ("N", ctypes.c_int64), ("K", ctypes.c_int64),
         ("hi", ctypes.c_void_p), ("lo", ctypes.c_void_p), ("base", ctypes.c_void_p),
-        ("esc_row_ptr", ctypes.c_void_p), ("esc_col", ctypes.c_void_p), ("esc_val", ctypes.c_void_p),
+        ("esc_ptr", ctypes.c_void_p), ("esc", ctypes.c_void_p),
         ("esc_cap", ctypes.c_int64), ("n_esc", ctypes.c_int64),
     ]
 
@@ -89,6 +90,8 @@ def load(path: str | None = None):
             "w12_cols_padded": (i64, [i64]),
             "w12_hi_bytes": (i64, [i64, i64]),
             "w12_lo_bytes": (i64, [i64, i64]),
+            "w12_groups": (i64, [i64]),
+            "w12_esc_ptr_len": (i64, [i64, i64]),
             "w12_encode": (st, [vp, i64, ctypes.POINTER(_Tensor), vp]),
             "w12_decode": (st, [ctypes.POINTER(_Tensor), vp, i64, vp]),
             "w12_verify_workspace_bytes": (sz, []),
@@ -141,44 +144,48 @@ class W12Tensor:
     hi: torch.Tensor       # uint8 [Np*Kp]
     lo: torch.Tensor       # uint8 [Np*Kp/2]
     base: torch.Tensor     # uint8 [N]
-    row_ptr: torch.Tensor  # int32 [N+1]
-    esc_col: torch.Tensor  # int32 [esc_cap]
-    esc_val: torch.Tensor  # int16 [esc_cap] (raw BF16 bits)
+    esc_ptr: torch.Tensor  # int32 [Np/16 * groups(K) + 1]
+    esc: torch.Tensor      # int32 [esc_cap] (bit pattern of key<<16 | BF16 bits)
     n_esc: int
 
     @property
     def esc_cap(self) -> int:
-        return self.esc_col.numel()
+        return self.esc.numel()
 
     def struct(self) -> _Tensor:
         return _Tensor(self.N, self.K, self.hi.data_ptr(), self.lo.data_ptr(), self.base.data_ptr(),
-                       self.row_ptr.data_ptr(), self.esc_col.data_ptr(), self.esc_val.data_ptr(),
-                       self.esc_cap, self.n_esc)
+                       self.esc_ptr.data_ptr(), self.esc.data_ptr(), self.esc_cap, self.n_esc)
 
     def nbytes(self) -> int:
-        """Bytes the GEMM reads: both planes, bases, row offsets, escapes."""
-        return self.hi.numel() + self.lo.numel() + self.N + 4 * (self.N + 1) + 6 * self.n_esc
+        """Bytes the tensor stores (all of which the GEMM reads): both
+        planes, bases, group offsets and escape entries."""
+        return self.hi.numel() + self.lo.numel() + self.N + 4 * self.esc_ptr.numel() + 4 * self.n_esc
 
     def bits_per_weight(self) -> float:
         return 8.0 * self.nbytes() / max(1, self.N * self.K)
 
     def rows(self, n0: int, n1: int) -> "W12Tensor":
         """Rows [n0, n1) as a W12 tensor of their own (n0 a multiple of 16):
-        plane tiles and bases are sliced; the escape offsets are rebased on
-        the device (the new row offsets are a fresh tensor)."""
+        plane tiles, bases and the stripes' escape entries are sliced, the
+        group offsets rebased (a fresh device tensor)."""
         assert 0 <= n0 <= n1 <= self.N and n0 % 16 == 0
-        KT = self.hi.numel() // max(1, rows_padded(self.N)) // 64
+        KT = cols_padded(self.K) // 64
+        G = groups(self.K)
         t0, t1 = n0 // 16, (n1 + 15) // 16
-        rp = self.row_ptr[n0:n1 + 1]
-        e0 = int(rp[0].item())
-        e1 = int(rp[-1].item())
+        ptr = self.esc_ptr[t0 * G:t1 * G + 1]
+        e0 = int(ptr[0].item())
+        e1 = int(ptr[-1].item())
         return W12Tensor(n1 - n0, self.K, self.hi[t0 * KT * 1024:t1 * KT * 1024],
-                         self.lo[t0 * KT * 512:t1 * KT * 512], self.base[n0:n1], (rp - e0).contiguous(),
-                         self.esc_col[e0:e1], self.esc_val[e0:e1], e1 - e0)
+                         self.lo[t0 * KT * 512:t1 * KT * 512], self.base[n0:n1], (ptr - e0).contiguous(),
+                         self.esc[e0:e1], e1 - e0)
 
 
 def rows_padded(N: int) -> int:
     return int(load().w12_rows_padded(N))
+
+
+def groups(K: int) -> int:
+    return int(load().w12_groups(K))
 
 
 def cols_padded(K: int) -> int:
@@ -190,11 +197,10 @@ def empty_tensor(N: int, K: int, esc_cap: int, device) -> W12Tensor:
     hi = torch.empty(max(1, lib.w12_hi_bytes(N, K)), dtype=torch.uint8, device=device)
     lo = torch.empty(max(1, lib.w12_lo_bytes(N, K)), dtype=torch.uint8, device=device)
     base = torch.empty(max(1, N), dtype=torch.uint8, device=device)
-    row_ptr = torch.empty(N + 1, dtype=torch.int32, device=device)
-    esc_col = torch.empty(max(1, esc_cap), dtype=torch.int32, device=device)
-    esc_val = torch.empty(max(1, esc_cap), dtype=torch.int16, device=device)
-    return W12Tensor(N, K, hi[:lib.w12_hi_bytes(N, K)], lo[:lib.w12_lo_bytes(N, K)], base[:N], row_ptr,
-                     esc_col[:esc_cap], esc_val[:esc_cap], 0)
+    esc_ptr = torch.empty(lib.w12_esc_ptr_len(N, K), dtype=torch.int32, device=device)
+    esc = torch.empty(max(1, esc_cap), dtype=torch.int32, device=device)
+    return W12Tensor(N, K, hi[:lib.w12_hi_bytes(N, K)], lo[:lib.w12_lo_bytes(N, K)], base[:N], esc_ptr,
+                     esc[:esc_cap], 0)
 
 
 def w12_encode(W: torch.Tensor, esc_cap: int | None = None, stream=None) -> W12Tensor:
@@ -214,8 +220,7 @@ def w12_encode(W: torch.Tensor, esc_cap: int | None = None, stream=None) -> W12T
             esc_cap = s.n_esc
             continue
         _check(st, "w12_encode")
-        t.esc_col = t.esc_col[:t.n_esc]
-        t.esc_val = t.esc_val[:t.n_esc]
+        t.esc = t.esc[:t.n_esc]
         return t
     raise W12Error(W12_ERR_CAPACITY, "w12_encode")
 

@@ -22,12 +22,13 @@ w12_status check_tensor(const w12_tensor *w) {
     if (!w) return W12_ERR_INVALID;
     if (w->N < 0 || w->K < 0 || w->N > kMaxN || w->K > kMaxK) return W12_ERR_INVALID;
     if (w->esc_cap < 0 || w->n_esc < 0) return W12_ERR_INVALID;
-    if (w->N > 0 && (!w->base || !w->esc_row_ptr)) return W12_ERR_INVALID;
+    if (!w->esc_ptr) return W12_ERR_INVALID;
+    if (w->N > 0 && !w->base) return W12_ERR_INVALID;
     if (w->N > 0 && w->K > 0) {
         if (!w->hi || !w->lo) return W12_ERR_INVALID;
         if (!aligned16(w->hi) || !aligned16(w->lo)) return W12_ERR_ALIGN;
     }
-    if (w->esc_cap > 0 && (!w->esc_col || !w->esc_val)) return W12_ERR_INVALID;
+    if (w->esc_cap > 0 && !w->esc) return W12_ERR_INVALID;
     return W12_OK;
 }
 
@@ -38,12 +39,12 @@ TensorView view_of(const w12_tensor *w) {
     t.Np = rows_padded(w->N);
     t.Kp = cols_padded(w->K);
     t.KT = t.Kp / 64;
+    t.G = groups_of(w->K);
     t.hi = w->hi;
     t.lo = w->lo;
     t.base = w->base;
-    t.row_ptr = w->esc_row_ptr;
-    t.esc_col = w->esc_col;
-    t.esc_val = w->esc_val;
+    t.esc_ptr = w->esc_ptr;
+    t.esc = w->esc;
     t.n_esc = w->n_esc < w->esc_cap ? w->n_esc : w->esc_cap;
     return t;
 }
@@ -99,6 +100,11 @@ int64_t w12_lo_bytes(int64_t N, int64_t K) {
     return (N < 0 || K < 0) ? -1 : rows_padded(N) * cols_padded(K) / 2;
 }
 
+int64_t w12_groups(int64_t K) { return K < 0 ? -1 : groups_of(K); }
+int64_t w12_esc_ptr_len(int64_t N, int64_t K) {
+    return (N < 0 || K < 0) ? -1 : rows_padded(N) / 16 * groups_of(K) + 1;
+}
+
 int32_t w12_version(void) { return (1 << 16) | 0; }
 
 const char *w12_status_string(w12_status s) {
@@ -123,24 +129,18 @@ w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_strea
     if (out->N > 0 && out->K > 0 && !W) return W12_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t N = out->N, K = out->K;
-    if (N == 0) {
-        int32_t zero = 0;
-        if (cudaMemcpyAsync(out->esc_row_ptr, &zero, 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaStreamSynchronize(s) != cudaSuccess)
-            return W12_ERR_CUDA;
-        out->n_esc = 0;
-        return W12_OK;
-    }
-    if (launch_window_count(W, ldw, N, K, out->base, out->esc_row_ptr, s) != cudaSuccess) return W12_ERR_CUDA;
-    if (launch_row_scan(out->esc_row_ptr, N, s) != cudaSuccess) return W12_ERR_CUDA;
+    const int64_t P = rows_padded(N) / 16 * groups_of(K);  // (stripe, group) count
+    if (cudaMemsetAsync(out->esc_ptr, 0, 4 * (size_t)(P + 1), s) != cudaSuccess) return W12_ERR_CUDA;
+    if (launch_window_count(W, ldw, N, K, out->base, out->esc_ptr, s) != cudaSuccess) return W12_ERR_CUDA;
+    if (launch_ptr_scan(out->esc_ptr, P, s) != cudaSuccess) return W12_ERR_CUDA;
     int32_t total = 0;
-    if (cudaMemcpyAsync(&total, out->esc_row_ptr + N, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+    if (cudaMemcpyAsync(&total, out->esc_ptr + P, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return W12_ERR_CUDA;
     if (total < 0) return W12_ERR_INVALID;  // more escapes than an int32 offset can index
     out->n_esc = total;
-    if (launch_pack(W, ldw, N, K, out->base, out->esc_row_ptr, out->hi, out->lo, out->esc_col, out->esc_val,
-                    out->esc_cap, s) != cudaSuccess)
+    if (launch_pack(W, ldw, N, K, out->base, out->esc_ptr, out->hi, out->lo, out->esc, out->esc_cap, s) !=
+        cudaSuccess)
         return W12_ERR_CUDA;
     return total > out->esc_cap ? W12_ERR_CAPACITY : W12_OK;
 }

@@ -1,9 +1,10 @@
-// W12 codec kernels: encode (window search, escape count, row scan, pack),
-// decode, load-time verify and escape-list structure check.
+// W12 codec kernels: encode (window search, escape count, offset scan,
+// pack), decode, load-time verify and escape-list structure check.
 //
 // All of them are HBM-bound integer work (SpecPilot, arXiv 2611.02501,
 // section 4.1: conversion to W12 and the bit-for-bit check of every decoded
-// tensor at load time).
+// tensor at load time).  Work is organised around the 16-row x 256-column
+// group, the unit the escape list is indexed by.
 #include <cstdint>
 #include <cstring>
 
@@ -13,17 +14,34 @@
 namespace w12 {
 namespace {
 
+// Eight consecutive weights of a row, zero past K (0 is "not counted" and
+// "not an escape" for the callers, which mask with k < K anyway).
+__device__ __forceinline__ void load8(const uint16_t *row, bool vec, int64_t k, int64_t K, uint16_t v[8]) {
+    if (vec && k + 8 <= K) {
+        uint4 q = *reinterpret_cast<const uint4 *>(row + k);
+        memcpy(v, &q, 16);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = (k + j < K) ? row[k + j] : 0;
+    }
+}
+
+__device__ __forceinline__ bool is_escape(uint16_t w, int b) {
+    const int e = (w >> 7) & 0xFF;
+    return e == 0 || e == 255 || e < b || e > b + 15;
+}
+
 // ---------------------------------------------------------------------------
 // a1 + a2: one warp per row.  Histogram of the exponent field over the row's
 // normal finite weights, window sums over 16 consecutive exponents, argmax
-// with ties to the largest base; the escape count is K minus the winning
-// window's count.
+// with ties to the largest base.  A second pass over the row counts its
+// escapes per 256-column group into esc_ptr[t*G+g+1].
 // ---------------------------------------------------------------------------
 constexpr int kWinWarps = 8;
 
 __global__ __launch_bounds__(kWinWarps * 32) void k_window_count(
     const uint16_t *__restrict__ W, int64_t ldw, int64_t N, int64_t K, uint8_t *__restrict__ base,
-    int32_t *__restrict__ row_ptr) {
+    int32_t *__restrict__ esc_ptr) {
     __shared__ int hist[kWinWarps][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n = (int64_t)blockIdx.x * kWinWarps + warp;
@@ -36,13 +54,7 @@ __global__ __launch_bounds__(kWinWarps * 32) void k_window_count(
     for (int64_t k0 = 0; k0 < K; k0 += 256) {
         const int64_t k = k0 + lane * 8;
         uint16_t v[8];
-        if (vec && k + 8 <= K) {
-            uint4 q = *reinterpret_cast<const uint4 *>(row + k);
-            memcpy(v, &q, 16);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = (k + j < K) ? row[k + j] : 0;
-        }
+        load8(row, vec, k, K, v);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int e = (v[j] >> 7) & 0xFF;
@@ -72,23 +84,34 @@ __global__ __launch_bounds__(kWinWarps * 32) void k_window_count(
             best_b = obb;
         }
     }
-    if (lane == 0) {
-        base[n] = (uint8_t)best_b;
-        row_ptr[n + 1] = (int32_t)(K - best);
+    if (lane == 0) base[n] = (uint8_t)best_b;
+    // escapes per 256-column group (the row was just read: mostly L2 hits)
+    const int64_t G = groups_of(K);
+    int32_t *cnt = esc_ptr + 1 + (n / 16) * G;
+    for (int64_t k0 = 0, g = 0; k0 < K; k0 += 256, ++g) {
+        const int64_t k = k0 + lane * 8;
+        uint16_t v[8];
+        load8(row, vec, k, K, v);
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c += (k + j < K) && is_escape(v[j], best_b);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+        if (lane == 0 && c) atomicAdd(&cnt[g], c);
     }
 }
 
 // ---------------------------------------------------------------------------
-// a2: inclusive scan of the per-row counts in row_ptr[1..N] (one block).
-// row_ptr[N] = -1 flags a total that does not fit an int32 offset.
+// a2: inclusive scan of the per-group counts in esc_ptr[1..P] (one block).
+// esc_ptr[P] = -1 flags a total that does not fit an int32 offset.
 // ---------------------------------------------------------------------------
-__global__ __launch_bounds__(1024) void k_row_scan(int32_t *__restrict__ row_ptr, int64_t N) {
+__global__ __launch_bounds__(1024) void k_ptr_scan(int32_t *__restrict__ ptr, int64_t P) {
     __shared__ long long warp_sums[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     long long carry = 0;
-    for (int64_t c0 = 0; c0 < N; c0 += 1024) {
+    for (int64_t c0 = 0; c0 < P; c0 += 1024) {
         const int64_t i = c0 + threadIdx.x;
-        long long v = (i < N) ? (long long)row_ptr[i + 1] : 0;
+        long long v = (i < P) ? (long long)ptr[i + 1] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const long long t = __shfl_up_sync(kFull, v, o);
@@ -107,96 +130,98 @@ __global__ __launch_bounds__(1024) void k_row_scan(int32_t *__restrict__ row_ptr
         }
         __syncthreads();
         const long long incl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + v;
-        if (i < N) row_ptr[i + 1] = (int32_t)(incl > 0x7fffffffLL ? -1 : incl);
+        if (i < P) ptr[i + 1] = (int32_t)(incl > 0x7fffffffLL ? -1 : incl);
         carry += warp_sums[31];
         __syncthreads();
     }
     if (threadIdx.x == 0) {
-        row_ptr[0] = 0;
-        if (carry > 0x7fffffffLL) row_ptr[N] = -1;
+        ptr[0] = 0;
+        if (carry > 0x7fffffffLL) ptr[P] = -1;
     }
 }
 
 // ---------------------------------------------------------------------------
 // a3: pack.  One block per 16-row stripe, one warp per row; each step covers
-// 256 columns (4 tiles).  Records are assembled into the tile layout in
-// shared memory and written out as whole tiles; escapes are written in
-// column order at row_ptr[n] + rank (rank from a warp prefix sum).
+// one 256-column group (4 tiles, 8 columns per lane).  Records are assembled
+// into the tile layout in shared memory and written out as whole tiles.  An
+// escape at (tile c4, row i, column j) goes to
+//   esc_ptr[t*G+g] + #escapes of the group before (c4,i) + rank inside (c4,i)
+// with the per-(c4,i) counts exchanged through shared memory.
 // ---------------------------------------------------------------------------
 __global__ __launch_bounds__(512) void k_pack(const uint16_t *__restrict__ W, int64_t ldw, int64_t N,
                                               int64_t K, const uint8_t *__restrict__ base,
-                                              const int32_t *__restrict__ row_ptr,
+                                              const int32_t *__restrict__ esc_ptr,
                                               uint8_t *__restrict__ hi, uint8_t *__restrict__ lo,
-                                              int32_t *__restrict__ esc_col,
-                                              uint16_t *__restrict__ esc_val, int64_t esc_cap) {
+                                              uint32_t *__restrict__ esc, int64_t esc_cap) {
     __shared__ __align__(16) uint8_t sh_hi[4 * kHiTileBytes];
     __shared__ __align__(16) uint8_t sh_lo[4 * kLoTileBytes];
+    __shared__ int sh_cnt[2][64];  // [c4*16 + i]: counts, then exclusive prefix
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = blockIdx.x;
-    const int64_t Kp = cols_padded(K), KT = Kp / 64;
+    const int64_t Kp = cols_padded(K), KT = Kp / 64, G = groups_of(K);
     const int i = warp;  // row inside the stripe
     const int64_t n = t * 16 + i;
     const bool row_ok = n < N;
     const int b = row_ok ? base[n] : 0;
-    int64_t eidx = row_ok ? row_ptr[n] : 0;
     const uint16_t *row = W + (row_ok ? n : 0) * ldw;
     const bool vec = row_ok && (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    const int c4 = lane >> 3;         // tile inside the group
+    const int jl = (lane & 7) * 8;    // first column inside the tile
+    const int L = (i & 7) * 4 + (jl >> 4);  // fragment slot
 
-    for (int64_t k0 = 0; k0 < Kp; k0 += 256) {
-        const int64_t k = k0 + lane * 8;
+    for (int64_t g = 0; g < G; ++g) {
+        const int buf = (int)(g & 1);
+        const int64_t k = g * 256 + lane * 8;
         uint16_t v[8];
-        if (vec && k + 8 <= K) {
-            uint4 q = *reinterpret_cast<const uint4 *>(row + k);
-            memcpy(v, &q, 16);
+        if (row_ok) {
+            load8(row, vec, k, K, v);
         } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = (row_ok && k + j < K) ? row[k + j] : 0;
+            for (int j = 0; j < 8; ++j) v[j] = 0;
         }
         uint32_t rec[8];
         unsigned emask = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const bool in = row_ok && (k + j < K);
+            const bool esc_ = in && is_escape(v[j], b);
+            if (esc_) emask |= 1u << j;
             const int e = (v[j] >> 7) & 0xFF;
-            const bool esc = in && (e == 0 || e == 255 || e < b || e > b + 15);
-            if (esc) emask |= 1u << j;
-            rec[j] = (in && !esc) ? (uint32_t)(((v[j] >> 15) << 11) | ((e - b) << 7) | (v[j] & 0x7F)) : 0u;
+            rec[j] = (in && !esc_) ? (uint32_t)(((v[j] >> 15) << 11) | ((e - b) << 7) | (v[j] & 0x7F)) : 0u;
         }
+        // per-(c4, i) count and this lane's exclusive prefix inside its 8 lanes
         const int cnt = __popc(emask);
         int incl = cnt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int tmp = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += tmp;
+        for (int o = 1; o < 8; o <<= 1) {
+            const int tmp = __shfl_up_sync(kFull, incl, o, 8);
+            if ((lane & 7) >= o) incl += tmp;
         }
-        const int total = __shfl_sync(kFull, incl, 31);
-        int64_t pos = eidx + (incl - cnt);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if ((emask >> j) & 1u) {
-                if (pos < esc_cap) {
-                    esc_col[pos] = (int32_t)(k + j);
-                    esc_val[pos] = v[j];
-                }
-                ++pos;
-            }
-        }
-        eidx += total;
+        if ((lane & 7) == 7) sh_cnt[buf][c4 * 16 + i] = incl;
         if (k < Kp) {
-            const int c_local = lane >> 3;
-            const int jl = (lane & 7) * 8;          // column inside the tile
-            const int L = (i & 7) * 4 + (jl >> 4);  // slot
             const uint32_t h0 = (rec[0] >> 4) | ((rec[1] >> 4) << 8) | ((rec[2] >> 4) << 16) | ((rec[3] >> 4) << 24);
             const uint32_t h1 = (rec[4] >> 4) | ((rec[5] >> 4) << 8) | ((rec[6] >> 4) << 16) | ((rec[7] >> 4) << 24);
-            *reinterpret_cast<uint2 *>(sh_hi + c_local * kHiTileBytes + (i >> 3) * 512 + L * 16 + (jl & 15)) =
+            *reinterpret_cast<uint2 *>(sh_hi + c4 * kHiTileBytes + (i >> 3) * 512 + L * 16 + (jl & 15)) =
                 make_uint2(h0, h1);
             uint32_t lw = 0;
 #pragma unroll
             for (int u = 0; u < 4; ++u) lw |= (((rec[u] & 0xFu) << 4) | (rec[u + 4] & 0xFu)) << (8 * u);
-            *reinterpret_cast<uint32_t *>(sh_lo + c_local * kLoTileBytes + L * 16 + (i >> 3) * 8 + ((jl & 15) >> 3) * 4) = lw;
+            *reinterpret_cast<uint32_t *>(sh_lo + c4 * kLoTileBytes + L * 16 + (i >> 3) * 8 + ((jl & 15) >> 3) * 4) = lw;
         }
         __syncthreads();
-        const int64_t c_first = k0 / 64;
+        if (warp == 0) {  // exclusive scan of the 64 counts in (c4, i) order
+            const int a0 = sh_cnt[buf][2 * lane], a1 = sh_cnt[buf][2 * lane + 1];
+            int s = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tmp = __shfl_up_sync(kFull, s, o);
+                if (lane >= o) s += tmp;
+            }
+            const int ex = s - a0 - a1;
+            sh_cnt[buf][2 * lane] = ex;
+            sh_cnt[buf][2 * lane + 1] = ex + a0;
+        }
+        const int64_t c_first = g * 4;
         const int ntiles = (int)((KT - c_first) < 4 ? (KT - c_first) : 4);
         for (int x = threadIdx.x; x < ntiles * 96; x += blockDim.x) {
             if (x < ntiles * 64) {
@@ -211,22 +236,32 @@ __global__ __launch_bounds__(512) void k_pack(const uint16_t *__restrict__ W, in
             }
         }
         __syncthreads();
+        if (emask) {
+            int64_t pos = (int64_t)esc_ptr[t * G + g] + sh_cnt[buf][c4 * 16 + i] + (incl - cnt);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if ((emask >> j) & 1u) {
+                    if (pos < esc_cap)
+                        esc[pos] = ((uint32_t)((c4 << 10) | (i << 6) | (jl + j)) << 16) | v[j];
+                    ++pos;
+                }
+            }
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
-// a4 / a5: decode a (stripe, 256-column chunk) into shared memory, apply the
-// escapes of the chunk, then either store it (decode) or compare it with the
-// original bits (verify).
+// a4 / a5: decode one (stripe, group) into shared memory, apply the group's
+// escapes (one thread per entry), then either store it (decode) or compare
+// it with the original bits (verify).
 // ---------------------------------------------------------------------------
 constexpr int kStageStride = 256 + 8;  // elements; 528 bytes keeps 16-byte alignment
 
-__global__ __launch_bounds__(256) void k_decode_chunk(TensorView t, uint16_t *__restrict__ out, int64_t ldo,
+__global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__restrict__ out, int64_t ldo,
                                                       const uint16_t *__restrict__ W_cmp, int64_t ldw,
                                                       unsigned long long *__restrict__ mismatches) {
     __shared__ __align__(16) uint16_t stage[16 * kStageStride];
-    const int64_t nchunk = (t.KT + 3) / 4;
-    const int64_t st = blockIdx.x / nchunk, c0 = (blockIdx.x % nchunk) * 4;
+    const int64_t st = blockIdx.x / t.G, g = blockIdx.x % t.G, c0 = g * 4;
     const int tid = threadIdx.x;
     {
         const int ct = tid >> 6, h = (tid >> 5) & 1, L = tid & 31;
@@ -245,18 +280,15 @@ __global__ __launch_bounds__(256) void k_decode_chunk(TensorView t, uint16_t *__
         }
     }
     __syncthreads();
-    if (tid < 16) {
-        const int64_t n = st * 16 + tid;
-        if (n < t.N) {
-            int64_t lo, hi;
-            escape_range(t.row_ptr, n, t.n_esc, lo, hi);
-            const int64_t k0 = c0 * 64;
-            const int64_t k1 = (k0 + 256 < t.K) ? k0 + 256 : t.K;
-            for (int64_t e = lower_bound_col(t.esc_col, lo, hi, k0); e < hi; ++e) {
-                const int64_t col = t.esc_col[e];
-                if (col >= k1) break;
-                if (col >= k0) stage[tid * kStageStride + (col - k0)] = t.esc_val[e];
-            }
+    {
+        int64_t p0, p1;
+        escape_range(t.esc_ptr, st * t.G + g, t.n_esc, p0, p1);
+        for (int64_t e = p0 + tid; e < p1; e += blockDim.x) {
+            const uint32_t ent = t.esc[e];
+            const int key = (int)(ent >> 16);
+            const int r = (key >> 6) & 15, col = 64 * (key >> 10) + (key & 63);
+            if (key < 4096 && st * 16 + r < t.N && g * 256 + col < t.K)
+                stage[r * kStageStride + col] = (uint16_t)(ent & 0xFFFFu);
         }
     }
     __syncthreads();
@@ -298,28 +330,31 @@ __global__ __launch_bounds__(256) void k_decode_chunk(TensorView t, uint16_t *__
 // ---------------------------------------------------------------------------
 // Escape-list structure checks.
 // ---------------------------------------------------------------------------
-__global__ void k_check_rows(const int32_t *__restrict__ row_ptr, int64_t N, int64_t n_esc,
-                             unsigned long long *__restrict__ bad) {
+__global__ void k_check_ptr(const int32_t *__restrict__ ptr, int64_t P, int64_t n_esc,
+                            unsigned long long *__restrict__ bad) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i > N) return;
+    if (i > P) return;
     int v = 0;
-    if (i == 0 && row_ptr[0] != 0) ++v;
-    if (i == N && (int64_t)row_ptr[N] != n_esc) ++v;
-    if (i < N && row_ptr[i + 1] < row_ptr[i]) ++v;
+    if (i == 0 && ptr[0] != 0) ++v;
+    if (i == P && (int64_t)ptr[P] != n_esc) ++v;
+    if (i < P && ptr[i + 1] < ptr[i]) ++v;
     if (v) atomicAdd(bad, (unsigned long long)v);
 }
 
-__global__ void k_check_cols(TensorView t, unsigned long long *__restrict__ bad) {
+// One warp per (stripe, group).
+__global__ void k_check_entries(TensorView t, unsigned long long *__restrict__ bad) {
     const int lane = threadIdx.x & 31;
-    const int64_t n = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (n >= t.N) return;
-    int64_t lo, hi;
-    escape_range(t.row_ptr, n, t.n_esc, lo, hi);
+    const int64_t grp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (grp >= (t.Np / 16) * t.G) return;
+    const int64_t st = grp / t.G, g = grp % t.G;
+    int64_t p0, p1;
+    escape_range(t.esc_ptr, grp, t.n_esc, p0, p1);
     int v = 0;
-    for (int64_t e = lo + lane; e < hi; e += 32) {
-        const int32_t col = t.esc_col[e];
-        if (col < 0 || col >= t.K) ++v;
-        if (e + 1 < hi && t.esc_col[e + 1] <= col) ++v;
+    for (int64_t e = p0 + lane; e < p1; e += 32) {
+        const uint32_t key = t.esc[e] >> 16;
+        const int64_t n = st * 16 + ((key >> 6) & 15), k = g * 256 + 64 * (key >> 10) + (key & 63);
+        if (key >= 4096 || n >= t.N || k >= t.K) ++v;
+        if (e + 1 < p1 && (t.esc[e + 1] >> 16) <= key) ++v;
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
@@ -329,51 +364,50 @@ __global__ void k_check_cols(TensorView t, unsigned long long *__restrict__ bad)
 }  // namespace
 
 cudaError_t launch_window_count(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base,
-                                int32_t *row_ptr, cudaStream_t s) {
+                                int32_t *esc_ptr, cudaStream_t s) {
     if (N == 0) return cudaSuccess;
     const int64_t blocks = (N + kWinWarps - 1) / kWinWarps;
-    k_window_count<<<(unsigned)blocks, kWinWarps * 32, 0, s>>>(W, ldw, N, K, base, row_ptr);
+    k_window_count<<<(unsigned)blocks, kWinWarps * 32, 0, s>>>(W, ldw, N, K, base, esc_ptr);
     return cudaGetLastError();
 }
 
-cudaError_t launch_row_scan(int32_t *row_ptr, int64_t N, cudaStream_t s) {
-    k_row_scan<<<1, 1024, 0, s>>>(row_ptr, N);
+cudaError_t launch_ptr_scan(int32_t *esc_ptr, int64_t P, cudaStream_t s) {
+    k_ptr_scan<<<1, 1024, 0, s>>>(esc_ptr, P);
     return cudaGetLastError();
 }
 
 cudaError_t launch_pack(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const uint8_t *base,
-                        const int32_t *row_ptr, uint8_t *hi, uint8_t *lo, int32_t *esc_col,
-                        uint16_t *esc_val, int64_t esc_cap, cudaStream_t s) {
+                        const int32_t *esc_ptr, uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap,
+                        cudaStream_t s) {
     const int64_t stripes = rows_padded(N) / 16;
     if (stripes == 0 || K == 0) return cudaSuccess;
-    k_pack<<<(unsigned)stripes, 512, 0, s>>>(W, ldw, N, K, base, row_ptr, hi, lo, esc_col, esc_val, esc_cap);
+    k_pack<<<(unsigned)stripes, 512, 0, s>>>(W, ldw, N, K, base, esc_ptr, hi, lo, esc, esc_cap);
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s) {
-    const int64_t blocks = (t.Np / 16) * ((t.KT + 3) / 4);
+    const int64_t blocks = (t.Np / 16) * t.G;
     if (blocks == 0) return cudaSuccess;
-    k_decode_chunk<<<(unsigned)blocks, 256, 0, s>>>(t, out, ldo, nullptr, 0, nullptr);
+    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, out, ldo, nullptr, 0, nullptr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_verify(const TensorView &t, const uint16_t *W, int64_t ldw, unsigned long long *count,
                           cudaStream_t s) {
-    const int64_t blocks = (t.Np / 16) * ((t.KT + 3) / 4);
+    const int64_t blocks = (t.Np / 16) * t.G;
     if (blocks == 0) return cudaSuccess;
-    k_decode_chunk<<<(unsigned)blocks, 256, 0, s>>>(t, nullptr, 0, W, ldw, count);
+    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, nullptr, 0, W, ldw, count);
     return cudaGetLastError();
 }
 
 cudaError_t launch_check_structure(const TensorView &t, int64_t esc_cap, unsigned long long *bad,
                                    cudaStream_t s) {
     (void)esc_cap;
-    const int64_t b1 = (t.N + 1 + 255) / 256;
-    k_check_rows<<<(unsigned)b1, 256, 0, s>>>(t.row_ptr, t.N, t.n_esc, bad);
+    const int64_t P = (t.Np / 16) * t.G;
+    k_check_ptr<<<(unsigned)((P + 1 + 255) / 256), 256, 0, s>>>(t.esc_ptr, P, t.n_esc, bad);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || t.N == 0) return e;
-    const int64_t b2 = (t.N * 32 + 255) / 256;
-    k_check_cols<<<(unsigned)b2, 256, 0, s>>>(t, bad);
+    if (e != cudaSuccess || P == 0) return e;
+    k_check_entries<<<(unsigned)((P * 32 + 255) / 256), 256, 0, s>>>(t, bad);
     return cudaGetLastError();
 }
 

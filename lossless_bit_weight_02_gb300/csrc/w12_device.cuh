@@ -58,25 +58,12 @@ __device__ __forceinline__ void decode16(uint4 h, uint32_t l0, uint32_t l1, uint
     out[7] = decode_pair(prmt(h.w, l1s, 0x3726), base2);
 }
 
-// First index in esc_col[lo, hi) whose column is >= k (columns ascend within
-// a row).
-__device__ __forceinline__ int64_t lower_bound_col(const int32_t *__restrict__ esc_col, int64_t lo,
-                                                   int64_t hi, int64_t k) {
-    while (lo < hi) {
-        int64_t mid = (lo + hi) >> 1;
-        if (esc_col[mid] < k)
-            lo = mid + 1;
-        else
-            hi = mid;
-    }
-    return lo;
-}
-
-// The escape range of row n, clamped to [0, n_esc] so that a malformed row
-// offset can never index outside the escape arrays.
-__device__ __forceinline__ void escape_range(const int32_t *__restrict__ row_ptr, int64_t n,
-                                             int64_t n_esc, int64_t &lo, int64_t &hi) {
-    int64_t a = row_ptr[n], b = row_ptr[n + 1];
+// Entries [lo, hi) of offset slot i (ptr[i] .. ptr[i+1]), clamped to
+// [0, n_esc] so that a malformed offset can never index outside the escape
+// array.
+__device__ __forceinline__ void escape_range(const int32_t *__restrict__ ptr, int64_t i, int64_t n_esc,
+                                             int64_t &lo, int64_t &hi) {
+    int64_t a = ptr[i], b = ptr[i + 1];
     a = a < 0 ? 0 : (a > n_esc ? n_esc : a);
     b = b < a ? a : (b > n_esc ? n_esc : b);
     lo = a;

@@ -19,7 +19,6 @@
 //     go to an FP32 workspace and the last warp to finish a stripe sums them
 //     in the order s = 0..S-1 and writes BF16.  S depends on (M, N, K) only,
 //     so the result is identical for any grid.
-#include <climits>
 #include <cstdint>
 
 #include "w12_device.cuh"
@@ -66,6 +65,33 @@ __device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int
     }
 }
 
+// Escape entries of one 256-column group, one per lane (lane < cnt).
+struct EscBatch {
+    uint32_t ent;  // key<<16 | BF16 bits
+    int cnt;       // entries in the group (warp-uniform)
+    int64_t p0;    // index of the group's first entry
+};
+
+__device__ __forceinline__ EscBatch load_group_escapes(const TensorView &t, int64_t p0, int64_t p1, int lane) {
+    EscBatch b;
+    b.p0 = p0;
+    b.cnt = (int)(p1 - p0);
+    b.ent = (lane < b.cnt) ? __ldg(t.esc + p0 + lane) : 0u;
+    return b;
+}
+
+// Writes escape `ent` (key<<16 | bits) of tile c4 into the per-warp copy of
+// the A fragments: slot = 4*(row%8) + col/16, component (pair&1)*2 + row/8,
+// half = col&1.
+__device__ __forceinline__ void patch_one(uint4 (*patch)[32], uint32_t ent) {
+    const int key = (int)(ent >> 16);
+    const int r = (key >> 6) & 15, j = key & 63;
+    const int slot = (r & 7) * 4 + (j >> 4);
+    const int j16 = j & 15, pr = j16 >> 1;
+    const int comp = (pr & 1) * 2 + (r >> 3);
+    reinterpret_cast<uint16_t *>(&patch[pr >> 1][slot])[comp * 2 + (j16 & 1)] = (uint16_t)(ent & 0xFFFFu);
+}
+
 template <int NB>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16)
 __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs g) {
     __shared__ __align__(16) uint4 patch[kWarps][4][32];
@@ -80,23 +106,61 @@ __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs
          item += (int64_t)gridDim.x * kWarps) {
         const int64_t st = item / S;
         const int s = (int)(item % S);
-        const int64_t c_beg = (s * t.KT) / S, c_end = ((s + 1) * t.KT) / S;
+        // Chunk s covers whole 256-column groups [g_beg, g_end).
+        const int64_t g_beg = (s * t.G) / S, g_end = ((s + 1) * t.G) / S;
+        const int64_t c_beg = 4 * g_beg;
+        const int64_t c_end = (4 * g_end < t.KT) ? 4 * g_end : t.KT;
         const int64_t n0 = st * 16;
         const int64_t rowA = n0 + gid, rowB = n0 + gid + 8;
-        const uint32_t base2A = (rowA < t.N ? (uint32_t)t.base[rowA] : 0u) * 0x00800080u;
-        const uint32_t base2B = (rowB < t.N ? (uint32_t)t.base[rowB] : 0u) * 0x00800080u;
 
-        // Escape cursor: lane r < 16 walks the escapes of row n0 + r.
-        int64_t e_cur = 0, e_end = 0;
-        int64_t e_col = LLONG_MAX;
-        uint16_t e_val = 0;
-        if (lane < 16 && n0 + lane < t.N) {
-            escape_range(t.row_ptr, n0 + lane, t.n_esc, e_cur, e_end);
-            if (c_beg > 0) e_cur = lower_bound_col(t.esc_col, e_cur, e_end, c_beg * 64);
-            if (e_cur < e_end) {
-                e_col = t.esc_col[e_cur];
-                e_val = t.esc_val[e_cur];
+        // 1. weight stream first, so that its latency covers the set-up below
+        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + st * t.KT * 64 + lane;
+        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + st * t.KT * 32 + lane;
+        uint4 bh0[kPrefetch], bh1[kPrefetch], bl[kPrefetch];
+#pragma unroll
+        for (int p = 0; p < kPrefetch; ++p) {
+            const int64_t c = c_beg + p;
+            if (c < c_end) {
+                bh0[p] = ld_stream(hp + c * 64);
+                bh1[p] = ld_stream(hp + c * 64 + 32);
+                bl[p] = ld_stream(lp + c * 32);
             }
+        }
+        // 2. bases, group offsets (lane l holds the offset of group g_beg + l),
+        //    escapes of the first two groups
+        const uint32_t base2A = (rowA < t.N ? (uint32_t)__ldg(t.base + rowA) : 0u) * 0x00800080u;
+        const uint32_t base2B = (rowB < t.N ? (uint32_t)__ldg(t.base + rowB) : 0u) * 0x00800080u;
+        const int64_t pbase = st * t.G;
+        int64_t gw0 = g_beg;  // first group of the offset window
+        auto load_window = [&](int64_t first) -> int64_t {
+            const int64_t gi = first + lane;
+            int64_t v = 0;
+            if (gi <= g_end) {
+                v = __ldg(t.esc_ptr + pbase + gi);
+                v = v < 0 ? 0 : (v > t.n_esc ? t.n_esc : v);
+            }
+            return v;
+        };
+        int64_t ptrw = load_window(gw0);
+        auto group_bounds = [&](int64_t gg, int64_t &p0, int64_t &p1) {
+            if (gg + 1 - gw0 >= 32) {  // slide the window (rare: > 30 groups per chunk)
+                gw0 = gg;
+                ptrw = load_window(gw0);
+            }
+            p0 = __shfl_sync(kFull, ptrw, (int)(gg - gw0));
+            p1 = __shfl_sync(kFull, ptrw, (int)(gg + 1 - gw0));
+            if (p1 < p0) p1 = p0;
+        };
+        int64_t p0, p1;
+        group_bounds(g_beg, p0, p1);
+        EscBatch cur = load_group_escapes(t, p0, p1, lane);
+        EscBatch nxt;
+        nxt.cnt = 0;
+        nxt.ent = 0;
+        nxt.p0 = 0;
+        if (g_beg + 1 < g_end) {
+            group_bounds(g_beg + 1, p0, p1);
+            nxt = load_group_escapes(t, p0, p1, lane);
         }
 
         // Activation rows of this lane (token m = 8*b + gid).
@@ -113,22 +177,10 @@ __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs
 #pragma unroll
         for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
 
-        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + st * t.KT * 64 + lane;
-        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + st * t.KT * 32 + lane;
-        uint4 bh0[kPrefetch], bh1[kPrefetch], bl[kPrefetch];
+        for (int64_t gg = g_beg; gg < g_end; ++gg) {
+            const int64_t cc = 4 * gg;
 #pragma unroll
-        for (int p = 0; p < kPrefetch; ++p) {
-            const int64_t c = c_beg + p;
-            if (c < c_end) {
-                bh0[p] = ld_stream(hp + c * 64);
-                bh1[p] = ld_stream(hp + c * 64 + 32);
-                bl[p] = ld_stream(lp + c * 32);
-            }
-        }
-
-        for (int64_t cc = c_beg; cc < c_end; cc += kPrefetch) {
-#pragma unroll
-            for (int p = 0; p < kPrefetch; ++p) {
+            for (int p = 0; p < kPrefetch; ++p) {  // tile p of the group
                 const int64_t c = cc + p;
                 if (c < c_end) {
                     uint32_t dA[8], dB[8];
@@ -142,30 +194,21 @@ __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs
                     }
 
                     // Escapes of this tile replace the decoded placeholders.
-                    const int64_t k_lo = c * 64, k_hi = k_lo + 64;
-                    bool pend = e_col < k_hi;
-                    if (__any_sync(kFull, pend)) {
+                    const bool mine = lane < cur.cnt && (int)(cur.ent >> 26) == p;
+                    const bool many = cur.cnt > 32;  // warp-uniform
+                    if (__any_sync(kFull, mine) || many) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             patch[warp][i][lane] = make_uint4(dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1]);
                         __syncwarp();
-                        while (pend) {
-                            const int64_t kl = e_col - k_lo;
-                            if (kl >= 0) {
-                                const int r = lane;
-                                const int slot = (r & 7) * 4 + (int)(kl >> 4);
-                                const int j16 = (int)(kl & 15), pr = j16 >> 1;
-                                const int comp = (pr & 1) * 2 + (r >> 3);
-                                reinterpret_cast<uint16_t *>(&patch[warp][pr >> 1][slot])[comp * 2 + (j16 & 1)] = e_val;
+                        if (!many) {
+                            if (mine) patch_one(patch[warp], cur.ent);
+                        } else {
+                            // more than 32 escapes in the group: walk it in batches of 32
+                            for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
+                                const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
+                                if (b0 + lane < cur.cnt && (int)(e >> 26) == p) patch_one(patch[warp], e);
                             }
-                            ++e_cur;
-                            if (e_cur < e_end) {
-                                e_col = t.esc_col[e_cur];
-                                e_val = t.esc_val[e_cur];
-                            } else {
-                                e_col = LLONG_MAX;
-                            }
-                            pend = e_col < k_hi;
                         }
                         __syncwarp();
 #pragma unroll
@@ -184,7 +227,7 @@ __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
                         if (mval[b]) {
-                            load_act16(arow[b], k_lo + 16 * q, t.K, bw[b]);
+                            load_act16(arow[b], c * 64 + 16 * q, t.K, bw[b]);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 8; ++j) bw[b][j] = 0u;
@@ -198,6 +241,12 @@ __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs
                                      bw[b][2 * i + 1]);
                     }
                 }
+            }
+            // next group's escapes are already in flight; fetch the one after
+            cur = nxt;
+            if (gg + 2 < g_end) {
+                group_bounds(gg + 2, p0, p1);
+                nxt = load_group_escapes(t, p0, p1, lane);
             }
         }
 
@@ -297,16 +346,16 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
 
 int64_t gemm_mma_partial_cols(int64_t M) { return M <= 8 ? 8 : 16; }
 
-// Split factor from (M, N, K) only: enough (stripe, chunk) items to keep
-// about 16 warps on each of 152 SMs streaming, at least 4 tiles per chunk.
+// Split factor from (M, N, K) only: as many (stripe, chunk) items as fit
+// one wave of 16 resident warps on each of 152 SMs, chunks of whole
+// 256-column groups.
 int gemm_mma_split(int64_t M, int64_t N, int64_t K) {
     (void)M;
-    const int64_t T = (N + 15) / 16, KT = (K + 63) / 64;
-    if (T == 0 || KT == 0) return 1;
+    const int64_t T = (N + 15) / 16, G = groups_of(K);
+    if (T == 0 || G == 0) return 1;
     const int64_t target = 152 * 16;
-    int64_t S = (target + T / 2) / T;
-    const int64_t smax = KT / 4 > 1 ? KT / 4 : 1;
-    if (S > smax) S = smax;
+    int64_t S = target / T;
+    if (S > G) S = G;
     if (S > 32) S = 32;
     if (S < 1) S = 1;
     return (int)S;

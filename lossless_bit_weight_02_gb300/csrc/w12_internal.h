@@ -12,26 +12,29 @@ namespace w12 {
 // Device view of a W12 tensor (plain pointers, sizes precomputed).
 struct TensorView {
     int64_t N, K, Np, Kp, KT;  // KT = Kp / 64 tiles per row stripe
+    int64_t G;                 // 256-column groups per stripe
     const uint8_t *hi;
     const uint8_t *lo;
     const uint8_t *base;
-    const int32_t *row_ptr;
-    const int32_t *esc_col;
-    const uint16_t *esc_val;
+    const int32_t *esc_ptr;    // [Np/16*G + 1]
+    const uint32_t *esc;       // entries key<<16 | BF16 bits
     int64_t n_esc;
 };
 
+__host__ __device__ inline int64_t groups_of(int64_t K) { return ((K + 63) / 64 + 3) / 4; }
+
 // ---- codec (w12_codec.cu) ----
-// a1 + a2: base[n] and the escape count of row n into row_ptr[n+1].
+// a1 + a2: base[n] and, added into esc_ptr[t*G+g+1] (zeroed by the caller),
+// the escape count of every (stripe, group).
 cudaError_t launch_window_count(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base,
-                                int32_t *row_ptr, cudaStream_t s);
-// a2: in-place scan of row_ptr[1..N] and row_ptr[0] = 0; row_ptr[N] = -1 on
+                                int32_t *esc_ptr, cudaStream_t s);
+// a2: in-place scan of esc_ptr[1..P] and esc_ptr[0] = 0; esc_ptr[P] = -1 on
 // int32 overflow.
-cudaError_t launch_row_scan(int32_t *row_ptr, int64_t N, cudaStream_t s);
+cudaError_t launch_ptr_scan(int32_t *esc_ptr, int64_t P, cudaStream_t s);
 // a3: planes + escapes (escape writes limited to esc_cap).
 cudaError_t launch_pack(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const uint8_t *base,
-                        const int32_t *row_ptr, uint8_t *hi, uint8_t *lo, int32_t *esc_col,
-                        uint16_t *esc_val, int64_t esc_cap, cudaStream_t s);
+                        const int32_t *esc_ptr, uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap,
+                        cudaStream_t s);
 // a4
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s);
 // escape-list structure violations added to *bad (device counter).

@@ -68,12 +68,15 @@ def _load():
             "w12ref_is_escape": (ctypes.c_int, [ctypes.c_uint16, ctypes.c_int]),
             "w12ref_record": (ctypes.c_int, [ctypes.c_uint16, ctypes.c_int]),
             "w12ref_decode_record": (ctypes.c_uint16, [ctypes.c_int, ctypes.c_int]),
-            "w12ref_encode": (ctypes.c_int, [p, i64, i64, i64, p, p, p, p, p, p, i64, p]),
+            "w12ref_groups": (i64, [i64]),
+            "w12ref_ptr_len": (i64, [i64, i64]),
+            "w12ref_key": (ctypes.c_int, [i64, i64]),
+            "w12ref_encode": (ctypes.c_int, [p, i64, i64, i64, p, p, p, p, p, i64, p]),
             "w12ref_check_structure": (i64, [i64, i64, p, p, i64, i64]),
-            "w12ref_decode": (ctypes.c_int, [i64, i64, p, p, p, p, p, p, i64, p, i64]),
-            "w12ref_verify": (ctypes.c_int, [p, i64, i64, i64, p, p, p, p, p, p, i64, i64, p]),
-            "w12ref_gemm": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, p, p, i64, p, i64, p, p]),
-            "w12ref_gemm_sample": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, p, p, i64,
+            "w12ref_decode": (ctypes.c_int, [i64, i64, p, p, p, p, p, i64, p, i64]),
+            "w12ref_verify": (ctypes.c_int, [p, i64, i64, i64, p, p, p, p, p, i64, i64, p]),
+            "w12ref_gemm": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, p, i64, p, i64, p, p]),
+            "w12ref_gemm_sample": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, p, i64,
                                                   p, p, i64, p, p, p]),
             "w12ref_bits_per_weight": (ctypes.c_double, [i64, i64, i64]),
             "w12ref_num_threads": (ctypes.c_int, []),
@@ -99,21 +102,48 @@ class W12Ref:
     hi: np.ndarray        # uint8 [Np*Kp]
     lo: np.ndarray        # uint8 [Np*Kp/2]
     base: np.ndarray      # uint8 [N]
-    row_ptr: np.ndarray   # int32 [N+1]
-    esc_col: np.ndarray   # int32 [esc_cap]
-    esc_val: np.ndarray   # uint16 [esc_cap]
+    esc_ptr: np.ndarray   # int32 [Np/16 * groups(K) + 1]
+    esc: np.ndarray       # uint32 [esc_cap]: key << 16 | raw BF16 bits
     n_esc: int
+
+    @property
+    def esc_key(self) -> np.ndarray:
+        return (self.esc >> 16).astype(np.uint16)
+
+    @property
+    def esc_val(self) -> np.ndarray:
+        return (self.esc & 0xFFFF).astype(np.uint16)
 
     def bits_per_weight(self) -> float:
         return bits_per_weight(self.N, self.K, self.n_esc)
 
     def copy(self) -> "W12Ref":
         return W12Ref(self.N, self.K, self.hi.copy(), self.lo.copy(), self.base.copy(),
-                      self.row_ptr.copy(), self.esc_col.copy(), self.esc_val.copy(), self.n_esc)
+                      self.esc_ptr.copy(), self.esc.copy(), self.n_esc)
+
+    def position(self, e: int):
+        """(n, k) of escape entry e."""
+        G = groups(self.K)
+        i = int(np.searchsorted(self.esc_ptr, e, side="right")) - 1
+        t, g = divmod(i, G)
+        key = int(self.esc[e] >> 16)
+        return 16 * t + ((key >> 6) & 15), 256 * g + 64 * (key >> 10) + (key & 63)
 
 
 def num_threads() -> int:
     return _load().w12ref_num_threads()
+
+
+def groups(K: int) -> int:
+    return _load().w12ref_groups(K)
+
+
+def ptr_len(N: int, K: int) -> int:
+    return _load().w12ref_ptr_len(N, K)
+
+
+def key(n: int, k: int) -> int:
+    return _load().w12ref_key(n, k)
 
 
 def rows_padded(N: int) -> int:
@@ -165,39 +195,38 @@ def bits_per_weight(N: int, K: int, n_esc: int) -> float:
 
 
 def encode(W: np.ndarray, esc_cap: int | None = None):
-    """Encode BF16 bits W [N,K] (uint16).  Returns (status, W12Ref)."""
+    """Encode BF16 bits W [N,K] (uint16).  Returns (status, W12Ref).  With
+    esc_cap=None the escape arrays are sized exactly (one counting pass)."""
     W = np.ascontiguousarray(W, dtype=np.uint16)
     N, K = W.shape
     lib = _load()
     if esc_cap is None:
-        esc_cap = N * K
+        st, t = encode(W, esc_cap=0)
+        if st == OK:
+            return st, t
+        esc_cap = t.n_esc
     hi = np.zeros(lib.w12ref_hi_bytes(N, K), np.uint8)
     lo = np.zeros(lib.w12ref_lo_bytes(N, K), np.uint8)
     base = np.zeros(N, np.uint8)
-    row_ptr = np.zeros(N + 1, np.int32)
-    esc_col = np.zeros(max(esc_cap, 1), np.int32)
-    esc_val = np.zeros(max(esc_cap, 1), np.uint16)
+    esc_ptr = np.zeros(lib.w12ref_ptr_len(N, K), np.int32)
+    esc = np.zeros(max(esc_cap, 1), np.uint32)
     n_esc = ctypes.c_int64()
-    st = lib.w12ref_encode(_ptr(W), N, K, K, _ptr(hi), _ptr(lo), _ptr(base), _ptr(row_ptr),
-                           _ptr(esc_col), _ptr(esc_val), esc_cap, ctypes.byref(n_esc))
-    t = W12Ref(N, K, hi, lo, base, row_ptr, esc_col[:esc_cap].copy(), esc_val[:esc_cap].copy(),
-               n_esc.value)
+    st = lib.w12ref_encode(_ptr(W), N, K, K, _ptr(hi), _ptr(lo), _ptr(base), _ptr(esc_ptr),
+                           _ptr(esc), esc_cap, ctypes.byref(n_esc))
+    t = W12Ref(N, K, hi, lo, base, esc_ptr, esc[:esc_cap].copy(), n_esc.value)
     if st == OK:
-        t.esc_col = t.esc_col[:t.n_esc].copy()
-        t.esc_val = t.esc_val[:t.n_esc].copy()
+        t.esc = t.esc[:t.n_esc].copy()
     return st, t
 
 
 def _tensor_args(t: W12Ref):
-    col = t.esc_col if t.esc_col.size else np.zeros(1, np.int32)
-    val = t.esc_val if t.esc_val.size else np.zeros(1, np.uint16)
-    return (_ptr(t.hi), _ptr(t.lo), _ptr(t.base), _ptr(t.row_ptr), _ptr(col), _ptr(val))
+    esc = t.esc if t.esc.size else np.zeros(1, np.uint32)
+    return (_ptr(t.hi), _ptr(t.lo), _ptr(t.base), _ptr(t.esc_ptr), _ptr(esc))
 
 
 def check_structure(t: W12Ref) -> int:
-    col = t.esc_col if t.esc_col.size else np.zeros(1, np.int32)
-    return _load().w12ref_check_structure(t.N, t.K, _ptr(t.row_ptr), _ptr(col), t.n_esc,
-                                          t.esc_col.size)
+    esc = t.esc if t.esc.size else np.zeros(1, np.uint32)
+    return _load().w12ref_check_structure(t.N, t.K, _ptr(t.esc_ptr), _ptr(esc), t.n_esc, t.esc.size)
 
 
 def decode(t: W12Ref):
@@ -212,7 +241,7 @@ def verify(W: np.ndarray, t: W12Ref):
     W = np.ascontiguousarray(W, dtype=np.uint16)
     nm = ctypes.c_int64()
     st = _load().w12ref_verify(_ptr(W), t.K, t.N, t.K, *_tensor_args(t), t.n_esc,
-                               t.esc_col.size, ctypes.byref(nm))
+                               t.esc.size, ctypes.byref(nm))
     return st, nm.value
 
 

@@ -30,8 +30,11 @@
  *   R3 base in [1,239] so that base+off <= 254 is always a finite normal;
  *   R4 Inf/NaN (exponent 255) are escaped too;
  *   R5 escaped and padding slots hold record 0;
- *   R6 escape list = row CSR (row_ptr i32[N+1], col i32, raw BF16 bits u16),
- *      columns strictly ascending inside a row;
+ *   R6 escape list = 32-bit entries key<<16 | raw BF16 bits, ordered
+ *      by row stripe (16 rows), then 256-column group, then tile, row and
+ *      column; esc_ptr[t*G+g] is the index of the first entry of stripe t,
+ *      group g (G = groups per stripe), esc_ptr[T*G] = the entry count.  The
+ *      key of weight (n,k) inside its group is (k%256/64)<<10 | (n%16)<<6 | k%64;
  *   R7 an output channel is a row of W[N,K] (Y = A * W^T);
  *   R8 planes are padded to Np = N rounded up to 16 and Kp = K rounded up to
  *      64 and stored tile by tile (16 rows x 64 columns); the in-tile order is
@@ -173,66 +176,82 @@ int w12ref_record(uint16_t w, int base)
     return (bf_sign(w) << 11) | ((bf_exp(w) - base) << 7) | bf_man(w);
 }
 
+/* Escape-list geometry (reading R6). */
+int64_t w12ref_groups(int64_t K) { return (w12ref_cols_padded(K) / 64 + 3) / 4; }
+int64_t w12ref_ptr_len(int64_t N, int64_t K) { return w12ref_rows_padded(N) / 16 * w12ref_groups(K) + 1; }
+
+int w12ref_key(int64_t n, int64_t k) { return (int)(((k % 256) / 64) << 10 | (n % 16) << 6 | (k % 64)); }
+
+/* Row and column of the entry `key` of stripe t, group g. */
+static void key_position(int64_t t, int64_t g, int key, int64_t *n, int64_t *k)
+{
+    *n = 16 * t + ((key >> 6) & 15);
+    *k = 256 * g + 64 * (key >> 10) + (key & 63);
+}
+
 /* ---- step a3: encode ----
  * W is [N,K] BF16 bits with row stride ldw.  Outputs: hi [Np*Kp], lo
- * [Np*Kp/2], base [N], row_ptr [N+1], esc_col/esc_val [esc_cap].
- * When the tensor needs more than esc_cap escapes, the planes, base and
- * row_ptr are still complete, only the first esc_cap escapes are written, and
- * the function returns REF_ERR_CAPACITY with *n_esc = the number needed. */
+ * [Np*Kp/2], base [N], esc_ptr [w12ref_ptr_len(N,K)], esc [esc_cap].  When the tensor needs more than esc_cap escapes, the planes,
+ * base and esc_ptr are still complete, only the first esc_cap escapes are
+ * written, and the function returns REF_ERR_CAPACITY with *n_esc = the
+ * number needed. */
 int w12ref_encode(const uint16_t *W, int64_t N, int64_t K, int64_t ldw,
-                  uint8_t *hi, uint8_t *lo, uint8_t *base, int32_t *row_ptr,
-                  int32_t *esc_col, uint16_t *esc_val, int64_t esc_cap, int64_t *n_esc)
+                  uint8_t *hi, uint8_t *lo, uint8_t *base, int32_t *esc_ptr,
+                  uint32_t *esc, int64_t esc_cap, int64_t *n_esc)
 {
     if (N < 0 || K < 0 || ldw < K || !n_esc) return REF_ERR_INVALID;
-    int64_t Kp = w12ref_cols_padded(K);
+    int64_t Kp = w12ref_cols_padded(K), T = w12ref_rows_padded(N) / 16, G = w12ref_groups(K);
     memset(hi, 0, (size_t)w12ref_hi_bytes(N, K)); /* reading R5: padding = record 0 */
     memset(lo, 0, (size_t)w12ref_lo_bytes(N, K));
 
-    /* window and escape count per row (rows are independent) */
-    int64_t *count = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
-    if (!count) return REF_ERR_INVALID;
+    /* a1: the window of every row */
 #pragma omp parallel for schedule(dynamic, 16)
-    for (int64_t n = 0; n < N; ++n) {
-        const uint16_t *row = W + n * ldw;
-        int b = w12ref_window_base(row, K);
-        base[n] = (uint8_t)b;
-        int64_t c = 0;
-        for (int64_t k = 0; k < K; ++k) c += w12ref_is_escape(row[k], b);
-        count[n] = c;
-    }
-    /* row CSR offsets (reading R6) */
+    for (int64_t n = 0; n < N; ++n) base[n] = (uint8_t)w12ref_window_base(W + n * ldw, K);
+
+    /* a2: escapes per (stripe, group), then their offsets */
     int64_t E = 0;
-    for (int64_t n = 0; n < N; ++n) {
-        row_ptr[n] = (int32_t)E;
-        E += count[n];
+    esc_ptr[0] = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t g = 0; g < G; ++g) {
+            for (int64_t n = 16 * t; n < 16 * t + 16 && n < N; ++n)
+                for (int64_t k = 256 * g; k < 256 * g + 256 && k < K; ++k)
+                    E += w12ref_is_escape(W[n * ldw + k], base[n]);
+            esc_ptr[t * G + g + 1] = (int32_t)E;
+        }
     }
-    row_ptr[N] = (int32_t)E;
-    free(count);
     *n_esc = E;
 
-#pragma omp parallel for schedule(dynamic, 16)
-    for (int64_t n = 0; n < N; ++n) {
-        const uint16_t *row = W + n * ldw;
-        int b = base[n];
-        int64_t idx = row_ptr[n];
-        for (int64_t k = 0; k < K; ++k) {
-            uint16_t w = row[k];
-            int r;
-            if (w12ref_is_escape(w, b)) {
-                if (idx < esc_cap) {
-                    esc_col[idx] = (int32_t)k;
-                    esc_val[idx] = w;
+    /* a3: records into the planes, escapes in (stripe, group, tile, row,
+     * column) order */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t g = 0; g < G; ++g) {
+            int64_t idx = esc_ptr[t * G + g];
+            for (int64_t c4 = 0; c4 < 4; ++c4) {
+                for (int64_t i = 0; i < 16; ++i) {
+                    int64_t n = 16 * t + i;
+                    if (n >= N) continue;
+                    for (int64_t j = 0; j < 64; ++j) {
+                        int64_t k = 256 * g + 64 * c4 + j;
+                        if (k >= K) break;
+                        uint16_t w = W[n * ldw + k];
+                        int b = base[n];
+                        int r;
+                        if (w12ref_is_escape(w, b)) {
+                            if (idx < esc_cap) esc[idx] = ((uint32_t)w12ref_key(n, k) << 16) | w;
+                            idx++;
+                            r = 0;
+                        } else {
+                            r = w12ref_record(w, b);
+                        }
+                        hi[w12ref_hi_offset(n, k, Kp)] = (uint8_t)(r >> 4);
+                        int64_t lb;
+                        int sh;
+                        w12ref_lo_position(n, k, Kp, &lb, &sh);
+                        lo[lb] = (uint8_t)(lo[lb] | ((r & 0xF) << sh));
+                    }
                 }
-                idx++;
-                r = 0;
-            } else {
-                r = w12ref_record(w, b);
             }
-            hi[w12ref_hi_offset(n, k, Kp)] = (uint8_t)(r >> 4);
-            int64_t lb;
-            int sh;
-            w12ref_lo_position(n, k, Kp, &lb, &sh);
-            lo[lb] = (uint8_t)(lo[lb] | ((r & 0xF) << sh));
         }
     }
     return E <= esc_cap ? REF_OK : REF_ERR_CAPACITY;
@@ -256,44 +275,71 @@ uint16_t w12ref_decode_record(int r, int base)
     return (uint16_t)((s << 15) | (((off + base) & 0xFF) << 7) | m);
 }
 
-/* Escape-list well-formedness (reading R6): row_ptr[0] = 0, non-decreasing,
- * row_ptr[N] = n_esc <= esc_cap, every column in [0,K), columns strictly
- * ascending inside each row.  Returns the number of violations. */
-int64_t w12ref_check_structure(int64_t N, int64_t K, const int32_t *row_ptr,
-                               const int32_t *esc_col, int64_t n_esc, int64_t esc_cap)
+/* Escape-list well-formedness (reading R6): esc_ptr[0] = 0, non-decreasing,
+ * esc_ptr[T*G] = n_esc <= esc_cap; inside each group the keys strictly
+ * ascend, are below 4096 and name a weight inside the tensor.  Returns the
+ * number of violations. */
+int64_t w12ref_check_structure(int64_t N, int64_t K, const int32_t *esc_ptr,
+                               const uint32_t *esc, int64_t n_esc, int64_t esc_cap)
 {
+    int64_t T = w12ref_rows_padded(N) / 16, G = w12ref_groups(K), P = T * G;
     int64_t bad = 0;
     if (n_esc < 0 || n_esc > esc_cap) bad++;
-    if (row_ptr[0] != 0) bad++;
-    if ((int64_t)row_ptr[N] != n_esc) bad++;
-    for (int64_t n = 0; n < N; ++n)
-        if (row_ptr[n + 1] < row_ptr[n]) bad++;
-    if (bad) return bad; /* the rows cannot be walked safely */
-    for (int64_t n = 0; n < N; ++n) {
-        for (int64_t i = row_ptr[n]; i < row_ptr[n + 1]; ++i) {
-            if (esc_col[i] < 0 || esc_col[i] >= K) bad++;
-            if (i + 1 < row_ptr[n + 1] && esc_col[i + 1] <= esc_col[i]) bad++;
+    if (esc_ptr[0] != 0) bad++;
+    if ((int64_t)esc_ptr[P] != n_esc) bad++;
+    for (int64_t i = 0; i < P; ++i)
+        if (esc_ptr[i + 1] < esc_ptr[i]) bad++;
+    if (bad) return bad; /* the groups cannot be walked safely */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t g = 0; g < G; ++g) {
+            for (int64_t e = esc_ptr[t * G + g]; e < esc_ptr[t * G + g + 1]; ++e) {
+                int64_t n, k;
+                int key = (int)(esc[e] >> 16);
+                key_position(t, g, key, &n, &k);
+                if (key >= 4096 || n >= N || k >= K) bad++;
+                if (e + 1 < esc_ptr[t * G + g + 1] && (esc[e + 1] >> 16) <= (esc[e] >> 16)) bad++;
+            }
         }
     }
     return bad;
 }
 
+/* Applies the escapes of stripe t that fall in row n to row[] (columns
+ * 0..K-1). */
+static void patch_row(int64_t n, int64_t K, const int32_t *esc_ptr, const uint32_t *esc,
+                      uint16_t *row)
+{
+    int64_t t = n / 16, G = w12ref_groups(K);
+    for (int64_t g = 0; g < G; ++g) {
+        for (int64_t e = esc_ptr[t * G + g]; e < esc_ptr[t * G + g + 1]; ++e) {
+            int64_t rn, rk;
+            key_position(t, g, (int)(esc[e] >> 16), &rn, &rk);
+            if (rn == n) row[rk] = (uint16_t)(esc[e] & 0xFFFF);
+        }
+    }
+}
+
+/* One decoded row (no structure check; the caller has done it). */
+static void decode_row(int64_t n, int64_t K, int64_t Kp, const uint8_t *hi, const uint8_t *lo,
+                       const uint8_t *base, const int32_t *esc_ptr, const uint32_t *esc,
+                       uint16_t *row)
+{
+    for (int64_t k = 0; k < K; ++k) row[k] = w12ref_decode_record(record_at(hi, lo, n, k, Kp), base[n]);
+    patch_row(n, K, esc_ptr, esc, row);
+}
+
 /* ---- step a4: decode ----  out is [N,K] with row stride ldo.  Every weight
- * comes from its record, then each escape of the row overwrites its column
- * with the stored BF16 bits. */
+ * comes from its record, then each escape overwrites its position with the
+ * stored BF16 bits. */
 int w12ref_decode(int64_t N, int64_t K, const uint8_t *hi, const uint8_t *lo,
-                  const uint8_t *base, const int32_t *row_ptr, const int32_t *esc_col,
-                  const uint16_t *esc_val, int64_t n_esc, uint16_t *out, int64_t ldo)
+                  const uint8_t *base, const int32_t *esc_ptr, const uint32_t *esc,
+                  int64_t n_esc, uint16_t *out, int64_t ldo)
 {
     if (N < 0 || K < 0 || ldo < K) return REF_ERR_INVALID;
-    if (w12ref_check_structure(N, K, row_ptr, esc_col, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
+    if (w12ref_check_structure(N, K, esc_ptr, esc, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
     int64_t Kp = w12ref_cols_padded(K);
 #pragma omp parallel for schedule(dynamic, 16)
-    for (int64_t n = 0; n < N; ++n) {
-        uint16_t *row = out + n * ldo;
-        for (int64_t k = 0; k < K; ++k) row[k] = w12ref_decode_record(record_at(hi, lo, n, k, Kp), base[n]);
-        for (int64_t i = row_ptr[n]; i < row_ptr[n + 1]; ++i) row[esc_col[i]] = esc_val[i];
-    }
+    for (int64_t n = 0; n < N; ++n) decode_row(n, K, Kp, hi, lo, base, esc_ptr, esc, out + n * ldo);
     return REF_OK;
 }
 
@@ -301,18 +347,17 @@ int w12ref_decode(int64_t N, int64_t K, const uint8_t *hi, const uint8_t *lo,
  * decoded bits differ from W.  A malformed escape list gives REF_ERR_CORRUPT
  * and *n_mismatch = -1; any mismatch gives REF_ERR_MISMATCH. */
 int w12ref_verify(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const uint8_t *hi,
-                  const uint8_t *lo, const uint8_t *base, const int32_t *row_ptr,
-                  const int32_t *esc_col, const uint16_t *esc_val, int64_t n_esc,
-                  int64_t esc_cap, int64_t *n_mismatch)
+                  const uint8_t *lo, const uint8_t *base, const int32_t *esc_ptr,
+                  const uint32_t *esc, int64_t n_esc, int64_t esc_cap, int64_t *n_mismatch)
 {
     if (N < 0 || K < 0 || ldw < K || !n_mismatch) return REF_ERR_INVALID;
-    if (w12ref_check_structure(N, K, row_ptr, esc_col, n_esc, esc_cap) != 0) {
+    if (w12ref_check_structure(N, K, esc_ptr, esc, n_esc, esc_cap) != 0) {
         *n_mismatch = -1;
         return REF_ERR_CORRUPT;
     }
     uint16_t *dec = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(N * K > 0 ? N * K : 1));
     if (!dec) return REF_ERR_INVALID;
-    w12ref_decode(N, K, hi, lo, base, row_ptr, esc_col, esc_val, n_esc, dec, K);
+    w12ref_decode(N, K, hi, lo, base, esc_ptr, esc, n_esc, dec, K);
     int64_t bad = 0;
 #pragma omp parallel for reduction(+ : bad)
     for (int64_t n = 0; n < N; ++n)
@@ -320,15 +365,6 @@ int w12ref_verify(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const ui
     free(dec);
     *n_mismatch = bad;
     return bad ? REF_ERR_MISMATCH : REF_OK;
-}
-
-/* One decoded row (no structure check; the caller has done it). */
-static void decode_row(int64_t n, int64_t K, int64_t Kp, const uint8_t *hi, const uint8_t *lo,
-                       const uint8_t *base, const int32_t *row_ptr, const int32_t *esc_col,
-                       const uint16_t *esc_val, uint16_t *row)
-{
-    for (int64_t k = 0; k < K; ++k) row[k] = w12ref_decode_record(record_at(hi, lo, n, k, Kp), base[n]);
-    for (int64_t i = row_ptr[n]; i < row_ptr[n + 1]; ++i) row[esc_col[i]] = esc_val[i];
 }
 
 /* ---- steps a6-a9: the GEMM ----
@@ -339,11 +375,10 @@ static void decode_row(int64_t n, int64_t K, int64_t Kp, const uint8_t *hi, cons
  * [M,N] row-major, used to judge tolerances. */
 int w12ref_gemm(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int64_t K,
                 const uint8_t *hi, const uint8_t *lo, const uint8_t *base,
-                const int32_t *row_ptr, const int32_t *esc_col, const uint16_t *esc_val,
-                int64_t n_esc, uint16_t *Y, int64_t ldy, double *Y64, double *absdot)
+                const int32_t *esc_ptr, const uint32_t *esc, int64_t n_esc, uint16_t *Y, int64_t ldy, double *Y64, double *absdot)
 {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldy < N) return REF_ERR_INVALID;
-    if (w12ref_check_structure(N, K, row_ptr, esc_col, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
+    if (w12ref_check_structure(N, K, esc_ptr, esc, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
     int64_t Kp = w12ref_cols_padded(K);
     double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
     if (!a) return REF_ERR_INVALID;
@@ -355,7 +390,7 @@ int w12ref_gemm(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int64_t K,
         double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
 #pragma omp for schedule(dynamic, 8)
         for (int64_t n = 0; n < N; ++n) {
-            decode_row(n, K, Kp, hi, lo, base, row_ptr, esc_col, esc_val, row);
+            decode_row(n, K, Kp, hi, lo, base, esc_ptr, esc, row);
             for (int64_t k = 0; k < K; ++k) w[k] = w12ref_bf16_to_double(row[k]);
             for (int64_t m = 0; m < M; ++m) {
                 double acc = 0.0, mag = 0.0;
@@ -380,12 +415,11 @@ int w12ref_gemm(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int64_t K,
  * have `count` entries. */
 int w12ref_gemm_sample(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int64_t K,
                        const uint8_t *hi, const uint8_t *lo, const uint8_t *base,
-                       const int32_t *row_ptr, const int32_t *esc_col, const uint16_t *esc_val,
-                       int64_t n_esc, const int64_t *ms, const int64_t *ns, int64_t count,
+                       const int32_t *esc_ptr, const uint32_t *esc, int64_t n_esc, const int64_t *ms, const int64_t *ns, int64_t count,
                        uint16_t *y, double *y64, double *absdot)
 {
     if (M < 0 || N < 0 || K < 0 || lda < K) return REF_ERR_INVALID;
-    if (w12ref_check_structure(N, K, row_ptr, esc_col, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
+    if (w12ref_check_structure(N, K, esc_ptr, esc, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
     int64_t Kp = w12ref_cols_padded(K);
     for (int64_t i = 0; i < count; ++i)
         if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N) return REF_ERR_INVALID;
@@ -394,7 +428,7 @@ int w12ref_gemm_sample(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int
         uint16_t *row = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(K > 0 ? K : 1));
 #pragma omp for schedule(dynamic, 1)
         for (int64_t i = 0; i < count; ++i) {
-            decode_row(ns[i], K, Kp, hi, lo, base, row_ptr, esc_col, esc_val, row);
+            decode_row(ns[i], K, Kp, hi, lo, base, esc_ptr, esc, row);
             double acc = 0.0, mag = 0.0;
             for (int64_t k = 0; k < K; ++k) {
                 double av = w12ref_bf16_to_double(A[ms[i] * lda + k]);
@@ -412,11 +446,12 @@ int w12ref_gemm_sample(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int
 }
 
 /* Storage cost in bits per weight, counting everything the tensor stores:
- * both planes (with padding), the bases, the row offsets and the escapes. */
+ * both planes (with padding), the bases, the group offsets and the escapes
+ * (one 32-bit entry each). */
 double w12ref_bits_per_weight(int64_t N, int64_t K, int64_t n_esc)
 {
     double bytes = (double)w12ref_hi_bytes(N, K) + (double)w12ref_lo_bytes(N, K) + (double)N +
-                   4.0 * (double)(N + 1) + 6.0 * (double)n_esc;
+                   4.0 * (double)w12ref_ptr_len(N, K) + 4.0 * (double)n_esc;
     return 8.0 * bytes / ((double)N * (double)K);
 }
 

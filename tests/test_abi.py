@@ -41,22 +41,28 @@ def test_size_queries(w12lib):
     assert lib.w12_lo_bytes(5121, 17400) == 5136 * 17408 // 2
     assert lib.w12_rows_padded(-1) == -1
     assert lib.w12_verify_workspace_bytes() == 16
+    assert lib.w12_groups(5120) == 20 and lib.w12_groups(17400) == 68 and lib.w12_groups(65) == 1
+    assert lib.w12_esc_ptr_len(5121, 17400) == 321 * 68 + 1
     assert (lib.w12_version() >> 16) == 1
 
 
 def test_oracle_and_library_agree_on_sizes(w12lib, oracle):
-    for N, K in ((1, 1), (16, 64), (17, 65), (5121, 17400), (34816, 5120)):
+    lib = w12lib.load()
+    for N, K in ((1, 1), (16, 64), (17, 65), (5121, 17400), (34816, 5120), (3, 300)):
         assert w12lib.rows_padded(N) == oracle.rows_padded(N)
         assert w12lib.cols_padded(K) == oracle.cols_padded(K)
+        assert lib.w12_groups(K) == oracle.groups(K)
+        assert lib.w12_esc_ptr_len(N, K) == oracle.ptr_len(N, K)
 
 
 def test_gemm_workspace_query(w12lib):
     o = w12lib.make_opts()
     # one stripe count of counters + S partial slabs of [Np, 8] floats
     nb = w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, o)
-    S = 8  # about 16 warps on each of 152 SMs over 320 stripes
-    assert nb == 256 + 4 * 65536 + S * 5120 * 8 * 4
-    assert w12lib.w12_gemm_workspace_bytes(16, 5120, 5120, o) == 256 + 4 * 65536 + S * 5120 * 16 * 4
+    slab = 5120 * 8 * 4  # one [Np, 8] FP32 partial slab
+    S, rem = divmod(nb - 256 - 4 * 65536, slab)
+    assert rem == 0 and 2 <= S <= 20  # a split of the 20 column groups
+    assert w12lib.w12_gemm_workspace_bytes(16, 5120, 5120, o) == 256 + 4 * 65536 + S * 2 * slab
     assert w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, w12lib.make_opts(split_k=1)) == 256
     assert w12lib.w12_gemm_workspace_bytes(17, 64, 64, w12lib.make_opts(path=w12lib.W12_PATH_MMA)) == 0
     bad = w12lib.GemmOpts(0, 0, 0, 1)  # reserved must be 0
@@ -72,16 +78,16 @@ def test_invalid_arguments_rejected_on_host(w12lib):
     """These calls fail validation before any CUDA call is made."""
     lib = w12lib.load()
     T = w12lib._Tensor
-    t = T(4, 64, None, None, None, None, None, None, 0, 0)
+    t = T(4, 64, None, None, None, None, None, 0, 0)
     assert lib.w12_decode(ctypes.byref(t), None, 64, None) == w12lib.W12_ERR_INVALID
     assert lib.w12_encode(None, 64, None, None) == w12lib.W12_ERR_INVALID
-    neg = T(-1, 64, None, None, None, None, None, None, 0, 0)
+    neg = T(-1, 64, None, None, None, None, None, 0, 0)
     assert lib.w12_decode(ctypes.byref(neg), None, 64, None) == w12lib.W12_ERR_INVALID
     # misaligned planes
-    good = T(4, 64, 16, 17, 32, 48, 64, 80, 1, 0)
+    good = T(4, 64, 16, 17, 32, 48, 64, 1, 0)
     assert lib.w12_decode(ctypes.byref(good), ctypes.c_void_p(4096), 64, None) == w12lib.W12_ERR_ALIGN
     # M > 16 on the mma path
-    t2 = T(16, 64, 256, 512, 768, 1024, 1280, 1536, 1, 0)
+    t2 = T(16, 64, 256, 512, 768, 1024, 1280, 1, 0)
     o = w12lib.make_opts(path=w12lib.W12_PATH_MMA)
     st = lib.w12_gemm(ctypes.c_void_p(4096), 64, ctypes.byref(t2), ctypes.c_void_p(8192), 16, 17,
                       ctypes.c_void_p(16384), 1 << 20, ctypes.byref(o), None)

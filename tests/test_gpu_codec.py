@@ -21,19 +21,16 @@ def host_view(t):
     """A GPU W12Tensor's arrays as numpy (for comparison only)."""
     return dict(
         hi=t.hi.cpu().numpy(), lo=t.lo.cpu().numpy(), base=t.base.cpu().numpy(),
-        row_ptr=t.row_ptr.cpu().numpy(), esc_col=t.esc_col[:t.n_esc].cpu().numpy(),
-        esc_val=t.esc_val[:t.n_esc].cpu().numpy().view(np.uint16), n_esc=t.n_esc)
+        esc_ptr=t.esc_ptr.cpu().numpy(), esc=t.esc[:t.n_esc].cpu().numpy().view(np.uint32), n_esc=t.n_esc)
 
 
 def upload(w, ref):
     """An oracle-built (host) W12 tensor copied to the device."""
     dev = "cuda"
-    col = torch.from_numpy(ref.esc_col.astype(np.int32)).to(dev) if ref.esc_col.size else \
+    esc = torch.from_numpy(ref.esc.view(np.int32)).to(dev) if ref.esc.size else \
         torch.zeros(0, dtype=torch.int32, device=dev)
-    val = torch.from_numpy(ref.esc_val.view(np.int16)).to(dev) if ref.esc_val.size else \
-        torch.zeros(0, dtype=torch.int16, device=dev)
     return w.W12Tensor(ref.N, ref.K, torch.from_numpy(ref.hi).to(dev), torch.from_numpy(ref.lo).to(dev),
-                       torch.from_numpy(ref.base).to(dev), torch.from_numpy(ref.row_ptr).to(dev), col, val,
+                       torch.from_numpy(ref.base).to(dev), torch.from_numpy(ref.esc_ptr).to(dev), esc,
                        ref.n_esc)
 
 
@@ -70,7 +67,7 @@ def test_encode_decode_verify_bit_exact(name, w12lib, oracle):
     torch.cuda.synchronize()
     g = host_view(t)
     assert g["n_esc"] == ref.n_esc
-    for key in ("hi", "lo", "base", "row_ptr", "esc_col", "esc_val"):
+    for key in ("hi", "lo", "base", "esc_ptr", "esc"):
         assert np.array_equal(g[key], getattr(ref, key)), key
     D = w12lib.w12_decode(t)
     assert np.array_equal(synth.tensor_to_bits(D), W)
@@ -94,7 +91,7 @@ def test_encode_strided_input(w12lib, oracle):
     t = w12lib.w12_encode(Wd)
     st, ref = oracle.encode(W)
     assert np.array_equal(t.hi.cpu().numpy(), ref.hi)
-    assert np.array_equal(t.esc_col.cpu().numpy(), ref.esc_col)
+    assert np.array_equal(t.esc.cpu().numpy().view(np.uint32), ref.esc)
 
 
 def test_encode_capacity_path(w12lib, oracle):
@@ -111,17 +108,17 @@ def test_encode_capacity_path(w12lib, oracle):
     assert rc == w12lib.W12_ERR_CAPACITY and s.n_esc == full.n_esc
     assert np.array_equal(t.hi.cpu().numpy(), full.hi)
     assert np.array_equal(t.lo.cpu().numpy(), full.lo)
-    assert np.array_equal(t.row_ptr.cpu().numpy(), full.row_ptr)
-    assert np.array_equal(t.esc_col.cpu().numpy(), full.esc_col[:cap])
-    assert np.array_equal(t.esc_val.cpu().numpy().view(np.uint16), full.esc_val[:cap])
+    assert np.array_equal(t.esc_ptr.cpu().numpy(), full.esc_ptr)
+    assert np.array_equal(t.esc.cpu().numpy().view(np.uint32), full.esc[:cap])
 
 
 def test_empty_shapes(w12lib):
     t = w12lib.w12_encode(torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda"))
-    assert t.n_esc == 0 and int(t.row_ptr[0]) == 0
+    assert t.n_esc == 0 and t.esc_ptr.cpu().tolist() == [0]
     Wk0 = torch.zeros(5, 0, dtype=torch.bfloat16, device="cuda")
     t = w12lib.w12_encode(Wk0)
-    assert t.n_esc == 0 and t.row_ptr.cpu().tolist() == [0] * 6
+    assert t.n_esc == 0 and t.esc_ptr.cpu().tolist() == [0]
+    assert (t.base.cpu().numpy() == 239).all()
     assert w12lib.w12_decode(t).shape == (5, 0)
     assert w12lib.w12_verify_roundtrip(Wk0, t) == (w12lib.W12_OK, 0)
 
@@ -148,7 +145,7 @@ def test_verify_counts_host_corruption(w12lib, oracle):
             c.base[idx] ^= np.uint8(1 << int(rng.integers(0, 7)))
         else:
             idx = rng.choice(c.n_esc, size=min(5, c.n_esc), replace=False)
-            c.esc_val[idx] ^= np.uint16(0x0040)
+            c.esc[idx] ^= np.uint32(0x0040)
         plans.append(c)
     for c in plans:
         want = oracle.verify(W, c)
@@ -160,18 +157,37 @@ def test_verify_flags_malformed_escape_list(w12lib, oracle):
     W = synth.dense_weights(32, 512, seed=13)
     Wd = synth.bits_to_tensor(W, "cuda")
     st, ref = oracle.encode(W)
-    r = next(n for n in range(32) if ref.row_ptr[n + 1] - ref.row_ptr[n] >= 2)
+    g = next(i for i in range(ref.esc_ptr.size - 1) if ref.esc_ptr[i + 1] - ref.esc_ptr[i] >= 2)
     c = ref.copy()
-    i = c.row_ptr[r]
-    c.esc_col[i], c.esc_col[i + 1] = c.esc_col[i + 1], c.esc_col[i]
+    i = c.esc_ptr[g]
+    c.esc[i], c.esc[i + 1] = c.esc[i + 1], c.esc[i]  # keys out of order
     assert oracle.verify(W, c) == (oracle.ERR_CORRUPT, -1)
     assert w12lib.w12_verify_roundtrip(Wd, upload(w12lib, c)) == (w12lib.W12_ERR_CORRUPT, -1)
     c = ref.copy()
-    c.esc_col[0] = 512  # column out of range
+    c.esc[0] |= np.uint32(0xF000 << 16)  # key >= 4096
+    assert oracle.verify(W, c) == (oracle.ERR_CORRUPT, -1)
     assert w12lib.w12_verify_roundtrip(Wd, upload(w12lib, c)) == (w12lib.W12_ERR_CORRUPT, -1)
     c = ref.copy()
-    c.row_ptr[5] = c.row_ptr[6] + 1  # offsets not monotone
+    c.esc_ptr[3] = c.esc_ptr[4] + 1  # offsets not monotone
+    assert oracle.verify(W, c) == (oracle.ERR_CORRUPT, -1)
     assert w12lib.w12_verify_roundtrip(Wd, upload(w12lib, c)) == (w12lib.W12_ERR_CORRUPT, -1)
+
+
+def test_verify_counts_moved_escape(w12lib, oracle):
+    """An escape key rewritten to name another weight: the oracle's count of
+    mismatches, on the GPU too."""
+    W = synth.dense_weights(48, 700, seed=16)
+    Wd = synth.bits_to_tensor(W, "cuda")
+    st, ref = oracle.encode(W)
+    rng = np.random.default_rng(17)
+    for _ in range(6):
+        c = ref.copy()
+        e = int(rng.integers(0, c.n_esc))
+        key = int(c.esc[e] >> 16)
+        new_key = (key & ~0x3F) | int(rng.integers(0, 64))  # another column of the same tile row
+        c.esc[e] = np.uint32((new_key << 16) | (int(c.esc[e]) & 0xFFFF))
+        want = oracle.verify(W, c)
+        assert w12lib.w12_verify_roundtrip(Wd, upload(w12lib, c)) == want
 
 
 def test_row_slice_is_a_w12_tensor(w12lib, oracle):
@@ -192,7 +208,7 @@ def test_full_size_gate_up_encode_matches_oracle_on_sampled_stripes(w12lib, orac
     Wd = synth.dense_weights_device(N, K, seed=1002)
     t = w12lib.w12_encode(Wd)
     assert w12lib.w12_verify_roundtrip(Wd, t) == (w12lib.W12_OK, 0)
-    KT = K // 64
+    KT, G = K // 64, K // 256
     rng = np.random.default_rng(15)
     for st_ in list(rng.choice(N // 16, size=6, replace=False)) + [N // 16 - 1]:
         rows = slice(16 * st_, 16 * st_ + 16)
@@ -201,7 +217,6 @@ def test_full_size_gate_up_encode_matches_oracle_on_sampled_stripes(w12lib, orac
         assert np.array_equal(t.hi[st_ * KT * 1024:(st_ + 1) * KT * 1024].cpu().numpy(), ref.hi)
         assert np.array_equal(t.lo[st_ * KT * 512:(st_ + 1) * KT * 512].cpu().numpy(), ref.lo)
         assert np.array_equal(t.base[rows].cpu().numpy(), ref.base)
-        rp = t.row_ptr[16 * st_:16 * st_ + 17].cpu().numpy()
-        assert np.array_equal(rp - rp[0], ref.row_ptr)
-        assert np.array_equal(t.esc_col[rp[0]:rp[-1]].cpu().numpy(), ref.esc_col)
-        assert np.array_equal(t.esc_val[rp[0]:rp[-1]].cpu().numpy().view(np.uint16), ref.esc_val)
+        ptr = t.esc_ptr[st_ * G:st_ * G + G + 1].cpu().numpy()
+        assert np.array_equal(ptr - ptr[0], ref.esc_ptr)
+        assert np.array_equal(t.esc[ptr[0]:ptr[-1]].cpu().numpy().view(np.uint32), ref.esc)

@@ -167,20 +167,29 @@ def test_layout_is_a_bijection(oracle):
     assert (hi_seen == 1).all() and (lo_seen == 1).all()
 
 
+def escaped_mask(W, base):
+    e = (W.astype(np.int64) >> 7) & 0xFF
+    b = base.astype(np.int64)[:, None]
+    return (e == 0) | (e == 255) | (e < b) | (e > b + 15)
+
+
 def check_invariants(oracle, W, t):
     N, K = W.shape
     assert oracle.check_structure(t) == 0
-    assert t.row_ptr[0] == 0 and t.row_ptr[-1] == t.n_esc
-    e = (W.astype(np.int64) >> 7) & 0xFF
+    assert t.esc_ptr[0] == 0 and t.esc_ptr[-1] == t.n_esc
+    assert t.esc_ptr.size == (oracle.rows_padded(N) // 16) * oracle.groups(K) + 1
+    assert ((t.base >= 1) & (t.base <= 239)).all()
+    esc = escaped_mask(W, t.base)
+    # the list holds exactly the escaped positions, each once, with its bits
+    pos = [t.position(e) for e in range(t.n_esc)]
+    assert sorted(pos) == sorted(map(tuple, np.argwhere(esc).tolist()))
+    for e, (n, k) in enumerate(pos):
+        assert t.esc_val[e] == W[n, k]
+        assert t.esc_key[e] == oracle.key(n, k)
+    # order: stripe, group, then tile, row, column inside the group
+    order = [(n // 16, k // 256, (k % 256) // 64, n % 16, k % 64) for n, k in pos]
+    assert order == sorted(order)
     Kp = oracle.cols_padded(K)
-    for n in range(N):
-        base = int(t.base[n])
-        assert 1 <= base <= 239
-        cols = t.esc_col[t.row_ptr[n]:t.row_ptr[n + 1]]
-        assert (np.diff(cols) > 0).all()
-        esc = (e[n] == 0) | (e[n] == 255) | (e[n] < base) | (e[n] > base + 15)
-        assert np.array_equal(np.nonzero(esc)[0], cols)  # no in-window weight escaped
-        assert np.array_equal(t.esc_val[t.row_ptr[n]:t.row_ptr[n + 1]], W[n, cols])
     # the nested 8-bit view: the hi byte of an in-window weight is its top 8
     # record bits s|off|m[6:4]
     rng = np.random.default_rng(1)
@@ -242,10 +251,9 @@ def test_capacity_path_keeps_planes(oracle):
     cap = full.n_esc // 2
     st, part = oracle.encode(W, esc_cap=cap)
     assert st == oracle.ERR_CAPACITY and part.n_esc == full.n_esc
-    for name in ("hi", "lo", "base", "row_ptr"):
+    for name in ("hi", "lo", "base", "esc_ptr"):
         assert np.array_equal(getattr(part, name), getattr(full, name))
-    assert np.array_equal(part.esc_col[:cap], full.esc_col[:cap])
-    assert np.array_equal(part.esc_val[:cap], full.esc_val[:cap])
+    assert np.array_equal(part.esc[:cap], full.esc[:cap])
 
 
 def test_bits_per_weight_gaussian_matches_pages(oracle):
@@ -258,9 +266,10 @@ def test_bits_per_weight_gaussian_matches_pages(oracle):
     assert st == oracle.OK
     bpw = t.bits_per_weight()
     assert fig["bits_per_weight_low"] - 0.005 <= bpw <= fig["bits_per_weight_high"], bpw
-    # the closed form of the accounting: 12 bits of planes + 40 bits of row
-    # metadata per row + 48 bits per escape
-    assert bpw == pytest.approx(12.0 + (8 + 32) / 5120 + 32 / (1024 * 5120) + 48 * t.n_esc / (1024 * 5120))
+    # the closed form of the accounting: 12 bits of planes, 8 bits of base per
+    # row, a 32-bit offset per 16 x 256 group (+1), 32 bits per escape
+    groups = 1024 // 16 * 5120 // 256
+    assert bpw == pytest.approx(12.0 + 8 / 5120 + 32 * (groups + 1) / (1024 * 5120) + 32 * t.n_esc / (1024 * 5120))
     # escapes of a Gaussian row fall below the 16-binade window: ~6e-5
     assert 1e-5 < t.n_esc / W.size < 2e-4
 
@@ -281,9 +290,7 @@ def test_verify_counts_planted_corruption(oracle):
     W = synth.dense_weights(48, 320, seed=13)
     st, t = oracle.encode(W)
     Kp = oracle.cols_padded(320)
-    esc = np.zeros(W.shape, bool)
-    for n in range(48):
-        esc[n, t.esc_col[t.row_ptr[n]:t.row_ptr[n + 1]]] = True
+    esc = escaped_mask(W, t.base)
     rng = np.random.default_rng(0)
     # (1) a hi bit of an in-window weight: exactly one mismatch
     n, k = next((int(a), int(b)) for a, b in zip(rng.integers(0, 48, 999), rng.integers(0, 320, 999))
@@ -307,11 +314,33 @@ def test_verify_counts_planted_corruption(oracle):
     assert oracle.verify(W, c) == (oracle.ERR_MISMATCH, 320 - int(esc[5].sum()))
     # (5) an escape value: one mismatch
     c = t.copy()
-    c.esc_val[3] ^= 0x0100
+    c.esc[3] ^= 0x0100
     assert oracle.verify(W, c) == (oracle.ERR_MISMATCH, 1)
-    # (6) escape columns out of order: malformed
+    # (6) an escape key moved to another in-window weight of the same group:
+    # two mismatches (the old slot loses its value, the new one gets it)
     c = t.copy()
-    r = next(n for n in range(48) if t.row_ptr[n + 1] - t.row_ptr[n] >= 2)
-    i = t.row_ptr[r]
-    c.esc_col[i], c.esc_col[i + 1] = c.esc_col[i + 1], c.esc_col[i]
+    e = int(np.nonzero(np.diff(t.esc_ptr) >= 1)[0][0])
+    first = int(t.esc_ptr[e])
+    last = int(t.esc_ptr[e + 1]) - 1
+    n0, k0 = t.position(last)
+    k1 = next(kk for kk in range(k0 + 1, min(320, (k0 // 256 + 1) * 256)) if not esc[n0, kk]) \
+        if any(not esc[n0, kk] for kk in range(k0 + 1, min(320, (k0 // 256 + 1) * 256))) else None
+    if k1 is not None:
+        c.esc[last] = (oracle.key(n0, k1) << 16) | (int(c.esc[last]) & 0xFFFF)
+        assert oracle.verify(W, c) == (oracle.ERR_MISMATCH, 2)
+    # (7) keys out of order inside a group: malformed
+    c = t.copy()
+    g = next(i for i in range(t.esc_ptr.size - 1) if t.esc_ptr[i + 1] - t.esc_ptr[i] >= 2)
+    i = t.esc_ptr[g]
+    c.esc[i], c.esc[i + 1] = c.esc[i + 1], c.esc[i]
     assert oracle.verify(W, c) == (oracle.ERR_CORRUPT, -1)
+    # (8) a key naming a column past K: malformed
+    c = t.copy()
+    last_group = t.esc_ptr.size - 2  # group 1 of the last stripe covers columns 256..319
+    c2 = t.copy()
+    c2.esc_ptr[:] = t.esc_ptr
+    if t.esc_ptr[last_group + 1] > t.esc_ptr[last_group]:
+        j = int(t.esc_ptr[last_group + 1]) - 1
+        key = (1 << 10) | (int(t.esc[j] >> 16) & 0x3C0) | 0x3F  # column 256+64+63 >= 320
+        c2.esc[j] = (key << 16) | (int(t.esc[j]) & 0xFFFF)
+        assert oracle.verify(W, c2) == (oracle.ERR_CORRUPT, -1)
