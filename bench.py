@@ -406,6 +406,37 @@ def run_reference(args):
     }
 
 
+def run_case(args):
+    """One layer GEMM launched `iters` times (for profiler captures): prints
+    the median kernel time and weight-GB/s, no JSON contract."""
+    import torch
+
+    import lossless_bit_weight_02_gb300 as w12
+    from lossless_bit_weight_02_gb300 import synth
+
+    shapes = {name: (i, N, K) for i, (name, N, K) in enumerate(synth.LAYER_SHAPES)}
+    i, N, K = shapes[args.case]
+    Wd = synth.dense_weights_device(N, K, seed=1000 + i)
+    t = w12.w12_encode(Wd)
+    del Wd
+    A = synth.activations_device(args.m, K, seed=2000 + 10 * args.m + i)
+    Y = torch.empty(args.m, N, dtype=torch.bfloat16, device="cuda")
+    ws = w12.Workspace("cuda", w12.w12_gemm_workspace_bytes(args.m, N, K))
+    call = w12.GemmCall(A, t, Y, ws)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    times = []
+    for _ in range(args.iters):
+        flush.zero_()  # evict the weights from L2 between launches
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    med = statistics.median(times)
+    print(f"case {args.case} M={args.m}: {med * 1e3:.2f} us, {t.nbytes() / (med * 1e-3) / 1e9:.1f} weight-GB/s")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,7 +446,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down)")
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--iters", type=int, default=5)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

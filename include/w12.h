@@ -24,7 +24,7 @@
  *     that share a workspace must not run concurrently.
  *
  * Tensor layout (the "packed-record layout"; the paper does not fix one):
- *   Np = N rounded up to 16, Kp = K rounded up to 64.  The 12-bit record of
+ *   Np = N rounded up to 16, Kp = K rounded up to 256.  The 12-bit record of
  *   weight (n,k) is s<<11 | off<<7 | m (off = exponent - base[n]); escaped
  *   and padding slots hold record 0.  The records live in two planes, stored
  *   as tiles of 16 rows x 64 columns, tile (t,c) = (n/16, k/64) at index
@@ -107,7 +107,7 @@ int64_t w12_rows_padded(int64_t N);          /* Np */
 int64_t w12_cols_padded(int64_t K);          /* Kp */
 int64_t w12_hi_bytes(int64_t N, int64_t K);  /* Np*Kp */
 int64_t w12_lo_bytes(int64_t N, int64_t K);  /* Np*Kp/2 */
-int64_t w12_groups(int64_t K);               /* 256-column groups per stripe: ceil(Kp/256) */
+int64_t w12_groups(int64_t K);               /* 256-column groups per stripe: Kp/256 */
 int64_t w12_esc_ptr_len(int64_t N, int64_t K);  /* Np/16 * w12_groups(K) + 1 */
 
 /* ---- w12_encode ----  BF16 [N,K] -> W12 (paper section 4.1: window per

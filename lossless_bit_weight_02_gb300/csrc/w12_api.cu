@@ -219,6 +219,9 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     g.error = reinterpret_cast<int32_t *>(ws);
     g.counters = reinterpret_cast<int32_t *>(ws + pl.counters_off);
     g.partials = reinterpret_cast<float *>(ws + pl.partials_off);
+    g.c28 = 1u << 28;
+    g.one = 1u;
+    g.c16 = 16u;
     return cuda_status(launch_gemm_mma(view_of(w), g, reinterpret_cast<cudaStream_t>(stream)));
 }
 

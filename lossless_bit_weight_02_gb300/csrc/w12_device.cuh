@@ -19,7 +19,7 @@ constexpr int kLoTileBytes = kTileRows * kTileCols / 2;  // 512
 constexpr uint32_t kFull = 0xffffffffu;
 
 __host__ __device__ inline int64_t rows_padded(int64_t N) { return (N + 15) / 16 * 16; }
-__host__ __device__ inline int64_t cols_padded(int64_t K) { return (K + 63) / 64 * 64; }
+__host__ __device__ inline int64_t cols_padded(int64_t K) { return (K + 255) / 256 * 256; }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;

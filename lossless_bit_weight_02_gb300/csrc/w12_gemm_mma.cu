@@ -27,8 +27,7 @@
 namespace w12 {
 namespace {
 
-constexpr int kWarps = 4;     // warps per block
-constexpr int kPrefetch = 4;  // tiles in flight per warp
+constexpr int kWarps = 4;  // warps per block; each warp keeps one 4-tile group in flight
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 r;
@@ -47,15 +46,19 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 16 activations A[m, k .. k+15] as 8 BF16 pairs, zero past K.
-__device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int64_t k, int64_t K,
+// 16 activations A[m, k .. k+15] as 8 BF16 pairs.  Lanes whose token does
+// not exist (pred false) load nothing and keep their registers (zero).
+__device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int64_t k, int64_t K, bool valid,
                                            uint32_t w[8]) {
-    if (k + 16 <= K) {
-        const uint4 x0 = __ldg(reinterpret_cast<const uint4 *>(row + k));
-        const uint4 x1 = __ldg(reinterpret_cast<const uint4 *>(row + k + 8));
-        w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
-        w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
-    } else {
+    const bool full = k + 16 <= K;
+    const uint16_t *p = row + k;
+    asm volatile(
+        "{\n.reg .pred pp;\nsetp.ne.u32 pp, %8, 0;\n"
+        "@pp ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%9];\n"
+        "@pp ld.global.nc.v4.u32 {%4,%5,%6,%7}, [%10];\n}"
+        : "+r"(w[0]), "+r"(w[1]), "+r"(w[2]), "+r"(w[3]), "+r"(w[4]), "+r"(w[5]), "+r"(w[6]), "+r"(w[7])
+        : "r"((uint32_t)(valid && full)), "l"(p), "l"(p + 8));
+    if (valid && !full) {  // the ragged end of K (last tile only)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint32_t lo = (k + 2 * j < K) ? row[k + 2 * j] : 0u;
@@ -65,14 +68,38 @@ __device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int
     }
 }
 
+// Record-pair decode (as decode_pair in w12_device.cuh) with the right shift
+// done as a high multiply and the base added with a multiply-add, so that two
+// of the five operations run on the FMA pipe instead of the ALU.  c28 = 2^28
+// and one = 1 arrive as kernel arguments so that they stay multiplications.
+__device__ __forceinline__ uint32_t decode_pair_fma(uint32_t Z, uint32_t base2, uint32_t c28, uint32_t one) {
+    const uint32_t t = __umulhi(Z, c28) & 0x07FF07FFu;  // (Z >> 4) & mask
+    uint32_t u;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(u) : "r"(t), "r"(one), "r"(base2));
+    return (Z & 0x80008000u) | (u & 0x7FFF7FFFu);
+}
+
+__device__ __forceinline__ void decode16_fma(uint4 h, uint32_t l0, uint32_t l1, uint32_t base2, uint32_t c28,
+                                             uint32_t one, uint32_t c16, uint32_t out[8]) {
+    const uint32_t l0s = l0 * c16, l1s = l1 * c16;  // << 4, on the FMA pipe
+    out[0] = decode_pair_fma(prmt(h.x, l0, 0x1504), base2, c28, one);
+    out[1] = decode_pair_fma(prmt(h.x, l0, 0x3726), base2, c28, one);
+    out[2] = decode_pair_fma(prmt(h.y, l0s, 0x1504), base2, c28, one);
+    out[3] = decode_pair_fma(prmt(h.y, l0s, 0x3726), base2, c28, one);
+    out[4] = decode_pair_fma(prmt(h.z, l1, 0x1504), base2, c28, one);
+    out[5] = decode_pair_fma(prmt(h.z, l1, 0x3726), base2, c28, one);
+    out[6] = decode_pair_fma(prmt(h.w, l1s, 0x1504), base2, c28, one);
+    out[7] = decode_pair_fma(prmt(h.w, l1s, 0x3726), base2, c28, one);
+}
+
 // Escape entries of one 256-column group, one per lane (lane < cnt).
 struct EscBatch {
     uint32_t ent;  // key<<16 | BF16 bits
     int cnt;       // entries in the group (warp-uniform)
-    int64_t p0;    // index of the group's first entry
+    int p0;        // index of the group's first entry (offsets are int32)
 };
 
-__device__ __forceinline__ EscBatch load_group_escapes(const TensorView &t, int64_t p0, int64_t p1, int lane) {
+__device__ __forceinline__ EscBatch load_group_escapes(const TensorView &t, int p0, int p1, int lane) {
     EscBatch b;
     b.p0 = p0;
     b.cnt = (int)(p1 - p0);
@@ -80,8 +107,17 @@ __device__ __forceinline__ EscBatch load_group_escapes(const TensorView &t, int6
     return b;
 }
 
-// Writes escape `ent` (key<<16 | bits) of tile c4 into the per-warp copy of
-// the A fragments: slot = 4*(row%8) + col/16, component (pair&1)*2 + row/8,
+// Bit p set when tile p of the group holds an escape (all bits when the group
+// holds more than 32, which are then walked from memory).
+__device__ __forceinline__ uint32_t escape_tiles(const EscBatch &b, int lane) {
+    if (b.cnt > 32) return 0xFu;
+    const uint32_t c4 = b.ent >> 26;
+    const uint32_t bit = (lane < b.cnt && c4 < 4) ? (1u << c4) : 0u;
+    return __reduce_or_sync(kFull, bit);
+}
+
+// Writes escape `ent` (key<<16 | bits) into the per-warp copy of the A
+// fragments: slot = 4*(row%8) + col/16, component (pair&1)*2 + row/8,
 // half = col&1.
 __device__ __forceinline__ void patch_one(uint4 (*patch)[32], uint32_t ent) {
     const int key = (int)(ent >> 16);
@@ -93,7 +129,7 @@ __device__ __forceinline__ void patch_one(uint4 (*patch)[32], uint32_t ent) {
 }
 
 template <int NB>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16)
-__global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs g) {
+__global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(TensorView t, GemmArgs g) {
     __shared__ __align__(16) uint4 patch[kWarps][4][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, q = lane & 3;
@@ -101,69 +137,72 @@ __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs
     const int64_t T = t.Np / 16;
     const int64_t items = T * S;
     constexpr int MP = 8 * NB;
+    const uint32_t c28 = g.c28, one = g.one, c16 = g.c16;
 
     for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < items;
          item += (int64_t)gridDim.x * kWarps) {
         const int64_t st = item / S;
         const int s = (int)(item % S);
-        // Chunk s covers whole 256-column groups [g_beg, g_end).
+        // Chunk s covers whole 256-column groups [g_beg, g_end) (4 tiles each).
         const int64_t g_beg = (s * t.G) / S, g_end = ((s + 1) * t.G) / S;
-        const int64_t c_beg = 4 * g_beg;
-        const int64_t c_end = (4 * g_end < t.KT) ? 4 * g_end : t.KT;
-        const int64_t n0 = st * 16;
-        const int64_t rowA = n0 + gid, rowB = n0 + gid + 8;
+        const int n0 = (int)(st * 16);  // rows < 2^30
+        const int rowA = n0 + gid, rowB = n0 + gid + 8;
 
         // 1. weight stream first, so that its latency covers the set-up below
-        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + st * t.KT * 64 + lane;
-        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + st * t.KT * 32 + lane;
-        uint4 bh0[kPrefetch], bh1[kPrefetch], bl[kPrefetch];
+        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg) * 64 + lane;
+        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg) * 32 + lane;
+        uint4 bh0[4], bh1[4], bl[4];
+        if (g_beg < g_end) {
 #pragma unroll
-        for (int p = 0; p < kPrefetch; ++p) {
-            const int64_t c = c_beg + p;
-            if (c < c_end) {
-                bh0[p] = ld_stream(hp + c * 64);
-                bh1[p] = ld_stream(hp + c * 64 + 32);
-                bl[p] = ld_stream(lp + c * 32);
+            for (int p = 0; p < 4; ++p) {
+                bh0[p] = ld_stream(hp + p * 64);
+                bh1[p] = ld_stream(hp + p * 64 + 32);
+                bl[p] = ld_stream(lp + p * 32);
             }
         }
-        // 2. bases, group offsets (lane l holds the offset of group g_beg + l),
+        // 2. bases, group offsets (lane l holds the offset of group gw0 + l),
         //    escapes of the first two groups
         const uint32_t base2A = (rowA < t.N ? (uint32_t)__ldg(t.base + rowA) : 0u) * 0x00800080u;
         const uint32_t base2B = (rowB < t.N ? (uint32_t)__ldg(t.base + rowB) : 0u) * 0x00800080u;
-        const int64_t pbase = st * t.G;
-        int64_t gw0 = g_beg;  // first group of the offset window
-        auto load_window = [&](int64_t first) -> int64_t {
-            const int64_t gi = first + lane;
-            int64_t v = 0;
-            if (gi <= g_end) {
-                v = __ldg(t.esc_ptr + pbase + gi);
-                v = v < 0 ? 0 : (v > t.n_esc ? t.n_esc : v);
+        const int32_t *gptr = t.esc_ptr + st * t.G;
+        const int n_esc = (int)t.n_esc;  // offsets are int32
+        int gw0 = (int)g_beg;
+        const int gend = (int)g_end;
+        auto load_window = [&](int first) -> int {
+            const int gi = first + lane;
+            int v = 0;
+            if (gi <= gend) {
+                v = __ldg(gptr + gi);
+                v = v < 0 ? 0 : (v > n_esc ? n_esc : v);
             }
             return v;
         };
-        int64_t ptrw = load_window(gw0);
-        auto group_bounds = [&](int64_t gg, int64_t &p0, int64_t &p1) {
-            if (gg + 1 - gw0 >= 32) {  // slide the window (rare: > 30 groups per chunk)
+        int ptrw = load_window(gw0);
+        auto group_bounds = [&](int gg, int &p0, int &p1) {
+            if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per chunk)
                 gw0 = gg;
                 ptrw = load_window(gw0);
             }
-            p0 = __shfl_sync(kFull, ptrw, (int)(gg - gw0));
-            p1 = __shfl_sync(kFull, ptrw, (int)(gg + 1 - gw0));
+            p0 = __shfl_sync(kFull, ptrw, gg - gw0);
+            p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
             if (p1 < p0) p1 = p0;
         };
-        int64_t p0, p1;
-        group_bounds(g_beg, p0, p1);
-        EscBatch cur = load_group_escapes(t, p0, p1, lane);
-        EscBatch nxt;
-        nxt.cnt = 0;
-        nxt.ent = 0;
-        nxt.p0 = 0;
+        int p0 = 0, p1 = 0;
+        EscBatch cur, nxt;
+        cur.cnt = nxt.cnt = 0;
+        cur.ent = nxt.ent = 0;
+        cur.p0 = nxt.p0 = 0;
+        if (g_beg < g_end) {
+            group_bounds((int)g_beg, p0, p1);
+            cur = load_group_escapes(t, p0, p1, lane);
+        }
         if (g_beg + 1 < g_end) {
-            group_bounds(g_beg + 1, p0, p1);
+            group_bounds((int)g_beg + 1, p0, p1);
             nxt = load_group_escapes(t, p0, p1, lane);
         }
 
-        // Activation rows of this lane (token m = 8*b + gid).
+        // Activation rows of this lane (token m = 8*b + gid); B fragments are
+        // double-buffered one tile ahead.
         const uint16_t *arow[NB];
         bool mval[NB];
 #pragma unroll
@@ -172,80 +211,80 @@ __global__ __launch_bounds__(kWarps * 32) void k_gemm_mma(TensorView t, GemmArgs
             mval[b] = m < g.M;
             arow[b] = g.A + (mval[b] ? (int64_t)m * g.lda : 0);
         }
+        uint32_t bw[2][NB][8];
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) bw[0][b][j] = bw[1][b][j] = 0u;
+        if (g_beg < g_end) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) load_act16(arow[b], g_beg * 256 + 16 * q, t.K, mval[b], bw[0][b]);
+        }
+        uint32_t emask = (g_beg < g_end) ? escape_tiles(cur, lane) : 0u;
 
         float acc[NB][4];
 #pragma unroll
         for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
 
         for (int64_t gg = g_beg; gg < g_end; ++gg) {
-            const int64_t cc = 4 * gg;
+            const bool more = gg + 1 < g_end;
 #pragma unroll
-            for (int p = 0; p < kPrefetch; ++p) {  // tile p of the group
-                const int64_t c = cc + p;
-                if (c < c_end) {
-                    uint32_t dA[8], dB[8];
-                    decode16(bh0[p], bl[p].x, bl[p].y, base2A, dA);
-                    decode16(bh1[p], bl[p].z, bl[p].w, base2B, dB);
-                    const int64_t cn = c + kPrefetch;
-                    if (cn < c_end) {
-                        bh0[p] = ld_stream(hp + cn * 64);
-                        bh1[p] = ld_stream(hp + cn * 64 + 32);
-                        bl[p] = ld_stream(lp + cn * 32);
-                    }
+            for (int p = 0; p < 4; ++p) {  // tile p of group gg
+                uint32_t dA[8], dB[8];
+                decode16_fma(bh0[p], bl[p].x, bl[p].y, base2A, c28, one, c16, dA);
+                decode16_fma(bh1[p], bl[p].z, bl[p].w, base2B, c28, one, c16, dB);
+                if (more) {  // the same tile of the next group
+                    bh0[p] = ld_stream(hp + 256 + p * 64);
+                    bh1[p] = ld_stream(hp + 256 + p * 64 + 32);
+                    bl[p] = ld_stream(lp + 128 + p * 32);
+                }
+                if (p < 3 || more) {  // activations of the next tile
+                    const int64_t kn = gg * 256 + (p + 1) * 64 + 16 * q;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) load_act16(arow[b], kn, t.K, mval[b], bw[(p + 1) & 1][b]);
+                }
 
-                    // Escapes of this tile replace the decoded placeholders.
-                    const bool mine = lane < cur.cnt && (int)(cur.ent >> 26) == p;
-                    const bool many = cur.cnt > 32;  // warp-uniform
-                    if (__any_sync(kFull, mine) || many) {
+                // Escapes of this tile replace the decoded placeholders.
+                if ((emask >> p) & 1u) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            patch[warp][i][lane] = make_uint4(dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1]);
-                        __syncwarp();
-                        if (!many) {
-                            if (mine) patch_one(patch[warp], cur.ent);
-                        } else {
-                            // more than 32 escapes in the group: walk it in batches of 32
-                            for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
-                                const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
-                                if (b0 + lane < cur.cnt && (int)(e >> 26) == p) patch_one(patch[warp], e);
-                            }
-                        }
-                        __syncwarp();
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint4 v = patch[warp][i][lane];
-                            dA[2 * i] = v.x;
-                            dB[2 * i] = v.y;
-                            dA[2 * i + 1] = v.z;
-                            dB[2 * i + 1] = v.w;
-                        }
-                        __syncwarp();
-                    }
-
-                    // B fragments: lane (gid, q) holds A[m, 64c + 16q .. +15].
-                    uint32_t bw[NB][8];
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        if (mval[b]) {
-                            load_act16(arow[b], c * 64 + 16 * q, t.K, bw[b]);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) bw[b][j] = 0u;
+                    for (int i = 0; i < 4; ++i)
+                        patch[warp][i][lane] = make_uint4(dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1]);
+                    __syncwarp();
+                    if (cur.cnt <= 32) {
+                        if (lane < cur.cnt && (int)(cur.ent >> 26) == p) patch_one(patch[warp], cur.ent);
+                    } else {  // more than 32 escapes in the group: walk it in batches
+                        for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
+                            const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
+                            if (b0 + lane < cur.cnt && (int)(e >> 26) == p) patch_one(patch[warp], e);
                         }
                     }
+                    __syncwarp();
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                        for (int b = 0; b < NB; ++b)
-                            mma16816(acc[b], dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1], bw[b][2 * i],
-                                     bw[b][2 * i + 1]);
+                        const uint4 v = patch[warp][i][lane];
+                        dA[2 * i] = v.x;
+                        dB[2 * i] = v.y;
+                        dA[2 * i + 1] = v.z;
+                        dB[2 * i + 1] = v.w;
                     }
+                    __syncwarp();
+                }
+
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        mma16816(acc[b], dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1], bw[p & 1][b][2 * i],
+                                 bw[p & 1][b][2 * i + 1]);
                 }
             }
-            // next group's escapes are already in flight; fetch the one after
+            hp += 256;
+            lp += 128;
+            // the next group's escapes are already in flight; fetch the one after
             cur = nxt;
+            emask = more ? escape_tiles(cur, lane) : 0u;
             if (gg + 2 < g_end) {
-                group_bounds(gg + 2, p0, p1);
+                group_bounds((int)gg + 2, p0, p1);
                 nxt = load_group_escapes(t, p0, p1, lane);
             }
         }

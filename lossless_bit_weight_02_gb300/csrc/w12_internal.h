@@ -21,7 +21,7 @@ struct TensorView {
     int64_t n_esc;
 };
 
-__host__ __device__ inline int64_t groups_of(int64_t K) { return ((K + 63) / 64 + 3) / 4; }
+__host__ __device__ inline int64_t groups_of(int64_t K) { return (K + 255) / 256; }
 
 // ---- codec (w12_codec.cu) ----
 // a1 + a2: base[n] and, added into esc_ptr[t*G+g+1] (zeroed by the caller),
@@ -56,6 +56,7 @@ struct GemmArgs {
     float *partials;     // [S][Np][MP] fp32 (S > 1)
     int32_t *counters;   // [Np/16] arrival counters (S > 1)
     int32_t *error;      // device error word
+    uint32_t c28, one, c16;  // 1<<28, 1, 16: multiplicands the decoder needs at run time
 };
 
 // Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).

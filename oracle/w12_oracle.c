@@ -37,8 +37,9 @@
  *      key of weight (n,k) inside its group is (k%256/64)<<10 | (n%16)<<6 | k%64;
  *   R7 an output channel is a row of W[N,K] (Y = A * W^T);
  *   R8 planes are padded to Np = N rounded up to 16 and Kp = K rounded up to
- *      64 and stored tile by tile (16 rows x 64 columns); the in-tile order is
- *      fixed by w12ref_hi_offset / w12ref_lo_position below.
+ *      256 (whole escape groups of 4 tiles) and stored tile by tile (16 rows x
+ *      64 columns); the in-tile order is fixed by w12ref_hi_offset /
+ *      w12ref_lo_position below.
  *
  * All functions return 0 on success and a negative code on bad arguments.
  */
@@ -105,7 +106,7 @@ uint16_t w12ref_bf16_from_double(double x)
 
 /* ---- shape helpers (reading R8) ---- */
 int64_t w12ref_rows_padded(int64_t N) { return (N + 15) / 16 * 16; }
-int64_t w12ref_cols_padded(int64_t K) { return (K + 63) / 64 * 64; }
+int64_t w12ref_cols_padded(int64_t K) { return (K + 255) / 256 * 256; }
 int64_t w12ref_hi_bytes(int64_t N, int64_t K) { return w12ref_rows_padded(N) * w12ref_cols_padded(K); }
 int64_t w12ref_lo_bytes(int64_t N, int64_t K) { return w12ref_rows_padded(N) * w12ref_cols_padded(K) / 2; }
 
@@ -177,7 +178,7 @@ int w12ref_record(uint16_t w, int base)
 }
 
 /* Escape-list geometry (reading R6). */
-int64_t w12ref_groups(int64_t K) { return (w12ref_cols_padded(K) / 64 + 3) / 4; }
+int64_t w12ref_groups(int64_t K) { return w12ref_cols_padded(K) / 256; }
 int64_t w12ref_ptr_len(int64_t N, int64_t K) { return w12ref_rows_padded(N) / 16 * w12ref_groups(K) + 1; }
 
 int w12ref_key(int64_t n, int64_t k) { return (int)(((k % 256) / 64) << 10 | (n % 16) << 6 | (k % 64)); }

@@ -42,6 +42,7 @@ def test_size_queries(w12lib):
     assert lib.w12_rows_padded(-1) == -1
     assert lib.w12_verify_workspace_bytes() == 16
     assert lib.w12_groups(5120) == 20 and lib.w12_groups(17400) == 68 and lib.w12_groups(65) == 1
+    assert lib.w12_cols_padded(65) == 256 and lib.w12_cols_padded(1000) == 1024
     assert lib.w12_esc_ptr_len(5121, 17400) == 321 * 68 + 1
     assert (lib.w12_version() >> 16) == 1
 

@@ -153,9 +153,9 @@ def test_record_closed_form(oracle):
 def test_layout_is_a_bijection(oracle):
     """Every (n,k) of the padded Np x Kp grid owns a distinct hi byte and a
     distinct lo nibble, covering both planes exactly once."""
-    N, K = 37, 200
+    N, K = 37, 300
     Np, Kp = oracle.rows_padded(N), oracle.cols_padded(K)
-    assert (Np, Kp) == (48, 256)
+    assert (Np, Kp) == (48, 512)
     hi_seen = np.zeros(Np * Kp, np.int32)
     lo_seen = np.zeros(Np * Kp, np.int32)
     for n in range(Np):
