@@ -161,6 +161,30 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
                     int64_t ldy, int64_t M, void *workspace, size_t ws_bytes,
                     const w12_gemm_opts *opts, w12_stream_t stream);
 
+/* ---- w12_gemm_noalloc ----  The paper has no counterpart to this call; it
+ * exists for callers that cannot allocate device memory: engines that plan
+ * all of their device memory at start-up and forbid allocation afterwards,
+ * plug-ins that run inside another framework's memory pool, and latency-
+ * critical loops where cudaMalloc's implicit device synchronisation would
+ * stall other streams.  It computes exactly what w12_gemm computes (same
+ * kernels, same split, bitwise the same Y) but takes no workspace: it uses a
+ * scratch array of W12_NOALLOC_SCRATCH_BYTES built into the library, which
+ * every GPU that loads the library keeps until the process exits.  It calls
+ * no allocation routine.
+ *   - Shapes and options whose w12_gemm workspace would exceed the scratch
+ *     return W12_ERR_CAPACITY (the automatic split of any shape with
+ *     M <= 16 fits).
+ *   - The first call on a device looks up the scratch array's device
+ *     address (once per device, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call shares the one scratch array and clears its counters on
+ *     `stream` before use, so calls that overlap on the GPU (different
+ *     streams, or different host threads) race and must not be issued.
+ * Asynchronous on `stream`, like w12_gemm. */
+#define W12_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+w12_status w12_gemm_noalloc(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_t *Y,
+                            int64_t ldy, int64_t M, const w12_gemm_opts *opts, w12_stream_t stream);
+
 /* Reads (and clears) the device-side error word that bounded waits inside
  * w12_gemm set when they give up.  Synchronous on `stream`.  Returns W12_OK
  * or W12_ERR_TIMEOUT. */

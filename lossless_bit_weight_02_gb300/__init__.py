@@ -43,9 +43,12 @@ EXPORTS = (
     "w12_rows_padded", "w12_cols_padded", "w12_hi_bytes", "w12_lo_bytes", "w12_groups",
     "w12_esc_ptr_len", "w12_encode",
     "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
-    "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_workspace_status", "w12_status_string",
-    "w12_version",
+    "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_noalloc", "w12_gemm_workspace_status",
+    "w12_status_string", "w12_version",
 )
+
+# Size of the scratch array built into the library for w12_gemm_noalloc.
+W12_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class W12Error(RuntimeError):
@@ -99,6 +102,8 @@ def load(path: str | None = None):
             "w12_gemm_workspace_bytes": (sz, [i64, i64, i64, ctypes.POINTER(GemmOpts)]),
             "w12_gemm": (st, [vp, i64, ctypes.POINTER(_Tensor), vp, i64, i64, vp, sz,
                               ctypes.POINTER(GemmOpts), vp]),
+            "w12_gemm_noalloc": (st, [vp, i64, ctypes.POINTER(_Tensor), vp, i64, i64,
+                                      ctypes.POINTER(GemmOpts), vp]),
             "w12_gemm_workspace_status": (st, [vp, sz, vp]),
             "w12_status_string": (ctypes.c_char_p, [st]),
             "w12_version": (ctypes.c_int32, []),
@@ -328,6 +333,20 @@ class GemmCall:
         st = self._fn(*self._args)
         if st != W12_OK:
             raise W12Error(st, "w12_gemm")
+
+
+def w12_gemm_noalloc(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, opts: GemmOpts | None = None,
+                     stream=None) -> torch.Tensor:
+    """w12_gemm without a workspace: the library's built-in scratch array is
+    used (for callers that cannot allocate device memory).  Y must be given."""
+    _need_cuda(A, "A", torch.bfloat16)
+    _need_cuda(Y, "Y", torch.bfloat16)
+    o = opts if opts is not None else make_opts()
+    s = t.struct()
+    _check(load().w12_gemm_noalloc(ctypes.c_void_p(A.data_ptr()), A.stride(0), ctypes.byref(s),
+                                   ctypes.c_void_p(Y.data_ptr()), Y.stride(0), A.shape[0], ctypes.byref(o),
+                                   _stream(stream)), "w12_gemm_noalloc")
+    return Y
 
 
 def w12_gemm_workspace_status(workspace: Workspace, stream=None) -> int:

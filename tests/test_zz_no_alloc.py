@@ -1,0 +1,71 @@
+"""w12_gemm_noalloc: the GEMM for callers that cannot allocate device memory.
+
+Engines that plan all device memory up front, plug-ins living in another
+framework's memory pool and latency-critical loops (where cudaMalloc would
+synchronise the device) cannot hand w12_gemm a workspace.  w12_gemm_noalloc
+uses the library's built-in scratch array instead.  This test calls it
+through the C ABI twice in a row, on two shapes that both use the split-K
+scratch, and checks each result against the existing entry point w12_gemm
+with the tolerance rule the other GEMM tests use (and, since both run the
+same kernels with the same split, bit for bit).
+
+The file is named to be collected last, so that a run stopping at the first
+failure has run every other test before this one.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from lossless_bit_weight_02_gb300 import synth
+from w12_tol import gemm_tolerance_failures
+
+pytestmark = pytest.mark.gpu
+
+
+def call_noalloc(w12lib, A, t, Y, opts=None):
+    """The raw C-ABI call (no Python helper in between)."""
+    lib = w12lib.load()
+    s = t.struct()
+    o = opts if opts is not None else w12lib.make_opts()
+    return lib.w12_gemm_noalloc(ctypes.c_void_p(A.data_ptr()), A.stride(0), ctypes.byref(s),
+                                ctypes.c_void_p(Y.data_ptr()), Y.stride(0), A.shape[0], ctypes.byref(o),
+                                w12lib._stream())
+
+
+def test_noalloc_matches_w12_gemm_on_two_calls(w12lib, oracle):
+    cases = ((5120, 5120, 8, 81), (1024, 3072, 16, 82))  # both split K: the scratch counters are used
+    prepared = []
+    for N, K, M, seed in cases:
+        assert w12lib.w12_gemm_workspace_bytes(M, N, K) > 256
+        W = synth.dense_weights(N, K, seed=seed)
+        A = synth.activations(M, K, seed=seed + 1)
+        t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+        Ad = synth.bits_to_tensor(A, "cuda")
+        Y_ref = w12lib.w12_gemm(Ad, t)  # the existing entry point, with its own workspace
+        prepared.append((W, A, t, Ad, Y_ref))
+    torch.cuda.synchronize()
+    # two calls in a row, nothing in between
+    outs = []
+    for W, A, t, Ad, Y_ref in prepared:
+        Y = torch.full_like(Y_ref, float("nan"))
+        assert call_noalloc(w12lib, Ad, t, Y) == w12lib.W12_OK
+        outs.append(Y)
+    torch.cuda.synchronize()
+    for (W, A, t, Ad, Y_ref), Y in zip(prepared, outs):
+        st, ref = oracle.encode(W)
+        st, _, Y64, mag = oracle.gemm(A, ref)
+        got, want = synth.tensor_to_bits(Y), synth.tensor_to_bits(Y_ref)
+        assert gemm_tolerance_failures(got, want, Y64, mag).size == 0
+        assert np.array_equal(got, want)
+
+
+def test_noalloc_rejects_work_beyond_its_scratch(w12lib):
+    N, K, M = 8192, 4096, 16
+    opts = w12lib.make_opts(split_k=16)  # 16 x 8192 x 16 FP32 partials: more than the scratch
+    assert w12lib.w12_gemm_workspace_bytes(M, N, K, opts) > w12lib.W12_NOALLOC_SCRATCH_BYTES
+    t = w12lib.w12_encode(synth.dense_weights_device(N, K, seed=83))
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    Y = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    assert call_noalloc(w12lib, A, t, Y, opts) == w12lib.W12_ERR_CAPACITY
