@@ -16,7 +16,6 @@ constexpr int64_t kMaxN = 1LL << 30;
 constexpr int64_t kMaxCounters = 1LL << 16;  // split-K stripes with an arrival counter
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 w12_status check_tensor(const w12_tensor *w) {
     if (!w) return W12_ERR_INVALID;
@@ -59,7 +58,7 @@ struct GemmPlan {
 int choose_path(int64_t M, const w12_gemm_opts *o) {
     const int p = o ? o->path : W12_PATH_AUTO;
     if (p != W12_PATH_AUTO) return p;
-    return W12_PATH_MMA;
+    return M <= 16 ? W12_PATH_MMA : W12_PATH_TC;
 }
 
 w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, GemmPlan &pl) {
@@ -69,15 +68,16 @@ w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, Ge
     pl.path = choose_path(M, o);
     if (pl.path != W12_PATH_MMA && pl.path != W12_PATH_TC) return W12_ERR_INVALID;
     if (pl.path == W12_PATH_MMA && M > 16) return W12_ERR_UNSUPPORTED;
-    if (pl.path == W12_PATH_TC) return W12_ERR_UNSUPPORTED;
-    int split = (o && o->split_k > 0) ? o->split_k : gemm_mma_split(M, N, K);
-    const int64_t KT = cols_padded(K) / 64;
+    if (pl.path == W12_PATH_TC && M > 256) return W12_ERR_UNSUPPORTED;
+    const bool tc = pl.path == W12_PATH_TC;
+    int split = (o && o->split_k > 0) ? o->split_k : (tc ? gemm_tc_split(M, N, K) : gemm_mma_split(M, N, K));
+    const int64_t G = groups_of(K);
     const int64_t Np = rows_padded(N);
-    if (KT == 0) split = 1;
-    if (split > KT && KT > 0) split = (int)KT;
+    if (G == 0) split = 1;
+    if (split > G && G > 0) split = (int)G;
     if (Np / 16 > kMaxCounters) split = 1;  // arrival counters exist for at most kMaxCounters stripes
     pl.split = split;
-    pl.mp = gemm_mma_partial_cols(M);
+    pl.mp = tc ? gemm_tc_pad(M) : gemm_mma_partial_cols(M);
     // Fixed layout, the same for every shape, so that the counter region is
     // never reused for partials: [0,256) error word | [256, 256+4*kMaxCounters)
     // arrival counters (zero between calls) | FP32 partials.
@@ -205,6 +205,9 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     GemmPlan pl;
     st = plan_gemm(M, w->N, w->K, opts, pl);
     if (st != W12_OK) return st;
+    if (w->K == 0)  // empty reduction: Y = 0
+        return cuda_status(cudaMemset2DAsync(Y, (size_t)ldy * 2, 0, (size_t)w->N * 2, (size_t)M,
+                                             reinterpret_cast<cudaStream_t>(stream)));
     if (!workspace || ws_bytes < pl.bytes) return W12_ERR_CAPACITY;
     if (!aligned16(workspace)) return W12_ERR_ALIGN;
     char *ws = static_cast<char *>(workspace);
@@ -222,7 +225,12 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     g.c28 = 1u << 28;
     g.one = 1u;
     g.c16 = 16u;
-    return cuda_status(launch_gemm_mma(view_of(w), g, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.path == W12_PATH_TC) {
+        const cudaError_t e = launch_gemm_tc(view_of(w), g, s);
+        return e == cudaErrorNotSupported ? W12_ERR_UNSUPPORTED : cuda_status(e);
+    }
+    return cuda_status(launch_gemm_mma(view_of(w), g, s));
 }
 
 w12_status w12_gemm_workspace_status(void *workspace, size_t ws_bytes, w12_stream_t stream) {

@@ -23,19 +23,12 @@
 
 #include "w12_device.cuh"
 #include "w12_internal.h"
+#include "w12_stream.cuh"
 
 namespace w12 {
 namespace {
 
 constexpr int kWarps = 4;  // warps per block; each warp keeps one 4-tile group in flight
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -66,54 +59,6 @@ __device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int
             w[j] = lo | (hi << 16);
         }
     }
-}
-
-// Record-pair decode (as decode_pair in w12_device.cuh) with the right shift
-// done as a high multiply and the base added with a multiply-add, so that two
-// of the five operations run on the FMA pipe instead of the ALU.  c28 = 2^28
-// and one = 1 arrive as kernel arguments so that they stay multiplications.
-__device__ __forceinline__ uint32_t decode_pair_fma(uint32_t Z, uint32_t base2, uint32_t c28, uint32_t one) {
-    const uint32_t t = __umulhi(Z, c28) & 0x07FF07FFu;  // (Z >> 4) & mask
-    uint32_t u;
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(u) : "r"(t), "r"(one), "r"(base2));
-    return (Z & 0x80008000u) | (u & 0x7FFF7FFFu);
-}
-
-__device__ __forceinline__ void decode16_fma(uint4 h, uint32_t l0, uint32_t l1, uint32_t base2, uint32_t c28,
-                                             uint32_t one, uint32_t c16, uint32_t out[8]) {
-    const uint32_t l0s = l0 * c16, l1s = l1 * c16;  // << 4, on the FMA pipe
-    out[0] = decode_pair_fma(prmt(h.x, l0, 0x1504), base2, c28, one);
-    out[1] = decode_pair_fma(prmt(h.x, l0, 0x3726), base2, c28, one);
-    out[2] = decode_pair_fma(prmt(h.y, l0s, 0x1504), base2, c28, one);
-    out[3] = decode_pair_fma(prmt(h.y, l0s, 0x3726), base2, c28, one);
-    out[4] = decode_pair_fma(prmt(h.z, l1, 0x1504), base2, c28, one);
-    out[5] = decode_pair_fma(prmt(h.z, l1, 0x3726), base2, c28, one);
-    out[6] = decode_pair_fma(prmt(h.w, l1s, 0x1504), base2, c28, one);
-    out[7] = decode_pair_fma(prmt(h.w, l1s, 0x3726), base2, c28, one);
-}
-
-// Escape entries of one 256-column group, one per lane (lane < cnt).
-struct EscBatch {
-    uint32_t ent;  // key<<16 | BF16 bits
-    int cnt;       // entries in the group (warp-uniform)
-    int p0;        // index of the group's first entry (offsets are int32)
-};
-
-__device__ __forceinline__ EscBatch load_group_escapes(const TensorView &t, int p0, int p1, int lane) {
-    EscBatch b;
-    b.p0 = p0;
-    b.cnt = (int)(p1 - p0);
-    b.ent = (lane < b.cnt) ? __ldg(t.esc + p0 + lane) : 0u;
-    return b;
-}
-
-// Bit p set when tile p of the group holds an escape (all bits when the group
-// holds more than 32, which are then walked from memory).
-__device__ __forceinline__ uint32_t escape_tiles(const EscBatch &b, int lane) {
-    if (b.cnt > 32) return 0xFu;
-    const uint32_t c4 = b.ent >> 26;
-    const uint32_t bit = (lane < b.cnt && c4 < 4) ? (1u << c4) : 0u;
-    return __reduce_or_sync(kFull, bit);
 }
 
 // Writes escape `ent` (key<<16 | bits) into the per-warp copy of the A

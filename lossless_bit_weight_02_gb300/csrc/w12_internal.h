@@ -59,6 +59,12 @@ struct GemmArgs {
     uint32_t c28, one, c16;  // 1<<28, 1, 16: multiplicands the decoder needs at run time
 };
 
+// Tensor-core path: tcgen05.mma with TMEM accumulators (M <= 256; partials
+// laid out [S][Mpad][Np]).
+cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t s);
+int gemm_tc_split(int64_t M, int64_t N, int64_t K);
+int64_t gemm_tc_pad(int64_t M);
+
 // Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).
 cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s);
 int gemm_mma_split(int64_t M, int64_t N, int64_t K);

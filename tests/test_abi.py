@@ -66,6 +66,11 @@ def test_gemm_workspace_query(w12lib):
     assert w12lib.w12_gemm_workspace_bytes(16, 5120, 5120, o) == 256 + 4 * 65536 + S * 2 * slab
     assert w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, w12lib.make_opts(split_k=1)) == 256
     assert w12lib.w12_gemm_workspace_bytes(17, 64, 64, w12lib.make_opts(path=w12lib.W12_PATH_MMA)) == 0
+    assert w12lib.w12_gemm_workspace_bytes(257, 64, 64, o) == 0  # beyond the tensor-core path
+    # the tensor-core path keeps [S][Mpad][Np] partials
+    nb = w12lib.w12_gemm_workspace_bytes(40, 1024, 4096, o)
+    S, rem = divmod(nb - 256 - 4 * 65536, 48 * 1024 * 4)
+    assert rem == 0 and S >= 2
     bad = w12lib.GemmOpts(0, 0, 0, 1)  # reserved must be 0
     assert w12lib.w12_gemm_workspace_bytes(1, 64, 64, bad) == 0
 

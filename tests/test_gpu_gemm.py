@@ -170,3 +170,12 @@ def test_full_size_layers_sampled(name, N, K, w12lib, oracle):
         st, y, y64, mag = oracle.gemm_sample(synth.tensor_to_bits(Ad), ref, ms, np.arange(48))
         assert st == oracle.OK
         assert gemm_tolerance_failures(Y[ms, ns], y, y64, mag).size == 0
+
+
+def test_k_zero_writes_zeros(w12lib):
+    t = w12lib.w12_encode(torch.zeros(40, 0, dtype=torch.bfloat16, device="cuda"))
+    for M in (3, 40):
+        A = torch.zeros(M, 8, dtype=torch.bfloat16, device="cuda")[:, :0]
+        Y = torch.full((M, 40), 5.0, dtype=torch.bfloat16, device="cuda")
+        w12lib.w12_gemm(A, t, Y=Y)
+        assert (Y == 0).all()
