@@ -66,8 +66,8 @@ def test_tc_forced_splits(split, w12lib, oracle):
 
 
 def test_tc_adversarial_m33(w12lib, oracle):
-    W = synth.adversarial_weights(400, 1500, seed=33)
-    A = synth.activations(33, 1500, seed=3300)
+    W = synth.adversarial_weights(400, 1496, seed=33)
+    A = synth.activations(33, 1496, seed=3300)
     parity(w12lib, oracle, W, A, reps=3)
 
 
