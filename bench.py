@@ -32,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 M_VALUES = (1, 2, 4, 8)
-SWEEP_M = (16,)
+SWEEP_M = (16, 24, 32, 63, 64, 128, 256)  # tree / batch verification rows
 METRIC = "W12 GEMM weight-GB/s & % HBM roofline at M=1/16/64 (27B-class layers)"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -168,7 +168,9 @@ def run_gpu(args):
             for M in Ms for name, t in layers}
     wsp = w12.Workspace(dev, max(w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in Ms for _, t in layers))
     stream = torch.cuda.current_stream(dev)
-    wsp.ensure(max(w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in Ms for _, t in layers))
+    wsp.ensure(max([w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in Ms for _, t in layers] +
+                   [w12.w12_gemm_workspace_bytes(16, t.N, t.K, w12.make_opts(path=w12.W12_PATH_TC))
+                    for _, t in layers]))
     calls = {(M, name): w12.GemmCall(acts[(M, name)], t, outs[(M, name)], wsp, stream=stream)
              for M in Ms for name, t in layers}
 
@@ -235,23 +237,38 @@ def run_gpu(args):
                                                 / hbm_peak, 4)}
     per_layer = {name: round(statistics.median(dur[(1, name)]) * 1e3, 2) for name, _ in layers}
 
-    # ---- M = 16 (tree / batch verification), timed the same way ----
-    sweep = {}
-    for M in SWEEP_M:
+    # ---- M = 16..256 (tree / batch verification), timed the same way ----
+    # roofline per M: max(algorithmic bytes / HBM peak, 2MNK / BF16 peak)
+    def sweep_point(M, call_of):
         ev2 = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in range(len(layers))]
-        ts = []
         for _ in range(max(3, args.warmup)):
-            one_step(None, (M,))
-        for _ in range(50):
-            one_step(ev2, (M,))
+            for name, _ in layers:
+                call_of(name)()
+        ts = []
+        for _ in range(30):
+            for j, (name, _) in enumerate(layers):
+                ev2[j][0].record(stream)
+                call_of(name)()
+                ev2[j][1].record(stream)
             torch.cuda.synchronize()
             ts.append(sum(e[0].elapsed_time(e[1]) for e in ev2))
         ms = statistics.median(ts)
         b = sum(t.nbytes() for _, t in layers)
         ab = sum(alg_bytes[(M, n)] for n, _ in layers)
-        sweep[str(M)] = {"weight_gbs": round(b / (ms * 1e-3) / 1e9, 1),
-                         "roofline_frac": round(ab / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
+        flops = sum(2.0 * M * t.N * t.K for _, t in layers)
+        floor_s = max(ab / (hbm_peak * 1e9), flops / (bf16_peak * 1e12))
+        return {"weight_gbs": round(b / (ms * 1e-3) / 1e9, 1), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                "roofline_frac": round(floor_s / (ms * 1e-3), 4), "us": round(ms * 1e3, 1)}
+
+    sweep = {}
+    for M in SWEEP_M:
+        sweep[str(M)] = sweep_point(M, lambda name, M=M: calls[(M, name)])
+        sweep[str(M)]["path"] = "mma" if M <= 16 else "tcgen05"
+    tc16 = {name: w12.GemmCall(acts[(16, name)], t, outs[(16, name)], wsp, stream=stream,
+                               opts=w12.make_opts(path=w12.W12_PATH_TC)) for name, t in layers}
+    sweep["16_tcgen05"] = sweep_point(16, lambda name: tc16[name])
+    sweep["16_tcgen05"]["path"] = "tcgen05"
 
     # ---- end to end through the public API with host buffers ----
     h_in = {key: a.cpu().pin_memory() for key, a in acts.items() if key[0] in M_VALUES}

@@ -319,10 +319,10 @@ class GemmCall:
                  opts: GemmOpts | None = None, stream=None):
         _need_cuda(A, "A", torch.bfloat16)
         _need_cuda(Y, "Y", torch.bfloat16)
-        self._keep = (A, t, Y, workspace)
         self._opts = opts if opts is not None else make_opts()
         need = w12_gemm_workspace_bytes(A.shape[0], t.N, t.K, self._opts)
         ws = workspace.ensure(max(need, 256))
+        self._keep = (A, t, Y, ws)  # the buffer itself: a later ensure() may replace it
         self._struct = t.struct()
         self._fn = load().w12_gemm
         self._args = (ctypes.c_void_p(A.data_ptr()), A.stride(0), ctypes.byref(self._struct),
