@@ -61,6 +61,16 @@ __device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int
     }
 }
 
+// The same 16 activations when the tile lies inside K (no bounds checks).
+__device__ __forceinline__ void load_act16_inside(const uint16_t *__restrict__ p, bool valid, uint32_t w[8]) {
+    asm volatile(
+        "{\n.reg .pred pp;\nsetp.ne.u32 pp, %8, 0;\n"
+        "@pp ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%9];\n"
+        "@pp ld.global.nc.v4.u32 {%4,%5,%6,%7}, [%9+16];\n}"
+        : "+r"(w[0]), "+r"(w[1]), "+r"(w[2]), "+r"(w[3]), "+r"(w[4]), "+r"(w[5]), "+r"(w[6]), "+r"(w[7])
+        : "r"((uint32_t)valid), "l"(p));
+}
+
 // Writes escape `ent` (key<<16 | bits) into the per-warp copy of the A
 // fragments: slot = 4*(row%8) + col/16, component (pair&1)*2 + row/8,
 // half = col&1.
@@ -146,8 +156,10 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
             nxt = load_group_escapes(t, p0, p1, lane);
         }
 
-        // Activation rows of this lane (token m = 8*b + gid); B fragments are
-        // double-buffered one tile ahead.
+        // Activation rows of this lane (token m = 8*b + gid) at its 16 columns
+        // of a tile; B fragments are double-buffered one tile ahead.  Chunks
+        // that end inside K (only the last one of a ragged K) take the
+        // bounds-checked load.
         const uint16_t *arow[NB];
         bool mval[NB];
 #pragma unroll
@@ -156,6 +168,7 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
             mval[b] = m < g.M;
             arow[b] = g.A + (mval[b] ? (int64_t)m * g.lda : 0);
         }
+        const bool kfull = 256 * g_end <= t.K;  // warp-uniform
         uint32_t bw[2][NB][8];
 #pragma unroll
         for (int b = 0; b < NB; ++b)
@@ -165,7 +178,34 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
 #pragma unroll
             for (int b = 0; b < NB; ++b) load_act16(arow[b], g_beg * 256 + 16 * q, t.K, mval[b], bw[0][b]);
         }
-        uint32_t emask = (g_beg < g_end) ? escape_tiles(cur, lane) : 0u;
+        const uint16_t *ag[NB];  // arow + 256*gg + 16q
+#pragma unroll
+        for (int b = 0; b < NB; ++b) ag[b] = arow[b] + g_beg * 256 + 16 * q;
+
+        // This lane's escape of the current group (at most one while the
+        // group holds <= 32): its tile, its byte in the per-warp fragment
+        // copy (slot 4*(row%8)+col/16, component (pair&1)*2+row/8, half
+        // col&1), its bits.
+        uint8_t *pw = reinterpret_cast<uint8_t *>(patch[warp]);
+        uint32_t e_tile = 4, e_off = 0;
+        uint16_t e_val = 0;
+        auto own_escape = [&]() {
+            e_tile = 4;
+            if (lane < cur.cnt && cur.cnt <= 32) {
+                const uint32_t key = cur.ent >> 16;
+                const uint32_t r = (key >> 6) & 15, j = key & 63;
+                const uint32_t slot = (r & 7) * 4 + (j >> 4), j16 = j & 15, pr = j16 >> 1;
+                const uint32_t comp = (pr & 1) * 2 + (r >> 3);
+                e_tile = key >> 10;
+                e_off = ((pr >> 1) * 32 + slot) * 16 + comp * 4 + (j16 & 1) * 2;
+                e_val = (uint16_t)(cur.ent & 0xFFFFu);
+            }
+        };
+        uint32_t emask = 0u;
+        if (g_beg < g_end) {
+            emask = escape_tiles(cur, lane);
+            own_escape();
+        }
 
         float acc[NB][4];
 #pragma unroll
@@ -184,9 +224,14 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
                     bl[p] = ld_stream(lp + 128 + p * 32);
                 }
                 if (p < 3 || more) {  // activations of the next tile
-                    const int64_t kn = gg * 256 + (p + 1) * 64 + 16 * q;
+                    if (kfull) {
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) load_act16(arow[b], kn, t.K, mval[b], bw[(p + 1) & 1][b]);
+                        for (int b = 0; b < NB; ++b) load_act16_inside(ag[b] + (p + 1) * 64, mval[b], bw[(p + 1) & 1][b]);
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < NB; ++b)
+                            load_act16(arow[b], gg * 256 + (p + 1) * 64 + 16 * q, t.K, mval[b], bw[(p + 1) & 1][b]);
+                    }
                 }
 
                 // Escapes of this tile replace the decoded placeholders.
@@ -196,7 +241,7 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
                         patch[warp][i][lane] = make_uint4(dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1]);
                     __syncwarp();
                     if (cur.cnt <= 32) {
-                        if (lane < cur.cnt && (int)(cur.ent >> 26) == p) patch_one(patch[warp], cur.ent);
+                        if (e_tile == (uint32_t)p) *reinterpret_cast<uint16_t *>(pw + e_off) = e_val;
                     } else {  // more than 32 escapes in the group: walk it in batches
                         for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
                             const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
@@ -225,9 +270,14 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
             }
             hp += 256;
             lp += 128;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) ag[b] += 256;
             // the next group's escapes are already in flight; fetch the one after
             cur = nxt;
-            emask = more ? escape_tiles(cur, lane) : 0u;
+            if (more) {
+                emask = escape_tiles(cur, lane);
+                own_escape();
+            }
             if (gg + 2 < g_end) {
                 group_bounds((int)gg + 2, p0, p1);
                 nxt = load_group_escapes(t, p0, p1, lane);
