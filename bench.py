@@ -171,7 +171,10 @@ def run_gpu(args):
     wsp.ensure(max([w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in Ms for _, t in layers] +
                    [w12.w12_gemm_workspace_bytes(16, t.N, t.K, w12.make_opts(path=w12.W12_PATH_TC))
                     for _, t in layers]))
-    calls = {(M, name): w12.GemmCall(acts[(M, name)], t, outs[(M, name)], wsp, stream=stream)
+    # weights are resident and never written while the step runs, so every
+    # GEMM may overlap the previous one (programmatic dependent launch)
+    overlap = w12.make_opts(flags=w12.W12_GEMM_OVERLAP_PREVIOUS)
+    calls = {(M, name): w12.GemmCall(acts[(M, name)], t, outs[(M, name)], wsp, stream=stream, opts=overlap)
              for M in Ms for name, t in layers}
 
     def one_step(ev=None, m_values=M_VALUES):
@@ -193,8 +196,10 @@ def run_gpu(args):
         one_step()
     torch.cuda.synchronize()
 
-    # per-launch events for (up to) the first 400 timed steps
-    n_ev = min(args.steps, 400)
+    # per-launch events on every 10th timed step only: an event between two
+    # launches keeps the second from overlapping the first
+    ev_steps = list(range(0, args.steps, 10))
+    n_ev = len(ev_steps)
     evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
             for _ in range(launches_per_step)] for _ in range(n_ev)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -205,8 +210,9 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
+    ev_of = {k: i for i, k in enumerate(ev_steps)}
     for k in range(args.steps):
-        one_step(evs[k] if k < n_ev else None)
+        one_step(evs[ev_of[k]] if k in ev_of else None)
     stop.record(stream)
     torch.cuda.synchronize()
     if ws_n > 1:
@@ -266,7 +272,8 @@ def run_gpu(args):
         sweep[str(M)] = sweep_point(M, lambda name, M=M: calls[(M, name)])
         sweep[str(M)]["path"] = "mma" if M <= 16 else "tcgen05"
     tc16 = {name: w12.GemmCall(acts[(16, name)], t, outs[(16, name)], wsp, stream=stream,
-                               opts=w12.make_opts(path=w12.W12_PATH_TC)) for name, t in layers}
+                               opts=w12.make_opts(path=w12.W12_PATH_TC, flags=w12.W12_GEMM_OVERLAP_PREVIOUS))
+            for name, t in layers}
     sweep["16_tcgen05"] = sweep_point(16, lambda name: tc16[name])
     sweep["16_tcgen05"]["path"] = "tcgen05"
 

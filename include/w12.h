@@ -93,13 +93,22 @@ typedef struct {
 #define W12_PATH_MMA 1      /* decode in registers + mma.sync, 1 <= M <= 16 */
 #define W12_PATH_TC 2       /* tcgen05 / TMEM path, 16 <= M <= 256 */
 
+/* w12_gemm_opts.flags bits.
+ * W12_GEMM_OVERLAP_PREVIOUS: the caller promises that the W12 tensor is not
+ * being written by work still in flight on `stream`.  The GEMM is then
+ * launched as a programmatic dependent launch and starts streaming its
+ * weights while the previous kernel on the stream drains; it reads A and
+ * writes Y and the workspace only after that kernel has completed.  For
+ * back-to-back GEMMs over resident weights (a model's forward pass). */
+#define W12_GEMM_OVERLAP_PREVIOUS 1
+
 /* Options of w12_gemm (NULL = all defaults).  Results are bitwise identical
- * for any max_ctas; they depend only on (M, N, K, path, split_k). */
+ * for any max_ctas and flags; they depend only on (M, N, K, path, split_k). */
 typedef struct {
     int32_t max_ctas;       /* 0 = as many as fit; >0 caps the grid (tests) */
     int32_t split_k;        /* 0 = chosen from (M,N,K); >0 forces the split */
     int32_t path;           /* W12_PATH_* */
-    int32_t reserved;       /* must be 0 */
+    int32_t flags;          /* W12_GEMM_* bits; unknown bits are rejected */
 } w12_gemm_opts;
 
 /* ---- size queries (host only, no CUDA call) ---- */

@@ -37,6 +37,7 @@ W12_ERR_CORRUPT = -7
 W12_ERR_UNSUPPORTED = -8
 
 W12_PATH_AUTO, W12_PATH_MMA, W12_PATH_TC = 0, 1, 2
+W12_GEMM_OVERLAP_PREVIOUS = 1
 
 # Every symbol include/w12.h declares.
 EXPORTS = (
@@ -68,7 +69,7 @@ class _Tensor(ctypes.Structure):
 
 class GemmOpts(ctypes.Structure):
     _fields_ = [("max_ctas", ctypes.c_int32), ("split_k", ctypes.c_int32),
-                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("path", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -265,8 +266,8 @@ def w12_verify_roundtrip(W: torch.Tensor, t: W12Tensor, workspace: torch.Tensor 
     return st, nm.value
 
 
-def make_opts(max_ctas=0, split_k=0, path=W12_PATH_AUTO) -> GemmOpts:
-    return GemmOpts(max_ctas, split_k, path, 0)
+def make_opts(max_ctas=0, split_k=0, path=W12_PATH_AUTO, flags=0) -> GemmOpts:
+    return GemmOpts(max_ctas, split_k, path, flags)
 
 
 def w12_gemm_workspace_bytes(M: int, N: int, K: int, opts: GemmOpts | None = None) -> int:

@@ -93,6 +93,8 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
     const int64_t items = T * S;
     constexpr int MP = 8 * NB;
     const uint32_t c28 = g.c28, one = g.one, c16 = g.c16;
+    grid_dep_launch();
+    bool dep_done = false;
 
     for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < items;
          item += (int64_t)gridDim.x * kWarps) {
@@ -154,6 +156,13 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
         if (g_beg + 1 < g_end) {
             group_bounds((int)g_beg + 1, p0, p1);
             nxt = load_group_escapes(t, p0, p1, lane);
+        }
+
+        // Everything above reads only the W12 tensor; activations, Y and the
+        // workspace may belong to the previous kernel on the stream.
+        if (!dep_done) {
+            grid_dep_wait();
+            dep_done = true;
         }
 
         // Activation rows of this lane (token m = 8*b + gid) at its 16 columns
@@ -372,8 +381,16 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
     if (blocks > resident) blocks = resident;
     if (g.max_ctas > 0 && blocks > g.max_ctas) blocks = g.max_ctas;
     if (blocks < 1) blocks = 1;
-    k_gemm_mma<NB><<<(unsigned)blocks, kWarps * 32, 0, s>>>(t, g);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g.overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_gemm_mma<NB>, t, g);
 }
 
 }  // namespace

@@ -183,6 +183,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_launch();
 
     if (warp < kDecWarps) {
         // ------------------------------------------------------------------
@@ -236,6 +237,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
             }
         }
         uint32_t emask = (live && nkb > 0) ? escape_tiles(cur, lane) : 0u;
+        grid_dep_wait();  // Y and the workspace may belong to the previous kernel
         bool ok = true;
         for (int64_t gg = g_beg; gg < g_end && ok; ++gg) {
             const bool more = gg + 1 < g_end;
@@ -359,6 +361,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         // Activations: one TMA tile [Mp x 64] per k-block.
         // ------------------------------------------------------------------
         if (lane == 0) {
+            grid_dep_wait();  // A may be written by the previous kernel
             int issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int stage = kb % R;
@@ -488,8 +491,17 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
     }
     const int64_t blocks = ((t.Np + 127) / 128) * (int64_t)g.split;
     if (blocks == 0) return cudaSuccess;
-    k_gemm_tc<<<(unsigned)blocks, kThreads, smem, s>>>(t, g, tp, map);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g.overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc, t, g, tp, map);
 }
 
 }  // namespace w12

@@ -53,6 +53,7 @@ struct GemmArgs {
     int64_t M;
     int split;           // S >= 1
     int max_ctas;        // 0 = occupancy-limited persistent grid
+    bool overlap;        // launch as a programmatic dependent of the previous kernel
     float *partials;     // [S][Np][MP] fp32 (S > 1)
     int32_t *counters;   // [Np/16] arrival counters (S > 1)
     int32_t *error;      // device error word

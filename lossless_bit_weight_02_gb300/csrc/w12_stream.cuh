@@ -10,6 +10,14 @@
 
 namespace w12 {
 
+// Programmatic dependent launch: a kernel may start (and prefetch its weights)
+// before the previous kernel on the stream has finished; wait() returns once
+// that kernel has completed and its writes are visible (a no-op when the
+// launch was an ordinary one).  launch_dependents() lets the next kernel be
+// scheduled.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 16-byte weight-plane load: read once, kept out of L1.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 r;

@@ -179,3 +179,31 @@ def test_k_zero_writes_zeros(w12lib):
         Y = torch.full((M, 40), 5.0, dtype=torch.bfloat16, device="cuda")
         w12lib.w12_gemm(A, t, Y=Y)
         assert (Y == 0).all()
+
+
+@pytest.mark.parametrize("M", [4, 16, 64])
+def test_overlap_flag_on_a_dependent_chain(M, w12lib):
+    """With W12_GEMM_OVERLAP_PREVIOUS each GEMM may start streaming weights
+    before the previous kernel ends, but it reads A only after that kernel
+    completed: a chain where each GEMM consumes the previous Y gives the
+    same bits as the chain without the flag."""
+    dims = (512, 1024, 768, 256)
+    ts = [w12lib.w12_encode(synth.dense_weights_device(dims[i + 1], dims[i], seed=90 + i))
+          for i in range(len(dims) - 1)]
+    A0 = synth.activations_device(M, dims[0], seed=95)
+    ws = w12lib.Workspace("cuda", 1 << 24)
+
+    def chain(flags):
+        x = A0
+        outs = []
+        for t in ts:
+            x = w12lib.w12_gemm(x, t, workspace=ws, opts=w12lib.make_opts(flags=flags))
+            outs.append(x)
+        torch.cuda.synchronize()
+        return [synth.tensor_to_bits(o) for o in outs]
+
+    plain = chain(0)
+    for _ in range(3):
+        over = chain(w12lib.W12_GEMM_OVERLAP_PREVIOUS)
+        for a, b in zip(plain, over):
+            assert np.array_equal(a, b)
