@@ -83,6 +83,108 @@ __device__ __forceinline__ void patch_one(uint4 (*patch)[32], uint32_t ent) {
     reinterpret_cast<uint16_t *>(&patch[pr >> 1][slot])[comp * 2 + (j16 & 1)] = (uint16_t)(ent & 0xFFFFu);
 }
 
+// Per-warp streaming state of one work item.
+template <int NB>
+struct Stream {
+    uint4 bh0[4], bh1[4], bl[4];  // the 4 tiles of the current group (prefetched)
+    const uint4 *hp, *lp;         // hi / lo planes at the current group, this lane
+    uint32_t base2A, base2B;      // row bases * 0x00800080 (rows g, g+8)
+    const uint16_t *ag[NB];       // activation row + 256*group + 16q
+    bool mval[NB];                // token exists
+    uint32_t bw[2][NB][8];        // B fragments, double-buffered a tile ahead
+    float acc[NB][4];
+    EscBatch cur;                 // escapes of the current group
+    uint32_t emask;               // tiles of the group holding an escape
+    uint32_t e_tile, e_off;       // this lane's escape: tile, byte in the fragment copy
+    uint16_t e_val;
+};
+
+// One 256-column group: for each of its 4 tiles decode the two rows, prefetch
+// the same tile of the next group (or, on the last group, the same tile again:
+// an L2 hit), load the next tile's activations, patch the tile's escapes and
+// run the MMAs.  GUARD selects bounds-checked activation loads (a chunk that
+// ends inside K).
+template <int NB, bool GUARD>
+__device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, const GemmArgs &g, int64_t gg,
+                                           bool more, uint4 (*patch)[32], uint8_t *pw, int lane, int q,
+                                           uint32_t c28, uint32_t one, uint32_t c16) {
+    const int next = more ? 256 : 0;    // uint4 offset of the next group's hi tiles
+    const int nextl = more ? 128 : 0;   // ... and lo tiles
+    const int nexta = more ? 256 : 192;  // activation offset of the tile after the last one
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t dA[8], dB[8];
+        decode16_fma(w.bh0[p], w.bl[p].x, w.bl[p].y, w.base2A, c28, one, c16, dA);
+        decode16_fma(w.bh1[p], w.bl[p].z, w.bl[p].w, w.base2B, c28, one, c16, dB);
+        w.bh0[p] = ld_stream(w.hp + next + p * 64);
+        w.bh1[p] = ld_stream(w.hp + next + p * 64 + 32);
+        w.bl[p] = ld_stream(w.lp + nextl + p * 32);
+        const int an = (p < 3) ? (p + 1) * 64 : nexta;  // next tile's activations
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (GUARD)  // row = ag - 256*gg - 16q, column 256*gg + an + 16q
+                load_act16(w.ag[b] - (gg * 256 + 16 * q), gg * 256 + an + 16 * q, t.K, w.mval[b],
+                           w.bw[(p + 1) & 1][b]);
+            else
+                load_act16_inside(w.ag[b] + an, w.mval[b], w.bw[(p + 1) & 1][b]);
+        }
+
+        // Escapes of this tile replace the decoded placeholders.
+        if ((w.emask >> p) & 1u) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                patch[i][lane] = make_uint4(dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1]);
+            __syncwarp();
+            if (w.cur.cnt <= 32) {
+                asm volatile("{\n.reg .pred pp;\nsetp.eq.u32 pp, %0, %1;\n@pp st.shared.u16 [%2], %3;\n}" ::"r"(w.e_tile),
+                             "r"((uint32_t)p), "r"((uint32_t)__cvta_generic_to_shared(pw + w.e_off)), "h"(w.e_val)
+                             : "memory");
+            } else {  // more than 32 escapes in the group: walk it in batches
+                for (int b0 = 0; b0 < w.cur.cnt; b0 += 32) {
+                    const uint32_t e = (b0 + lane < w.cur.cnt) ? __ldg(t.esc + w.cur.p0 + b0 + lane) : 0u;
+                    if (b0 + lane < w.cur.cnt && (int)(e >> 26) == p) patch_one(patch, e);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = patch[i][lane];
+                dA[2 * i] = v.x;
+                dB[2 * i] = v.y;
+                dA[2 * i + 1] = v.z;
+                dB[2 * i + 1] = v.w;
+            }
+            __syncwarp();
+        }
+
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                mma16816(w.acc[b], dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1], w.bw[p & 1][b][2 * i],
+                         w.bw[p & 1][b][2 * i + 1]);
+        }
+    }
+}
+
+// This lane's escape of the current group (at most one while the group holds
+// <= 32): its tile, its byte in the per-warp fragment copy (slot
+// 4*(row%8)+col/16, component (pair&1)*2+row/8, half col&1), its bits.
+template <int NB>
+__device__ __forceinline__ void own_escape(Stream<NB> &w, int lane) {
+    w.emask = escape_tiles(w.cur, lane);
+    w.e_tile = 4;
+    if (lane < w.cur.cnt && w.cur.cnt <= 32) {
+        const uint32_t key = w.cur.ent >> 16;
+        const uint32_t r = (key >> 6) & 15, j = key & 63;
+        const uint32_t slot = (r & 7) * 4 + (j >> 4), j16 = j & 15, pr = j16 >> 1;
+        const uint32_t comp = (pr & 1) * 2 + (r >> 3);
+        w.e_tile = key >> 10;
+        w.e_off = ((pr >> 1) * 32 + slot) * 16 + comp * 4 + (j16 & 1) * 2;
+        w.e_val = (uint16_t)(w.cur.ent & 0xFFFFu);
+    }
+}
+
 template <int NB>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16)
 __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(TensorView t, GemmArgs g) {
     __shared__ __align__(16) uint4 patch[kWarps][4][32];
@@ -93,6 +195,7 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
     const int64_t items = T * S;
     constexpr int MP = 8 * NB;
     const uint32_t c28 = g.c28, one = g.one, c16 = g.c16;
+    uint8_t *pw = reinterpret_cast<uint8_t *>(patch[warp]);
     grid_dep_launch();
     bool dep_done = false;
 
@@ -104,23 +207,23 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
         const int64_t g_beg = (s * t.G) / S, g_end = ((s + 1) * t.G) / S;
         const int n0 = (int)(st * 16);  // rows < 2^30
         const int rowA = n0 + gid, rowB = n0 + gid + 8;
+        Stream<NB> w;
 
         // 1. weight stream first, so that its latency covers the set-up below
-        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg) * 64 + lane;
-        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg) * 32 + lane;
-        uint4 bh0[4], bh1[4], bl[4];
+        w.hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg) * 64 + lane;
+        w.lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg) * 32 + lane;
         if (g_beg < g_end) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                bh0[p] = ld_stream(hp + p * 64);
-                bh1[p] = ld_stream(hp + p * 64 + 32);
-                bl[p] = ld_stream(lp + p * 32);
+                w.bh0[p] = ld_stream(w.hp + p * 64);
+                w.bh1[p] = ld_stream(w.hp + p * 64 + 32);
+                w.bl[p] = ld_stream(w.lp + p * 32);
             }
         }
         // 2. bases, group offsets (lane l holds the offset of group gw0 + l),
         //    escapes of the first two groups
-        const uint32_t base2A = (rowA < t.N ? (uint32_t)__ldg(t.base + rowA) : 0u) * 0x00800080u;
-        const uint32_t base2B = (rowB < t.N ? (uint32_t)__ldg(t.base + rowB) : 0u) * 0x00800080u;
+        w.base2A = (rowA < t.N ? (uint32_t)__ldg(t.base + rowA) : 0u) * 0x00800080u;
+        w.base2B = (rowB < t.N ? (uint32_t)__ldg(t.base + rowB) : 0u) * 0x00800080u;
         const int32_t *gptr = t.esc_ptr + st * t.G;
         const int n_esc = (int)t.n_esc;  // offsets are int32
         int gw0 = (int)g_beg;
@@ -145,13 +248,13 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
             if (p1 < p0) p1 = p0;
         };
         int p0 = 0, p1 = 0;
-        EscBatch cur, nxt;
-        cur.cnt = nxt.cnt = 0;
-        cur.ent = nxt.ent = 0;
-        cur.p0 = nxt.p0 = 0;
+        EscBatch nxt;
+        w.cur.cnt = nxt.cnt = 0;
+        w.cur.ent = nxt.ent = 0;
+        w.cur.p0 = nxt.p0 = 0;
         if (g_beg < g_end) {
             group_bounds((int)g_beg, p0, p1);
-            cur = load_group_escapes(t, p0, p1, lane);
+            w.cur = load_group_escapes(t, p0, p1, lane);
         }
         if (g_beg + 1 < g_end) {
             group_bounds((int)g_beg + 1, p0, p1);
@@ -166,132 +269,46 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
         }
 
         // Activation rows of this lane (token m = 8*b + gid) at its 16 columns
-        // of a tile; B fragments are double-buffered one tile ahead.  Chunks
-        // that end inside K (only the last one of a ragged K) take the
-        // bounds-checked load.
-        const uint16_t *arow[NB];
-        bool mval[NB];
+        // of a tile; B fragments are double-buffered one tile ahead.  A chunk
+        // that ends inside K (only the last one of a ragged K) takes the
+        // bounds-checked loads on its last group.
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const int m = 8 * b + gid;
-            mval[b] = m < g.M;
-            arow[b] = g.A + (mval[b] ? (int64_t)m * g.lda : 0);
+            w.mval[b] = m < g.M;
+            w.ag[b] = g.A + (w.mval[b] ? (int64_t)m * g.lda : 0) + g_beg * 256 + 16 * q;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w.bw[0][b][j] = w.bw[1][b][j] = 0u;
+            w.acc[b][0] = w.acc[b][1] = w.acc[b][2] = w.acc[b][3] = 0.f;
         }
-        const bool kfull = 256 * g_end <= t.K;  // warp-uniform
-        uint32_t bw[2][NB][8];
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) bw[0][b][j] = bw[1][b][j] = 0u;
+        const bool ragged = 256 * g_end > t.K;  // the last group crosses K
         if (g_beg < g_end) {
 #pragma unroll
-            for (int b = 0; b < NB; ++b) load_act16(arow[b], g_beg * 256 + 16 * q, t.K, mval[b], bw[0][b]);
-        }
-        const uint16_t *ag[NB];  // arow + 256*gg + 16q
-#pragma unroll
-        for (int b = 0; b < NB; ++b) ag[b] = arow[b] + g_beg * 256 + 16 * q;
-
-        // This lane's escape of the current group (at most one while the
-        // group holds <= 32): its tile, its byte in the per-warp fragment
-        // copy (slot 4*(row%8)+col/16, component (pair&1)*2+row/8, half
-        // col&1), its bits.
-        uint8_t *pw = reinterpret_cast<uint8_t *>(patch[warp]);
-        uint32_t e_tile = 4, e_off = 0;
-        uint16_t e_val = 0;
-        auto own_escape = [&]() {
-            e_tile = 4;
-            if (lane < cur.cnt && cur.cnt <= 32) {
-                const uint32_t key = cur.ent >> 16;
-                const uint32_t r = (key >> 6) & 15, j = key & 63;
-                const uint32_t slot = (r & 7) * 4 + (j >> 4), j16 = j & 15, pr = j16 >> 1;
-                const uint32_t comp = (pr & 1) * 2 + (r >> 3);
-                e_tile = key >> 10;
-                e_off = ((pr >> 1) * 32 + slot) * 16 + comp * 4 + (j16 & 1) * 2;
-                e_val = (uint16_t)(cur.ent & 0xFFFFu);
-            }
-        };
-        uint32_t emask = 0u;
-        if (g_beg < g_end) {
-            emask = escape_tiles(cur, lane);
-            own_escape();
+            for (int b = 0; b < NB; ++b)
+                load_act16(w.ag[b] - (g_beg * 256 + 16 * q), g_beg * 256 + 16 * q, t.K, w.mval[b], w.bw[0][b]);
+            own_escape(w, lane);
         }
 
-        float acc[NB][4];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
-
+        const int64_t g_fast = ragged ? g_end - 1 : g_end;
         for (int64_t gg = g_beg; gg < g_end; ++gg) {
             const bool more = gg + 1 < g_end;
+            if (gg < g_fast)
+                group_step<NB, false>(w, t, g, gg, more, patch[warp], pw, lane, q, c28, one, c16);
+            else
+                group_step<NB, true>(w, t, g, gg, more, patch[warp], pw, lane, q, c28, one, c16);
+            w.hp += 256;
+            w.lp += 128;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {  // tile p of group gg
-                uint32_t dA[8], dB[8];
-                decode16_fma(bh0[p], bl[p].x, bl[p].y, base2A, c28, one, c16, dA);
-                decode16_fma(bh1[p], bl[p].z, bl[p].w, base2B, c28, one, c16, dB);
-                if (more) {  // the same tile of the next group
-                    bh0[p] = ld_stream(hp + 256 + p * 64);
-                    bh1[p] = ld_stream(hp + 256 + p * 64 + 32);
-                    bl[p] = ld_stream(lp + 128 + p * 32);
-                }
-                if (p < 3 || more) {  // activations of the next tile
-                    if (kfull) {
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) load_act16_inside(ag[b] + (p + 1) * 64, mval[b], bw[(p + 1) & 1][b]);
-                    } else {
-#pragma unroll
-                        for (int b = 0; b < NB; ++b)
-                            load_act16(arow[b], gg * 256 + (p + 1) * 64 + 16 * q, t.K, mval[b], bw[(p + 1) & 1][b]);
-                    }
-                }
-
-                // Escapes of this tile replace the decoded placeholders.
-                if ((emask >> p) & 1u) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        patch[warp][i][lane] = make_uint4(dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1]);
-                    __syncwarp();
-                    if (cur.cnt <= 32) {
-                        if (e_tile == (uint32_t)p) *reinterpret_cast<uint16_t *>(pw + e_off) = e_val;
-                    } else {  // more than 32 escapes in the group: walk it in batches
-                        for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
-                            const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
-                            if (b0 + lane < cur.cnt && (int)(e >> 26) == p) patch_one(patch[warp], e);
-                        }
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 v = patch[warp][i][lane];
-                        dA[2 * i] = v.x;
-                        dB[2 * i] = v.y;
-                        dA[2 * i + 1] = v.z;
-                        dB[2 * i + 1] = v.w;
-                    }
-                    __syncwarp();
-                }
-
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                    for (int b = 0; b < NB; ++b)
-                        mma16816(acc[b], dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1], bw[p & 1][b][2 * i],
-                                 bw[p & 1][b][2 * i + 1]);
-                }
-            }
-            hp += 256;
-            lp += 128;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) ag[b] += 256;
+            for (int b = 0; b < NB; ++b) w.ag[b] += 256;
             // the next group's escapes are already in flight; fetch the one after
-            cur = nxt;
-            if (more) {
-                emask = escape_tiles(cur, lane);
-                own_escape();
-            }
+            w.cur = nxt;
+            if (more) own_escape(w, lane);
             if (gg + 2 < g_end) {
                 group_bounds((int)gg + 2, p0, p1);
                 nxt = load_group_escapes(t, p0, p1, lane);
             }
         }
+        float (&acc)[NB][4] = w.acc;
 
         // Epilogue.  acc[b] = {(rowA, m0), (rowA, m0+1), (rowB, m0), (rowB, m0+1)}, m0 = 8b + 2q.
         if (S == 1) {
