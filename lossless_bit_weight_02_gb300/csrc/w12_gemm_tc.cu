@@ -37,9 +37,9 @@
 namespace w12 {
 namespace {
 
-constexpr int kDecWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;  // the warp after the producer issues the MMAs
+constexpr int kDecWarps = 16;     // two per 16-row stripe (even / odd tiles of each group)
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;      // the warp after the producer issues the MMAs
 constexpr int kThreads = 32 * (kDecWarps + 2);
 constexpr uint32_t kAStageBytes = 128 * 128;  // 128 rows x 64 BF16
 constexpr long long kWaitPolls = 1LL << 20;    // each poll is a try_wait (which may itself block)
@@ -165,7 +165,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < R; ++i) {
-            mbar_init(&full_a[i], kDecWarps * 32);
+            mbar_init(&full_a[i], (kDecWarps / 2) * 32);  // the 8 warps of one tile parity
             mbar_init(&full_b[i], 1);
             mbar_init(&empty[i], 1);
         }
@@ -187,17 +187,19 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
 
     if (warp < kDecWarps) {
         // ------------------------------------------------------------------
-        // Decoders: stripe st = 8*tt + warp.
+        // Decoders: warp w handles stripe st = 8*tt + (w%8) and the tiles
+        // p = w/8 and w/8 + 2 of every group.
         // ------------------------------------------------------------------
         const int gid = lane >> 2, q = lane & 3;
+        const int sw = warp & 7, par = warp >> 3;
         const int64_t T = t.Np / 16;
-        const int64_t st = tt * 8 + warp;
+        const int64_t st = tt * 8 + sw;
         const bool live = st < T;  // warp-uniform
-        const int rA = 16 * warp + gid, rB = rA + 8;
+        const int rA = 16 * sw + gid, rB = rA + 8;
         const uint32_t c28 = g.c28, one = g.one, c16 = g.c16;
-        uint4 bh0[4], bh1[4], bl[4];
-        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg) * 64 + lane;
-        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg) * 32 + lane;
+        uint4 bh0[2], bh1[2], bl[2];
+        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg + par) * 64 + lane;
+        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg + par) * 32 + lane;
         uint32_t base2A = 0, base2B = 0;
         EscBatch cur, nxt;
         cur.cnt = nxt.cnt = 0;
@@ -205,25 +207,36 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         cur.p0 = nxt.p0 = 0;
         const int32_t *gptr = t.esc_ptr + (live ? st : 0) * t.G;
         const int n_esc = (int)t.n_esc;
-        auto bounds = [&](int64_t gg, int &p0, int &p1) {  // offsets of group gg (two broadcast loads)
-            int a = 0, b = 0;
-            if (lane == 0) {
-                a = __ldg(gptr + gg);
-                b = __ldg(gptr + gg + 1);
+        // group offsets: lane l holds the offset of group gw0 + l (one
+        // coalesced load per 31 groups, no dependent load inside the loop)
+        int gw0 = (int)g_beg;
+        const int gend = (int)g_end;
+        auto load_window = [&](int first) -> int {
+            const int gi = first + lane;
+            int v = 0;
+            if (live && gi <= gend) {
+                v = __ldg(gptr + gi);
+                v = v < 0 ? 0 : (v > n_esc ? n_esc : v);
             }
-            a = __shfl_sync(kFull, a, 0);
-            b = __shfl_sync(kFull, b, 0);
-            a = a < 0 ? 0 : (a > n_esc ? n_esc : a);
-            b = b < a ? a : (b > n_esc ? n_esc : b);
-            p0 = a;
-            p1 = b;
+            return v;
+        };
+        int ptrw = load_window(gw0);
+        auto bounds = [&](int64_t gg64, int &p0, int &p1) {
+            const int gg = (int)gg64;
+            if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per chunk)
+                gw0 = gg;
+                ptrw = load_window(gw0);
+            }
+            p0 = __shfl_sync(kFull, ptrw, gg - gw0);
+            p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
+            if (p1 < p0) p1 = p0;
         };
         if (live && nkb > 0) {
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                bh0[p] = ld_stream(hp + p * 64);
-                bh1[p] = ld_stream(hp + p * 64 + 32);
-                bl[p] = ld_stream(lp + p * 32);
+            for (int i = 0; i < 2; ++i) {
+                bh0[i] = ld_stream(hp + i * 128);
+                bh1[i] = ld_stream(hp + i * 128 + 32);
+                bl[i] = ld_stream(lp + i * 64);
             }
             const int64_t nA = st * 16 + gid, nB = nA + 8;
             base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
@@ -242,18 +255,19 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         for (int64_t gg = g_beg; gg < g_end && ok; ++gg) {
             const bool more = gg + 1 < g_end;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
+            for (int i = 0; i < 2; ++i) {
+                const int p = par + 2 * i;  // tile of the group
                 const int kb = (int)(4 * (gg - g_beg)) + p;
                 const int stage = kb % R;
                 const uint32_t ph = (uint32_t)((kb / R) & 1);
                 uint32_t dA[8], dB[8];
                 if (live) {
-                    decode16_fma(bh0[p], bl[p].x, bl[p].y, base2A, c28, one, c16, dA);
-                    decode16_fma(bh1[p], bl[p].z, bl[p].w, base2B, c28, one, c16, dB);
+                    decode16_fma(bh0[i], bl[i].x, bl[i].y, base2A, c28, one, c16, dA);
+                    decode16_fma(bh1[i], bl[i].z, bl[i].w, base2B, c28, one, c16, dB);
                     if (more) {
-                        bh0[p] = ld_stream(hp + 256 + p * 64);
-                        bh1[p] = ld_stream(hp + 256 + p * 64 + 32);
-                        bl[p] = ld_stream(lp + 128 + p * 32);
+                        bh0[i] = ld_stream(hp + 256 + i * 128);
+                        bh1[i] = ld_stream(hp + 256 + i * 128 + 32);
+                        bl[i] = ld_stream(lp + 128 + i * 64);
                     }
                 }
                 // the whole warp leaves together, so no lane is left behind at
@@ -272,7 +286,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
                         __syncwarp();
                         auto put = [&](uint32_t e) {
                             const int key = (int)(e >> 16);
-                            const int r = 16 * warp + ((key >> 6) & 15), j = key & 63;
+                            const int r = 16 * sw + ((key >> 6) & 15), j = key & 63;
                             *reinterpret_cast<uint16_t *>(A + swz(r, j >> 3) + (j & 7) * 2) = (uint16_t)(e & 0xFFFFu);
                         };
                         if (cur.cnt <= 32) {
@@ -302,17 +316,17 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         }
 
         // ------------------------------------------------------------------
-        // Epilogue: TMEM lanes 32*(warp%4).. ; warps w and w+4 split the
-        // 16-column chunks.
+        // Epilogue: TMEM lanes 32*(warp%4).. ; the four warps w, w+4, w+8,
+        // w+12 split the 16-column chunks.
         // ------------------------------------------------------------------
         const bool fin = __all_sync(kFull, mbar_wait(done, 0, abort_flag, g.error));
         tc_fence_after();
-        const int quarter = warp & 3, half = warp >> 2;
+        const int quarter = warp & 3, half = warp >> 2;  // half: 0..3
         const int64_t n = tt * 128 + 32 * quarter + lane;
         const int chunks = Mp / 16;
         const bool have = __all_sync(kFull, fin && ok && !*abort_flag);
         if (have) {
-            for (int c = half; c < chunks; c += 2) {
+            for (int c = half; c < chunks; c += 4) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(16 * c), v);
                 if (nkb == 0) {
@@ -343,7 +357,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
             if (*last_flag) {
                 __threadfence();
                 if (n < t.N) {
-                    for (int c = half; c < chunks; c += 2) {
+                    for (int c = half; c < chunks; c += 4) {
                         for (int j = 0; j < 16; ++j) {
                             const int m = 16 * c + j;
                             if (m >= g.M) break;
@@ -423,10 +437,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-int tc_stages(int Mp) {
+int tc_stages(int Mp) {  // one CTA per SM: up to ~200 KB of stages
     const int stage = (int)kAStageBytes + Mp * 128;
-    int r = (100 * 1024) / stage;
-    return r < 2 ? 2 : (r > 4 ? 4 : r);
+    int r = (200 * 1024) / stage;
+    return r < 2 ? 2 : (r > 6 ? 6 : r);
 }
 
 size_t tc_smem_bytes(int Mp, int R) {
@@ -437,13 +451,13 @@ size_t tc_smem_bytes(int Mp, int R) {
 
 int64_t gemm_tc_pad(int64_t M) { return (M + 15) / 16 * 16; }
 
-// Split from (M, N, K) only: about two CTAs per SM on 152 SMs, no more chunks
+// Split from (M, N, K) only: about one CTA per SM on 152 SMs, no more chunks
 // than column groups, and few enough that the FP32 partial traffic
 // (2*S*Mpad*N*4 bytes) stays small next to the weights (1.5*N*K bytes).
 int gemm_tc_split(int64_t M, int64_t N, int64_t K) {
     const int64_t T = (N + 127) / 128, G = groups_of(K), Mp = gemm_tc_pad(M);
     if (T == 0 || G == 0) return 1;
-    int64_t S = (2 * 152) / T;
+    int64_t S = 152 / T;
     const int64_t traffic_cap = (int64_t)(0.0375 * (double)K / (double)Mp);
     if (S > traffic_cap) S = traffic_cap;
     if (S > G) S = G;
