@@ -306,6 +306,85 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
+    # ---- codec throughput on the config-1 layer (rows a1-a5): encode, decode, verify ----
+    codec = {}
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    enc_ms = dec_ms = ver_ms = 0.0
+    enc_bytes = dec_bytes = ver_bytes = 0
+    for i, (name, N, K) in enumerate(synth.LAYER_SHAPES):
+        Wd = synth.dense_weights_device(N, K, seed=1000 + i, device=dev)
+        w12.w12_encode(Wd)  # warm
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        t = w12.w12_encode(Wd)
+        torch.cuda.synchronize()
+        enc_ms += (time.perf_counter() - t0) * 1e3  # includes the one host sync for the escape count
+        enc_bytes += 2 * 2 * N * K + t.nbytes()  # W read twice (window, pack) + W12 written
+        out = torch.empty_like(Wd)
+        a, b = ev(), ev()
+        a.record(stream)
+        w12.w12_decode(t, out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        dec_ms += a.elapsed_time(b)
+        dec_bytes += t.nbytes() + 2 * N * K
+        t0 = time.perf_counter()
+        st, nm = w12.w12_verify_roundtrip(Wd, t)
+        ver_ms += (time.perf_counter() - t0) * 1e3
+        ver_bytes += t.nbytes() + 2 * N * K
+        assert st == w12.W12_OK
+        del Wd, out
+    codec = {"encode_gbs": round(enc_bytes / (enc_ms * 1e-3) / 1e9, 1),
+             "decode_gbs": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
+             "verify_gbs": round(ver_bytes / (ver_ms * 1e-3) / 1e9, 1),
+             "note": "algorithmic bytes / time over the four layer tensors; encode and verify are "
+                     "host-synchronous calls timed on the host clock"}
+    torch.cuda.empty_cache()
+
+    # ---- 64-layer stack (config 3): convert + load-time check, then stream ----
+    stack = None
+    if not args.no_stack:
+        t_conv = time.perf_counter()
+        stk = []
+        for layer in range(64):
+            for i, (name, N, K) in enumerate(synth.LAYER_SHAPES):
+                Wd = synth.dense_weights_device(N, K, seed=3000 + 16 * layer + i, device=dev)
+                t = w12.w12_encode(Wd)
+                st, nm = w12.w12_verify_roundtrip(Wd, t)
+                assert st == w12.W12_OK, (layer, name, st, nm)
+                del Wd
+                stk.append(t)
+        torch.cuda.synchronize()
+        conv_s = time.perf_counter() - t_conv
+        torch.cuda.empty_cache()
+        sb = sum(t.nbytes() for t in stk)
+        nw = sum(t.N * t.K for t in stk)
+        stack = {"layers": 64, "tensors": len(stk), "w12_gb": round(sb / 1e9, 3), "bf16_gb": round(2 * nw / 1e9, 3),
+                 "bits_per_weight": round(8 * sb / nw, 4),
+                 "convert_and_verify_s": round(conv_s, 2)}
+        for M in (1, 16):
+            acts_s = {K: synth.activations_device(M, K, seed=M * 100 + K, device=dev) for _, _, K in synth.LAYER_SHAPES}
+            outs_s = {N: torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _, N, _ in synth.LAYER_SHAPES}
+            wsp.ensure(max(w12.w12_gemm_workspace_bytes(M, t.N, t.K) for t in stk[:4]))
+            cs = [w12.GemmCall(acts_s[t.K], t, outs_s[t.N], wsp, stream=stream, opts=overlap) for t in stk]
+            for c in cs:
+                c()
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            reps = 5
+            a.record(stream)
+            for _ in range(reps):
+                for c in cs:
+                    c()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / reps
+            stack[f"m{M}"] = {"pass_ms": round(ms, 3), "weight_gbs": round(sb / (ms * 1e-3) / 1e9, 1),
+                              "roofline_frac": round(sum(algorithmic_bytes(t, M) for t in stk) / (ms * 1e-3) / 1e9
+                                                     / hbm_peak, 4)}
+        del stk
+        torch.cuda.empty_cache()
+
     value = step_bytes * args.steps * ws_n / (total_ms * 1e-3) / 1e9
     e2e_val = step_bytes * e2e_steps * ws_n / (e2e_ms * 1e-3) / 1e9
     top_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers) / launches_per_step
@@ -326,7 +405,7 @@ def run_gpu(args):
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)"},
-        "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep,
+        "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -470,6 +549,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack measurement")
     ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down)")
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--iters", type=int, default=5)
