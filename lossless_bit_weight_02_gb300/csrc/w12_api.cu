@@ -225,7 +225,6 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     g.counters = reinterpret_cast<int32_t *>(ws + pl.counters_off);
     g.partials = reinterpret_cast<float *>(ws + pl.partials_off);
     g.c28 = 1u << 28;
-    g.one = 1u;
     g.c16 = 16u;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.path == W12_PATH_TC) {

@@ -9,12 +9,17 @@
 //     loads of the hi plane and one of the lo plane - the tile layout puts
 //     exactly the lane's tensor-core A fragment (rows g and g+8, 16 columns
 //     each) behind those loads, so a warp reads 1.5 KB contiguous per tile.
-//   * Records are decoded to BF16 pairs with ~2.6 integer ops per weight
-//     (prmt / shift / and / add / select), escapes of the tile are patched in
-//     (through a 2 KB per-warp shared-memory copy of the fragment, only for
-//     tiles that hold an escape), then four mma.sync.m16n8k16 per 8 tokens
-//     accumulate in FP32.  The 64 columns of a tile are fed to the four MMAs
-//     in a fixed permuted order; activations use the same permutation.
+//   * Records are decoded to BF16 pairs with two integer ops per weight
+//     (prmt / and / multiply-add-high / select per pair), escapes of the
+//     tile are patched in (through a 2 KB per-warp shared-memory copy of the
+//     fragment, only for tiles that hold an escape), then four
+//     mma.sync.m16n8k16 per 8 tokens accumulate in FP32.  The 64 columns of
+//     a tile are fed to the four MMAs in a fixed permuted order; activations
+//     use the same permutation.
+//   * Activations: every warp copies the next group's 256 columns of the
+//     token rows into its own shared-memory buffer with cp.async while it
+//     works on the current group, so the B fragments come from shared memory
+//     (the warps of an SM would otherwise all wait on the same L2 lines).
 //   * Fixed-order reduction: chunk partials start from zero; when S > 1 they
 //     go to an FP32 workspace and the last warp to finish a stripe sums them
 //     in the order s = 0..S-1 and writes BF16.  S depends on (M, N, K) only,
@@ -39,37 +44,45 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 16 activations A[m, k .. k+15] as 8 BF16 pairs.  Lanes whose token does
-// not exist (pred false) load nothing and keep their registers (zero).
-__device__ __forceinline__ void load_act16(const uint16_t *__restrict__ row, int64_t k, int64_t K, bool valid,
-                                           uint32_t w[8]) {
-    const bool full = k + 16 <= K;
-    const uint16_t *p = row + k;
-    asm volatile(
-        "{\n.reg .pred pp;\nsetp.ne.u32 pp, %8, 0;\n"
-        "@pp ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%9];\n"
-        "@pp ld.global.nc.v4.u32 {%4,%5,%6,%7}, [%10];\n}"
-        : "+r"(w[0]), "+r"(w[1]), "+r"(w[2]), "+r"(w[3]), "+r"(w[4]), "+r"(w[5]), "+r"(w[6]), "+r"(w[7])
-        : "r"((uint32_t)(valid && full)), "l"(p), "l"(p + 8));
-    if (valid && !full) {  // the ragged end of K (last tile only)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t lo = (k + 2 * j < K) ? row[k + 2 * j] : 0u;
-            const uint32_t hi = (k + 2 * j + 1 < K) ? row[k + 2 * j + 1] : 0u;
-            w[j] = lo | (hi << 16);
-        }
-    }
+// Activations are staged in shared memory a whole 256-column group ahead:
+// each warp owns two buffers of 8*NB token rows x kActPitch BF16 (the 8
+// padding columns put the rows of one 8-lane phase on different banks, so
+// the fragment reads below are conflict-free).
+constexpr int kActPitch = 264;
+
+template <int NB>
+__host__ __device__ constexpr uint32_t act_buf_bytes() {
+    return 8 * NB * kActPitch * 2;
+}
+template <int NB>
+__host__ __device__ constexpr int smem_bytes() {
+    return kWarps * (4 * 32 * 16 + 2 * act_buf_bytes<NB>());
 }
 
-// The same 16 activations when the tile lies inside K (no bounds checks).
-__device__ __forceinline__ void load_act16_inside(const uint16_t *__restrict__ p, bool valid, uint32_t w[8]) {
-    asm volatile(
-        "{\n.reg .pred pp;\nsetp.ne.u32 pp, %8, 0;\n"
-        "@pp ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%9];\n"
-        "@pp ld.global.nc.v4.u32 {%4,%5,%6,%7}, [%9+16];\n}"
-        : "+r"(w[0]), "+r"(w[1]), "+r"(w[2]), "+r"(w[3]), "+r"(w[4]), "+r"(w[5]), "+r"(w[6]), "+r"(w[7])
-        : "r"((uint32_t)valid), "l"(p));
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Copies columns 256*gg .. 256*gg+255 of the first `rows` token rows of A into
+// the buffer at shared address `dst`: lane l takes columns 8l .. 8l+7 of each
+// row (16 bytes; A rows are 16-byte aligned).  Columns at or beyond K read as
+// zero.
+template <int NB>
+__device__ __forceinline__ void stage_group(uint32_t dst, const uint16_t *__restrict__ A, int64_t lda, int rows,
+                                            int64_t gg, int64_t K, int lane) {
+    const int64_t col = gg * 256 + 8 * lane;
+    const int64_t rem = K - col;
+    const uint32_t bytes = rem >= 8 ? 16u : (rem > 0 ? (uint32_t)rem * 2u : 0u);
+    const uint16_t *src = bytes ? A + col : A;
+    const int64_t step = bytes ? lda : 0;
+#pragma unroll
+    for (int i = 0; i < 8 * NB; ++i)
+        if (i < rows) cp_async16(dst + (uint32_t)(i * kActPitch + 8 * lane) * 2u, src + i * step, bytes);
+    cp_async_commit();
+}
+
 
 // Writes escape `ent` (key<<16 | bits) into the per-warp copy of the A
 // fragments: slot = 4*(row%8) + col/16, component (pair&1)*2 + row/8,
@@ -89,9 +102,6 @@ struct Stream {
     uint4 bh0[4], bh1[4], bl[4];  // the 4 tiles of the current group (prefetched)
     const uint4 *hp, *lp;         // hi / lo planes at the current group, this lane
     uint32_t base2A, base2B;      // row bases * 0x00800080 (rows g, g+8)
-    const uint16_t *ag[NB];       // activation row + 256*group + 16q
-    bool mval[NB];                // token exists
-    uint32_t bw[2][NB][8];        // B fragments, double-buffered a tile ahead
     float acc[NB][4];
     EscBatch cur;                 // escapes of the current group
     uint32_t emask;               // tiles of the group holding an escape
@@ -99,35 +109,39 @@ struct Stream {
     uint16_t e_val;
 };
 
-// One 256-column group: for each of its 4 tiles decode the two rows, prefetch
-// the same tile of the next group (or, on the last group, the same tile again:
-// an L2 hit), load the next tile's activations, patch the tile's escapes and
-// run the MMAs.  GUARD selects bounds-checked activation loads (a chunk that
-// ends inside K).
-template <int NB, bool GUARD>
+// One 256-column group: stage the next group's activations, then for each of
+// the 4 tiles read the B fragments from shared memory, decode the two rows,
+// prefetch the same tile of the next group (or, on the last group, the same
+// tile again: an L2 hit), patch the tile's escapes and run the MMAs.
+template <int NB>
 __device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, const GemmArgs &g, int64_t gg,
-                                           bool more, uint4 (*patch)[32], uint8_t *pw, int lane, int q,
-                                           uint32_t c28, uint32_t one, uint32_t c16) {
+                                           bool more, uint4 (*patch)[32], uint8_t *pw, int lane, int rows,
+                                           uint32_t act, const unsigned char *actp, uint32_t frag, uint32_t c28,
+                                           uint32_t c16) {
+    // This lane's copies of group gg have landed; after the warp barrier so
+    // have every lane's, and every lane is done reading the other buffer.
+    cp_async_wait_all();
+    __syncwarp();
+    if (more) stage_group<NB>(act + (uint32_t)((gg + 1) & 1) * act_buf_bytes<NB>(), g.A, g.lda, rows, gg + 1, t.K, lane);
+    const unsigned char *ab = actp + (gg & 1) * act_buf_bytes<NB>() + frag;
     const int next = more ? 256 : 0;    // uint4 offset of the next group's hi tiles
     const int nextl = more ? 128 : 0;   // ... and lo tiles
-    const int nexta = more ? 256 : 192;  // activation offset of the tile after the last one
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
+        uint32_t bw[NB][8];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const uint4 *a = reinterpret_cast<const uint4 *>(ab + (8 * b * kActPitch + 64 * p) * 2);
+            const uint4 v0 = a[0], v1 = a[1];
+            bw[b][0] = v0.x; bw[b][1] = v0.y; bw[b][2] = v0.z; bw[b][3] = v0.w;
+            bw[b][4] = v1.x; bw[b][5] = v1.y; bw[b][6] = v1.z; bw[b][7] = v1.w;
+        }
         uint32_t dA[8], dB[8];
-        decode16_fma(w.bh0[p], w.bl[p].x, w.bl[p].y, w.base2A, c28, one, c16, dA);
-        decode16_fma(w.bh1[p], w.bl[p].z, w.bl[p].w, w.base2B, c28, one, c16, dB);
+        decode16_fma(w.bh0[p], w.bl[p].x, w.bl[p].y, w.base2A, c28, c16, dA);
+        decode16_fma(w.bh1[p], w.bl[p].z, w.bl[p].w, w.base2B, c28, c16, dB);
         w.bh0[p] = ld_stream(w.hp + next + p * 64);
         w.bh1[p] = ld_stream(w.hp + next + p * 64 + 32);
         w.bl[p] = ld_stream(w.lp + nextl + p * 32);
-        const int an = (p < 3) ? (p + 1) * 64 : nexta;  // next tile's activations
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            if (GUARD)  // row = ag - 256*gg - 16q, column 256*gg + an + 16q
-                load_act16(w.ag[b] - (gg * 256 + 16 * q), gg * 256 + an + 16 * q, t.K, w.mval[b],
-                           w.bw[(p + 1) & 1][b]);
-            else
-                load_act16_inside(w.ag[b] + an, w.mval[b], w.bw[(p + 1) & 1][b]);
-        }
 
         // Escapes of this tile replace the decoded placeholders.
         if ((w.emask >> p) & 1u) {
@@ -161,8 +175,8 @@ __device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, c
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int b = 0; b < NB; ++b)
-                mma16816(w.acc[b], dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1], w.bw[p & 1][b][2 * i],
-                         w.bw[p & 1][b][2 * i + 1]);
+                mma16816(w.acc[b], dA[2 * i], dB[2 * i], dA[2 * i + 1], dB[2 * i + 1], bw[b][2 * i],
+                         bw[b][2 * i + 1]);
         }
     }
 }
@@ -187,15 +201,22 @@ __device__ __forceinline__ void own_escape(Stream<NB> &w, int lane) {
 
 template <int NB>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16)
 __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(TensorView t, GemmArgs g) {
-    __shared__ __align__(16) uint4 patch[kWarps][4][32];
+    // [kWarps][4][32] uint4 escape-patch copies, then [kWarps][2][8*NB][kActPitch] activations
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint4 (*patch)[4][32] = reinterpret_cast<uint4 (*)[4][32]>(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, q = lane & 3;
     const int S = g.split;
     const int64_t T = t.Np / 16;
     const int64_t items = T * S;
     constexpr int MP = 8 * NB;
-    const uint32_t c28 = g.c28, one = g.one, c16 = g.c16;
+    const uint32_t c28 = g.c28, c16 = g.c16;
     uint8_t *pw = reinterpret_cast<uint8_t *>(patch[warp]);
+    const int rows = g.M < MP ? (int)g.M : MP;  // staged token rows
+    // this warp's two activation buffers, and this lane's fragment in a buffer
+    const unsigned char *actp = smem + kWarps * 2048 + warp * 2 * act_buf_bytes<NB>();
+    const uint32_t act = (uint32_t)__cvta_generic_to_shared(actp);
+    const uint32_t frag = (uint32_t)(gid * kActPitch + 16 * q) * 2u;
     grid_dep_launch();
     bool dep_done = false;
 
@@ -268,38 +289,22 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
             dep_done = true;
         }
 
-        // Activation rows of this lane (token m = 8*b + gid) at its 16 columns
-        // of a tile; B fragments are double-buffered one tile ahead.  A chunk
-        // that ends inside K (only the last one of a ragged K) takes the
-        // bounds-checked loads on its last group.
+        // Token rows beyond M are never staged: whatever their buffer rows
+        // hold only reaches accumulator columns that are never stored.
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int m = 8 * b + gid;
-            w.mval[b] = m < g.M;
-            w.ag[b] = g.A + (w.mval[b] ? (int64_t)m * g.lda : 0) + g_beg * 256 + 16 * q;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) w.bw[0][b][j] = w.bw[1][b][j] = 0u;
-            w.acc[b][0] = w.acc[b][1] = w.acc[b][2] = w.acc[b][3] = 0.f;
-        }
-        const bool ragged = 256 * g_end > t.K;  // the last group crosses K
+        for (int b = 0; b < NB; ++b) w.acc[b][0] = w.acc[b][1] = w.acc[b][2] = w.acc[b][3] = 0.f;
         if (g_beg < g_end) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                load_act16(w.ag[b] - (g_beg * 256 + 16 * q), g_beg * 256 + 16 * q, t.K, w.mval[b], w.bw[0][b]);
+            // every lane is done with the buffers of this warp's previous item
+            __syncwarp();
+            stage_group<NB>(act + (uint32_t)(g_beg & 1) * act_buf_bytes<NB>(), g.A, g.lda, rows, g_beg, t.K, lane);
             own_escape(w, lane);
         }
 
-        const int64_t g_fast = ragged ? g_end - 1 : g_end;
         for (int64_t gg = g_beg; gg < g_end; ++gg) {
             const bool more = gg + 1 < g_end;
-            if (gg < g_fast)
-                group_step<NB, false>(w, t, g, gg, more, patch[warp], pw, lane, q, c28, one, c16);
-            else
-                group_step<NB, true>(w, t, g, gg, more, patch[warp], pw, lane, q, c28, one, c16);
+            group_step<NB>(w, t, g, gg, more, patch[warp], pw, lane, rows, act, actp, frag, c28, c16);
             w.hp += 256;
             w.lp += 128;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) w.ag[b] += 256;
             // the next group's escapes are already in flight; fetch the one after
             w.cur = nxt;
             if (more) own_escape(w, lane);
@@ -388,7 +393,9 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
     }
     if (lc.occ[NB] == 0) {
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_gemm_mma<NB>, kWarps * 32, 0);
+        e = cudaFuncSetAttribute(k_gemm_mma<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NB>());
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_gemm_mma<NB>, kWarps * 32, smem_bytes<NB>());
         if (e != cudaSuccess) return e;
         lc.occ[NB] = occ > 0 ? occ : 1;
     }
@@ -401,6 +408,7 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem_bytes<NB>();
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

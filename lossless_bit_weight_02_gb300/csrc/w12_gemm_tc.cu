@@ -196,7 +196,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         const int64_t st = tt * 8 + sw;
         const bool live = st < T;  // warp-uniform
         const int rA = 16 * sw + gid, rB = rA + 8;
-        const uint32_t c28 = g.c28, one = g.one, c16 = g.c16;
+        const uint32_t c28 = g.c28, c16 = g.c16;
         uint4 bh0[2], bh1[2], bl[2];
         const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg + par) * 64 + lane;
         const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg + par) * 32 + lane;
@@ -262,8 +262,8 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
                 const uint32_t ph = (uint32_t)((kb / R) & 1);
                 uint32_t dA[8], dB[8];
                 if (live) {
-                    decode16_fma(bh0[i], bl[i].x, bl[i].y, base2A, c28, one, c16, dA);
-                    decode16_fma(bh1[i], bl[i].z, bl[i].w, base2B, c28, one, c16, dB);
+                    decode16_fma(bh0[i], bl[i].x, bl[i].y, base2A, c28, c16, dA);
+                    decode16_fma(bh1[i], bl[i].z, bl[i].w, base2B, c28, c16, dB);
                     if (more) {
                         bh0[i] = ld_stream(hp + 256 + i * 128);
                         bh1[i] = ld_stream(hp + 256 + i * 128 + 32);

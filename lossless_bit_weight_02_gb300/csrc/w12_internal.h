@@ -57,7 +57,7 @@ struct GemmArgs {
     float *partials;     // [S][Np][MP] fp32 (S > 1)
     int32_t *counters;   // [Np/16] arrival counters (S > 1)
     int32_t *error;      // device error word
-    uint32_t c28, one, c16;  // 1<<28, 1, 16: multiplicands the decoder needs at run time
+    uint32_t c28, c16;  // 1<<28, 16: multiplicands the decoder needs at run time
 };
 
 // Tensor-core path: tcgen05.mma with TMEM accumulators (M <= 256; partials

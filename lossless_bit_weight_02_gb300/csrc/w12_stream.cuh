@@ -27,28 +27,32 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return r;
 }
 
-// Record-pair decode (as decode_pair in w12_device.cuh) with the right shift
-// done as a high multiply and the base added with a multiply-add, so that two
-// of the five operations run on the FMA pipe instead of the ALU.  c28 = 2^28
-// and one = 1 arrive as kernel arguments so that they stay multiplications.
-__device__ __forceinline__ uint32_t decode_pair_fma(uint32_t Z, uint32_t base2, uint32_t c28, uint32_t one) {
-    const uint32_t t = __umulhi(Z, c28) & 0x07FF07FFu;  // (Z >> 4) & mask
+// Record-pair decode (same result as decode_pair in w12_device.cuh) in four
+// operations, one of them on the FMA pipe: with Z holding the two records in
+// bits 4..15 and 20..31 (sign on top of each half, the neighbouring nibble
+// below), clear the signs and the neighbour nibbles, then one multiply-add
+// high does "shift right by 4, add base << 7" for both halves at once (no
+// carry crosses a half: (base + offset) << 7 | m < 2^16 for any base byte,
+// and bit 15 stays clear for the encoder's bases, which are at most 239),
+// and the signs go back in.
+// c28 = 2^28 arrives as a kernel argument so that it stays a multiplication.
+__device__ __forceinline__ uint32_t decode_pair_fma(uint32_t Z, uint32_t base2, uint32_t c28) {
     uint32_t u;
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(u) : "r"(t), "r"(one), "r"(base2));
-    return (Z & 0x80008000u) | (u & 0x7FFF7FFFu);
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(u) : "r"(Z & 0x7FF07FF0u), "r"(c28), "r"(base2));
+    return (Z & 0x80008000u) | u;
 }
 
 __device__ __forceinline__ void decode16_fma(uint4 h, uint32_t l0, uint32_t l1, uint32_t base2, uint32_t c28,
-                                             uint32_t one, uint32_t c16, uint32_t out[8]) {
+                                             uint32_t c16, uint32_t out[8]) {
     const uint32_t l0s = l0 * c16, l1s = l1 * c16;  // << 4, on the FMA pipe
-    out[0] = decode_pair_fma(prmt(h.x, l0, 0x1504), base2, c28, one);
-    out[1] = decode_pair_fma(prmt(h.x, l0, 0x3726), base2, c28, one);
-    out[2] = decode_pair_fma(prmt(h.y, l0s, 0x1504), base2, c28, one);
-    out[3] = decode_pair_fma(prmt(h.y, l0s, 0x3726), base2, c28, one);
-    out[4] = decode_pair_fma(prmt(h.z, l1, 0x1504), base2, c28, one);
-    out[5] = decode_pair_fma(prmt(h.z, l1, 0x3726), base2, c28, one);
-    out[6] = decode_pair_fma(prmt(h.w, l1s, 0x1504), base2, c28, one);
-    out[7] = decode_pair_fma(prmt(h.w, l1s, 0x3726), base2, c28, one);
+    out[0] = decode_pair_fma(prmt(h.x, l0, 0x1504), base2, c28);
+    out[1] = decode_pair_fma(prmt(h.x, l0, 0x3726), base2, c28);
+    out[2] = decode_pair_fma(prmt(h.y, l0s, 0x1504), base2, c28);
+    out[3] = decode_pair_fma(prmt(h.y, l0s, 0x3726), base2, c28);
+    out[4] = decode_pair_fma(prmt(h.z, l1, 0x1504), base2, c28);
+    out[5] = decode_pair_fma(prmt(h.z, l1, 0x3726), base2, c28);
+    out[6] = decode_pair_fma(prmt(h.w, l1s, 0x1504), base2, c28);
+    out[7] = decode_pair_fma(prmt(h.w, l1s, 0x3726), base2, c28);
 }
 
 // Escape entries of one 256-column group, one per lane (lane < cnt).
