@@ -51,6 +51,7 @@ TensorView view_of(const w12_tensor *w) {
 struct GemmPlan {
     int path;
     int split;
+    GemmArgs cut{};  // small-M path range cut
     int64_t mp;  // partial columns
     size_t counters_off, partials_off, bytes;
 };
@@ -71,20 +72,31 @@ w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, Ge
     if (pl.path == W12_PATH_MMA && M > 16) return W12_ERR_UNSUPPORTED;
     if (pl.path == W12_PATH_TC && M > 256) return W12_ERR_UNSUPPORTED;
     const bool tc = pl.path == W12_PATH_TC;
-    int split = (o && o->split_k > 0) ? o->split_k : (tc ? gemm_tc_split(M, N, K) : gemm_mma_split(M, N, K));
     const int64_t G = groups_of(K);
     const int64_t Np = rows_padded(N);
-    if (G == 0) split = 1;
-    if (split > G && G > 0) split = (int)G;
-    if (Np / 16 > kMaxCounters) split = 1;  // arrival counters exist for at most kMaxCounters stripes
-    pl.split = split;
-    pl.mp = tc ? gemm_tc_pad(M) : gemm_mma_partial_cols(M);
+    const bool counters_ok = Np / 16 <= kMaxCounters;  // arrival counters exist for at most kMaxCounters stripes
     // Fixed layout, the same for every shape, so that the counter region is
     // never reused for partials: [0,256) error word | [256, 256+4*kMaxCounters)
     // arrival counters (zero between calls) | FP32 partials.
     pl.counters_off = 256;
     pl.partials_off = 256 + 4 * kMaxCounters;
-    pl.bytes = split > 1 ? pl.partials_off + (size_t)split * Np * pl.mp * 4 : 256;
+    if (tc) {
+        int split = (o && o->split_k > 0) ? o->split_k : gemm_tc_split(M, N, K);
+        if (G == 0) split = 1;
+        if (split > G && G > 0) split = (int)G;
+        if (!counters_ok) split = 1;
+        pl.split = split;
+        pl.mp = gemm_tc_pad(M);
+        pl.bytes = split > 1 ? pl.partials_off + (size_t)split * Np * pl.mp * 4 : 256;
+    } else {
+        // The kernel numbers (stripe, group) units with int32; a tensor with
+        // 2^31 units would hold 8 TB of hi plane, so this never binds.
+        if (Np / 16 * G >= (1LL << 31)) return W12_ERR_INVALID;
+        pl.split = 1;
+        pl.mp = gemm_mma_partial_cols(M);
+        const int64_t slots = gemm_mma_plan(M, N, K, o ? o->split_k : 0, counters_ok, pl.cut);
+        pl.bytes = slots > 0 ? pl.partials_off + (size_t)slots * 16 * pl.mp * 4 : 256;
+    }
     return W12_OK;
 }
 
@@ -219,6 +231,11 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     g.ldy = ldy;
     g.M = M;
     g.split = pl.split;
+    g.ranges = pl.cut.ranges;
+    g.seglen = pl.cut.seglen;
+    g.per = pl.cut.per;
+    g.q = pl.cut.q;
+    g.rem = pl.cut.rem;
     g.max_ctas = opts ? opts->max_ctas : 0;
     g.overlap = opts ? (opts->flags & W12_GEMM_OVERLAP_PREVIOUS) != 0 : false;
     g.error = reinterpret_cast<int32_t *>(ws);

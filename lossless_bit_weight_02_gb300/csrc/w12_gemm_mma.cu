@@ -4,8 +4,11 @@
 // deterministic").
 //
 // Design (HBM-bound: ~1.33*M flop per weight byte):
-//   * Work item = (row stripe of 16 weight rows, K-chunk s of S).  Each warp
-//     streams its item's tiles: per 16x64 tile every lane issues two 128-bit
+//   * Work: the (16-row stripe, 256-column group) units, in stripe-major
+//     order, are cut into one contiguous range per resident warp, so every
+//     warp streams the same number of groups whatever the stripe count; a
+//     range may start and end inside stripes.  Each warp streams its range's
+//     tiles: per 16x64 tile every lane issues two 128-bit
 //     loads of the hi plane and one of the lo plane - the tile layout puts
 //     exactly the lane's tensor-core A fragment (rows g and g+8, 16 columns
 //     each) behind those loads, so a warp reads 1.5 KB contiguous per tile.
@@ -20,10 +23,11 @@
 //     token rows into its own shared-memory buffer with cp.async while it
 //     works on the current group, so the B fragments come from shared memory
 //     (the warps of an SM would otherwise all wait on the same L2 lines).
-//   * Fixed-order reduction: chunk partials start from zero; when S > 1 they
-//     go to an FP32 workspace and the last warp to finish a stripe sums them
-//     in the order s = 0..S-1 and writes BF16.  S depends on (M, N, K) only,
-//     so the result is identical for any grid.
+//   * Fixed-order reduction: a stripe that lies inside one range is rounded
+//     and stored directly; the pieces of a stripe cut by range boundaries go
+//     to an FP32 workspace, and the warp delivering the last piece sums them
+//     in range order and writes BF16.  The cut depends on (M, N, K) only, so
+//     the result is identical for any grid.
 #include <cstdint>
 
 #include "w12_device.cuh"
@@ -109,21 +113,22 @@ struct Stream {
     uint16_t e_val;
 };
 
-// One 256-column group: stage the next group's activations, then for each of
-// the 4 tiles read the B fragments from shared memory, decode the two rows,
-// prefetch the same tile of the next group (or, on the last group, the same
-// tile again: an L2 hit), patch the tile's escapes and run the MMAs.
+// One unit u (a 256-column group of one stripe): stage the next unit's
+// activations (column group gnext), then for each of the 4 tiles read the B
+// fragments from shared memory, decode the two rows, prefetch the same tile
+// of the next unit (or, on the last unit, the same tile again: an L2 hit),
+// patch the tile's escapes and run the MMAs.
 template <int NB>
-__device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, const GemmArgs &g, int64_t gg,
-                                           bool more, uint4 (*patch)[32], uint8_t *pw, int lane, int rows,
-                                           uint32_t act, const unsigned char *actp, uint32_t frag, uint32_t c28,
-                                           uint32_t c16) {
-    // This lane's copies of group gg have landed; after the warp barrier so
+__device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, const GemmArgs &g, int u,
+                                           int gnext, bool more, uint4 (*patch)[32], uint8_t *pw, int lane,
+                                           int rows, uint32_t act, const unsigned char *actp, uint32_t frag,
+                                           uint32_t c28, uint32_t c16) {
+    // This lane's copies for unit u have landed; after the warp barrier so
     // have every lane's, and every lane is done reading the other buffer.
     cp_async_wait_all();
     __syncwarp();
-    if (more) stage_group<NB>(act + (uint32_t)((gg + 1) & 1) * act_buf_bytes<NB>(), g.A, g.lda, rows, gg + 1, t.K, lane);
-    const unsigned char *ab = actp + (gg & 1) * act_buf_bytes<NB>() + frag;
+    if (more) stage_group<NB>(act + (uint32_t)((u + 1) & 1) * act_buf_bytes<NB>(), g.A, g.lda, rows, gnext, t.K, lane);
+    const unsigned char *ab = actp + (u & 1) * act_buf_bytes<NB>() + frag;
     const int next = more ? 256 : 0;    // uint4 offset of the next group's hi tiles
     const int nextl = more ? 128 : 0;   // ... and lo tiles
 #pragma unroll
@@ -199,6 +204,25 @@ __device__ __forceinline__ void own_escape(Stream<NB> &w, int lane) {
     }
 }
 
+// Ranges: the T*G (stripe, group) units, numbered u = stripe*G + group, are
+// split into segments of g.seglen units (the whole tensor, or one stripe),
+// and each segment into g.per contiguous ranges: the first g.rem ranges of a
+// segment hold g.q + 1 units, the others g.q.  Because both planes and the
+// escape offsets are stored stripe-major with whole groups, a range is one
+// contiguous stream however many stripe boundaries it crosses.  All of it
+// is 32-bit integer arithmetic (unit and range counts are below 2^31).
+__device__ __forceinline__ int range_begin(int v, const GemmArgs &g) {
+    const int seg = v / g.per, j = v - seg * g.per;
+    return seg * g.seglen + j * g.q + (j < g.rem ? j : g.rem);
+}
+// the range holding unit u
+__device__ __forceinline__ int range_of(int u, const GemmArgs &g) {
+    const int seg = u / g.seglen, x = u - seg * g.seglen;
+    const int big = g.rem * (g.q + 1);  // units in the segment's longer ranges
+    const int j = x < big ? x / (g.q + 1) : g.rem + (x - big) / g.q;
+    return seg * g.per + j;
+}
+
 template <int NB>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16)
 __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(TensorView t, GemmArgs g) {
     // [kWarps][4][32] uint4 escape-patch copies, then [kWarps][2][8*NB][kActPitch] activations
@@ -206,10 +230,9 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
     uint4 (*patch)[4][32] = reinterpret_cast<uint4 (*)[4][32]>(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, q = lane & 3;
-    const int S = g.split;
-    const int64_t T = t.Np / 16;
-    const int64_t items = T * S;
+    const int G = (int)t.G;  // unit indices fit an int32 (checked on the host)
     constexpr int MP = 8 * NB;
+    constexpr int kSlot = 16 * MP;  // floats in one partial (16 rows x MP tokens)
     const uint32_t c28 = g.c28, c16 = g.c16;
     uint8_t *pw = reinterpret_cast<uint8_t *>(patch[warp]);
     const int rows = g.M < MP ? (int)g.M : MP;  // staged token rows
@@ -217,68 +240,68 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
     const unsigned char *actp = smem + kWarps * 2048 + warp * 2 * act_buf_bytes<NB>();
     const uint32_t act = (uint32_t)__cvta_generic_to_shared(actp);
     const uint32_t frag = (uint32_t)(gid * kActPitch + 16 * q) * 2u;
+    const uint4 *hi4 = reinterpret_cast<const uint4 *>(t.hi);
+    const uint4 *lo4 = reinterpret_cast<const uint4 *>(t.lo);
+    const int n_esc = (int)t.n_esc;  // offsets are int32
     grid_dep_launch();
     bool dep_done = false;
 
-    for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < items;
-         item += (int64_t)gridDim.x * kWarps) {
-        const int64_t st = item / S;
-        const int s = (int)(item % S);
-        // Chunk s covers whole 256-column groups [g_beg, g_end) (4 tiles each).
-        const int64_t g_beg = (s * t.G) / S, g_end = ((s + 1) * t.G) / S;
-        const int n0 = (int)(st * 16);  // rows < 2^30
-        const int rowA = n0 + gid, rowB = n0 + gid + 8;
+    const int ranges = (int)g.ranges;
+    for (int v = blockIdx.x * kWarps + warp; v < ranges; v += gridDim.x * kWarps) {
+        const int u0 = range_begin(v, g), u1 = range_begin(v + 1, g);
+        if (u0 >= u1) continue;
+        const int nu = (int)(u1 - u0);  // units in the range
         Stream<NB> w;
 
         // 1. weight stream first, so that its latency covers the set-up below
-        w.hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg) * 64 + lane;
-        w.lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg) * 32 + lane;
-        if (g_beg < g_end) {
+        w.hp = hi4 + (int64_t)u0 * 256 + lane;
+        w.lp = lo4 + (int64_t)u0 * 128 + lane;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                w.bh0[p] = ld_stream(w.hp + p * 64);
-                w.bh1[p] = ld_stream(w.hp + p * 64 + 32);
-                w.bl[p] = ld_stream(w.lp + p * 32);
-            }
+        for (int p = 0; p < 4; ++p) {
+            w.bh0[p] = ld_stream(w.hp + p * 64);
+            w.bh1[p] = ld_stream(w.hp + p * 64 + 32);
+            w.bl[p] = ld_stream(w.lp + p * 32);
         }
-        // 2. bases, group offsets (lane l holds the offset of group gw0 + l),
-        //    escapes of the first two groups
-        w.base2A = (rowA < t.N ? (uint32_t)__ldg(t.base + rowA) : 0u) * 0x00800080u;
-        w.base2B = (rowB < t.N ? (uint32_t)__ldg(t.base + rowB) : 0u) * 0x00800080u;
-        const int32_t *gptr = t.esc_ptr + st * t.G;
-        const int n_esc = (int)t.n_esc;  // offsets are int32
-        int gw0 = (int)g_beg;
-        const int gend = (int)g_end;
-        auto load_window = [&](int first) -> int {
-            const int gi = first + lane;
-            int v = 0;
-            if (gi <= gend) {
-                v = __ldg(gptr + gi);
-                v = v < 0 ? 0 : (v > n_esc ? n_esc : v);
-            }
-            return v;
+        // 2. the first stripe's bases, escape offsets (lane l holds the
+        //    offset of unit u0 + iw0 + l), escapes of the first two units
+        int st = u0 / G;
+        int gi = u0 - st * G;  // group of unit u in its stripe
+        auto bases = [&](int stripe, uint32_t &bA, uint32_t &bB) {
+            const int rA = stripe * 16 + gid, rB = rA + 8;
+            bA = (rA < t.N ? (uint32_t)__ldg(t.base + rA) : 0u) * 0x00800080u;
+            bB = (rB < t.N ? (uint32_t)__ldg(t.base + rB) : 0u) * 0x00800080u;
         };
-        int ptrw = load_window(gw0);
-        auto group_bounds = [&](int gg, int &p0, int &p1) {
-            if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per chunk)
-                gw0 = gg;
-                ptrw = load_window(gw0);
+        bases(st, w.base2A, w.base2B);
+        const int32_t *gptr = t.esc_ptr + u0;
+        int iw0 = 0;
+        auto load_window = [&](int first) -> int {
+            const int i = first + lane;
+            int x = 0;
+            if (i <= nu) {
+                x = __ldg(gptr + i);
+                x = x < 0 ? 0 : (x > n_esc ? n_esc : x);
             }
-            p0 = __shfl_sync(kFull, ptrw, gg - gw0);
-            p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
+            return x;
+        };
+        int ptrw = load_window(0);
+        auto unit_bounds = [&](int i, int &p0, int &p1) {
+            if (i + 1 - iw0 >= 32) {  // slide the window (more than 30 units per range)
+                iw0 = i;
+                ptrw = load_window(iw0);
+            }
+            p0 = __shfl_sync(kFull, ptrw, i - iw0);
+            p1 = __shfl_sync(kFull, ptrw, i + 1 - iw0);
             if (p1 < p0) p1 = p0;
         };
         int p0 = 0, p1 = 0;
         EscBatch nxt;
-        w.cur.cnt = nxt.cnt = 0;
-        w.cur.ent = nxt.ent = 0;
-        w.cur.p0 = nxt.p0 = 0;
-        if (g_beg < g_end) {
-            group_bounds((int)g_beg, p0, p1);
-            w.cur = load_group_escapes(t, p0, p1, lane);
-        }
-        if (g_beg + 1 < g_end) {
-            group_bounds((int)g_beg + 1, p0, p1);
+        nxt.cnt = 0;
+        nxt.ent = 0;
+        nxt.p0 = 0;
+        unit_bounds(0, p0, p1);
+        w.cur = load_group_escapes(t, p0, p1, lane);
+        if (nu > 1) {
+            unit_bounds(1, p0, p1);
             nxt = load_group_escapes(t, p0, p1, lane);
         }
 
@@ -289,82 +312,130 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
             dep_done = true;
         }
 
-        // Token rows beyond M are never staged: whatever their buffer rows
-        // hold only reaches accumulator columns that are never stored.
-#pragma unroll
-        for (int b = 0; b < NB; ++b) w.acc[b][0] = w.acc[b][1] = w.acc[b][2] = w.acc[b][3] = 0.f;
-        if (g_beg < g_end) {
-            // every lane is done with the buffers of this warp's previous item
-            __syncwarp();
-            stage_group<NB>(act + (uint32_t)(g_beg & 1) * act_buf_bytes<NB>(), g.A, g.lda, rows, g_beg, t.K, lane);
-            own_escape(w, lane);
-        }
+        // every lane is done with the buffers of this warp's previous range
+        __syncwarp();
+        stage_group<NB>(act + (uint32_t)(u0 & 1) * act_buf_bytes<NB>(), g.A, g.lda, rows, gi, t.K, lane);
+        own_escape(w, lane);
 
-        for (int64_t gg = g_beg; gg < g_end; ++gg) {
-            const bool more = gg + 1 < g_end;
-            group_step<NB>(w, t, g, gg, more, patch[warp], pw, lane, rows, act, actp, frag, c28, c16);
-            w.hp += 256;
-            w.lp += 128;
-            // the next group's escapes are already in flight; fetch the one after
-            w.cur = nxt;
-            if (more) own_escape(w, lane);
-            if (gg + 2 < g_end) {
-                group_bounds((int)gg + 2, p0, p1);
-                nxt = load_group_escapes(t, p0, p1, lane);
-            }
-        }
-        float (&acc)[NB][4] = w.acc;
-
-        // Epilogue.  acc[b] = {(rowA, m0), (rowA, m0+1), (rowB, m0), (rowB, m0+1)}, m0 = 8b + 2q.
-        if (S == 1) {
+        // Arrival counts still to be read: lane 0's count for the range's
+        // first piece when later units follow (-1: none; its stripe is the
+        // one holding u0), and for the range's last piece.
+        int pend_old = -1, last_old = 0;
+        int last_st = -1;
+        int i = 0;  // units of the range done
+        // One stripe piece per pass: units [u0 + i, u0 + pe) of stripe st.
+        while (i < nu) {
+            const int piece0 = u0 + i;
+            const int pe = (st + 1) * G - u0 < nu ? (st + 1) * G - u0 : nu;
+            // Token rows beyond M are never staged: whatever their buffer rows
+            // hold only reaches accumulator columns that are never stored.
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int m = 8 * b + 2 * q + h;
-                    if (m < g.M) {
-                        if (rowA < t.N) g.Y[(int64_t)m * g.ldy + rowA] = f32_to_bf16_rn(acc[b][h]);
-                        if (rowB < t.N) g.Y[(int64_t)m * g.ldy + rowB] = f32_to_bf16_rn(acc[b][2 + h]);
-                    }
+            for (int b = 0; b < NB; ++b) w.acc[b][0] = w.acc[b][1] = w.acc[b][2] = w.acc[b][3] = 0.f;
+            for (; i < pe; ++i) {
+                const bool more = i + 1 < nu;
+                group_step<NB>(w, t, g, u0 + i, gi + 1 == G ? 0 : gi + 1, more, patch[warp], pw, lane, rows, act,
+                               actp, frag, c28, c16);
+                w.hp += 256;
+                w.lp += 128;
+                ++gi;
+                // the next unit's escapes are already in flight; fetch the one after
+                w.cur = nxt;
+                if (more) own_escape(w, lane);
+                if (i + 2 < nu) {
+                    unit_bounds(i + 2, p0, p1);
+                    nxt = load_group_escapes(t, p0, p1, lane);
                 }
             }
-        } else {
-            float *P = g.partials;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                *reinterpret_cast<float2 *>(P + ((int64_t)s * t.Np + rowA) * MP + 8 * b + 2 * q) =
-                    make_float2(acc[b][0], acc[b][1]);
-                *reinterpret_cast<float2 *>(P + ((int64_t)s * t.Np + rowB) * MP + 8 * b + 2 * q) =
-                    make_float2(acc[b][2], acc[b][3]);
-            }
-            __threadfence();
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) last = (atomicAdd(&g.counters[st], 1) == S - 1);
-            last = __shfl_sync(kFull, last, 0);
-            if (last) {
-                __threadfence();
+
+            // The piece [piece0, u0 + pe) of stripe st ends here.
+            // acc[b] = {(rowA, m0), (rowA, m0+1), (rowB, m0), (rowB, m0+1)}, m0 = 8b + 2q.
+            const int n0 = st * 16, sbeg = st * G;
+            const int rowA = n0 + gid, rowB = n0 + gid + 8;
+            const bool more = i < nu;
+            if (piece0 == sbeg && gi == G) {  // the whole stripe: round and store
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int64_t row = rr ? rowB : rowA;
-                        float2 v = __ldcg(reinterpret_cast<const float2 *>(P + row * MP + 8 * b + 2 * q));
-                        for (int ss = 1; ss < S; ++ss) {
-                            const float2 w =
-                                __ldcg(reinterpret_cast<const float2 *>(P + ((int64_t)ss * t.Np + row) * MP + 8 * b + 2 * q));
-                            v.x += w.x;
-                            v.y += w.y;
-                        }
-                        if (row < t.N) {
-                            const int m = 8 * b + 2 * q;
-                            if (m < g.M) g.Y[(int64_t)m * g.ldy + row] = f32_to_bf16_rn(v.x);
-                            if (m + 1 < g.M) g.Y[(int64_t)(m + 1) * g.ldy + row] = f32_to_bf16_rn(v.y);
+                    for (int h = 0; h < 2; ++h) {
+                        const int m = 8 * b + 2 * q + h;
+                        if (m < g.M) {
+                            if (rowA < t.N) g.Y[(int64_t)m * g.ldy + rowA] = f32_to_bf16_rn(w.acc[b][h]);
+                            if (rowB < t.N) g.Y[(int64_t)m * g.ldy + rowB] = f32_to_bf16_rn(w.acc[b][2 + h]);
                         }
                     }
                 }
-                if (lane == 0) g.counters[st] = 0;
+            } else {
+                // Partial: slot v for the range's first piece, v + ranges for
+                // a later one.  The arrival count is read only at the end of
+                // the range, so the atomic's round trip never stalls the
+                // stream; the last of the stripe's pieces to arrive then sums
+                // them in range order and stores.
+                float *slot = g.partials + ((int64_t)v + (piece0 == u0 ? 0 : ranges)) * kSlot;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    *reinterpret_cast<float2 *>(slot + gid * MP + 8 * b + 2 * q) = make_float2(w.acc[b][0], w.acc[b][1]);
+                    *reinterpret_cast<float2 *>(slot + (gid + 8) * MP + 8 * b + 2 * q) =
+                        make_float2(w.acc[b][2], w.acc[b][3]);
+                }
+                __threadfence();
+                __syncwarp();
+                int old = 0;
+                if (lane == 0) old = atomicAdd(&g.counters[st], 1);
+                if (piece0 == u0 && more) {
+                    pend_old = old;
+                } else {
+                    last_st = st;
+                    last_old = old;
+                }
             }
+            if (more) {  // on to the next stripe (its first unit's weights are in flight already)
+                ++st;
+                gi = 0;
+                bases(st, w.base2A, w.base2B);
+            }
+        }
+
+        // Stripes whose last piece this warp delivered: sum their partials.
+        pend_old = __shfl_sync(kFull, pend_old, 0);
+        for (int k = 0; k < 2; ++k) {
+            const int rs = k == 0 ? (pend_old >= 0 ? u0 / G : -1) : last_st;
+            if (rs < 0) continue;
+            const int sbeg = rs * G;
+            const int va = range_of(sbeg, g), vb = range_of(sbeg + G - 1, g);
+            const int fin = __shfl_sync(kFull, (k == 0 ? pend_old : last_old) == (int)(vb - va), 0);
+            if (!fin) continue;
+            __threadfence();
+            // only range va can start before the stripe (its piece is then a later one)
+            const float *first = g.partials + ((int64_t)va + (range_begin(va, g) < sbeg ? ranges : 0)) * kSlot;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int lr = gid + 8 * rr;
+                    const int off = lr * MP + 8 * b + 2 * q;
+                    float2 sum = __ldcg(reinterpret_cast<const float2 *>(first + off));
+                    for (int x = va + 1; x <= vb; x += 4) {  // four independent loads at a time
+                        float2 y[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (x + j <= vb)
+                                y[j] = __ldcg(reinterpret_cast<const float2 *>(g.partials + (int64_t)(x + j) * kSlot + off));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (x + j <= vb) {
+                                sum.x += y[j].x;
+                                sum.y += y[j].y;
+                            }
+                    }
+                    const int row = rs * 16 + lr;
+                    if (row < t.N) {
+                        const int m = 8 * b + 2 * q;
+                        if (m < g.M) g.Y[(int64_t)m * g.ldy + row] = f32_to_bf16_rn(sum.x);
+                        if (m + 1 < g.M) g.Y[(int64_t)(m + 1) * g.ldy + row] = f32_to_bf16_rn(sum.y);
+                    }
+                }
+            }
+            if (lane == 0) g.counters[rs] = 0;
         }
     }
 }
@@ -399,8 +470,7 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         lc.occ[NB] = occ > 0 ? occ : 1;
     }
-    const int64_t items = (t.Np / 16) * (int64_t)g.split;
-    int64_t blocks = (items + kWarps - 1) / kWarps;
+    int64_t blocks = (g.ranges + kWarps - 1) / kWarps;
     const int64_t resident = (int64_t)lc.sms * lc.occ[NB];
     if (blocks > resident) blocks = resident;
     if (g.max_ctas > 0 && blocks > g.max_ctas) blocks = g.max_ctas;
@@ -422,19 +492,42 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
 
 int64_t gemm_mma_partial_cols(int64_t M) { return M <= 8 ? 8 : 16; }
 
-// Split factor from (M, N, K) only: as many (stripe, chunk) items as fit
-// one wave of 16 resident warps on each of 152 SMs, chunks of whole
-// 256-column groups.
-int gemm_mma_split(int64_t M, int64_t N, int64_t K) {
-    (void)M;
-    const int64_t T = (N + 15) / 16, G = groups_of(K);
-    if (T == 0 || G == 0) return 1;
-    const int64_t target = 152 * 16;
-    int64_t S = target / T;
-    if (S > G) S = G;
-    if (S > 32) S = 32;
-    if (S < 1) S = 1;
-    return (int)S;
+// The range cut depends on (M, N, K, split_k) only, never on the grid, so
+// the summation order (and the result) is the same for any launch.
+//  * automatic: one range per resident warp of a 152-SM GPU (16 warps per
+//    SM for M <= 8, 12 for M <= 16) over the whole tensor, so that every
+//    warp streams the same number of groups whatever the stripe count; at
+//    most one range per unit.
+//  * forced split S: S ranges of whole groups per stripe.
+//  * no arrival counters (more stripes than counters): one range per stripe.
+int64_t gemm_mma_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters_ok, GemmArgs &g) {
+    const int64_t T = (N + 15) / 16, G = groups_of(K), U = T * G;
+    auto cut = [&](int64_t seglen, int64_t per, int64_t nseg) {
+        g.seglen = (int)seglen, g.per = (int)per;
+        g.q = (int)(seglen / per), g.rem = (int)(seglen % per);
+        g.ranges = nseg * per;
+    };
+    if (U == 0) {
+        cut(1, 1, 1);
+        return 0;
+    }
+    if (!counters_ok || split_k == 1) {
+        cut(G, 1, T);
+        return 0;
+    }
+    if (split_k > 1) {
+        const int64_t S = split_k < G ? split_k : G;
+        cut(G, S, T);
+        return S > 1 ? g.ranges : 0;
+    }
+    int64_t V = (M <= 8 ? 16 : 12) * 152;
+    if (V > U) V = U;
+    cut(U, V, 1);
+    for (int64_t v = 1; v < V; ++v) {  // any range boundary inside a stripe needs partials
+        const int64_t b = v * g.q + (v < g.rem ? v : g.rem);
+        if (b % G != 0) return 2 * V;
+    }
+    return 0;
 }
 
 cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s) {

@@ -51,10 +51,15 @@ struct GemmArgs {
     uint16_t *Y;
     int64_t ldy;
     int64_t M;
-    int split;           // S >= 1
+    int split;           // tensor-core path: K-chunks per stripe, S >= 1
+    // small-M path: the T*G (stripe, group) units are cut into segments of
+    // seglen units, each segment into `per` contiguous ranges (the first rem
+    // of q+1 units, the rest of q); `ranges` in all
+    int64_t ranges;
+    int seglen, per, q, rem;
     int max_ctas;        // 0 = occupancy-limited persistent grid
     bool overlap;        // launch as a programmatic dependent of the previous kernel
-    float *partials;     // [S][Np][MP] fp32 (S > 1)
+    float *partials;     // tensor-core path: [S][Mpad][Np]; small-M path: [2*ranges][16][MP] fp32
     int32_t *counters;   // [Np/16] arrival counters (S > 1)
     int32_t *error;      // device error word
     uint32_t c28, c16;  // 1<<28, 16: multiplicands the decoder needs at run time
@@ -68,7 +73,10 @@ int64_t gemm_tc_pad(int64_t M);
 
 // Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).
 cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s);
-int gemm_mma_split(int64_t M, int64_t N, int64_t K);
 int64_t gemm_mma_partial_cols(int64_t M);  // MP
+// The range cut of the small-M path for (M, N, K) and a forced split (0 =
+// automatic): fills ranges / seglen / per / q / rem and returns the number of
+// partial slots the cut needs (0 when every stripe lies inside one range).
+int64_t gemm_mma_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters_ok, GemmArgs &g);
 
 }  // namespace w12

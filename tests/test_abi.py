@@ -58,12 +58,15 @@ def test_oracle_and_library_agree_on_sizes(w12lib, oracle):
 
 def test_gemm_workspace_query(w12lib):
     o = w12lib.make_opts()
-    # one stripe count of counters + S partial slabs of [Np, 8] floats
-    nb = w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, o)
-    slab = 5120 * 8 * 4  # one [Np, 8] FP32 partial slab
-    S, rem = divmod(nb - 256 - 4 * 65536, slab)
-    assert rem == 0 and 2 <= S <= 20  # a split of the 20 column groups
-    assert w12lib.w12_gemm_workspace_bytes(16, 5120, 5120, o) == 256 + 4 * 65536 + S * 2 * slab
+    base = 256 + 4 * 65536  # error word + arrival counters
+    T, G = 5120 // 16, 5120 // 256
+    # small-M path: FP32 partial slots of [16 rows, MP tokens], MP = 8 (M <= 8) or 16 (M <= 16);
+    # the automatic cut has at most two partial pieces per range and one range per unit
+    for M, mp in ((1, 8), (16, 16)):
+        slots, rem = divmod(w12lib.w12_gemm_workspace_bytes(M, 5120, 5120, o) - base, 16 * mp * 4)
+        assert rem == 0 and 0 < slots <= 2 * T * G
+    # a forced split of S K-chunks per stripe: one slot per (stripe, chunk)
+    assert w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, w12lib.make_opts(split_k=4)) == base + T * 4 * 16 * 8 * 4
     assert w12lib.w12_gemm_workspace_bytes(1, 5120, 5120, w12lib.make_opts(split_k=1)) == 256
     assert w12lib.w12_gemm_workspace_bytes(17, 64, 64, w12lib.make_opts(path=w12lib.W12_PATH_MMA)) == 0
     assert w12lib.w12_gemm_workspace_bytes(257, 64, 64, o) == 0  # beyond the tensor-core path

@@ -131,6 +131,30 @@ def test_deterministic_across_runs_and_grids(w12lib):
             assert np.array_equal(o, outs[0])
 
 
+@pytest.mark.parametrize("N,K", [(77829, 256), (40003, 296), (9001, 2304)])
+def test_ranges_across_stripes(N, K, w12lib, oracle):
+    """The small-M kernel cuts the (stripe, 256-column group) units into one
+    contiguous range per resident warp.  Here ranges hold several whole
+    stripes (K = 256: one group per stripe), start and end inside stripes
+    (K = 296: two groups, the second ragged), or hold a few groups of one or
+    two stripes (K = 2304).  Every output is compared with the oracle at
+    M = 1, 5 and 16 (both kernel variants), and the result is bitwise the
+    same for several grid caps."""
+    W = synth.dense_weights(N, K, seed=N + K)
+    st, ref = oracle.encode(W)
+    t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+    for M in (1, 5, 16):
+        A = synth.activations(M, K, seed=M + K)
+        st, Yr, Y64, mag = oracle.gemm(A, ref)
+        Ad = synth.bits_to_tensor(A, "cuda")
+        outs = [synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, opts=w12lib.make_opts(max_ctas=cap)))
+                for cap in (0, 5, 200)]
+        bad = gemm_tolerance_failures(outs[0], Yr, Y64, mag)
+        assert bad.size == 0, (M, bad[:10])
+        for o in outs[1:]:
+            assert np.array_equal(o, outs[0])
+
+
 def test_workspace_left_clean_and_reusable(w12lib, oracle):
     """Counters return to zero after each call, so one workspace serves a
     sequence of different shapes."""
