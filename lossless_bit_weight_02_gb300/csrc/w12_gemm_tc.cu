@@ -5,22 +5,30 @@
 //
 // One CTA owns 128 weight rows (8 stripes of 16) and a chunk of whole
 // 256-column groups; per 64-column k-block:
-//   * 8 decoder warps (one stripe each) stream their tile (1.5 KB, the same
-//     fragment-native loads as the small-M kernel, one 4-tile group in
-//     flight), decode it in registers and store it as BF16 into the UMMA A
-//     operand: 128 rows x 128 bytes, K-major, 128-byte swizzle.  Escapes of
-//     the tile are written over their slots in shared memory.  Each thread
-//     then fences the generic->async proxy and arrives on the stage's
-//     "A full" barrier;
-//   * one producer thread loads the activation tile [Mpad x 64] with TMA
-//     (rows >= M and columns >= K come back as zeros) into the B operand;
-//   * one MMA thread waits for both, issues four tcgen05.mma (M=128,
-//     N=Mpad, K=16) accumulating in TMEM, and commits to the stage's "empty"
-//     barrier.
-// The epilogue warps read the accumulator with tcgen05.ld.  With a split of
-// S > 1 the chunk partials go to the FP32 workspace and the last CTA of a row
-// tile adds them in the order s = 0..S-1; S depends only on (M, N, K).
-// Every mbarrier wait is bounded: on expiry the CTA records W12_ERR_TIMEOUT in
+//   * a weight-producer warp fetches the 8 tiles of the k-block (12 KB of
+//     W12 planes) with two tiled TMA copies (the planes seen as 4-D u8
+//     tensors), up to a whole ring of k-blocks ahead of the decoders;
+//   * 16 decoder warps (two per stripe, even / odd k-blocks) read their
+//     tile from that ring (the fragment-native order makes this three
+//     conflict-free 16-byte loads per lane), decode it in registers and
+//     store it as BF16 into the UMMA A operand: 128 rows x 128 bytes,
+//     K-major, 128-byte swizzle.  Escapes of the tile are written over
+//     their slots.  Each warp then fences the generic->async proxy and one
+//     lane arrives on the stage's "A full" barrier;
+//   * an activation-producer warp loads the tile [Mpad x 64] with TMA (rows
+//     >= M and columns >= K come back as zeros) into the B operand;
+//   * an MMA warp waits for both, and one elected lane issues four
+//     tcgen05.mma (M=128, N=Mpad, K=16) accumulating in TMEM and commits to
+//     the stages' "empty" barriers.  The producer and MMA loops run on the
+//     whole (converged) warp so that their addresses stay in uniform
+//     registers; only the issue is elected.
+// Ring depths (decoded A, weight planes, activations) fill the shared
+// memory for the given Mpad.  The epilogue warps read the accumulator with
+// tcgen05.ld.  With a split of S > 1 the chunk partials go to the FP32
+// workspace and the last CTA of a row tile adds them in the order
+// s = 0..S-1; S depends only on (M, N, K).
+// Every mbarrier wait is bounded (try_wait with a suspend hint, so waiting
+// warps take no issue slots): on expiry the CTA records W12_ERR_TIMEOUT in
 // the workspace error word, waits (bounded) for its own copies and MMAs, and
 // frees its TMEM.
 #include <cuda.h>
@@ -37,18 +45,36 @@
 namespace w12 {
 namespace {
 
-constexpr int kDecWarps = 16;     // two per 16-row stripe (even / odd tiles of each group)
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;      // the warp after the producer issues the MMAs
-constexpr int kThreads = 32 * (kDecWarps + 2);
-constexpr uint32_t kAStageBytes = 128 * 128;  // 128 rows x 64 BF16
-constexpr long long kWaitPolls = 1LL << 20;    // each poll is a try_wait (which may itself block)
+constexpr int kDecWarps = 16;     // two per 16-row stripe (even / odd k-blocks)
+constexpr int kWProdWarp = 16;    // streams the weight planes (and owns TMEM)
+constexpr int kBProdWarp = 17;    // streams the activations
+constexpr int kMmaWarp = 18;      // issues the MMAs
+constexpr int kThreads = 32 * (kDecWarps + 3);
+constexpr uint32_t kAStageBytes = 128 * 128;   // decoded A: 128 rows x 64 BF16, swizzled
+constexpr uint32_t kWStageBytes = 8 * 1536;    // the 8 stripes of a row tile, one k-block: 8 KB hi, 4 KB lo
+constexpr int kMaxStages = 8;    // per ring
+constexpr int kSuspendNs = 20000;               // longest sleep of one try_wait
+constexpr long long kWaitPolls = 1LL << 16;    // try_waits before a wait gives up (~1.3 s)
 
 struct TcParams {
-    int Mp;         // tokens padded to a multiple of 16 (UMMA N)
-    int stages;     // pipeline depth
-    int tmem_cols;  // power of two >= max(32, Mp)
-    uint32_t idesc; // tcgen05 instruction descriptor
+    int Mp;                // tokens padded to a multiple of 16 (UMMA N)
+    int a_st, w_st, b_st;  // depths of the decoded-A, weight-plane and activation rings (2..kMaxStages)
+    int tmem_cols;         // power of two >= max(32, Mp)
+    uint32_t idesc;        // tcgen05 instruction descriptor
+};
+
+// Stage index and phase parity of a ring position, advanced by `step`
+// positions at a time (step <= depth).
+struct RingPos {
+    int stage = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance(int step, int depth) {
+        stage += step;
+        if (stage >= depth) {
+            stage -= depth;
+            phase ^= 1u;
+        }
+    }
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -65,12 +91,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
 }
+// try_wait suspends the thread (no issue slots spent) until the phase
+// completes or kSuspendNs elapse, whichever comes first.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -78,14 +106,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Bounded wait for the completion of phase `parity`.  Gives up (returns
 // false) when another thread of the CTA has given up, or after kWaitPolls
 // polls, in which case it raises the CTA's abort flag and the error word.
-__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
     for (long long i = 0; i < kWaitPolls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 255 && *abort_flag) return false;
+        if ((i & 15) == 15 && *abort_flag) return false;
     }
     *abort_flag = 1;
     atomicExch(err, 1);
     return false;
+}
+
+// true on one lane of the (converged) warp
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile("{\n.reg .pred p;\nelect.sync _|p, 0xffffffff;\nselp.u32 %0, 1, 0, p;\n}" : "=r"(r));
+    return r != 0;
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -123,6 +158,8 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     uint32_t r[16];
     asm volatile(
@@ -140,18 +177,38 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c2, int c3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// tmap: activations [M, K] BF16, box [Mp, 64], 128-byte swizzle.
+// hmap / lmap: the hi / lo plane as u8 [stripes][k-blocks][4 or 2][256], box
+// [8 stripes][1 k-block][4 or 2][256]: one copy brings the row tile's 8
+// tiles of a k-block (stripes past the end read as zero).
 __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs g, TcParams tp,
-                                                         const __grid_constant__ CUtensorMap tmap) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int R = tp.stages, Mp = tp.Mp;
+                                                         const __grid_constant__ CUtensorMap tmap,
+                                                         const __grid_constant__ CUtensorMap hmap,
+                                                         const __grid_constant__ CUtensorMap lmap) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned, by an offset so that the compiler keeps the
+    // shared address space (ld.shared / st.shared, not generic accesses)
+    uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int RA = tp.a_st, RW = tp.w_st, RB = tp.b_st, Mp = tp.Mp;
     const uint32_t b_stage_bytes = (uint32_t)Mp * 128;
-    uint8_t *a_st = base;
-    uint8_t *b_st = base + R * kAStageBytes;
-    uint64_t *full_a = reinterpret_cast<uint64_t *>(b_st + R * b_stage_bytes);
-    uint64_t *full_b = full_a + R;
-    uint64_t *empty = full_b + R;
-    uint64_t *done = empty + R;
+    uint8_t *a_st = base;                                // RA x 16 KB (1024-aligned)
+    uint8_t *b_st = a_st + RA * kAStageBytes;            // RB x Mp*128 B (1024-aligned)
+    uint8_t *w_st = b_st + RB * b_stage_bytes;           // RW x 12 KB (1024-aligned)
+    uint64_t *w_full = reinterpret_cast<uint64_t *>(w_st + RW * kWStageBytes);
+    uint64_t *w_empty = w_full + RW;
+    uint64_t *a_full = w_empty + RW;
+    uint64_t *a_empty = a_full + RA;
+    uint64_t *b_full = a_empty + RA;
+    uint64_t *b_empty = b_full + RB;
+    uint64_t *done = b_empty + RB;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
@@ -162,18 +219,26 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
     const int s = (int)(blockIdx.x % S);
     const int64_t g_beg = (s * t.G) / S, g_end = ((s + 1) * t.G) / S;
     const int nkb = (int)(4 * (g_end - g_beg));
+    const int64_t T = t.Np / 16;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < R; ++i) {
-            mbar_init(&full_a[i], (kDecWarps / 2) * 32);  // the 8 warps of one tile parity
-            mbar_init(&full_b[i], 1);
-            mbar_init(&empty[i], 1);
+        for (int i = 0; i < RW; ++i) {
+            mbar_init(&w_full[i], 1);                // the producer's expect_tx
+            mbar_init(&w_empty[i], kDecWarps / 2);   // one arrival per decoder warp of the k-block
+        }
+        for (int i = 0; i < RA; ++i) {
+            mbar_init(&a_full[i], kDecWarps / 2);
+            mbar_init(&a_empty[i], 1);               // tcgen05.commit
+        }
+        for (int i = 0; i < RB; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kProducerWarp) {
+    if (warp == kWProdWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                      "r"(tp.tmem_cols)
                      : "memory");
@@ -187,19 +252,17 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
 
     if (warp < kDecWarps) {
         // ------------------------------------------------------------------
-        // Decoders: warp w handles stripe st = 8*tt + (w%8) and the tiles
-        // p = w/8 and w/8 + 2 of every group.
+        // Decoders: warp w handles stripe st = 8*tt + (w%8) on the k-blocks
+        // of parity w/8 (tiles p = w/8 and w/8 + 2 of every group): the
+        // tile's planes come from the weight ring, the BF16 tile goes to the
+        // A ring (K-major, 128-byte swizzle), escapes over their slots.
         // ------------------------------------------------------------------
         const int gid = lane >> 2, q = lane & 3;
         const int sw = warp & 7, par = warp >> 3;
-        const int64_t T = t.Np / 16;
         const int64_t st = tt * 8 + sw;
         const bool live = st < T;  // warp-uniform
         const int rA = 16 * sw + gid, rB = rA + 8;
         const uint32_t c28 = g.c28, c16 = g.c16;
-        uint4 bh0[2], bh1[2], bl[2];
-        const uint4 *hp = reinterpret_cast<const uint4 *>(t.hi) + (st * t.KT + 4 * g_beg + par) * 64 + lane;
-        const uint4 *lp = reinterpret_cast<const uint4 *>(t.lo) + (st * t.KT + 4 * g_beg + par) * 32 + lane;
         uint32_t base2A = 0, base2B = 0;
         EscBatch cur, nxt;
         cur.cnt = nxt.cnt = 0;
@@ -232,12 +295,6 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
             if (p1 < p0) p1 = p0;
         };
         if (live && nkb > 0) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                bh0[i] = ld_stream(hp + i * 128);
-                bh1[i] = ld_stream(hp + i * 128 + 32);
-                bl[i] = ld_stream(lp + i * 64);
-            }
             const int64_t nA = st * 16 + gid, nB = nA + 8;
             base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
             base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
@@ -252,67 +309,69 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         uint32_t emask = (live && nkb > 0) ? escape_tiles(cur, lane) : 0u;
         grid_dep_wait();  // Y and the workspace may belong to the previous kernel
         bool ok = true;
-        for (int64_t gg = g_beg; gg < g_end && ok; ++gg) {
-            const bool more = gg + 1 < g_end;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int p = par + 2 * i;  // tile of the group
-                const int kb = (int)(4 * (gg - g_beg)) + p;
-                const int stage = kb % R;
-                const uint32_t ph = (uint32_t)((kb / R) & 1);
-                uint32_t dA[8], dB[8];
-                if (live) {
-                    decode16_fma(bh0[i], bl[i].x, bl[i].y, base2A, c28, c16, dA);
-                    decode16_fma(bh1[i], bl[i].z, bl[i].w, base2B, c28, c16, dB);
-                    if (more) {
-                        bh0[i] = ld_stream(hp + 256 + i * 128);
-                        bh1[i] = ld_stream(hp + 256 + i * 128 + 32);
-                        bl[i] = ld_stream(lp + 128 + i * 64);
-                    }
-                }
-                // the whole warp leaves together, so no lane is left behind at
-                // a warp-wide instruction
-                if (!__all_sync(kFull, mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.error))) {
-                    ok = false;
-                    break;
-                }
-                if (live) {
-                    uint8_t *A = a_st + stage * kAStageBytes;
-                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q)) = make_uint4(dA[0], dA[1], dA[2], dA[3]);
-                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q + 1)) = make_uint4(dA[4], dA[5], dA[6], dA[7]);
-                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q)) = make_uint4(dB[0], dB[1], dB[2], dB[3]);
-                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q + 1)) = make_uint4(dB[4], dB[5], dB[6], dB[7]);
-                    if ((emask >> p) & 1u) {  // escapes of this tile overwrite their slots
-                        __syncwarp();
-                        auto put = [&](uint32_t e) {
-                            const int key = (int)(e >> 16);
-                            const int r = 16 * sw + ((key >> 6) & 15), j = key & 63;
-                            *reinterpret_cast<uint16_t *>(A + swz(r, j >> 3) + (j & 7) * 2) = (uint16_t)(e & 0xFFFFu);
-                        };
-                        if (cur.cnt <= 32) {
-                            if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
-                        } else {
-                            for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
-                                const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
-                                if (b0 + lane < cur.cnt && (int)(e >> 26) == p) put(e);
-                            }
-                        }
-                    }
-                }
-                fence_proxy_async();
-                mbar_arrive(&full_a[stage]);
-            }
-            if (live) {
-                hp += 256;
-                lp += 128;
+        RingPos wp, ap;  // ring positions of k-block kb
+        wp.advance(par, RW);
+        ap.advance(par, RA);
+        for (int kb = par; kb < nkb && ok; kb += 2, wp.advance(2, RW), ap.advance(2, RA)) {
+            const int p = kb & 3;  // tile of the group
+            if (kb >= 4 && p == par && live) {  // first tile of a new group for this warp
+                const int64_t gg = g_beg + (kb >> 2);
                 cur = nxt;
-                emask = more ? escape_tiles(cur, lane) : 0u;
-                if (gg + 2 < g_end) {
+                emask = escape_tiles(cur, lane);
+                if (gg + 1 < g_end) {
                     int p0, p1;
-                    bounds(gg + 2, p0, p1);
+                    bounds(gg + 1, p0, p1);
                     nxt = load_group_escapes(t, p0, p1, lane);
                 }
             }
+            const int ws = wp.stage, as = ap.stage;
+            const uint32_t wph = wp.phase, aph = ap.phase;
+            // the whole warp leaves together, so no lane is left behind at a
+            // warp-wide instruction
+            if (!__all_sync(kFull, mbar_wait(&w_full[ws], wph, abort_flag, g.error))) {
+                ok = false;
+                break;
+            }
+            uint32_t dA[8], dB[8];
+            if (live) {
+                const uint8_t *W = w_st + ws * kWStageBytes;
+                const uint4 h0 = lds128(W + sw * 1024 + lane * 16), h1 = lds128(W + sw * 1024 + 512 + lane * 16);
+                const uint4 l = lds128(W + 8192 + sw * 512 + lane * 16);
+                decode16_fma(h0, l.x, l.y, base2A, c28, c16, dA);
+                decode16_fma(h1, l.z, l.w, base2B, c28, c16, dB);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[ws]);  // the planes are in registers
+            if (!__all_sync(kFull, mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, g.error))) {
+                ok = false;
+                break;
+            }
+            if (live) {
+                uint8_t *A = a_st + as * kAStageBytes;
+                *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q)) = make_uint4(dA[0], dA[1], dA[2], dA[3]);
+                *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q + 1)) = make_uint4(dA[4], dA[5], dA[6], dA[7]);
+                *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q)) = make_uint4(dB[0], dB[1], dB[2], dB[3]);
+                *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q + 1)) = make_uint4(dB[4], dB[5], dB[6], dB[7]);
+                if ((emask >> p) & 1u) {  // escapes of this tile overwrite their slots
+                    __syncwarp();
+                    auto put = [&](uint32_t e) {
+                        const int key = (int)(e >> 16);
+                        const int r = 16 * sw + ((key >> 6) & 15), j = key & 63;
+                        *reinterpret_cast<uint16_t *>(A + swz(r, j >> 3) + (j & 7) * 2) = (uint16_t)(e & 0xFFFFu);
+                    };
+                    if (cur.cnt <= 32) {
+                        if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
+                    } else {
+                        for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
+                            const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
+                            if (b0 + lane < cur.cnt && (int)(e >> 26) == p) put(e);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[as]);
         }
 
         // ------------------------------------------------------------------
@@ -358,62 +417,102 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
                 __threadfence();
                 if (n < t.N) {
                     for (int c = half; c < chunks; c += 4) {
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = 16 * c + j;
-                            if (m >= g.M) break;
-                            float acc = __ldcg(g.partials + (int64_t)m * t.Np + n);
-                            for (int ss = 1; ss < S; ++ss) acc += __ldcg(g.partials + ((int64_t)ss * Mp + m) * t.Np + n);
-                            g.Y[(int64_t)m * g.ldy + n] = f32_to_bf16_rn(acc);
+                        // 16 independent loads per chunk s, summed in the order s = 0..S-1
+                        float acc[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] = __ldcg(g.partials + (int64_t)(16 * c + j) * t.Np + n);
+                        for (int ss = 1; ss < S; ++ss) {
+                            float v[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                v[j] = __ldcg(g.partials + ((int64_t)ss * Mp + 16 * c + j) * t.Np + n);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] += v[j];
                         }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (16 * c + j < g.M) g.Y[(int64_t)(16 * c + j) * g.ldy + n] = f32_to_bf16_rn(acc[j]);
                     }
                 }
                 if (threadIdx.x == 0) g.counters[tt] = 0;
             }
         }
-    } else if (warp == kProducerWarp) {
+    } else if (warp == kWProdWarp) {
+        // ------------------------------------------------------------------
+        // Weight planes: one k-block (8 tiles of 1.5 KB) per stage, with
+        // tiled copies, up to RW k-blocks ahead of the decoders.  Reads
+        // only the W12 tensor, so it starts before the previous kernel ends.
+        // ------------------------------------------------------------------
+        // The whole warp runs the loop (warp-uniform values stay in uniform
+        // registers); one elected lane issues.
+        int issued = 0;
+        RingPos wp;
+        for (int kb = 0; kb < nkb; ++kb, wp.advance(1, RW)) {
+            const int ws = wp.stage;
+            if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) break;
+            if (elect_one()) {
+                // the full box is counted, out-of-range stripes included (zero-filled)
+                mbar_expect_tx(&w_full[ws], kWStageBytes);
+                uint8_t *dst = w_st + ws * kWStageBytes;
+                const int kbg = (int)(4 * g_beg) + kb, st0 = (int)(tt * 8);
+                tma_load_4d(dst, &hmap, kbg, st0, &w_full[ws]);
+                tma_load_4d(dst + 8192, &lmap, kbg, st0, &w_full[ws]);
+            }
+            __syncwarp();
+            ++issued;
+        }
+        // the copies issued last must have landed before the CTA exits
+        for (int i = issued > RW ? issued - RW : 0; i < issued; ++i)
+            mbar_wait(&w_full[i % RW], (uint32_t)((i / RW) & 1), abort_flag, g.error);
+    } else if (warp == kBProdWarp) {
         // ------------------------------------------------------------------
         // Activations: one TMA tile [Mp x 64] per k-block.
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            grid_dep_wait();  // A may be written by the previous kernel
-            int issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int stage = kb % R;
-                const uint32_t ph = (uint32_t)((kb / R) & 1);
-                if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, g.error)) break;
-                mbar_expect_tx(&full_b[stage], b_stage_bytes);
-                tma_load_2d(b_st + stage * b_stage_bytes, &tmap, (int)((4 * g_beg + kb) * 64), 0, &full_b[stage]);
-                ++issued;
+        grid_dep_wait();  // A may be written by the previous kernel
+        int issued = 0;
+        RingPos bp;
+        for (int kb = 0; kb < nkb; ++kb, bp.advance(1, RB)) {
+            const int stage = bp.stage;
+            if (!__all_sync(kFull, mbar_wait(&b_empty[stage], bp.phase ^ 1u, abort_flag, g.error))) break;
+            if (elect_one()) {
+                mbar_expect_tx(&b_full[stage], b_stage_bytes);
+                tma_load_2d(b_st + stage * b_stage_bytes, &tmap, (int)((4 * g_beg + kb) * 64), 0, &b_full[stage]);
             }
-            // the copies issued last must have landed before the CTA exits
-            for (int i = issued > R ? issued - R : 0; i < issued; ++i)
-                mbar_wait(&full_b[i % R], (uint32_t)((i / R) & 1), abort_flag, g.error);
+            __syncwarp();
+            ++issued;
         }
+        // the copies issued last must have landed before the CTA exits
+        for (int i = issued > RB ? issued - RB : 0; i < issued; ++i)
+            mbar_wait(&b_full[i % RB], (uint32_t)((i / RB) & 1), abort_flag, g.error);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------
         // MMA issue (one thread).
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int stage = kb % R;
-                const uint32_t ph = (uint32_t)((kb / R) & 1);
-                if (!mbar_wait(&full_a[stage], ph, abort_flag, g.error)) break;
-                if (!mbar_wait(&full_b[stage], ph, abort_flag, g.error)) break;
-                tc_fence_after();
-                const uint32_t a0 = smem_addr(a_st + stage * kAStageBytes);
-                const uint32_t b0 = smem_addr(b_st + stage * b_stage_bytes);
+        // The whole warp runs the loop; one elected lane issues the MMAs.
+        RingPos ap, bp;
+        for (int kb = 0; kb < nkb; ++kb, ap.advance(1, RA), bp.advance(1, RB)) {
+            const int as = ap.stage, bs = bp.stage;
+            if (!__all_sync(kFull, mbar_wait(&a_full[as], ap.phase, abort_flag, g.error))) break;
+            if (!__all_sync(kFull, mbar_wait(&b_full[bs], bp.phase, abort_flag, g.error))) break;
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(a_st + as * kAStageBytes);
+            const uint32_t b0 = smem_addr(b_st + bs * b_stage_bytes);
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     umma(tmem, smem_desc(a0 + 32 * kk), smem_desc(b0 + 32 * kk), tp.idesc, (kb | kk) != 0);
-                umma_commit(&empty[stage]);
+                umma_commit(&a_empty[as]);
+                umma_commit(&b_empty[bs]);
             }
-            umma_commit(done);  // arrives once every MMA issued above has completed
+            __syncwarp();
         }
+        if (elect_one()) umma_commit(done);  // arrives once every MMA issued above has completed
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kProducerWarp) {
+    if (warp == kWProdWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tp.tmem_cols)
                      : "memory");
@@ -437,14 +536,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-int tc_stages(int Mp) {  // one CTA per SM: up to ~200 KB of stages
-    const int stage = (int)kAStageBytes + Mp * 128;
-    int r = (200 * 1024) / stage;
-    return r < 2 ? 2 : (r > 6 ? 6 : r);
+size_t tc_smem_bytes(const TcParams &tp) {
+    return 1024 + (size_t)tp.a_st * kAStageBytes + (size_t)tp.b_st * tp.Mp * 128 + (size_t)tp.w_st * kWStageBytes +
+           (size_t)(2 * (tp.a_st + tp.w_st + tp.b_st) + 1) * 8 + 16;
 }
 
-size_t tc_smem_bytes(int Mp, int R) {
-    return 1024 + (size_t)R * (kAStageBytes + (size_t)Mp * 128) + (size_t)(3 * R + 1) * 8 + 16;
+// Ring depths within the 227 KB of shared memory one CTA may use: about
+// 48 KB of activation stages (at least 2), then as many decoded-A stages
+// as leave room for 4 weight stages (at most 6), then weight stages.
+void tc_rings(TcParams &tp) {
+    const size_t budget = 227 * 1024;
+    const size_t bst = (size_t)tp.Mp * 128;
+    tp.b_st = (int)(48 * 1024 / bst);
+    tp.b_st = tp.b_st < 2 ? 2 : (tp.b_st > 6 ? 6 : tp.b_st);
+    tp.a_st = 2;
+    tp.w_st = 2;
+    auto fits = [&](int a, int w) {
+        TcParams x = tp;
+        x.a_st = a, x.w_st = w;
+        return tc_smem_bytes(x) <= budget;
+    };
+    for (int a = 6; a >= 2; --a)
+        if (fits(a, 4)) {
+            tp.a_st = a;
+            break;
+        }
+    for (int w = kMaxStages; w >= 2; --w)
+        if (fits(tp.a_st, w)) {
+            tp.w_st = w;
+            break;
+        }
 }
 
 }  // namespace
@@ -471,7 +592,7 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
     if (!enc) return cudaErrorNotSupported;
     TcParams tp;
     tp.Mp = (int)gemm_tc_pad(g.M);
-    tp.stages = tc_stages(tp.Mp);
+    tc_rings(tp);
     tp.tmem_cols = 32;
     while (tp.tmem_cols < tp.Mp) tp.tmem_cols <<= 1;
     tp.idesc = (1u << 4)                         // D: FP32
@@ -493,7 +614,30 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
     } else {
         memset(&map, 0, sizeof map);
     }
-    const size_t smem = tc_smem_bytes(tp.Mp, tp.stages);
+    // The planes as 4-D u8 tensors [stripes][k-blocks][rows of 256 B][256 B].
+    CUtensorMap hmap, lmap;
+    {
+        const cuuint64_t T = (cuuint64_t)(t.Np / 16), KT = (cuuint64_t)(t.KT > 0 ? t.KT : 1);
+        const cuuint32_t e4[4] = {1, 1, 1, 1};
+        const cuuint64_t hd[4] = {256, 4, KT, T}, hs[3] = {256, 1024, KT * 1024};
+        const cuuint32_t hb[4] = {256, 4, 1, 8};
+        const cuuint64_t ld[4] = {256, 2, KT, T}, ls[3] = {256, 512, KT * 512};
+        const cuuint32_t lb[4] = {256, 2, 1, 8};
+        if (t.K > 0) {
+            CUresult r = enc(&hmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(t.hi), hd, hs, hb, e4,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+            r = enc(&lmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(t.lo), ld, ls, lb, e4,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        } else {
+            memset(&hmap, 0, sizeof hmap);
+            memset(&lmap, 0, sizeof lmap);
+        }
+    }
+    const size_t smem = tc_smem_bytes(tp);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -515,7 +659,7 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g.overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc, t, g, tp, map);
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc, t, g, tp, map, hmap, lmap);
 }
 
 }  // namespace w12
