@@ -105,7 +105,7 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lossless_bit_weight_02_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.startswith("w12_gemm_mma") or fn == "w12_device.cuh":
+        if fn.startswith("w12_gemm_mma") or fn in ("w12_device.cuh", "w12_stream.cuh"):
             h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
@@ -385,6 +385,32 @@ def run_gpu(args):
         del stk
         torch.cuda.empty_cache()
 
+    # ---- what a plain device copy reaches at these sizes (context for the roofline) ----
+    # MEASURED_PEAKS' HBM figure is a 2 GiB copy; a copy of one layer's W12 bytes
+    # pays the same launch, ramp-up and tail costs that a single GEMM launch does.
+    size_cal = {}
+    flush_c = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for name, t in layers:
+        nb = t.nbytes()
+        src = torch.empty(nb, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        best = None
+        for _ in range(8):
+            flush_c.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            dst.copy_(src)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        size_cal[name] = {"w12_mb": round(nb / 1e6, 1), "copy_gbs": round(2 * nb / (best * 1e-3) / 1e9, 1)}
+        del src, dst
+    del flush_c
+    torch.cuda.empty_cache()
+    size_cal["method"] = ("torch dst.copy_(src) of the layer's W12 byte count, read+write bytes / best of 8, "
+                          "L2 flushed before each copy")
+
     value = step_bytes * args.steps * ws_n / (total_ms * 1e-3) / 1e9
     e2e_val = step_bytes * e2e_steps * ws_n / (e2e_ms * 1e-3) / 1e9
     top_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers) / launches_per_step
@@ -406,6 +432,7 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
+        "size_calibration": size_cal,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
