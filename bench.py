@@ -382,6 +382,32 @@ def run_gpu(args):
             stack[f"m{M}"] = {"pass_ms": round(ms, 3), "weight_gbs": round(sb / (ms * 1e-3) / 1e9, 1),
                               "roofline_frac": round(sum(algorithmic_bytes(t, M) for t in stk) / (ms * 1e-3) / 1e9
                                                      / hbm_peak, 4)}
+            # the same 256 launches captured once in a CUDA graph (on a side
+            # stream: capture needs one) and replayed
+            gs = torch.cuda.Stream(dev)
+            gcs = [w12.GemmCall(acts_s[t.K], t, outs_s[t.N], wsp, stream=gs, opts=overlap) for t in stk]
+            torch.cuda.synchronize()
+            with torch.cuda.stream(gs):
+                for c in gcs:  # fills the launch caches before capture
+                    c()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gs):
+                for c in gcs:
+                    c()
+            with torch.cuda.stream(gs):
+                graph.replay()
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            a.record(gs)
+            with torch.cuda.stream(gs):
+                for _ in range(reps):
+                    graph.replay()
+            b.record(gs)
+            torch.cuda.synchronize()
+            gms = a.elapsed_time(b) / reps
+            stack[f"m{M}"]["graph"] = {"pass_ms": round(gms, 3), "weight_gbs": round(sb / (gms * 1e-3) / 1e9, 1)}
+            del graph, gcs
         del stk
         torch.cuda.empty_cache()
 

@@ -155,6 +155,24 @@ def test_ranges_across_stripes(N, K, w12lib, oracle):
             assert np.array_equal(o, outs[0])
 
 
+@pytest.mark.parametrize("M", [1, 9])
+def test_ranges_across_stripes_with_many_escapes(M, w12lib, oracle):
+    """Escape-heavy weights (2% of entries far outside the window, zero and
+    denormal rows: groups with more than 32 escapes) on a shape whose
+    stripes are cut by range boundaries (2.3 groups per range)."""
+    N, K = 40003, 600
+    W = synth.adversarial_weights(N, K, seed=96)
+    st, ref = oracle.encode(W)
+    A = synth.activations(M, K, seed=97)
+    st, Yr, Y64, mag = oracle.gemm(A, ref)
+    t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+    Ad = synth.bits_to_tensor(A, "cuda")
+    outs = [synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, opts=w12lib.make_opts(max_ctas=cap))) for cap in (0, 9)]
+    bad = gemm_tolerance_failures(outs[0], Yr, Y64, mag)
+    assert bad.size == 0, bad[:10]
+    assert np.array_equal(outs[0], outs[1])
+
+
 def test_workspace_left_clean_and_reusable(w12lib, oracle):
     """Counters return to zero after each call, so one workspace serves a
     sequence of different shapes."""
