@@ -78,6 +78,8 @@ def _load():
             "w12ref_gemm": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, p, i64, p, i64, p, p]),
             "w12ref_gemm_sample": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, p, i64,
                                                   p, p, i64, p, p, p]),
+            "w12ref_decode_nested8": (ctypes.c_int, [i64, i64, p, p, p, p, i64, p, i64]),
+            "w12ref_gemm_nested8": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, i64, p, i64, p, p]),
             "w12ref_bits_per_weight": (ctypes.c_double, [i64, i64, i64]),
             "w12ref_num_threads": (ctypes.c_int, []),
         }
@@ -254,6 +256,31 @@ def gemm(A: np.ndarray, t: W12Ref):
     mag = np.zeros((M, t.N), np.float64)
     st = _load().w12ref_gemm(_ptr(A), M, t.K, t.N, t.K, *_tensor_args(t), t.n_esc, _ptr(Y), t.N,
                              _ptr(Y64), _ptr(mag))
+    return st, Y, Y64, mag
+
+
+def _nested8_args(t: W12Ref):
+    esc = t.esc if t.esc.size else np.zeros(1, np.uint32)
+    return _ptr(t.hi), _ptr(t.base), _ptr(t.esc_ptr), _ptr(esc)
+
+
+def decode_nested8(t: W12Ref):
+    """The nested 8-bit view as BF16 bits [N,K] (hi plane + base; escapes
+    truncated to 3 mantissa bits).  Returns (status, array)."""
+    out = np.zeros((t.N, t.K), np.uint16)
+    st = _load().w12ref_decode_nested8(t.N, t.K, *_nested8_args(t), t.n_esc, _ptr(out), t.K)
+    return st, out
+
+
+def gemm_nested8(A: np.ndarray, t: W12Ref):
+    """Y = A * V^T with V the nested 8-bit view.  Returns (status, Y, Y64, absdot)."""
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    M = A.shape[0]
+    Y = np.zeros((M, t.N), np.uint16)
+    Y64 = np.zeros((M, t.N), np.float64)
+    mag = np.zeros((M, t.N), np.float64)
+    st = _load().w12ref_gemm_nested8(_ptr(A), M, t.K, t.N, t.K, *_nested8_args(t), t.n_esc, _ptr(Y), t.N,
+                                     _ptr(Y64), _ptr(mag))
     return st, Y, Y64, mag
 
 

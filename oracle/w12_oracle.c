@@ -446,6 +446,87 @@ int w12ref_gemm_sample(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int
     return REF_OK;
 }
 
+/* ---- the nested 8-bit view ----  SpecPilot, section 4.1 and the news
+ * article's "two-level verification": a low-precision pass reads the 8-bit
+ * weight view nested in W12.  The hi byte of a record holds the sign, the
+ * 4-bit exponent offset and the top 3 mantissa bits, so the view of an
+ * in-window weight is (-1)^s * 2^(base+off-127) * (1 + m_hi/8): the BF16
+ * bits s<<15 | (base+off)<<7 | m_hi<<4.  The pages do not say what the view
+ * holds at an escaped position; the reading taken here is the escape's own
+ * BF16 bits with the 4 low mantissa bits cleared (truncation toward zero,
+ * which keeps outliers, zeros, Inf and NaN in their class).  Padding columns
+ * are never read. */
+static uint16_t nested8_value(int hi_byte, int base)
+{
+    int s = (hi_byte >> 7) & 1, off = (hi_byte >> 3) & 15, mh = hi_byte & 7;
+    return (uint16_t)((s << 15) | (((base + off) & 0xFF) << 7) | (mh << 4));
+}
+
+static void decode_row_nested8(int64_t n, int64_t K, int64_t Kp, const uint8_t *hi, const uint8_t *base,
+                               const int32_t *esc_ptr, const uint32_t *esc, uint16_t *row)
+{
+    for (int64_t k = 0; k < K; ++k) row[k] = nested8_value(hi[w12ref_hi_offset(n, k, Kp)], base[n]);
+    int64_t t = n / 16, G = w12ref_groups(K);
+    for (int64_t g = 0; g < G; ++g) {
+        for (int64_t e = esc_ptr[t * G + g]; e < esc_ptr[t * G + g + 1]; ++e) {
+            int64_t rn, rk;
+            key_position(t, g, (int)(esc[e] >> 16), &rn, &rk);
+            if (rn == n) row[rk] = (uint16_t)(esc[e] & 0xFFF0);
+        }
+    }
+}
+
+/* The nested 8-bit view of the whole tensor, [N,K] with row stride ldo. */
+int w12ref_decode_nested8(int64_t N, int64_t K, const uint8_t *hi, const uint8_t *base,
+                          const int32_t *esc_ptr, const uint32_t *esc, int64_t n_esc, uint16_t *out, int64_t ldo)
+{
+    if (N < 0 || K < 0 || ldo < K) return REF_ERR_INVALID;
+    if (w12ref_check_structure(N, K, esc_ptr, esc, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
+    int64_t Kp = w12ref_cols_padded(K);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t n = 0; n < N; ++n) decode_row_nested8(n, K, Kp, hi, base, esc_ptr, esc, out + n * ldo);
+    return REF_OK;
+}
+
+/* Y = A * V^T with V the nested 8-bit view: the same exact FP64 sum in
+ * ascending k, rounded once to BF16, as the GEMM above. */
+int w12ref_gemm_nested8(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int64_t K, const uint8_t *hi,
+                        const uint8_t *base, const int32_t *esc_ptr, const uint32_t *esc, int64_t n_esc,
+                        uint16_t *Y, int64_t ldy, double *Y64, double *absdot)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldy < N) return REF_ERR_INVALID;
+    if (w12ref_check_structure(N, K, esc_ptr, esc, n_esc, n_esc) != 0) return REF_ERR_CORRUPT;
+    int64_t Kp = w12ref_cols_padded(K);
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    if (!a) return REF_ERR_INVALID;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) a[m * K + k] = w12ref_bf16_to_double(A[m * lda + k]);
+#pragma omp parallel
+    {
+        uint16_t *row = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(K > 0 ? K : 1));
+        double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t n = 0; n < N; ++n) {
+            decode_row_nested8(n, K, Kp, hi, base, esc_ptr, esc, row);
+            for (int64_t k = 0; k < K; ++k) w[k] = w12ref_bf16_to_double(row[k]);
+            for (int64_t m = 0; m < M; ++m) {
+                double acc = 0.0, mag = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    acc += a[m * K + k] * w[k];
+                    mag += fabs(a[m * K + k]) * fabs(w[k]);
+                }
+                Y[m * ldy + n] = w12ref_bf16_from_double(acc);
+                if (Y64) Y64[m * N + n] = acc;
+                if (absdot) absdot[m * N + n] = mag;
+            }
+        }
+        free(row);
+        free(w);
+    }
+    free(a);
+    return REF_OK;
+}
+
 /* Storage cost in bits per weight, counting everything the tensor stores:
  * both planes (with padding), the bases, the group offsets and the escapes
  * (one 32-bit entry each). */
