@@ -306,6 +306,41 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
+    # ---- the nested 8-bit view (W12_GEMM_NESTED8): the same GEMMs reading the hi plane only ----
+    nested = {}
+    for M in (1, 16, 64):
+        row = {}
+        for label, flags in (("exact", w12.W12_GEMM_OVERLAP_PREVIOUS),
+                             ("nested8", w12.W12_GEMM_OVERLAP_PREVIOUS | w12.W12_GEMM_NESTED8)):
+            o = w12.make_opts(flags=flags)
+            xs = {K: synth.activations_device(M, K, seed=5000 + M + K, device=dev) for _, _, K in synth.LAYER_SHAPES}
+            ys = {N: torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _, N, _ in synth.LAYER_SHAPES}
+            wsp.ensure(max(w12.w12_gemm_workspace_bytes(M, t.N, t.K, o) for _, t in layers))
+            cs = [w12.GemmCall(xs[t.K], t, ys[t.N], wsp, stream=stream, opts=o) for _, t in layers]
+            for c in cs:
+                c()
+            torch.cuda.synchronize()
+            reps = 50
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                for c in cs:
+                    c()
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / reps
+            # bytes each pass must read: the hi plane (and the lo plane for the exact pass), bases,
+            # group offsets, escapes, activations and outputs
+            rd = sum(t.hi.numel() + (0 if label == "nested8" else t.lo.numel()) + t.base.numel() +
+                     4 * t.esc_ptr.numel() + 4 * t.n_esc + 2 * M * t.K + 2 * M * t.N for _, t in layers)
+            row[label] = {"us_per_4_layers": round(us, 2), "gbs_read": round(rd / (us * 1e-6) / 1e9, 1),
+                          "roofline_frac": round(rd / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+            del cs, xs, ys
+        row["speedup"] = round(row["exact"]["us_per_4_layers"] / row["nested8"]["us_per_4_layers"], 3)
+        nested[str(M)] = row
+    nested["note"] = ("four layer GEMMs per round, 50 rounds back to back (PDL on); nested8 reads the hi plane "
+                      "only (1 B/weight vs 1.5)")
+
     # ---- codec throughput on the config-1 layer (rows a1-a5): encode, decode, verify ----
     codec = {}
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -458,7 +493,7 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
-        "size_calibration": size_cal,
+        "size_calibration": size_cal, "nested8": nested,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

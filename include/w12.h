@@ -102,8 +102,21 @@ typedef struct {
  * back-to-back GEMMs over resident weights (a model's forward pass). */
 #define W12_GEMM_OVERLAP_PREVIOUS 1
 
+/* W12_GEMM_NESTED8: multiply by the 8-bit view nested in W12 instead of the
+ * exact weights (SpecPilot, section 4.1, and the two-level verification of
+ * the news article: a low-precision pass reads "the 8-bit weight view nested
+ * in W12").  Only the hi plane is read (1 byte per weight instead of 1.5):
+ * an in-window weight becomes (-1)^s * 2^(base+off-127) * (1 + m_hi/8), its
+ * top 3 mantissa bits.  The pages do not say what the view holds at an
+ * escaped position; this library uses the escape's BF16 bits with the 4 low
+ * mantissa bits cleared.  So every weight w is replaced by w & 0xFFF0
+ * (truncation toward zero).  Accumulation, rounding and determinism are as
+ * for the exact GEMM. */
+#define W12_GEMM_NESTED8 2
+
 /* Options of w12_gemm (NULL = all defaults).  Results are bitwise identical
- * for any max_ctas and flags; they depend only on (M, N, K, path, split_k). */
+ * for any max_ctas and with or without W12_GEMM_OVERLAP_PREVIOUS; they depend
+ * only on (M, N, K, path, split_k, W12_GEMM_NESTED8). */
 typedef struct {
     int32_t max_ctas;       /* 0 = as many as fit; >0 caps the grid (tests) */
     int32_t split_k;        /* 0 = chosen from (M,N,K); >0 forces the split */

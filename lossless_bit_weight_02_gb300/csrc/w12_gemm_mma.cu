@@ -91,13 +91,13 @@ __device__ __forceinline__ void stage_group(uint32_t dst, const uint16_t *__rest
 // Writes escape `ent` (key<<16 | bits) into the per-warp copy of the A
 // fragments: slot = 4*(row%8) + col/16, component (pair&1)*2 + row/8,
 // half = col&1.
-__device__ __forceinline__ void patch_one(uint4 (*patch)[32], uint32_t ent) {
+__device__ __forceinline__ void patch_one(uint4 (*patch)[32], uint32_t ent, uint32_t vmask) {
     const int key = (int)(ent >> 16);
     const int r = (key >> 6) & 15, j = key & 63;
     const int slot = (r & 7) * 4 + (j >> 4);
     const int j16 = j & 15, pr = j16 >> 1;
     const int comp = (pr & 1) * 2 + (r >> 3);
-    reinterpret_cast<uint16_t *>(&patch[pr >> 1][slot])[comp * 2 + (j16 & 1)] = (uint16_t)(ent & 0xFFFFu);
+    reinterpret_cast<uint16_t *>(&patch[pr >> 1][slot])[comp * 2 + (j16 & 1)] = (uint16_t)(ent & vmask);
 }
 
 // Per-warp streaming state of one work item.
@@ -117,8 +117,10 @@ struct Stream {
 // activations (column group gnext), then for each of the 4 tiles read the B
 // fragments from shared memory, decode the two rows, prefetch the same tile
 // of the next unit (or, on the last unit, the same tile again: an L2 hit),
-// patch the tile's escapes and run the MMAs.
-template <int NB>
+// patch the tile's escapes and run the MMAs.  Q: the nested 8-bit view (the
+// lo plane is neither loaded nor used; escape values lose their 4 low
+// mantissa bits).
+template <int NB, bool Q>
 __device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, const GemmArgs &g, int u,
                                            int gnext, bool more, uint4 (*patch)[32], uint8_t *pw, int lane,
                                            int rows, uint32_t act, const unsigned char *actp, uint32_t frag,
@@ -142,11 +144,16 @@ __device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, c
             bw[b][4] = v1.x; bw[b][5] = v1.y; bw[b][6] = v1.z; bw[b][7] = v1.w;
         }
         uint32_t dA[8], dB[8];
-        decode16_fma(w.bh0[p], w.bl[p].x, w.bl[p].y, w.base2A, c28, c16, dA);
-        decode16_fma(w.bh1[p], w.bl[p].z, w.bl[p].w, w.base2B, c28, c16, dB);
+        if (Q) {
+            decode16_fma(w.bh0[p], 0u, 0u, w.base2A, c28, c16, dA);
+            decode16_fma(w.bh1[p], 0u, 0u, w.base2B, c28, c16, dB);
+        } else {
+            decode16_fma(w.bh0[p], w.bl[p].x, w.bl[p].y, w.base2A, c28, c16, dA);
+            decode16_fma(w.bh1[p], w.bl[p].z, w.bl[p].w, w.base2B, c28, c16, dB);
+        }
         w.bh0[p] = ld_stream(w.hp + next + p * 64);
         w.bh1[p] = ld_stream(w.hp + next + p * 64 + 32);
-        w.bl[p] = ld_stream(w.lp + nextl + p * 32);
+        if (!Q) w.bl[p] = ld_stream(w.lp + nextl + p * 32);
 
         // Escapes of this tile replace the decoded placeholders.
         if ((w.emask >> p) & 1u) {
@@ -161,7 +168,7 @@ __device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, c
             } else {  // more than 32 escapes in the group: walk it in batches
                 for (int b0 = 0; b0 < w.cur.cnt; b0 += 32) {
                     const uint32_t e = (b0 + lane < w.cur.cnt) ? __ldg(t.esc + w.cur.p0 + b0 + lane) : 0u;
-                    if (b0 + lane < w.cur.cnt && (int)(e >> 26) == p) patch_one(patch, e);
+                    if (b0 + lane < w.cur.cnt && (int)(e >> 26) == p) patch_one(patch, e, Q ? 0xFFF0u : 0xFFFFu);
                 }
             }
             __syncwarp();
@@ -189,7 +196,7 @@ __device__ __forceinline__ void group_step(Stream<NB> &w, const TensorView &t, c
 // This lane's escape of the current group (at most one while the group holds
 // <= 32): its tile, its byte in the per-warp fragment copy (slot
 // 4*(row%8)+col/16, component (pair&1)*2+row/8, half col&1), its bits.
-template <int NB>
+template <int NB, bool Q>
 __device__ __forceinline__ void own_escape(Stream<NB> &w, int lane) {
     w.emask = escape_tiles(w.cur, lane);
     w.e_tile = 4;
@@ -200,7 +207,7 @@ __device__ __forceinline__ void own_escape(Stream<NB> &w, int lane) {
         const uint32_t comp = (pr & 1) * 2 + (r >> 3);
         w.e_tile = key >> 10;
         w.e_off = ((pr >> 1) * 32 + slot) * 16 + comp * 4 + (j16 & 1) * 2;
-        w.e_val = (uint16_t)(w.cur.ent & 0xFFFFu);
+        w.e_val = (uint16_t)(w.cur.ent & (Q ? 0xFFF0u : 0xFFFFu));
     }
 }
 
@@ -223,7 +230,7 @@ __device__ __forceinline__ int range_of(int u, const GemmArgs &g) {
     return seg * g.per + j;
 }
 
-template <int NB>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16)
+template <int NB, bool Q>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16); Q: nested 8-bit view
 __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(TensorView t, GemmArgs g) {
     // [kWarps][4][32] uint4 escape-patch copies, then [kWarps][2][8*NB][kActPitch] activations
     extern __shared__ __align__(16) unsigned char smem[];
@@ -260,7 +267,7 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
         for (int p = 0; p < 4; ++p) {
             w.bh0[p] = ld_stream(w.hp + p * 64);
             w.bh1[p] = ld_stream(w.hp + p * 64 + 32);
-            w.bl[p] = ld_stream(w.lp + p * 32);
+            if (!Q) w.bl[p] = ld_stream(w.lp + p * 32);
         }
         // 2. the first stripe's bases, escape offsets (lane l holds the
         //    offset of unit u0 + iw0 + l), escapes of the first two units
@@ -315,7 +322,7 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
         // every lane is done with the buffers of this warp's previous range
         __syncwarp();
         stage_group<NB>(act + (uint32_t)(u0 & 1) * act_buf_bytes<NB>(), g.A, g.lda, rows, gi, t.K, lane);
-        own_escape(w, lane);
+        own_escape<NB, Q>(w, lane);
 
         // Arrival counts still to be read: lane 0's count for the range's
         // first piece when later units follow (-1: none; its stripe is the
@@ -333,14 +340,14 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
             for (int b = 0; b < NB; ++b) w.acc[b][0] = w.acc[b][1] = w.acc[b][2] = w.acc[b][3] = 0.f;
             for (; i < pe; ++i) {
                 const bool more = i + 1 < nu;
-                group_step<NB>(w, t, g, u0 + i, gi + 1 == G ? 0 : gi + 1, more, patch[warp], pw, lane, rows, act,
+                group_step<NB, Q>(w, t, g, u0 + i, gi + 1 == G ? 0 : gi + 1, more, patch[warp], pw, lane, rows, act,
                                actp, frag, c28, c16);
                 w.hp += 256;
                 w.lp += 128;
                 ++gi;
                 // the next unit's escapes are already in flight; fetch the one after
                 w.cur = nxt;
-                if (more) own_escape(w, lane);
+                if (more) own_escape<NB, Q>(w, lane);
                 if (i + 2 < nu) {
                     unit_bounds(i + 2, p0, p1);
                     nxt = load_group_escapes(t, p0, p1, lane);
@@ -442,7 +449,7 @@ __global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(Tenso
 
 struct LaunchCache {
     int sms = 0;
-    int occ[3] = {0, 0, 0};
+    int occ[3][2] = {};
 };
 
 LaunchCache &cache_for_device(int dev) {
@@ -450,7 +457,7 @@ LaunchCache &cache_for_device(int dev) {
     return caches[dev & 63];
 }
 
-template <int NB>
+template <int NB, bool Q>
 cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -462,16 +469,17 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         lc.sms = sms;
     }
-    if (lc.occ[NB] == 0) {
+    int &occ_slot = lc.occ[NB][Q ? 1 : 0];
+    if (occ_slot == 0) {
         int occ = 0;
-        e = cudaFuncSetAttribute(k_gemm_mma<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NB>());
+        e = cudaFuncSetAttribute(k_gemm_mma<NB, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NB>());
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_gemm_mma<NB>, kWarps * 32, smem_bytes<NB>());
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_gemm_mma<NB, Q>, kWarps * 32, smem_bytes<NB>());
         if (e != cudaSuccess) return e;
-        lc.occ[NB] = occ > 0 ? occ : 1;
+        occ_slot = occ > 0 ? occ : 1;
     }
     int64_t blocks = (g.ranges + kWarps - 1) / kWarps;
-    const int64_t resident = (int64_t)lc.sms * lc.occ[NB];
+    const int64_t resident = (int64_t)lc.sms * occ_slot;
     if (blocks > resident) blocks = resident;
     if (g.max_ctas > 0 && blocks > g.max_ctas) blocks = g.max_ctas;
     if (blocks < 1) blocks = 1;
@@ -485,7 +493,7 @@ cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g.overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_gemm_mma<NB>, t, g);
+    return cudaLaunchKernelEx(&cfg, k_gemm_mma<NB, Q>, t, g);
 }
 
 }  // namespace
@@ -531,8 +539,8 @@ int64_t gemm_mma_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counter
 }
 
 cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
-    if (g.M <= 8) return launch_nb<1>(t, g, s);
-    return launch_nb<2>(t, g, s);
+    if (g.nested8) return g.M <= 8 ? launch_nb<1, true>(t, g, s) : launch_nb<2, true>(t, g, s);
+    return g.M <= 8 ? launch_nb<1, false>(t, g, s) : launch_nb<2, false>(t, g, s);
 }
 
 }  // namespace w12

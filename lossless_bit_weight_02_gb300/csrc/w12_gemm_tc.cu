@@ -52,7 +52,7 @@ constexpr int kMmaWarp = 18;      // issues the MMAs
 constexpr int kThreads = 32 * (kDecWarps + 3);
 constexpr uint32_t kAStageBytes = 128 * 128;   // decoded A: 128 rows x 64 BF16, swizzled
 constexpr uint32_t kWStageBytes = 8 * 1536;    // the 8 stripes of a row tile, one k-block: 8 KB hi, 4 KB lo
-constexpr int kMaxStages = 8;    // per ring
+constexpr int kMaxStages = 12;   // per ring
 constexpr int kSuspendNs = 20000;               // longest sleep of one try_wait
 constexpr long long kWaitPolls = 1LL << 16;    // try_waits before a wait gives up (~1.3 s)
 
@@ -263,6 +263,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         const bool live = st < T;  // warp-uniform
         const int rA = 16 * sw + gid, rB = rA + 8;
         const uint32_t c28 = g.c28, c16 = g.c16;
+        const uint32_t vmask = g.nested8 ? 0xFFF0u : 0xFFFFu;  // escape bits kept
         uint32_t base2A = 0, base2B = 0;
         EscBatch cur, nxt;
         cur.cnt = nxt.cnt = 0;
@@ -336,7 +337,8 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
             if (live) {
                 const uint8_t *W = w_st + ws * kWStageBytes;
                 const uint4 h0 = lds128(W + sw * 1024 + lane * 16), h1 = lds128(W + sw * 1024 + 512 + lane * 16);
-                const uint4 l = lds128(W + 8192 + sw * 512 + lane * 16);
+                // the nested 8-bit view reads no lo plane: records with zero low nibbles
+                const uint4 l = g.nested8 ? make_uint4(0u, 0u, 0u, 0u) : lds128(W + 8192 + sw * 512 + lane * 16);
                 decode16_fma(h0, l.x, l.y, base2A, c28, c16, dA);
                 decode16_fma(h1, l.z, l.w, base2B, c28, c16, dB);
             }
@@ -357,7 +359,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
                     auto put = [&](uint32_t e) {
                         const int key = (int)(e >> 16);
                         const int r = 16 * sw + ((key >> 6) & 15), j = key & 63;
-                        *reinterpret_cast<uint16_t *>(A + swz(r, j >> 3) + (j & 7) * 2) = (uint16_t)(e & 0xFFFFu);
+                        *reinterpret_cast<uint16_t *>(A + swz(r, j >> 3) + (j & 7) * 2) = (uint16_t)(e & vmask);
                     };
                     if (cur.cnt <= 32) {
                         if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
@@ -452,11 +454,11 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
             if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) break;
             if (elect_one()) {
                 // the full box is counted, out-of-range stripes included (zero-filled)
-                mbar_expect_tx(&w_full[ws], kWStageBytes);
+                mbar_expect_tx(&w_full[ws], g.nested8 ? 8192u : kWStageBytes);
                 uint8_t *dst = w_st + ws * kWStageBytes;
                 const int kbg = (int)(4 * g_beg) + kb, st0 = (int)(tt * 8);
                 tma_load_4d(dst, &hmap, kbg, st0, &w_full[ws]);
-                tma_load_4d(dst + 8192, &lmap, kbg, st0, &w_full[ws]);
+                if (!g.nested8) tma_load_4d(dst + 8192, &lmap, kbg, st0, &w_full[ws]);
             }
             __syncwarp();
             ++issued;
@@ -542,8 +544,9 @@ size_t tc_smem_bytes(const TcParams &tp) {
 }
 
 // Ring depths within the 227 KB of shared memory one CTA may use: about
-// 48 KB of activation stages (at least 2), then as many decoded-A stages
-// as leave room for 4 weight stages (at most 6), then weight stages.
+// 48 KB of activation stages (at least 2), 3 decoded-A stages, and the rest
+// for weight stages: the weight ring is what keeps HBM busy (a k-block's
+// planes take a few microseconds to arrive under load).
 void tc_rings(TcParams &tp) {
     const size_t budget = 227 * 1024;
     const size_t bst = (size_t)tp.Mp * 128;
@@ -556,11 +559,7 @@ void tc_rings(TcParams &tp) {
         x.a_st = a, x.w_st = w;
         return tc_smem_bytes(x) <= budget;
     };
-    for (int a = 6; a >= 2; --a)
-        if (fits(a, 4)) {
-            tp.a_st = a;
-            break;
-        }
+    tp.a_st = 3;
     for (int w = kMaxStages; w >= 2; --w)
         if (fits(tp.a_st, w)) {
             tp.w_st = w;

@@ -74,7 +74,7 @@ def test_gemm_workspace_query(w12lib):
     nb = w12lib.w12_gemm_workspace_bytes(40, 1024, 4096, o)
     S, rem = divmod(nb - 256 - 4 * 65536, 48 * 1024 * 4)
     assert rem == 0 and S >= 2
-    bad = w12lib.GemmOpts(0, 0, 0, 2)  # unknown flag bit
+    bad = w12lib.GemmOpts(0, 0, 0, 4)  # unknown flag bit
     assert w12lib.w12_gemm_workspace_bytes(1, 64, 64, bad) == 0
 
 
