@@ -114,6 +114,15 @@ typedef struct {
  * for the exact GEMM. */
 #define W12_GEMM_NESTED8 2
 
+/* W12_GEMM_TEST_STALL (tests only): on the tensor-core path (M > 16) one
+ * wait of the kernel waits for an event that never comes.  Every wait of the
+ * kernel is bounded (about a second), so the wait gives up, the CTA aborts,
+ * drains its own copies and MMAs, frees its TMEM and records the failure in
+ * the workspace error word: the call completes, Y is unspecified and
+ * w12_gemm_workspace_status reports W12_ERR_TIMEOUT.  No effect on the
+ * small-M path, which has no waits. */
+#define W12_GEMM_TEST_STALL (1 << 30)
+
 /* Options of w12_gemm (NULL = all defaults).  Results are bitwise identical
  * for any max_ctas and with or without W12_GEMM_OVERLAP_PREVIOUS; they depend
  * only on (M, N, K, path, split_k, W12_GEMM_NESTED8). */

@@ -39,6 +39,7 @@ W12_ERR_UNSUPPORTED = -8
 W12_PATH_AUTO, W12_PATH_MMA, W12_PATH_TC = 0, 1, 2
 W12_GEMM_OVERLAP_PREVIOUS = 1
 W12_GEMM_NESTED8 = 2  # multiply by the nested 8-bit view (hi plane only)
+W12_GEMM_TEST_STALL = 1 << 30  # tests only: one wait of the tensor-core kernel runs out
 
 # Every symbol include/w12.h declares.
 EXPORTS = (

@@ -64,7 +64,8 @@ int choose_path(int64_t M, const w12_gemm_opts *o) {
 
 w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, GemmPlan &pl) {
     if (M < 0 || N < 0 || K < 0 || N > kMaxN || K > kMaxK) return W12_ERR_INVALID;
-    if (o && ((o->flags & ~(W12_GEMM_OVERLAP_PREVIOUS | W12_GEMM_NESTED8)) != 0 || o->max_ctas < 0 || o->split_k < 0 ||
+    if (o && ((o->flags & ~(W12_GEMM_OVERLAP_PREVIOUS | W12_GEMM_NESTED8 | W12_GEMM_TEST_STALL)) != 0 ||
+              o->max_ctas < 0 || o->split_k < 0 ||
               o->split_k > 256))
         return W12_ERR_INVALID;
     pl.path = choose_path(M, o);
@@ -239,6 +240,7 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     g.max_ctas = opts ? opts->max_ctas : 0;
     g.overlap = opts ? (opts->flags & W12_GEMM_OVERLAP_PREVIOUS) != 0 : false;
     g.nested8 = opts ? (opts->flags & W12_GEMM_NESTED8) != 0 : false;
+    g.test_stall = opts ? (opts->flags & W12_GEMM_TEST_STALL) != 0 : false;
     g.error = reinterpret_cast<int32_t *>(ws);
     g.counters = reinterpret_cast<int32_t *>(ws + pl.counters_off);
     g.partials = reinterpret_cast<float *>(ws + pl.partials_off);

@@ -116,6 +116,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     return false;
 }
 
+// Bounded wait that does not give up when the CTA aborts: for work already
+// handed to the asynchronous units (TMA copies, MMAs), which must finish
+// before the CTA may free its shared memory and TMEM.  Returns false (and
+// raises the error word) only when the limit runs out.
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity, int32_t *err) {
+    for (long long i = 0; i < kWaitPolls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicExch(err, 1);
+    return false;
+}
+
 // true on one lane of the (converged) warp
 __device__ __forceinline__ bool elect_one() {
     uint32_t r;
@@ -380,7 +391,8 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         // Epilogue: TMEM lanes 32*(warp%4).. ; the four warps w, w+4, w+8,
         // w+12 split the 16-column chunks.
         // ------------------------------------------------------------------
-        const bool fin = __all_sync(kFull, mbar_wait(done, 0, abort_flag, g.error));
+        // every MMA issued has completed (also after an abort: TMEM is freed below)
+        const bool fin = __all_sync(kFull, mbar_drain(done, 0, g.error));
         tc_fence_after();
         const int quarter = warp & 3, half = warp >> 2;  // half: 0..3
         const int64_t n = tt * 128 + 32 * quarter + lane;
@@ -465,7 +477,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         }
         // the copies issued last must have landed before the CTA exits
         for (int i = issued > RW ? issued - RW : 0; i < issued; ++i)
-            mbar_wait(&w_full[i % RW], (uint32_t)((i / RW) & 1), abort_flag, g.error);
+            mbar_drain(&w_full[i % RW], (uint32_t)((i / RW) & 1), g.error);
     } else if (warp == kBProdWarp) {
         // ------------------------------------------------------------------
         // Activations: one TMA tile [Mp x 64] per k-block.
@@ -485,12 +497,14 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         }
         // the copies issued last must have landed before the CTA exits
         for (int i = issued > RB ? issued - RB : 0; i < issued; ++i)
-            mbar_wait(&b_full[i % RB], (uint32_t)((i / RB) & 1), abort_flag, g.error);
+            mbar_drain(&b_full[i % RB], (uint32_t)((i / RB) & 1), g.error);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------
         // MMA issue (one thread).
         // ------------------------------------------------------------------
         // The whole warp runs the loop; one elected lane issues the MMAs.
+        if (g.test_stall)  // a wait that nothing completes: it runs out and aborts the CTA
+            (void)__all_sync(kFull, mbar_wait(done, 0, abort_flag, g.error));
         RingPos ap, bp;
         for (int kb = 0; kb < nkb; ++kb, ap.advance(1, RA), bp.advance(1, RB)) {
             const int as = ap.stage, bs = bp.stage;

@@ -60,6 +60,7 @@ struct GemmArgs {
     int max_ctas;        // 0 = occupancy-limited persistent grid
     bool overlap;        // launch as a programmatic dependent of the previous kernel
     bool nested8;        // multiply by the nested 8-bit view (hi plane only, escapes & 0xFFF0)
+    bool test_stall;     // tensor-core path: make one bounded wait run out (tests of the timeout path)
     float *partials;     // tensor-core path: [S][Mpad][Np]; small-M path: [2*ranges][16][MP] fp32
     int32_t *counters;   // [Np/16] arrival counters (S > 1)
     int32_t *error;      // device error word

@@ -1,0 +1,41 @@
+"""The bounded waits of the tensor-core GEMM, made to run out on purpose.
+
+Every mbarrier wait in the tcgen05 kernel is bounded (about a second).  With
+W12_GEMM_TEST_STALL one wait of the MMA warp waits for an event that never
+comes: it gives up, the CTA aborts, drains its own copies and MMAs, frees its
+TMEM and records the failure in the workspace error word.  The call returns,
+w12_gemm_workspace_status reports W12_ERR_TIMEOUT (and clears it), the
+workspace counters stay clean, and the next normal call on the same context
+gives the right result.  Nothing here traps or faults the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+from lossless_bit_weight_02_gb300 import synth
+from w12_tol import gemm_tolerance_failures
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N,K", [(1024, 1024), (1024, 8192)])  # one K-chunk, and a split of the reduction
+def test_stalled_wait_reports_timeout_and_the_context_stays_usable(N, K, w12lib, oracle):
+    M = 32
+    W = synth.dense_weights(N, K, seed=150 + K)
+    A = synth.activations(M, K, seed=151)
+    t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+    Ad = synth.bits_to_tensor(A, "cuda")
+    ws = w12lib.Workspace("cuda", 1 << 22)
+
+    w12lib.w12_gemm(Ad, t, workspace=ws, opts=w12lib.make_opts(flags=w12lib.W12_GEMM_TEST_STALL))
+    torch.cuda.synchronize()
+    assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_ERR_TIMEOUT
+    assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_OK  # read and cleared
+    assert int(ws.buf[256:256 + 4 * 64].sum()) == 0  # no arrival counter left behind
+
+    st, ref = oracle.encode(W)
+    st, Yr, Y64, mag = oracle.gemm(A, ref)
+    Y = synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, workspace=ws))
+    torch.cuda.synchronize()
+    assert gemm_tolerance_failures(Y, Yr, Y64, mag).size == 0
+    assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_OK
