@@ -4,11 +4,15 @@
 // registers and splits its reduction in a fixed order).
 //
 // One CTA owns 128 weight rows (8 stripes of 16) and a chunk of whole
-// 256-column groups; per 64-column k-block:
+// 256-column groups.  Two builds of the kernel: one CTA per SM with 16
+// decoder warps (two per stripe), or two CTAs per SM with 8 decoder warps
+// (one per stripe) each; the second wins when the grid holds enough CTAs to
+// fill 2 x 152 slots.  Per 64-column k-block:
 //   * a weight-producer warp fetches the 8 tiles of the k-block (12 KB of
 //     W12 planes) with two tiled TMA copies (the planes seen as 4-D u8
 //     tensors), up to a whole ring of k-blocks ahead of the decoders;
-//   * 16 decoder warps (two per stripe, even / odd k-blocks) read their
+//   * the decoder warps (one or two per stripe, taking every k-block, or
+//     the even / odd ones) read their
 //     tile from that ring (the fragment-native order makes this three
 //     conflict-free 16-byte loads per lane), decode it in registers and
 //     store it as BF16 into the UMMA A operand: 128 rows x 128 bytes,
@@ -27,9 +31,9 @@
 // tcgen05.ld.  With a split of S > 1 the chunk partials go to the FP32
 // workspace and the last CTA of a row tile adds them in the order
 // s = 0..S-1; S depends only on (M, N, K).
-// Every mbarrier wait is bounded (try_wait with a suspend hint, so waiting
-// warps take no issue slots): on expiry the CTA records W12_ERR_TIMEOUT in
-// the workspace error word, waits (bounded) for its own copies and MMAs, and
+// Every mbarrier wait is bounded in time (about a second, read from the
+// global nanosecond timer): on expiry the CTA records W12_ERR_TIMEOUT in the
+// workspace error word, waits (bounded) for its own copies and MMAs, and
 // frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -45,16 +49,29 @@
 namespace w12 {
 namespace {
 
-constexpr int kDecWarps = 16;     // two per 16-row stripe (even / odd k-blocks)
-constexpr int kWProdWarp = 16;    // streams the weight planes (and owns TMEM)
-constexpr int kBProdWarp = 17;    // streams the activations
-constexpr int kMmaWarp = 18;      // issues the MMAs
-constexpr int kThreads = 32 * (kDecWarps + 3);
+// Warp roles of a CTA with D decoder warps (D = 16: two per 16-row stripe,
+// even / odd k-blocks, one CTA per SM; D = 8: one per stripe, two CTAs per
+// SM): warps 0..D-1 decode, D streams the weight planes (and owns TMEM),
+// D+1 streams the activations, D+2 issues the MMAs.
+template <int D>
+struct Roles {
+    static constexpr int kDecWarps = D;
+    static constexpr int kPar = D / 8;          // decoder warps per stripe
+    static constexpr int kCtasPerSm = 16 / D;
+    static constexpr int kWProdWarp = D;
+    static constexpr int kBProdWarp = D + 1;
+    static constexpr int kMmaWarp = D + 2;
+    static constexpr int kThreads = 32 * (D + 3);
+};
 constexpr uint32_t kAStageBytes = 128 * 128;   // decoded A: 128 rows x 64 BF16, swizzled
 constexpr uint32_t kWStageBytes = 8 * 1536;    // the 8 stripes of a row tile, one k-block: 8 KB hi, 4 KB lo
 constexpr int kMaxStages = 12;   // per ring
-constexpr int kSuspendNs = 20000;               // longest sleep of one try_wait
-constexpr long long kWaitPolls = 1LL << 16;    // try_waits before a wait gives up (~1.3 s)
+constexpr uint64_t kWaitNs = 1000000000ull;    // a wait gives up after ~1 s ...
+constexpr long long kWaitPollCap = 1LL << 28;  // ... or after this many polls, whichever comes first
+// A grid of at least this many CTAs takes the two-CTAs-per-SM build (about
+// 85% of its 2 x 152 slots); measured on GB300, smaller grids ran faster with
+// 16 decoder warps per CTA.
+constexpr int64_t kTwoPerSmMinCtas = 258;
 
 struct TcParams {
     int Mp;                // tokens padded to a multiple of 16 (UMMA N)
@@ -91,25 +108,38 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
 }
-// try_wait suspends the thread (no issue slots spent) until the phase
-// completes or kSuspendNs elapse, whichever comes first.
+// try_wait without a time hint: returns when the phase completes or after
+// a short, hardware-chosen time.  (A suspend-time hint made every wait a few
+// percent slower on GB300: the thread wakes later after the phase flips.)
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
+        : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Bounded wait for the completion of phase `parity`.  Gives up (returns
-// false) when another thread of the CTA has given up, or after kWaitPolls
-// polls, in which case it raises the CTA's abort flag and the error word.
+// false) when another thread of the CTA has given up, or after kWaitNs (or
+// kWaitPollCap polls), in which case it raises the CTA's abort flag and the
+// error word.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
-    for (long long i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (long long i = 1; i < kWaitPollCap; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15) == 15 && *abort_flag) return false;
+        if ((i & 15) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitNs) break;
+        }
     }
     *abort_flag = 1;
     atomicExch(err, 1);
@@ -121,8 +151,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // before the CTA may free its shared memory and TMEM.  Returns false (and
 // raises the error word) only when the limit runs out.
 __device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity, int32_t *err) {
-    for (long long i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (long long i = 1; i < kWaitPollCap; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15) == 0 && global_ns() - t0 > kWaitNs) break;
+    }
     atomicExch(err, 1);
     return false;
 }
@@ -200,10 +234,13 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
 // hmap / lmap: the hi / lo plane as u8 [stripes][k-blocks][4 or 2][256], box
 // [8 stripes][1 k-block][4 or 2][256]: one copy brings the row tile's 8
 // tiles of a k-block (stripes past the end read as zero).
-__global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs g, TcParams tp,
-                                                         const __grid_constant__ CUtensorMap tmap,
-                                                         const __grid_constant__ CUtensorMap hmap,
-                                                         const __grid_constant__ CUtensorMap lmap) {
+template <int D>
+__global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_gemm_tc(
+    TensorView t, GemmArgs g, TcParams tp, const __grid_constant__ CUtensorMap tmap,
+    const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap lmap) {
+    using R = Roles<D>;
+    constexpr int kDecWarps = R::kDecWarps, kPar = R::kPar;
+    constexpr int kWProdWarp = R::kWProdWarp, kBProdWarp = R::kBProdWarp, kMmaWarp = R::kMmaWarp;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned, by an offset so that the compiler keeps the
     // shared address space (ld.shared / st.shared, not generic accesses)
@@ -235,10 +272,10 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RW; ++i) {
             mbar_init(&w_full[i], 1);                // the producer's expect_tx
-            mbar_init(&w_empty[i], kDecWarps / 2);   // one arrival per decoder warp of the k-block
+            mbar_init(&w_empty[i], 8);   // one arrival per stripe's decoder warp of the k-block
         }
         for (int i = 0; i < RA; ++i) {
-            mbar_init(&a_full[i], kDecWarps / 2);
+            mbar_init(&a_full[i], 8);
             mbar_init(&a_empty[i], 1);               // tcgen05.commit
         }
         for (int i = 0; i < RB; ++i) {
@@ -263,10 +300,11 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
 
     if (warp < kDecWarps) {
         // ------------------------------------------------------------------
-        // Decoders: warp w handles stripe st = 8*tt + (w%8) on the k-blocks
-        // of parity w/8 (tiles p = w/8 and w/8 + 2 of every group): the
-        // tile's planes come from the weight ring, the BF16 tile goes to the
-        // A ring (K-major, 128-byte swizzle), escapes over their slots.
+        // Decoders: warp w handles stripe st = 8*tt + (w%8) on every k-block
+        // (8 decoder warps) or on the k-blocks of parity w/8 (16 warps:
+        // tiles p = w/8 and w/8 + 2 of every group): the tile's planes come
+        // from the weight ring, the BF16 tile goes to the A ring (K-major,
+        // 128-byte swizzle), escapes over their slots.
         // ------------------------------------------------------------------
         const int gid = lane >> 2, q = lane & 3;
         const int sw = warp & 7, par = warp >> 3;
@@ -324,7 +362,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         RingPos wp, ap;  // ring positions of k-block kb
         wp.advance(par, RW);
         ap.advance(par, RA);
-        for (int kb = par; kb < nkb && ok; kb += 2, wp.advance(2, RW), ap.advance(2, RA)) {
+        for (int kb = par; kb < nkb && ok; kb += kPar, wp.advance(kPar, RW), ap.advance(kPar, RA)) {
             const int p = kb & 3;  // tile of the group
             if (kb >= 4 && p == par && live) {  // first tile of a new group for this warp
                 const int64_t gg = g_beg + (kb >> 2);
@@ -388,18 +426,18 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
         }
 
         // ------------------------------------------------------------------
-        // Epilogue: TMEM lanes 32*(warp%4).. ; the four warps w, w+4, w+8,
-        // w+12 split the 16-column chunks.
+        // Epilogue: TMEM lanes 32*(warp%4).. ; the warps w, w+4, ... (two or
+        // four of them) split the 16-column chunks.
         // ------------------------------------------------------------------
         // every MMA issued has completed (also after an abort: TMEM is freed below)
         const bool fin = __all_sync(kFull, mbar_drain(done, 0, g.error));
         tc_fence_after();
-        const int quarter = warp & 3, half = warp >> 2;  // half: 0..3
+        const int quarter = warp & 3, half = warp >> 2;  // half: 0 .. kDecWarps/4 - 1
         const int64_t n = tt * 128 + 32 * quarter + lane;
         const int chunks = Mp / 16;
         const bool have = __all_sync(kFull, fin && ok && !*abort_flag);
         if (have) {
-            for (int c = half; c < chunks; c += 4) {
+            for (int c = half; c < chunks; c += kDecWarps / 4) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(16 * c), v);
                 if (nkb == 0) {
@@ -430,7 +468,7 @@ __global__ __launch_bounds__(kThreads, 1) void k_gemm_tc(TensorView t, GemmArgs 
             if (*last_flag) {
                 __threadfence();
                 if (n < t.N) {
-                    for (int c = half; c < chunks; c += 4) {
+                    for (int c = half; c < chunks; c += kDecWarps / 4) {
                         // 16 independent loads per chunk s, summed in the order s = 0..S-1
                         float acc[16];
 #pragma unroll
@@ -557,47 +595,99 @@ size_t tc_smem_bytes(const TcParams &tp) {
            (size_t)(2 * (tp.a_st + tp.w_st + tp.b_st) + 1) * 8 + 16;
 }
 
-// Ring depths within the 227 KB of shared memory one CTA may use: about
-// 48 KB of activation stages (at least 2), 3 decoded-A stages, and the rest
-// for weight stages: the weight ring is what keeps HBM busy (a k-block's
-// planes take a few microseconds to arrive under load).
-void tc_rings(TcParams &tp) {
-    const size_t budget = 227 * 1024;
+// Dynamic shared memory one CTA may use: all 227 KB with one CTA per SM;
+// with two, half of the SM's 228 KB less the 1 KB each CTA reserves.
+size_t tc_smem_budget(int ctas_per_sm) { return ctas_per_sm > 1 ? 227 * 1024 / 2 - 1024 : 227 * 1024; }
+
+// Ring depths within the shared-memory budget: about 48 KB (24 KB with two
+// CTAs per SM) of activation stages (at least 2), 3 (2) decoded-A stages,
+// and the rest for weight stages: the weight ring is what keeps HBM busy (a
+// k-block's planes take a few microseconds to arrive under load).  Returns
+// false if not even two weight stages fit.
+bool tc_rings(TcParams &tp, int ctas_per_sm) {
+    const size_t budget = tc_smem_budget(ctas_per_sm);
     const size_t bst = (size_t)tp.Mp * 128;
-    tp.b_st = (int)(48 * 1024 / bst);
+    tp.b_st = (int)((ctas_per_sm > 1 ? 24 : 48) * 1024 / bst);
     tp.b_st = tp.b_st < 2 ? 2 : (tp.b_st > 6 ? 6 : tp.b_st);
-    tp.a_st = 2;
-    tp.w_st = 2;
-    auto fits = [&](int a, int w) {
+    tp.a_st = ctas_per_sm > 1 ? 2 : 3;
+    tp.w_st = 0;
+    for (int w = kMaxStages; w >= 2; --w) {
         TcParams x = tp;
-        x.a_st = a, x.w_st = w;
-        return tc_smem_bytes(x) <= budget;
-    };
-    tp.a_st = 3;
-    for (int w = kMaxStages; w >= 2; --w)
-        if (fits(tp.a_st, w)) {
+        x.w_st = w;
+        if (tc_smem_bytes(x) <= budget) {
             tp.w_st = w;
             break;
         }
+    }
+    return tp.w_st >= 2;
+}
+
+// Split of the K groups over S chunks for a grid of at most `slots` CTAs:
+// no more chunks than column groups, and few enough that the FP32 partial
+// traffic (2*S*Mpad*N*4 bytes) stays small next to the weights (1.5*N*K
+// bytes).
+int64_t tc_split_for(int64_t T, int64_t G, int64_t Mp, int64_t K, int64_t slots) {
+    int64_t S = slots / T;
+    const int64_t traffic_cap = (int64_t)(0.0375 * (double)K / (double)Mp);
+    if (S > traffic_cap) S = traffic_cap;
+    if (S > G) S = G;
+    if (S > 16) S = 16;
+    if (S < 1) S = 1;
+    return S;
+}
+
+template <int D>
+cudaError_t launch_variant(const TensorView &t, const GemmArgs &g, const TcParams &tp, const CUtensorMap &map,
+                           const CUtensorMap &hmap, const CUtensorMap &lmap, cudaStream_t s) {
+    const size_t smem = tc_smem_bytes(tp);
+    const size_t budget = tc_smem_budget(Roles<D>::kCtasPerSm);
+    if (smem > budget) return cudaErrorInvalidConfiguration;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int configured[64] = {0};
+    if (dev >= 0 && dev < 64 && configured[dev] < (int)smem) {
+        e = cudaFuncSetAttribute(k_gemm_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+        if (e != cudaSuccess) return e;
+        configured[dev] = (int)budget;
+    }
+    const int64_t blocks = ((t.Np + 127) / 128) * (int64_t)g.split;
+    if (blocks == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(Roles<D>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g.overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<D>, t, g, tp, map, hmap, lmap);
 }
 
 }  // namespace
 
 int64_t gemm_tc_pad(int64_t M) { return (M + 15) / 16 * 16; }
 
-// Split from (M, N, K) only: about one CTA per SM on 152 SMs, no more chunks
-// than column groups, and few enough that the FP32 partial traffic
-// (2*S*Mpad*N*4 bytes) stays small next to the weights (1.5*N*K bytes).
+// Split from (M, N, K) only.  With Mpad <= 128, if a split over 2 x 152
+// slots gives a grid of at least kTwoPerSmMinCtas CTAs, that split (and the
+// two-CTAs-per-SM build); otherwise about one CTA per SM on 152 SMs.
 int gemm_tc_split(int64_t M, int64_t N, int64_t K) {
     const int64_t T = (N + 127) / 128, G = groups_of(K), Mp = gemm_tc_pad(M);
     if (T == 0 || G == 0) return 1;
-    int64_t S = 152 / T;
-    const int64_t traffic_cap = (int64_t)(0.0375 * (double)K / (double)Mp);
-    if (S > traffic_cap) S = traffic_cap;
-    if (S > G) S = G;
-    if (S > 16) S = 16;
-    if (S < 1) S = 1;
-    return (int)S;
+    if (Mp <= 128) {
+        const int64_t S2 = tc_split_for(T, G, Mp, K, 2 * 152);
+        if (T * S2 >= kTwoPerSmMinCtas) return (int)S2;
+    }
+    return (int)tc_split_for(T, G, Mp, K, 152);
+}
+
+// The build a launch takes, from (M, N, K) and the split in use: two CTAs
+// per SM for Mpad <= 128 and a grid of at least kTwoPerSmMinCtas CTAs.
+int gemm_tc_ctas_per_sm(int64_t M, int64_t N, int64_t split) {
+    const int64_t T = (N + 127) / 128;
+    return (gemm_tc_pad(M) <= 128 && T * split >= kTwoPerSmMinCtas) ? 2 : 1;
 }
 
 cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
@@ -605,7 +695,8 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
     if (!enc) return cudaErrorNotSupported;
     TcParams tp;
     tp.Mp = (int)gemm_tc_pad(g.M);
-    tc_rings(tp);
+    const int cps = gemm_tc_ctas_per_sm(g.M, t.N, g.split);
+    if (!tc_rings(tp, cps)) return cudaErrorInvalidConfiguration;
     tp.tmem_cols = 32;
     while (tp.tmem_cols < tp.Mp) tp.tmem_cols <<= 1;
     tp.idesc = (1u << 4)                         // D: FP32
@@ -650,29 +741,8 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
             memset(&lmap, 0, sizeof lmap);
         }
     }
-    const size_t smem = tc_smem_bytes(tp);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    static int configured[64] = {0};
-    if (dev >= 0 && dev < 64 && configured[dev] < (int)smem) {
-        e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        configured[dev] = 227 * 1024;
-    }
-    const int64_t blocks = ((t.Np + 127) / 128) * (int64_t)g.split;
-    if (blocks == 0) return cudaSuccess;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = g.overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc, t, g, tp, map, hmap, lmap);
+    return cps > 1 ? launch_variant<8>(t, g, tp, map, hmap, lmap, s)
+                   : launch_variant<16>(t, g, tp, map, hmap, lmap, s);
 }
 
 }  // namespace w12

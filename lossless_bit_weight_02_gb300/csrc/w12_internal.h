@@ -71,6 +71,8 @@ struct GemmArgs {
 // laid out [S][Mpad][Np]).
 cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t s);
 int gemm_tc_split(int64_t M, int64_t N, int64_t K);
+// 1 or 2: CTAs per SM of the tensor-core build a launch with this split takes
+int gemm_tc_ctas_per_sm(int64_t M, int64_t N, int64_t split);
 int64_t gemm_tc_pad(int64_t M);
 
 // Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).

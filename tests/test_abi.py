@@ -78,6 +78,35 @@ def test_gemm_workspace_query(w12lib):
     assert w12lib.w12_gemm_workspace_bytes(1, 64, 64, bad) == 0
 
 
+def tc_split(w12lib, M, N, K, opts=None):
+    """The tensor-core split S, read back from the workspace size ([S][Mpad][Np] FP32 partials)."""
+    nb = w12lib.w12_gemm_workspace_bytes(M, N, K, opts or w12lib.make_opts())
+    if nb == 256:
+        return 1
+    mp, np_ = (M + 15) // 16 * 16, (N + 15) // 16 * 16
+    S, rem = divmod(nb - 256 - 4 * 65536, mp * np_ * 4)
+    assert rem == 0
+    return S
+
+
+@pytest.mark.parametrize("M,N,K,S", [
+    (24, 7168, 5120, 5),    # 56 row tiles x 5 = 280 CTAs: two CTAs per SM
+    (64, 7168, 5120, 2),    # partial-traffic cap 3 -> 168 CTAs: one CTA per SM, 152/56 = 2
+    (128, 7168, 5120, 1),   # cap 1
+    (64, 34816, 5120, 1),   # 272 row tiles fill two CTAs per SM without a split
+    (24, 5120, 17408, 7),   # 40 x 7 = 280
+    (64, 5120, 17408, 7),
+    (128, 5120, 17408, 3),  # cap 5 -> 200 CTAs: one CTA per SM, 152/40 = 3
+    (144, 5120, 17408, 3),  # Mpad > 128 never takes two CTAs per SM
+    (24, 5120, 5120, 3),    # cap 6 -> 240 CTAs, below the two-per-SM threshold
+])
+def test_tc_split_rule(M, N, K, S, w12lib):
+    """The split (and with it the build) depends on (M, N, K) only: S chunks over 2 x 152
+    slots when that grid has >= 258 CTAs and Mpad <= 128, else over 152 slots; each
+    capped by the column groups, 16, and the partial traffic 0.0375*K/Mpad."""
+    assert tc_split(w12lib, M, N, K) == S
+
+
 def test_status_strings(w12lib):
     for code, name in ((0, "W12_OK"), (-3, "W12_ERR_CAPACITY"), (-7, "W12_ERR_CORRUPT")):
         assert w12lib.status_string(code) == name

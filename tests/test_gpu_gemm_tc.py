@@ -65,6 +65,26 @@ def test_tc_forced_splits(split, w12lib, oracle):
     parity(w12lib, oracle, W, A, opts=w12lib.make_opts(split_k=split), reps=2)
 
 
+# Grids of at least 258 CTAs with Mpad <= 128 run two CTAs per SM (8 decoder
+# warps each, one per stripe, every k-block); smaller grids one CTA per SM
+# with 16.  N = 4096 has 32 row tiles: a forced split of 9 gives 288 CTAs,
+# one of 8 gives 256.
+@pytest.mark.parametrize("M,split", [(40, 9), (40, 8), (17, 9), (128, 9), (129, 9)])
+@pytest.mark.parametrize("kind", ["dense", "adversarial"])
+def test_tc_both_builds(M, split, kind, w12lib, oracle):
+    N, K = 4000, 2304 + 40  # ragged rows and columns; 10 column groups
+    W = (synth.dense_weights if kind == "dense" else synth.adversarial_weights)(N, K, seed=M + split)
+    A = synth.activations(M, K, seed=3400 + M)
+    parity(w12lib, oracle, W, A, opts=w12lib.make_opts(split_k=split), reps=2)
+
+
+def test_tc_two_per_sm_automatic_split(w12lib, oracle):
+    """QKV-sized layer at M = 24: the automatic split (5) fills two CTAs per SM."""
+    W = synth.dense_weights(7168, 5120, seed=1000)
+    A = synth.activations(24, 5120, seed=3500)
+    parity(w12lib, oracle, W, A, reps=2)
+
+
 def test_tc_adversarial_m33(w12lib, oracle):
     W = synth.adversarial_weights(400, 1496, seed=33)
     A = synth.activations(33, 1496, seed=3300)

@@ -43,6 +43,20 @@ def test_nested8_parity(N, K, M, kind, w12lib, oracle):
     assert np.array_equal(Y, Yt)
 
 
+def test_nested8_two_ctas_per_sm(w12lib, oracle):
+    """A split-9 grid of 288 CTAs: the tensor-core build with two CTAs per SM."""
+    W = synth.adversarial_weights(4096, 2304, seed=144)
+    A = synth.activations(40, 2304, seed=145)
+    st, ref = oracle.encode(W)
+    st, Yr, Y64, mag = oracle.gemm_nested8(A, ref)
+    t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+    Ad = synth.bits_to_tensor(A, "cuda")
+    Y = synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, opts=nested(w12lib, split_k=9)))
+    assert gemm_tolerance_failures(Y, Yr, Y64, mag).size == 0
+    tt = w12lib.w12_encode(synth.bits_to_tensor(W & 0xFFF0, "cuda"))
+    assert np.array_equal(Y, synth.tensor_to_bits(w12lib.w12_gemm(Ad, tt, opts=w12lib.make_opts(split_k=9))))
+
+
 @pytest.mark.parametrize("M", [1, 16, 48])
 def test_nested8_deterministic_across_grids(M, w12lib):
     N, K = 5121, 4000

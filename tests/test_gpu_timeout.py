@@ -18,16 +18,17 @@ from w12_tol import gemm_tolerance_failures
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("N,K", [(1024, 1024), (1024, 8192)])  # one K-chunk, and a split of the reduction
-def test_stalled_wait_reports_timeout_and_the_context_stays_usable(N, K, w12lib, oracle):
+# one K-chunk; a split of the reduction; a split-9 grid of 288 CTAs (two CTAs per SM)
+@pytest.mark.parametrize("N,K,split", [(1024, 1024, 0), (1024, 8192, 0), (4096, 2304, 9)])
+def test_stalled_wait_reports_timeout_and_the_context_stays_usable(N, K, split, w12lib, oracle):
     M = 32
     W = synth.dense_weights(N, K, seed=150 + K)
     A = synth.activations(M, K, seed=151)
     t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
     Ad = synth.bits_to_tensor(A, "cuda")
-    ws = w12lib.Workspace("cuda", 1 << 22)
+    ws = w12lib.Workspace("cuda", 1 << 24)
 
-    w12lib.w12_gemm(Ad, t, workspace=ws, opts=w12lib.make_opts(flags=w12lib.W12_GEMM_TEST_STALL))
+    w12lib.w12_gemm(Ad, t, workspace=ws, opts=w12lib.make_opts(flags=w12lib.W12_GEMM_TEST_STALL, split_k=split))
     torch.cuda.synchronize()
     assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_ERR_TIMEOUT
     assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_OK  # read and cleared
@@ -35,7 +36,7 @@ def test_stalled_wait_reports_timeout_and_the_context_stays_usable(N, K, w12lib,
 
     st, ref = oracle.encode(W)
     st, Yr, Y64, mag = oracle.gemm(A, ref)
-    Y = synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, workspace=ws))
+    Y = synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, workspace=ws, opts=w12lib.make_opts(split_k=split)))
     torch.cuda.synchronize()
     assert gemm_tolerance_failures(Y, Yr, Y64, mag).size == 0
     assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_OK
