@@ -623,12 +623,14 @@ bool tc_rings(TcParams &tp, int ctas_per_sm) {
 }
 
 // Split of the K groups over S chunks for a grid of at most `slots` CTAs:
-// no more chunks than column groups, and few enough that the FP32 partial
-// traffic (2*S*Mpad*N*4 bytes) stays small next to the weights (1.5*N*K
-// bytes).
+// no more chunks than column groups (or 16), and S <= 0.1*K/Mpad, so that
+// the FP32 partials (2*S*Mpad*N*4 bytes written and read back) stay within
+// about half the weight bytes (1.5*N*K); at these sizes they live in L2.
+// (A cap of 0.0375*K/Mpad left QKV and O at M = 128 with 40-56 CTAs; on
+// GB300 0.1 ran M = 128 and 256 13-17% faster and M <= 64 the same.)
 int64_t tc_split_for(int64_t T, int64_t G, int64_t Mp, int64_t K, int64_t slots) {
     int64_t S = slots / T;
-    const int64_t traffic_cap = (int64_t)(0.0375 * (double)K / (double)Mp);
+    const int64_t traffic_cap = (int64_t)(0.1 * (double)K / (double)Mp);
     if (S > traffic_cap) S = traffic_cap;
     if (S > G) S = G;
     if (S > 16) S = 16;

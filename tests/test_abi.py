@@ -91,20 +91,27 @@ def tc_split(w12lib, M, N, K, opts=None):
 
 @pytest.mark.parametrize("M,N,K,S", [
     (24, 7168, 5120, 5),    # 56 row tiles x 5 = 280 CTAs: two CTAs per SM
-    (64, 7168, 5120, 2),    # partial-traffic cap 3 -> 168 CTAs: one CTA per SM, 152/56 = 2
-    (128, 7168, 5120, 1),   # cap 1
+    (64, 7168, 5120, 5),
+    (128, 7168, 5120, 2),   # 56 x 4 (partial-traffic cap 4) = 224 < 258: one CTA per SM, 152/56 = 2
+    (256, 5120, 5120, 2),   # Mpad > 128; the cap (2) binds: 152/40 = 3
+    (128, 5120, 2048, 1),   # cap 1.6
     (64, 34816, 5120, 1),   # 272 row tiles fill two CTAs per SM without a split
     (24, 5120, 17408, 7),   # 40 x 7 = 280
-    (64, 5120, 17408, 7),
-    (128, 5120, 17408, 3),  # cap 5 -> 200 CTAs: one CTA per SM, 152/40 = 3
+    (128, 5120, 17408, 7),
     (144, 5120, 17408, 3),  # Mpad > 128 never takes two CTAs per SM
-    (24, 5120, 5120, 3),    # cap 6 -> 240 CTAs, below the two-per-SM threshold
+    (24, 1024, 5120, 16),   # 8 row tiles: at most 16 chunks
+    (24, 1024, 1024, 3),    # cap 3.2 (below the 4 column groups whenever Mpad > 25.6)
 ])
 def test_tc_split_rule(M, N, K, S, w12lib):
     """The split (and with it the build) depends on (M, N, K) only: S chunks over 2 x 152
     slots when that grid has >= 258 CTAs and Mpad <= 128, else over 152 slots; each
-    capped by the column groups, 16, and the partial traffic 0.0375*K/Mpad."""
+    capped by the column groups, 16, and the partial traffic 0.1*K/Mpad."""
     assert tc_split(w12lib, M, N, K) == S
+
+
+def test_tc_split_at_most_one_chunk_per_group(w12lib):
+    # Mpad = 16 (the tensor-core path forced at M <= 16): cap 6.4, 4 column groups
+    assert tc_split(w12lib, 16, 1024, 1024, w12lib.make_opts(path=w12lib.W12_PATH_TC)) == 4
 
 
 def test_status_strings(w12lib):
