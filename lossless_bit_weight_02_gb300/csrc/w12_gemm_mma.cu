@@ -37,7 +37,16 @@
 namespace w12 {
 namespace {
 
-constexpr int kWarps = 4;  // warps per block; each warp keeps one 4-tile group in flight
+// Warps per block, each keeping one 4-tile group in flight: a whole SM's
+// worth (16 for M <= 8, 12 for M <= 16, which is what the registers and the
+// shared memory allow) in one block.  The warp scheduler favours older
+// blocks: with four 4-warp blocks per SM, the youngest block's warps streamed
+// their ranges ~20% slower than the oldest's, and each SM ended its launch
+// with few warps left.  The warps of one block run at the same pace.
+template <int NB>
+__host__ __device__ constexpr int warps_of() {
+    return NB == 1 ? 16 : 12;
+}
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -60,7 +69,7 @@ __host__ __device__ constexpr uint32_t act_buf_bytes() {
 }
 template <int NB>
 __host__ __device__ constexpr int smem_bytes() {
-    return kWarps * (4 * 32 * 16 + 2 * act_buf_bytes<NB>());
+    return warps_of<NB>() * (4 * 32 * 16 + 2 * act_buf_bytes<NB>());
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -231,7 +240,8 @@ __device__ __forceinline__ int range_of(int u, const GemmArgs &g) {
 }
 
 template <int NB, bool Q>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16); Q: nested 8-bit view
-__global__ __launch_bounds__(kWarps * 32, NB == 1 ? 4 : 3) void k_gemm_mma(TensorView t, GemmArgs g) {
+__global__ __launch_bounds__(warps_of<NB>() * 32, 1) void k_gemm_mma(TensorView t, GemmArgs g) {
+    constexpr int kWarps = warps_of<NB>();
     // [kWarps][4][32] uint4 escape-patch copies, then [kWarps][2][8*NB][kActPitch] activations
     extern __shared__ __align__(16) unsigned char smem[];
     uint4 (*patch)[4][32] = reinterpret_cast<uint4 (*)[4][32]>(smem);
@@ -459,6 +469,7 @@ LaunchCache &cache_for_device(int dev) {
 
 template <int NB, bool Q>
 cudaError_t launch_nb(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
+    constexpr int kWarps = warps_of<NB>();
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
