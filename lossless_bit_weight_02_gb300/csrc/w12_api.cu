@@ -82,13 +82,10 @@ w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, Ge
     pl.counters_off = 256;
     pl.partials_off = 256 + 4 * kMaxCounters;
     if (tc) {
-        int split = (o && o->split_k > 0) ? o->split_k : gemm_tc_split(M, N, K);
-        if (G == 0) split = 1;
-        if (split > G && G > 0) split = (int)G;
-        if (!counters_ok) split = 1;
-        pl.split = split;
         pl.mp = gemm_tc_pad(M);
-        pl.bytes = split > 1 ? pl.partials_off + (size_t)split * Np * pl.mp * 4 : 256;
+        const int64_t pbytes = gemm_tc_plan(M, N, K, o ? o->split_k : 0, counters_ok, pl.cut);
+        pl.split = pl.cut.split;
+        pl.bytes = pbytes > 0 ? pl.partials_off + (size_t)pbytes : 256;
     } else {
         // The kernel numbers (stripe, group) units with int32; a tensor with
         // 2^31 units would hold 8 TB of hi plane, so this never binds.
@@ -237,6 +234,8 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     g.per = pl.cut.per;
     g.q = pl.cut.q;
     g.rem = pl.cut.rem;
+    g.tc_cps = pl.cut.tc_cps;
+    g.tc_ranges = pl.cut.tc_ranges;
     g.max_ctas = opts ? opts->max_ctas : 0;
     g.overlap = opts ? (opts->flags & W12_GEMM_OVERLAP_PREVIOUS) != 0 : false;
     g.nested8 = opts ? (opts->flags & W12_GEMM_NESTED8) != 0 : false;

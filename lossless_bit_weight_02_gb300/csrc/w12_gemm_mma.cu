@@ -220,25 +220,6 @@ __device__ __forceinline__ void own_escape(Stream<NB> &w, int lane) {
     }
 }
 
-// Ranges: the T*G (stripe, group) units, numbered u = stripe*G + group, are
-// split into segments of g.seglen units (the whole tensor, or one stripe),
-// and each segment into g.per contiguous ranges: the first g.rem ranges of a
-// segment hold g.q + 1 units, the others g.q.  Because both planes and the
-// escape offsets are stored stripe-major with whole groups, a range is one
-// contiguous stream however many stripe boundaries it crosses.  All of it
-// is 32-bit integer arithmetic (unit and range counts are below 2^31).
-__device__ __forceinline__ int range_begin(int v, const GemmArgs &g) {
-    const int seg = v / g.per, j = v - seg * g.per;
-    return seg * g.seglen + j * g.q + (j < g.rem ? j : g.rem);
-}
-// the range holding unit u
-__device__ __forceinline__ int range_of(int u, const GemmArgs &g) {
-    const int seg = u / g.seglen, x = u - seg * g.seglen;
-    const int big = g.rem * (g.q + 1);  // units in the segment's longer ranges
-    const int j = x < big ? x / (g.q + 1) : g.rem + (x - big) / g.q;
-    return seg * g.per + j;
-}
-
 template <int NB, bool Q>  // NB = number of 8-token column blocks (1: M <= 8, 2: M <= 16); Q: nested 8-bit view
 __global__ __launch_bounds__(warps_of<NB>() * 32, 1) void k_gemm_mma(TensorView t, GemmArgs g) {
     constexpr int kWarps = warps_of<NB>();

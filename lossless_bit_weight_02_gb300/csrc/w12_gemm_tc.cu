@@ -573,6 +573,458 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
     }
 }
 
+// Balanced range cut (used for Mpad > 128 on large layers, one CTA per SM):
+// the units u = row_tile*G + group are cut into one contiguous range per
+// CTA (range_begin), so every SM streams the same number of units whatever
+// the row-tile count.  A range is walked piece by piece (the part of it
+// inside one row tile).  Piece j accumulates in TMEM buffer j & 1; its
+// epilogue is deferred until piece j + 2 needs the buffer (for most ranges,
+// to the end), so the decoders go straight on to the next row tile, whose
+// bases and group offsets they fetch during the last group of the current
+// one.  A piece that covers its whole row tile is rounded and stored; the
+// range's first and last pieces otherwise go to FP32 slots v and v + V, and
+// the last CTA to arrive at a row tile sums its pieces in range order.
+template <int D>
+__global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_gemm_tc_ranges(
+    TensorView t, GemmArgs g, TcParams tp, const __grid_constant__ CUtensorMap tmap,
+    const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap lmap) {
+    using R = Roles<D>;
+    constexpr int kDecWarps = R::kDecWarps, kPar = R::kPar;
+    constexpr int kWProdWarp = R::kWProdWarp, kBProdWarp = R::kBProdWarp, kMmaWarp = R::kMmaWarp;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned, by an offset so that the compiler keeps the
+    // shared address space (ld.shared / st.shared, not generic accesses)
+    uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int RA = tp.a_st, RW = tp.w_st, RB = tp.b_st, Mp = tp.Mp;
+    const uint32_t b_stage_bytes = (uint32_t)Mp * 128;
+    uint8_t *a_st = base;                                // RA x 16 KB (1024-aligned)
+    uint8_t *b_st = a_st + RA * kAStageBytes;            // RB x Mp*128 B (1024-aligned)
+    uint8_t *w_st = b_st + RB * b_stage_bytes;           // RW x 12 KB (1024-aligned)
+    uint64_t *w_full = reinterpret_cast<uint64_t *>(w_st + RW * kWStageBytes);
+    uint64_t *w_empty = w_full + RW;
+    uint64_t *a_full = w_empty + RW;
+    uint64_t *a_empty = a_full + RA;
+    uint64_t *b_full = a_empty + RA;
+    uint64_t *b_empty = b_full + RB;
+    uint64_t *done = b_empty + RB;  // [2]: per accumulator buffer, one phase per piece using it
+    uint64_t *fin = done + 2;        // every MMA this CTA issued has completed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *arr_tt = abort_flag + 1;    // [2] row tiles of this range's partial first / last piece
+    volatile int *arr_last = arr_tt + 2;      // [2] this CTA delivered the row tile's last piece
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // This CTA's range of units u = row_tile*G + group; a piece is the part of
+    // the range inside one row tile.
+    const int G = (int)t.G;
+    const int v = blockIdx.x;
+    const int V = (int)g.ranges;
+    const int u0 = range_begin(v, g), u1 = range_begin(v + 1, g);
+    const int64_t T = t.Np / 16;  // stripes
+    const int tt0 = u0 / G, ga0 = u0 - tt0 * G;
+    const int npieces = (u1 - 1) / G - tt0 + 1;
+    // piece jj: row tile tt0 + jj, groups [ga, gb) of it, accumulated in TMEM
+    // buffer jj & 1 (columns (jj & 1) * acc_cols ..)
+    auto piece = [&](int jj, int &tt, int &ga, int &gb) {
+        tt = tt0 + jj;
+        ga = jj == 0 ? ga0 : 0;
+        const int e = u1 - tt * G;
+        gb = e < G ? e : G;
+    };
+    const uint32_t acc_cols = tp.tmem_cols / 2;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RW; ++i) {
+            mbar_init(&w_full[i], 1);    // the producer's expect_tx
+            mbar_init(&w_empty[i], 8);   // one arrival per stripe's decoder warp of the k-block
+        }
+        for (int i = 0; i < RA; ++i) {
+            mbar_init(&a_full[i], 8);
+            mbar_init(&a_empty[i], 1);   // tcgen05.commit
+        }
+        for (int i = 0; i < RB; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
+        mbar_init(&done[0], 1);
+        mbar_init(&done[1], 1);
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        arr_tt[0] = arr_tt[1] = -1;
+        arr_last[0] = arr_last[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kWProdWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(tp.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    grid_dep_launch();
+
+    if (warp < kDecWarps) {
+        // ------------------------------------------------------------------
+        // Decoders: per piece (row tile tt, groups [ga, gb)), warp w handles
+        // stripe st = 8*tt + (w%8) on every k-block (8 decoder warps) or on
+        // the k-blocks of parity w/8 (16 warps: tiles p = w/8 and w/8 + 2 of
+        // every group): the tile's planes come from the weight ring, the BF16
+        // tile goes to the A ring (K-major, 128-byte swizzle), escapes over
+        // their slots.  Then the piece's epilogue.
+        // ------------------------------------------------------------------
+        const int gid = lane >> 2, q = lane & 3;
+        const int sw = warp & 7, par = warp >> 3;
+        const int rA = 16 * sw + gid, rB = rA + 8;
+        const uint32_t c28 = g.c28, c16 = g.c16;
+        const uint32_t vmask = g.nested8 ? 0xFFF0u : 0xFFFFu;  // escape bits kept
+        const int n_esc = (int)t.n_esc;
+        const int quarter = warp & 3, half = warp >> 2;  // TMEM lanes 32*quarter..; half: 0 .. kDecWarps/4 - 1
+        const int r = 32 * quarter + lane;               // epilogue row within the row tile
+        const int chunks = Mp / 16;
+        bool ok = true;
+
+        // Piece epilogue (after its MMAs completed).  A piece covering its
+        // whole row tile is rounded and stored; any other piece goes to FP32
+        // slot v (the range's first piece) or v + V (its last), and the row
+        // tile's arrival count goes up.  Every decoder warp runs the same
+        // barriers whether or not the CTA has aborted.
+        auto epilogue = [&](int jj) {
+            int tt, ga, gb;
+            piece(jj, tt, ga, gb);
+            if (ok && !__all_sync(kFull, mbar_wait(&done[jj & 1], (uint32_t)((jj >> 1) & 1), abort_flag, g.error)))
+                ok = false;
+            tc_fence_after();
+            const bool whole = ga == 0 && gb == G;
+            const int64_t slot = jj == 0 ? v : (int64_t)v + V;
+            const int64_t n = (int64_t)tt * 128 + r;
+            if (ok) {
+                const uint32_t acc = tmem + (uint32_t)(jj & 1) * acc_cols + ((uint32_t)(32 * quarter) << 16);
+                for (int c = half; c < chunks; c += kDecWarps / 4) {
+                    float x[16];
+                    tmem_ld16(acc + (uint32_t)(16 * c), x);
+                    if (whole) {
+                        if (n < t.N) {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const int m = 16 * c + k;
+                                if (m < g.M) g.Y[(int64_t)m * g.ldy + n] = f32_to_bf16_rn(x[k]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) g.partials[(slot * Mp + 16 * c + k) * 128 + r] = x[k];
+                    }
+                }
+                if (!whole) __threadfence();
+            }
+            // every TMEM read of this buffer is done before any decoder warp
+            // hands the MMA warp a tile of the piece that reuses it
+            tc_fence_before();
+            asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+            if (!whole && threadIdx.x == 0 && !*abort_flag) {
+                const int k = jj == 0 ? 0 : 1;
+                const int va = range_of(tt * G, g), vb = range_of(tt * G + G - 1, g);
+                arr_tt[k] = tt;
+                arr_last[k] = atomicAdd(&g.counters[tt], 1) == vb - va;
+            }
+        };
+
+        // Per-piece state read from memory: row bases and the group offsets
+        // (lane l holds the offset of group gw0 + l: one coalesced load per 31
+        // groups, no dependent load inside the loop).  The next piece's is
+        // fetched during the current piece's last group.
+        struct PieceMeta {
+            uint32_t base2A, base2B;
+            int ptrw;
+        };
+        auto load_window = [&](const int32_t *gptr, bool live, int first, int gb) -> int {
+            const int gi = first + lane;
+            int x = 0;
+            if (live && gi <= gb) {
+                x = __ldg(gptr + gi);
+                x = x < 0 ? 0 : (x > n_esc ? n_esc : x);
+            }
+            return x;
+        };
+        auto fetch_meta = [&](int jj) -> PieceMeta {
+            int tt, ga, gb;
+            piece(jj, tt, ga, gb);
+            const int64_t st = (int64_t)tt * 8 + sw;
+            const bool live = st < T;
+            PieceMeta pm;
+            pm.base2A = pm.base2B = 0;
+            if (live) {
+                const int64_t nA = st * 16 + gid, nB = nA + 8;
+                pm.base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
+                pm.base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
+            }
+            pm.ptrw = load_window(t.esc_ptr + (live ? st : 0) * t.G, live, ga, gb);
+            return pm;
+        };
+
+        RingPos wp, ap;  // ring positions of this warp's next k-block
+        wp.advance(par, RW);
+        ap.advance(par, RA);
+        PieceMeta meta = fetch_meta(0);
+        for (int j = 0; j < npieces; ++j) {
+            int tt, ga, gb;
+            piece(j, tt, ga, gb);
+            const int nkb = 4 * (gb - ga);
+            const int64_t st = (int64_t)tt * 8 + sw;
+            const bool live = st < T;  // warp-uniform
+            const uint32_t base2A = meta.base2A, base2B = meta.base2B;
+            const int32_t *gptr = t.esc_ptr + (live ? st : 0) * t.G;
+            int gw0 = ga, ptrw = meta.ptrw;
+            auto bounds = [&](int gg, int &p0, int &p1) {
+                if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per piece)
+                    gw0 = gg;
+                    ptrw = load_window(gptr, live, gw0, gb);
+                }
+                p0 = __shfl_sync(kFull, ptrw, gg - gw0);
+                p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
+                if (p1 < p0) p1 = p0;
+            };
+            EscBatch cur, nxt;
+            cur.cnt = nxt.cnt = 0;
+            cur.ent = nxt.ent = 0;
+            cur.p0 = nxt.p0 = 0;
+            if (live) {
+                int p0, p1;
+                bounds(ga, p0, p1);
+                cur = load_group_escapes(t, p0, p1, lane);
+                if (ga + 1 < gb) {
+                    bounds(ga + 1, p0, p1);
+                    nxt = load_group_escapes(t, p0, p1, lane);
+                }
+            }
+            uint32_t emask = live ? escape_tiles(cur, lane) : 0u;
+            if (j == 0) grid_dep_wait();  // Y and the workspace may belong to the previous kernel
+            if (j >= 2) epilogue(j - 2);  // frees the accumulator buffer this piece uses
+            const int last_g = gb - ga - 1;
+            // Each piece holds a multiple of 4 k-blocks, so this warp's k-blocks of
+            // the piece start at parity `par` and its ring positions carry over.
+            for (int kb = par; kb < nkb && ok; kb += kPar, wp.advance(kPar, RW), ap.advance(kPar, RA)) {
+                const int p = kb & 3;  // tile of the group
+                if (kb >= 4 && p == par && live) {  // first tile of a new group for this warp
+                    const int gg = ga + (kb >> 2);
+                    cur = nxt;
+                    emask = escape_tiles(cur, lane);
+                    if (gg + 1 < gb) {
+                        int p0, p1;
+                        bounds(gg + 1, p0, p1);
+                        nxt = load_group_escapes(t, p0, p1, lane);
+                    }
+                }
+                if ((kb >> 2) == last_g && p == par && j + 1 < npieces) meta = fetch_meta(j + 1);
+                const int ws = wp.stage, as = ap.stage;
+                const uint32_t wph = wp.phase, aph = ap.phase;
+                // the whole warp leaves together, so no lane is left behind at a
+                // warp-wide instruction
+                if (!__all_sync(kFull, mbar_wait(&w_full[ws], wph, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                uint32_t dA[8], dB[8];
+                if (live) {
+                    const uint8_t *W = w_st + ws * kWStageBytes;
+                    const uint4 h0 = lds128(W + sw * 1024 + lane * 16), h1 = lds128(W + sw * 1024 + 512 + lane * 16);
+                    // the nested 8-bit view reads no lo plane: records with zero low nibbles
+                    const uint4 l = g.nested8 ? make_uint4(0u, 0u, 0u, 0u) : lds128(W + 8192 + sw * 512 + lane * 16);
+                    decode16_fma(h0, l.x, l.y, base2A, c28, c16, dA);
+                    decode16_fma(h1, l.z, l.w, base2B, c28, c16, dB);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[ws]);  // the planes are in registers
+                if (!__all_sync(kFull, mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                if (live) {
+                    uint8_t *A = a_st + as * kAStageBytes;
+                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q)) = make_uint4(dA[0], dA[1], dA[2], dA[3]);
+                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q + 1)) = make_uint4(dA[4], dA[5], dA[6], dA[7]);
+                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q)) = make_uint4(dB[0], dB[1], dB[2], dB[3]);
+                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q + 1)) = make_uint4(dB[4], dB[5], dB[6], dB[7]);
+                    if ((emask >> p) & 1u) {  // escapes of this tile overwrite their slots
+                        __syncwarp();
+                        auto put = [&](uint32_t e) {
+                            const int key = (int)(e >> 16);
+                            const int rr = 16 * sw + ((key >> 6) & 15), jj = key & 63;
+                            *reinterpret_cast<uint16_t *>(A + swz(rr, jj >> 3) + (jj & 7) * 2) = (uint16_t)(e & vmask);
+                        };
+                        if (cur.cnt <= 32) {
+                            if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
+                        } else {
+                            for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
+                                const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
+                                if (b0 + lane < cur.cnt && (int)(e >> 26) == p) put(e);
+                            }
+                        }
+                    }
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[as]);
+            }
+        }
+        if (npieces >= 2) epilogue(npieces - 2);
+        epilogue(npieces - 1);
+
+        // every MMA issued has completed (also after an abort: TMEM is freed below)
+        (void)__all_sync(kFull, mbar_drain(fin, 0, g.error));
+        asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+        // Row tiles whose last piece this CTA delivered: sum the pieces in
+        // range order and store.  (Only range va can start before the row
+        // tile; its piece there is its last one.)
+        for (int k = 0; k < 2; ++k) {
+            const int tt = arr_tt[k];
+            if (tt < 0 || !arr_last[k] || *abort_flag) continue;
+            __threadfence();
+            const int va = range_of(tt * G, g), vb = range_of(tt * G + G - 1, g);
+            const int64_t s0 = range_begin(va, g) < tt * G ? (int64_t)va + V : va;
+            const int64_t n = (int64_t)tt * 128 + r;
+            if (n < t.N) {
+                for (int c = half; c < chunks; c += kDecWarps / 4) {
+                    float acc[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) acc[jj] = __ldcg(g.partials + (s0 * Mp + 16 * c + jj) * 128 + r);
+                    for (int x = va + 1; x <= vb; ++x) {
+                        float y[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            y[jj] = __ldcg(g.partials + ((int64_t)x * Mp + 16 * c + jj) * 128 + r);
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) acc[jj] += y[jj];
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        if (16 * c + jj < g.M) g.Y[(int64_t)(16 * c + jj) * g.ldy + n] = f32_to_bf16_rn(acc[jj]);
+                }
+            }
+            if (threadIdx.x == 0) g.counters[tt] = 0;
+        }
+    } else if (warp == kWProdWarp) {
+        // ------------------------------------------------------------------
+        // Weight planes: one k-block (8 tiles of 1.5 KB) per stage, with
+        // tiled copies, up to RW k-blocks ahead of the decoders, unit after
+        // unit of the range.  Reads only the W12 tensor, so it starts before
+        // the previous kernel ends.
+        // ------------------------------------------------------------------
+        // The whole warp runs the loop (warp-uniform values stay in uniform
+        // registers); one elected lane issues.
+        int issued = 0;
+        bool ok = true;
+        RingPos wp;
+        int tt = u0 / G, grp = u0 - tt * G;
+        for (int u = u0; u < u1 && ok; ++u) {
+            for (int p = 0; p < 4; ++p, wp.advance(1, RW)) {
+                const int ws = wp.stage;
+                if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
+                    // the full box is counted, out-of-range stripes included (zero-filled)
+                    mbar_expect_tx(&w_full[ws], g.nested8 ? 8192u : kWStageBytes);
+                    uint8_t *dst = w_st + ws * kWStageBytes;
+                    tma_load_4d(dst, &hmap, 4 * grp + p, tt * 8, &w_full[ws]);
+                    if (!g.nested8) tma_load_4d(dst + 8192, &lmap, 4 * grp + p, tt * 8, &w_full[ws]);
+                }
+                __syncwarp();
+                ++issued;
+            }
+            if (++grp == G) {
+                grp = 0;
+                ++tt;
+            }
+        }
+        // the copies issued last must have landed before the CTA exits
+        for (int i = issued > RW ? issued - RW : 0; i < issued; ++i)
+            mbar_drain(&w_full[i % RW], (uint32_t)((i / RW) & 1), g.error);
+    } else if (warp == kBProdWarp) {
+        // ------------------------------------------------------------------
+        // Activations: one TMA tile [Mp x 64] per k-block.
+        // ------------------------------------------------------------------
+        grid_dep_wait();  // A may be written by the previous kernel
+        int issued = 0;
+        bool ok = true;
+        RingPos bp;
+        int grp = u0 % G;
+        for (int u = u0; u < u1 && ok; ++u) {
+            for (int p = 0; p < 4; ++p, bp.advance(1, RB)) {
+                const int stage = bp.stage;
+                if (!__all_sync(kFull, mbar_wait(&b_empty[stage], bp.phase ^ 1u, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
+                    mbar_expect_tx(&b_full[stage], b_stage_bytes);
+                    tma_load_2d(b_st + stage * b_stage_bytes, &tmap, (4 * grp + p) * 64, 0, &b_full[stage]);
+                }
+                __syncwarp();
+                ++issued;
+            }
+            if (++grp == G) grp = 0;
+        }
+        // the copies issued last must have landed before the CTA exits
+        for (int i = issued > RB ? issued - RB : 0; i < issued; ++i)
+            mbar_drain(&b_full[i % RB], (uint32_t)((i / RB) & 1), g.error);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------------
+        // MMA issue.  The accumulator restarts at each piece's first k-block;
+        // after a piece's last k-block a commit completes `done`.
+        // ------------------------------------------------------------------
+        // The whole warp runs the loop; one elected lane issues the MMAs.
+        if (g.test_stall)  // a wait that nothing completes: it runs out and aborts the CTA
+            (void)__all_sync(kFull, mbar_wait(fin, 0, abort_flag, g.error));
+        bool ok = true;
+        RingPos ap, bp;
+        int grp = u0 % G;
+        int j = -1;  // piece
+        for (int u = u0; u < u1 && ok; ++u) {
+            const bool first = u == u0 || grp == 0;
+            const bool last = u + 1 == u1 || grp + 1 == G;
+            if (first) ++j;
+            const uint32_t d = tmem + (uint32_t)(j & 1) * acc_cols;
+            for (int p = 0; p < 4; ++p, ap.advance(1, RA), bp.advance(1, RB)) {
+                const int as = ap.stage, bs = bp.stage;
+                if (!__all_sync(kFull, mbar_wait(&a_full[as], ap.phase, abort_flag, g.error)) ||
+                    !__all_sync(kFull, mbar_wait(&b_full[bs], bp.phase, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_addr(a_st + as * kAStageBytes);
+                const uint32_t b0 = smem_addr(b_st + bs * b_stage_bytes);
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma(d, smem_desc(a0 + 32 * kk), smem_desc(b0 + 32 * kk), tp.idesc,
+                             !(first && p == 0 && kk == 0));
+                    umma_commit(&a_empty[as]);
+                    umma_commit(&b_empty[bs]);
+                    if (last && p == 3) umma_commit(&done[j & 1]);
+                }
+                __syncwarp();
+            }
+            if (++grp == G) grp = 0;
+        }
+        if (elect_one()) umma_commit(fin);  // arrives once every MMA issued above has completed
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWProdWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tp.tmem_cols)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
@@ -592,7 +1044,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 size_t tc_smem_bytes(const TcParams &tp) {
     return 1024 + (size_t)tp.a_st * kAStageBytes + (size_t)tp.b_st * tp.Mp * 128 + (size_t)tp.w_st * kWStageBytes +
-           (size_t)(2 * (tp.a_st + tp.w_st + tp.b_st) + 1) * 8 + 16;
+           (size_t)(2 * (tp.a_st + tp.w_st + tp.b_st) + 3) * 8 + 32;  // rings, barriers, flags
 }
 
 // Dynamic shared memory one CTA may use: all 227 KB with one CTA per SM;
@@ -638,9 +1090,20 @@ int64_t tc_split_for(int64_t T, int64_t G, int64_t Mp, int64_t K, int64_t slots)
     return S;
 }
 
+// the kernel of a launch: K-chunks or balanced ranges
+template <int D, bool Ranges>
+struct TcKernel {
+    static constexpr auto fn = k_gemm_tc<D>;
+};
 template <int D>
+struct TcKernel<D, true> {
+    static constexpr auto fn = k_gemm_tc_ranges<D>;
+};
+
+template <int D, bool Ranges>
 cudaError_t launch_variant(const TensorView &t, const GemmArgs &g, const TcParams &tp, const CUtensorMap &map,
                            const CUtensorMap &hmap, const CUtensorMap &lmap, cudaStream_t s) {
+    constexpr auto kern = TcKernel<D, Ranges>::fn;
     const size_t smem = tc_smem_bytes(tp);
     const size_t budget = tc_smem_budget(Roles<D>::kCtasPerSm);
     if (smem > budget) return cudaErrorInvalidConfiguration;
@@ -649,11 +1112,12 @@ cudaError_t launch_variant(const TensorView &t, const GemmArgs &g, const TcParam
     if (e != cudaSuccess) return e;
     static int configured[64] = {0};
     if (dev >= 0 && dev < 64 && configured[dev] < (int)smem) {
-        e = cudaFuncSetAttribute(k_gemm_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
         if (e != cudaSuccess) return e;
         configured[dev] = (int)budget;
     }
-    const int64_t blocks = ((t.Np + 127) / 128) * (int64_t)g.split;
+    // one CTA per range, or per (row tile, K-chunk)
+    const int64_t blocks = Ranges ? g.ranges : ((t.Np + 127) / 128) * (int64_t)g.split;
     if (blocks == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
@@ -665,31 +1129,69 @@ cudaError_t launch_variant(const TensorView &t, const GemmArgs &g, const TcParam
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g.overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc<D>, t, g, tp, map, hmap, lmap);
+    return cudaLaunchKernelEx(&cfg, kern, t, g, tp, map, hmap, lmap);
 }
 
 }  // namespace
 
 int64_t gemm_tc_pad(int64_t M) { return (M + 15) / 16 * 16; }
 
-// Split from (M, N, K) only.  With Mpad <= 128, if a split over 2 x 152
-// slots gives a grid of at least kTwoPerSmMinCtas CTAs, that split (and the
-// two-CTAs-per-SM build); otherwise about one CTA per SM on 152 SMs.
-int gemm_tc_split(int64_t M, int64_t N, int64_t K) {
-    const int64_t T = (N + 127) / 128, G = groups_of(K), Mp = gemm_tc_pad(M);
-    if (T == 0 || G == 0) return 1;
-    if (Mp <= 128) {
-        const int64_t S2 = tc_split_for(T, G, Mp, K, 2 * 152);
-        if (T * S2 >= kTwoPerSmMinCtas) return (int)S2;
+// The work of one launch, from (M, N, K) and a forced split only (never the
+// grid), so the summation order is fixed.  Two schemes:
+//  * K-chunks (k_gemm_tc): S chunks of whole groups per 128-row tile, one CTA
+//    each; with Mpad <= 128, a split over 2 x 152 slots (two CTAs per SM)
+//    when its grid holds at least kTwoPerSmMinCtas CTAs, otherwise about one
+//    CTA per SM on 152 SMs.  S <= column groups, <= 16, and <= 0.1*K/Mpad, so
+//    that the FP32 partials (2*S*Mpad*N*4 bytes written and read) stay within
+//    about half the weight bytes (1.5*N*K); at these sizes they live in L2.
+//  * balanced ranges (k_gemm_tc_ranges): with Mpad > 128 and at least 16
+//    units (row tile, group) per SM, 152 contiguous ranges of units, one CTA
+//    per SM.  There the K-chunk grid runs in more than one wave or leaves SMs
+//    idle (gate/up, 272 row tiles; down, 120 CTAs), and the range kernel was
+//    20% faster on GB300; with fewer units per CTA its per-piece costs made
+//    it slower.
+// Returns the bytes of FP32 partials the launch needs (0: none).
+int64_t gemm_tc_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters_ok, GemmArgs &g) {
+    const int64_t T = (N + 127) / 128, G = groups_of(K), Mp = gemm_tc_pad(M), Np = (N + 15) / 16 * 16;
+    const int64_t U = T * G;
+    g.tc_ranges = false;
+    g.ranges = 0;
+    if (split_k == 0 && counters_ok && Mp > 128 && U >= 16 * 152) {
+        const int64_t V = 152;
+        g.seglen = (int)U, g.per = (int)V;
+        g.q = (int)(U / V), g.rem = (int)(U % V);
+        g.ranges = V;
+        g.split = 1;
+        g.tc_cps = 1;
+        g.tc_ranges = true;
+        for (int64_t v = 1; v < V; ++v) {  // any range boundary inside a row tile needs partials
+            const int64_t b = v * g.q + (v < g.rem ? v : g.rem);
+            if (b % G != 0) return 2 * V * Mp * 128 * 4;
+        }
+        return 0;
     }
-    return (int)tc_split_for(T, G, Mp, K, 152);
-}
-
-// The build a launch takes, from (M, N, K) and the split in use: two CTAs
-// per SM for Mpad <= 128 and a grid of at least kTwoPerSmMinCtas CTAs.
-int gemm_tc_ctas_per_sm(int64_t M, int64_t N, int64_t split) {
-    const int64_t T = (N + 127) / 128;
-    return (gemm_tc_pad(M) <= 128 && T * split >= kTwoPerSmMinCtas) ? 2 : 1;
+    int64_t S = 1;
+    int cps = 1;
+    if (split_k > 0) {
+        S = split_k;
+        cps = (Mp <= 128 && T * S >= kTwoPerSmMinCtas) ? 2 : 1;
+    } else if (T > 0 && G > 0) {
+        S = tc_split_for(T, G, Mp, K, 152);
+        if (Mp <= 128) {
+            const int64_t S2 = tc_split_for(T, G, Mp, K, 2 * 152);
+            if (T * S2 >= kTwoPerSmMinCtas) {
+                S = S2;
+                cps = 2;
+            }
+        }
+    }
+    if (G == 0) S = 1;
+    if (S > G && G > 0) S = G;
+    if (!counters_ok) S = 1;
+    if (S == 1) cps = (Mp <= 128 && T >= kTwoPerSmMinCtas) ? 2 : 1;
+    g.split = (int)S;
+    g.tc_cps = cps;
+    return S > 1 ? S * Np * Mp * 4 : 0;
 }
 
 cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t s) {
@@ -697,10 +1199,12 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
     if (!enc) return cudaErrorNotSupported;
     TcParams tp;
     tp.Mp = (int)gemm_tc_pad(g.M);
-    const int cps = gemm_tc_ctas_per_sm(g.M, t.N, g.split);
+    const int cps = g.tc_cps;
     if (!tc_rings(tp, cps)) return cudaErrorInvalidConfiguration;
+    // a power of two >= max(32, Mp) columns per accumulator; the range kernel keeps two
     tp.tmem_cols = 32;
     while (tp.tmem_cols < tp.Mp) tp.tmem_cols <<= 1;
+    if (g.tc_ranges) tp.tmem_cols *= 2;
     tp.idesc = (1u << 4)                         // D: FP32
                | (1u << 7) | (1u << 10)          // A, B: BF16
                | ((uint32_t)(tp.Mp >> 3) << 17)  // N
@@ -743,8 +1247,9 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
             memset(&lmap, 0, sizeof lmap);
         }
     }
-    return cps > 1 ? launch_variant<8>(t, g, tp, map, hmap, lmap, s)
-                   : launch_variant<16>(t, g, tp, map, hmap, lmap, s);
+    if (g.tc_ranges) return launch_variant<16, true>(t, g, tp, map, hmap, lmap, s);
+    return cps > 1 ? launch_variant<8, false>(t, g, tp, map, hmap, lmap, s)
+                   : launch_variant<16, false>(t, g, tp, map, hmap, lmap, s);
 }
 
 }  // namespace w12

@@ -51,28 +51,32 @@ struct GemmArgs {
     uint16_t *Y;
     int64_t ldy;
     int64_t M;
-    int split;           // tensor-core path: K-chunks per stripe, S >= 1
-    // small-M path: the T*G (stripe, group) units are cut into segments of
-    // seglen units, each segment into `per` contiguous ranges (the first rem
-    // of q+1 units, the rest of q); `ranges` in all
+    int split;           // forced split (K-chunks per stripe or row tile), 1 otherwise
+    // the work units (small-M path: (stripe, group), u = stripe*G + group;
+    // tensor-core path: (row tile, group), u = row_tile*G + group) are cut
+    // into segments of seglen units, each segment into `per` contiguous
+    // ranges (the first rem of q+1 units, the rest of q); `ranges` in all
     int64_t ranges;
     int seglen, per, q, rem;
+    int tc_cps;          // tensor-core path: CTAs per SM of the build (1: 16 decoder warps, 2: 8)
+    bool tc_ranges;      // tensor-core path: balanced range cut (else S K-chunks per row tile)
     int max_ctas;        // 0 = occupancy-limited persistent grid
     bool overlap;        // launch as a programmatic dependent of the previous kernel
     bool nested8;        // multiply by the nested 8-bit view (hi plane only, escapes & 0xFFF0)
     bool test_stall;     // tensor-core path: make one bounded wait run out (tests of the timeout path)
-    float *partials;     // tensor-core path: [S][Mpad][Np]; small-M path: [2*ranges][16][MP] fp32
-    int32_t *counters;   // [Np/16] arrival counters (S > 1)
+    float *partials;     // tensor-core path: [S][Mpad][Np] (K-chunks) or [2*ranges][Mpad][128] (ranges);
+                         // small-M path: [2*ranges][16][MP] fp32
+    int32_t *counters;   // arrival counters per stripe (small-M) or row tile (tensor-core)
     int32_t *error;      // device error word
     uint32_t c28, c16;  // 1<<28, 16: multiplicands the decoder needs at run time
 };
 
 // Tensor-core path: tcgen05.mma with TMEM accumulators (M <= 256; partials
-// laid out [S][Mpad][Np]).
+// laid out [slots][Mpad][128]).
 cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t s);
-int gemm_tc_split(int64_t M, int64_t N, int64_t K);
-// 1 or 2: CTAs per SM of the tensor-core build a launch with this split takes
-int gemm_tc_ctas_per_sm(int64_t M, int64_t N, int64_t split);
+// The scheme, cut and build of the tensor-core path for (M, N, K) and a
+// forced split (0 = automatic); returns the bytes of FP32 partials it needs.
+int64_t gemm_tc_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters_ok, GemmArgs &g);
 int64_t gemm_tc_pad(int64_t M);
 
 // Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).

@@ -79,4 +79,24 @@ __device__ __forceinline__ uint32_t escape_tiles(const EscBatch &b, int lane) {
     return __reduce_or_sync(kFull, bit);
 }
 
+// Ranges: work units are cut into segments of g.seglen units (the whole
+// tensor, or one stripe / row tile), and each segment into g.per contiguous
+// ranges: the first g.rem ranges of a segment hold g.q + 1 units, the others
+// g.q.  The small-M kernel numbers its units u = stripe*G + group, the
+// tensor-core kernel u = row_tile*G + group; both planes and the escape
+// offsets are stored stripe-major with whole groups, so a range is one
+// contiguous stream however many stripe boundaries it crosses.  All of it
+// is 32-bit integer arithmetic (unit and range counts are below 2^31).
+__device__ __forceinline__ int range_begin(int v, const GemmArgs &g) {
+    const int seg = v / g.per, j = v - seg * g.per;
+    return seg * g.seglen + j * g.q + (j < g.rem ? j : g.rem);
+}
+// the range holding unit u
+__device__ __forceinline__ int range_of(int u, const GemmArgs &g) {
+    const int seg = u / g.seglen, x = u - seg * g.seglen;
+    const int big = g.rem * (g.q + 1);  // units in the segment's longer ranges
+    const int j = x < big ? x / (g.q + 1) : g.rem + (x - big) / g.q;
+    return seg * g.per + j;
+}
+
 }  // namespace w12

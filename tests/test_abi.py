@@ -98,7 +98,7 @@ def tc_split(w12lib, M, N, K, opts=None):
     (64, 34816, 5120, 1),   # 272 row tiles fill two CTAs per SM without a split
     (24, 5120, 17408, 7),   # 40 x 7 = 280
     (128, 5120, 17408, 7),
-    (144, 5120, 17408, 3),  # Mpad > 128 never takes two CTAs per SM
+    (144, 5120, 8192, 3),   # Mpad > 128 never takes two CTAs per SM (40 x 32 units: too few for ranges)
     (24, 1024, 5120, 16),   # 8 row tiles: at most 16 chunks
     (24, 1024, 1024, 3),    # cap 3.2 (below the 4 column groups whenever Mpad > 25.6)
 ])
@@ -107,6 +107,26 @@ def test_tc_split_rule(M, N, K, S, w12lib):
     slots when that grid has >= 258 CTAs and Mpad <= 128, else over 152 slots; each
     capped by the column groups, 16, and the partial traffic 0.1*K/Mpad."""
     assert tc_split(w12lib, M, N, K) == S
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (256, 34816, 5120),   # 272 row tiles x 20 groups = 5440 units
+    (256, 5120, 17408),   # 40 x 68 = 2720
+    (144, 5120, 17408),
+    (136, 9728, 8192),    # 76 x 32 = 2432 = 16 x 152: the smallest such grid
+])
+def test_tc_balanced_ranges_plan(M, N, K, w12lib):
+    """Mpad > 128 and at least 16 (row tile, group) units per SM: 152 balanced ranges, two FP32
+    slots of [Mpad][128] each (a range's first and last piece), instead of K-chunks."""
+    mp = (M + 15) // 16 * 16
+    assert w12lib.w12_gemm_workspace_bytes(M, N, K, w12lib.make_opts()) == 256 + 4 * 65536 + 2 * 152 * mp * 128 * 4
+
+
+def test_tc_balanced_ranges_not_taken(w12lib):
+    # fewer than 16 units per SM (76 x 31 = 2356), Mpad <= 128, or a forced split: K-chunks
+    assert tc_split(w12lib, 136, 9728, 7936) == 2  # 152/76 = 2 chunks
+    assert tc_split(w12lib, 128, 9728, 8192) == 4  # Mpad <= 128: 76 row tiles x 4 = 304 CTAs, two per SM
+    assert tc_split(w12lib, 256, 34816, 5120, w12lib.make_opts(split_k=2)) == 2
 
 
 def test_tc_split_at_most_one_chunk_per_group(w12lib):

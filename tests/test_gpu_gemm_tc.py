@@ -78,6 +78,21 @@ def test_tc_both_builds(M, split, kind, w12lib, oracle):
     parity(w12lib, oracle, W, A, opts=w12lib.make_opts(split_k=split), reps=2)
 
 
+# Balanced ranges (Mpad > 128 and >= 16 units of (128-row tile, 256-column
+# group) per SM): 152 contiguous ranges of units, one per CTA.  A range's
+# first and last pieces are partial (summed in range order by the row
+# tile's last arriving CTA); the row tiles in between are stored directly.
+@pytest.mark.parametrize("N,K,M,kind", [
+    (9728, 8192, 136, "dense"),         # 76 x 32 = 2432 units, 16 per range: 2 pieces per range
+    (9700, 8192, 256, "adversarial"),   # ragged last row tile
+    (31232, 2560, 144, "dense"),        # 244 x 10 units, ranges of ~1.6 row tiles
+])
+def test_tc_balanced_ranges(N, K, M, kind, w12lib, oracle):
+    W = (synth.dense_weights if kind == "dense" else synth.adversarial_weights)(N, K, seed=N + M)
+    A = synth.activations(M, K, seed=3600 + M)
+    parity(w12lib, oracle, W, A, reps=2)
+
+
 def test_tc_two_per_sm_automatic_split(w12lib, oracle):
     """QKV-sized layer at M = 24: the automatic split (5) fills two CTAs per SM."""
     W = synth.dense_weights(7168, 5120, seed=1000)
@@ -113,7 +128,7 @@ def test_tc_workspace_error_word_clear(w12lib, oracle):
     assert int(ws.buf[256:256 + 4 * 64].sum()) == 0
 
 
-@pytest.mark.parametrize("name,N,K", [("o", 5120, 5120), ("down", 5120, 17408)])
+@pytest.mark.parametrize("name,N,K", [("o", 5120, 5120), ("down", 5120, 17408), ("gate_up", 34816, 5120)])
 def test_tc_full_size_layers_sampled(name, N, K, w12lib, oracle):
     seed = 1000 + [s[0] for s in synth.LAYER_SHAPES].index(name)
     Wd = synth.dense_weights_device(N, K, seed=seed)

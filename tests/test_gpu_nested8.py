@@ -43,6 +43,17 @@ def test_nested8_parity(N, K, M, kind, w12lib, oracle):
     assert np.array_equal(Y, Yt)
 
 
+def test_nested8_balanced_ranges(w12lib, oracle):
+    """Mpad > 128 on 2432 (row tile, group) units: the balanced-range kernel."""
+    W = synth.adversarial_weights(9728, 8192, seed=146)
+    A = synth.activations(136, 8192, seed=147)
+    st, ref = oracle.encode(W)
+    st, Yr, Y64, mag = oracle.gemm_nested8(A, ref)
+    t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+    Y = synth.tensor_to_bits(w12lib.w12_gemm(synth.bits_to_tensor(A, "cuda"), t, opts=nested(w12lib)))
+    assert gemm_tolerance_failures(Y, Yr, Y64, mag).size == 0
+
+
 def test_nested8_two_ctas_per_sm(w12lib, oracle):
     """A split-9 grid of 288 CTAs: the tensor-core build with two CTAs per SM."""
     W = synth.adversarial_weights(4096, 2304, seed=144)

@@ -18,21 +18,22 @@ from w12_tol import gemm_tolerance_failures
 pytestmark = pytest.mark.gpu
 
 
-# one K-chunk; a split of the reduction; a split-9 grid of 288 CTAs (two CTAs per SM)
-@pytest.mark.parametrize("N,K,split", [(1024, 1024, 0), (1024, 8192, 0), (4096, 2304, 9)])
-def test_stalled_wait_reports_timeout_and_the_context_stays_usable(N, K, split, w12lib, oracle):
-    M = 32
+# one K-chunk; a split of the reduction; a split-9 grid of 288 CTAs (two CTAs
+# per SM); 152 balanced ranges (Mpad > 128, 2432 units)
+@pytest.mark.parametrize("N,K,split,M", [(1024, 1024, 0, 32), (1024, 8192, 0, 32), (4096, 2304, 9, 32),
+                                         (9728, 8192, 0, 136)])
+def test_stalled_wait_reports_timeout_and_the_context_stays_usable(N, K, split, M, w12lib, oracle):
     W = synth.dense_weights(N, K, seed=150 + K)
     A = synth.activations(M, K, seed=151)
     t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
     Ad = synth.bits_to_tensor(A, "cuda")
-    ws = w12lib.Workspace("cuda", 1 << 24)
+    ws = w12lib.Workspace("cuda", 1 << 25)
 
     w12lib.w12_gemm(Ad, t, workspace=ws, opts=w12lib.make_opts(flags=w12lib.W12_GEMM_TEST_STALL, split_k=split))
     torch.cuda.synchronize()
     assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_ERR_TIMEOUT
     assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_OK  # read and cleared
-    assert int(ws.buf[256:256 + 4 * 64].sum()) == 0  # no arrival counter left behind
+    assert int(ws.buf[256:256 + 4 * 256].sum()) == 0  # no arrival counter left behind
 
     st, ref = oracle.encode(W)
     st, Yr, Y64, mag = oracle.gemm(A, ref)
