@@ -465,6 +465,9 @@ def run_gpu(args):
         del stk
         torch.cuda.empty_cache()
 
+    # ---- best-first draft-tree node selection (the next row after the GEMM) ----
+    tree = tree_bench(dev, cpu=(rank == 0 and not args.no_cpu_baseline))
+
     # ---- what a plain device copy reaches at these sizes (context for the roofline) ----
     # MEASURED_PEAKS' HBM figure is a 2 GiB copy; a copy of one layer's W12 bytes
     # pays the same launch, ramp-up and tail costs that a single GEMM launch does.
@@ -512,6 +515,7 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
+        "tree": tree,
         "size_calibration": size_cal, "nested8": nested,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "matches_device_outputs": e2e_match,
                 "method": "per step: one pinned host->device copy of all 16 activations, the 16 w12_gemm calls "
@@ -570,6 +574,50 @@ class OracleSample:
                 break
             rows *= 2
         return rows
+
+
+TREE_CASES = (  # (requests, positions, candidates, budget, shared)
+    (1, 8, 8, 32, False),    # one request, 8-position lattice, 32 nodes
+    (1, 16, 8, 63, False),   # 16 positions, 63 nodes
+    (64, 8, 8, 32, False),   # a batch, 32 nodes per request
+    (8, 16, 8, 256, True),   # a node budget shared by 8 requests
+)
+
+
+def tree_bench(dev, cpu: bool):
+    """w12_tree_select on the pages' tree sizes (Dirichlet(0.3) log-probabilities):
+    device time per call (CUDA events over 200 calls) and, beside it, the oracle."""
+    res = {}
+    for R, D, C, B, shared in TREE_CASES:
+        rng = np.random.default_rng(R * 100 + D)
+        lp_h = np.log(rng.dirichlet(np.full(C, 0.3), size=(R, D))).astype(np.float32)
+        lp = torch.from_numpy(lp_h).to(dev)
+        call = w12.TreeCall(lp, B, shared)
+        for _ in range(10):
+            out = call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(200):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / 200
+        kept = int(out["count"].sum())
+        row = {"us": round(us, 2), "nodes": kept, "nodes_per_s": round(kept / (us * 1e-6), 1)}
+        if cpu:
+            from oracle import tree as tree_oracle
+            t0 = time.perf_counter()
+            n = 0
+            while time.perf_counter() - t0 < 0.5:
+                tree_oracle.select(lp_h, B, shared)
+                n += 1
+            row["oracle_us"] = round((time.perf_counter() - t0) * 1e6 / n, 1)
+        res[f"R{R}_D{D}_C{C}_B{B}_{'shared' if shared else 'per_request'}"] = row
+    res["note"] = ("GPU: one warp per request (best-first with first-child / next-sibling successors) plus a "
+                   "one-warp merge for a shared budget; the time includes the host launch of 2 kernels. "
+                   "oracle_us: the Python oracle (test infrastructure), one host thread")
+    return res
 
 
 def cpu_baseline(layers=None, budget_s=10.0):

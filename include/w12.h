@@ -221,6 +221,44 @@ w12_status w12_gemm_noalloc(const uint16_t *A, int64_t lda, const w12_tensor *w,
  * or W12_ERR_TIMEOUT. */
 w12_status w12_gemm_workspace_status(void *workspace, size_t ws_bytes, w12_stream_t stream);
 
+/* ---- w12_tree_select ----  Best-first draft-tree node selection: which
+ * drafted nodes a verify pass checks (paper: the news-article page's part
+ * "(2) best-first tree verification"; the English summary's section 4.4, a
+ * node budget shared across requests, and 6.4, best-first trees on an
+ * 8-position lattice).
+ *   lp: device FP32 [R][D][C], 4-byte aligned: lp[r][d][c] is the drafter's
+ *     log-probability of candidate c at position d of request r, given the
+ *     prefix before it.  Values must be finite (NaN gives an unspecified
+ *     order).
+ *   A node is a path (c_0..c_{t-1}) from the root, depth t in 1..D; its
+ *   score is the FP32 sum lp[r][0][c_0] + lp[r][1][c_1] + ..., added left to
+ *   right.  Nodes are kept best-first in the order: score descending, then
+ *   depth, then request, then path (lexicographic on candidate indices).
+ *   A child never comes before its parent, so the kept nodes form a tree.
+ *   shared = 0: the first `budget` nodes of every request, on its own;
+ *   shared = 1: the first `budget` nodes over all requests.
+ * Outputs (device, caller-owned), one entry per kept node:
+ *   req (int32), depth (int32), path (uint64, 8-byte aligned: candidate
+ *   indices, 4 bits per position, position 0 in the lowest bits), score
+ *   (float), parent (int32: output index of the parent node, -1 at depth 1).
+ *   shared = 1: `budget` entries, filled in the order above; count[0] = the
+ *   number kept (less than budget only if the lattices hold fewer nodes).
+ *   shared = 0: R segments of `budget` entries, request r's nodes in order
+ *   at [r*budget, r*budget + count[r]); count has R entries.
+ * workspace: device, w12_tree_workspace_bytes(R, budget) bytes, 16-byte
+ * aligned, no initial contents needed.  Limits: 1 <= R <= W12_TREE_MAX_REQUESTS,
+ * 1 <= D <= W12_TREE_MAX_DEPTH, 1 <= C <= W12_TREE_MAX_CANDIDATES,
+ * 1 <= budget <= W12_TREE_MAX_BUDGET (W12_ERR_INVALID otherwise).
+ * Asynchronous. */
+#define W12_TREE_MAX_DEPTH 16
+#define W12_TREE_MAX_CANDIDATES 16
+#define W12_TREE_MAX_BUDGET 256
+#define W12_TREE_MAX_REQUESTS 65536
+size_t w12_tree_workspace_bytes(int32_t R, int32_t budget);
+w12_status w12_tree_select(const float *lp, int32_t R, int32_t D, int32_t C, int32_t budget, int32_t shared,
+                           int32_t *req, int32_t *depth, uint64_t *path, float *score, int32_t *parent,
+                           int32_t *count, void *workspace, size_t ws_bytes, w12_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *w12_status_string(w12_status status);
 

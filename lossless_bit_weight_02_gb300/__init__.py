@@ -47,6 +47,7 @@ EXPORTS = (
     "w12_esc_ptr_len", "w12_encode",
     "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
     "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_noalloc", "w12_gemm_workspace_status",
+    "w12_tree_workspace_bytes", "w12_tree_select",
     "w12_status_string", "w12_version",
 )
 
@@ -108,6 +109,9 @@ def load(path: str | None = None):
             "w12_gemm_noalloc": (st, [vp, i64, ctypes.POINTER(_Tensor), vp, i64, i64,
                                       ctypes.POINTER(GemmOpts), vp]),
             "w12_gemm_workspace_status": (st, [vp, sz, vp]),
+            "w12_tree_workspace_bytes": (sz, [ctypes.c_int32, ctypes.c_int32]),
+            "w12_tree_select": (st, [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "w12_status_string": (ctypes.c_char_p, [st]),
             "w12_version": (ctypes.c_int32, []),
         }
@@ -350,6 +354,52 @@ def w12_gemm_noalloc(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, opts: GemmO
                                    ctypes.c_void_p(Y.data_ptr()), Y.stride(0), A.shape[0], ctypes.byref(o),
                                    _stream(stream)), "w12_gemm_noalloc")
     return Y
+
+
+W12_TREE_MAX_DEPTH = 16
+W12_TREE_MAX_CANDIDATES = 16
+W12_TREE_MAX_BUDGET = 256
+
+
+class TreeCall:
+    """w12_tree_select with its outputs and workspace allocated and every
+    argument marshalled once: calling the object only invokes the C entry
+    point.  lp: CUDA float32 [R, D, C] log-probabilities (read at each call).
+    Outputs (device): req, depth, path (int64 holding the uint64 bits), score,
+    parent ([budget] when shared, else [R, budget]) and count ([1] or [R])."""
+
+    def __init__(self, lp: torch.Tensor, budget: int, shared: bool, stream=None):
+        if not (lp.is_cuda and lp.dtype == torch.float32 and lp.dim() == 3 and lp.is_contiguous()):
+            raise ValueError("lp must be a contiguous CUDA float32 [R, D, C] tensor")
+        R, D, C = lp.shape
+        n = budget if shared else R * budget
+        dev = lp.device
+        self.out = {"req": torch.empty(n, dtype=torch.int32, device=dev),
+                    "depth": torch.empty(n, dtype=torch.int32, device=dev),
+                    "path": torch.empty(n, dtype=torch.int64, device=dev),
+                    "score": torch.empty(n, dtype=torch.float32, device=dev),
+                    "parent": torch.empty(n, dtype=torch.int32, device=dev),
+                    "count": torch.empty(1 if shared else R, dtype=torch.int32, device=dev)}
+        need = int(load().w12_tree_workspace_bytes(R, budget))
+        self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self._keep = lp
+        self._fn = load().w12_tree_select
+        self._args = (ctypes.c_void_p(lp.data_ptr()), R, D, C, budget, 1 if shared else 0,
+                      *(ctypes.c_void_p(self.out[k].data_ptr())
+                        for k in ("req", "depth", "path", "score", "parent", "count")),
+                      ctypes.c_void_p(self._ws.data_ptr()), self._ws.numel(), _stream(stream))
+        if not shared:
+            for k in ("req", "depth", "path", "score", "parent"):
+                self.out[k] = self.out[k].view(R, budget)
+
+    def __call__(self) -> dict:
+        _check(self._fn(*self._args), "w12_tree_select")
+        return self.out
+
+
+def w12_tree_select(lp: torch.Tensor, budget: int, shared: bool, stream=None) -> dict:
+    """Best-first draft-tree node selection (w12_tree_select); see TreeCall."""
+    return TreeCall(lp, budget, shared, stream)()
 
 
 def w12_gemm_workspace_status(workspace: Workspace, stream=None) -> int:

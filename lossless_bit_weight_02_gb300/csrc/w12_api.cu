@@ -253,6 +253,28 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     return cuda_status(launch_gemm_mma(view_of(w), g, s));
 }
 
+size_t w12_tree_workspace_bytes(int32_t R, int32_t budget) {
+    if (R < 1 || R > W12_TREE_MAX_REQUESTS || budget < 1 || budget > W12_TREE_MAX_BUDGET) return 0;
+    return tree_workspace_bytes(R, budget);
+}
+
+w12_status w12_tree_select(const float *lp, int32_t R, int32_t D, int32_t C, int32_t budget, int32_t shared,
+                           int32_t *req, int32_t *depth, uint64_t *path, float *score, int32_t *parent,
+                           int32_t *count, void *workspace, size_t ws_bytes, w12_stream_t stream) {
+    if (R < 1 || R > W12_TREE_MAX_REQUESTS || D < 1 || D > W12_TREE_MAX_DEPTH || C < 1 ||
+        C > W12_TREE_MAX_CANDIDATES || budget < 1 || budget > W12_TREE_MAX_BUDGET || (shared != 0 && shared != 1))
+        return W12_ERR_INVALID;
+    if (!lp || !req || !depth || !path || !score || !parent || !count || !workspace) return W12_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(lp) & 3) || (reinterpret_cast<uintptr_t>(path) & 7) ||
+        (reinterpret_cast<uintptr_t>(req) & 3) || (reinterpret_cast<uintptr_t>(depth) & 3) ||
+        (reinterpret_cast<uintptr_t>(score) & 3) || (reinterpret_cast<uintptr_t>(parent) & 3) ||
+        (reinterpret_cast<uintptr_t>(count) & 3) || !aligned16(workspace))
+        return W12_ERR_ALIGN;
+    if (ws_bytes < tree_workspace_bytes(R, budget)) return W12_ERR_CAPACITY;
+    return cuda_status(launch_tree_select(lp, R, D, C, budget, shared != 0, req, depth, path, score, parent, count,
+                                         workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w12_status w12_gemm_workspace_status(void *workspace, size_t ws_bytes, w12_stream_t stream) {
     if (!workspace || ws_bytes < 256) return W12_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

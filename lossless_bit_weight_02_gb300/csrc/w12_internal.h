@@ -79,6 +79,12 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
 int64_t gemm_tc_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters_ok, GemmArgs &g);
 int64_t gemm_tc_pad(int64_t M);
 
+// Best-first draft-tree node selection (w12_tree.cu).
+size_t tree_workspace_bytes(int64_t R, int64_t budget);
+cudaError_t launch_tree_select(const float *lp, int R, int D, int C, int budget, bool shared, int32_t *req,
+                               int32_t *depth, uint64_t *path, float *score, int32_t *parent, int32_t *count,
+                               void *workspace, cudaStream_t s);
+
 // Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).
 cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s);
 int64_t gemm_mma_partial_cols(int64_t M);  // MP

@@ -169,3 +169,21 @@ def test_invalid_arguments_rejected_on_host(w12lib):
     st = lib.w12_verify_roundtrip(ctypes.c_void_p(4096), 64, ctypes.byref(t2), ctypes.byref(nm),
                                   ctypes.c_void_p(16384), 4, None)
     assert st == w12lib.W12_ERR_CAPACITY
+
+
+def test_tree_select_argument_checks(w12lib):
+    """Host-side validation of w12_tree_select: nothing is launched (no GPU needed)."""
+    lib = w12lib.load()
+    assert lib.w12_tree_workspace_bytes(0, 8) == 0 and lib.w12_tree_workspace_bytes(4, 257) == 0
+    assert lib.w12_tree_workspace_bytes(64, 63) > 0
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation
+    args = [p] * 6 + [p, ctypes.c_size_t(1 << 30), None]
+    for R, D, C, B, shared in ((0, 8, 8, 32, 0), (4, 0, 8, 32, 0), (4, 17, 8, 32, 0), (4, 8, 17, 32, 0),
+                               (4, 8, 8, 0, 0), (4, 8, 8, 257, 1), (4, 8, 8, 32, 2)):
+        assert lib.w12_tree_select(p, R, D, C, B, shared, *args) == w12lib.W12_ERR_INVALID
+    assert lib.w12_tree_select(None, 4, 8, 8, 32, 0, *args) == w12lib.W12_ERR_INVALID
+    odd = ctypes.c_void_p((1 << 20) + 4)  # path must be 8-byte aligned
+    assert lib.w12_tree_select(p, 4, 8, 8, 32, 0, p, p, odd, p, p, p, p, ctypes.c_size_t(1 << 30),
+                               None) == w12lib.W12_ERR_ALIGN
+    small = ctypes.c_size_t(lib.w12_tree_workspace_bytes(4, 32) - 1)
+    assert lib.w12_tree_select(p, 4, 8, 8, 32, 0, p, p, p, p, p, p, p, small, None) == w12lib.W12_ERR_CAPACITY
