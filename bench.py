@@ -587,6 +587,8 @@ TREE_CASES = (  # (requests, positions, candidates, budget, shared)
 def tree_bench(dev, cpu: bool):
     """w12_tree_select on the pages' tree sizes (Dirichlet(0.3) log-probabilities):
     device time per call (CUDA events over 200 calls) and, beside it, the oracle."""
+    import torch
+    import lossless_bit_weight_02_gb300 as w12
     res = {}
     for R, D, C, B, shared in TREE_CASES:
         rng = np.random.default_rng(R * 100 + D)
@@ -604,7 +606,27 @@ def tree_bench(dev, cpu: bool):
         torch.cuda.synchronize()
         us = a.elapsed_time(b) * 1e3 / 200
         kept = int(out["count"].sum())
-        row = {"us": round(us, 2), "nodes": kept, "nodes_per_s": round(kept / (us * 1e-6), 1)}
+        # device time without the host: 20 calls captured in a CUDA graph, replayed
+        gs = torch.cuda.Stream(dev)
+        gcall = w12.TreeCall(lp, B, shared, stream=gs)
+        with torch.cuda.stream(gs):
+            gcall()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(20):
+                gcall()
+        with torch.cuda.stream(gs):  # replays, and the events around them, on one stream
+            graph.replay()
+            torch.cuda.synchronize()
+            a.record(gs)
+            for _ in range(10):
+                graph.replay()
+            b.record(gs)
+        torch.cuda.synchronize()
+        g_us = a.elapsed_time(b) * 1e3 / 200
+        row = {"us": round(us, 2), "us_graph": round(g_us, 2), "nodes": kept,
+               "nodes_per_s": round(kept / (g_us * 1e-6), 1)}
         if cpu:
             from oracle import tree as tree_oracle
             t0 = time.perf_counter()
@@ -614,9 +636,11 @@ def tree_bench(dev, cpu: bool):
                 n += 1
             row["oracle_us"] = round((time.perf_counter() - t0) * 1e6 / n, 1)
         res[f"R{R}_D{D}_C{C}_B{B}_{'shared' if shared else 'per_request'}"] = row
-    res["note"] = ("GPU: one warp per request (best-first with first-child / next-sibling successors) plus a "
-                   "one-warp merge for a shared budget; the time includes the host launch of 2 kernels. "
-                   "oracle_us: the Python oracle (test infrastructure), one host thread")
+    res["note"] = ("GPU: one warp per request (best-first with first-child / next-sibling successors); a shared "
+                   "budget adds a one-warp merge (and, if a short first-pass list runs out, a second pass). us: "
+                   "eager calls back to back (host launch included); us_graph: the same calls replayed from a "
+                   "CUDA graph (device time; nodes_per_s uses it). oracle_us: the Python oracle (test "
+                   "infrastructure), one host thread")
     return res
 
 

@@ -19,8 +19,13 @@
 // frontier entry `budget` times yields the request's first nodes in order.
 // The frontier lives in shared memory (at most budget + 1 entries); each
 // step is a lane scan plus a shuffle argmax.
-// k_tree_merge (shared budget): one warp merges the requests' sorted lists
-// in the total order and rewrites parent indices.
+// Per-request budget: the search writes the output directly.
+// Shared budget: a first search keeps K1 = min(budget, 2*ceil(budget/R) + 4)
+// nodes per request, and k_tree_merge (one warp) merges the requests' sorted
+// lists in the total order, rewriting parent indices.  If the merge needs a
+// node beyond a list that was cut short, the result is not yet known: it
+// raises a flag, and a second search and merge (which return at once when
+// the flag is clear) redo the work with `budget` nodes per request.
 #include <cstdint>
 
 #include "w12.h"
@@ -34,7 +39,7 @@ constexpr int kMaxDepth = W12_TREE_MAX_DEPTH;      // 16: 4-bit path fields in 6
 constexpr int kMaxCand = W12_TREE_MAX_CANDIDATES;  // 16
 constexpr int kMaxBudget = W12_TREE_MAX_BUDGET;    // 256
 constexpr int kSlotsPerLane = (kMaxBudget + 1 + 31) / 32;  // frontier capacity per lane
-constexpr int kWarpsPerBlock = 4;
+constexpr int kWarpsPerBlock = 2;  // static shared memory: 2 x 12.8 KB
 
 // Paths are kept as lexicographic keys: position i in the nibble at bits
 // 60-4i.., so that for equal depths the numeric order is the path order.
@@ -42,29 +47,74 @@ __device__ __forceinline__ uint64_t lex_put(uint64_t key, int pos, uint32_t v) {
     const int sh = 60 - 4 * pos;
     return (key & ~(0xFull << sh)) | ((uint64_t)v << sh);
 }
-__device__ __forceinline__ uint32_t lex_get(uint64_t key, int pos) { return (uint32_t)(key >> (60 - 4 * pos)) & 0xFu; }
-// position 0 in the lowest nibble (the output form)
-__device__ __forceinline__ uint64_t lex_to_path(uint64_t key) {
-    uint64_t p = 0;
+
+struct TreeOut {
+    int32_t *req, *depth;
+    uint64_t *path;
+    float *score;
+    int32_t *parent, *count;
+};
+
+// Order key of a node within a request: the score made an unsigned integer
+// that grows with the score (+0 and -0 alike), then depth (smaller first),
+// so that "a before b" is k1a > k1b, or k1a == k1b and path key a < b.
+__device__ __forceinline__ uint64_t order_k1(float score, int depth) {
+    const uint32_t u = __float_as_uint(__fadd_rn(score, 0.0f));  // -0 -> +0
+    const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((uint64_t)o << 32) | (uint32_t)(0xFFFF - depth);
+}
+__device__ __forceinline__ int k1_depth(uint64_t k1) { return 0xFFFF - (int)(k1 & 0xFFFF); }
+__device__ __forceinline__ bool before_k(uint64_t k1a, uint64_t ka, uint64_t k1b, uint64_t kb) {
+    return k1a > k1b || (k1a == k1b && ka < kb);
+}
+
+// The lane holding the warp's first entry in the order, or -1 if no lane
+// has one.  Each lane offers its own best (have, k1, key; `tag` is compared
+// after k1 and before key: the request in the merge, 0 in the search).
+// Fast path: one lane holds the largest score (the high word of k1, never
+// 0 for a finite score); otherwise a shuffle tournament on the full keys.
+__device__ __forceinline__ int warp_first(bool have, uint64_t k1, int tag, uint64_t key) {
+    const uint32_t hi = have ? (uint32_t)(k1 >> 32) : 0u;
+    const uint32_t m = __reduce_max_sync(kFull, hi);
+    const uint32_t ball = __ballot_sync(kFull, have && hi == m);
+    if (ball == 0) return -1;
+    if ((ball & (ball - 1)) == 0) return __ffs(ball) - 1;
+    bool h = have && hi == m;
+    int bl = h ? (int)(threadIdx.x & 31) : -1;
+    uint64_t b1 = k1, bk = key;
+    int bt = tag;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) p |= (uint64_t)lex_get(key, i) << (4 * i);
-    return p;
+    for (int off = 16; off > 0; off >>= 1) {
+        const int ol = __shfl_xor_sync(kFull, bl, off);
+        const uint64_t o1 = __shfl_xor_sync(kFull, b1, off);
+        const int ot = __shfl_xor_sync(kFull, bt, off);
+        const uint64_t ok = __shfl_xor_sync(kFull, bk, off);
+        const bool better = o1 > b1 || (o1 == b1 && (ot < bt || (ot == bt && ok < bk)));
+        if (ol >= 0 && (bl < 0 || better)) {
+            bl = ol;
+            b1 = o1;
+            bt = ot;
+            bk = ok;
+        }
+    }
+    return bl;
 }
 
 // One kept node as the per-request lists store it.
 struct TreeNode {
-    float score;
-    int32_t depth;
-    int32_t parent;  // index in the same request's list, -1 at depth 1
-    int32_t pad;
-    uint64_t key;    // lexicographic path key
+    uint64_t k1;    // order key (score, depth)
+    uint64_t key;   // lexicographic path key
+    uint64_t path;  // output form of the path
+    float score;    // the FP32 sum itself (the order key maps -0 to +0)
+    int32_t parent; // index in the same request's list, -1 at depth 1
 };
 
 struct Frontier {
-    float score, pscore;  // the node's score, its parent's (0 at depth 1)
-    int32_t depth, parent;
-    uint64_t rank_key;    // ranks, lexicographic layout
-    uint64_t key;         // candidate indices, lexicographic layout
+    uint64_t k1, key, path;
+    float score;
+    float pscore;      // the parent's score (unused at depth 1)
+    int16_t parent;    // index in the request's list, -1 at depth 1 (budget <= 256)
+    int16_t last_rank; // rank of the candidate at the last position
 };
 
 struct WarpSmem {
@@ -73,19 +123,20 @@ struct WarpSmem {
     Frontier f[kSlotsPerLane * 32];
 };
 
-// true when node a comes before node b in the order (same request)
-__device__ __forceinline__ bool before(float sa, int da, uint64_t ka, float sb, int db, uint64_t kb) {
-    if (sa != sb) return sa > sb;
-    if (da != db) return da < db;
-    return ka < kb;
-}
-
+// mode 0: per-request budget, output written directly (K = budget);
+// mode 1: first search of a shared budget (K = K1, lists of stride `stride`);
+// mode 2: second search (K = stride = budget), only when *flag is set.
 __global__ __launch_bounds__(32 * kWarpsPerBlock) void k_tree_topk(const float *__restrict__ lp, int R, int D, int C,
-                                                                   int K, TreeNode *__restrict__ lists,
-                                                                   int32_t *__restrict__ counts) {
+                                                                   int K, int stride, int mode,
+                                                                   TreeNode *__restrict__ lists,
+                                                                   int32_t *__restrict__ counts,
+                                                                   int32_t *__restrict__ more, int32_t *flag,
+                                                                   TreeOut o) {
     __shared__ WarpSmem sm[kWarpsPerBlock];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * kWarpsPerBlock + warp;
+    if (mode == 2 && *(volatile int32_t *)flag == 0) return;  // the first pass was enough
+    if (mode == 1 && blockIdx.x == 0 && threadIdx.x == 0) *flag = 0;
     if (r >= R) return;  // whole warps only
     WarpSmem &S = sm[warp];
     const float *L = lp + (int64_t)r * D * C;
@@ -105,207 +156,186 @@ __global__ __launch_bounds__(32 * kWarpsPerBlock) void k_tree_topk(const float *
     }
     __syncwarp();
 
-    int fsize = 1;
     if (lane == 0) {
         Frontier e;
         e.score = S.cand_lp[0][0];
+        e.k1 = order_k1(e.score, 1);
         e.pscore = 0.f;
-        e.depth = 1;
         e.parent = -1;
-        e.rank_key = 0;
+        e.last_rank = 0;
         e.key = lex_put(0, 0, S.cand_idx[0][0]);
+        e.path = S.cand_idx[0][0];
         S.f[0] = e;
     }
     __syncwarp();
-    TreeNode *out = lists + (int64_t)r * K;
-    int k = 0;
+    TreeNode *out = lists + (int64_t)r * stride;
+    const int64_t seg = (int64_t)r * K;  // mode 0: this request's output segment
+    int fsize = 1, k = 0;
     for (; k < K && fsize > 0; ++k) {
-        // the best frontier entry: lane scan, then a shuffle argmax
+        // this lane's best frontier entry, then the warp's
         int bi = -1;
-        float bs = 0.f;
-        int bd = 0;
-        uint64_t bk = 0;
-        for (int j = 0; j < kSlotsPerLane; ++j) {
-            const int i = lane + 32 * j;
-            if (i < fsize) {
-                const Frontier &e = S.f[i];
-                if (bi < 0 || before(e.score, e.depth, e.key, bs, bd, bk)) {
-                    bi = i;
-                    bs = e.score;
-                    bd = e.depth;
-                    bk = e.key;
-                }
+        uint64_t b1 = 0, bk = 0;
+        for (int i = lane; i < fsize; i += 32) {
+            const uint64_t k1 = S.f[i].k1, kk = S.f[i].key;
+            if (bi < 0 || before_k(k1, kk, b1, bk)) {
+                bi = i;
+                b1 = k1;
+                bk = kk;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const int oi = __shfl_xor_sync(kFull, bi, off);
-            const float os = __shfl_xor_sync(kFull, bs, off);
-            const int od = __shfl_xor_sync(kFull, bd, off);
-            const uint64_t ok = __shfl_xor_sync(kFull, bk, off);
-            if (oi >= 0 && (bi < 0 || before(os, od, ok, bs, bd, bk))) {
-                bi = oi;
-                bs = os;
-                bd = od;
-                bk = ok;
-            }
-        }
-        // every lane holds the same winner
+        bi = __shfl_sync(kFull, bi, warp_first(bi >= 0, b1, 0, bk));
+        // every lane reads the winner and the last entry, then lanes 0..2
+        // write in parallel: the output and the move of the last entry into
+        // the winner's slot; the first child; the next sibling.
+        const Frontier e = S.f[bi];
+        const Frontier last = S.f[fsize - 1];
+        const int t = k1_depth(e.k1);  // positions 0 .. t-1 are set
+        const bool child = t < D;
+        const int nr = e.last_rank + 1;
+        const bool sib = nr < C;
+        __syncwarp();
         if (lane == 0) {
-            const Frontier e = S.f[bi];
-            TreeNode n;
-            n.score = e.score;
-            n.depth = e.depth;
-            n.parent = e.parent;
-            n.pad = 0;
-            n.key = e.key;
-            out[k] = n;
-            // remove it, then add its first child and its next sibling
-            int sz = fsize - 1;
-            S.f[bi] = S.f[sz];
-            const int t = e.depth;  // positions 0 .. t-1 are set
-            if (t < D) {
-                Frontier c;
-                c.pscore = e.score;
-                c.score = __fadd_rn(e.score, S.cand_lp[t][0]);
-                c.depth = t + 1;
-                c.parent = k;
-                c.rank_key = lex_put(e.rank_key, t, 0);
-                c.key = lex_put(e.key, t, S.cand_idx[t][0]);
-                S.f[sz++] = c;
+            if (mode == 0) {
+                o.req[seg + k] = r;
+                o.depth[seg + k] = t;
+                o.path[seg + k] = e.path;
+                o.score[seg + k] = e.score;
+                o.parent[seg + k] = e.parent < 0 ? -1 : (int32_t)(seg + e.parent);
+            } else {
+                TreeNode n;
+                n.k1 = e.k1;
+                n.key = e.key;
+                n.path = e.path;
+                n.score = e.score;
+                n.parent = e.parent;
+                out[k] = n;
             }
-            const uint32_t nr = lex_get(e.rank_key, t - 1) + 1;
-            if ((int)nr < C) {
-                Frontier s;
-                s.pscore = e.pscore;
-                s.score = t == 1 ? S.cand_lp[0][nr] : __fadd_rn(e.pscore, S.cand_lp[t - 1][nr]);
-                s.depth = t;
-                s.parent = e.parent;
-                s.rank_key = lex_put(e.rank_key, t - 1, nr);
-                s.key = lex_put(e.key, t - 1, S.cand_idx[t - 1][nr]);
-                S.f[sz++] = s;
-            }
-            fsize = sz;
+            if (bi != fsize - 1) S.f[bi] = last;
+        } else if (lane == 1 && child) {
+            Frontier c;
+            c.pscore = e.score;
+            c.score = __fadd_rn(e.score, S.cand_lp[t][0]);
+            c.k1 = order_k1(c.score, t + 1);
+            c.parent = (int16_t)k;
+            c.last_rank = 0;
+            const uint32_t ci = S.cand_idx[t][0];
+            c.key = lex_put(e.key, t, ci);
+            c.path = e.path | ((uint64_t)ci << (4 * t));
+            S.f[fsize - 1] = c;
+        } else if (lane == 2 && sib) {
+            Frontier sb;
+            sb.pscore = e.pscore;
+            sb.score = t == 1 ? S.cand_lp[0][nr] : __fadd_rn(e.pscore, S.cand_lp[t - 1][nr]);
+            sb.k1 = order_k1(sb.score, t);
+            sb.parent = e.parent;
+            sb.last_rank = (int16_t)nr;
+            const uint32_t ci = S.cand_idx[t - 1][nr];
+            sb.key = lex_put(e.key, t - 1, ci);
+            sb.path = (e.path & ~(0xFull << (4 * (t - 1)))) | ((uint64_t)ci << (4 * (t - 1)));
+            S.f[fsize - 1 + (child ? 1 : 0)] = sb;
         }
-        fsize = __shfl_sync(kFull, fsize, 0);
+        fsize += (child ? 1 : 0) + (sib ? 1 : 0) - 1;
         __syncwarp();
     }
-    if (lane == 0) counts[r] = k;
-}
-
-// Per-request budget: the lists become the output, request after request in
-// segments of `budget` entries, parents as indices into the whole output.
-__global__ void k_tree_emit(const TreeNode *__restrict__ lists, const int32_t *__restrict__ counts, int R, int K,
-                            int32_t *req, int32_t *depth, uint64_t *path, float *score, int32_t *parent,
-                            int32_t *count) {
-    const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (x >= (int64_t)R * K) return;
-    const int r = (int)(x / K), i = (int)(x - (int64_t)r * K);
-    if (i == 0) count[r] = counts[r];
-    if (i >= counts[r]) return;
-    const TreeNode n = lists[x];
-    req[x] = r;
-    depth[x] = n.depth;
-    path[x] = lex_to_path(n.key);
-    score[x] = n.score;
-    parent[x] = n.parent < 0 ? -1 : (int32_t)((int64_t)r * K + n.parent);
+    if (lane == 0) {
+        if (mode == 0) {
+            o.count[r] = k;
+        } else {
+            counts[r] = k;
+            more[r] = fsize > 0;  // the list was cut short
+        }
+    }
 }
 
 // Shared budget: `budget` steps of a warp argmax over the requests' list
 // heads in the total order (the request is the third key).  map[r][i] is
 // the output index of list entry i of request r; a parent is emitted before
 // its children.
-__device__ __forceinline__ bool before_r(float sa, int da, int ra, uint64_t ka, float sb, int db, int rb,
-                                         uint64_t kb) {
-    if (sa != sb) return sa > sb;
-    if (da != db) return da < db;
+__device__ __forceinline__ bool before_r(uint64_t k1a, int ra, uint64_t ka, uint64_t k1b, int rb, uint64_t kb) {
+    if (k1a != k1b) return k1a > k1b;
     if (ra != rb) return ra < rb;
     return ka < kb;
 }
 
 __global__ __launch_bounds__(32) void k_tree_merge(const TreeNode *__restrict__ lists,
-                                                   const int32_t *__restrict__ counts, int R, int K, int budget,
-                                                   int32_t *__restrict__ heads, int32_t *__restrict__ map,
-                                                   int32_t *req, int32_t *depth, uint64_t *path, float *score,
-                                                   int32_t *parent, int32_t *count) {
+                                                   const int32_t *__restrict__ counts,
+                                                   const int32_t *__restrict__ more, int32_t *flag, int pass, int R,
+                                                   int K, int budget, int32_t *__restrict__ heads,
+                                                   int32_t *__restrict__ map, TreeOut o) {
     const int lane = threadIdx.x;
+    if (pass == 2 && *(volatile int32_t *)flag == 0) return;
     for (int r = lane; r < R; r += 32) heads[r] = 0;
     __syncwarp();
     int n_out = 0;
     for (; n_out < budget; ++n_out) {
         int br = -1;
-        float bs = 0.f;
-        int bd = 0;
-        uint64_t bk = 0;
+        uint64_t b1 = 0, bk = 0;
+        bool cut = false;  // a list cut short has run out: its next node is unknown
         for (int r = lane; r < R; r += 32) {
             const int h = heads[r];
+            if (pass == 1 && h == counts[r] && more[r]) cut = true;
             if (h < counts[r]) {
                 const TreeNode &n = lists[(int64_t)r * K + h];
-                if (br < 0 || before_r(n.score, n.depth, r, n.key, bs, bd, br, bk)) {
+                if (br < 0 || before_r(n.k1, r, n.key, b1, br, bk)) {
                     br = r;
-                    bs = n.score;
-                    bd = n.depth;
+                    b1 = n.k1;
                     bk = n.key;
                 }
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const int orr = __shfl_xor_sync(kFull, br, off);
-            const float os = __shfl_xor_sync(kFull, bs, off);
-            const int od = __shfl_xor_sync(kFull, bd, off);
-            const uint64_t ok = __shfl_xor_sync(kFull, bk, off);
-            if (orr >= 0 && (br < 0 || before_r(os, od, orr, ok, bs, bd, br, bk))) {
-                br = orr;
-                bs = os;
-                bd = od;
-                bk = ok;
-            }
+        const int wl = warp_first(br >= 0, b1, br, bk);
+        br = wl < 0 ? -1 : __shfl_sync(kFull, br, wl);
+        if (__any_sync(kFull, cut)) {  // redo with full lists
+            if (lane == 0) *flag = 1;
+            return;
         }
         if (br < 0) break;  // every list is exhausted (warp-uniform)
         if (lane == 0) {
             const int h = heads[br];
             const TreeNode n = lists[(int64_t)br * K + h];
-            req[n_out] = br;
-            depth[n_out] = n.depth;
-            path[n_out] = lex_to_path(n.key);
-            score[n_out] = n.score;
-            parent[n_out] = n.parent < 0 ? -1 : map[(int64_t)br * K + n.parent];
+            o.req[n_out] = br;
+            o.depth[n_out] = k1_depth(n.k1);
+            o.path[n_out] = n.path;
+            o.score[n_out] = n.score;
+            o.parent[n_out] = n.parent < 0 ? -1 : map[(int64_t)br * K + n.parent];
             map[(int64_t)br * K + h] = n_out;
             heads[br] = h + 1;
         }
         __syncwarp();
     }
-    if (lane == 0) *count = n_out;
+    if (lane == 0) *o.count = n_out;
 }
 
 }  // namespace
 
 size_t tree_workspace_bytes(int64_t R, int64_t budget) {
-    const size_t lists = (size_t)R * budget * sizeof(TreeNode);
-    return 256 + lists + (size_t)R * 4 * 2 + (size_t)R * budget * 4;
+    // flag | lists [R][budget] | counts, more, heads [R] | map [R][budget]
+    return 256 + (size_t)R * budget * sizeof(TreeNode) + (size_t)R * 4 * 3 + (size_t)R * budget * 4;
 }
 
 cudaError_t launch_tree_select(const float *lp, int R, int D, int C, int budget, bool shared, int32_t *req,
                                int32_t *depth, uint64_t *path, float *score, int32_t *parent, int32_t *count,
                                void *workspace, cudaStream_t s) {
     char *ws = static_cast<char *>(workspace);
+    int32_t *flag = reinterpret_cast<int32_t *>(ws);
     TreeNode *lists = reinterpret_cast<TreeNode *>(ws + 256);
     int32_t *counts = reinterpret_cast<int32_t *>(ws + 256 + (size_t)R * budget * sizeof(TreeNode));
-    int32_t *heads = counts + R;
+    int32_t *more = counts + R;
+    int32_t *heads = more + R;
     int32_t *map = heads + R;
+    const TreeOut o{req, depth, path, score, parent, count};
     const int blocks = (R + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    k_tree_topk<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(lp, R, D, C, budget, lists, counts);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (shared) {
-        k_tree_merge<<<1, 32, 0, s>>>(lists, counts, R, budget, budget, heads, map, req, depth, path, score, parent,
-                                      count);
-    } else {
-        const int64_t n = (int64_t)R * budget;
-        k_tree_emit<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(lists, counts, R, budget, req, depth, path, score,
-                                                                 parent, count);
+    const dim3 grid(blocks), block(32 * kWarpsPerBlock);
+    if (!shared) {
+        k_tree_topk<<<grid, block, 0, s>>>(lp, R, D, C, budget, budget, 0, lists, counts, more, flag, o);
+        return cudaGetLastError();
     }
+    int k1 = 2 * ((budget + R - 1) / R) + 4;
+    if (k1 > budget) k1 = budget;
+    k_tree_topk<<<grid, block, 0, s>>>(lp, R, D, C, k1, budget, 1, lists, counts, more, flag, o);
+    k_tree_merge<<<1, 32, 0, s>>>(lists, counts, more, flag, 1, R, budget, budget, heads, map, o);
+    k_tree_topk<<<grid, block, 0, s>>>(lp, R, D, C, budget, budget, 2, lists, counts, more, flag, o);
+    k_tree_merge<<<1, 32, 0, s>>>(lists, counts, more, flag, 2, R, budget, budget, heads, map, o);
     return cudaGetLastError();
 }
 

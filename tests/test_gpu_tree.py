@@ -88,3 +88,24 @@ def test_tree_select_worked_example(w12lib):
     for shared, budget, want in cases:
         got = gpu_select(w12lib, lp, budget, shared)
         assert got == [(r, t, tree.pack_path(p), s, pa) for r, t, p, s, pa in want]
+
+
+def test_tree_select_shared_budget_falls_back_when_one_request_dominates(w12lib):
+    """Request 0's log-probabilities are near 0, the others' near -10: the whole shared budget
+    goes to request 0, past its first-pass list (2*ceil(256/8) + 4 = 68 nodes), so the second
+    pass with full lists must run."""
+    rng = np.random.default_rng(12)
+    lp = np.log(rng.dirichlet(np.full(8, 0.3), size=(8, 16))).astype(np.float32) - 10
+    lp[0] = -rng.random((16, 8)).astype(np.float32) * 0.01
+    want = oracle_select(lp, 256, True)
+    assert all(n[0] == 0 for n in want)
+    check(w12lib, lp, 256, True)
+    # and the next call on the same lattice shape (first pass enough) is still right
+    check(w12lib, lattice(rng, 8, 16, 8, "dirichlet"), 256, True)
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_tree_select_signed_zero_scores(shared, w12lib):
+    """-0.0 log-probabilities: scores keep the sign of zero of the FP32 sums, and -0 ties +0."""
+    lp = np.array([[[-0.0, 0.0, -1.0], [-0.0, -0.5, 0.0]], [[0.0, -0.0, -2.0], [-0.25, -0.0, 0.0]]], np.float32)
+    check(w12lib, lp, 8, shared)
