@@ -86,6 +86,7 @@ def test_tc_both_builds(M, split, kind, w12lib, oracle):
     (9728, 8192, 136, "dense"),         # 76 x 32 = 2432 units, 16 per range: 2 pieces per range
     (9700, 8192, 256, "adversarial"),   # ragged last row tile
     (31232, 2560, 144, "dense"),        # 244 x 10 units, ranges of ~1.6 row tiles
+    (9728, 8000, 160, "adversarial"),   # ragged K (Kp = 8192): zero-padded columns in the last group
 ])
 def test_tc_balanced_ranges(N, K, M, kind, w12lib, oracle):
     W = (synth.dense_weights if kind == "dense" else synth.adversarial_weights)(N, K, seed=N + M)
