@@ -373,7 +373,7 @@ int w12ref_verify(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const ui
  * Every product of two BF16 values is exact in FP64; the products are added
  * in ascending k in FP64 and the sum is rounded once to BF16.  Optional
  * outputs: Y64 (the FP64 sum) and absdot (sum_k |A[m,k]|*|W[n,k]|), both
- * [M,N] row-major, used to judge tolerances. */
+ * [M,N] row-major, used by the tolerance rule. */
 int w12ref_gemm(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int64_t K,
                 const uint8_t *hi, const uint8_t *lo, const uint8_t *base,
                 const int32_t *esc_ptr, const uint32_t *esc, int64_t n_esc, uint16_t *Y, int64_t ldy, double *Y64, double *absdot)
