@@ -703,6 +703,17 @@ def run_case(args):
     i, N, K = shapes[args.case]
     Wd = synth.dense_weights_device(N, K, seed=1000 + i)
     t = w12.w12_encode(Wd)
+    if args.codec:  # encode, decode and verify of the layer, `iters` times each
+        out = torch.empty_like(Wd)
+        for _ in range(args.iters):
+            t = w12.w12_encode(Wd)
+            w12.w12_decode(t, out)
+            st, nm = w12.w12_verify_roundtrip(Wd, t)
+            assert st == w12.W12_OK and nm == 0
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), Wd.view(torch.int16))
+        print(f"case {args.case} codec: {args.iters} encode/decode/verify rounds, bit-exact")
+        return
     del Wd
     A = synth.activations_device(args.m, K, seed=2000 + 10 * args.m + i)
     Y = torch.empty(args.m, N, dtype=torch.bfloat16, device="cuda")
@@ -734,6 +745,7 @@ def main():
     ap.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack measurement")
     ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down)")
     ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--codec", action="store_true", help="with --case: encode, decode and verify the layer")
     ap.add_argument("--iters", type=int, default=5)
     args = ap.parse_args()
     if args.case:

@@ -59,9 +59,10 @@ __global__ __launch_bounds__(kWinWarps * 32) void k_window_count(
         for (int j = 0; j < 8; ++j) {
             const int e = (v[j] >> 7) & 0xFF;
             const bool counted = (k + j < K) && e >= 1 && e <= 254;
-            const unsigned key = counted ? (unsigned)e : 0x10000u;
-            const unsigned peers = __match_any_sync(kFull, key);
-            if (counted && lane == __ffs(peers) - 1) atomicAdd(&h[e], __popc(peers));
+            // plain shared-memory atomics: the hardware merges lanes that hit the
+            // same bin (grouping them first with __match_any_sync was 13% slower
+            // over the whole encode on GB300)
+            if (counted) atomicAdd(&h[e], 1);
         }
     }
     __syncwarp();
