@@ -26,10 +26,14 @@ __device__ __forceinline__ void load8(const uint16_t *row, bool vec, int64_t k, 
     }
 }
 
-__device__ __forceinline__ bool is_escape(uint16_t w, int b) {
-    const int e = (w >> 7) & 0xFF;
-    return e == 0 || e == 255 || e < b || e > b + 15;
+// Offset-and-mantissa field of w in the window of base b: (e-b)<<7 | m, in
+// [0, 0x7FF] exactly when e is in [b, b+15].  With b in [1, 239] every other
+// exponent lands outside that range as an unsigned value: e = 0 and e < b
+// give a negative difference, e = 255 and e > b+15 one of at least 0x800.
+__device__ __forceinline__ uint32_t window_field(uint16_t w, int b) {
+    return (uint32_t)((int)(w & 0x7FFF) - (b << 7));
 }
+__device__ __forceinline__ bool is_escape(uint16_t w, int b) { return window_field(w, b) > 0x7FFu; }
 
 // ---------------------------------------------------------------------------
 // a1 + a2: one warp per row.  Histogram of the exponent field over the row's
@@ -185,10 +189,10 @@ __global__ __launch_bounds__(512) void k_pack(const uint16_t *__restrict__ W, in
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const bool in = row_ok && (k + j < K);
-            const bool esc_ = in && is_escape(v[j], b);
+            const uint32_t f = window_field(v[j], b);
+            const bool esc_ = in && f > 0x7FFu;
             if (esc_) emask |= 1u << j;
-            const int e = (v[j] >> 7) & 0xFF;
-            rec[j] = (in && !esc_) ? (uint32_t)(((v[j] >> 15) << 11) | ((e - b) << 7) | (v[j] & 0x7F)) : 0u;
+            rec[j] = (in && !esc_) ? ((uint32_t)(v[j] >> 15) << 11) | f : 0u;  // s<<11 | (e-b)<<7 | m
         }
         // per-(c4, i) count and this lane's exclusive prefix inside its 8 lanes
         const int cnt = __popc(emask);
