@@ -21,11 +21,12 @@
 // step is a lane scan plus a shuffle argmax.
 // Per-request budget: the search writes the output directly.
 // Shared budget: a first search keeps K1 = min(budget, 2*ceil(budget/R) + 4)
-// nodes per request, and k_tree_merge (one warp) merges the requests' sorted
-// lists in the total order, rewriting parent indices.  If the merge needs a
-// node beyond a list that was cut short, the result is not yet known: it
-// raises a flag, and a second search and merge (which return at once when
-// the flag is clear) redo the work with `budget` nodes per request.
+// nodes per request; every list entry then finds its rank in the total order
+// over all lists (k_tree_rank, binary searches in parallel), which is its
+// output position, and k_tree_parents maps parent links to ranks.  If a list
+// that was cut short could still contribute, a flag is raised and a second
+// search / rank / parents pass (which return at once when the flag is clear)
+// redoes the work with `budget` nodes per request.
 #include <cstdint>
 
 #include "w12.h"
@@ -247,69 +248,88 @@ __global__ __launch_bounds__(32 * kWarpsPerBlock) void k_tree_topk(const float *
     }
 }
 
-// Shared budget: `budget` steps of a warp argmax over the requests' list
-// heads in the total order (the request is the third key).  map[r][i] is
-// the output index of list entry i of request r; a parent is emitted before
-// its children.
+// Shared budget: a node's output position is its rank, the number of list
+// entries (over all requests) that come before it in the order (score,
+// depth, request, path).  One warp per list entry; lane j binary-searches
+// the lists j, j + 32, ... (sorted in the order) for how many of their
+// entries come first.  map[r][k] = rank.  If the last entry of a list cut
+// short ranks inside the budget, the lists are not long enough: the flag is
+// raised and the second pass redoes everything with full lists (entries a
+// cut list lacks all come after its last entry, so when that entry ranks
+// outside the budget every rank inside it is exact).
 __device__ __forceinline__ bool before_r(uint64_t k1a, int ra, uint64_t ka, uint64_t k1b, int rb, uint64_t kb) {
     if (k1a != k1b) return k1a > k1b;
     if (ra != rb) return ra < rb;
     return ka < kb;
 }
 
-__global__ __launch_bounds__(32) void k_tree_merge(const TreeNode *__restrict__ lists,
+__global__ __launch_bounds__(256) void k_tree_rank(const TreeNode *__restrict__ lists,
                                                    const int32_t *__restrict__ counts,
                                                    const int32_t *__restrict__ more, int32_t *flag, int pass, int R,
-                                                   int K, int budget, int32_t *__restrict__ heads,
-                                                   int32_t *__restrict__ map, TreeOut o) {
-    const int lane = threadIdx.x;
+                                                   int K, int budget, int32_t *__restrict__ map, TreeOut o) {
     if (pass == 2 && *(volatile int32_t *)flag == 0) return;
-    for (int r = lane; r < R; r += 32) heads[r] = 0;
-    __syncwarp();
-    int n_out = 0;
-    for (; n_out < budget; ++n_out) {
-        int br = -1;
-        uint64_t b1 = 0, bk = 0;
-        bool cut = false;  // a list cut short has run out: its next node is unknown
-        for (int r = lane; r < R; r += 32) {
-            const int h = heads[r];
-            if (pass == 1 && h == counts[r] && more[r]) cut = true;
-            if (h < counts[r]) {
-                const TreeNode &n = lists[(int64_t)r * K + h];
-                if (br < 0 || before_r(n.k1, r, n.key, b1, br, bk)) {
-                    br = r;
-                    b1 = n.k1;
-                    bk = n.key;
-                }
-            }
+    const int lane = threadIdx.x & 31;
+    const int64_t x = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // list entry (warp-uniform)
+    if (x >= (int64_t)R * K) return;
+    const int r = (int)(x / K), k = (int)(x - (int64_t)r * K);
+    if (k >= counts[r]) return;
+    const TreeNode n = lists[x];
+    int64_t rank = 0;
+    for (int q = lane; q < R; q += 32) {
+        if (q == r) {
+            rank += k;  // its own list is sorted
+            continue;
         }
-        const int wl = warp_first(br >= 0, b1, br, bk);
-        br = wl < 0 ? -1 : __shfl_sync(kFull, br, wl);
-        if (__any_sync(kFull, cut)) {  // redo with full lists
-            if (lane == 0) *flag = 1;
-            return;
+        int lo = 0, hi = counts[q];  // first entry of list q that does not come before n
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            const TreeNode &m = lists[(int64_t)q * K + mid];
+            if (before_r(m.k1, q, m.key, n.k1, r, n.key))
+                lo = mid + 1;
+            else
+                hi = mid;
         }
-        if (br < 0) break;  // every list is exhausted (warp-uniform)
-        if (lane == 0) {
-            const int h = heads[br];
-            const TreeNode n = lists[(int64_t)br * K + h];
-            o.req[n_out] = br;
-            o.depth[n_out] = k1_depth(n.k1);
-            o.path[n_out] = n.path;
-            o.score[n_out] = n.score;
-            o.parent[n_out] = n.parent < 0 ? -1 : map[(int64_t)br * K + n.parent];
-            map[(int64_t)br * K + h] = n_out;
-            heads[br] = h + 1;
-        }
-        __syncwarp();
+        rank += lo;
     }
-    if (lane == 0) *o.count = n_out;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) rank += __shfl_xor_sync(kFull, rank, off);
+    if (lane == 0) {
+        map[x] = rank < budget ? (int32_t)rank : -1;
+        if (pass == 1 && more[r] && k == counts[r] - 1 && rank < budget) *flag = 1;
+        if (rank < budget) {
+            o.req[rank] = r;
+            o.depth[rank] = k1_depth(n.k1);
+            o.path[rank] = n.path;
+            o.score[rank] = n.score;
+        }
+    }
+}
+
+// Parents (by their ranks) and the count, once every rank is known.
+__global__ __launch_bounds__(256) void k_tree_parents(const TreeNode *__restrict__ lists,
+                                                      const int32_t *__restrict__ counts, int32_t *flag, int pass,
+                                                      int R, int K, int budget, const int32_t *__restrict__ map,
+                                                      TreeOut o) {
+    const int f = *(volatile int32_t *)flag;
+    if ((pass == 2) != (f != 0)) return;  // pass 1 stands unless the flag is up; then pass 2 does this
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < (int64_t)R * K;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(x / K), k = (int)(x - (int64_t)r * K);
+        if (k >= counts[r] || map[x] < 0) continue;
+        const int p = lists[x].parent;
+        o.parent[map[x]] = p < 0 ? -1 : map[(int64_t)r * K + p];
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        int64_t total = 0;
+        for (int r = 0; r < R; ++r) total += counts[r];
+        *o.count = (int32_t)(total < budget ? total : budget);
+    }
 }
 
 }  // namespace
 
 size_t tree_workspace_bytes(int64_t R, int64_t budget) {
-    // flag | lists [R][budget] | counts, more, heads [R] | map [R][budget]
+    // flag | lists [R][budget] | counts, more, (spare) [R] | map [R][budget]
     return 256 + (size_t)R * budget * sizeof(TreeNode) + (size_t)R * 4 * 3 + (size_t)R * budget * 4;
 }
 
@@ -332,10 +352,15 @@ cudaError_t launch_tree_select(const float *lp, int R, int D, int C, int budget,
     }
     int k1 = 2 * ((budget + R - 1) / R) + 4;
     if (k1 > budget) k1 = budget;
-    k_tree_topk<<<grid, block, 0, s>>>(lp, R, D, C, k1, budget, 1, lists, counts, more, flag, o);
-    k_tree_merge<<<1, 32, 0, s>>>(lists, counts, more, flag, 1, R, budget, budget, heads, map, o);
-    k_tree_topk<<<grid, block, 0, s>>>(lp, R, D, C, budget, budget, 2, lists, counts, more, flag, o);
-    k_tree_merge<<<1, 32, 0, s>>>(lists, counts, more, flag, 2, R, budget, budget, heads, map, o);
+    const int64_t entries = (int64_t)R * budget;
+    const unsigned rank_blocks = (unsigned)((entries * 32 + 255) / 256);
+    const unsigned fix_blocks = (unsigned)((entries + 255) / 256 < 1024 ? (entries + 255) / 256 : 1024);
+    for (int pass = 1; pass <= 2; ++pass) {
+        k_tree_topk<<<grid, block, 0, s>>>(lp, R, D, C, pass == 1 ? k1 : budget, budget, pass, lists, counts, more,
+                                           flag, o);
+        k_tree_rank<<<rank_blocks, 256, 0, s>>>(lists, counts, more, flag, pass, R, budget, budget, map, o);
+        k_tree_parents<<<fix_blocks, 256, 0, s>>>(lists, counts, flag, pass, R, budget, budget, map, o);
+    }
     return cudaGetLastError();
 }
 
