@@ -699,6 +699,16 @@ def run_case(args):
     import lossless_bit_weight_02_gb300 as w12
     from lossless_bit_weight_02_gb300 import synth
 
+    if args.case == "tree":  # one best-first selection, `iters` times: --tree R D C B shared
+        R, D, C, B, shared = args.tree
+        rng = np.random.default_rng(R * 100 + D)
+        lp = torch.from_numpy(np.log(rng.dirichlet(np.full(C, 0.3), size=(R, D))).astype(np.float32)).cuda()
+        call = w12.TreeCall(lp, B, bool(shared))
+        for _ in range(args.iters):
+            out = call()
+        torch.cuda.synchronize()
+        print(f"case tree R={R} D={D} C={C} B={B} shared={shared}: {int(out['count'].sum())} nodes kept")
+        return
     shapes = {name: (i, N, K) for i, (name, N, K) in enumerate(synth.LAYER_SHAPES)}
     i, N, K = shapes[args.case]
     Wd = synth.dense_weights_device(N, K, seed=1000 + i)
@@ -743,9 +753,11 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack measurement")
-    ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down)")
+    ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down) or the tree selection (tree)")
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--codec", action="store_true", help="with --case: encode, decode and verify the layer")
+    ap.add_argument("--tree", type=int, nargs=5, default=(1, 8, 8, 32, 0), metavar=("R", "D", "C", "B", "SHARED"),
+                    help="with --case tree: requests, positions, candidates, budget, shared (0/1)")
     ap.add_argument("--iters", type=int, default=5)
     args = ap.parse_args()
     if args.case:
