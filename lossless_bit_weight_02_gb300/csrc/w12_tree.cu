@@ -18,7 +18,8 @@
 // such predecessor, which precedes it in the order, so popping the best
 // frontier entry `budget` times yields the request's first nodes in order.
 // The frontier lives in shared memory (at most budget + 1 entries); each
-// step is a lane scan plus a shuffle argmax.
+// step is a lane scan plus a warp argmax (redux on the score, a shuffle
+// tournament only on equal scores).
 // Per-request budget: the search writes the output directly.
 // Shared budget: a first search keeps K1 = min(budget, 2*ceil(budget/R) + 4)
 // nodes per request; every list entry then finds its rank in the total order
@@ -70,8 +71,8 @@ __device__ __forceinline__ bool before_k(uint64_t k1a, uint64_t ka, uint64_t k1b
 }
 
 // The lane holding the warp's first entry in the order, or -1 if no lane
-// has one.  Each lane offers its own best (have, k1, key; `tag` is compared
-// after k1 and before key: the request in the merge, 0 in the search).
+// has one.  Each lane offers its own best (have, k1, key; `tag`, compared
+// after k1 and before key, is 0 within one request).
 // Fast path: one lane holds the largest score (the high word of k1, never
 // 0 for a finite score); otherwise a shuffle tournament on the full keys.
 __device__ __forceinline__ int warp_first(bool have, uint64_t k1, int tag, uint64_t key) {
