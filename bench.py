@@ -132,6 +132,23 @@ def dist_env():
     return ws, rank, local
 
 
+def job_time_ms(local_ms: float, ws_n: int, device) -> float:
+    """The whole job's time for the timed region: the slowest rank's (every
+    rank runs the same units, so the job ends when the last one does)."""
+    if ws_n <= 1:
+        return local_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_step: float, steps: int, ws_n: int, total_ms: float) -> float:
+    """Whole-job throughput in GB/s: every rank streams bytes_per_step per step."""
+    return bytes_per_step * steps * ws_n / (total_ms * 1e-3) / 1e9
+
+
 def algorithmic_bytes(t, M: int) -> int:
     """W12 bytes + activations read + outputs written."""
     return t.nbytes() + 2 * M * t.K + 2 * M * t.N
@@ -218,11 +235,7 @@ def run_gpu(args):
     if ws_n > 1:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms = start.elapsed_time(stop)
-    if ws_n > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = job_time_ms(start.elapsed_time(stop), ws_n, dev)
 
     # per-launch kernel durations -> per (M, layer) and overall
     dur = {}
@@ -494,7 +507,7 @@ def run_gpu(args):
     size_cal["method"] = ("torch dst.copy_(src) of the layer's W12 byte count, read+write bytes / best of 8, "
                           "L2 flushed before each copy")
 
-    value = step_bytes * args.steps * ws_n / (total_ms * 1e-3) / 1e9
+    value = job_value(step_bytes, args.steps, ws_n, total_ms)
     e2e_val = step_bytes * e2e_steps * ws_n / (e2e_ms * 1e-3) / 1e9
     top_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers) / launches_per_step
     traffic = ncu_traffic(top_bytes)
