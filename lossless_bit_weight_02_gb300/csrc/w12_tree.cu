@@ -213,28 +213,23 @@ __global__ __launch_bounds__(32 * kWarpsPerBlock) void k_tree_topk(const float *
                 out[k] = n;
             }
             if (bi != fsize - 1) S.f[bi] = last;
-        } else if (lane == 1 && child) {
-            Frontier c;
-            c.pscore = e.score;
-            c.score = __fadd_rn(e.score, S.cand_lp[t][0]);
-            c.k1 = order_k1(c.score, t + 1);
-            c.parent = (int16_t)k;
-            c.last_rank = 0;
-            const uint32_t ci = S.cand_idx[t][0];
-            c.key = lex_put(e.key, t, ci);
-            c.path = e.path | ((uint64_t)ci << (4 * t));
-            S.f[fsize - 1] = c;
-        } else if (lane == 2 && sib) {
-            Frontier sb;
-            sb.pscore = e.pscore;
-            sb.score = t == 1 ? S.cand_lp[0][nr] : __fadd_rn(e.pscore, S.cand_lp[t - 1][nr]);
-            sb.k1 = order_k1(sb.score, t);
-            sb.parent = e.parent;
-            sb.last_rank = (int16_t)nr;
-            const uint32_t ci = S.cand_idx[t - 1][nr];
-            sb.key = lex_put(e.key, t - 1, ci);
-            sb.path = (e.path & ~(0xFull << (4 * (t - 1)))) | ((uint64_t)ci << (4 * (t - 1)));
-            S.f[fsize - 1 + (child ? 1 : 0)] = sb;
+        } else if ((lane == 1 && child) || (lane == 2 && sib)) {
+            // one code path for both successors: lane 1 the first child
+            // (rank 0 at position t), lane 2 the next sibling (rank nr at t-1)
+            const bool is_child = lane == 1;
+            const int pos = is_child ? t : t - 1;
+            const int rk = is_child ? 0 : nr;
+            const float lpv = S.cand_lp[pos][rk];
+            const uint32_t ci = S.cand_idx[pos][rk];
+            Frontier x;
+            x.pscore = is_child ? e.score : e.pscore;
+            x.score = (!is_child && t == 1) ? lpv : __fadd_rn(x.pscore, lpv);
+            x.k1 = order_k1(x.score, is_child ? t + 1 : t);
+            x.parent = is_child ? (int16_t)k : e.parent;
+            x.last_rank = (int16_t)rk;
+            x.key = lex_put(e.key, pos, ci);
+            x.path = (e.path & ~(0xFull << (4 * pos))) | ((uint64_t)ci << (4 * pos));
+            S.f[fsize - 1 + (is_child ? 0 : (child ? 1 : 0))] = x;
         }
         fsize += (child ? 1 : 0) + (sib ? 1 : 0) - 1;
         __syncwarp();
