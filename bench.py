@@ -213,9 +213,10 @@ def run_gpu(args):
         one_step()
     torch.cuda.synchronize()
 
-    # per-launch events on every 10th timed step only: an event between two
-    # launches keeps the second from overlapping the first
-    ev_steps = list(range(0, args.steps, 10))
+    # per-launch events on every 40th timed step only: an event between two
+    # launches keeps the second from overlapping the first, so an
+    # instrumented step runs its 16 launches without the overlap
+    ev_steps = list(range(0, args.steps, 40))
     n_ev = len(ev_steps)
     evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
             for _ in range(launches_per_step)] for _ in range(n_ev)]
@@ -236,6 +237,33 @@ def run_gpu(args):
         dist.barrier()
     clocks = sampler.stop()
     total_ms = job_time_ms(start.elapsed_time(stop), ws_n, dev)
+
+    # the same step replayed from a CUDA graph (how a serving engine launches a
+    # fixed sequence of GEMMs): 10 steps per graph, on a side stream
+    gstream = torch.cuda.Stream(dev)
+    gcalls = [w12.GemmCall(acts[(M, name)], t, outs[(M, name)], wsp, stream=gstream, opts=overlap)
+              for M in M_VALUES for name, t in layers]
+    with torch.cuda.stream(gstream):
+        for c in gcalls:
+            c()
+    torch.cuda.synchronize()
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph, stream=gstream):
+        for _ in range(10):
+            for c in gcalls:
+                c()
+    g_reps = max(3, args.steps // 10)
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(gstream):
+        step_graph.replay()
+        ga.record(gstream)
+        for _ in range(g_reps):
+            step_graph.replay()
+        gb.record(gstream)
+    torch.cuda.synchronize()
+    graph_ms = job_time_ms(ga.elapsed_time(gb), ws_n, dev)
+    value_graph = job_value(step_bytes, 10 * g_reps, ws_n, graph_ms)
+    del step_graph, gcalls
 
     # per-launch kernel durations -> per (M, layer) and overall
     dur = {}
@@ -527,6 +555,8 @@ def run_gpu(args):
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)"},
+        "value_graph": {"value": round(value_graph, 1), "unit": "GB/s",
+                        "note": "the same 16-launch step replayed from a CUDA graph (10 steps per graph)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
         "tree": tree,
         "size_calibration": size_cal, "nested8": nested,
