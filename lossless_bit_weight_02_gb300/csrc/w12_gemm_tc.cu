@@ -205,6 +205,11 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter) ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     uint32_t r[16];
     asm volatile(
@@ -269,6 +274,15 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
     const int nkb = (int)(4 * (g_end - g_beg));
     const int64_t T = t.Np / 16;
 
+    // the descriptors of the first copies load while the barriers are set up
+    if (nkb > 0 && lane == 0) {
+        if (warp == kWProdWarp) {
+            prefetch_tmap(&hmap);
+            if (!g.nested8) prefetch_tmap(&lmap);
+        } else if (warp == kBProdWarp) {
+            prefetch_tmap(&tmap);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < RW; ++i) {
             mbar_init(&w_full[i], 1);                // the producer's expect_tx
@@ -468,16 +482,31 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
             if (*last_flag) {
                 __threadfence();
                 if (n < t.N) {
+                    auto part = [&](int ss, int c, int j) {
+                        return __ldcg(g.partials + ((int64_t)ss * Mp + 16 * c + j) * t.Np + n);
+                    };
                     for (int c = half; c < chunks; c += kDecWarps / 4) {
-                        // 16 independent loads per chunk s, summed in the order s = 0..S-1
+                        // summed in the order s = 0..S-1; the loads of four
+                        // chunks at a time are in flight together
                         float acc[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[j] = __ldcg(g.partials + (int64_t)(16 * c + j) * t.Np + n);
-                        for (int ss = 1; ss < S; ++ss) {
+                        for (int j = 0; j < 16; ++j) acc[j] = part(0, c, j);
+                        int ss = 1;
+                        for (; ss + 3 < S; ss += 4) {
+                            float v[4][16];
+#pragma unroll
+                            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[b][j] = part(ss + b, c, j);
+#pragma unroll
+                            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) acc[j] += v[b][j];
+                        }
+                        for (; ss < S; ++ss) {
                             float v[16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                v[j] = __ldcg(g.partials + ((int64_t)ss * Mp + 16 * c + j) * t.Np + n);
+                            for (int j = 0; j < 16; ++j) v[j] = part(ss, c, j);
 #pragma unroll
                             for (int j = 0; j < 16; ++j) acc[j] += v[j];
                         }
@@ -633,6 +662,15 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
     };
     const uint32_t acc_cols = tp.tmem_cols / 2;
 
+    // the descriptors of the first copies load while the barriers are set up
+    if (u1 > u0 && lane == 0) {
+        if (warp == kWProdWarp) {
+            prefetch_tmap(&hmap);
+            if (!g.nested8) prefetch_tmap(&lmap);
+        } else if (warp == kBProdWarp) {
+            prefetch_tmap(&tmap);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < RW; ++i) {
             mbar_init(&w_full[i], 1);    // the producer's expect_tx
