@@ -259,6 +259,55 @@ w12_status w12_tree_select(const float *lp, int32_t R, int32_t D, int32_t C, int
                            int32_t *req, int32_t *depth, uint64_t *path, float *score, int32_t *parent,
                            int32_t *count, void *workspace, size_t ws_bytes, w12_stream_t stream);
 
+/* ---- w12_gdn_tree ----  Recurrent (Gated DeltaNet) layer outputs for the
+ * nodes of draft trees, for tree verification on hybrid models (paper: the
+ * news-article page's part "(2)", hybrid models with Gated DeltaNet layers;
+ * the English summary's section 4.2 bullet on hybrid targets: each node's
+ * state is recomputed from the root state along its root path, and a WY
+ * kernel turns the chain of rank-one updates into matrix products on tensor
+ * cores, differing from the path kernel only in rounding).
+ * The recurrence (the published gated delta rule; the pages name the layer
+ * but do not write it out), per head, state S a D x D matrix (row = value
+ * index, column = key index): along a root path, node t applies
+ *     S <- alpha_t S (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ * starting from S0 of the node's request, and the node's output is
+ * o = S q_t after its own update.
+ *   S0: device FP32 [R][H][D][D], the state before the tree, per request.
+ *   q, k, v: device BF16 bits [n][H][D] (keys are normally unit length).
+ *   alpha, beta: device FP32 [n][H] (decay and write strength, usually in
+ *     (0, 1]).
+ *   parent: device int32 [n]: parent[i] in [-1, i) (-1: a child of the root,
+ *     i.e. of the request's last accepted token); a root path has at most
+ *     W12_GDN_MAX_DEPTH nodes.  The tree-selection call's `parent` output has
+ *     this form.
+ *   req: device int32 [n] request of each node, in [0, R); a child is in its
+ *     parent's request.  NULL: every node in request 0.
+ *   o: device FP32 [n][H][D], caller-owned.
+ *   mode: W12_GDN_PATH (one CTA per node and head applies the path's updates
+ *     one by one) or W12_GDN_WY (one product of all keys and queries with S0
+ *     on the tensor cores, then a level-by-level pass over the tree).  The two
+ *     agree up to FP32 rounding; each is deterministic.
+ * workspace: device, w12_gdn_workspace_bytes(n, H, D, mode) bytes, 16-byte
+ * aligned, no initial contents needed.  Alignment: S0, q, k, v, o 16 bytes;
+ * alpha, beta, parent, req 4 bytes (W12_ERR_ALIGN).  Limits: 0 <= n <=
+ * W12_GDN_MAX_NODES, D in {64, 128}, 1 <= H <= 65535 (W12_ERR_INVALID).
+ * A tree that breaks the rules on parent / req / depth is detected on the
+ * device: the nodes concerned get NaN outputs and w12_gdn_status reports
+ * W12_ERR_INVALID for this call.  Asynchronous. */
+#define W12_GDN_PATH 0
+#define W12_GDN_WY 1
+#define W12_GDN_MAX_DEPTH 16
+#define W12_GDN_MAX_NODES 1024
+size_t w12_gdn_workspace_bytes(int64_t n, int64_t H, int64_t D, int32_t mode);
+w12_status w12_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                        const float *beta, const int32_t *parent, const int32_t *req, int64_t n, int64_t H,
+                        int64_t R, int64_t D, float *o, void *workspace, size_t ws_bytes, int32_t mode,
+                        w12_stream_t stream);
+/* The device-side tree check of the last w12_gdn_tree call on this
+ * workspace: W12_OK, or W12_ERR_INVALID if the tree broke a rule.
+ * Synchronous on `stream`. */
+w12_status w12_gdn_status(void *workspace, size_t ws_bytes, w12_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *w12_status_string(w12_status status);
 

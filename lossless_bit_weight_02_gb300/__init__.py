@@ -48,6 +48,7 @@ EXPORTS = (
     "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
     "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_noalloc", "w12_gemm_workspace_status",
     "w12_tree_workspace_bytes", "w12_tree_select",
+    "w12_gdn_workspace_bytes", "w12_gdn_tree", "w12_gdn_status",
     "w12_status_string", "w12_version",
 )
 
@@ -112,6 +113,10 @@ def load(path: str | None = None):
             "w12_tree_workspace_bytes": (sz, [ctypes.c_int32, ctypes.c_int32]),
             "w12_tree_select": (st, [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                      ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "w12_gdn_workspace_bytes": (sz, [i64, i64, i64, ctypes.c_int32]),
+            "w12_gdn_tree": (st, [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, sz,
+                                  ctypes.c_int32, vp]),
+            "w12_gdn_status": (st, [vp, sz, vp]),
             "w12_status_string": (ctypes.c_char_p, [st]),
             "w12_version": (ctypes.c_int32, []),
         }
@@ -359,6 +364,10 @@ def w12_gemm_noalloc(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, opts: GemmO
 W12_TREE_MAX_DEPTH = 16
 W12_TREE_MAX_CANDIDATES = 16
 W12_TREE_MAX_BUDGET = 256
+W12_GDN_PATH = 0
+W12_GDN_WY = 1
+W12_GDN_MAX_DEPTH = 16
+W12_GDN_MAX_NODES = 1024
 
 
 class TreeCall:
@@ -400,6 +409,55 @@ class TreeCall:
 def w12_tree_select(lp: torch.Tensor, budget: int, shared: bool, stream=None) -> dict:
     """Best-first draft-tree node selection (w12_tree_select); see TreeCall."""
     return TreeCall(lp, budget, shared, stream)()
+
+
+class GdnCall:
+    """w12_gdn_tree with its output and workspace allocated and every argument
+    marshalled once: calling the object only invokes the C entry point.
+    S0: CUDA float32 [R, H, D, D]; q, k, v: CUDA bfloat16 [n, H, D]; alpha,
+    beta: CUDA float32 [n, H]; parent: CUDA int32 [n]; req: CUDA int32 [n] or
+    None.  mode: W12_GDN_PATH or W12_GDN_WY.  Output `out`: float32 [n, H, D]."""
+
+    def __init__(self, S0, q, k, v, alpha, beta, parent, req=None, mode=None, stream=None):
+        mode = W12_GDN_WY if mode is None else mode
+        if not (S0.is_cuda and S0.dtype == torch.float32 and S0.dim() == 4 and S0.is_contiguous()):
+            raise ValueError("S0 must be a contiguous CUDA float32 [R, H, D, D] tensor")
+        R, H, D, D2 = S0.shape
+        if D2 != D:
+            raise ValueError("S0 must be square per head")
+        n = q.shape[0]
+        for name, x, shape, dt in (("q", q, (n, H, D), torch.bfloat16), ("k", k, (n, H, D), torch.bfloat16),
+                                   ("v", v, (n, H, D), torch.bfloat16), ("alpha", alpha, (n, H), torch.float32),
+                                   ("beta", beta, (n, H), torch.float32), ("parent", parent, (n,), torch.int32)):
+            if not (x.is_cuda and x.dtype == dt and tuple(x.shape) == shape and x.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {shape}")
+        if req is not None and not (req.is_cuda and req.dtype == torch.int32 and tuple(req.shape) == (n,)
+                                    and req.is_contiguous()):
+            raise ValueError("req must be a contiguous CUDA int32 [n] tensor or None")
+        self.out = torch.empty(n, H, D, dtype=torch.float32, device=q.device)
+        need = int(load().w12_gdn_workspace_bytes(n, H, D, mode))
+        if need == 0:
+            raise W12Error(W12_ERR_INVALID, "w12_gdn_workspace_bytes")
+        self._ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+        self._keep = (S0, q, k, v, alpha, beta, parent, req)
+        self._fn = load().w12_gdn_tree
+        ptr = lambda x: ctypes.c_void_p(x.data_ptr() if x is not None else None)  # noqa: E731
+        self._args = (ptr(S0), ptr(q), ptr(k), ptr(v), ptr(alpha), ptr(beta), ptr(parent), ptr(req),
+                      n, H, R, D, ptr(self.out), ptr(self._ws), self._ws.numel(), mode, _stream(stream))
+        self._stream = stream
+
+    def __call__(self) -> torch.Tensor:
+        _check(self._fn(*self._args), "w12_gdn_tree")
+        return self.out
+
+    def status(self) -> int:
+        """The device-side tree check of the last call (synchronous)."""
+        return load().w12_gdn_status(ctypes.c_void_p(self._ws.data_ptr()), self._ws.numel(), _stream(self._stream))
+
+
+def w12_gdn_tree(S0, q, k, v, alpha, beta, parent, req=None, mode=None, stream=None) -> torch.Tensor:
+    """Gated-delta-rule outputs of draft-tree nodes (w12_gdn_tree); see GdnCall."""
+    return GdnCall(S0, q, k, v, alpha, beta, parent, req, mode, stream)()
 
 
 def w12_gemm_workspace_status(workspace: Workspace, stream=None) -> int:

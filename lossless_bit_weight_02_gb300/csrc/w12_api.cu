@@ -275,6 +275,43 @@ w12_status w12_tree_select(const float *lp, int32_t R, int32_t D, int32_t C, int
                                          workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t w12_gdn_workspace_bytes(int64_t n, int64_t H, int64_t D, int32_t mode) {
+    if (n < 0 || n > W12_GDN_MAX_NODES || H < 1 || H > 65535 || (D != 64 && D != 128) ||
+        (mode != W12_GDN_PATH && mode != W12_GDN_WY))
+        return 0;
+    return gdn_workspace_bytes(n, H, D, mode);
+}
+
+w12_status w12_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                        const float *beta, const int32_t *parent, const int32_t *req, int64_t n, int64_t H,
+                        int64_t R, int64_t D, float *o, void *workspace, size_t ws_bytes, int32_t mode,
+                        w12_stream_t stream) {
+    if (n < 0 || n > W12_GDN_MAX_NODES || H < 1 || H > 65535 || R < 1 || R > (1LL << 30) ||
+        (D != 64 && D != 128) || (mode != W12_GDN_PATH && mode != W12_GDN_WY))
+        return W12_ERR_INVALID;
+    if (!workspace || (n > 0 && (!S0 || !q || !k || !v || !alpha || !beta || !parent || !o)))
+        return W12_ERR_INVALID;
+    if (!aligned16(workspace) || (n > 0 && (!aligned16(S0) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+                                            !aligned16(o) || (reinterpret_cast<uintptr_t>(alpha) & 3) ||
+                                            (reinterpret_cast<uintptr_t>(beta) & 3) ||
+                                            (reinterpret_cast<uintptr_t>(parent) & 3) ||
+                                            (reinterpret_cast<uintptr_t>(req) & 3))))
+        return W12_ERR_ALIGN;
+    if (ws_bytes < gdn_workspace_bytes(n, H, D, mode)) return W12_ERR_CAPACITY;
+    return cuda_status(launch_gdn_tree(S0, q, k, v, alpha, beta, parent, req, (int)n, (int)H, (int)R, (int)D, o,
+                                       workspace, mode, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w12_status w12_gdn_status(void *workspace, size_t ws_bytes, w12_stream_t stream) {
+    if (!workspace || ws_bytes < 256) return W12_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t err = 0;
+    if (cudaMemcpyAsync(&err, workspace, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    return err == 0 ? W12_OK : W12_ERR_INVALID;
+}
+
 w12_status w12_gemm_workspace_status(void *workspace, size_t ws_bytes, w12_stream_t stream) {
     if (!workspace || ws_bytes < 256) return W12_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -79,6 +79,13 @@ cudaError_t launch_gemm_tc(const TensorView &t, const GemmArgs &g, cudaStream_t 
 int64_t gemm_tc_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters_ok, GemmArgs &g);
 int64_t gemm_tc_pad(int64_t M);
 
+// Gated delta rule along draft-tree root paths (w12_gdn.cu); mode 0 = path
+// kernel, 1 = WY.
+size_t gdn_workspace_bytes(int64_t n, int64_t H, int64_t D, int mode);
+cudaError_t launch_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *alpha, const float *beta, const int32_t *parent, const int32_t *req,
+                            int n, int H, int R, int D, float *o, void *workspace, int mode, cudaStream_t s);
+
 // Best-first draft-tree node selection (w12_tree.cu).
 size_t tree_workspace_bytes(int64_t R, int64_t budget);
 cudaError_t launch_tree_select(const float *lp, int R, int D, int C, int budget, bool shared, int32_t *req,

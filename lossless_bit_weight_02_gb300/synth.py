@@ -124,3 +124,49 @@ def all_patterns(rows: int, seed: int) -> np.ndarray:
     assert 65536 % rows == 0
     rng = np.random.default_rng(seed)
     return rng.permutation(65536).astype(np.uint16).reshape(rows, 65536 // rows)
+
+
+# Gated-delta-rule tree inputs (recurrent layers of a hybrid model, tree
+# verification).  A GDN layer of a 27B-class hybrid target: 32 heads of
+# dimension 128 with unit-length queries and keys, decay near 1, write
+# strengths spread over (0, 1), and a root state of a few tenths per entry.
+GDN_HEADS, GDN_DIM = 32, 128
+
+
+def random_tree(n: int, seed: int, max_depth: int = 16, new_root: float = 0.15) -> np.ndarray:
+    """parent[i] in [-1, i): each node hangs off a random earlier node whose
+    depth is below max_depth, or off the root with probability new_root."""
+    rng = np.random.default_rng(seed)
+    parent = np.full(n, -1, np.int32)
+    depth = np.zeros(n, np.int64)
+    for i in range(n):
+        if i > 0 and rng.random() >= new_root:
+            cand = np.flatnonzero(depth[:i] < max_depth)
+            if len(cand):
+                parent[i] = int(rng.choice(cand))
+        depth[i] = 1 if parent[i] < 0 else depth[parent[i]] + 1
+    return parent
+
+
+def gdn_inputs(n: int, H: int, D: int, seed: int, R: int = 1, parent=None, req=None):
+    """Host arrays: S0 float32 [R,H,D,D]; q, k, v BF16 bits [n,H,D] (q and k
+    of unit length before the cast); alpha, beta float32 [n,H]; parent int32
+    [n]; req int32 [n] (a root child draws its request, children inherit)."""
+    rng = np.random.default_rng(seed)
+    S0 = (rng.standard_normal((R, H, D, D)) * 0.3).astype(np.float32)
+    q = rng.standard_normal((n, H, D))
+    k = rng.standard_normal((n, H, D))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((n, H, D))
+    alpha = rng.uniform(0.85, 1.0, size=(n, H)).astype(np.float32)
+    beta = rng.uniform(0.1, 0.9, size=(n, H)).astype(np.float32)
+    if parent is None:
+        parent = random_tree(n, seed + 1)
+    parent = np.asarray(parent, np.int32)
+    if req is None:
+        req = np.zeros(n, np.int32)
+        for i in range(n):
+            req[i] = rng.integers(R) if parent[i] < 0 else req[parent[i]]
+    return (S0, _to_bf16_bits(q), _to_bf16_bits(k), _to_bf16_bits(v), alpha, beta, parent,
+            np.asarray(req, np.int32))

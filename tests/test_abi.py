@@ -187,3 +187,36 @@ def test_tree_select_argument_checks(w12lib):
                                None) == w12lib.W12_ERR_ALIGN
     small = ctypes.c_size_t(lib.w12_tree_workspace_bytes(4, 32) - 1)
     assert lib.w12_tree_select(p, 4, 8, 8, 32, 0, p, p, p, p, p, p, p, small, None) == w12lib.W12_ERR_CAPACITY
+
+
+def test_gdn_argument_checks(w12lib):
+    """Host-side validation of w12_gdn_tree: nothing is launched (no GPU needed)."""
+    lib = w12lib.load()
+    PATH, WY = w12lib.W12_GDN_PATH, w12lib.W12_GDN_WY
+    assert lib.w12_gdn_workspace_bytes(63, 32, 128, PATH) == 256
+    assert lib.w12_gdn_workspace_bytes(63, 32, 128, WY) == 256 + 3 * 63 * 32 * 128 * 4
+    for n, H, D, mode in ((-1, 4, 64, WY), (1025, 4, 64, WY), (8, 0, 64, WY), (8, 4, 96, WY), (8, 4, 64, 2)):
+        assert lib.w12_gdn_workspace_bytes(n, H, D, mode) == 0
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation
+    big = ctypes.c_size_t(1 << 30)
+
+    def call(*ptrs, n=8, H=4, R=1, D=64, ws=big, mode=WY):
+        return lib.w12_gdn_tree(*ptrs[:8], n, H, R, D, ptrs[8], ptrs[9], ws, mode, None)
+
+    ok = [p] * 10
+    for kw in ({"n": -1}, {"n": 1025}, {"H": 0}, {"R": 0}, {"D": 32}, {"D": 100}, {"mode": 3}):
+        assert call(*ok, **kw) == w12lib.W12_ERR_INVALID, kw
+    for i in range(10):
+        if i == 7:  # req may be NULL
+            continue
+        ptrs = list(ok)
+        ptrs[i] = None
+        assert call(*ptrs) == w12lib.W12_ERR_INVALID, i
+    for i, off in ((0, 4), (1, 2), (3, 8), (4, 2), (6, 1), (7, 2), (8, 4), (9, 8)):
+        ptrs = list(ok)
+        ptrs[i] = ctypes.c_void_p((1 << 20) + off)
+        assert call(*ptrs) == w12lib.W12_ERR_ALIGN, i
+    need = lib.w12_gdn_workspace_bytes(8, 4, 64, WY)
+    assert call(*ok, ws=ctypes.c_size_t(need - 1)) == w12lib.W12_ERR_CAPACITY
+    assert lib.w12_gdn_status(None, 256, None) == w12lib.W12_ERR_INVALID
+    assert lib.w12_gdn_status(p, 255, None) == w12lib.W12_ERR_INVALID
