@@ -527,6 +527,7 @@ def run_gpu(args):
 
     # ---- best-first draft-tree node selection (the next row after the GEMM) ----
     tree = tree_bench(dev, cpu=(rank == 0 and not args.no_cpu_baseline))
+    gdn = gdn_bench(dev, cpu=(rank == 0 and not args.no_cpu_baseline), hbm_peak=hbm_peak)
 
     # ---- what a plain device copy reaches at these sizes (context for the roofline) ----
     # MEASURED_PEAKS' HBM figure is a 2 GiB copy; a copy of one layer's W12 bytes
@@ -578,6 +579,7 @@ def run_gpu(args):
                         "note": "the same 16-launch step replayed from a CUDA graph (10 steps per graph)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
         "tree": tree,
+        "gdn": gdn,
         "size_calibration": size_cal, "nested8": nested,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "matches_device_outputs": e2e_match,
                 "method": "per step: one pinned host->device copy of all 16 activations, the 16 w12_gemm calls "
@@ -706,6 +708,105 @@ def tree_bench(dev, cpu: bool):
     return res
 
 
+GDN_CASES = (  # (requests, positions, candidates, node budget shared by the requests)
+    (1, 16, 8, 63),
+    (8, 16, 8, 256),
+)
+
+
+def gdn_trees(dev, R, Dp, C, B):
+    """A best-first tree from w12_tree_select (Dirichlet(0.3) log-probabilities,
+    `B` nodes shared by `R` requests of `Dp` positions): parent and req."""
+    import torch
+    import lossless_bit_weight_02_gb300 as w12
+    rng = np.random.default_rng(700 + R)
+    lp = torch.from_numpy(np.log(rng.dirichlet(np.full(C, 0.3), size=(R, Dp))).astype(np.float32)).to(dev)
+    sel = w12.w12_tree_select(lp, B, True)
+    n = int(sel["count"][0])
+    return sel["parent"][:n].cpu().numpy().astype(np.int32), sel["req"][:n].cpu().numpy().astype(np.int32)
+
+
+def gdn_bench(dev, cpu: bool, hbm_peak: float):
+    """w12_gdn_tree on best-first trees (one GDN layer: 32 heads of 128):
+    device time per call for the path and WY kernels, the HBM floor of the
+    bytes the call must move, and the oracle beside it."""
+    import torch
+    import lossless_bit_weight_02_gb300 as w12
+    from lossless_bit_weight_02_gb300 import synth
+    H, D = synth.GDN_HEADS, synth.GDN_DIM
+    res = {}
+    for R, Dp, C, B in GDN_CASES:
+        parent, req = gdn_trees(dev, R, Dp, C, B)
+        n = len(parent)
+        host = synth.gdn_inputs(n, H, D, seed=800 + R, R=R, parent=parent, req=req)
+        S0, q, k, v, alpha, beta = host[:6]
+        bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa
+        args = (t(S0), bf(q), bf(k), bf(v), t(alpha), t(beta), t(parent), t(req))
+        # bytes a call must move at least: S0, q, k, v, alpha, beta, parent, req in; o out
+        alg = S0.nbytes + q.nbytes + k.nbytes + v.nbytes + alpha.nbytes + beta.nbytes + 8 * n + n * H * D * 4
+        row = {"nodes": n, "requests": R, "heads": H, "dim": D, "depth_max": int(max(
+            len(_gdn_path_len(parent, i)) for i in range(n))), "bytes": alg,
+               "floor_us": round(alg / (hbm_peak * 1e9) * 1e6, 2)}
+        outs = {}
+        for mode, name in ((w12.W12_GDN_PATH, "path"), (w12.W12_GDN_WY, "wy")):
+            gs = torch.cuda.Stream(dev)
+            call = w12.GdnCall(*args, mode=mode, stream=gs)
+            with torch.cuda.stream(gs):
+                for _ in range(5):
+                    call()
+            torch.cuda.synchronize()
+            assert call.status() == w12.W12_OK
+            outs[name] = call.out.clone()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(10):
+                    call()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(gs):
+                graph.replay()
+                torch.cuda.synchronize()
+                a.record(gs)
+                for _ in range(20):
+                    graph.replay()
+                b.record(gs)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / 200
+            row[name] = {"us_graph": round(us, 2), "nodes_per_s": round(n / (us * 1e-6), 1),
+                         "roofline_frac": round(row["floor_us"] / us, 4)}
+        d = (outs["wy"] - outs["path"]).abs()
+        row["wy_vs_path_max_rel"] = float((d / outs["path"].abs().clamp_min(1e-3)).max())
+        if cpu:
+            from oracle import gdn as gdn_oracle
+            f32 = lambda b: (np.asarray(b).astype(np.uint32) << 16).view(np.float32)  # noqa
+            hs = 2  # a sample of heads; the oracle's time scales with the head count
+            t0 = time.perf_counter()
+            for r in range(R):
+                idx = np.flatnonzero(req == r)
+                remap = {int(j): x for x, j in enumerate(idx)}
+                par = np.array([remap[int(parent[j])] if parent[j] >= 0 else -1 for j in idx], np.int64)
+                gdn_oracle.path_outputs(S0[r, :hs], f32(q[idx, :hs]), f32(k[idx, :hs]), f32(v[idx, :hs]),
+                                        alpha[idx, :hs], beta[idx, :hs], par)
+            row["oracle_us"] = round((time.perf_counter() - t0) * 1e6 * H / hs, 1)
+            row["oracle_sample"] = f"{hs} of {H} heads, scaled by {H // hs}"
+        res[f"R{R}_B{B}"] = row
+    res["note"] = ("Gated delta rule along every node's root path (hybrid-model tree verification), trees from "
+                   "w12_tree_select; path: one CTA per (node, head), sequential rank-one updates; wy: keys and "
+                   "queries times the root state on the tensor cores, then a warp per (node, head) solves its own "
+                   "path's coefficients. "
+                   "us_graph: CUDA-graph replay, device time per call. floor_us: the call's minimum bytes at "
+                   "the measured HBM peak. oracle_us: the FP64 Python oracle (path definition), one host thread")
+    return res
+
+
+def _gdn_path_len(parent, i):
+    path = []
+    while i >= 0:
+        path.append(i)
+        i = int(parent[i])
+    return path
+
+
 def cpu_baseline(layers=None, budget_s=10.0):
     smp = OracleSample()
     rows = smp.rows_for(budget_s / 4)
@@ -771,6 +872,22 @@ def run_case(args):
         torch.cuda.synchronize()
         print(f"case tree R={R} D={D} C={C} B={B} shared={shared}: {int(out['count'].sum())} nodes kept")
         return
+    if args.case == "gdn":  # the 256-node, 8-request GDN tree, both kernels, `iters` times each
+        R, Dp, C, B = GDN_CASES[-1]
+        parent, req = gdn_trees(torch.device("cuda"), R, Dp, C, B)
+        n, H, D = len(parent), synth.GDN_HEADS, synth.GDN_DIM
+        host = synth.gdn_inputs(n, H, D, seed=800 + R, R=R, parent=parent, req=req)
+        bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()  # noqa
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa
+        dargs = (t(host[0]), bf(host[1]), bf(host[2]), bf(host[3]), t(host[4]), t(host[5]), t(parent), t(req))
+        for mode in (w12.W12_GDN_PATH, w12.W12_GDN_WY):
+            call = w12.GdnCall(*dargs, mode=mode)
+            for _ in range(args.iters):
+                call()
+            torch.cuda.synchronize()
+            assert call.status() == w12.W12_OK
+        print(f"case gdn: {n} nodes, {R} requests, {H} heads of {D}: path and WY, {args.iters} calls each")
+        return
     shapes = {name: (i, N, K) for i, (name, N, K) in enumerate(synth.LAYER_SHAPES)}
     i, N, K = shapes[args.case]
     Wd = synth.dense_weights_device(N, K, seed=1000 + i)
@@ -815,7 +932,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack measurement")
-    ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down) or the tree selection (tree)")
+    ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down), the tree selection (tree) or the "
+                    "GDN tree kernels (gdn)")
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--codec", action="store_true", help="with --case: encode, decode and verify the layer")
     ap.add_argument("--tree", type=int, nargs=5, default=(1, 8, 8, 32, 0), metavar=("R", "D", "C", "B", "SHARED"),

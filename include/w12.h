@@ -285,8 +285,9 @@ w12_status w12_tree_select(const float *lp, int32_t R, int32_t D, int32_t C, int
  *   o: device FP32 [n][H][D], caller-owned.
  *   mode: W12_GDN_PATH (one CTA per node and head applies the path's updates
  *     one by one) or W12_GDN_WY (one product of all keys and queries with S0
- *     on the tensor cores, then a level-by-level pass over the tree).  The two
- *     agree up to FP32 rounding; each is deterministic.
+ *     on the tensor cores, then one warp per node and head solves its own
+ *     root path's rank-one coefficients).  The two agree up to FP32 rounding;
+ *     each is deterministic.
  * workspace: device, w12_gdn_workspace_bytes(n, H, D, mode) bytes, 16-byte
  * aligned, no initial contents needed.  Alignment: S0, q, k, v, o 16 bytes;
  * alpha, beta, parent, req 4 bytes (W12_ERR_ALIGN).  Limits: 0 <= n <=

@@ -24,9 +24,10 @@
 //     j down to t).  S_0 enters only through K S_0^T and Q S_0^T for every
 //     node at once: k_gdn_proj computes them with mma.sync (BF16 operands,
 //     S_0 split into a BF16 high and low part so that the product keeps
-//     FP32-level accuracy).  k_gdn_wy_tree then walks the tree level by level
-//     (one CTA per head, one warp per node), each node a few dot products and
-//     vector sums of length D.
+//     FP32-level accuracy).  k_gdn_wy_paths then gives every (node, head) a
+//     warp that recomputes the f of its own root path (no stored state, no
+//     exchange between warps): the path keys' Gram matrix from mma.sync, a
+//     forward substitution of at most 16 steps, and the output sum.
 // Every sum runs in a fixed order, so both kernels are deterministic.
 // Invalid trees (a parent outside [-1, i), a parent in another request, a
 // request id outside [0, R), a path longer than 16) give NaN outputs for the
@@ -41,8 +42,6 @@ namespace w12 {
 namespace {
 
 constexpr int kGdnMaxDepth = 16;
-constexpr int kGdnMaxNodes = 1024;
-constexpr int kTreeThreads = 512;
 
 struct GdnArgs {
     const float *S0;                 // [R][H][D][D]
@@ -54,7 +53,6 @@ struct GdnArgs {
     float *o;                        // [n][H][D]
     int32_t *err;                    // workspace error word
     float *G;                        // [2][n][H][D]: K S_0^T, Q S_0^T (WY only)
-    float *f;                        // [n][H][D] (WY only)
 };
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -149,10 +147,10 @@ __global__ __launch_bounds__(2 * D, 2) void k_gdn_path(GdnArgs a) {
 
 // ---------------------------------------------------------------------------
 // WY, step 1: G[0] = K S_0^T and G[1] = Q S_0^T for every node and head.
-// A CTA takes 16 nodes of one head and one of K / Q; warp w the output
-// columns 32w .. 32w+31 (four m16n8 tiles).  S_0 = hi + lo, both BF16:
-// acc += X hi^T, then acc += X lo^T, per 16-wide k step.  Rows of the tile
-// that belong to different requests are done one request after another.
+// One CTA per (request, head) loads S_0 once, split into BF16 hi + lo parts
+// in shared memory (row pitch D + 8: conflict-free fragment reads), lists
+// the request's nodes, and its warps take 16-node tiles of K or Q:
+// acc += X hi^T, then acc += X lo^T, per 16-wide k step, for all D columns.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -172,137 +170,250 @@ __device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo) {
     lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
 }
 
+constexpr int kProjWarps = 8;
+
 template <int D>
-__global__ __launch_bounds__(D) void k_gdn_proj(GdnArgs a) {
-    const int tile = blockIdx.x >> 1, which = blockIdx.x & 1, h = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
-    const uint16_t *X = which ? a.q : a.k;
-    const int rA = tile * 16 + g, rB = rA + 8;
-    const bool okA = rA < a.n, okB = rB < a.n;
-    const int reqA = okA ? req_of(a, rA) : -1, reqB = okB ? req_of(a, rB) : -1;
-    // requests still to do for this lane's two rows (an invalid id is never done)
-    bool todoA = okA && reqA >= 0 && reqA < a.R, todoB = okB && reqB >= 0 && reqB < a.R;
-    const uint32_t *xa = reinterpret_cast<const uint32_t *>(X + ((int64_t)(okA ? rA : 0) * a.H + h) * D);
-    const uint32_t *xb = reinterpret_cast<const uint32_t *>(X + ((int64_t)(okB ? rB : 0) * a.H + h) * D);
-    float *G = a.G + (int64_t)which * a.n * a.H * D;
-    while (__any_sync(kFull, todoA || todoB)) {
-        // the smallest request id still to do in the tile
-        const unsigned mine = todoA ? (unsigned)reqA : (todoB ? (unsigned)reqB : 0xFFFFFFFFu);
-        const unsigned mineB = todoB ? (unsigned)reqB : 0xFFFFFFFFu;
-        const int rq = (int)__reduce_min_sync(kFull, mine < mineB ? mine : mineB);
-        const float *S0 = a.S0 + ((int64_t)rq * a.H + h) * D * D;
-        float acc[4][4];
+__host__ __device__ constexpr int proj_smem_bytes() {
+    return 2 * D * (D + 8) * 2 + 4 * 1024 + 16;
+}
+
+template <int D>
+__global__ __launch_bounds__(32 * kProjWarps) void k_gdn_proj(GdnArgs a) {
+    constexpr int KP = D + 8, RW = KP / 2;  // BF16 row pitch, in u32
+    extern __shared__ __align__(16) uint8_t smem_proj[];
+    uint16_t *hi = reinterpret_cast<uint16_t *>(smem_proj);  // [D][KP]: row c = S_0 row c (value index)
+    uint16_t *lo = hi + D * KP;
+    int *list = reinterpret_cast<int *>(lo + D * KP);         // nodes of this request
+    int *cnt = list + 1024;
+    const int r = blockIdx.x, h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q4 = lane & 3;
+    if (tid == 0) *cnt = 0;
+    __syncthreads();
+    // the nodes of request r (their order does not matter: MMA rows are independent)
+    for (int i = tid; i < a.n; i += 32 * kProjWarps)
+        if (req_of(a, i) == r) list[atomicAdd(cnt, 1)] = i;
+    __syncthreads();
+    const int nr = *cnt, tiles = (nr + 15) / 16;
+    if (nr == 0) return;  // CTA-uniform
+    // S_0[r][h] into the two BF16 parts (coalesced 16-byte loads, all in flight)
+    const float4 *S0 = reinterpret_cast<const float4 *>(a.S0 + ((int64_t)r * a.H + h) * D * D);
+#pragma unroll 4
+    for (int x = tid; x < D * D / 4; x += 32 * kProjWarps) {
+        const float4 v4 = S0[x];
+        const int c = (4 * x) / D, kk = (4 * x) % D;
+        uint32_t h0, l0, h1, l1;
+        split2(make_float2(v4.x, v4.y), h0, l0);
+        split2(make_float2(v4.z, v4.w), h1, l1);
+        *reinterpret_cast<uint2 *>(hi + c * KP + kk) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2 *>(lo + c * KP + kk) = make_uint2(l0, l1);
+    }
+    __syncthreads();
+    const uint32_t *H32 = reinterpret_cast<const uint32_t *>(hi), *L32 = reinterpret_cast<const uint32_t *>(lo);
+    for (int item = warp; item < 2 * tiles; item += kProjWarps) {
+        const int tile = item >> 1, which = item & 1;
+        const uint16_t *X = which ? a.q : a.k;
+        const int iA = 16 * tile + g, iB = iA + 8;
+        const bool okA = iA < nr, okB = iB < nr;
+        const int rA = okA ? list[iA] : 0, rB = okB ? list[iB] : 0;
+        const uint32_t *xa = reinterpret_cast<const uint32_t *>(X + ((int64_t)rA * a.H + h) * D);
+        const uint32_t *xb = reinterpret_cast<const uint32_t *>(X + ((int64_t)rB * a.H + h) * D);
+        uint32_t af[D / 16][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int s = 0; s < D / 16; ++s) {
+            const int w0 = 8 * s + q4;
+            af[s][0] = okA ? xa[w0] : 0u;
+            af[s][1] = okB ? xb[w0] : 0u;
+            af[s][2] = okA ? xa[w0 + 4] : 0u;
+            af[s][3] = okB ? xb[w0 + 4] : 0u;
+        }
+        float *G = a.G + (int64_t)which * a.n * a.H * D;
+#pragma unroll 1
+        for (int nt0 = 0; nt0 < D / 8; nt0 += 4) {  // four 8-column tiles at a time
+            float acc[4][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-        for (int kk = 0; kk < D; kk += 16) {
-            const int w0 = (kk >> 1) + q4;  // u32 index of columns kk + 2q4, +1
-            const uint32_t a0 = okA ? xa[w0] : 0u, a1 = okB ? xb[w0] : 0u;
-            const uint32_t a2 = okA ? xa[w0 + 4] : 0u, a3 = okB ? xb[w0 + 4] : 0u;
+            for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int c = warp * 32 + nt * 8 + g;  // output column = row c of S_0
-                const float *srow = S0 + (int64_t)c * D + kk + 2 * q4;
-                uint32_t h0, l0, h1, l1;
-                split2(*reinterpret_cast<const float2 *>(srow), h0, l0);
-                split2(*reinterpret_cast<const float2 *>(srow + 8), h1, l1);
-                mma_bf16(acc[nt], a0, a1, a2, a3, h0, h1);
-                mma_bf16(acc[nt], a0, a1, a2, a3, l0, l1);
+                for (int e = 0; e < 4; ++e) acc[u][e] = 0.f;
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s) {
+                const int w0 = 8 * s + q4;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = (nt0 + u) * 8 + g;
+                    mma_bf16(acc[u], af[s][0], af[s][1], af[s][2], af[s][3], H32[c * RW + w0], H32[c * RW + w0 + 4]);
+                    mma_bf16(acc[u], af[s][0], af[s][1], af[s][2], af[s][3], L32[c * RW + w0], L32[c * RW + w0 + 4]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = (nt0 + u) * 8 + 2 * q4;
+                if (okA) *reinterpret_cast<float2 *>(G + ((int64_t)rA * a.H + h) * D + c) = make_float2(acc[u][0], acc[u][1]);
+                if (okB) *reinterpret_cast<float2 *>(G + ((int64_t)rB * a.H + h) * D + c) = make_float2(acc[u][2], acc[u][3]);
             }
         }
-        const bool wA = todoA && reqA == rq, wB = todoB && reqB == rq;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int c = warp * 32 + nt * 8 + 2 * q4;
-            if (wA) *reinterpret_cast<float2 *>(G + ((int64_t)rA * a.H + h) * D + c) = make_float2(acc[nt][0], acc[nt][1]);
-            if (wB) *reinterpret_cast<float2 *>(G + ((int64_t)rB * a.H + h) * D + c) = make_float2(acc[nt][2], acc[nt][3]);
-        }
-        if (wA) todoA = false;
-        if (wB) todoB = false;
     }
 }
 
 // ---------------------------------------------------------------------------
-// WY, step 2: one CTA per head walks the tree level by level; warp per node,
-// lane l holds columns l, l + 32, ...  Per node, the path's nodes j are
-// visited node side first: running decay ratio G_ij, the dot products
-// k_i.k_j and q_i.k_j (fixed butterfly), and the sums of f_j.
+// WY, step 2: one warp per (node, head) recomputes the coefficient vectors f
+// of its own root path (up to 16) from the step-1 products, with no state
+// and no exchange between warps:
+//   * the path's keys go to shared memory as a 16 x D BF16 matrix Kp (rows
+//     past the path are zero); their Gram matrix Kp Kp^T comes from
+//     mma.sync (2 n-tiles x D/16 k-steps) and q_i . k_j from warp sums, and
+//     then the f vectors take the keys' place in shared memory;
+//   * w_t = v_t - gamma_t (K S_0^T)_t for every path node, then, root side
+//     first, f_t = beta_t (w_t - sum_{j<t} G_tj Gram_tj f_j), j descending
+//     (G_tj = alpha_{j+1} ... alpha_t, a running product);
+//   * o = gamma (Q S_0^T)_i + sum_j G_ij (q_i.k_j) f_j, j descending.
+// Lane l holds columns l, l + 32, ... of every vector.
 // ---------------------------------------------------------------------------
+constexpr int kPathWarps = 4;  // warps (nodes) per CTA
+
 template <int D>
-__global__ __launch_bounds__(kTreeThreads) void k_gdn_wy_tree(GdnArgs a) {
-    constexpr int P = D / 32;
-    __shared__ uint16_t up_s[kGdnMaxNodes][kGdnMaxDepth];
-    __shared__ uint8_t dep[kGdnMaxNodes];
-    __shared__ int maxdep;
-    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr int nw = kTreeThreads / 32;
-    if (tid == 0) maxdep = 0;
-    __syncthreads();
-    for (int i = tid; i < a.n; i += kTreeThreads) {
-        const int L = walk_up(a, i, up_s[i]);
-        dep[i] = (uint8_t)L;
-        if (L > 0) {
-            atomicMax(&maxdep, L);
-        } else {
-            atomicExch(a.err, 1);
-            float *out = a.o + ((int64_t)i * a.H + h) * D;
-            for (int c = 0; c < D; ++c) out[c] = __int_as_float(0x7FC00000);
+__host__ __device__ constexpr int path_warp_bytes() {
+    // the path keys (BF16, until their products are formed) and then the f
+    // vectors (FP32) share the first region
+    return (16 * (D + 8) * 2 > 16 * D * 4 ? 16 * (D + 8) * 2 : 16 * D * 4) + 16 * 17 * 4 + 5 * 16 * 4;
+}
+
+template <int D>
+__global__ __launch_bounds__(32 * kPathWarps) void k_gdn_wy_paths(GdnArgs a) {
+    constexpr int P = D / 32, KP = D + 8;
+    extern __shared__ __align__(16) uint8_t smem_gdn[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
+    const int i = blockIdx.x * kPathWarps + warp, h = blockIdx.y;
+    if (i >= a.n) return;  // warp-uniform; the kernel has no block barrier
+    uint8_t *base = smem_gdn + warp * path_warp_bytes<D>();
+    constexpr int kRegion = 16 * (D + 8) * 2 > 16 * D * 4 ? 16 * (D + 8) * 2 : 16 * D * 4;
+    uint16_t *Kp = reinterpret_cast<uint16_t *>(base);  // [16][KP], then
+    float *fs = reinterpret_cast<float *>(base);        // [16][D] over it
+    float *gram = reinterpret_cast<float *>(base + kRegion);  // [16][17]
+    float *al = gram + 16 * 17, *be = al + 16, *gm = be + 16, *qk = gm + 16;  // [16] each
+    int *up = reinterpret_cast<int *>(qk + 16);                                 // [16]
+    int L = 0;
+    if (lane == 0) L = walk_up(a, i, up);
+    L = __shfl_sync(kFull, L, 0);
+    __syncwarp();
+    const int64_t ih = ((int64_t)i * a.H + h) * D;
+    float *out = a.o + ih;
+    if (L == 0) {
+#pragma unroll
+        for (int m = 0; m < P; ++m) out[lane + 32 * m] = __int_as_float(0x7FC00000);
+        if (lane == 0) atomicExch(a.err, 1);
+        return;
+    }
+    // path node t (root side first) is up[L - 1 - t].  The path's alpha and
+    // beta, q_i, (Q S_0^T)_i and the key rows are all requested here.
+    if (lane < 16) {
+        const int node = lane < L ? up[L - 1 - lane] : 0;
+        al[lane] = lane < L ? a.alpha[(int64_t)node * a.H + h] : 0.f;
+        be[lane] = lane < L ? a.beta[(int64_t)node * a.H + h] : 0.f;
+    }
+    const float *G2 = a.G + (int64_t)a.n * a.H * D;
+    float qi[P], g2[P];
+#pragma unroll
+    for (int m = 0; m < P; ++m) {
+        qi[m] = bf2f(a.q[ih + lane + 32 * m]);
+        g2[m] = G2[ih + lane + 32 * m];
+    }
+    constexpr int CH = D / 8;  // 16-byte chunks per key row
+    for (int c = lane; c < 16 * CH; c += 32) {
+        const int t = c / CH, ch = c - t * CH;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (t < L) x = *reinterpret_cast<const uint4 *>(a.k + ((int64_t)up[L - 1 - t] * a.H + h) * D + 8 * ch);
+        *reinterpret_cast<uint4 *>(Kp + t * KP + 8 * ch) = x;
+    }
+    __syncwarp();
+    if (lane < 16) {  // gamma_t = alpha_0 ... alpha_t
+        float gam = 1.f;
+        for (int t = 0; t <= lane; ++t) gam *= al[t];
+        gm[lane] = gam;
+    }
+    __syncwarp();
+    // Gram = Kp Kp^T
+    {
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        const uint32_t *K32 = reinterpret_cast<const uint32_t *>(Kp);
+        constexpr int RW = KP / 2;  // u32 per row
+#pragma unroll
+        for (int kk = 0; kk < D; kk += 16) {
+            const int w0 = (kk >> 1) + q4;
+            const uint32_t a0 = K32[g * RW + w0], a1 = K32[(g + 8) * RW + w0];
+            const uint32_t a2 = K32[g * RW + w0 + 4], a3 = K32[(g + 8) * RW + w0 + 4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int rn = nt * 8 + g;
+                mma_bf16(acc[nt], a0, a1, a2, a3, K32[rn * RW + w0], K32[rn * RW + w0 + 4]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            gram[g * 17 + nt * 8 + 2 * q4] = acc[nt][0];
+            gram[g * 17 + nt * 8 + 2 * q4 + 1] = acc[nt][1];
+            gram[(g + 8) * 17 + nt * 8 + 2 * q4] = acc[nt][2];
+            gram[(g + 8) * 17 + nt * 8 + 2 * q4 + 1] = acc[nt][3];
         }
     }
-    __syncthreads();
-    const int md = maxdep;
-    const float *G1 = a.G, *G2 = a.G + (int64_t)a.n * a.H * D;
-    for (int lev = 1; lev <= md; ++lev) {
-        for (int i = warp; i < a.n; i += nw) {
-            if (dep[i] != lev) continue;
-            const int64_t ih = ((int64_t)i * a.H + h) * D;
-            float ki[P], qi[P], facc[P], oacc[P];
+    // q_i . k_j for the path's keys
+    for (int j = 0; j < L; ++j) {
+        float pq = 0.f;
 #pragma unroll
-            for (int m = 0; m < P; ++m) {
-                ki[m] = bf2f(a.k[ih + lane + 32 * m]);
-                qi[m] = bf2f(a.q[ih + lane + 32 * m]);
-                facc[m] = 0.f;
-                oacc[m] = 0.f;
-            }
-            // the ancestors j = up[1..lev-1]; ratio = product of alpha over up[0..s-1]
-            float ratio = a.alpha[(int64_t)i * a.H + h];
-            for (int s = 1; s < lev; ++s) {
-                const int j = up_s[i][s];
-                const int64_t jh = ((int64_t)j * a.H + h) * D;
-                float pk = 0.f, pq = 0.f, kj[P];
-#pragma unroll
-                for (int m = 0; m < P; ++m) {
-                    kj[m] = bf2f(a.k[jh + lane + 32 * m]);
-                    pk = fmaf(ki[m], kj[m], pk);
-                    pq = fmaf(qi[m], kj[m], pq);
-                }
-                const float ck = ratio * warp_sum(pk), cq = ratio * warp_sum(pq);
-#pragma unroll
-                for (int m = 0; m < P; ++m) {
-                    const float fj = a.f[jh + lane + 32 * m];
-                    facc[m] = fmaf(ck, fj, facc[m]);
-                    oacc[m] = fmaf(cq, fj, oacc[m]);
-                }
-                ratio *= a.alpha[(int64_t)j * a.H + h];
-            }
-            const float gamma = ratio;  // alpha over the whole path
-            const float be = a.beta[(int64_t)i * a.H + h];
-            float pself = 0.f;
-#pragma unroll
-            for (int m = 0; m < P; ++m) pself = fmaf(qi[m], ki[m], pself);
-            const float cself = warp_sum(pself);
-            float *out = a.o + ih;
-#pragma unroll
-            for (int m = 0; m < P; ++m) {
-                const int c = lane + 32 * m;
-                const float fi = be * (bf2f(a.v[ih + c]) - fmaf(gamma, G1[ih + c], facc[m]));
-                a.f[ih + c] = fi;
-                out[c] = fmaf(gamma, G2[ih + c], fmaf(cself, fi, oacc[m]));
-            }
-        }
-        __syncthreads();  // this level's f is read by the next
+        for (int m = 0; m < P; ++m) pq = fmaf(qi[m], bf2f(Kp[j * KP + lane + 32 * m]), pq);
+        pq = warp_sum(pq);
+        if (lane == 0) qk[j] = pq;
     }
+    __syncwarp();  // the keys are no longer read: fs takes their place
+    // w_t = v_t - gamma_t (K S_0^T)_t into fs, four columns per chunk
+#pragma unroll 8
+    for (int x = lane; x < 16 * (D / 4); x += 32) {
+        const int t = x / (D / 4), c = 4 * (x % (D / 4));
+        if (t < L) {
+            const int64_t th = ((int64_t)up[L - 1 - t] * a.H + h) * D + c;
+            const float4 g1 = *reinterpret_cast<const float4 *>(a.G + th);
+            const uint2 vv = *reinterpret_cast<const uint2 *>(a.v + th);
+            const float gam = gm[t];
+            *reinterpret_cast<float4 *>(fs + t * D + c) =
+                make_float4(__uint_as_float(vv.x << 16) - gam * g1.x, __uint_as_float(vv.x & 0xFFFF0000u) - gam * g1.y,
+                            __uint_as_float(vv.y << 16) - gam * g1.z, __uint_as_float(vv.y & 0xFFFF0000u) - gam * g1.w);
+        }
+    }
+    __syncwarp();
+    // f_t, root side first
+    for (int t = 0; t < L; ++t) {
+        float s[P];
+#pragma unroll
+        for (int m = 0; m < P; ++m) s[m] = 0.f;
+        float r = 1.f;
+        for (int j = t - 1; j >= 0; --j) {
+            r *= al[j + 1];
+            const float cf = r * gram[t * 17 + j];
+#pragma unroll
+            for (int m = 0; m < P; ++m) s[m] = fmaf(cf, fs[j * D + lane + 32 * m], s[m]);
+        }
+        const float bt = be[t];
+#pragma unroll
+        for (int m = 0; m < P; ++m) fs[t * D + lane + 32 * m] = bt * (fs[t * D + lane + 32 * m] - s[m]);
+        __syncwarp();
+    }
+    // output of node i (path node L - 1)
+    float o[P];
+    const float gam = gm[L - 1];
+#pragma unroll
+    for (int m = 0; m < P; ++m) o[m] = 0.f;
+    float r = 1.f;
+    for (int j = L - 1; j >= 0; --j) {
+        if (j < L - 1) r *= al[j + 1];
+        const float cf = r * qk[j];
+#pragma unroll
+        for (int m = 0; m < P; ++m) o[m] = fmaf(cf, fs[j * D + lane + 32 * m], o[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < P; ++m) out[lane + 32 * m] = fmaf(gam, g2[m], o[m]);
 }
 
 template <int D>
@@ -311,10 +422,23 @@ cudaError_t launch_gdn_d(const GdnArgs &a, int mode, cudaStream_t s) {
         k_gdn_path<D><<<dim3((unsigned)a.n, (unsigned)a.H), 2 * D, 0, s>>>(a);
         return cudaGetLastError();
     }
-    k_gdn_proj<D><<<dim3((unsigned)(2 * ((a.n + 15) / 16)), (unsigned)a.H), D, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    constexpr int smem = kPathWarps * path_warp_bytes<D>(), psmem = proj_smem_bytes<D>();
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    k_gdn_wy_tree<D><<<(unsigned)a.H, kTreeThreads, 0, s>>>(a);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(k_gdn_wy_paths<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_gdn_proj<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    k_gdn_proj<D><<<dim3((unsigned)a.R, (unsigned)a.H), 32 * kProjWarps, psmem, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_gdn_wy_paths<D><<<dim3((unsigned)((a.n + kPathWarps - 1) / kPathWarps), (unsigned)a.H), 32 * kPathWarps,
+                         smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -322,7 +446,7 @@ cudaError_t launch_gdn_d(const GdnArgs &a, int mode, cudaStream_t s) {
 
 size_t gdn_workspace_bytes(int64_t n, int64_t H, int64_t D, int mode) {
     if (mode == 0) return 256;
-    return 256 + (size_t)3 * (size_t)n * (size_t)H * (size_t)D * 4;
+    return 256 + (size_t)2 * (size_t)n * (size_t)H * (size_t)D * 4;
 }
 
 cudaError_t launch_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -345,7 +469,6 @@ cudaError_t launch_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *
     a.o = o;
     a.err = static_cast<int32_t *>(workspace);
     a.G = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + 256);
-    a.f = a.G + (int64_t)2 * n * H * D;
     if (D == 64) return launch_gdn_d<64>(a, mode, s);
     if (D == 128) return launch_gdn_d<128>(a, mode, s);
     return cudaErrorInvalidValue;
