@@ -53,6 +53,7 @@ struct GdnArgs {
     float *o;                        // [n][H][D]
     int32_t *err;                    // workspace error word
     float *G;                        // [2][n][H][D]: K S_0^T, Q S_0^T (WY only)
+    int32_t *paths;                  // [n][17]: path length (0 = invalid), then the path, node side first (WY only)
 };
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -147,9 +148,10 @@ __global__ __launch_bounds__(2 * D, 2) void k_gdn_path(GdnArgs a) {
 
 // ---------------------------------------------------------------------------
 // WY, step 1: G[0] = K S_0^T and G[1] = Q S_0^T for every node and head.
-// One CTA per (request, head) loads S_0 once, split into BF16 hi + lo parts
-// in shared memory (row pitch D + 8: conflict-free fragment reads), lists
-// the request's nodes, and its warps take 16-node tiles of K or Q:
+// One CTA per (request, head) lists the request's nodes (the head-0 CTA also
+// walks and checks their root paths for step 2), loads S_0 once, split into
+// BF16 hi + lo parts in shared memory (row pitch D + 8: conflict-free
+// fragment reads), and its warps take 16-node tiles of K or Q:
 // acc += X hi^T, then acc += X lo^T, per 16-wide k step, for all D columns.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -195,6 +197,13 @@ __global__ __launch_bounds__(32 * kProjWarps) void k_gdn_proj(GdnArgs a) {
     __syncthreads();
     const int nr = *cnt, tiles = (nr + 15) / 16;
     if (nr == 0) return;  // CTA-uniform
+    if (h == 0) {  // every node's root path, once per request, for the per-path kernel
+        for (int x = tid; x < nr; x += 32 * kProjWarps) {
+            const int i = list[x];
+            int32_t *pw = a.paths + (int64_t)i * 17;
+            pw[0] = walk_up(a, i, pw + 1);
+        }
+    }
     // S_0[r][h] into the two BF16 parts (coalesced 16-byte loads, all in flight)
     const float4 *S0 = reinterpret_cast<const float4 *>(a.S0 + ((int64_t)r * a.H + h) * D * D);
 #pragma unroll 4
@@ -256,8 +265,8 @@ __global__ __launch_bounds__(32 * kProjWarps) void k_gdn_proj(GdnArgs a) {
 
 // ---------------------------------------------------------------------------
 // WY, step 2: one warp per (node, head) recomputes the coefficient vectors f
-// of its own root path (up to 16) from the step-1 products, with no state
-// and no exchange between warps:
+// of its own root path (up to 16; walked and checked by step 1) from the
+// step-1 products, with no state and no exchange between warps:
 //   * the path's keys go to shared memory as a 16 x D BF16 matrix Kp (rows
 //     past the path are zero); their Gram matrix Kp Kp^T comes from
 //     mma.sync (2 n-tiles x D/16 k-steps) and q_i . k_j from warp sums, and
@@ -291,11 +300,24 @@ __global__ __launch_bounds__(32 * kPathWarps) void k_gdn_wy_paths(GdnArgs a) {
     float *gram = reinterpret_cast<float *>(base + kRegion);  // [16][17]
     float *al = gram + 16 * 17, *be = al + 16, *gm = be + 16, *qk = gm + 16;  // [16] each
     int *up = reinterpret_cast<int *>(qk + 16);                                 // [16]
-    int L = 0;
-    if (lane == 0) L = walk_up(a, i, up);
-    L = __shfl_sync(kFull, L, 0);
-    __syncwarp();
     const int64_t ih = ((int64_t)i * a.H + h) * D;
+    const float *G2 = a.G + (int64_t)a.n * a.H * D;
+    float qi[P], g2[P];
+#pragma unroll
+    for (int m = 0; m < P; ++m) {
+        qi[m] = bf2f(a.q[ih + lane + 32 * m]);
+        g2[m] = G2[ih + lane + 32 * m];
+    }
+    // the root path, walked and checked once per request by the projection
+    // kernel (a node with a bad request id is in no request's list)
+    const int rq = req_of(a, i);
+    int L = 0;
+    if (rq >= 0 && rq < a.R) {
+        const int32_t *pw = a.paths + (int64_t)i * 17;
+        L = pw[0];
+        if (lane < L) up[lane] = pw[1 + lane];
+    }
+    __syncwarp();
     float *out = a.o + ih;
     if (L == 0) {
 #pragma unroll
@@ -304,22 +326,16 @@ __global__ __launch_bounds__(32 * kPathWarps) void k_gdn_wy_paths(GdnArgs a) {
         return;
     }
     // path node t (root side first) is up[L - 1 - t].  The path's alpha and
-    // beta, q_i, (Q S_0^T)_i and the key rows are all requested here.
+    // beta and the key rows are all requested here.
     if (lane < 16) {
         const int node = lane < L ? up[L - 1 - lane] : 0;
         al[lane] = lane < L ? a.alpha[(int64_t)node * a.H + h] : 0.f;
         be[lane] = lane < L ? a.beta[(int64_t)node * a.H + h] : 0.f;
     }
-    const float *G2 = a.G + (int64_t)a.n * a.H * D;
-    float qi[P], g2[P];
-#pragma unroll
-    for (int m = 0; m < P; ++m) {
-        qi[m] = bf2f(a.q[ih + lane + 32 * m]);
-        g2[m] = G2[ih + lane + 32 * m];
-    }
     constexpr int CH = D / 8;  // 16-byte chunks per key row
-    for (int c = lane; c < 16 * CH; c += 32) {
-        const int t = c / CH, ch = c - t * CH;
+#pragma unroll
+    for (int it = 0; it < 16 * CH / 32; ++it) {
+        const int c = lane + 32 * it, t = c / CH, ch = c - t * CH;
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
         if (t < L) x = *reinterpret_cast<const uint4 *>(a.k + ((int64_t)up[L - 1 - t] * a.H + h) * D + 8 * ch);
         *reinterpret_cast<uint4 *>(Kp + t * KP + 8 * ch) = x;
@@ -370,8 +386,8 @@ __global__ __launch_bounds__(32 * kPathWarps) void k_gdn_wy_paths(GdnArgs a) {
     __syncwarp();  // the keys are no longer read: fs takes their place
     // w_t = v_t - gamma_t (K S_0^T)_t into fs, four columns per chunk
 #pragma unroll 8
-    for (int x = lane; x < 16 * (D / 4); x += 32) {
-        const int t = x / (D / 4), c = 4 * (x % (D / 4));
+    for (int it = 0; it < 16 * (D / 4) / 32; ++it) {
+        const int x = lane + 32 * it, t = x / (D / 4), c = 4 * (x % (D / 4));
         if (t < L) {
             const int64_t th = ((int64_t)up[L - 1 - t] * a.H + h) * D + c;
             const float4 g1 = *reinterpret_cast<const float4 *>(a.G + th);
@@ -446,7 +462,7 @@ cudaError_t launch_gdn_d(const GdnArgs &a, int mode, cudaStream_t s) {
 
 size_t gdn_workspace_bytes(int64_t n, int64_t H, int64_t D, int mode) {
     if (mode == 0) return 256;
-    return 256 + (size_t)2 * (size_t)n * (size_t)H * (size_t)D * 4;
+    return 256 + (size_t)2 * (size_t)n * (size_t)H * (size_t)D * 4 + ((size_t)n * 17 * 4 + 15) / 16 * 16;
 }
 
 cudaError_t launch_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -469,6 +485,7 @@ cudaError_t launch_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *
     a.o = o;
     a.err = static_cast<int32_t *>(workspace);
     a.G = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + 256);
+    a.paths = reinterpret_cast<int32_t *>(a.G + (int64_t)2 * n * H * D);
     if (D == 64) return launch_gdn_d<64>(a, mode, s);
     if (D == 128) return launch_gdn_d<128>(a, mode, s);
     return cudaErrorInvalidValue;

@@ -194,7 +194,7 @@ def test_gdn_argument_checks(w12lib):
     lib = w12lib.load()
     PATH, WY = w12lib.W12_GDN_PATH, w12lib.W12_GDN_WY
     assert lib.w12_gdn_workspace_bytes(63, 32, 128, PATH) == 256
-    assert lib.w12_gdn_workspace_bytes(63, 32, 128, WY) == 256 + 2 * 63 * 32 * 128 * 4
+    assert lib.w12_gdn_workspace_bytes(63, 32, 128, WY) == 256 + 2 * 63 * 32 * 128 * 4 + (63 * 17 * 4 + 15) // 16 * 16
     for n, H, D, mode in ((-1, 4, 64, WY), (1025, 4, 64, WY), (8, 0, 64, WY), (8, 4, 96, WY), (8, 4, 64, 2)):
         assert lib.w12_gdn_workspace_bytes(n, H, D, mode) == 0
     p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation
