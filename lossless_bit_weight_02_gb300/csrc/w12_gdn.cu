@@ -206,8 +206,9 @@ __global__ __launch_bounds__(32 * kProjWarps) void k_gdn_proj(GdnArgs a) {
     }
     // S_0[r][h] into the two BF16 parts (coalesced 16-byte loads, all in flight)
     const float4 *S0 = reinterpret_cast<const float4 *>(a.S0 + ((int64_t)r * a.H + h) * D * D);
-#pragma unroll 4
-    for (int x = tid; x < D * D / 4; x += 32 * kProjWarps) {
+#pragma unroll
+    for (int it = 0; it < D * D / 4 / (32 * kProjWarps); ++it) {
+        const int x = tid + 32 * kProjWarps * it;
         const float4 v4 = S0[x];
         const int c = (4 * x) / D, kk = (4 * x) % D;
         uint32_t h0, l0, h1, l1;

@@ -187,3 +187,25 @@ def test_selected_tree_feeds_the_recurrence():
 def test_maximum_nodes():
     """1024 nodes (the limit) over 2 requests, 4 heads, D = 128."""
     check_case(synth.gdn_inputs(1024, 4, 128, seed=19, R=2))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_shapes_and_gates(seed):
+    """Seeded draws of size, heads, dimension, requests and tree shape, with
+    decay and write strength over the whole [0, 1] (exact 0 and 1 included)."""
+    rng = np.random.default_rng(900 + seed)
+    n = int(rng.integers(1, 200))
+    H = int(rng.integers(1, 4))
+    D = int(rng.choice([64, 128]))
+    R = int(rng.integers(1, 5))
+    parent = synth.random_tree(n, seed=950 + seed, max_depth=int(rng.integers(1, 17)),
+                               new_root=float(rng.uniform(0.02, 0.5)))
+    S0, q, k, v, alpha, beta, parent, req = synth.gdn_inputs(n, H, D, seed=970 + seed, R=R, parent=parent)
+    alpha = rng.uniform(0.0, 1.0, size=alpha.shape).astype(np.float32)
+    beta = rng.uniform(0.0, 1.0, size=beta.shape).astype(np.float32)
+    pick = rng.random(alpha.shape)
+    alpha[pick < 0.05] = 0.0
+    alpha[pick > 0.9] = 1.0
+    beta[pick < 0.1] = 1.0
+    beta[(pick > 0.5) & (pick < 0.55)] = 0.0
+    check_case((S0, q, k, v, alpha, beta, parent, req))
