@@ -12,7 +12,11 @@ of rank-one updates into matrix products).  The definition
   * the composition of explicit per-step affine maps (library matrix
     products), with dk != dv so that a transposed state shows;
   * prefix independence: a node's output does not depend on other branches.
-The matrix form (`wy_outputs`) is checked against the definition.
+The matrix form (`wy_outputs`) is checked against the definition.  Copies of
+the recurrence with a planted mistake (a sign, a missing decay or write
+strength, the decay on the wrong term, the key projection missing or on the
+wrong side, the output taken before the update, the path applied leaf first)
+must each fail at least one of the pins.
 """
 import json
 import os
@@ -133,3 +137,84 @@ def test_depth_limit_and_bad_parent():
         gdn.depths(np.array([-1, 1, 0]))
     with pytest.raises(ValueError):
         gdn.depths(np.array([-2]))
+
+
+# ---- the pins catch plausible mistakes: each planted in a copy of the oracle's recurrence ----
+
+def _path_variant(step, out_before=False, leaf_first=False):
+    """path_outputs with the update `step(S, k, v, alpha, beta)` swapped in."""
+    def fn(S0, q, k, v, alpha, beta, parent):
+        S0 = np.asarray(S0, np.float64)
+        q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
+        alpha, beta = np.asarray(alpha, np.float64), np.asarray(beta, np.float64)
+        o = np.zeros((q.shape[0], S0.shape[0], S0.shape[1]))
+        for i in range(q.shape[0]):
+            path = gdn.root_path(parent, i)
+            if leaf_first:
+                path = path[::-1]
+            for h in range(S0.shape[0]):
+                S = S0[h].copy()
+                for t in path:
+                    if out_before and t == i:
+                        o[i, h] = S @ q[i, h]
+                    S = step(S, k[t, h], v[t, h], alpha[t, h], beta[t, h])
+                if not out_before:
+                    o[i, h] = S @ q[i, h]
+        return o
+    return fn
+
+
+def _right(S, k, v, a, b):
+    return a * (S - b * np.outer(S @ k, k)) + b * np.outer(v, k)
+
+
+MUTANTS = {
+    "sign of the erase term": lambda S, k, v, a, b: a * (S + b * np.outer(S @ k, k)) + b * np.outer(v, k),
+    "decay missing on the erase term": lambda S, k, v, a, b: a * S - b * np.outer(S @ k, k) + b * np.outer(v, k),
+    "decay applied after the write": lambda S, k, v, a, b: a * (S - b * np.outer(S @ k, k) + b * np.outer(v, k)),
+    "write strength missing on the value": lambda S, k, v, a, b: a * (S - b * np.outer(S @ k, k)) + np.outer(v, k),
+    "erase term without the key projection": lambda S, k, v, a, b: a * (S - b * S) + b * np.outer(v, k),
+    "erase term with the key on the wrong side": lambda S, k, v, a, b: _left_erase(S, k, v, a, b),
+}
+
+
+def _left_erase(S, k, v, a, b):
+    """(I - b k k^T) S instead of S (I - b k k^T); only defined for square states."""
+    if S.shape[0] != S.shape[1]:
+        raise ValueError("left erase needs dv == dk")
+    return a * (S - b * np.outer(k, k @ S)) + b * np.outer(v, k)
+
+
+def _pins_pass(fn):
+    """True when `fn` passes every pin of this file (shapes as in the tests above)."""
+    ok = True
+    try:
+        cases = json.load(open(os.path.join(HERE, "golden", "worked_gdn.json")))["cases"]
+        for c in cases:
+            args = [np.array(c[x], np.float64) for x in ("S0", "q", "k", "v", "alpha", "beta")]
+            ok &= np.allclose(fn(*args, np.array(c["parent"])), np.array(c["o"]), rtol=0, atol=1e-12)
+        rng = np.random.default_rng(2)
+        S0, q, k, v, alpha, beta, parent = random_case(rng, 24, 3, 8, 5)
+        beta[:] = 1.0
+        ok &= np.allclose(fn(S0, k.copy(), k, v, alpha, beta, parent), v, rtol=0, atol=1e-12)
+        for dk, dv in [(5, 3), (3, 6), (4, 4)]:
+            case = random_case(np.random.default_rng(10 + dk * 7 + dv), 18, 2, dk, dv, unit_keys=False)
+            ok &= np.allclose(fn(*case), gdn.composite_outputs(*case), rtol=1e-11, atol=1e-11)
+    except (ValueError, IndexError):  # a shape error is a failed pin too
+        return False
+    return bool(ok)
+
+
+def test_pins_accept_the_oracle():
+    assert _pins_pass(_path_variant(_right))
+    assert _pins_pass(gdn.path_outputs)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_planted_update_mistakes(name):
+    assert not _pins_pass(_path_variant(MUTANTS[name])), name
+
+
+def test_pins_reject_output_before_update_and_reversed_order():
+    assert not _pins_pass(_path_variant(_right, out_before=True))
+    assert not _pins_pass(_path_variant(_right, leaf_first=True))
