@@ -238,6 +238,22 @@ def run_gpu(args):
     clocks = sampler.stop()
     total_ms = job_time_ms(start.elapsed_time(stop), ws_n, dev)
 
+    # run-to-run spread of the same step: 5 more batches of 50 steps, events
+    # around each batch only (not part of `value`)
+    batch_ms = []
+    for _ in range(5):
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(50):
+            one_step()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        batch_ms.append(b0.elapsed_time(b1) / 50)
+    batch_ms.sort()
+    noise = {"batches": 5, "steps_per_batch": 50,
+             "gbs": [round(step_bytes / (x * 1e-3) / 1e9, 1) for x in batch_ms[::-1]],
+             "spread_pct": round(100.0 * (batch_ms[-1] - batch_ms[0]) / statistics.median(batch_ms), 2)}
+
     # the same step replayed from a CUDA graph (how a serving engine launches a
     # fixed sequence of GEMMs): 10 steps per graph, on a side stream
     gstream = torch.cuda.Stream(dev)
@@ -580,6 +596,7 @@ def run_gpu(args):
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
         "tree": tree,
         "gdn": gdn,
+        "noise": noise,
         "size_calibration": size_cal, "nested8": nested,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "matches_device_outputs": e2e_match,
                 "method": "per step: one pinned host->device copy of all 16 activations, the 16 w12_gemm calls "
