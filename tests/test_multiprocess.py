@@ -7,7 +7,8 @@ library groups them by 16-row stripe).  Each rank slices its rows with
 W12Tensor.rows (host logic, here on CPU tensors), computes its block of Y
 with the oracle, and an all-gather must give exactly the unsharded oracle
 result.  The benchmark's whole-job time is the slowest rank's, and its
-value counts the bytes of every rank.
+value counts the bytes of every rank.  The recurrent-layer outputs of draft
+trees shard by request and by head, also with no exchange.
 """
 import importlib.util
 import os
@@ -102,3 +103,61 @@ def test_two_ranks_n_sharded_gemm_and_job_time(N, K, M, split, w12lib, oracle):
         assert same, rank
         assert t_job == 2.5  # the slower rank's 2.5 ms on both
         assert v == pytest.approx(1e9 * 10 * 2 / 2.5e-3 / 1e9)
+
+
+def gdn_worker(rank, world, port, q):
+    """Each rank takes half of the requests of a shared-budget tree and half of
+    the heads: its block of the recurrent-layer outputs, computed with the
+    oracle on its own nodes and heads, must equal the same block of the
+    unsharded result (requests and heads exchange nothing)."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import sys
+        sys.path.insert(0, ROOT)
+        from lossless_bit_weight_02_gb300 import synth
+        from oracle import gdn
+
+        n, H, D, R = 48, 4, 8, 4
+        S0, qb, kb, vb, alpha, beta, parent, req = synth.gdn_inputs(n, H, D, seed=31, R=R)
+        f = lambda b: (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)  # noqa: E731
+        qf, kf, vf = f(qb), f(kb), f(vb)
+
+        def outputs(reqs, heads):
+            o = np.zeros((n, len(heads), D))
+            for r in reqs:
+                idx = np.flatnonzero(req == r)
+                remap = {int(j): x for x, j in enumerate(idx)}
+                par = np.array([remap[int(parent[j])] if parent[j] >= 0 else -1 for j in idx], np.int64)
+                o[idx] = gdn.path_outputs(S0[r][heads], qf[idx][:, heads], kf[idx][:, heads], vf[idx][:, heads],
+                                          alpha[idx][:, heads], beta[idx][:, heads], par)
+            return o
+
+        mine_r = [r for r in range(R) if r % world == rank]
+        mine_h = [h for h in range(H) if h % world == rank]
+        block = torch.from_numpy(outputs(mine_r, mine_h))
+        got = [torch.zeros_like(block) for _ in range(world)]
+        dist.all_gather(got, block)
+        full = outputs(range(R), list(range(H)))
+        ok = True
+        for src in range(world):
+            rows = np.isin(req, [r for r in range(R) if r % world == src])
+            heads = [h for h in range(H) if h % world == src]
+            ok &= bool(np.array_equal(got[src].numpy()[rows], full[rows][:, heads]))
+        q.put((rank, ok))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_gdn_tree_sharded_by_request_and_head():
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    port = free_port()
+    procs = [ctx.Process(target=gdn_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=300)
+        assert p.exitcode == 0
+    res = sorted(q.get() for _ in range(2))
+    assert all(ok for _, ok in res), res
