@@ -41,7 +41,8 @@
 namespace w12 {
 namespace {
 
-constexpr int kGdnMaxDepth = 16;
+constexpr int kGdnMaxDepth = W12_GDN_MAX_DEPTH;  // nodes on a root path
+constexpr int kGdnMaxNodes = W12_GDN_MAX_NODES;  // nodes in one call
 
 struct GdnArgs {
     const float *S0;                 // [R][H][D][D]
@@ -176,7 +177,7 @@ constexpr int kProjWarps = 8;
 
 template <int D>
 __host__ __device__ constexpr int proj_smem_bytes() {
-    return 2 * D * (D + 8) * 2 + 4 * 1024 + 16;
+    return 2 * D * (D + 8) * 2 + 4 * kGdnMaxNodes + 16;
 }
 
 template <int D>
@@ -186,7 +187,7 @@ __global__ __launch_bounds__(32 * kProjWarps) void k_gdn_proj(GdnArgs a) {
     uint16_t *hi = reinterpret_cast<uint16_t *>(smem_proj);  // [D][KP]: row c = S_0 row c (value index)
     uint16_t *lo = hi + D * KP;
     int *list = reinterpret_cast<int *>(lo + D * KP);         // nodes of this request
-    int *cnt = list + 1024;
+    int *cnt = list + kGdnMaxNodes;
     const int r = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q4 = lane & 3;
     if (tid == 0) *cnt = 0;
@@ -279,6 +280,7 @@ __global__ __launch_bounds__(32 * kProjWarps) void k_gdn_proj(GdnArgs a) {
 // Lane l holds columns l, l + 32, ... of every vector.
 // ---------------------------------------------------------------------------
 constexpr int kPathWarps = 4;  // warps (nodes) per CTA
+static_assert(kGdnMaxDepth == 16, "a root path fills the 16 rows of one m16n8k16 tile");
 
 template <int D>
 __host__ __device__ constexpr int path_warp_bytes() {
