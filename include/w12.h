@@ -291,7 +291,8 @@ w12_status w12_tree_select(const float *lp, int32_t R, int32_t D, int32_t C, int
  * workspace: device, w12_gdn_workspace_bytes(n, H, D, mode) bytes, 16-byte
  * aligned, no initial contents needed.  Alignment: S0, q, k, v, o 16 bytes;
  * alpha, beta, parent, req 4 bytes (W12_ERR_ALIGN).  Limits: 0 <= n <=
- * W12_GDN_MAX_NODES, D in {64, 128}, 1 <= H <= 65535 (W12_ERR_INVALID).
+ * W12_GDN_MAX_NODES, D in {64, 128}, 1 <= H <= 65535, 1 <= R <=
+ * W12_GDN_MAX_REQUESTS (W12_ERR_INVALID).
  * A tree that breaks the rules on parent / req / depth is detected on the
  * device: the nodes concerned get NaN outputs and w12_gdn_status reports
  * W12_ERR_INVALID for this call.  Asynchronous. */
@@ -299,6 +300,7 @@ w12_status w12_tree_select(const float *lp, int32_t R, int32_t D, int32_t C, int
 #define W12_GDN_WY 1
 #define W12_GDN_MAX_DEPTH 16
 #define W12_GDN_MAX_NODES 1024
+#define W12_GDN_MAX_REQUESTS 65536
 size_t w12_gdn_workspace_bytes(int64_t n, int64_t H, int64_t D, int32_t mode);
 w12_status w12_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                         const float *beta, const int32_t *parent, const int32_t *req, int64_t n, int64_t H,

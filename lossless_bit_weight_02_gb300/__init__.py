@@ -368,6 +368,7 @@ W12_GDN_PATH = 0
 W12_GDN_WY = 1
 W12_GDN_MAX_DEPTH = 16
 W12_GDN_MAX_NODES = 1024
+W12_GDN_MAX_REQUESTS = 65536
 
 
 class TreeCall:

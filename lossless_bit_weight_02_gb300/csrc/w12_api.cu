@@ -286,7 +286,7 @@ w12_status w12_gdn_tree(const float *S0, const uint16_t *q, const uint16_t *k, c
                         const float *beta, const int32_t *parent, const int32_t *req, int64_t n, int64_t H,
                         int64_t R, int64_t D, float *o, void *workspace, size_t ws_bytes, int32_t mode,
                         w12_stream_t stream) {
-    if (n < 0 || n > W12_GDN_MAX_NODES || H < 1 || H > 65535 || R < 1 || R > (1LL << 30) ||
+    if (n < 0 || n > W12_GDN_MAX_NODES || H < 1 || H > 65535 || R < 1 || R > W12_GDN_MAX_REQUESTS ||
         (D != 64 && D != 128) || (mode != W12_GDN_PATH && mode != W12_GDN_WY))
         return W12_ERR_INVALID;
     if (!workspace || (n > 0 && (!S0 || !q || !k || !v || !alpha || !beta || !parent || !o)))

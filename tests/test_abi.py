@@ -204,7 +204,8 @@ def test_gdn_argument_checks(w12lib):
         return lib.w12_gdn_tree(*ptrs[:8], n, H, R, D, ptrs[8], ptrs[9], ws, mode, None)
 
     ok = [p] * 10
-    for kw in ({"n": -1}, {"n": 1025}, {"H": 0}, {"R": 0}, {"D": 32}, {"D": 100}, {"mode": 3}):
+    for kw in ({"n": -1}, {"n": 1025}, {"H": 0}, {"R": 0}, {"R": w12lib.W12_GDN_MAX_REQUESTS + 1}, {"D": 32},
+               {"D": 100}, {"mode": 3}):
         assert call(*ok, **kw) == w12lib.W12_ERR_INVALID, kw
     for i in range(10):
         if i == 7:  # req may be NULL
