@@ -124,6 +124,28 @@ def ncu_traffic(shape_bytes):
     return None if ratio is None else ratio * shape_bytes
 
 
+def tc_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lossless_bit_weight_02_gb300", "csrc")
+    for fn in ("w12_gemm_tc.cu", "w12_device.cuh", "w12_stream.cuh"):
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def tensor_pipe_share():
+    """sm__pipe_tensor_cycles_active (% of peak) of the tcgen05 kernel at
+    M = 64 from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemm_tc_tensor_pipe.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != tc_source_hash():
+        return None
+    return d.get("tensor_pipe_active_pct")
+
+
 # ---------------------------------------------------------------------------
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -213,13 +235,6 @@ def run_gpu(args):
         one_step()
     torch.cuda.synchronize()
 
-    # per-launch events on every 40th timed step only: an event between two
-    # launches keeps the second from overlapping the first, so an
-    # instrumented step runs its 16 launches without the overlap
-    ev_steps = list(range(0, args.steps, 40))
-    n_ev = len(ev_steps)
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-            for _ in range(launches_per_step)] for _ in range(n_ev)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -228,15 +243,25 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
-    ev_of = {k: i for i, k in enumerate(ev_steps)}
     for k in range(args.steps):
-        one_step(evs[ev_of[k]] if k in ev_of else None)
+        one_step()
     stop.record(stream)
     torch.cuda.synchronize()
     if ws_n > 1:
         dist.barrier()
     clocks = sampler.stop()
     total_ms = job_time_ms(start.elapsed_time(stop), ws_n, dev)
+
+    # Per-launch events, after the timed region, on 10 more steps: an event
+    # between two launches keeps the second from overlapping the first, so
+    # these launches run serialised (each pays its own fill and drain); they
+    # explain the step, they are not its time.
+    n_ev = 10
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(launches_per_step)] for _ in range(n_ev)]
+    for k in range(n_ev):
+        one_step(evs[k])
+    torch.cuda.synchronize()
 
     # run-to-run spread of the same step: 5 more batches of 50 steps, events
     # around each batch only (not part of `value`)
@@ -281,7 +306,7 @@ def run_gpu(args):
     value_graph = job_value(step_bytes, 10 * g_reps, ws_n, graph_ms)
     del step_graph, gcalls
 
-    # per-launch kernel durations -> per (M, layer) and overall
+    # per-launch kernel durations (serialised launches) -> per (M, layer)
     dur = {}
     j = 0
     for M in M_VALUES:
@@ -290,7 +315,14 @@ def run_gpu(args):
             j += 1
     kern_ms = sum(sum(v) for v in dur.values())
     kern_bytes = sum(alg_bytes[key] * len(v) for key, v in dur.items())
-    achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
+    achieved_serial = kern_bytes / (kern_ms * 1e-3) / 1e9
+    # The step's only kernel is k_gemm_mma<1> (every M <= 8); its launches
+    # overlap one another (programmatic dependent launch), so the kernel's
+    # device time per step is the step's device time, and the roofline's
+    # achieved rate is the step's algorithmic bytes over it.
+    step_alg_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers)
+    step_ms = total_ms / args.steps
+    achieved = step_alg_bytes / (step_ms * 1e-3) / 1e9
     per_m = {}
     for M in M_VALUES:
         b = sum(layers_t.nbytes() for _, layers_t in layers)
@@ -343,7 +375,8 @@ def run_gpu(args):
                 "roofline_frac": round(floor_s / (ms * 1e-3), 4), "us": round(ms * 1e3, 1),
                 "us_launch_events": round(statistics.median(tl) * 1e3, 1)}
 
-    sweep = {}
+    sweep = {"1": sweep_point(1, lambda name: calls[(1, name)])}
+    sweep["1"]["path"] = "mma"
     for M in SWEEP_M:
         sweep[str(M)] = sweep_point(M, lambda name, M=M: calls[(M, name)])
         sweep[str(M)]["path"] = "mma" if M <= 16 else "tcgen05"
@@ -571,6 +604,18 @@ def run_gpu(args):
     size_cal["method"] = ("torch dst.copy_(src) of the layer's W12 byte count, read+write bytes / best of 8, "
                           "L2 flushed before each copy")
 
+    # the metric's three points, M = 1 / 16 / 64, each the four layers back to
+    # back (the sweep's method); M = 64 runs on the tcgen05 path
+    roofline_by_m = {}
+    for M in (1, 16, 64):
+        sp = sweep[str(M)]
+        roofline_by_m[str(M)] = {"frac": sp["roofline_frac"], "weight_gbs": sp["weight_gbs"],
+                                 "tflops": sp["tflops"], "us_4_layers": sp["us"], "path": sp["path"],
+                                 "bound": "hbm" if M < 200 else "hbm+tensor"}
+    tp = tensor_pipe_share()
+    if tp is not None:
+        roofline_by_m["64"]["tensor_pipe_active_pct_ncu"] = tp
+
     value = job_value(step_bytes, args.steps, ws_n, total_ms)
     e2e_val = step_bytes * e2e_steps * ws_n / (e2e_ms * 1e-3) / 1e9
     top_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers) / launches_per_step
@@ -590,7 +635,17 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
-                     else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)"},
+                     else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)",
+                     "method": "algorithmic bytes of the step's 16 launches (W12 bytes + activations + "
+                               "outputs) / the step's device time in the timed region (the kernel is the "
+                               "step's only one; its launches overlap)",
+                     "bytes_per_step": step_alg_bytes,
+                     "serialised_launches": {
+                         "achieved": round(achieved_serial, 1), "frac": round(achieved_serial / hbm_peak, 4),
+                         "steps": n_ev,
+                         "note": "CUDA events around every launch of 10 steps after the timed region; an event "
+                                 "between launches serialises them, so each pays its own fill and drain"}},
+        "roofline_by_m": roofline_by_m,
         "value_graph": {"value": round(value_graph, 1), "unit": "GB/s",
                         "note": "the same 16-launch step replayed from a CUDA graph (10 steps per graph)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,

@@ -125,9 +125,20 @@ typedef struct {
 
 /* Options of w12_gemm (NULL = all defaults).  Results are bitwise identical
  * for any max_ctas and with or without W12_GEMM_OVERLAP_PREVIOUS; they depend
- * only on (M, N, K, path, split_k, W12_GEMM_NESTED8). */
+ * only on (M, N, K, path, split_k, W12_GEMM_NESTED8).
+ *
+ * How the work is cut.  Both paths cut a GEMM into work items that are a
+ * function of (M, N, K, path, split_k) alone, and every CTA walks items
+ * blockIdx.x, blockIdx.x + gridDim.x, ...; the order of every sum is fixed
+ * by the items, so the grid (max_ctas, the device's SM count, occupancy)
+ * never changes a result.  The automatic cut is sized for W12_PLAN_SMS SMs,
+ * the SM count of a GB300: one range of work per resident warp (small-M
+ * path) or per SM (balanced tensor-core ranges), and K-chunk splits that fill
+ * one or two CTAs per SM.  On a part with another SM count the results stay
+ * the same and correct; only the balance of work across SMs changes. */
+#define W12_PLAN_SMS 152
 typedef struct {
-    int32_t max_ctas;       /* 0 = as many as fit; >0 caps the grid (tests) */
+    int32_t max_ctas;       /* 0 = as many as fit; >0 caps the grid on either path (tests) */
     int32_t split_k;        /* 0 = chosen from (M,N,K); >0 forces the split */
     int32_t path;           /* W12_PATH_* */
     int32_t flags;          /* W12_GEMM_* bits; unknown bits are rejected */
@@ -203,18 +214,31 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
  * every GPU that loads the library keeps until the process exits.  It calls
  * no allocation routine.
  *   - Shapes and options whose w12_gemm workspace would exceed the scratch
- *     return W12_ERR_CAPACITY (the automatic split of any shape with
- *     M <= 16 fits).
+ *     return W12_ERR_CAPACITY.  The automatic plan of every shape with
+ *     M <= 16 (the small-M path) fits.  Most automatic tensor-core plans
+ *     (M > 16) on large layers do not: their split-K partials need 4.8 MB
+ *     (M = 17..32) to 40 MB (M = 256) on the 27B-class layer shapes.  With
+ *     split_k = 1 forced, every M <= 256 fits (no partials are needed).
+ *   - Options that w12_gemm rejects get the same status here.
  *   - The first call on a device looks up the scratch array's device
- *     address (once per device, with that device current); make that first
- *     call before any stream capture.
- *   - Every call shares the one scratch array and clears its counters on
- *     `stream` before use, so calls that overlap on the GPU (different
- *     streams, or different host threads) race and must not be issued.
+ *     address there (loading the library's device code on that device); make
+ *     that first call before any stream capture.
+ *   - Every call shares the one scratch array and clears its counters and
+ *     error word on `stream` before use, so calls that overlap on the GPU
+ *     (different streams, or different host threads) race and must not be
+ *     issued.
  * Asynchronous on `stream`, like w12_gemm. */
 #define W12_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 w12_status w12_gemm_noalloc(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_t *Y,
                             int64_t ldy, int64_t M, const w12_gemm_opts *opts, w12_stream_t stream);
+
+/* ---- w12_gemm_noalloc_status ----  The paper has no counterpart either.
+ * Reads and clears the scratch array's error word on the current device:
+ * W12_ERR_TIMEOUT if a bounded wait of the last w12_gemm_noalloc call
+ * there gave up (its Y is then unspecified), else W12_OK.  Synchronous on
+ * `stream`; call it after the w12_gemm_noalloc call it checks and before the
+ * next one, which clears the word. */
+w12_status w12_gemm_noalloc_status(w12_stream_t stream);
 
 /* Reads (and clears) the device-side error word that bounded waits inside
  * w12_gemm set when they give up.  Synchronous on `stream`.  Returns W12_OK

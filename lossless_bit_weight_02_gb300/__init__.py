@@ -46,7 +46,8 @@ EXPORTS = (
     "w12_rows_padded", "w12_cols_padded", "w12_hi_bytes", "w12_lo_bytes", "w12_groups",
     "w12_esc_ptr_len", "w12_encode",
     "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
-    "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_noalloc", "w12_gemm_workspace_status",
+    "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_noalloc", "w12_gemm_noalloc_status",
+    "w12_gemm_workspace_status",
     "w12_tree_workspace_bytes", "w12_tree_select",
     "w12_gdn_workspace_bytes", "w12_gdn_tree", "w12_gdn_status",
     "w12_status_string", "w12_version",
@@ -109,6 +110,7 @@ def load(path: str | None = None):
                               ctypes.POINTER(GemmOpts), vp]),
             "w12_gemm_noalloc": (st, [vp, i64, ctypes.POINTER(_Tensor), vp, i64, i64,
                                       ctypes.POINTER(GemmOpts), vp]),
+            "w12_gemm_noalloc_status": (st, [vp]),
             "w12_gemm_workspace_status": (st, [vp, sz, vp]),
             "w12_tree_workspace_bytes": (sz, [ctypes.c_int32, ctypes.c_int32]),
             "w12_tree_select": (st, [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -151,6 +153,30 @@ def _need_cuda(t: torch.Tensor, name: str, dtype=None):
         raise ValueError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check_gemm_operands(A: torch.Tensor, t: "W12Tensor", Y: torch.Tensor | None):
+    """The C side trusts lda / ldy and writes M rows of N outputs, so the
+    shapes, strides and devices are checked here, before any pointer is
+    passed: A is [M, K] and Y is [M, N], both with unit column stride, on the
+    device that holds the W12 tensor, which must be the current device (the
+    library launches on the current device)."""
+    _need_cuda(A, "A", torch.bfloat16)
+    if A.dim() != 2 or A.shape[1] != t.K or (A.shape[0] > 0 and t.K > 0 and A.stride(1) != 1):
+        raise ValueError(f"A must be [M, {t.K}] with unit column stride, got {tuple(A.shape)} "
+                         f"strides {A.stride()}")
+    dev = t.hi.device
+    if A.device != dev:
+        raise ValueError(f"A is on {A.device}, the W12 tensor on {dev}")
+    if dev.index != torch.cuda.current_device():
+        raise ValueError(f"the W12 tensor is on {dev} but the current device is cuda:{torch.cuda.current_device()}")
+    if Y is not None:
+        _need_cuda(Y, "Y", torch.bfloat16)
+        if Y.dim() != 2 or tuple(Y.shape) != (A.shape[0], t.N) or (Y.numel() > 0 and Y.stride(1) != 1):
+            raise ValueError(f"Y must be [{A.shape[0]}, {t.N}] with unit column stride, got {tuple(Y.shape)} "
+                             f"strides {Y.stride()}")
+        if Y.device != dev:
+            raise ValueError(f"Y is on {Y.device}, the W12 tensor on {dev}")
 
 
 @dataclass
@@ -309,7 +335,7 @@ def default_workspace(device) -> Workspace:
 def w12_gemm(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor | None = None, workspace: Workspace | None = None,
              opts: GemmOpts | None = None, stream=None) -> torch.Tensor:
     """Y[M,N] = A[M,K] * W^T with W in W12 (BF16 out, FP32 accumulation)."""
-    _need_cuda(A, "A", torch.bfloat16)
+    _check_gemm_operands(A, t, Y)
     M = A.shape[0]
     if Y is None:
         Y = torch.empty(M, t.N, dtype=torch.bfloat16, device=A.device)
@@ -329,8 +355,7 @@ class GemmCall:
 
     def __init__(self, A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, workspace: Workspace,
                  opts: GemmOpts | None = None, stream=None):
-        _need_cuda(A, "A", torch.bfloat16)
-        _need_cuda(Y, "Y", torch.bfloat16)
+        _check_gemm_operands(A, t, Y)
         self._opts = opts if opts is not None else make_opts()
         need = w12_gemm_workspace_bytes(A.shape[0], t.N, t.K, self._opts)
         ws = workspace.ensure(max(need, 256))
@@ -351,8 +376,9 @@ def w12_gemm_noalloc(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, opts: GemmO
                      stream=None) -> torch.Tensor:
     """w12_gemm without a workspace: the library's built-in scratch array is
     used (for callers that cannot allocate device memory).  Y must be given."""
-    _need_cuda(A, "A", torch.bfloat16)
-    _need_cuda(Y, "Y", torch.bfloat16)
+    if Y is None:
+        raise ValueError("w12_gemm_noalloc needs the output Y")
+    _check_gemm_operands(A, t, Y)
     o = opts if opts is not None else make_opts()
     s = t.struct()
     _check(load().w12_gemm_noalloc(ctypes.c_void_p(A.data_ptr()), A.stride(0), ctypes.byref(s),
@@ -459,6 +485,12 @@ class GdnCall:
 def w12_gdn_tree(S0, q, k, v, alpha, beta, parent, req=None, mode=None, stream=None) -> torch.Tensor:
     """Gated-delta-rule outputs of draft-tree nodes (w12_gdn_tree); see GdnCall."""
     return GdnCall(S0, q, k, v, alpha, beta, parent, req, mode, stream)()
+
+
+def w12_gemm_noalloc_status(stream=None) -> int:
+    """W12_ERR_TIMEOUT if a bounded wait of the last w12_gemm_noalloc call on
+    the current device gave up (read and cleared; synchronous), else W12_OK."""
+    return load().w12_gemm_noalloc_status(_stream(stream))
 
 
 def w12_gemm_workspace_status(workspace: Workspace, stream=None) -> int:

@@ -13,7 +13,6 @@ using namespace w12;
 
 constexpr int64_t kMaxK = (1LL << 31) - 128;  // columns are int32 in the escape list
 constexpr int64_t kMaxN = 1LL << 30;
-constexpr int64_t kMaxCounters = 1LL << 16;  // split-K stripes with an arrival counter
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -75,12 +74,11 @@ w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, Ge
     const bool tc = pl.path == W12_PATH_TC;
     const int64_t G = groups_of(K);
     const int64_t Np = rows_padded(N);
-    const bool counters_ok = Np / 16 <= kMaxCounters;  // arrival counters exist for at most kMaxCounters stripes
+    const bool counters_ok = Np / 16 <= kWsMaxCounters;  // arrival counters exist for at most kWsMaxCounters stripes
     // Fixed layout, the same for every shape, so that the counter region is
-    // never reused for partials: [0,256) error word | [256, 256+4*kMaxCounters)
-    // arrival counters (zero between calls) | FP32 partials.
-    pl.counters_off = 256;
-    pl.partials_off = 256 + 4 * kMaxCounters;
+    // never reused for partials (w12_internal.h).
+    pl.counters_off = kWsCountersOff;
+    pl.partials_off = kWsPartialsOff;
     if (tc) {
         pl.mp = gemm_tc_pad(M);
         const int64_t pbytes = gemm_tc_plan(M, N, K, o ? o->split_k : 0, counters_ok, pl.cut);
@@ -101,6 +99,15 @@ w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, Ge
 w12_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W12_OK : W12_ERR_CUDA; }
 
 }  // namespace
+
+namespace w12 {
+w12_status gemm_plan_bytes(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *opts, size_t *bytes) {
+    GemmPlan pl;
+    const w12_status st = plan_gemm(M, N, K, opts, pl);
+    *bytes = st == W12_OK ? pl.bytes : 0;
+    return st;
+}
+}  // namespace w12
 
 extern "C" {
 

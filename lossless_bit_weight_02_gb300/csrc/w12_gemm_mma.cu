@@ -520,7 +520,7 @@ int64_t gemm_mma_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counter
         cut(G, S, T);
         return S > 1 ? g.ranges : 0;
     }
-    int64_t V = (M <= 8 ? 16 : 12) * 152;
+    int64_t V = (M <= 8 ? 16 : 12) * (int64_t)W12_PLAN_SMS;
     if (V > U) V = U;
     cut(U, V, 1);
     for (int64_t v = 1; v < V; ++v) {  // any range boundary inside a stripe needs partials

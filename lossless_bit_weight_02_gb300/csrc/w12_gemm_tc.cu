@@ -30,7 +30,10 @@
 // memory for the given Mpad.  The epilogue warps read the accumulator with
 // tcgen05.ld.  With a split of S > 1 the chunk partials go to the FP32
 // workspace and the last CTA of a row tile adds them in the order
-// s = 0..S-1; S depends only on (M, N, K).
+// s = 0..S-1; S depends only on (M, N, K).  The work items (row tile,
+// K-chunk) or balanced ranges are fixed by (M, N, K) too; a CTA walks items
+// blockIdx.x, blockIdx.x + gridDim.x, ..., so a grid capped by
+// w12_gemm_opts.max_ctas computes bitwise the same result.
 // Every mbarrier wait is bounded in time (about a second, read from the
 // global nanosecond timer): on expiry the CTA records W12_ERR_TIMEOUT in the
 // workspace error word, waits (bounded) for its own copies and MMAs, and
@@ -239,6 +242,15 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
 // hmap / lmap: the hi / lo plane as u8 [stripes][k-blocks][4 or 2][256], box
 // [8 stripes][1 k-block][4 or 2][256]: one copy brings the row tile's 8
 // tiles of a k-block (stripes past the end read as zero).
+//
+// Work items are (row tile, K-chunk) pairs, item = row_tile*S + chunk.  A CTA
+// takes items blockIdx.x, blockIdx.x + gridDim.x, ...: with the default grid
+// (one CTA per item) that is one item, with a capped grid several.  The rings
+// and their phases run on from one item to the next; the accumulator in TMEM
+// is reused, and every decoder warp finishes reading it (the item's epilogue)
+// before any of them decodes a tile of the next item, so no MMA of the next
+// item can overwrite it early.  The item, its chunk bounds and the order of
+// the split-K sum depend on (M, N, K) only, never on the grid.
 template <int D>
 __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_gemm_tc(
     TensorView t, GemmArgs g, TcParams tp, const __grid_constant__ CUtensorMap tmap,
@@ -261,21 +273,26 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
     uint64_t *a_empty = a_full + RA;
     uint64_t *b_full = a_empty + RA;
     uint64_t *b_empty = b_full + RB;
-    uint64_t *done = b_empty + RB;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *done = b_empty + RB;  // one phase per item: its MMAs have completed
+    uint64_t *fin = done + 1;        // the MMA warp's own last wait: every MMA it issued has completed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = g.split;
-    const int64_t tt = blockIdx.x / S;  // 128-row tile
-    const int s = (int)(blockIdx.x % S);
-    const int64_t g_beg = (s * t.G) / S, g_end = ((s + 1) * t.G) / S;
-    const int nkb = (int)(4 * (g_end - g_beg));
     const int64_t T = t.Np / 16;
+    const int items = (int)((t.Np + 127) / 128) * S;
+    // groups [g_beg, g_end) of item `item` and its row tile
+    auto item_span = [&](int item, int64_t &tt, int64_t &g_beg, int64_t &g_end) {
+        tt = item / S;
+        const int s = item - (int)tt * S;
+        g_beg = (s * t.G) / S;
+        g_end = ((s + 1) * t.G) / S;
+    };
 
     // the descriptors of the first copies load while the barriers are set up
-    if (nkb > 0 && lane == 0) {
+    if (lane == 0) {
         if (warp == kWProdWarp) {
             prefetch_tmap(&hmap);
             if (!g.nested8) prefetch_tmap(&lmap);
@@ -297,6 +314,7 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
             mbar_init(&b_empty[i], 1);
         }
         mbar_init(done, 1);
+        mbar_init(fin, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -318,229 +336,254 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
         // (8 decoder warps) or on the k-blocks of parity w/8 (16 warps:
         // tiles p = w/8 and w/8 + 2 of every group): the tile's planes come
         // from the weight ring, the BF16 tile goes to the A ring (K-major,
-        // 128-byte swizzle), escapes over their slots.
+        // 128-byte swizzle), escapes over their slots.  Every decoder warp
+        // runs every item and every named barrier, also after an abort
+        // (its waits then return at once), so the barriers always match.
         // ------------------------------------------------------------------
         const int gid = lane >> 2, q = lane & 3;
         const int sw = warp & 7, par = warp >> 3;
-        const int64_t st = tt * 8 + sw;
-        const bool live = st < T;  // warp-uniform
         const int rA = 16 * sw + gid, rB = rA + 8;
         const uint32_t c28 = g.c28, c16 = g.c16;
         const uint32_t vmask = g.nested8 ? 0xFFF0u : 0xFFFFu;  // escape bits kept
-        uint32_t base2A = 0, base2B = 0;
-        EscBatch cur, nxt;
-        cur.cnt = nxt.cnt = 0;
-        cur.ent = nxt.ent = 0;
-        cur.p0 = nxt.p0 = 0;
-        const int32_t *gptr = t.esc_ptr + (live ? st : 0) * t.G;
         const int n_esc = (int)t.n_esc;
-        // group offsets: lane l holds the offset of group gw0 + l (one
-        // coalesced load per 31 groups, no dependent load inside the loop)
-        int gw0 = (int)g_beg;
-        const int gend = (int)g_end;
-        auto load_window = [&](int first) -> int {
-            const int gi = first + lane;
-            int v = 0;
-            if (live && gi <= gend) {
-                v = __ldg(gptr + gi);
-                v = v < 0 ? 0 : (v > n_esc ? n_esc : v);
-            }
-            return v;
-        };
-        int ptrw = load_window(gw0);
-        auto bounds = [&](int64_t gg64, int &p0, int &p1) {
-            const int gg = (int)gg64;
-            if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per chunk)
-                gw0 = gg;
-                ptrw = load_window(gw0);
-            }
-            p0 = __shfl_sync(kFull, ptrw, gg - gw0);
-            p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
-            if (p1 < p0) p1 = p0;
-        };
-        if (live && nkb > 0) {
-            const int64_t nA = st * 16 + gid, nB = nA + 8;
-            base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
-            base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
-            int p0, p1;
-            bounds(g_beg, p0, p1);
-            cur = load_group_escapes(t, p0, p1, lane);
-            if (g_beg + 1 < g_end) {
-                bounds(g_beg + 1, p0, p1);
-                nxt = load_group_escapes(t, p0, p1, lane);
-            }
-        }
-        uint32_t emask = (live && nkb > 0) ? escape_tiles(cur, lane) : 0u;
-        grid_dep_wait();  // Y and the workspace may belong to the previous kernel
-        bool ok = true;
-        RingPos wp, ap;  // ring positions of k-block kb
+        const int quarter = warp & 3, half = warp >> 2;  // epilogue: TMEM lanes 32*quarter..; half: 0 .. kDecWarps/4 - 1
+        const int chunks = Mp / 16;
+        RingPos wp, ap;   // ring positions of this warp's next k-block
         wp.advance(par, RW);
         ap.advance(par, RA);
-        for (int kb = par; kb < nkb && ok; kb += kPar, wp.advance(kPar, RW), ap.advance(kPar, RA)) {
-            const int p = kb & 3;  // tile of the group
-            if (kb >= 4 && p == par && live) {  // first tile of a new group for this warp
-                const int64_t gg = g_beg + (kb >> 2);
-                cur = nxt;
-                emask = escape_tiles(cur, lane);
-                if (gg + 1 < g_end) {
-                    int p0, p1;
-                    bounds(gg + 1, p0, p1);
+        int it = 0;  // items this CTA has done
+        for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+            int64_t tt, g_beg, g_end;
+            item_span(item, tt, g_beg, g_end);
+            const int nkb = (int)(4 * (g_end - g_beg));
+            const int64_t st = tt * 8 + sw;
+            const bool live = st < T;  // warp-uniform
+            uint32_t base2A = 0, base2B = 0;
+            EscBatch cur, nxt;
+            cur.cnt = nxt.cnt = 0;
+            cur.ent = nxt.ent = 0;
+            cur.p0 = nxt.p0 = 0;
+            const int32_t *gptr = t.esc_ptr + (live ? st : 0) * t.G;
+            // group offsets: lane l holds the offset of group gw0 + l (one
+            // coalesced load per 31 groups, no dependent load inside the loop)
+            int gw0 = (int)g_beg;
+            const int gend = (int)g_end;
+            auto load_window = [&](int first) -> int {
+                const int gi = first + lane;
+                int v = 0;
+                if (live && gi <= gend) {
+                    v = __ldg(gptr + gi);
+                    v = v < 0 ? 0 : (v > n_esc ? n_esc : v);
+                }
+                return v;
+            };
+            int ptrw = load_window(gw0);
+            auto bounds = [&](int64_t gg64, int &p0, int &p1) {
+                const int gg = (int)gg64;
+                if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per chunk)
+                    gw0 = gg;
+                    ptrw = load_window(gw0);
+                }
+                p0 = __shfl_sync(kFull, ptrw, gg - gw0);
+                p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
+                if (p1 < p0) p1 = p0;
+            };
+            if (live && nkb > 0) {
+                const int64_t nA = st * 16 + gid, nB = nA + 8;
+                base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
+                base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
+                int p0, p1;
+                bounds(g_beg, p0, p1);
+                cur = load_group_escapes(t, p0, p1, lane);
+                if (g_beg + 1 < g_end) {
+                    bounds(g_beg + 1, p0, p1);
                     nxt = load_group_escapes(t, p0, p1, lane);
                 }
             }
-            const int ws = wp.stage, as = ap.stage;
-            const uint32_t wph = wp.phase, aph = ap.phase;
-            // the whole warp leaves together, so no lane is left behind at a
-            // warp-wide instruction
-            if (!__all_sync(kFull, mbar_wait(&w_full[ws], wph, abort_flag, g.error))) {
-                ok = false;
-                break;
-            }
-            uint32_t dA[8], dB[8];
-            if (live) {
-                const uint8_t *W = w_st + ws * kWStageBytes;
-                const uint4 h0 = lds128(W + sw * 1024 + lane * 16), h1 = lds128(W + sw * 1024 + 512 + lane * 16);
-                // the nested 8-bit view reads no lo plane: records with zero low nibbles
-                const uint4 l = g.nested8 ? make_uint4(0u, 0u, 0u, 0u) : lds128(W + 8192 + sw * 512 + lane * 16);
-                decode16_fma(h0, l.x, l.y, base2A, c28, c16, dA);
-                decode16_fma(h1, l.z, l.w, base2B, c28, c16, dB);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&w_empty[ws]);  // the planes are in registers
-            if (!__all_sync(kFull, mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, g.error))) {
-                ok = false;
-                break;
-            }
-            if (live) {
-                uint8_t *A = a_st + as * kAStageBytes;
-                *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q)) = make_uint4(dA[0], dA[1], dA[2], dA[3]);
-                *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q + 1)) = make_uint4(dA[4], dA[5], dA[6], dA[7]);
-                *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q)) = make_uint4(dB[0], dB[1], dB[2], dB[3]);
-                *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q + 1)) = make_uint4(dB[4], dB[5], dB[6], dB[7]);
-                if ((emask >> p) & 1u) {  // escapes of this tile overwrite their slots
-                    __syncwarp();
-                    auto put = [&](uint32_t e) {
-                        const int key = (int)(e >> 16);
-                        const int r = 16 * sw + ((key >> 6) & 15), j = key & 63;
-                        *reinterpret_cast<uint16_t *>(A + swz(r, j >> 3) + (j & 7) * 2) = (uint16_t)(e & vmask);
-                    };
-                    if (cur.cnt <= 32) {
-                        if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
-                    } else {
-                        for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
-                            const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
-                            if (b0 + lane < cur.cnt && (int)(e >> 26) == p) put(e);
+            uint32_t emask = (live && nkb > 0) ? escape_tiles(cur, lane) : 0u;
+            // Y and the workspace may belong to the previous kernel (the
+            // first item's metadata above reads only the W12 tensor)
+            if (it == 0) grid_dep_wait();
+            bool ok = !*abort_flag;
+            for (int kb = par; kb < nkb && ok; kb += kPar, wp.advance(kPar, RW), ap.advance(kPar, RA)) {
+                const int p = kb & 3;  // tile of the group
+                if (kb >= 4 && p == par && live) {  // first tile of a new group for this warp
+                    const int64_t gg = g_beg + (kb >> 2);
+                    cur = nxt;
+                    emask = escape_tiles(cur, lane);
+                    if (gg + 1 < g_end) {
+                        int p0, p1;
+                        bounds(gg + 1, p0, p1);
+                        nxt = load_group_escapes(t, p0, p1, lane);
+                    }
+                }
+                const int ws = wp.stage, as = ap.stage;
+                const uint32_t wph = wp.phase, aph = ap.phase;
+                // the whole warp leaves together, so no lane is left behind at a
+                // warp-wide instruction
+                if (!__all_sync(kFull, mbar_wait(&w_full[ws], wph, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                uint32_t dA[8], dB[8];
+                if (live) {
+                    const uint8_t *W = w_st + ws * kWStageBytes;
+                    const uint4 h0 = lds128(W + sw * 1024 + lane * 16), h1 = lds128(W + sw * 1024 + 512 + lane * 16);
+                    // the nested 8-bit view reads no lo plane: records with zero low nibbles
+                    const uint4 l = g.nested8 ? make_uint4(0u, 0u, 0u, 0u) : lds128(W + 8192 + sw * 512 + lane * 16);
+                    decode16_fma(h0, l.x, l.y, base2A, c28, c16, dA);
+                    decode16_fma(h1, l.z, l.w, base2B, c28, c16, dB);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[ws]);  // the planes are in registers
+                if (!__all_sync(kFull, mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                if (live) {
+                    uint8_t *A = a_st + as * kAStageBytes;
+                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q)) = make_uint4(dA[0], dA[1], dA[2], dA[3]);
+                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q + 1)) = make_uint4(dA[4], dA[5], dA[6], dA[7]);
+                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q)) = make_uint4(dB[0], dB[1], dB[2], dB[3]);
+                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q + 1)) = make_uint4(dB[4], dB[5], dB[6], dB[7]);
+                    if ((emask >> p) & 1u) {  // escapes of this tile overwrite their slots
+                        __syncwarp();
+                        auto put = [&](uint32_t e) {
+                            const int key = (int)(e >> 16);
+                            const int r = 16 * sw + ((key >> 6) & 15), j = key & 63;
+                            *reinterpret_cast<uint16_t *>(A + swz(r, j >> 3) + (j & 7) * 2) = (uint16_t)(e & vmask);
+                        };
+                        if (cur.cnt <= 32) {
+                            if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
+                        } else {
+                            for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
+                                const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
+                                if (b0 + lane < cur.cnt && (int)(e >> 26) == p) put(e);
+                            }
                         }
                     }
                 }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[as]);
             }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[as]);
-        }
 
-        // ------------------------------------------------------------------
-        // Epilogue: TMEM lanes 32*(warp%4).. ; the warps w, w+4, ... (two or
-        // four of them) split the 16-column chunks.
-        // ------------------------------------------------------------------
-        // every MMA issued has completed (also after an abort: TMEM is freed below)
-        const bool fin = __all_sync(kFull, mbar_drain(done, 0, g.error));
-        tc_fence_after();
-        const int quarter = warp & 3, half = warp >> 2;  // half: 0 .. kDecWarps/4 - 1
-        const int64_t n = tt * 128 + 32 * quarter + lane;
-        const int chunks = Mp / 16;
-        const bool have = __all_sync(kFull, fin && ok && !*abort_flag);
-        if (have) {
-            for (int c = half; c < chunks; c += kDecWarps / 4) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(16 * c), v);
-                if (nkb == 0) {
+            // --------------------------------------------------------------
+            // Epilogue: TMEM lanes 32*(warp%4).. ; the warps w, w+4, ... (two
+            // or four of them) split the 16-column chunks.
+            // --------------------------------------------------------------
+            // every MMA of the item has completed (a wait that gives up on an
+            // abort: the MMA warp then no longer keeps pace with the items,
+            // and it waits for its own MMAs before the CTA exits)
+            const bool mma_done = __all_sync(kFull, mbar_wait(done, (uint32_t)(it & 1), abort_flag, g.error));
+            tc_fence_after();
+            const int64_t n = tt * 128 + 32 * quarter + lane;
+            const int s = item - (int)tt * S;
+            const bool have = __all_sync(kFull, mma_done && ok && !*abort_flag);
+            if (have) {
+                for (int c = half; c < chunks; c += kDecWarps / 4) {
+                    float v[16];
+                    tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(16 * c), v);
+                    if (S == 1) {
+                        if (n < t.N) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                }
-                if (S == 1) {
-                    if (n < t.N) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = 16 * c + j;
-                            if (m < g.M) g.Y[(int64_t)m * g.ldy + n] = f32_to_bf16_rn(v[j]);
+                            for (int j = 0; j < 16; ++j) {
+                                const int m = 16 * c + j;
+                                if (m < g.M) g.Y[(int64_t)m * g.ldy + n] = f32_to_bf16_rn(v[j]);
+                            }
                         }
-                    }
-                } else if (n < t.Np) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        g.partials[((int64_t)s * Mp + 16 * c + j) * t.Np + n] = v[j];
-                }
-            }
-        }
-        if (S > 1) {
-            // fixed-order combination by the last CTA of this row tile
-            __threadfence();
-            asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
-            if (threadIdx.x == 0) *last_flag = have ? (atomicAdd(&g.counters[tt], 1) == S - 1) : 0;
-            asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
-            if (*last_flag) {
-                __threadfence();
-                if (n < t.N) {
-                    auto part = [&](int ss, int c, int j) {
-                        return __ldcg(g.partials + ((int64_t)ss * Mp + 16 * c + j) * t.Np + n);
-                    };
-                    for (int c = half; c < chunks; c += kDecWarps / 4) {
-                        // summed in the order s = 0..S-1; the loads of four
-                        // chunks at a time are in flight together
-                        float acc[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[j] = part(0, c, j);
-                        int ss = 1;
-                        for (; ss + 3 < S; ss += 4) {
-                            float v[4][16];
-#pragma unroll
-                            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) v[b][j] = part(ss + b, c, j);
-#pragma unroll
-                            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) acc[j] += v[b][j];
-                        }
-                        for (; ss < S; ++ss) {
-                            float v[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) v[j] = part(ss, c, j);
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) acc[j] += v[j];
-                        }
+                    } else if (n < t.Np) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (16 * c + j < g.M) g.Y[(int64_t)(16 * c + j) * g.ldy + n] = f32_to_bf16_rn(acc[j]);
+                            g.partials[((int64_t)s * Mp + 16 * c + j) * t.Np + n] = v[j];
                     }
                 }
-                if (threadIdx.x == 0) g.counters[tt] = 0;
+            }
+            // every decoder warp is done reading the accumulator before any of
+            // them hands the MMA warp a tile of the next item
+            tc_fence_before();
+            if (S > 1) __threadfence();
+            asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+            if (S > 1) {
+                // fixed-order combination by the last CTA of this row tile
+                if (threadIdx.x == 0) *last_flag = have ? (atomicAdd(&g.counters[tt], 1) == S - 1) : 0;
+                asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+                if (*last_flag) {
+                    __threadfence();
+                    if (n < t.N) {
+                        auto part = [&](int ss, int c, int j) {
+                            return __ldcg(g.partials + ((int64_t)ss * Mp + 16 * c + j) * t.Np + n);
+                        };
+                        for (int c = half; c < chunks; c += kDecWarps / 4) {
+                            // summed in the order s = 0..S-1; the loads of four
+                            // chunks at a time are in flight together
+                            float acc[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] = part(0, c, j);
+                            int ss = 1;
+                            for (; ss + 3 < S; ss += 4) {
+                                float v[4][16];
+#pragma unroll
+                                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) v[b][j] = part(ss + b, c, j);
+#pragma unroll
+                                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) acc[j] += v[b][j];
+                            }
+                            for (; ss < S; ++ss) {
+                                float v[16];
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[j] = part(ss, c, j);
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) acc[j] += v[j];
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (16 * c + j < g.M) g.Y[(int64_t)(16 * c + j) * g.ldy + n] = f32_to_bf16_rn(acc[j]);
+                        }
+                    }
+                    if (threadIdx.x == 0) g.counters[tt] = 0;
+                }
+                // (thread 0 writes last_flag again only after the next item's
+                // first barrier, which every decoder warp reaches after
+                // reading it here)
             }
         }
     } else if (warp == kWProdWarp) {
         // ------------------------------------------------------------------
         // Weight planes: one k-block (8 tiles of 1.5 KB) per stage, with
-        // tiled copies, up to RW k-blocks ahead of the decoders.  Reads
-        // only the W12 tensor, so it starts before the previous kernel ends.
+        // tiled copies, up to RW k-blocks ahead of the decoders, item after
+        // item.  Reads only the W12 tensor, so it starts before the previous
+        // kernel ends.
         // ------------------------------------------------------------------
         // The whole warp runs the loop (warp-uniform values stay in uniform
         // registers); one elected lane issues.
         int issued = 0;
+        bool ok = true;
         RingPos wp;
-        for (int kb = 0; kb < nkb; ++kb, wp.advance(1, RW)) {
-            const int ws = wp.stage;
-            if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) break;
-            if (elect_one()) {
-                // the full box is counted, out-of-range stripes included (zero-filled)
-                mbar_expect_tx(&w_full[ws], g.nested8 ? 8192u : kWStageBytes);
-                uint8_t *dst = w_st + ws * kWStageBytes;
-                const int kbg = (int)(4 * g_beg) + kb, st0 = (int)(tt * 8);
-                tma_load_4d(dst, &hmap, kbg, st0, &w_full[ws]);
-                if (!g.nested8) tma_load_4d(dst + 8192, &lmap, kbg, st0, &w_full[ws]);
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            int64_t tt, g_beg, g_end;
+            item_span(item, tt, g_beg, g_end);
+            const int nkb = (int)(4 * (g_end - g_beg));
+            for (int kb = 0; kb < nkb; ++kb, wp.advance(1, RW)) {
+                const int ws = wp.stage;
+                if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
+                    // the full box is counted, out-of-range stripes included (zero-filled)
+                    mbar_expect_tx(&w_full[ws], g.nested8 ? 8192u : kWStageBytes);
+                    uint8_t *dst = w_st + ws * kWStageBytes;
+                    const int kbg = (int)(4 * g_beg) + kb, st0 = (int)(tt * 8);
+                    tma_load_4d(dst, &hmap, kbg, st0, &w_full[ws]);
+                    if (!g.nested8) tma_load_4d(dst + 8192, &lmap, kbg, st0, &w_full[ws]);
+                }
+                __syncwarp();
+                ++issued;
             }
-            __syncwarp();
-            ++issued;
         }
         // the copies issued last must have landed before the CTA exits
         for (int i = issued > RW ? issued - RW : 0; i < issued; ++i)
@@ -551,46 +594,72 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
         // ------------------------------------------------------------------
         grid_dep_wait();  // A may be written by the previous kernel
         int issued = 0;
+        bool ok = true;
         RingPos bp;
-        for (int kb = 0; kb < nkb; ++kb, bp.advance(1, RB)) {
-            const int stage = bp.stage;
-            if (!__all_sync(kFull, mbar_wait(&b_empty[stage], bp.phase ^ 1u, abort_flag, g.error))) break;
-            if (elect_one()) {
-                mbar_expect_tx(&b_full[stage], b_stage_bytes);
-                tma_load_2d(b_st + stage * b_stage_bytes, &tmap, (int)((4 * g_beg + kb) * 64), 0, &b_full[stage]);
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            int64_t tt, g_beg, g_end;
+            item_span(item, tt, g_beg, g_end);
+            const int nkb = (int)(4 * (g_end - g_beg));
+            for (int kb = 0; kb < nkb; ++kb, bp.advance(1, RB)) {
+                const int stage = bp.stage;
+                if (!__all_sync(kFull, mbar_wait(&b_empty[stage], bp.phase ^ 1u, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
+                    mbar_expect_tx(&b_full[stage], b_stage_bytes);
+                    tma_load_2d(b_st + stage * b_stage_bytes, &tmap, (int)((4 * g_beg + kb) * 64), 0,
+                                &b_full[stage]);
+                }
+                __syncwarp();
+                ++issued;
             }
-            __syncwarp();
-            ++issued;
         }
         // the copies issued last must have landed before the CTA exits
         for (int i = issued > RB ? issued - RB : 0; i < issued; ++i)
             mbar_drain(&b_full[i % RB], (uint32_t)((i / RB) & 1), g.error);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------
-        // MMA issue (one thread).
+        // MMA issue.  After each item's MMAs (or, after an abort, none) a
+        // commit completes that item's phase of `done`, so the decoders'
+        // epilogue never waits longer than the MMAs already issued.
         // ------------------------------------------------------------------
         // The whole warp runs the loop; one elected lane issues the MMAs.
         if (g.test_stall)  // a wait that nothing completes: it runs out and aborts the CTA
-            (void)__all_sync(kFull, mbar_wait(done, 0, abort_flag, g.error));
+            (void)__all_sync(kFull, mbar_wait(fin, 0, abort_flag, g.error));
         RingPos ap, bp;
-        for (int kb = 0; kb < nkb; ++kb, ap.advance(1, RA), bp.advance(1, RB)) {
-            const int as = ap.stage, bs = bp.stage;
-            if (!__all_sync(kFull, mbar_wait(&a_full[as], ap.phase, abort_flag, g.error))) break;
-            if (!__all_sync(kFull, mbar_wait(&b_full[bs], bp.phase, abort_flag, g.error))) break;
-            tc_fence_after();
-            const uint32_t a0 = smem_addr(a_st + as * kAStageBytes);
-            const uint32_t b0 = smem_addr(b_st + bs * b_stage_bytes);
-            if (elect_one()) {
+        bool ok = true;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            int64_t tt, g_beg, g_end;
+            item_span(item, tt, g_beg, g_end);
+            const int nkb = (int)(4 * (g_end - g_beg));
+            for (int kb = 0; kb < nkb && ok; ++kb, ap.advance(1, RA), bp.advance(1, RB)) {
+                const int as = ap.stage, bs = bp.stage;
+                if (!__all_sync(kFull, mbar_wait(&a_full[as], ap.phase, abort_flag, g.error)) ||
+                    !__all_sync(kFull, mbar_wait(&b_full[bs], bp.phase, abort_flag, g.error))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_addr(a_st + as * kAStageBytes);
+                const uint32_t b0 = smem_addr(b_st + bs * b_stage_bytes);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma(tmem, smem_desc(a0 + 32 * kk), smem_desc(b0 + 32 * kk), tp.idesc, (kb | kk) != 0);
-                umma_commit(&a_empty[as]);
-                umma_commit(&b_empty[bs]);
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma(tmem, smem_desc(a0 + 32 * kk), smem_desc(b0 + 32 * kk), tp.idesc, (kb | kk) != 0);
+                    umma_commit(&a_empty[as]);
+                    umma_commit(&b_empty[bs]);
+                }
+                __syncwarp();
             }
+            if (elect_one()) umma_commit(done);  // arrives once every MMA issued above has completed
             __syncwarp();
         }
-        if (elect_one()) umma_commit(done);  // arrives once every MMA issued above has completed
+        // TMEM and the shared-memory operands stay allocated until every MMA
+        // issued has completed (after an abort the decoders stop waiting)
+        if (elect_one()) umma_commit(fin);
         __syncwarp();
+        (void)__all_sync(kFull, mbar_drain(fin, 0, g.error));
     }
 
     tc_fence_before();
@@ -603,16 +672,20 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
 }
 
 // Balanced range cut (used for Mpad > 128 on large layers, one CTA per SM):
-// the units u = row_tile*G + group are cut into one contiguous range per
-// CTA (range_begin), so every SM streams the same number of units whatever
-// the row-tile count.  A range is walked piece by piece (the part of it
-// inside one row tile).  Piece j accumulates in TMEM buffer j & 1; its
-// epilogue is deferred until piece j + 2 needs the buffer (for most ranges,
-// to the end), so the decoders go straight on to the next row tile, whose
-// bases and group offsets they fetch during the last group of the current
-// one.  A piece that covers its whole row tile is rounded and stored; the
-// range's first and last pieces otherwise go to FP32 slots v and v + V, and
-// the last CTA to arrive at a row tile sums its pieces in range order.
+// the units u = row_tile*G + group are cut into V contiguous ranges
+// (range_begin), one per SM-sized share, so every SM streams the same number
+// of units whatever the row-tile count.  A CTA takes ranges blockIdx.x,
+// blockIdx.x + gridDim.x, ... (one with the default grid of V CTAs).  A range
+// is walked piece by piece (the part of it inside one row tile).  The CTA's
+// pieces, counted over all its ranges, alternate between two TMEM
+// accumulator buffers; a piece's epilogue is deferred until the piece two
+// later needs its buffer (for most ranges, to the range's end), so the
+// decoders go straight on to the next row tile, whose bases and group offsets
+// they fetch during the last group of the current one.  A piece that covers
+// its whole row tile is rounded and stored; the range's first and last
+// pieces otherwise go to FP32 slots v and v + V, and the last CTA to arrive
+// at a row tile sums its pieces in range order.  The ranges and the order of
+// every sum depend on (M, N, K) only, never on the grid.
 template <int D>
 __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_gemm_tc_ranges(
     TensorView t, GemmArgs g, TcParams tp, const __grid_constant__ CUtensorMap tmap,
@@ -636,34 +709,41 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
     uint64_t *b_full = a_empty + RA;
     uint64_t *b_empty = b_full + RB;
     uint64_t *done = b_empty + RB;  // [2]: per accumulator buffer, one phase per piece using it
-    uint64_t *fin = done + 2;        // every MMA this CTA issued has completed
+    uint64_t *fin = done + 2;        // the MMA warp's own last wait: every MMA it issued has completed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *arr_tt = abort_flag + 1;    // [2] row tiles of this range's partial first / last piece
     volatile int *arr_last = arr_tt + 2;      // [2] this CTA delivered the row tile's last piece
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // This CTA's range of units u = row_tile*G + group; a piece is the part of
-    // the range inside one row tile.
+    // Ranges of units u = row_tile*G + group; a piece is the part of a range
+    // inside one row tile.
     const int G = (int)t.G;
-    const int v = blockIdx.x;
     const int V = (int)g.ranges;
-    const int u0 = range_begin(v, g), u1 = range_begin(v + 1, g);
     const int64_t T = t.Np / 16;  // stripes
-    const int tt0 = u0 / G, ga0 = u0 - tt0 * G;
-    const int npieces = (u1 - 1) / G - tt0 + 1;
-    // piece jj: row tile tt0 + jj, groups [ga, gb) of it, accumulated in TMEM
-    // buffer jj & 1 (columns (jj & 1) * acc_cols ..)
-    auto piece = [&](int jj, int &tt, int &ga, int &gb) {
-        tt = tt0 + jj;
-        ga = jj == 0 ? ga0 : 0;
-        const int e = u1 - tt * G;
+    // piece jj of range v: row tile tt0 + jj, groups [ga, gb) of it
+    struct Range {
+        int u0, u1, tt0, ga0, npieces;
+    };
+    auto range_at = [&](int v) -> Range {
+        Range rg;
+        rg.u0 = range_begin(v, g);
+        rg.u1 = range_begin(v + 1, g);
+        rg.tt0 = rg.u0 / G;
+        rg.ga0 = rg.u0 - rg.tt0 * G;
+        rg.npieces = rg.u1 > rg.u0 ? (rg.u1 - 1) / G - rg.tt0 + 1 : 0;
+        return rg;
+    };
+    auto piece = [&](const Range &rg, int jj, int &tt, int &ga, int &gb) {
+        tt = rg.tt0 + jj;
+        ga = jj == 0 ? rg.ga0 : 0;
+        const int e = rg.u1 - tt * G;
         gb = e < G ? e : G;
     };
     const uint32_t acc_cols = tp.tmem_cols / 2;
 
     // the descriptors of the first copies load while the barriers are set up
-    if (u1 > u0 && lane == 0) {
+    if (lane == 0) {
         if (warp == kWProdWarp) {
             prefetch_tmap(&hmap);
             if (!g.nested8) prefetch_tmap(&lmap);
@@ -711,7 +791,8 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
         // the k-blocks of parity w/8 (16 warps: tiles p = w/8 and w/8 + 2 of
         // every group): the tile's planes come from the weight ring, the BF16
         // tile goes to the A ring (K-major, 128-byte swizzle), escapes over
-        // their slots.  Then the piece's epilogue.
+        // their slots.  Then the piece's epilogue.  Every decoder warp runs
+        // every range, piece and named barrier, also after an abort.
         // ------------------------------------------------------------------
         const int gid = lane >> 2, q = lane & 3;
         const int sw = warp & 7, par = warp >> 3;
@@ -722,233 +803,255 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
         const int quarter = warp & 3, half = warp >> 2;  // TMEM lanes 32*quarter..; half: 0 .. kDecWarps/4 - 1
         const int r = 32 * quarter + lane;               // epilogue row within the row tile
         const int chunks = Mp / 16;
-        bool ok = true;
-
-        // Piece epilogue (after its MMAs completed).  A piece covering its
-        // whole row tile is rounded and stored; any other piece goes to FP32
-        // slot v (the range's first piece) or v + V (its last), and the row
-        // tile's arrival count goes up.  Every decoder warp runs the same
-        // barriers whether or not the CTA has aborted.
-        auto epilogue = [&](int jj) {
-            int tt, ga, gb;
-            piece(jj, tt, ga, gb);
-            if (ok && !__all_sync(kFull, mbar_wait(&done[jj & 1], (uint32_t)((jj >> 1) & 1), abort_flag, g.error)))
-                ok = false;
-            tc_fence_after();
-            const bool whole = ga == 0 && gb == G;
-            const int64_t slot = jj == 0 ? v : (int64_t)v + V;
-            const int64_t n = (int64_t)tt * 128 + r;
-            if (ok) {
-                const uint32_t acc = tmem + (uint32_t)(jj & 1) * acc_cols + ((uint32_t)(32 * quarter) << 16);
-                for (int c = half; c < chunks; c += kDecWarps / 4) {
-                    float x[16];
-                    tmem_ld16(acc + (uint32_t)(16 * c), x);
-                    if (whole) {
-                        if (n < t.N) {
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                const int m = 16 * c + k;
-                                if (m < g.M) g.Y[(int64_t)m * g.ldy + n] = f32_to_bf16_rn(x[k]);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) g.partials[(slot * Mp + 16 * c + k) * 128 + r] = x[k];
-                    }
-                }
-                if (!whole) __threadfence();
-            }
-            // every TMEM read of this buffer is done before any decoder warp
-            // hands the MMA warp a tile of the piece that reuses it
-            tc_fence_before();
-            asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
-            if (!whole && threadIdx.x == 0 && !*abort_flag) {
-                const int k = jj == 0 ? 0 : 1;
-                const int va = range_of(tt * G, g), vb = range_of(tt * G + G - 1, g);
-                arr_tt[k] = tt;
-                arr_last[k] = atomicAdd(&g.counters[tt], 1) == vb - va;
-            }
-        };
-
-        // Per-piece state read from memory: row bases and the group offsets
-        // (lane l holds the offset of group gw0 + l: one coalesced load per 31
-        // groups, no dependent load inside the loop).  The next piece's is
-        // fetched during the current piece's last group.
-        struct PieceMeta {
-            uint32_t base2A, base2B;
-            int ptrw;
-        };
-        auto load_window = [&](const int32_t *gptr, bool live, int first, int gb) -> int {
-            const int gi = first + lane;
-            int x = 0;
-            if (live && gi <= gb) {
-                x = __ldg(gptr + gi);
-                x = x < 0 ? 0 : (x > n_esc ? n_esc : x);
-            }
-            return x;
-        };
-        auto fetch_meta = [&](int jj) -> PieceMeta {
-            int tt, ga, gb;
-            piece(jj, tt, ga, gb);
-            const int64_t st = (int64_t)tt * 8 + sw;
-            const bool live = st < T;
-            PieceMeta pm;
-            pm.base2A = pm.base2B = 0;
-            if (live) {
-                const int64_t nA = st * 16 + gid, nB = nA + 8;
-                pm.base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
-                pm.base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
-            }
-            pm.ptrw = load_window(t.esc_ptr + (live ? st : 0) * t.G, live, ga, gb);
-            return pm;
-        };
 
         RingPos wp, ap;  // ring positions of this warp's next k-block
         wp.advance(par, RW);
         ap.advance(par, RA);
-        PieceMeta meta = fetch_meta(0);
-        for (int j = 0; j < npieces; ++j) {
-            int tt, ga, gb;
-            piece(j, tt, ga, gb);
-            const int nkb = 4 * (gb - ga);
-            const int64_t st = (int64_t)tt * 8 + sw;
-            const bool live = st < T;  // warp-uniform
-            const uint32_t base2A = meta.base2A, base2B = meta.base2B;
-            const int32_t *gptr = t.esc_ptr + (live ? st : 0) * t.G;
-            int gw0 = ga, ptrw = meta.ptrw;
-            auto bounds = [&](int gg, int &p0, int &p1) {
-                if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per piece)
-                    gw0 = gg;
-                    ptrw = load_window(gptr, live, gw0, gb);
+        int it = 0;   // ranges this CTA has done
+        int jb = 0;   // pieces this CTA has done in earlier ranges
+        for (int v = blockIdx.x; v < V; v += gridDim.x, ++it) {
+            const Range rg = range_at(v);
+            const int npieces = rg.npieces;
+            bool ok = !*abort_flag;
+
+            // Piece epilogue (after its MMAs completed).  A piece covering its
+            // whole row tile is rounded and stored; any other piece goes to
+            // FP32 slot v (the range's first piece) or v + V (its last), and
+            // the row tile's arrival count goes up.  Every decoder warp runs
+            // the same barriers whether or not the CTA has aborted.
+            auto epilogue = [&](int jj) {
+                int tt, ga, gb;
+                piece(rg, jj, tt, ga, gb);
+                const int J = jb + jj;  // the piece's number in this CTA: buffer J & 1
+                if (ok && !__all_sync(kFull, mbar_wait(&done[J & 1], (uint32_t)((J >> 1) & 1), abort_flag, g.error)))
+                    ok = false;
+                tc_fence_after();
+                const bool whole = ga == 0 && gb == G;
+                const int64_t slot = jj == 0 ? v : (int64_t)v + V;
+                const int64_t n = (int64_t)tt * 128 + r;
+                if (ok) {
+                    const uint32_t acc = tmem + (uint32_t)(J & 1) * acc_cols + ((uint32_t)(32 * quarter) << 16);
+                    for (int c = half; c < chunks; c += kDecWarps / 4) {
+                        float x[16];
+                        tmem_ld16(acc + (uint32_t)(16 * c), x);
+                        if (whole) {
+                            if (n < t.N) {
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) {
+                                    const int m = 16 * c + k;
+                                    if (m < g.M) g.Y[(int64_t)m * g.ldy + n] = f32_to_bf16_rn(x[k]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) g.partials[(slot * Mp + 16 * c + k) * 128 + r] = x[k];
+                        }
+                    }
+                    if (!whole) __threadfence();
                 }
-                p0 = __shfl_sync(kFull, ptrw, gg - gw0);
-                p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
-                if (p1 < p0) p1 = p0;
+                // every TMEM read of this buffer is done before any decoder warp
+                // hands the MMA warp a tile of the piece that reuses it
+                tc_fence_before();
+                asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+                if (!whole && threadIdx.x == 0 && !*abort_flag) {
+                    const int k = jj == 0 ? 0 : 1;
+                    const int va = range_of(tt * G, g), vb = range_of(tt * G + G - 1, g);
+                    arr_tt[k] = tt;
+                    arr_last[k] = atomicAdd(&g.counters[tt], 1) == vb - va;
+                }
             };
-            EscBatch cur, nxt;
-            cur.cnt = nxt.cnt = 0;
-            cur.ent = nxt.ent = 0;
-            cur.p0 = nxt.p0 = 0;
-            if (live) {
-                int p0, p1;
-                bounds(ga, p0, p1);
-                cur = load_group_escapes(t, p0, p1, lane);
-                if (ga + 1 < gb) {
-                    bounds(ga + 1, p0, p1);
-                    nxt = load_group_escapes(t, p0, p1, lane);
+
+            // Per-piece state read from memory: row bases and the group offsets
+            // (lane l holds the offset of group gw0 + l: one coalesced load per 31
+            // groups, no dependent load inside the loop).  The next piece's is
+            // fetched during the current piece's last group.
+            struct PieceMeta {
+                uint32_t base2A, base2B;
+                int ptrw;
+            };
+            auto load_window = [&](const int32_t *gptr, bool live, int first, int gb) -> int {
+                const int gi = first + lane;
+                int x = 0;
+                if (live && gi <= gb) {
+                    x = __ldg(gptr + gi);
+                    x = x < 0 ? 0 : (x > n_esc ? n_esc : x);
                 }
-            }
-            uint32_t emask = live ? escape_tiles(cur, lane) : 0u;
-            if (j == 0) grid_dep_wait();  // Y and the workspace may belong to the previous kernel
-            if (j >= 2) epilogue(j - 2);  // frees the accumulator buffer this piece uses
-            const int last_g = gb - ga - 1;
-            // Each piece holds a multiple of 4 k-blocks, so this warp's k-blocks of
-            // the piece start at parity `par` and its ring positions carry over.
-            for (int kb = par; kb < nkb && ok; kb += kPar, wp.advance(kPar, RW), ap.advance(kPar, RA)) {
-                const int p = kb & 3;  // tile of the group
-                if (kb >= 4 && p == par && live) {  // first tile of a new group for this warp
-                    const int gg = ga + (kb >> 2);
-                    cur = nxt;
-                    emask = escape_tiles(cur, lane);
-                    if (gg + 1 < gb) {
-                        int p0, p1;
-                        bounds(gg + 1, p0, p1);
+                return x;
+            };
+            auto fetch_meta = [&](int jj) -> PieceMeta {
+                int tt, ga, gb;
+                piece(rg, jj, tt, ga, gb);
+                const int64_t st = (int64_t)tt * 8 + sw;
+                const bool live = st < T;
+                PieceMeta pm;
+                pm.base2A = pm.base2B = 0;
+                if (live) {
+                    const int64_t nA = st * 16 + gid, nB = nA + 8;
+                    pm.base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
+                    pm.base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
+                }
+                pm.ptrw = load_window(t.esc_ptr + (live ? st : 0) * t.G, live, ga, gb);
+                return pm;
+            };
+
+            PieceMeta meta = fetch_meta(0);
+            for (int j = 0; j < npieces; ++j) {
+                int tt, ga, gb;
+                piece(rg, j, tt, ga, gb);
+                const int nkb = 4 * (gb - ga);
+                const int64_t st = (int64_t)tt * 8 + sw;
+                const bool live = st < T;  // warp-uniform
+                const uint32_t base2A = meta.base2A, base2B = meta.base2B;
+                const int32_t *gptr = t.esc_ptr + (live ? st : 0) * t.G;
+                int gw0 = ga, ptrw = meta.ptrw;
+                auto bounds = [&](int gg, int &p0, int &p1) {
+                    if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per piece)
+                        gw0 = gg;
+                        ptrw = load_window(gptr, live, gw0, gb);
+                    }
+                    p0 = __shfl_sync(kFull, ptrw, gg - gw0);
+                    p1 = __shfl_sync(kFull, ptrw, gg + 1 - gw0);
+                    if (p1 < p0) p1 = p0;
+                };
+                EscBatch cur, nxt;
+                cur.cnt = nxt.cnt = 0;
+                cur.ent = nxt.ent = 0;
+                cur.p0 = nxt.p0 = 0;
+                if (live) {
+                    int p0, p1;
+                    bounds(ga, p0, p1);
+                    cur = load_group_escapes(t, p0, p1, lane);
+                    if (ga + 1 < gb) {
+                        bounds(ga + 1, p0, p1);
                         nxt = load_group_escapes(t, p0, p1, lane);
                     }
                 }
-                if ((kb >> 2) == last_g && p == par && j + 1 < npieces) meta = fetch_meta(j + 1);
-                const int ws = wp.stage, as = ap.stage;
-                const uint32_t wph = wp.phase, aph = ap.phase;
-                // the whole warp leaves together, so no lane is left behind at a
-                // warp-wide instruction
-                if (!__all_sync(kFull, mbar_wait(&w_full[ws], wph, abort_flag, g.error))) {
-                    ok = false;
-                    break;
-                }
-                uint32_t dA[8], dB[8];
-                if (live) {
-                    const uint8_t *W = w_st + ws * kWStageBytes;
-                    const uint4 h0 = lds128(W + sw * 1024 + lane * 16), h1 = lds128(W + sw * 1024 + 512 + lane * 16);
-                    // the nested 8-bit view reads no lo plane: records with zero low nibbles
-                    const uint4 l = g.nested8 ? make_uint4(0u, 0u, 0u, 0u) : lds128(W + 8192 + sw * 512 + lane * 16);
-                    decode16_fma(h0, l.x, l.y, base2A, c28, c16, dA);
-                    decode16_fma(h1, l.z, l.w, base2B, c28, c16, dB);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&w_empty[ws]);  // the planes are in registers
-                if (!__all_sync(kFull, mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, g.error))) {
-                    ok = false;
-                    break;
-                }
-                if (live) {
-                    uint8_t *A = a_st + as * kAStageBytes;
-                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q)) = make_uint4(dA[0], dA[1], dA[2], dA[3]);
-                    *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q + 1)) = make_uint4(dA[4], dA[5], dA[6], dA[7]);
-                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q)) = make_uint4(dB[0], dB[1], dB[2], dB[3]);
-                    *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q + 1)) = make_uint4(dB[4], dB[5], dB[6], dB[7]);
-                    if ((emask >> p) & 1u) {  // escapes of this tile overwrite their slots
-                        __syncwarp();
-                        auto put = [&](uint32_t e) {
-                            const int key = (int)(e >> 16);
-                            const int rr = 16 * sw + ((key >> 6) & 15), jj = key & 63;
-                            *reinterpret_cast<uint16_t *>(A + swz(rr, jj >> 3) + (jj & 7) * 2) = (uint16_t)(e & vmask);
-                        };
-                        if (cur.cnt <= 32) {
-                            if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
-                        } else {
-                            for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
-                                const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
-                                if (b0 + lane < cur.cnt && (int)(e >> 26) == p) put(e);
+                uint32_t emask = live ? escape_tiles(cur, lane) : 0u;
+                // Y and the workspace may belong to the previous kernel (the
+                // first piece's metadata above reads only the W12 tensor)
+                if (it == 0 && j == 0) grid_dep_wait();
+                if (j >= 2) epilogue(j - 2);  // frees the accumulator buffer this piece uses
+                const int last_g = gb - ga - 1;
+                // Each piece holds a multiple of 4 k-blocks, so this warp's k-blocks of
+                // the piece start at parity `par` and its ring positions carry over.
+                for (int kb = par; kb < nkb && ok; kb += kPar, wp.advance(kPar, RW), ap.advance(kPar, RA)) {
+                    const int p = kb & 3;  // tile of the group
+                    if (kb >= 4 && p == par && live) {  // first tile of a new group for this warp
+                        const int gg = ga + (kb >> 2);
+                        cur = nxt;
+                        emask = escape_tiles(cur, lane);
+                        if (gg + 1 < gb) {
+                            int p0, p1;
+                            bounds(gg + 1, p0, p1);
+                            nxt = load_group_escapes(t, p0, p1, lane);
+                        }
+                    }
+                    if ((kb >> 2) == last_g && p == par && j + 1 < npieces) meta = fetch_meta(j + 1);
+                    const int ws = wp.stage, as = ap.stage;
+                    const uint32_t wph = wp.phase, aph = ap.phase;
+                    // the whole warp leaves together, so no lane is left behind at a
+                    // warp-wide instruction
+                    if (!__all_sync(kFull, mbar_wait(&w_full[ws], wph, abort_flag, g.error))) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t dA[8], dB[8];
+                    if (live) {
+                        const uint8_t *W = w_st + ws * kWStageBytes;
+                        const uint4 h0 = lds128(W + sw * 1024 + lane * 16),
+                                    h1 = lds128(W + sw * 1024 + 512 + lane * 16);
+                        // the nested 8-bit view reads no lo plane: records with zero low nibbles
+                        const uint4 l =
+                            g.nested8 ? make_uint4(0u, 0u, 0u, 0u) : lds128(W + 8192 + sw * 512 + lane * 16);
+                        decode16_fma(h0, l.x, l.y, base2A, c28, c16, dA);
+                        decode16_fma(h1, l.z, l.w, base2B, c28, c16, dB);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&w_empty[ws]);  // the planes are in registers
+                    if (!__all_sync(kFull, mbar_wait(&a_empty[as], aph ^ 1u, abort_flag, g.error))) {
+                        ok = false;
+                        break;
+                    }
+                    if (live) {
+                        uint8_t *A = a_st + as * kAStageBytes;
+                        *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q)) = make_uint4(dA[0], dA[1], dA[2], dA[3]);
+                        *reinterpret_cast<uint4 *>(A + swz(rA, 2 * q + 1)) = make_uint4(dA[4], dA[5], dA[6], dA[7]);
+                        *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q)) = make_uint4(dB[0], dB[1], dB[2], dB[3]);
+                        *reinterpret_cast<uint4 *>(A + swz(rB, 2 * q + 1)) = make_uint4(dB[4], dB[5], dB[6], dB[7]);
+                        if ((emask >> p) & 1u) {  // escapes of this tile overwrite their slots
+                            __syncwarp();
+                            auto put = [&](uint32_t e) {
+                                const int key = (int)(e >> 16);
+                                const int rr = 16 * sw + ((key >> 6) & 15), jj = key & 63;
+                                *reinterpret_cast<uint16_t *>(A + swz(rr, jj >> 3) + (jj & 7) * 2) =
+                                    (uint16_t)(e & vmask);
+                            };
+                            if (cur.cnt <= 32) {
+                                if (lane < cur.cnt && (int)(cur.ent >> 26) == p) put(cur.ent);
+                            } else {
+                                for (int b0 = 0; b0 < cur.cnt; b0 += 32) {
+                                    const uint32_t e = (b0 + lane < cur.cnt) ? __ldg(t.esc + cur.p0 + b0 + lane) : 0u;
+                                    if (b0 + lane < cur.cnt && (int)(e >> 26) == p) put(e);
+                                }
                             }
                         }
                     }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[as]);
                 }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[as]);
             }
-        }
-        if (npieces >= 2) epilogue(npieces - 2);
-        epilogue(npieces - 1);
+            if (npieces >= 2) epilogue(npieces - 2);
+            if (npieces >= 1) epilogue(npieces - 1);
 
-        // every MMA issued has completed (also after an abort: TMEM is freed below)
-        (void)__all_sync(kFull, mbar_drain(fin, 0, g.error));
-        asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
-        // Row tiles whose last piece this CTA delivered: sum the pieces in
-        // range order and store.  (Only range va can start before the row
-        // tile; its piece there is its last one.)
-        for (int k = 0; k < 2; ++k) {
-            const int tt = arr_tt[k];
-            if (tt < 0 || !arr_last[k] || *abort_flag) continue;
-            __threadfence();
-            const int va = range_of(tt * G, g), vb = range_of(tt * G + G - 1, g);
-            const int64_t s0 = range_begin(va, g) < tt * G ? (int64_t)va + V : va;
-            const int64_t n = (int64_t)tt * 128 + r;
-            if (n < t.N) {
-                for (int c = half; c < chunks; c += kDecWarps / 4) {
-                    float acc[16];
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) acc[jj] = __ldcg(g.partials + (s0 * Mp + 16 * c + jj) * 128 + r);
-                    for (int x = va + 1; x <= vb; ++x) {
-                        float y[16];
+            // thread 0 records the arrivals after each epilogue's barrier:
+            // one more barrier makes the last ones visible to every warp
+            asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+            // Row tiles whose last piece this CTA delivered: sum the pieces in
+            // range order and store.  (Only range va can start before the row
+            // tile; its piece there is its last one.)
+            for (int k = 0; k < 2; ++k) {
+                const int tt = arr_tt[k];
+                if (tt < 0 || !arr_last[k] || *abort_flag) continue;
+                __threadfence();
+                const int va = range_of(tt * G, g), vb = range_of(tt * G + G - 1, g);
+                const int64_t s0 = range_begin(va, g) < tt * G ? (int64_t)va + V : va;
+                const int64_t n = (int64_t)tt * 128 + r;
+                if (n < t.N) {
+                    for (int c = half; c < chunks; c += kDecWarps / 4) {
+                        float acc[16];
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj)
-                            y[jj] = __ldcg(g.partials + ((int64_t)x * Mp + 16 * c + jj) * 128 + r);
+                            acc[jj] = __ldcg(g.partials + (s0 * Mp + 16 * c + jj) * 128 + r);
+                        for (int x = va + 1; x <= vb; ++x) {
+                            float y[16];
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) acc[jj] += y[jj];
+                            for (int jj = 0; jj < 16; ++jj)
+                                y[jj] = __ldcg(g.partials + ((int64_t)x * Mp + 16 * c + jj) * 128 + r);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) acc[jj] += y[jj];
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (16 * c + jj < g.M) g.Y[(int64_t)(16 * c + jj) * g.ldy + n] = f32_to_bf16_rn(acc[jj]);
                     }
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj)
-                        if (16 * c + jj < g.M) g.Y[(int64_t)(16 * c + jj) * g.ldy + n] = f32_to_bf16_rn(acc[jj]);
                 }
+                if (threadIdx.x == 0) g.counters[tt] = 0;
             }
-            if (threadIdx.x == 0) g.counters[tt] = 0;
+            // every decoder warp has read this range's arrivals before thread
+            // 0 clears them for the next one
+            asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+            if (threadIdx.x == 0) {
+                arr_tt[0] = arr_tt[1] = -1;
+                arr_last[0] = arr_last[1] = 0;
+            }
+            jb += npieces;
         }
     } else if (warp == kWProdWarp) {
         // ------------------------------------------------------------------
         // Weight planes: one k-block (8 tiles of 1.5 KB) per stage, with
         // tiled copies, up to RW k-blocks ahead of the decoders, unit after
-        // unit of the range.  Reads only the W12 tensor, so it starts before
+        // unit of each range.  Reads only the W12 tensor, so it starts before
         // the previous kernel ends.
         // ------------------------------------------------------------------
         // The whole warp runs the loop (warp-uniform values stay in uniform
@@ -956,27 +1059,30 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
         int issued = 0;
         bool ok = true;
         RingPos wp;
-        int tt = u0 / G, grp = u0 - tt * G;
-        for (int u = u0; u < u1 && ok; ++u) {
-            for (int p = 0; p < 4; ++p, wp.advance(1, RW)) {
-                const int ws = wp.stage;
-                if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) {
-                    ok = false;
-                    break;
+        for (int v = blockIdx.x; v < V && ok; v += gridDim.x) {
+            const Range rg = range_at(v);
+            int tt = rg.tt0, grp = rg.ga0;
+            for (int u = rg.u0; u < rg.u1 && ok; ++u) {
+                for (int p = 0; p < 4; ++p, wp.advance(1, RW)) {
+                    const int ws = wp.stage;
+                    if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) {
+                        // the full box is counted, out-of-range stripes included (zero-filled)
+                        mbar_expect_tx(&w_full[ws], g.nested8 ? 8192u : kWStageBytes);
+                        uint8_t *dst = w_st + ws * kWStageBytes;
+                        tma_load_4d(dst, &hmap, 4 * grp + p, tt * 8, &w_full[ws]);
+                        if (!g.nested8) tma_load_4d(dst + 8192, &lmap, 4 * grp + p, tt * 8, &w_full[ws]);
+                    }
+                    __syncwarp();
+                    ++issued;
                 }
-                if (elect_one()) {
-                    // the full box is counted, out-of-range stripes included (zero-filled)
-                    mbar_expect_tx(&w_full[ws], g.nested8 ? 8192u : kWStageBytes);
-                    uint8_t *dst = w_st + ws * kWStageBytes;
-                    tma_load_4d(dst, &hmap, 4 * grp + p, tt * 8, &w_full[ws]);
-                    if (!g.nested8) tma_load_4d(dst + 8192, &lmap, 4 * grp + p, tt * 8, &w_full[ws]);
+                if (++grp == G) {
+                    grp = 0;
+                    ++tt;
                 }
-                __syncwarp();
-                ++issued;
-            }
-            if (++grp == G) {
-                grp = 0;
-                ++tt;
             }
         }
         // the copies issued last must have landed before the CTA exits
@@ -990,22 +1096,25 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
         int issued = 0;
         bool ok = true;
         RingPos bp;
-        int grp = u0 % G;
-        for (int u = u0; u < u1 && ok; ++u) {
-            for (int p = 0; p < 4; ++p, bp.advance(1, RB)) {
-                const int stage = bp.stage;
-                if (!__all_sync(kFull, mbar_wait(&b_empty[stage], bp.phase ^ 1u, abort_flag, g.error))) {
-                    ok = false;
-                    break;
+        for (int v = blockIdx.x; v < V && ok; v += gridDim.x) {
+            const Range rg = range_at(v);
+            int grp = rg.ga0;
+            for (int u = rg.u0; u < rg.u1 && ok; ++u) {
+                for (int p = 0; p < 4; ++p, bp.advance(1, RB)) {
+                    const int stage = bp.stage;
+                    if (!__all_sync(kFull, mbar_wait(&b_empty[stage], bp.phase ^ 1u, abort_flag, g.error))) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) {
+                        mbar_expect_tx(&b_full[stage], b_stage_bytes);
+                        tma_load_2d(b_st + stage * b_stage_bytes, &tmap, (4 * grp + p) * 64, 0, &b_full[stage]);
+                    }
+                    __syncwarp();
+                    ++issued;
                 }
-                if (elect_one()) {
-                    mbar_expect_tx(&b_full[stage], b_stage_bytes);
-                    tma_load_2d(b_st + stage * b_stage_bytes, &tmap, (4 * grp + p) * 64, 0, &b_full[stage]);
-                }
-                __syncwarp();
-                ++issued;
+                if (++grp == G) grp = 0;
             }
-            if (++grp == G) grp = 0;
         }
         // the copies issued last must have landed before the CTA exits
         for (int i = issued > RB ? issued - RB : 0; i < issued; ++i)
@@ -1020,38 +1129,44 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
             (void)__all_sync(kFull, mbar_wait(fin, 0, abort_flag, g.error));
         bool ok = true;
         RingPos ap, bp;
-        int grp = u0 % G;
-        int j = -1;  // piece
-        for (int u = u0; u < u1 && ok; ++u) {
-            const bool first = u == u0 || grp == 0;
-            const bool last = u + 1 == u1 || grp + 1 == G;
-            if (first) ++j;
-            const uint32_t d = tmem + (uint32_t)(j & 1) * acc_cols;
-            for (int p = 0; p < 4; ++p, ap.advance(1, RA), bp.advance(1, RB)) {
-                const int as = ap.stage, bs = bp.stage;
-                if (!__all_sync(kFull, mbar_wait(&a_full[as], ap.phase, abort_flag, g.error)) ||
-                    !__all_sync(kFull, mbar_wait(&b_full[bs], bp.phase, abort_flag, g.error))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a0 = smem_addr(a_st + as * kAStageBytes);
-                const uint32_t b0 = smem_addr(b_st + bs * b_stage_bytes);
-                if (elect_one()) {
+        int j = -1;  // the CTA's piece number
+        for (int v = blockIdx.x; v < V; v += gridDim.x) {
+            const Range rg = range_at(v);
+            int grp = rg.ga0;
+            for (int u = rg.u0; u < rg.u1 && ok; ++u) {
+                const bool first = u == rg.u0 || grp == 0;
+                const bool last = u + 1 == rg.u1 || grp + 1 == G;
+                if (first) ++j;
+                const uint32_t d = tmem + (uint32_t)(j & 1) * acc_cols;
+                for (int p = 0; p < 4; ++p, ap.advance(1, RA), bp.advance(1, RB)) {
+                    const int as = ap.stage, bs = bp.stage;
+                    if (!__all_sync(kFull, mbar_wait(&a_full[as], ap.phase, abort_flag, g.error)) ||
+                        !__all_sync(kFull, mbar_wait(&b_full[bs], bp.phase, abort_flag, g.error))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_addr(a_st + as * kAStageBytes);
+                    const uint32_t b0 = smem_addr(b_st + bs * b_stage_bytes);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma(d, smem_desc(a0 + 32 * kk), smem_desc(b0 + 32 * kk), tp.idesc,
-                             !(first && p == 0 && kk == 0));
-                    umma_commit(&a_empty[as]);
-                    umma_commit(&b_empty[bs]);
-                    if (last && p == 3) umma_commit(&done[j & 1]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma(d, smem_desc(a0 + 32 * kk), smem_desc(b0 + 32 * kk), tp.idesc,
+                                 !(first && p == 0 && kk == 0));
+                        umma_commit(&a_empty[as]);
+                        umma_commit(&b_empty[bs]);
+                        if (last && p == 3) umma_commit(&done[j & 1]);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
+                if (++grp == G) grp = 0;
             }
-            if (++grp == G) grp = 0;
         }
-        if (elect_one()) umma_commit(fin);  // arrives once every MMA issued above has completed
+        // TMEM and the shared-memory operands stay allocated until every MMA
+        // issued has completed (after an abort the decoders stop waiting)
+        if (elect_one()) umma_commit(fin);
         __syncwarp();
+        (void)__all_sync(kFull, mbar_drain(fin, 0, g.error));
     }
 
     tc_fence_before();
@@ -1148,15 +1263,23 @@ cudaError_t launch_variant(const TensorView &t, const GemmArgs &g, const TcParam
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    // the kernel's shared-memory limit, raised once per device (several host
+    // threads may launch at once)
+    static std::mutex configured_mutex;
     static int configured[64] = {0};
-    if (dev >= 0 && dev < 64 && configured[dev] < (int)smem) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
-        if (e != cudaSuccess) return e;
-        configured[dev] = (int)budget;
+    {
+        std::lock_guard<std::mutex> lock(configured_mutex);
+        if (dev < 0 || dev >= 64 || configured[dev] < (int)smem) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) configured[dev] = (int)budget;
+        }
     }
-    // one CTA per range, or per (row tile, K-chunk)
-    const int64_t blocks = Ranges ? g.ranges : ((t.Np + 127) / 128) * (int64_t)g.split;
+    // one CTA per range, or per (row tile, K-chunk) item; a capped grid
+    // walks the same items in the same cut (the result does not change)
+    int64_t blocks = Ranges ? g.ranges : ((t.Np + 127) / 128) * (int64_t)g.split;
     if (blocks == 0) return cudaSuccess;
+    if (g.max_ctas > 0 && blocks > g.max_ctas) blocks = g.max_ctas;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(Roles<D>::kThreads);
@@ -1194,8 +1317,8 @@ int64_t gemm_tc_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters
     const int64_t U = T * G;
     g.tc_ranges = false;
     g.ranges = 0;
-    if (split_k == 0 && counters_ok && Mp > 128 && U >= 16 * 152) {
-        const int64_t V = 152;
+    if (split_k == 0 && counters_ok && Mp > 128 && U >= 16 * W12_PLAN_SMS) {
+        const int64_t V = W12_PLAN_SMS;
         g.seglen = (int)U, g.per = (int)V;
         g.q = (int)(U / V), g.rem = (int)(U % V);
         g.ranges = V;
@@ -1214,9 +1337,9 @@ int64_t gemm_tc_plan(int64_t M, int64_t N, int64_t K, int split_k, bool counters
         S = split_k;
         cps = (Mp <= 128 && T * S >= kTwoPerSmMinCtas) ? 2 : 1;
     } else if (T > 0 && G > 0) {
-        S = tc_split_for(T, G, Mp, K, 152);
+        S = tc_split_for(T, G, Mp, K, W12_PLAN_SMS);
         if (Mp <= 128) {
-            const int64_t S2 = tc_split_for(T, G, Mp, K, 2 * 152);
+            const int64_t S2 = tc_split_for(T, G, Mp, K, 2 * W12_PLAN_SMS);
             if (T * S2 >= kTwoPerSmMinCtas) {
                 S = S2;
                 cps = 2;

@@ -23,6 +23,28 @@ struct TensorView {
 
 __host__ __device__ inline int64_t groups_of(int64_t K) { return (K + 255) / 256; }
 
+// GEMM workspace layout, the same for every shape so that one zeroed
+// workspace serves any sequence of calls: [0, 256) error word | arrival
+// counters for at most kWsMaxCounters stripes / row tiles (zero between
+// calls) | FP32 partials.
+constexpr int64_t kWsMaxCounters = 1LL << 16;
+constexpr size_t kWsCountersOff = 256;
+constexpr size_t kWsPartialsOff = kWsCountersOff + 4 * kWsMaxCounters;
+
+// The small-M path's automatic cut (one range per resident warp of
+// W12_PLAN_SMS SMs: 16 warps for M <= 8, 12 for M <= 16) needs at most two
+// partial slots per range of 16 rows x 8 or 16 token columns; those plans
+// fit the library's built-in scratch (w12_gemm_noalloc).
+constexpr size_t kMmaAutoPartialBytesM8 = 2 * 16 * (size_t)W12_PLAN_SMS * 16 * 8 * 4;
+constexpr size_t kMmaAutoPartialBytesM16 = 2 * 12 * (size_t)W12_PLAN_SMS * 16 * 16 * 4;
+static_assert(kWsPartialsOff + kMmaAutoPartialBytesM8 <= W12_NOALLOC_SCRATCH_BYTES &&
+                  kWsPartialsOff + kMmaAutoPartialBytesM16 <= W12_NOALLOC_SCRATCH_BYTES,
+              "automatic small-M plans must fit the w12_gemm_noalloc scratch");
+
+// Workspace bytes of w12_gemm for (M, N, K, opts), or the status that
+// w12_gemm would return for those options (w12_api.cu).
+w12_status gemm_plan_bytes(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *opts, size_t *bytes);
+
 // ---- codec (w12_codec.cu) ----
 // a1 + a2: base[n] and, added into esc_ptr[t*G+g+1] (zeroed by the caller),
 // the escape count of every (stripe, group).

@@ -12,43 +12,34 @@
 // loads the library holds until the process exits.
 //
 // The host-side name of the array is only a stand-in for it; its device
-// address comes from cudaGetSymbolAddress, called once per device (with that
-// device current) on the first call of this entry point on that device.
+// address comes from cudaGetSymbolAddress, asked on every call for the
+// device current at the time (so a reset or recreated context never leaves a
+// stale address behind).  The very first lookup on a device loads the
+// library's device code there, which is why the first call on a device
+// should come before any stream capture.
 #include <cstdint>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "w12.h"
+#include "w12_internal.h"
 
 namespace {
 
 constexpr size_t kScratchBytes = W12_NOALLOC_SCRATCH_BYTES;
 // Bytes at the front of a w12_gemm workspace that must be zero when a call
-// starts: the error word (256 bytes) and the split-K arrival counters
-// (4 bytes for each of at most 65536 row stripes).
-constexpr size_t kZeroedPrefix = 256 + 4 * 65536;
+// starts: the error word and the split-K arrival counters.
+constexpr size_t kZeroedPrefix = w12::kWsPartialsOff;
+static_assert(kZeroedPrefix < kScratchBytes, "the scratch must hold the zeroed prefix");
 
 static __device__ __align__(256) unsigned char g_w12_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array on the current device.
 cudaError_t scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_w12_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_w12_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -59,14 +50,22 @@ extern "C" w12_status w12_gemm_noalloc(const uint16_t *A, int64_t lda, const w12
                                        w12_stream_t stream) {
     if (!w || M < 0 || w->N < 0 || w->K < 0) return W12_ERR_INVALID;
     if (M == 0 || w->N == 0) return W12_OK;
-    const size_t need = w12_gemm_workspace_bytes(M, w->N, w->K, opts);
-    if (need == 0) return W12_ERR_INVALID;          // the shape or the options are not supported
+    size_t need = 0;
+    const w12_status st = w12::gemm_plan_bytes(M, w->N, w->K, opts, &need);
+    if (st != W12_OK) return st;                        // what w12_gemm returns for these options
     if (need > kScratchBytes) return W12_ERR_CAPACITY;  // beyond the built-in scratch
     void *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return W12_ERR_CUDA;
-    // The previous call may have failed part-way; start from clean counters.
+    // The previous call may have failed part-way; start from clean counters
+    // and a clear error word.
     const size_t zero = need < kZeroedPrefix ? need : kZeroedPrefix;
     if (cudaMemsetAsync(scratch, 0, zero, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return W12_ERR_CUDA;
     return w12_gemm(A, lda, w, Y, ldy, M, scratch, kScratchBytes, opts, stream);
+}
+
+extern "C" w12_status w12_gemm_noalloc_status(w12_stream_t stream) {
+    void *scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return W12_ERR_CUDA;
+    return w12_gemm_workspace_status(scratch, kScratchBytes, stream);
 }

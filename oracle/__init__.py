@@ -80,6 +80,9 @@ def _load():
                                                   p, p, i64, p, p, p]),
             "w12ref_decode_nested8": (ctypes.c_int, [i64, i64, p, p, p, p, i64, p, i64]),
             "w12ref_gemm_nested8": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, i64, p, i64, p, p]),
+            "w12ref_gemm_silu_mul": (ctypes.c_int, [p, i64, i64, i64, i64, p, p, p, p, p, i64, p, i64,
+                                                    p, p, p, p]),
+            "w12ref_round_bf16": (None, [p, i64, p]),
             "w12ref_bits_per_weight": (ctypes.c_double, [i64, i64, i64]),
             "w12ref_num_threads": (ctypes.c_int, []),
         }
@@ -257,6 +260,29 @@ def gemm(A: np.ndarray, t: W12Ref):
     st = _load().w12ref_gemm(_ptr(A), M, t.K, t.N, t.K, *_tensor_args(t), t.n_esc, _ptr(Y), t.N,
                              _ptr(Y64), _ptr(mag))
     return st, Y, Y64, mag
+
+
+def gemm_silu_mul(A: np.ndarray, t: W12Ref):
+    """The gate/up GEMM with its fused epilogue (reading R24): rows 16s+i
+    (gate) and 16s+8+i (up) of W give hidden unit 8s+i; Y[m, 8s+i] =
+    BF16(silu(g) * u) from the exact FP64 sums g, u, silu(x) = x/(1+exp(-x))
+    in FP64.  Returns (status, Y bits [M, N/2], g64, u64, magG, magU)."""
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    M = A.shape[0]
+    H = t.N // 2
+    Y = np.zeros((M, H), np.uint16)
+    out = [np.zeros((M, H), np.float64) for _ in range(4)]
+    st = _load().w12ref_gemm_silu_mul(_ptr(A), M, t.K, t.N, t.K, *_tensor_args(t), t.n_esc, _ptr(Y), H,
+                                      *(_ptr(o) for o in out))
+    return (st, Y, *out)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Doubles rounded to BF16 bits (nearest, ties to even), element-wise."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros(x.shape, np.uint16)
+    _load().w12ref_round_bf16(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def _nested8_args(t: W12Ref):

@@ -39,7 +39,9 @@
  *   R8 planes are padded to Np = N rounded up to 16 and Kp = K rounded up to
  *      256 (whole escape groups of 4 tiles) and stored tile by tile (16 rows x
  *      64 columns); the in-tile order is fixed by w12ref_hi_offset /
- *      w12ref_lo_position below.
+ *      w12ref_lo_position below;
+ *   R24 the fused gate/up epilogue silu(g) * u (not on the pages): gate row
+ *      16t+i and up row 16t+8+i of stripe t give hidden unit 8t+i.
  *
  * All functions return 0 on success and a negative code on bad arguments.
  */
@@ -525,6 +527,54 @@ int w12ref_gemm_nested8(const uint16_t *A, int64_t M, int64_t lda, int64_t N, in
     }
     free(a);
     return REF_OK;
+}
+
+/* ---- fused gate/up epilogue (reading R24) ----
+ * The pages do not write the layer an exact pass streams through; a gated
+ * MLP's gate/up GEMM is followed by silu(g) * u before the down GEMM, with
+ * silu(x) = x / (1 + exp(-x)).  Row layout (R24): in row stripe t of W
+ * (rows 16t .. 16t+15), row 16t+i is the gate row and row 16t+8+i the up
+ * row of hidden unit 8t+i, i = 0..7, so N is a multiple of 16 and the output
+ * has N/2 columns.  g and u are the exact FP64 sums of w12ref_gemm; silu(g)*u
+ * is evaluated in FP64 by the formula above and rounded once to BF16.
+ * Optional outputs, [M, N/2] row-major: G64, U64 (the two sums), magG, magU
+ * (their sum_k |A||W|), used by the tolerance rule. */
+int w12ref_gemm_silu_mul(const uint16_t *A, int64_t M, int64_t lda, int64_t N, int64_t K,
+                         const uint8_t *hi, const uint8_t *lo, const uint8_t *base,
+                         const int32_t *esc_ptr, const uint32_t *esc, int64_t n_esc, uint16_t *Y, int64_t ldy,
+                         double *G64, double *U64, double *magG, double *magU)
+{
+    if (M < 0 || N < 0 || N % 16 != 0 || ldy < N / 2) return REF_ERR_INVALID;
+    size_t cells = (size_t)(M * N > 0 ? M * N : 1);
+    uint16_t *full = (uint16_t *)malloc(sizeof(uint16_t) * cells);
+    double *sum = (double *)malloc(sizeof(double) * cells);
+    double *mag = (double *)malloc(sizeof(double) * cells);
+    int st = REF_ERR_INVALID;
+    if (full && sum && mag) st = w12ref_gemm(A, M, lda, N, K, hi, lo, base, esc_ptr, esc, n_esc, full, N, sum, mag);
+    if (st == REF_OK) {
+        int64_t H = N / 2;
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t j = 0; j < H; ++j) {
+                int64_t gate = (j / 8) * 16 + j % 8, up = gate + 8;
+                double g = sum[m * N + gate], u = sum[m * N + up];
+                double y = g / (1.0 + exp(-g)) * u;
+                Y[m * ldy + j] = w12ref_bf16_from_double(y);
+                if (G64) G64[m * H + j] = g;
+                if (U64) U64[m * H + j] = u;
+                if (magG) magG[m * H + j] = mag[m * N + gate];
+                if (magU) magU[m * H + j] = mag[m * N + up];
+            }
+    }
+    free(full);
+    free(sum);
+    free(mag);
+    return st;
+}
+
+/* Round doubles to BF16 bits, one by one (w12ref_bf16_from_double). */
+void w12ref_round_bf16(const double *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = w12ref_bf16_from_double(x[i]);
 }
 
 /* Storage cost in bits per weight, counting everything the tensor stores:

@@ -134,6 +134,42 @@ def test_tc_split_at_most_one_chunk_per_group(w12lib):
     assert tc_split(w12lib, 16, 1024, 1024, w12lib.make_opts(path=w12lib.W12_PATH_TC)) == 4
 
 
+def test_noalloc_scratch_holds_every_small_m_plan(w12lib):
+    """w12_gemm_noalloc promises that the automatic plan of every shape with
+    M <= 16 fits its built-in scratch; the automatic tensor-core plan of a
+    5120 x 5120 layer at M = 17 does not."""
+    from lossless_bit_weight_02_gb300 import synth
+    cap = w12lib.W12_NOALLOC_SCRATCH_BYTES
+    shapes = [(N, K) for _, N, K in synth.LAYER_SHAPES]
+    shapes += [(5121, 17400), (1, 1), (77829, 256), (16, 1 << 20)]
+    for N, K in shapes:
+        for M in range(1, 17):
+            nb = w12lib.w12_gemm_workspace_bytes(M, N, K)
+            assert 0 < nb <= cap, (M, N, K, nb)
+    assert w12lib.w12_gemm_workspace_bytes(17, 5120, 5120) > cap
+    # with split_k = 1 forced, the tensor-core path needs no partials at any M
+    for M in (17, 64, 256):
+        assert w12lib.w12_gemm_workspace_bytes(M, 34816, 5120, w12lib.make_opts(split_k=1)) == 256
+
+
+def test_noalloc_host_side_statuses(w12lib):
+    """w12_gemm_noalloc returns w12_gemm's status for options w12_gemm rejects,
+    and W12_ERR_CAPACITY for work beyond its scratch, before any CUDA call."""
+    lib = w12lib.load()
+    t = w12lib._Tensor(5120, 5120, 256, 512, 768, 1024, 1280, 1, 0)
+    mma = w12lib.make_opts(path=w12lib.W12_PATH_MMA)
+    st = lib.w12_gemm_noalloc(ctypes.c_void_p(4096), 5120, ctypes.byref(t), ctypes.c_void_p(8192), 5120, 17,
+                              ctypes.byref(mma), None)
+    assert st == w12lib.W12_ERR_UNSUPPORTED
+    st = lib.w12_gemm_noalloc(ctypes.c_void_p(4096), 5120, ctypes.byref(t), ctypes.c_void_p(8192), 5120, 17,
+                              None, None)
+    assert st == w12lib.W12_ERR_CAPACITY
+    bad = w12lib.GemmOpts(0, 0, 0, 4)  # unknown flag bit
+    st = lib.w12_gemm_noalloc(ctypes.c_void_p(4096), 5120, ctypes.byref(t), ctypes.c_void_p(8192), 5120, 1,
+                              ctypes.byref(bad), None)
+    assert st == w12lib.W12_ERR_INVALID
+
+
 def test_status_strings(w12lib):
     for code, name in ((0, "W12_OK"), (-3, "W12_ERR_CAPACITY"), (-7, "W12_ERR_CORRUPT")):
         assert w12lib.status_string(code) == name

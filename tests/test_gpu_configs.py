@@ -6,7 +6,8 @@ stack test converts 64 layers of the 27B-class shapes to W12 on the GPU (each
 tensor verified bit for bit, the BF16 copy freed), streams the 256 GEMMs at
 M = 1 and M = 16, and checks sampled outputs of layers 0 and 63 against the
 oracle.  The stress test runs N = 5121, K = 17400 with heavy-tailed weights,
-zero rows, denormals and maximum-exponent values at M = 1, 7, 33.
+zero rows, denormals and maximum-exponent values at M = 1, 7, 33, each on ten
+grid sizes (w12_gemm_opts.max_ctas), bitwise identical.
 """
 import numpy as np
 import pytest
@@ -73,9 +74,12 @@ def test_escape_stress_full_size(w12lib, oracle):
     assert w12lib.w12_verify_roundtrip(Wd, t) == (w12lib.W12_OK, 0)
     assert 0.01 < t.n_esc / (N * K) < 0.06  # 1-5% escapes
     rng = np.random.default_rng(8)
+    # ten runs on ten grids (max_ctas 0 = the default grid), bitwise identical;
+    # M = 33 takes the tensor-core path, M = 1 and 7 the small-M path
+    caps = (0, 1, 7, 76, 152, 304, 3, 64, 760, 2)
     for M in (1, 7, 33):
         Ad = synth.bits_to_tensor(synth.activations(M, K, seed=400 + M), "cuda")
-        outs = [synth.tensor_to_bits(w12lib.w12_gemm(Ad, t)) for _ in range(10)]
-        for o in outs[1:]:
-            assert np.array_equal(o, outs[0])  # ten runs, bitwise identical
+        outs = [synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, opts=w12lib.make_opts(max_ctas=c))) for c in caps]
+        for c, o in zip(caps[1:], outs[1:]):
+            assert np.array_equal(o, outs[0]), (M, c)
         assert sampled_check(w12lib, oracle, Wd, t, Ad, outs[0], rng, count=48) == 0

@@ -249,3 +249,31 @@ def test_overlap_flag_on_a_dependent_chain(M, w12lib):
         over = chain(w12lib.W12_GEMM_OVERLAP_PREVIOUS)
         for a, b in zip(plain, over):
             assert np.array_equal(a, b)
+
+
+def test_binding_rejects_bad_operands(w12lib):
+    """The C side trusts lda / ldy and writes M rows of N outputs, so the
+    Python binding refuses operands whose shape, stride or device does not
+    match before any pointer reaches the library."""
+    t = w12lib.w12_encode(synth.dense_weights_device(64, 512, seed=990))
+    A = synth.activations_device(4, 512, seed=991)
+    ok = torch.empty(4, 64, dtype=torch.bfloat16, device="cuda")
+    w12lib.w12_gemm(A, t, ok)
+    bad_y = (torch.empty(4, 63, dtype=torch.bfloat16, device="cuda"),       # too few columns
+             torch.empty(3, 64, dtype=torch.bfloat16, device="cuda"),       # too few rows
+             torch.empty(64, 4, dtype=torch.bfloat16, device="cuda").t(),   # transposed
+             torch.empty(4, 64, dtype=torch.float32, device="cuda"))        # wrong dtype
+    ws = w12lib.Workspace("cuda", 1 << 20)
+    for Y in bad_y:
+        with pytest.raises(ValueError):
+            w12lib.w12_gemm(A, t, Y)
+        with pytest.raises(ValueError):
+            w12lib.GemmCall(A, t, Y, ws)
+        with pytest.raises(ValueError):
+            w12lib.w12_gemm_noalloc(A, t, Y)
+    with pytest.raises(ValueError):
+        w12lib.w12_gemm(synth.activations_device(4, 256, seed=992), t)  # K does not match
+    with pytest.raises(ValueError):
+        w12lib.w12_gemm(torch.empty(512, 4, dtype=torch.bfloat16, device="cuda").t(), t)  # column stride
+    with pytest.raises(ValueError):
+        w12lib.w12_gemm(A.cpu(), t)

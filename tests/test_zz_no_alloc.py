@@ -69,3 +69,42 @@ def test_noalloc_rejects_work_beyond_its_scratch(w12lib):
     A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
     Y = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
     assert call_noalloc(w12lib, A, t, Y, opts) == w12lib.W12_ERR_CAPACITY
+
+
+def test_noalloc_capacity_of_the_automatic_tensor_core_plan(w12lib):
+    """Most automatic tensor-core plans (M > 16) need more split-K partials
+    than the scratch holds: M = 17 on a 5120 x 5120 layer gets
+    W12_ERR_CAPACITY, and the same shape with split_k = 1 runs."""
+    N = K = 5120
+    t = w12lib.w12_encode(synth.dense_weights_device(N, K, seed=84))
+    A = synth.activations_device(17, K, seed=85)
+    Y = torch.zeros(17, N, dtype=torch.bfloat16, device="cuda")
+    assert call_noalloc(w12lib, A, t, Y) == w12lib.W12_ERR_CAPACITY
+    one = w12lib.make_opts(split_k=1)
+    assert call_noalloc(w12lib, A, t, Y, one) == w12lib.W12_OK
+    ref = w12lib.w12_gemm(A, t, opts=one)
+    torch.cuda.synchronize()
+    assert torch.equal(Y.view(torch.int16), ref.view(torch.int16))
+
+
+def test_noalloc_reports_a_timeout(w12lib, oracle):
+    """A bounded wait that gives up inside a w12_gemm_noalloc call (made to
+    run out on purpose with W12_GEMM_TEST_STALL on the tensor-core path) is
+    reported by w12_gemm_noalloc_status, which reads and clears it; the next
+    call is correct again."""
+    lib = w12lib.load()
+    N, K, M = 1024, 2048, 32
+    W = synth.dense_weights(N, K, seed=86)
+    A = synth.activations(M, K, seed=87)
+    t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+    Ad = synth.bits_to_tensor(A, "cuda")
+    Y = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    stall = w12lib.make_opts(split_k=1, flags=w12lib.W12_GEMM_TEST_STALL)
+    assert call_noalloc(w12lib, Ad, t, Y, stall) == w12lib.W12_OK  # asynchronous: the launch succeeded
+    assert lib.w12_gemm_noalloc_status(w12lib._stream()) == w12lib.W12_ERR_TIMEOUT
+    assert lib.w12_gemm_noalloc_status(w12lib._stream()) == w12lib.W12_OK  # read and cleared
+    assert call_noalloc(w12lib, Ad, t, Y, w12lib.make_opts(split_k=1)) == w12lib.W12_OK
+    assert lib.w12_gemm_noalloc_status(w12lib._stream()) == w12lib.W12_OK
+    st, ref = oracle.encode(W)
+    st, Yr, Y64, mag = oracle.gemm(A, ref)
+    assert gemm_tolerance_failures(synth.tensor_to_bits(Y), Yr, Y64, mag).size == 0
