@@ -5,8 +5,10 @@ and the fraction of the HBM roofline, on the four GEMMs of a 27B-class dense
 decoder layer (QKV 5120->7168, O 5120->5120, gate/up 5120->34816,
 down 17408->5120).
 
-One step = the four layer GEMMs at each of M = 1, 2, 4, 8 (16 launches of
-w12_gemm), weights resident in HBM as W12, synthetic BF16 activations.  The
+One step = the four layer GEMMs at each of M = 1, 2, 4, 8 (16 GEMMs in one
+w12_gemm_list call, each reading its activations after the previous GEMM has
+completed; also timed as 16 separate w12_gemm calls), weights resident in HBM
+as W12, synthetic BF16 activations.  The
 per-step working set (4 x 496 MB of W12) is larger than the 129 MB L2 and the
 layers are visited round-robin, so every weight tensor is re-read only after
 at least 228 MB of other weights have passed through L2.
@@ -216,7 +218,8 @@ def run_gpu(args):
     calls = {(M, name): w12.GemmCall(acts[(M, name)], t, outs[(M, name)], wsp, stream=stream, opts=overlap)
              for M in Ms for name, t in layers}
 
-    def one_step(ev=None, m_values=M_VALUES):
+    def calls_step(ev=None, m_values=M_VALUES):
+        """The step as 16 w12_gemm calls chained by programmatic dependent launch."""
         j = 0
         for M in m_values:
             for name, t in layers:
@@ -227,13 +230,32 @@ def run_gpu(args):
                     ev[j][1].record(stream)
                 j += 1
 
-    launches_per_step = len(M_VALUES) * len(layers)
+    # The step as one w12_gemm_list call: the 16 GEMMs in one persistent
+    # launch, each reading its activations only after the GEMM before it has
+    # completed (the dependency a chain of layer GEMMs has).
+    step_keys = [(M, name) for M in M_VALUES for name, _ in layers]
+    tensor_of = dict(layers)
+    wsl = w12.Workspace(dev)
+    list_call = w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], j - 1, 0) for j, k in enumerate(step_keys)],
+                                 wsl, stream=stream)
+
+    def one_step():
+        list_call()
+
+    launches_per_step = 1
     step_bytes = sum(t.nbytes() for _, t in layers) * len(M_VALUES)
     alg_bytes = {(M, name): algorithmic_bytes(t, M) for M in Ms for name, t in layers}
 
     for _ in range(args.warmup):
         one_step()
+        calls_step()
     torch.cuda.synchronize()
+    # the list's outputs are bitwise those of the 16 separate calls
+    list_out = {k: outs[k].clone() for k in step_keys}
+    list_call()
+    torch.cuda.synchronize()
+    list_matches_calls = all(torch.equal(list_out[k].view(torch.int16), outs[k].view(torch.int16))
+                             for k in step_keys)
 
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -252,15 +274,25 @@ def run_gpu(args):
     clocks = sampler.stop()
     total_ms = job_time_ms(start.elapsed_time(stop), ws_n, dev)
 
-    # Per-launch events, after the timed region, on 10 more steps: an event
+    # The same step as 16 separate w12_gemm calls (programmatic dependent
+    # launch between them), timed the same way after the timed region.
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for k in range(args.steps):
+        calls_step()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    calls_ms = c0.elapsed_time(c1) / args.steps
+
+    # Per-launch events of the 16-call step on 10 more steps: an event
     # between two launches keeps the second from overlapping the first, so
-    # these launches run serialised (each pays its own fill and drain); they
-    # explain the step, they are not its time.
+    # these launches run serialised (each pays its own fill and drain).
     n_ev = 10
+    n_calls = len(step_keys)
     evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-            for _ in range(launches_per_step)] for _ in range(n_ev)]
+            for _ in range(n_calls)] for _ in range(n_ev)]
     for k in range(n_ev):
-        one_step(evs[k])
+        calls_step(evs[k])
     torch.cuda.synchronize()
 
     # run-to-run spread of the same step: 5 more batches of 50 steps, events
@@ -282,8 +314,8 @@ def run_gpu(args):
     # the same step replayed from a CUDA graph (how a serving engine launches a
     # fixed sequence of GEMMs): 10 steps per graph, on a side stream
     gstream = torch.cuda.Stream(dev)
-    gcalls = [w12.GemmCall(acts[(M, name)], t, outs[(M, name)], wsp, stream=gstream, opts=overlap)
-              for M in M_VALUES for name, t in layers]
+    gcalls = [w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], j - 1, 0) for j, k in enumerate(step_keys)],
+                               w12.Workspace(dev), stream=gstream)]
     with torch.cuda.stream(gstream):
         for c in gcalls:
             c()
@@ -306,7 +338,7 @@ def run_gpu(args):
     value_graph = job_value(step_bytes, 10 * g_reps, ws_n, graph_ms)
     del step_graph, gcalls
 
-    # per-launch kernel durations (serialised launches) -> per (M, layer)
+    # per-launch kernel durations (serialised launches of the 16-call step) -> per (M, layer)
     dur = {}
     j = 0
     for M in M_VALUES:
@@ -316,10 +348,10 @@ def run_gpu(args):
     kern_ms = sum(sum(v) for v in dur.values())
     kern_bytes = sum(alg_bytes[key] * len(v) for key, v in dur.items())
     achieved_serial = kern_bytes / (kern_ms * 1e-3) / 1e9
-    # The step's only kernel is k_gemm_mma<1> (every M <= 8); its launches
-    # overlap one another (programmatic dependent launch), so the kernel's
-    # device time per step is the step's device time, and the roofline's
-    # achieved rate is the step's algorithmic bytes over it.
+    # The step's only kernel is k_gemm_mma_list<1> (every M <= 8), launched
+    # once per step, so the kernel's device time per step is the step's
+    # device time, and the roofline's achieved rate is the step's
+    # algorithmic bytes over it.
     step_alg_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers)
     step_ms = total_ms / args.steps
     achieved = step_alg_bytes / (step_ms * 1e-3) / 1e9
@@ -360,6 +392,7 @@ def run_gpu(args):
             ts.append(e0.elapsed_time(e1) / 6)
         ms = statistics.median(ts)
         tl = []
+        per_layer = {name: [] for name, _ in layers}
         for _ in range(10):
             for j, (name, _) in enumerate(layers):
                 ev2[j][0].record(stream)
@@ -367,13 +400,16 @@ def run_gpu(args):
                 ev2[j][1].record(stream)
             torch.cuda.synchronize()
             tl.append(sum(e[0].elapsed_time(e[1]) for e in ev2))
+            for j, (name, _) in enumerate(layers):
+                per_layer[name].append(ev2[j][0].elapsed_time(ev2[j][1]))
         b = sum(t.nbytes() for _, t in layers)
         ab = sum(alg_bytes[(M, n)] for n, _ in layers)
         flops = sum(2.0 * M * t.N * t.K for _, t in layers)
         floor_s = max(ab / (hbm_peak * 1e9), flops / (bf16_peak * 1e12))
         return {"weight_gbs": round(b / (ms * 1e-3) / 1e9, 1), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
                 "roofline_frac": round(floor_s / (ms * 1e-3), 4), "us": round(ms * 1e3, 1),
-                "us_launch_events": round(statistics.median(tl) * 1e3, 1)}
+                "us_launch_events": round(statistics.median(tl) * 1e3, 1),
+                "us_launch_events_per_layer": {n: round(statistics.median(v) * 1e3, 1) for n, v in per_layer.items()}}
 
     sweep = {"1": sweep_point(1, lambda name: calls[(1, name)])}
     sweep["1"]["path"] = "mma"
@@ -388,9 +424,9 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host buffers ----
     # Every step copies all of its activations host -> device in one copy (from
-    # pinned memory), runs the 16 GEMMs through the public call (chained with
-    # programmatic dependent launch, as in the device step), and reads all the
-    # outputs back in one copy.
+    # pinned memory), runs the 16 GEMMs through the public call (one
+    # w12_gemm_list call, as in the device step), and reads all the outputs
+    # back in one copy.
     keys = [(M, name) for M in M_VALUES for name, _ in layers]
     align = lambda n: (n + 7) // 8 * 8  # 16-byte aligned views
     in_off, out_off, n_in, n_out = {}, {}, 0, 0
@@ -403,13 +439,14 @@ def run_gpu(args):
     d_in_all = torch.empty(n_in, dtype=torch.bfloat16, device=dev)
     d_out_all = torch.empty(n_out, dtype=torch.bfloat16, device=dev)
     h_out_all = torch.empty(n_out, dtype=torch.bfloat16).pin_memory()
-    e2e_calls = []
-    for key in keys:
+    e2e_entries = []
+    for j, key in enumerate(keys):
         a, o = acts[key], outs[key]
         t = dict(layers)[key[1]]
         d_a = d_in_all[in_off[key]:in_off[key] + a.numel()].view(a.shape)
         d_o = d_out_all[out_off[key]:out_off[key] + o.numel()].view(o.shape)
-        e2e_calls.append(w12.GemmCall(d_a, t, d_o, wsp, stream=stream, opts=overlap))
+        e2e_entries.append((d_a, t, d_o, j - 1, 0))
+    e2e_calls = [w12.GemmListCall(e2e_entries, w12.Workspace(dev), stream=stream)]
     h2d = sum(acts[key].numel() * 2 for key in keys)
     d2h = sum(outs[key].numel() * 2 for key in keys)
 
@@ -571,6 +608,42 @@ def run_gpu(args):
             gms = a.elapsed_time(b) / reps
             stack[f"m{M}"]["graph"] = {"pass_ms": round(gms, 3), "weight_gbs": round(sb / (gms * 1e-3) / 1e9, 1)}
             del graph, gcs
+            # The stack as one dependent chain through w12_gemm_list (256
+            # GEMMs, four launches of 64): per layer, QKV reads the layer
+            # input; O reads a fixed stand-in for the attention output and
+            # waits for QKV; gate/up reads O's output and writes silu(g) * u
+            # (W12_GEMM_SILU_MUL); down reads that and writes the next
+            # layer's input.
+            xs = [synth.activations_device(M, 5120, seed=M * 100 + 7, device=dev),
+                  torch.empty(M, 5120, dtype=torch.bfloat16, device=dev)]
+            attn = synth.activations_device(M, 5120, seed=M * 100 + 8, device=dev)
+            qb = torch.empty(M, 7168, dtype=torch.bfloat16, device=dev)
+            hb = torch.empty(M, 5120, dtype=torch.bfloat16, device=dev)
+            ab = torch.empty(M, 17408, dtype=torch.bfloat16, device=dev)
+            chain = []
+            for layer in range(64):
+                tq, to, tg, td = stk[4 * layer:4 * layer + 4]
+                j = len(chain)
+                chain += [(xs[layer % 2], tq, qb, j - 1, 0), (attn, to, hb, j, 0),
+                          (hb, tg, ab, j + 1, w12.W12_GEMM_SILU_MUL), (ab, td, xs[(layer + 1) % 2], j + 2, 0)]
+            lc = w12.GemmListCall(chain, w12.Workspace(dev), stream=stream)
+            lc()
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            a.record(stream)
+            for _ in range(reps):
+                lc()
+            b.record(stream)
+            torch.cuda.synchronize()
+            lms = a.elapsed_time(b) / reps
+            stack[f"m{M}"]["list_chain"] = {
+                "pass_ms": round(lms, 3), "weight_gbs": round(sb / (lms * 1e-3) / 1e9, 1),
+                "roofline_frac": round(sum(algorithmic_bytes(t, M) for t in stk) / (lms * 1e-3) / 1e9 / hbm_peak, 4),
+                "launches": (len(chain) + w12.W12_LIST_MAX - 1) // w12.W12_LIST_MAX,
+                "note": "256 GEMMs as a dependent chain (each layer: QKV; O after QKV; gate/up with the fused "
+                        "silu(g)*u epilogue after O; down after gate/up; next layer's QKV after down), "
+                        "w12_gemm_list"}
+            del lc, chain, xs, attn, qb, hb, ab
         del stk
         torch.cuda.empty_cache()
 
@@ -635,27 +708,33 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
-                     else "fallback 6.8 TB/s", "kernel": "k_gemm_mma<1> (w12_gemm, M<=8)",
-                     "method": "algorithmic bytes of the step's 16 launches (W12 bytes + activations + "
-                               "outputs) / the step's device time in the timed region (the kernel is the "
-                               "step's only one; its launches overlap)",
+                     else "fallback 6.8 TB/s", "kernel": "k_gemm_mma_list<1> (w12_gemm_list, M<=8)",
+                     "method": "algorithmic bytes of the step's 16 GEMMs (W12 bytes + activations + "
+                               "outputs) / the step's device time in the timed region (one launch per step, "
+                               "the step's only kernel)",
                      "bytes_per_step": step_alg_bytes,
                      "serialised_launches": {
                          "achieved": round(achieved_serial, 1), "frac": round(achieved_serial / hbm_peak, 4),
-                         "steps": n_ev,
-                         "note": "CUDA events around every launch of 10 steps after the timed region; an event "
-                                 "between launches serialises them, so each pays its own fill and drain"}},
+                         "steps": n_ev, "kernel": "k_gemm_mma<1> (w12_gemm)",
+                         "note": "the step as 16 w12_gemm calls with CUDA events around every launch, 10 steps "
+                                 "after the timed region; an event between launches serialises them, so each "
+                                 "pays its own fill and drain"}},
+        "value_calls": {"value": round(step_bytes / (calls_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                        "ms_per_step": round(calls_ms, 4), "list_matches_calls_bitwise": list_matches_calls,
+                        "note": "the same step as 16 w12_gemm calls chained by programmatic dependent launch "
+                                "(one launch per GEMM), timed over the same number of steps"},
         "roofline_by_m": roofline_by_m,
         "value_graph": {"value": round(value_graph, 1), "unit": "GB/s",
-                        "note": "the same 16-launch step replayed from a CUDA graph (10 steps per graph)"},
+                        "note": "the same step (one w12_gemm_list launch) replayed from a CUDA graph "
+                                "(10 steps per graph)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
         "tree": tree,
         "gdn": gdn,
         "noise": noise,
         "size_calibration": size_cal, "nested8": nested,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "matches_device_outputs": e2e_match,
-                "method": "per step: one pinned host->device copy of all 16 activations, the 16 w12_gemm calls "
-                          "(programmatic dependent launch), one device->host copy of all outputs",
+                "method": "per step: one pinned host->device copy of all 16 activations, one w12_gemm_list "
+                          "call over the 16 GEMMs, one device->host copy of all outputs",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

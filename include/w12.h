@@ -114,6 +114,17 @@ typedef struct {
  * for the exact GEMM. */
 #define W12_GEMM_NESTED8 2
 
+/* W12_GEMM_SILU_MUL: the fused epilogue of a gated MLP's gate/up GEMM.  The
+ * pages do not write the layer out; an exact pass over a dense target streams
+ * its gate/up weights, and what the next (down) GEMM reads is silu(g) * u,
+ * silu(x) = x / (1 + exp(-x)) (the published SiLU gating).  Row layout: in
+ * every stripe s of 16 rows, row 16s+i is the gate row and row 16s+8+i the up
+ * row of hidden unit 8s+i (i = 0..7), so N must be a multiple of 16
+ * (W12_ERR_INVALID otherwise).  Y is [M, N/2] with ldy >= N/2:
+ * Y[m, 8s+i] = BF16(silu(g) * u), g and u the FP32 sums of the two rows as the
+ * plain GEMM forms them, silu evaluated in FP32, one rounding to BF16. */
+#define W12_GEMM_SILU_MUL 4
+
 /* W12_GEMM_TEST_STALL (tests only): on the tensor-core path (M > 16) one
  * wait of the kernel waits for an event that never comes.  Every wait of the
  * kernel is bounded (about a second), so the wait gives up, the CTA aborts,
@@ -239,6 +250,54 @@ w12_status w12_gemm_noalloc(const uint16_t *A, int64_t lda, const w12_tensor *w,
  * `stream`; call it after the w12_gemm_noalloc call it checks and before the
  * next one, which clears the word. */
 w12_status w12_gemm_noalloc_status(w12_stream_t stream);
+
+/* ---- w12_gemm_list ----  Several small-M W12 GEMMs in one persistent
+ * launch.  The exact pass of a verify step streams every weight of the
+ * target (SpecPilot, section 4.1), and weight reads are 80% of the step
+ * (English summary, section 6.1): a layer pass is a chain of GEMMs whose
+ * launch boundaries would otherwise each cost a ramp-up and a drain.  Here
+ * every warp of one resident grid takes its range of each GEMM in list order
+ * (the same cut as w12_gemm, so every Y is bitwise what w12_gemm gives) and
+ * starts streaming the next GEMM's weights as soon as its own range is done.
+ *   items[i].A, lda, Y, ldy, M: as for w12_gemm (1 <= M <= 16, or M = 0 for
+ *     an item that does nothing); items[i].w: host pointer to the tensor.
+ *   items[i].after: -1, or the index j < i of an item this one depends on:
+ *     its A is read only after item j has written all of its Y (use it when
+ *     A is item j's output, or is computed from it).  Items without such a
+ *     dependency may overlap.
+ *   items[i].flags: 0 or W12_GEMM_SILU_MUL (then Y is [M, N/2]).
+ *   opts: max_ctas caps the grid; split_k forces every item's split; path
+ *     W12_PATH_AUTO or W12_PATH_MMA (W12_ERR_UNSUPPORTED for a tensor-core
+ *     path or an item with M > 16); flags: W12_GEMM_NESTED8 for every item;
+ *     W12_GEMM_OVERLAP_PREVIOUS: the launch may start streaming weights
+ *     while the previous kernel on the stream drains, as for w12_gemm (its
+ *     activations, outputs and workspace are touched only after that kernel
+ *     has completed); W12_GEMM_TEST_STALL (tests only) makes the first
+ *     item's dependency wait run out.
+ *   workspace: device, w12_gemm_list_workspace_bytes(items, n, opts) bytes,
+ *     16-byte aligned, zero-filled before its first use; every successful
+ *     call leaves it zeroed.
+ * Up to W12_LIST_MAX items go into one launch; a longer list is cut into
+ * several launches, one after the other on the stream.  Items with K = 0 get
+ * Y = 0 before the list's launch starts.  Every dependency wait is bounded
+ * (about a second): if one gives up, the call still completes, Y is
+ * unspecified and w12_gemm_workspace_status reports W12_ERR_TIMEOUT.  The
+ * launch is cooperative (every block resident), which those waits rely on.
+ * Asynchronous. */
+#define W12_LIST_MAX 64
+typedef struct {
+    const uint16_t *A;
+    int64_t lda;
+    const w12_tensor *w;
+    uint16_t *Y;
+    int64_t ldy;
+    int64_t M;
+    int32_t after;
+    int32_t flags;
+} w12_gemm_item;
+size_t w12_gemm_list_workspace_bytes(const w12_gemm_item *items, int32_t n, const w12_gemm_opts *opts);
+w12_status w12_gemm_list(const w12_gemm_item *items, int32_t n, void *workspace, size_t ws_bytes,
+                         const w12_gemm_opts *opts, w12_stream_t stream);
 
 /* Reads (and clears) the device-side error word that bounded waits inside
  * w12_gemm set when they give up.  Synchronous on `stream`.  Returns W12_OK

@@ -39,7 +39,9 @@ W12_ERR_UNSUPPORTED = -8
 W12_PATH_AUTO, W12_PATH_MMA, W12_PATH_TC = 0, 1, 2
 W12_GEMM_OVERLAP_PREVIOUS = 1
 W12_GEMM_NESTED8 = 2  # multiply by the nested 8-bit view (hi plane only)
-W12_GEMM_TEST_STALL = 1 << 30  # tests only: one wait of the tensor-core kernel runs out
+W12_GEMM_SILU_MUL = 4  # fused gate/up epilogue: Y[m, 8s+i] = silu(row 16s+i) * (row 16s+8+i)
+W12_GEMM_TEST_STALL = 1 << 30  # tests only: one bounded wait runs out
+W12_LIST_MAX = 64  # GEMMs per launch of w12_gemm_list
 
 # Every symbol include/w12.h declares.
 EXPORTS = (
@@ -47,7 +49,7 @@ EXPORTS = (
     "w12_esc_ptr_len", "w12_encode",
     "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
     "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_noalloc", "w12_gemm_noalloc_status",
-    "w12_gemm_workspace_status",
+    "w12_gemm_workspace_status", "w12_gemm_list_workspace_bytes", "w12_gemm_list",
     "w12_tree_workspace_bytes", "w12_tree_select",
     "w12_gdn_workspace_bytes", "w12_gdn_tree", "w12_gdn_status",
     "w12_status_string", "w12_version",
@@ -70,6 +72,12 @@ class _Tensor(ctypes.Structure):
         ("esc_ptr", ctypes.c_void_p), ("esc", ctypes.c_void_p),
         ("esc_cap", ctypes.c_int64), ("n_esc", ctypes.c_int64),
     ]
+
+
+class GemmItem(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("w", ctypes.POINTER(_Tensor)),
+                ("Y", ctypes.c_void_p), ("ldy", ctypes.c_int64), ("M", ctypes.c_int64),
+                ("after", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class GemmOpts(ctypes.Structure):
@@ -112,6 +120,9 @@ def load(path: str | None = None):
                                       ctypes.POINTER(GemmOpts), vp]),
             "w12_gemm_noalloc_status": (st, [vp]),
             "w12_gemm_workspace_status": (st, [vp, sz, vp]),
+            "w12_gemm_list_workspace_bytes": (sz, [ctypes.POINTER(GemmItem), ctypes.c_int32,
+                                                   ctypes.POINTER(GemmOpts)]),
+            "w12_gemm_list": (st, [ctypes.POINTER(GemmItem), ctypes.c_int32, vp, sz, ctypes.POINTER(GemmOpts), vp]),
             "w12_tree_workspace_bytes": (sz, [ctypes.c_int32, ctypes.c_int32]),
             "w12_tree_select": (st, [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                      ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
@@ -155,12 +166,19 @@ def _need_cuda(t: torch.Tensor, name: str, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
-def _check_gemm_operands(A: torch.Tensor, t: "W12Tensor", Y: torch.Tensor | None):
+def _out_cols(t: "W12Tensor", flags: int) -> int:
+    return t.N // 2 if flags & W12_GEMM_SILU_MUL else t.N
+
+
+def _check_gemm_operands(A: torch.Tensor, t: "W12Tensor", Y: torch.Tensor | None, flags: int = 0):
     """The C side trusts lda / ldy and writes M rows of N outputs, so the
     shapes, strides and devices are checked here, before any pointer is
-    passed: A is [M, K] and Y is [M, N], both with unit column stride, on the
-    device that holds the W12 tensor, which must be the current device (the
-    library launches on the current device)."""
+    passed: A is [M, K] and Y is [M, N] ([M, N/2] with W12_GEMM_SILU_MUL),
+    both with unit column stride, on the device that holds the W12 tensor,
+    which must be the current device (the library launches on the current
+    device)."""
+    if flags & W12_GEMM_SILU_MUL and t.N % 16:
+        raise ValueError(f"W12_GEMM_SILU_MUL needs N a multiple of 16, got {t.N}")
     _need_cuda(A, "A", torch.bfloat16)
     if A.dim() != 2 or A.shape[1] != t.K or (A.shape[0] > 0 and t.K > 0 and A.stride(1) != 1):
         raise ValueError(f"A must be [M, {t.K}] with unit column stride, got {tuple(A.shape)} "
@@ -172,8 +190,9 @@ def _check_gemm_operands(A: torch.Tensor, t: "W12Tensor", Y: torch.Tensor | None
         raise ValueError(f"the W12 tensor is on {dev} but the current device is cuda:{torch.cuda.current_device()}")
     if Y is not None:
         _need_cuda(Y, "Y", torch.bfloat16)
-        if Y.dim() != 2 or tuple(Y.shape) != (A.shape[0], t.N) or (Y.numel() > 0 and Y.stride(1) != 1):
-            raise ValueError(f"Y must be [{A.shape[0]}, {t.N}] with unit column stride, got {tuple(Y.shape)} "
+        cols = _out_cols(t, flags)
+        if Y.dim() != 2 or tuple(Y.shape) != (A.shape[0], cols) or (Y.numel() > 0 and Y.stride(1) != 1):
+            raise ValueError(f"Y must be [{A.shape[0]}, {cols}] with unit column stride, got {tuple(Y.shape)} "
                              f"strides {Y.stride()}")
         if Y.device != dev:
             raise ValueError(f"Y is on {Y.device}, the W12 tensor on {dev}")
@@ -335,11 +354,11 @@ def default_workspace(device) -> Workspace:
 def w12_gemm(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor | None = None, workspace: Workspace | None = None,
              opts: GemmOpts | None = None, stream=None) -> torch.Tensor:
     """Y[M,N] = A[M,K] * W^T with W in W12 (BF16 out, FP32 accumulation)."""
-    _check_gemm_operands(A, t, Y)
+    o = opts if opts is not None else make_opts()
+    _check_gemm_operands(A, t, Y, o.flags)
     M = A.shape[0]
     if Y is None:
-        Y = torch.empty(M, t.N, dtype=torch.bfloat16, device=A.device)
-    o = opts if opts is not None else make_opts()
+        Y = torch.empty(M, _out_cols(t, o.flags), dtype=torch.bfloat16, device=A.device)
     need = w12_gemm_workspace_bytes(M, t.N, t.K, o)
     ws = (workspace or default_workspace(A.device)).ensure(max(need, 256))
     s = t.struct()
@@ -355,8 +374,8 @@ class GemmCall:
 
     def __init__(self, A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, workspace: Workspace,
                  opts: GemmOpts | None = None, stream=None):
-        _check_gemm_operands(A, t, Y)
         self._opts = opts if opts is not None else make_opts()
+        _check_gemm_operands(A, t, Y, self._opts.flags)
         need = w12_gemm_workspace_bytes(A.shape[0], t.N, t.K, self._opts)
         ws = workspace.ensure(max(need, 256))
         self._keep = (A, t, Y, ws)  # the buffer itself: a later ensure() may replace it
@@ -372,14 +391,58 @@ class GemmCall:
             raise W12Error(st, "w12_gemm")
 
 
+class GemmListCall:
+    """w12_gemm_list with every argument marshalled once: calling the object
+    only invokes the C entry point.  entries: a sequence of (A, t, Y, after,
+    flags) with A [M, K] and Y [M, N] (or [M, N/2] with W12_GEMM_SILU_MUL)
+    CUDA bfloat16 tensors, t a W12Tensor, after -1 or the index of an earlier
+    entry whose output this entry's A depends on."""
+
+    def __init__(self, entries, workspace: Workspace, opts: GemmOpts | None = None, stream=None):
+        self._opts = opts if opts is not None else make_opts()
+        n = len(entries)
+        self._structs = []
+        items = (GemmItem * max(1, n))()
+        for i, (A, t, Y, after, flags) in enumerate(entries):
+            _check_gemm_operands(A, t, Y, flags)
+            if not -1 <= after < i:
+                raise ValueError(f"entry {i}: after must be -1 or an earlier entry, got {after}")
+            st = t.struct()
+            self._structs.append(st)
+            items[i] = GemmItem(A.data_ptr(), A.stride(0), ctypes.pointer(st), Y.data_ptr(), Y.stride(0),
+                                A.shape[0], after, flags)
+        self._items = items
+        need = int(load().w12_gemm_list_workspace_bytes(items, n, ctypes.byref(self._opts)))
+        if n and need == 0:
+            raise W12Error(W12_ERR_INVALID, "w12_gemm_list_workspace_bytes")
+        ws = workspace.ensure(max(need, 256))
+        self._keep = (entries, ws)
+        self._fn = load().w12_gemm_list
+        self._args = (items, n, ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.byref(self._opts),
+                      _stream(stream))
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != W12_OK:
+            raise W12Error(st, "w12_gemm_list")
+
+
+def w12_gemm_list(entries, workspace: Workspace | None = None, opts: GemmOpts | None = None, stream=None):
+    """Several small-M GEMMs in one persistent launch (w12_gemm_list); see
+    GemmListCall.  Returns the outputs."""
+    ws = workspace or default_workspace(entries[0][0].device if entries else "cuda")
+    GemmListCall(entries, ws, opts, stream)()
+    return [e[2] for e in entries]
+
+
 def w12_gemm_noalloc(A: torch.Tensor, t: W12Tensor, Y: torch.Tensor, opts: GemmOpts | None = None,
                      stream=None) -> torch.Tensor:
     """w12_gemm without a workspace: the library's built-in scratch array is
     used (for callers that cannot allocate device memory).  Y must be given."""
     if Y is None:
         raise ValueError("w12_gemm_noalloc needs the output Y")
-    _check_gemm_operands(A, t, Y)
     o = opts if opts is not None else make_opts()
+    _check_gemm_operands(A, t, Y, o.flags)
     s = t.struct()
     _check(load().w12_gemm_noalloc(ctypes.c_void_p(A.data_ptr()), A.stride(0), ctypes.byref(s),
                                    ctypes.c_void_p(Y.data_ptr()), Y.stride(0), A.shape[0], ctypes.byref(o),

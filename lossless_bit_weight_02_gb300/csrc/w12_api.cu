@@ -63,7 +63,8 @@ int choose_path(int64_t M, const w12_gemm_opts *o) {
 
 w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, GemmPlan &pl) {
     if (M < 0 || N < 0 || K < 0 || N > kMaxN || K > kMaxK) return W12_ERR_INVALID;
-    if (o && ((o->flags & ~(W12_GEMM_OVERLAP_PREVIOUS | W12_GEMM_NESTED8 | W12_GEMM_TEST_STALL)) != 0 ||
+    if (o && ((o->flags & ~(W12_GEMM_OVERLAP_PREVIOUS | W12_GEMM_NESTED8 | W12_GEMM_TEST_STALL |
+                            W12_GEMM_SILU_MUL)) != 0 ||
               o->max_ctas < 0 || o->split_k < 0 ||
               o->split_k > 256))
         return W12_ERR_INVALID;
@@ -85,9 +86,9 @@ w12_status plan_gemm(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *o, Ge
         pl.split = pl.cut.split;
         pl.bytes = pbytes > 0 ? pl.partials_off + (size_t)pbytes : 256;
     } else {
-        // The kernel numbers (stripe, group) units with int32; a tensor with
-        // 2^31 units would hold 8 TB of hi plane, so this never binds.
-        if (Np / 16 * G >= (1LL << 31)) return W12_ERR_INVALID;
+        // The kernel indexes a lane's hi-plane bytes with 256 * unit + lane in
+        // 32 bits: at most 2^24 (stripe, group) units, 64 GiB of hi plane.
+        if (Np / 16 * G >= (1LL << 24)) return W12_ERR_INVALID;
         pl.split = 1;
         pl.mp = gemm_mma_partial_cols(M);
         const int64_t slots = gemm_mma_plan(M, N, K, o ? o->split_k : 0, counters_ok, pl.cut);
@@ -215,7 +216,9 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     if (st != W12_OK) return st;
     if (M < 0) return W12_ERR_INVALID;
     if (M == 0 || w->N == 0) return W12_OK;
-    if (!Y || ldy < w->N) return W12_ERR_INVALID;
+    const bool silu = opts && (opts->flags & W12_GEMM_SILU_MUL) != 0;
+    if (silu && w->N % 16 != 0) return W12_ERR_INVALID;
+    if (!Y || ldy < (silu ? w->N / 2 : w->N)) return W12_ERR_INVALID;
     if (w->K > 0) {
         if (!A || lda < w->K) return W12_ERR_INVALID;
         if (!aligned16(A) || (lda % 8) != 0) return W12_ERR_ALIGN;
@@ -223,9 +226,9 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     GemmPlan pl;
     st = plan_gemm(M, w->N, w->K, opts, pl);
     if (st != W12_OK) return st;
-    if (w->K == 0)  // empty reduction: Y = 0
-        return cuda_status(cudaMemset2DAsync(Y, (size_t)ldy * 2, 0, (size_t)w->N * 2, (size_t)M,
-                                             reinterpret_cast<cudaStream_t>(stream)));
+    if (w->K == 0)  // empty reduction: Y = 0 (silu(0) * 0 = 0 too)
+        return cuda_status(cudaMemset2DAsync(Y, (size_t)ldy * 2, 0, (size_t)(silu ? w->N / 2 : w->N) * 2,
+                                             (size_t)M, reinterpret_cast<cudaStream_t>(stream)));
     if (!workspace || ws_bytes < pl.bytes) return W12_ERR_CAPACITY;
     if (!aligned16(workspace)) return W12_ERR_ALIGN;
     char *ws = static_cast<char *>(workspace);
@@ -247,6 +250,7 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
     g.overlap = opts ? (opts->flags & W12_GEMM_OVERLAP_PREVIOUS) != 0 : false;
     g.nested8 = opts ? (opts->flags & W12_GEMM_NESTED8) != 0 : false;
     g.test_stall = opts ? (opts->flags & W12_GEMM_TEST_STALL) != 0 : false;
+    g.silu = silu;
     g.error = reinterpret_cast<int32_t *>(ws);
     g.counters = reinterpret_cast<int32_t *>(ws + pl.counters_off);
     g.partials = reinterpret_cast<float *>(ws + pl.partials_off);
@@ -258,6 +262,139 @@ w12_status w12_gemm(const uint16_t *A, int64_t lda, const w12_tensor *w, uint16_
         return e == cudaErrorNotSupported ? W12_ERR_UNSUPPORTED : cuda_status(e);
     }
     return cuda_status(launch_gemm_mma(view_of(w), g, s));
+}
+
+// ---- w12_gemm_list ----
+// Workspace: [0,256) error word | kListSlices slices of arrival counters
+// (kWsMaxCounters each) | done[kListMax] + exit counter (256-byte aligned) |
+// kListSlices slices of FP32 partials.
+namespace {
+
+constexpr size_t kListCountersOff = 256;
+constexpr size_t kListDoneOff = kListCountersOff + 4 * (size_t)kListSlices * kWsMaxCounters;
+constexpr size_t kListPartialsOff = kListDoneOff + (4 * (kListMax + 1) + 255) / 256 * 256;
+
+// Checks every item and computes the bytes of one partial slice (the largest
+// over the list's launches).  Returns the status w12_gemm_list returns.
+w12_status plan_list(const w12_gemm_item *items, int32_t n, const w12_gemm_opts *o, size_t *slice_bytes) {
+    if (n < 0 || (n > 0 && !items)) return W12_ERR_INVALID;
+    if (o && ((o->flags & ~(W12_GEMM_OVERLAP_PREVIOUS | W12_GEMM_NESTED8 | W12_GEMM_TEST_STALL)) != 0 ||
+              o->max_ctas < 0 || o->split_k < 0 || o->split_k > 256))
+        return W12_ERR_INVALID;
+    if (o && o->path != W12_PATH_AUTO && o->path != W12_PATH_MMA)
+        return o->path == W12_PATH_TC ? W12_ERR_UNSUPPORTED : W12_ERR_INVALID;
+    size_t slice = 0;
+    for (int32_t c0 = 0; c0 < n; c0 += kListMax) {
+        const int32_t c1 = n - c0 < kListMax ? n : c0 + kListMax;
+        int64_t mmax = 0;
+        for (int32_t i = c0; i < c1; ++i) mmax = items[i].M > mmax ? items[i].M : mmax;
+        const int64_t mp = mmax <= 8 ? 8 : 16;
+        for (int32_t i = c0; i < c1; ++i) {
+            const w12_gemm_item &it = items[i];
+            w12_status st = check_tensor(it.w);
+            if (st != W12_OK) return st;
+            if (it.M < 0) return W12_ERR_INVALID;
+            if (it.M > 16) return W12_ERR_UNSUPPORTED;
+            if (it.after < -1 || it.after >= i) return W12_ERR_INVALID;
+            if ((it.flags & ~W12_GEMM_SILU_MUL) != 0) return W12_ERR_INVALID;
+            const bool silu = (it.flags & W12_GEMM_SILU_MUL) != 0;
+            const int64_t N = it.w->N, K = it.w->K;
+            if (it.M == 0 || N == 0) continue;
+            if (silu && N % 16 != 0) return W12_ERR_INVALID;
+            if (!it.Y || it.ldy < (silu ? N / 2 : N)) return W12_ERR_INVALID;
+            if (K > 0) {
+                if (!it.A || it.lda < K) return W12_ERR_INVALID;
+                if (!aligned16(it.A) || (it.lda % 8) != 0) return W12_ERR_ALIGN;
+            }
+            const int64_t G = groups_of(K), Np = rows_padded(N);
+            if (Np / 16 * G >= (1LL << 24)) return W12_ERR_INVALID;  // as for w12_gemm's small-M path
+            GemmArgs cut{};
+            const int64_t slots = gemm_mma_plan(it.M, N, K, o ? o->split_k : 0, Np / 16 <= kWsMaxCounters, cut);
+            const size_t b = (size_t)slots * 16 * (size_t)mp * 4;
+            slice = b > slice ? b : slice;
+        }
+    }
+    *slice_bytes = (slice + 255) / 256 * 256;
+    return W12_OK;
+}
+
+}  // namespace
+
+size_t w12_gemm_list_workspace_bytes(const w12_gemm_item *items, int32_t n, const w12_gemm_opts *opts) {
+    size_t slice = 0;
+    if (plan_list(items, n, opts, &slice) != W12_OK) return 0;
+    return kListPartialsOff + (size_t)kListSlices * slice;
+}
+
+w12_status w12_gemm_list(const w12_gemm_item *items, int32_t n, void *workspace, size_t ws_bytes,
+                         const w12_gemm_opts *opts, w12_stream_t stream) {
+    size_t slice = 0;
+    w12_status st = plan_list(items, n, opts, &slice);
+    if (st != W12_OK) return st;
+    if (n == 0) return W12_OK;
+    if (!workspace || ws_bytes < kListPartialsOff + (size_t)kListSlices * slice) return W12_ERR_CAPACITY;
+    if (!aligned16(workspace)) return W12_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    const bool nested8 = opts && (opts->flags & W12_GEMM_NESTED8) != 0;
+    const bool stall = opts && (opts->flags & W12_GEMM_TEST_STALL) != 0;
+    const bool overlap = opts && (opts->flags & W12_GEMM_OVERLAP_PREVIOUS) != 0;
+    static thread_local ListParams lp;  // 15 KB of descriptors: not on the stack
+    for (int32_t c0 = 0; c0 < n; c0 += kListMax) {
+        const int32_t c1 = n - c0 < kListMax ? n : c0 + kListMax;
+        memset(&lp, 0, sizeof lp);
+        lp.n = c1 - c0;
+        lp.done = reinterpret_cast<int32_t *>(ws + kListDoneOff);
+        lp.exit_count = lp.done + kListMax;
+        lp.error = reinterpret_cast<int32_t *>(ws);
+        lp.c28 = 1u << 28;
+        lp.c16 = 16u;
+        int64_t mmax = 0;
+        bool work = false;
+        for (int32_t i = c0; i < c1; ++i) {
+            const w12_gemm_item &it = items[i];
+            const int j = i - c0;
+            ListItem &li = lp.item[j];
+            li.t = view_of(it.w);
+            li.after = it.after >= c0 ? it.after - c0 : -1;  // earlier launches have completed
+            GemmArgs &g = li.g;
+            g.ranges = 0;  // no work unless set below
+            g.seglen = g.per = g.q = 1;
+            const bool silu = (it.flags & W12_GEMM_SILU_MUL) != 0;
+            if (it.M == 0 || it.w->N == 0) continue;
+            if (it.w->K == 0) {  // empty reduction: Y = 0 before the launch
+                if (cudaMemset2DAsync(it.Y, (size_t)it.ldy * 2, 0, (size_t)(silu ? it.w->N / 2 : it.w->N) * 2,
+                                      (size_t)it.M, s) != cudaSuccess)
+                    return W12_ERR_CUDA;
+                continue;
+            }
+            const int64_t Np = rows_padded(it.w->N);
+            (void)gemm_mma_plan(it.M, it.w->N, it.w->K, opts ? opts->split_k : 0, Np / 16 <= kWsMaxCounters, g);
+            g.A = it.A;
+            g.lda = it.lda;
+            g.Y = it.Y;
+            g.ldy = it.ldy;
+            g.M = it.M;
+            g.split = 1;
+            g.nested8 = nested8;
+            g.silu = silu;
+            g.partials = reinterpret_cast<float *>(ws + kListPartialsOff + (size_t)(j % kListSlices) * slice);
+            g.counters = reinterpret_cast<int32_t *>(ws + kListCountersOff) + (size_t)(j % kListSlices) * kWsMaxCounters;
+            g.error = lp.error;
+            g.c28 = lp.c28;
+            g.c16 = lp.c16;
+            mmax = it.M > mmax ? it.M : mmax;
+            work = true;
+        }
+        // tests only: the first item waits for a count that cannot be reached
+        // while it is waiting (every warp's exit), so the wait runs out
+        if (stall && c0 == 0) lp.item[0].after = -2;
+        if (!work) continue;
+        const cudaError_t e =
+            launch_gemm_mma_list(lp, mmax <= 8 ? 1 : 2, nested8, opts ? opts->max_ctas : 0, overlap || c0 > 0, s);
+        if (e != cudaSuccess) return e == cudaErrorCooperativeLaunchTooLarge ? W12_ERR_UNSUPPORTED : W12_ERR_CUDA;
+    }
+    return W12_OK;
 }
 
 size_t w12_tree_workspace_bytes(int32_t R, int32_t budget) {

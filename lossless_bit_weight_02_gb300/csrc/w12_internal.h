@@ -86,6 +86,7 @@ struct GemmArgs {
     bool overlap;        // launch as a programmatic dependent of the previous kernel
     bool nested8;        // multiply by the nested 8-bit view (hi plane only, escapes & 0xFFF0)
     bool test_stall;     // tensor-core path: make one bounded wait run out (tests of the timeout path)
+    bool silu;           // fused gate/up epilogue: Y[m, 8s+i] = silu(row 16s+i) * (row 16s+8+i)
     float *partials;     // tensor-core path: [S][Mpad][Np] (K-chunks) or [2*ranges][Mpad][128] (ranges);
                          // small-M path: [2*ranges][16][MP] fp32
     int32_t *counters;   // arrival counters per stripe (small-M) or row tile (tensor-core)
@@ -113,6 +114,30 @@ size_t tree_workspace_bytes(int64_t R, int64_t budget);
 cudaError_t launch_tree_select(const float *lp, int R, int D, int C, int budget, bool shared, int32_t *req,
                                int32_t *depth, uint64_t *path, float *score, int32_t *parent, int32_t *count,
                                void *workspace, cudaStream_t s);
+
+// A list of small-M GEMMs in one persistent launch (w12_gemm_list).  GEMM
+// i uses FP32 slots and arrival counters of slice i % kListSlices; a launch
+// holds at most kListMax GEMMs (its descriptors travel as kernel parameters).
+constexpr int kListSlices = 4;
+constexpr int kListMax = W12_LIST_MAX;
+struct ListItem {
+    TensorView t;
+    GemmArgs g;
+    int after;  // index (in this launch) of the GEMM whose completion A waits for; -1: none
+};
+struct ListParams {
+    int n;
+    int32_t *done;        // [kListMax] ranges completed per GEMM (zero between launches)
+    int32_t *exit_count;  // warps finished (zero between launches)
+    int32_t *error;       // workspace error word
+    uint32_t c28, c16;
+    ListItem item[kListMax];
+};
+static_assert(sizeof(ListParams) <= 32000, "list descriptors must fit the kernel-parameter space");
+// overlap: a programmatic dependent launch (the kernel reads A, Y and the
+// workspace only after the previous kernel on the stream has completed).
+cudaError_t launch_gemm_mma_list(const ListParams &lp, int nb, bool nested8, int max_ctas, bool overlap,
+                                 cudaStream_t s);
 
 // Small-M path: decode in registers + mma.sync m16n8k16 (M <= 16).
 cudaError_t launch_gemm_mma(const TensorView &t, const GemmArgs &g, cudaStream_t s);

@@ -55,6 +55,20 @@ __device__ __forceinline__ void decode16_fma(uint4 h, uint32_t l0, uint32_t l1, 
     out[7] = decode_pair_fma(prmt(h.w, l1s, 0x3726), base2, c28);
 }
 
+// silu(x) = x / (1 + e^-x) in FP32 (the fused gate/up epilogue): CUDA's
+// expf and an IEEE division; -0 for very negative x, x for very large x.
+__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
+
+// Fused gate/up epilogue on the tensor-core path, where lane l of a warp
+// holds row 32*(warp%4) + l of a 128-row tile: the gate row 16s+i and the up
+// row 16s+8+i of hidden unit 8s+i sit in lanes l and l^8.  Every lane of the
+// warp must call it (a shuffle); the result is silu(gate) * up on the gate
+// lanes (lane & 8 == 0), meaningless on the others.
+__device__ __forceinline__ float silu_pair(float v) {
+    const float up = __shfl_xor_sync(0xffffffffu, v, 8);
+    return silu_f32(v) * up;
+}
+
 // Escape entries of one 256-column group, one per lane (lane < cnt).
 struct EscBatch {
     uint32_t ent;  // key<<16 | BF16 bits

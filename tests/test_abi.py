@@ -74,7 +74,7 @@ def test_gemm_workspace_query(w12lib):
     nb = w12lib.w12_gemm_workspace_bytes(40, 1024, 4096, o)
     S, rem = divmod(nb - 256 - 4 * 65536, 48 * 1024 * 4)
     assert rem == 0 and S >= 2
-    bad = w12lib.GemmOpts(0, 0, 0, 4)  # unknown flag bit
+    bad = w12lib.GemmOpts(0, 0, 0, 8)  # unknown flag bit
     assert w12lib.w12_gemm_workspace_bytes(1, 64, 64, bad) == 0
 
 
@@ -164,7 +164,7 @@ def test_noalloc_host_side_statuses(w12lib):
     st = lib.w12_gemm_noalloc(ctypes.c_void_p(4096), 5120, ctypes.byref(t), ctypes.c_void_p(8192), 5120, 17,
                               None, None)
     assert st == w12lib.W12_ERR_CAPACITY
-    bad = w12lib.GemmOpts(0, 0, 0, 4)  # unknown flag bit
+    bad = w12lib.GemmOpts(0, 0, 0, 8)  # unknown flag bit
     st = lib.w12_gemm_noalloc(ctypes.c_void_p(4096), 5120, ctypes.byref(t), ctypes.c_void_p(8192), 5120, 1,
                               ctypes.byref(bad), None)
     assert st == w12lib.W12_ERR_INVALID

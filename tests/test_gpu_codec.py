@@ -220,3 +220,32 @@ def test_full_size_gate_up_encode_matches_oracle_on_sampled_stripes(w12lib, orac
         ptr = t.esc_ptr[st_ * G:st_ * G + G + 1].cpu().numpy()
         assert np.array_equal(ptr - ptr[0], ref.esc_ptr)
         assert np.array_equal(t.esc[ptr[0]:ptr[-1]].cpu().numpy().view(np.uint32), ref.esc)
+
+
+@pytest.mark.parametrize("name,N,K,seed", [(n, N, K, 1000 + i) for i, (n, N, K) in enumerate(synth.LAYER_SHAPES)] +
+                         [("stress", 5121, 17400, 4)])
+def test_full_size_encode_bytes_match_the_oracle_on_sampled_stripes(name, N, K, seed, w12lib, oracle):
+    """The 27B-class layers (and the escape-stress shape) encoded on the GPU
+    at full size, so the window, scan and pack kernels run their multi-block
+    grids; then sampled 16-row stripes (first, last, and random ones) are
+    compared byte for byte with the oracle's encoding of the same rows: hi and
+    lo planes, bases, group offsets (rebased to the stripe) and escapes."""
+    if name == "stress":
+        Wd = synth.bits_to_tensor(synth.adversarial_weights(N, K, seed=seed), "cuda")
+    else:
+        Wd = synth.dense_weights_device(N, K, seed=seed)
+    t = w12lib.w12_encode(Wd)
+    T = (N + 15) // 16
+    rng = np.random.default_rng(seed)
+    stripes = sorted({0, T - 1, T // 2, *rng.choice(T, size=3, replace=False).tolist()})
+    for s in stripes:
+        n0, n1 = 16 * s, min(N, 16 * s + 16)
+        got = host_view(t.rows(n0, n1))
+        st, ref = oracle.encode(synth.tensor_to_bits(Wd[n0:n1]))
+        assert st == oracle.OK
+        assert got["n_esc"] == ref.n_esc, (s, got["n_esc"], ref.n_esc)
+        assert np.array_equal(got["hi"], ref.hi), s
+        assert np.array_equal(got["lo"], ref.lo), s
+        assert np.array_equal(got["base"], ref.base), s
+        assert np.array_equal(got["esc_ptr"], ref.esc_ptr), s
+        assert np.array_equal(got["esc"], ref.esc[:ref.n_esc]), s

@@ -43,3 +43,31 @@ def gemm_tolerance_failures(y_bits, ref_bits, y64, absdot):
     ok_class = same_inf | same_nan
     ok = np.where(fin64, ok_num | same_inf | exempt, ok_class)
     return np.nonzero(~ok)[0]
+
+
+def silu_mul_tolerance_failures(y_bits, ref_bits, g64, u64, mag_g, mag_u):
+    """Rule for the fused gate/up epilogue y = silu(g) * u (reading R24).
+
+    The GPU forms g and u as FP32 sums: by the GEMM rule each lies within
+    e_g = 1e-3 * sum|a||w_g| (e_u likewise) of the FP64 sums g64, u64.  With
+    |silu'| <= 1.1, silu(g) * u then moves by at most
+        (|silu(g64)| + 1.1 e_g) e_u + 1.1 e_g |u64|,
+    the FP32 evaluation adds a few FP32 ulps (1e-6 relative) and the final
+    rounding half a BF16 ulp.  An element passes if it is within that bound
+    (plus one BF16 ulp) of the FP64 value, or within 2 BF16 ulp of the
+    oracle's BF16 result.  Non-finite references must match in class."""
+    y = bf16_bits_to_f64(np.asarray(y_bits)).reshape(-1)
+    r = bf16_bits_to_f64(np.asarray(ref_bits)).reshape(-1)
+    g = np.asarray(g64, np.float64).reshape(-1)
+    u = np.asarray(u64, np.float64).reshape(-1)
+    eg = 1e-3 * np.asarray(mag_g, np.float64).reshape(-1)
+    eu = 1e-3 * np.asarray(mag_u, np.float64).reshape(-1)
+    with np.errstate(over="ignore", invalid="ignore"):
+        s = g / (1.0 + np.exp(-g))
+        y64 = s * u
+        bound = (np.abs(s) + 1.1 * eg) * eu + 1.1 * eg * np.abs(u) + 1e-6 * np.abs(y64) + ulp_bf16(y64)
+        ok_num = np.isfinite(y) & ((np.abs(y - r) <= 2 * ulp_bf16(r)) | (np.abs(y - y64) <= bound))
+    fin = np.isfinite(y64)
+    same_class = (np.isnan(r) & np.isnan(y)) | (np.isinf(r) & np.isinf(y) & (np.sign(r) == np.sign(y)))
+    ok = np.where(fin, ok_num, same_class)
+    return np.nonzero(~ok)[0]
