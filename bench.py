@@ -5,10 +5,11 @@ and the fraction of the HBM roofline, on the four GEMMs of a 27B-class dense
 decoder layer (QKV 5120->7168, O 5120->5120, gate/up 5120->34816,
 down 17408->5120).
 
-One step = the four layer GEMMs at each of M = 1, 2, 4, 8 (16 GEMMs in one
+One step = the four layer GEMMs at each of M = 1, 2, 4, 8: 16 w12_gemm calls
+chained by programmatic dependent launch (STEP_FORM; the same GEMMs as one
 w12_gemm_list call, each reading its activations after the previous GEMM has
-completed; also timed as 16 separate w12_gemm calls), weights resident in HBM
-as W12, synthetic BF16 activations.  The
+completed, are timed beside it), weights resident in HBM as W12, synthetic
+BF16 activations.  The
 per-step working set (4 x 496 MB of W12) is larger than the 129 MB L2 and the
 layers are visited round-robin, so every weight tensor is re-read only after
 at least 228 MB of other weights have passed through L2.
@@ -34,6 +35,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 M_VALUES = (1, 2, 4, 8)
+# the form of the timed step: "calls" (16 w12_gemm calls chained by
+# programmatic dependent launch) or "list" (one w12_gemm_list call)
+STEP_FORM = "calls"
 SWEEP_M = (16, 24, 32, 63, 64, 128, 256)  # tree / batch verification rows
 METRIC = "W12 GEMM weight-GB/s & % HBM roofline at M=1/16/64 (27B-class layers)"
 FALLBACK_HBM_GBS = 6800.0
@@ -239,16 +243,22 @@ def run_gpu(args):
     list_call = w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], j - 1, 0) for j, k in enumerate(step_keys)],
                                  wsl, stream=stream)
 
-    def one_step():
-        list_call()
-
-    launches_per_step = 1
+    # Both forms of the step are timed over the same number of steps; the
+    # headline `value` is STEP_FORM's, the other is reported beside it.
+    forms = {"calls": (calls_step, len(step_keys), "k_gemm_mma<1> (w12_gemm, M<=8)",
+                       "16 w12_gemm calls chained by programmatic dependent launch"),
+             "list": (list_call, 1, "k_gemm_mma_list<1> (w12_gemm_list, M<=8)",
+                      "one w12_gemm_list call over the 16 GEMMs, each reading its activations after the "
+                      "GEMM before it has completed")}
+    other_form = "list" if STEP_FORM == "calls" else "calls"
+    one_step, launches_per_step, step_kernel, step_note = forms[STEP_FORM]
+    other_step = forms[other_form][0]
     step_bytes = sum(t.nbytes() for _, t in layers) * len(M_VALUES)
     alg_bytes = {(M, name): algorithmic_bytes(t, M) for M in Ms for name, t in layers}
 
     for _ in range(args.warmup):
         one_step()
-        calls_step()
+        other_step()
     torch.cuda.synchronize()
     # the list's outputs are bitwise those of the 16 separate calls
     list_out = {k: outs[k].clone() for k in step_keys}
@@ -274,15 +284,14 @@ def run_gpu(args):
     clocks = sampler.stop()
     total_ms = job_time_ms(start.elapsed_time(stop), ws_n, dev)
 
-    # The same step as 16 separate w12_gemm calls (programmatic dependent
-    # launch between them), timed the same way after the timed region.
+    # The other form of the step, timed the same way after the timed region.
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(stream)
     for k in range(args.steps):
-        calls_step()
+        other_step()
     c1.record(stream)
     torch.cuda.synchronize()
-    calls_ms = c0.elapsed_time(c1) / args.steps
+    other_ms = c0.elapsed_time(c1) / args.steps
 
     # Per-launch events of the 16-call step on 10 more steps: an event
     # between two launches keeps the second from overlapping the first, so
@@ -314,8 +323,12 @@ def run_gpu(args):
     # the same step replayed from a CUDA graph (how a serving engine launches a
     # fixed sequence of GEMMs): 10 steps per graph, on a side stream
     gstream = torch.cuda.Stream(dev)
-    gcalls = [w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], j - 1, 0) for j, k in enumerate(step_keys)],
-                               w12.Workspace(dev), stream=gstream)]
+    if STEP_FORM == "list":
+        gcalls = [w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], j - 1, 0) for j, k in enumerate(step_keys)],
+                                   w12.Workspace(dev), stream=gstream)]
+    else:
+        gcalls = [w12.GemmCall(acts[k], tensor_of[k[1]], outs[k], wsp, stream=gstream, opts=overlap)
+                  for k in step_keys]
     with torch.cuda.stream(gstream):
         for c in gcalls:
             c()
@@ -348,10 +361,10 @@ def run_gpu(args):
     kern_ms = sum(sum(v) for v in dur.values())
     kern_bytes = sum(alg_bytes[key] * len(v) for key, v in dur.items())
     achieved_serial = kern_bytes / (kern_ms * 1e-3) / 1e9
-    # The step's only kernel is k_gemm_mma_list<1> (every M <= 8), launched
-    # once per step, so the kernel's device time per step is the step's
-    # device time, and the roofline's achieved rate is the step's
-    # algorithmic bytes over it.
+    # The step's only kernel is k_gemm_mma<1> (16 launches that overlap by
+    # programmatic dependent launch) or k_gemm_mma_list<1> (one launch), so
+    # the kernel's device time per step is the step's device time, and the
+    # roofline's achieved rate is the step's algorithmic bytes over it.
     step_alg_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers)
     step_ms = total_ms / args.steps
     achieved = step_alg_bytes / (step_ms * 1e-3) / 1e9
@@ -446,7 +459,10 @@ def run_gpu(args):
         d_a = d_in_all[in_off[key]:in_off[key] + a.numel()].view(a.shape)
         d_o = d_out_all[out_off[key]:out_off[key] + o.numel()].view(o.shape)
         e2e_entries.append((d_a, t, d_o, j - 1, 0))
-    e2e_calls = [w12.GemmListCall(e2e_entries, w12.Workspace(dev), stream=stream)]
+    if STEP_FORM == "list":
+        e2e_calls = [w12.GemmListCall(e2e_entries, w12.Workspace(dev), stream=stream)]
+    else:
+        e2e_calls = [w12.GemmCall(a, t, o, wsp, stream=stream, opts=overlap) for a, t, o, _, _ in e2e_entries]
     h2d = sum(acts[key].numel() * 2 for key in keys)
     d2h = sum(outs[key].numel() * 2 for key in keys)
 
@@ -708,10 +724,10 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
-                     else "fallback 6.8 TB/s", "kernel": "k_gemm_mma_list<1> (w12_gemm_list, M<=8)",
+                     else "fallback 6.8 TB/s", "kernel": step_kernel,
                      "method": "algorithmic bytes of the step's 16 GEMMs (W12 bytes + activations + "
-                               "outputs) / the step's device time in the timed region (one launch per step, "
-                               "the step's only kernel)",
+                               "outputs) / the step's device time in the timed region (the step's only "
+                               "kernel; its launches overlap)",
                      "bytes_per_step": step_alg_bytes,
                      "serialised_launches": {
                          "achieved": round(achieved_serial, 1), "frac": round(achieved_serial / hbm_peak, 4),
@@ -719,22 +735,21 @@ def run_gpu(args):
                          "note": "the step as 16 w12_gemm calls with CUDA events around every launch, 10 steps "
                                  "after the timed region; an event between launches serialises them, so each "
                                  "pays its own fill and drain"}},
-        "value_calls": {"value": round(step_bytes / (calls_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                        "ms_per_step": round(calls_ms, 4), "list_matches_calls_bitwise": list_matches_calls,
-                        "note": "the same step as 16 w12_gemm calls chained by programmatic dependent launch "
-                                "(one launch per GEMM), timed over the same number of steps"},
+        "step_form": {"headline": STEP_FORM, "note": step_note,
+                      other_form: {"value": round(step_bytes / (other_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                                   "ms_per_step": round(other_ms, 4), "note": forms[other_form][3]},
+                      "list_matches_calls_bitwise": list_matches_calls},
         "roofline_by_m": roofline_by_m,
         "value_graph": {"value": round(value_graph, 1), "unit": "GB/s",
-                        "note": "the same step (one w12_gemm_list launch) replayed from a CUDA graph "
-                                "(10 steps per graph)"},
+                        "note": "the same step replayed from a CUDA graph (10 steps per graph)"},
         "per_m": per_m, "per_layer_us_m1": per_layer, "sweep": sweep, "codec": codec, "stack": stack,
         "tree": tree,
         "gdn": gdn,
         "noise": noise,
         "size_calibration": size_cal, "nested8": nested,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "matches_device_outputs": e2e_match,
-                "method": "per step: one pinned host->device copy of all 16 activations, one w12_gemm_list "
-                          "call over the 16 GEMMs, one device->host copy of all outputs",
+                "method": "per step: one pinned host->device copy of all 16 activations, the step's GEMMs "
+                          f"({step_note}), one device->host copy of all outputs",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
