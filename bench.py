@@ -1054,6 +1054,25 @@ def run_case(args):
             assert call.status() == w12.W12_OK
         print(f"case gdn: {n} nodes, {R} requests, {H} heads of {D}: path and WY, {args.iters} calls each")
         return
+    if args.case == "list":  # the bench step's 16 GEMMs as one dependent w12_gemm_list chain, `iters` times
+        layers = []
+        for i, (name, N, K) in enumerate(synth.LAYER_SHAPES):
+            layers.append((name, w12.w12_encode(synth.dense_weights_device(N, K, seed=1000 + i))))
+        keys = [(M, name) for M in M_VALUES for name, _ in layers]
+        tof = dict(layers)
+        entries = [(synth.activations_device(M, tof[n].K, seed=2000 + 10 * M + j), tof[n],
+                    torch.empty(M, tof[n].N, dtype=torch.bfloat16, device="cuda"), j - 1, 0)
+                   for j, (M, n) in enumerate(keys)]
+        call = w12.GemmListCall(entries, w12.Workspace("cuda"))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        call()
+        e0.record()
+        for _ in range(args.iters):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        print(f"case list: 16 dependent GEMMs per call, {e0.elapsed_time(e1) * 1e3 / args.iters:.1f} us per call")
+        return
     shapes = {name: (i, N, K) for i, (name, N, K) in enumerate(synth.LAYER_SHAPES)}
     i, N, K = shapes[args.case]
     Wd = synth.dense_weights_device(N, K, seed=1000 + i)
@@ -1098,8 +1117,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack measurement")
-    ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down), the tree selection (tree) or the "
-                    "GDN tree kernels (gdn)")
+    ap.add_argument("--case", default=None, help="profile one layer GEMM (qkv, o, gate_up, down), the step's GEMMs as one "
+                    "w12_gemm_list chain (list), the tree selection (tree) or the GDN tree kernels (gdn)")
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--codec", action="store_true", help="with --case: encode, decode and verify the layer")
     ap.add_argument("--tree", type=int, nargs=5, default=(1, 8, 8, 32, 0), metavar=("R", "D", "C", "B", "SHARED"),
