@@ -265,14 +265,26 @@ def empty_tensor(N: int, K: int, esc_cap: int, device) -> W12Tensor:
                      esc[:esc_cap], 0)
 
 
-def w12_encode(W: torch.Tensor, esc_cap: int | None = None, stream=None) -> W12Tensor:
-    """BF16 [N,K] (CUDA) -> W12Tensor.  Grows the escape arrays if needed."""
+def w12_encode(W: torch.Tensor, esc_cap: int | None = None, stream=None, out: W12Tensor | None = None) -> W12Tensor:
+    """BF16 [N,K] (CUDA) -> W12Tensor.  Grows the escape arrays if needed.
+    With `out` (a W12Tensor of the same N, K, e.g. from empty_tensor), encodes
+    into its buffers instead of allocating; its escape array keeps its
+    capacity (entries past n_esc are unused), and a tensor needing more
+    escapes than it holds raises W12Error(W12_ERR_CAPACITY)."""
     _need_cuda(W, "W", torch.bfloat16)
     assert W.dim() == 2 and W.stride(1) == 1
     N, K = W.shape
+    lib = load()
+    if out is not None:
+        if (out.N, out.K) != (N, K):
+            raise ValueError(f"out is {out.N}x{out.K}, W is {N}x{K}")
+        s = out.struct()
+        st = lib.w12_encode(ctypes.c_void_p(W.data_ptr()), W.stride(0), ctypes.byref(s), _stream(stream))
+        out.n_esc = s.n_esc
+        _check(st, "w12_encode")
+        return out
     if esc_cap is None:
         esc_cap = max(1024, (N * K) // 256)
-    lib = load()
     for _ in range(2):
         t = empty_tensor(N, K, esc_cap, W.device)
         s = t.struct()

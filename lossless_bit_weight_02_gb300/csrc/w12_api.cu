@@ -152,15 +152,17 @@ w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_strea
     if (cudaMemsetAsync(out->esc_ptr, 0, 4 * (size_t)(P + 1), s) != cudaSuccess) return W12_ERR_CUDA;
     if (launch_window_count(W, ldw, N, K, out->base, out->esc_ptr, s) != cudaSuccess) return W12_ERR_CUDA;
     if (launch_ptr_scan(out->esc_ptr, P, s) != cudaSuccess) return W12_ERR_CUDA;
+    // the pack kernel writes only the entries below esc_cap (none if the
+    // offsets overflowed), so the escape total is read once, at the end
+    if (launch_pack(W, ldw, N, K, out->base, out->esc_ptr, out->hi, out->lo, out->esc, out->esc_cap, s) !=
+        cudaSuccess)
+        return W12_ERR_CUDA;
     int32_t total = 0;
     if (cudaMemcpyAsync(&total, out->esc_ptr + P, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return W12_ERR_CUDA;
     if (total < 0) return W12_ERR_INVALID;  // more escapes than an int32 offset can index
     out->n_esc = total;
-    if (launch_pack(W, ldw, N, K, out->base, out->esc_ptr, out->hi, out->lo, out->esc, out->esc_cap, s) !=
-        cudaSuccess)
-        return W12_ERR_CUDA;
     return total > out->esc_cap ? W12_ERR_CAPACITY : W12_OK;
 }
 

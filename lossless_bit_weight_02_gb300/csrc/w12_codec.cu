@@ -7,6 +7,7 @@
 // group, the unit the escape list is indexed by.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "w12_device.cuh"
 #include "w12_internal.h"
@@ -14,69 +15,77 @@
 namespace w12 {
 namespace {
 
-// Eight consecutive weights of a row, zero past K (0 is "not counted" and
-// "not an escape" for the callers, which mask with k < K anyway).
-__device__ __forceinline__ void load8(const uint16_t *row, bool vec, int64_t k, int64_t K, uint16_t v[8]) {
-    if (vec && k + 8 <= K) {
-        uint4 q = *reinterpret_cast<const uint4 *>(row + k);
-        memcpy(v, &q, 16);
-    } else {
+// Eight consecutive weights of a row as four words (weight 2i in the low
+// half of word i); columns at or past K read as `fill`.
+__device__ __forceinline__ uint4 load8w(const uint16_t *row, bool vec, int64_t k, int64_t K, uint32_t fill) {
+    if (vec && k + 8 <= K) return __ldg(reinterpret_cast<const uint4 *>(row + k));
+    uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = (k + j < K) ? row[k + j] : 0;
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t a = (k + 2 * j < K) ? (uint32_t)row[k + 2 * j] : fill;
+        const uint32_t b = (k + 2 * j + 1 < K) ? (uint32_t)row[k + 2 * j + 1] : fill;
+        w[j] = a | (b << 16);
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Offset-and-mantissa field of w in the window of base b: (e-b)<<7 | m, in
-// [0, 0x7FF] exactly when e is in [b, b+15].  With b in [1, 239] every other
-// exponent lands outside that range as an unsigned value: e = 0 and e < b
-// give a negative difference, e = 255 and e > b+15 one of at least 0x800.
-__device__ __forceinline__ uint32_t window_field(uint16_t w, int b) {
-    return (uint32_t)((int)(w & 0x7FFF) - (b << 7));
+// The window test and the record field for two weights at once.  Per 16-bit
+// half, window_word gives h = (w & 0x7FFF) + 0x8000 - (base << 7), that is
+// 0x8000 + f with f = (w & 0x7FFF) - (base << 7) the record's offset-and-
+// mantissa field (e-base)<<7 | m.  For any base byte h stays in
+// [0x80, 0xFFFF], so no borrow or carry crosses the halves.  The weight lies
+// in the window [base, base+15] exactly when 0 <= f <= 0x7FF, i.e. when
+// h & 0xF800 == 0x8000: escape_bits is nonzero in the half of every weight
+// outside its window (e = 0 and e = 255 included, since base is in [1, 239]).
+__device__ __forceinline__ uint32_t window_c2(uint32_t b) { return 0x80008000u - b * 0x00800080u; }
+__device__ __forceinline__ uint32_t window_word(uint32_t x, uint32_t c2) { return (x & 0x7FFF7FFFu) + c2; }
+__device__ __forceinline__ uint32_t escape_bits(uint32_t d) { return (d & 0xF800F800u) ^ 0x80008000u; }
+__device__ __forceinline__ int halves_set(uint32_t e) { return ((e & 0xFFFFu) != 0u) + ((e >> 16) != 0u); }
+
+// ---------------------------------------------------------------------------
+// a1 + a2: the window search and escape count, one of two kernels by row
+// length.  Both build the exact histogram of the row's exponent field, take
+// the window of 16 consecutive exponents holding the most counted weights
+// (exponents 0 and 255 are always escapes and not counted; ties go to the
+// largest base), and then re-read the row (mostly L2 hits) to add its escapes
+// per 256-column group into esc_ptr[t*G+g+1].
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
+    asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
-__device__ __forceinline__ bool is_escape(uint16_t w, int b) { return window_field(w, b) > 0x7FFu; }
 
-// ---------------------------------------------------------------------------
-// a1 + a2: one warp per row.  Histogram of the exponent field over the row's
-// normal finite weights, window sums over 16 consecutive exponents, argmax
-// with ties to the largest base.  A second pass over the row counts its
-// escapes per 256-column group into esc_ptr[t*G+g+1].
-// ---------------------------------------------------------------------------
-constexpr int kWinWarps = 8;
-
-__global__ __launch_bounds__(kWinWarps * 32) void k_window_count(
-    const uint16_t *__restrict__ W, int64_t ldw, int64_t N, int64_t K, uint8_t *__restrict__ base,
-    int32_t *__restrict__ esc_ptr) {
-    __shared__ int hist[kWinWarps][256];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n = (int64_t)blockIdx.x * kWinWarps + warp;
-    if (n >= N) return;  // warp-uniform; no block-wide barrier below
-    int *h = hist[warp];
-    for (int i = lane; i < 256; i += 32) h[i] = 0;
-    __syncwarp();
-    const uint16_t *row = W + n * ldw;
-    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-    for (int64_t k0 = 0; k0 < K; k0 += 256) {
-        const int64_t k = k0 + lane * 8;
-        uint16_t v[8];
-        load8(row, vec, k, K, v);
+// The window base from a warp's counts, lane j holding h[i] = the count of
+// exponent 8j + i (0 for exponents 0 and 255).
+__device__ __forceinline__ int window_base(const uint32_t h[8], int lane) {
+    // c[i] = number of counted weights with exponent <= 8*lane + i
+    uint32_t c[8], run = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = (v[j] >> 7) & 0xFF;
-            const bool counted = (k + j < K) && e >= 1 && e <= 254;
-            // plain shared-memory atomics: the hardware merges lanes that hit the
-            // same bin (grouping them first with __match_any_sync was 13% slower
-            // over the whole encode on GB300)
-            if (counted) atomicAdd(&h[e], 1);
-        }
+    for (int i = 0; i < 8; ++i) {
+        run += h[i];
+        c[i] = run;
     }
-    __syncwarp();
+    uint32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - run;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] += excl;
+    // window b = 8*lane + i holds c(b+15) - c(b-1) weights: c(b+15) is lane
+    // lane+1's c[7] for i = 0 and lane lane+2's c[i-1] otherwise
+    uint32_t up[7];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) up[i] = __shfl_down_sync(kFull, c[i], 2);
+    const uint32_t next7 = __shfl_down_sync(kFull, c[7], 1);
     int best = -1, best_b = 0;
-    for (int b = 1 + lane; b <= 239; b += 32) {
-        int c = 0;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) c += h[b + e];
-        if (c > best || (c == best && b > best_b)) {
-            best = c;
+    for (int i = 0; i < 8; ++i) {
+        const int b = 8 * lane + i;
+        const int cnt = (int)((i == 0 ? next7 : up[i - 1]) - (i == 0 ? excl : c[i - 1]));
+        if (b >= 1 && b <= 239 && cnt >= best) {  // b ascending: ties go to the larger base
+            best = cnt;
             best_b = b;
         }
     }
@@ -89,169 +98,496 @@ __global__ __launch_bounds__(kWinWarps * 32) void k_window_count(
             best_b = obb;
         }
     }
-    if (lane == 0) base[n] = (uint8_t)best_b;
-    // escapes per 256-column group (the row was just read: mostly L2 hits)
-    const int64_t G = groups_of(K);
-    int32_t *cnt = esc_ptr + 1 + (n / 16) * G;
-    for (int64_t k0 = 0, g = 0; k0 < K; k0 += 256, ++g) {
-        const int64_t k = k0 + lane * 8;
-        uint16_t v[8];
-        load8(row, vec, k, K, v);
-        int c = 0;
+    return best_b;
+}
+
+// Adds the escapes of one lane's 8 weights of group g (a warp-wide call)
+// into cnt[g].
+__device__ __forceinline__ void count_group_escapes(int32_t *cnt, int g, const uint4 &x, uint32_t c2, int lane) {
+    const uint32_t e0 = escape_bits(window_word(x.x, c2)), e1 = escape_bits(window_word(x.y, c2));
+    const uint32_t e2 = escape_bits(window_word(x.z, c2)), e3 = escape_bits(window_word(x.w, c2));
+    const bool any = (e0 | e1 | e2 | e3) != 0u;
+    if (__any_sync(kFull, any)) {  // a third of a row's groups at the pages' escape rate
+        int k = any ? halves_set(e0) + halves_set(e1) + halves_set(e2) + halves_set(e3) : 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) c += (k + j < K) && is_escape(v[j], best_b);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-        if (lane == 0 && c) atomicAdd(&cnt[g], c);
+        for (int o = 16; o; o >>= 1) k += __shfl_xor_sync(kFull, k, o);
+        if (lane == 0 && k) atomicAdd(&cnt[g], k);
     }
+}
+
+constexpr int64_t kLongRow = 8192;  // columns: longer rows take the 4-warp kernel
+
+// Rows of at most kLongRow columns: one warp (and block) per row, 24 rows in
+// flight per SM.  The histogram lives in shared memory as 8-bit counters
+// private to each lane: exponent e of lane L is byte e/64 of the word at
+// (e%64)*128 + 4L.  A lane only ever touches its own bank (one shared
+// histogram took the lanes that hit the same exponent one after another), and
+// the low weight of a word x finds its counter word as (x & 0x1F80) | 4L,
+// exponent bits 0..5 already in place; the add is a shared-memory reduction
+// (a plain load, add and store measured 14% slower).  Every exponent is
+// counted, 0 and 255 included; those two bins are dropped before the window
+// search.  A lane adds 8 weights per 256-column step, so the counters are
+// folded into per-lane totals every 28 steps, before they can pass 255.
+// ---------------------------------------------------------------------------
+constexpr int kFoldSteps = 28;  // 28 * 8 = 224 < 256 adds per counter between folds
+
+// hl = the shared address of the counters + 4 * lane
+__device__ __forceinline__ void count_word(uint32_t hl, uint32_t x) {
+    red_add_shared(hl + (x & 0x1F80u), 1u << ((x >> 10) & 0x18u));
+    red_add_shared(hl + ((x >> 16) & 0x1F80u), 1u << ((x >> 26) & 0x18u));
+}
+
+// Lane j adds counter words j and j+32 of all 32 copies (reading copy
+// (i + j) % 32 at step i: distinct banks) into tot[m] = count of exponent
+// j + 32m, and optionally clears what it read.
+__device__ __forceinline__ void fold_counts(uint32_t *h, int lane, bool clear, uint32_t tot[8]) {
+    __syncwarp();
+    uint32_t a0 = 0, b0 = 0, a1 = 0, b1 = 0;  // two 16-bit sums each (at most 32 * 224)
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+        const int c = (i + lane) & 31;
+        const uint32_t x0 = h[32 * lane + c], x1 = h[32 * (lane + 32) + c];
+        if (clear) {
+            h[32 * lane + c] = 0u;
+            h[32 * (lane + 32) + c] = 0u;
+        }
+        a0 += x0 & 0x00FF00FFu;         // exponents j (low) and j + 128 (high)
+        b0 += (x0 >> 8) & 0x00FF00FFu;  // j + 64, j + 192
+        a1 += x1 & 0x00FF00FFu;         // j + 32, j + 160
+        b1 += (x1 >> 8) & 0x00FF00FFu;  // j + 96, j + 224
+    }
+    tot[0] += a0 & 0xFFFFu;
+    tot[1] += a1 & 0xFFFFu;
+    tot[2] += b0 & 0xFFFFu;
+    tot[3] += b1 & 0xFFFFu;
+    tot[4] += a0 >> 16;
+    tot[5] += a1 >> 16;
+    tot[6] += b0 >> 16;
+    tot[7] += b1 >> 16;
+    __syncwarp();
+}
+
+// Calls f(s, x) for the steps s = 0 .. full-1 of a row, x = this lane's 8
+// weights of step s (p[32 * s]), with four steps in flight per warp (24
+// warps per SM then keep ~48 KB of loads in flight, enough to cover HBM
+// latency).
+template <class F>
+__device__ __forceinline__ void for_full_steps(const uint4 *__restrict__ p, int full, F &&f) {
+    int s = 0;
+    if (full >= 8) {
+        uint4 n0 = __ldg(p), n1 = __ldg(p + 32), n2 = __ldg(p + 64), n3 = __ldg(p + 96);
+        for (; s + 8 <= full; s += 4) {
+            uint4 x = n0;
+            n0 = __ldg(p + 32 * (s + 4));
+            f(s, x);
+            x = n1;
+            n1 = __ldg(p + 32 * (s + 5));
+            f(s + 1, x);
+            x = n2;
+            n2 = __ldg(p + 32 * (s + 6));
+            f(s + 2, x);
+            x = n3;
+            n3 = __ldg(p + 32 * (s + 7));
+            f(s + 3, x);
+        }
+        f(s, n0);
+        f(s + 1, n1);
+        f(s + 2, n2);
+        f(s + 3, n3);
+        s += 4;
+    }
+    for (; s < full; ++s) f(s, __ldg(p + 32 * s));
+}
+
+__global__ __launch_bounds__(32) void k_window_count_warp(const uint16_t *__restrict__ W, int64_t ldw, int64_t N,
+                                                     int64_t K, uint8_t *__restrict__ base,
+                                                     int32_t *__restrict__ esc_ptr) {
+    __shared__ __align__(16) uint32_t hist[64 * 32];  // [e % 64][lane], byte e / 64
+    const int lane = threadIdx.x;
+    const int64_t n = blockIdx.x;
+    const uint32_t hl = (uint32_t)__cvta_generic_to_shared(hist) + (uint32_t)lane * 4u;
+#pragma unroll 8
+    for (int w = 0; w < 64; ++w) hist[32 * w + lane] = 0u;
+    __syncwarp();
+    const uint16_t *row = W + n * ldw;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    const int G = (int)groups_of(K);                  // steps of 256 columns (G < 2^24: checked on the host)
+    const int full = vec ? (int)(K >> 8) : 0;        // steps whose 8 columns are in range for every lane
+    const uint4 *p = reinterpret_cast<const uint4 *>(row) + lane;  // step s: p[32 * s]
+    uint32_t tot[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int since = 0;
+    auto count_step = [&](int s, const uint4 &x) {
+        count_word(hl, x.x);
+        count_word(hl, x.y);
+        count_word(hl, x.z);
+        count_word(hl, x.w);
+        if (++since == kFoldSteps && s + 1 < G) {
+            fold_counts(hist, lane, true, tot);
+            since = 0;
+        }
+    };
+    for_full_steps(p, full, count_step);
+    // the partial step (or every step of an unaligned row): past K reads as
+    // exponent 0, dropped
+    for (int s = full; s < G; ++s) count_step(s, load8w(row, vec, (int64_t)s * 256 + lane * 8, K, 0u));
+    fold_counts(hist, lane, false, tot);
+    if (lane == 0) tot[0] = 0;    // exponent 0: zeros and subnormals are escapes
+    if (lane == 31) tot[7] = 0;   // exponent 255: infinities and NaNs too
+    // regroup through shared memory: lane j then holds exponents 8j..8j+7
+#pragma unroll
+    for (int m = 0; m < 8; ++m) hist[lane + 32 * m] = tot[m];
+    __syncwarp();
+    const uint4 t0 = reinterpret_cast<const uint4 *>(hist)[2 * lane], t1 = reinterpret_cast<const uint4 *>(hist)[2 * lane + 1];
+    const uint32_t h[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+    const int best_b = window_base(h, lane);
+    if (lane == 0) base[n] = (uint8_t)best_b;
+    // escapes per 256-column group (columns past K read as a weight at offset
+    // 0 of the window: never an escape)
+    const uint32_t c2 = window_c2((uint32_t)best_b), fill = (uint32_t)best_b << 7;
+    int32_t *cnt = esc_ptr + 1 + (n / 16) * G;
+    auto count_group = [&](int g, const uint4 &x) { count_group_escapes(cnt, g, x, c2, lane); };
+    for_full_steps(p, full, count_group);
+    for (int g = full; g < G; ++g) count_group(g, load8w(row, vec, (int64_t)g * 256 + lane * 8, K, fill));
+}
+
+// Longer rows: one block of 4 warps per row, warp w taking the row's
+// 256-column steps w, w+4, ...  Fewer rows are in flight (6 per SM), so the
+// second pass still finds its row in L2 (one warp per row re-read a third of
+// the 17408-column layer from HBM), and each row's fixed costs (clearing and
+// summing the table, the search) are spread over more columns.
+//
+// The histogram is a shared-memory table of 32-bit counters with one column
+// per lane index: exponent e, lane L at byte 128*e + 4L, i.e. the counter of
+// the low weight of a word x sits at (x & 0x7F80) | 4L.  So a weight costs one
+// mask and one shared-memory reduction of a constant 1: no increment to build
+// and no lane ever collides with another lane of its warp (one counter per
+// exponent took the lanes that hit the same exponent one after another).
+// Lanes of the same index in the block's four warps share a column; their
+// reductions are separate instructions and need no ordering.  Every exponent
+// is counted, 0 and 255 included; those two bins are dropped before the
+// window search.
+// ---------------------------------------------------------------------------
+constexpr int kRowWarps = 4;
+
+// hl = shared address of the table + 4 * lane
+__device__ __forceinline__ void count_word32(uint32_t hl, uint32_t x) {
+    red_add_shared(hl + (x & 0x7F80u), 1u);
+    red_add_shared(hl + ((x >> 16) & 0x7F80u), 1u);
+}
+
+// Calls f(s, x) for this warp's steps s = w, w + 4, ... below `full` of a
+// row, x = this lane's 8 weights of step s (p[32 * s]), with four of the
+// warp's steps in flight.
+template <class F>
+__device__ __forceinline__ void for_warp_steps(const uint4 *__restrict__ p, int w, int full, F &&f) {
+    int s = w;
+    if (s + 12 < full) {
+        uint4 n0 = __ldg(p + 32 * s), n1 = __ldg(p + 32 * (s + 4));
+        uint4 n2 = __ldg(p + 32 * (s + 8)), n3 = __ldg(p + 32 * (s + 12));
+        for (; s + 28 < full; s += 16) {
+            uint4 x = n0;
+            n0 = __ldg(p + 32 * (s + 16));
+            f(s, x);
+            x = n1;
+            n1 = __ldg(p + 32 * (s + 20));
+            f(s + 4, x);
+            x = n2;
+            n2 = __ldg(p + 32 * (s + 24));
+            f(s + 8, x);
+            x = n3;
+            n3 = __ldg(p + 32 * (s + 28));
+            f(s + 12, x);
+        }
+        f(s, n0);
+        f(s + 4, n1);
+        f(s + 8, n2);
+        f(s + 12, n3);
+        s += 16;
+    }
+    for (; s < full; s += 4) f(s, __ldg(p + 32 * s));
+}
+
+__global__ __launch_bounds__(kRowWarps * 32) void k_window_count_block(const uint16_t *__restrict__ W, int64_t ldw,
+                                                                 int64_t N, int64_t K, uint8_t *__restrict__ base,
+                                                                 int32_t *__restrict__ esc_ptr) {
+    __shared__ __align__(16) uint32_t hist[256 * 32];  // [exponent][lane]
+    __shared__ uint32_t tot[256];
+    __shared__ int sh_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n = blockIdx.x;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) reinterpret_cast<uint4 *>(hist)[i * 128 + tid] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    const uint16_t *row = W + n * ldw;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    const int G = (int)groups_of(K);            // 256-column steps (K < 2^31: checked on the host)
+    const int full = vec ? (int)(K >> 8) : 0;  // steps whose 8 columns are in range for every lane
+    const uint4 *p = reinterpret_cast<const uint4 *>(row) + lane;  // step s: p[32 * s]
+    const uint32_t hl = (uint32_t)__cvta_generic_to_shared(hist) + (uint32_t)lane * 4u;
+    auto count_step = [&](int, const uint4 &x) {
+        count_word32(hl, x.x);
+        count_word32(hl, x.y);
+        count_word32(hl, x.z);
+        count_word32(hl, x.w);
+    };
+    for_warp_steps(p, warp, full, count_step);
+    // the partial step (or every step of an unaligned row): past K reads as
+    // exponent 0, dropped
+    for (int s = (full > warp ? full + ((warp - full) & 3) : warp); s < G; s += 4)
+        count_step(s, load8w(row, vec, (int64_t)s * 256 + lane * 8, K, 0u));
+    __syncthreads();
+    // thread t sums exponents 2t and 2t+1 over the 32 lane columns (128-byte
+    // rows read as eight 16-byte pieces, rotated by lane: conflict-free)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = 2 * tid + h;
+        const uint4 *r = reinterpret_cast<const uint4 *>(hist + 32 * e);
+        uint32_t s = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = r[(c + lane) & 7];
+            s += v.x + v.y + v.z + v.w;
+        }
+        tot[e] = (e == 0 || e == 255) ? 0u : s;  // exponents 0 and 255 are always escapes
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint4 t0 = reinterpret_cast<const uint4 *>(tot)[2 * lane], t1 = reinterpret_cast<const uint4 *>(tot)[2 * lane + 1];
+        const uint32_t h[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        const int b = window_base(h, lane);
+        if (lane == 0) {
+            base[n] = (uint8_t)b;
+            sh_base = b;
+        }
+    }
+    __syncthreads();
+    // escapes per 256-column group (columns past K read as a weight at offset
+    // 0 of the window: never an escape)
+    const int best_b = sh_base;
+    const uint32_t c2 = window_c2((uint32_t)best_b), fill = (uint32_t)best_b << 7;
+    int32_t *cnt = esc_ptr + 1 + (n / 16) * G;
+    auto count_group = [&](int g, const uint4 &x) { count_group_escapes(cnt, g, x, c2, lane); };
+    for_warp_steps(p, warp, full, count_group);
+    for (int g = (full > warp ? full + ((warp - full) & 3) : warp); g < G; g += 4)
+        count_group(g, load8w(row, vec, (int64_t)g * 256 + lane * 8, K, fill));
 }
 
 // ---------------------------------------------------------------------------
 // a2: inclusive scan of the per-group counts in esc_ptr[1..P] (one block).
-// esc_ptr[P] = -1 flags a total that does not fit an int32 offset.
+// Tiles of up to 1024 * 43 counts go through shared memory: coalesced loads,
+// each thread sums its `per` consecutive counts (per odd: no bank
+// conflicts), the block scans the 1024 sums, each thread rewrites its counts
+// as running totals, coalesced stores.  One tile covers every layer of a
+// 27B-class model.  esc_ptr[P] = -1 flags a total that does not fit an int32
+// offset.
 // ---------------------------------------------------------------------------
+constexpr int kScanMaxPer = 43;
+constexpr int kScanMaxTile = 1024 * kScanMaxPer;
+constexpr size_t kScanSmem = (size_t)kScanMaxTile * 4;
+
 __global__ __launch_bounds__(1024) void k_ptr_scan(int32_t *__restrict__ ptr, int64_t P) {
+    extern __shared__ int32_t sv[];
     __shared__ long long warp_sums[32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     long long carry = 0;
-    for (int64_t c0 = 0; c0 < P; c0 += 1024) {
-        const int64_t i = c0 + threadIdx.x;
-        long long v = (i < P) ? (long long)ptr[i + 1] : 0;
+    for (int64_t c0 = 0; c0 < P; c0 += kScanMaxTile) {
+        const int n = (int)((P - c0) < kScanMaxTile ? (P - c0) : kScanMaxTile);
+        const int per = ((n + 1023) / 1024) | 1;
+#pragma unroll 11
+        for (int i = tid; i < n; i += 1024) sv[i] = ptr[c0 + i + 1];  // loads in flight together
+        __syncthreads();
+        const int i0 = tid * per, i1 = (i0 + per < n) ? i0 + per : n;
+        long long s = 0;
+        for (int i = i0; i < i1; ++i) s += sv[i];
+        long long x = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const long long t = __shfl_up_sync(kFull, v, o);
-            if (lane >= o) v += t;
+            const long long t = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += t;
         }
-        if (lane == 31) warp_sums[warp] = v;
+        if (lane == 31) warp_sums[warp] = x;
         __syncthreads();
         if (warp == 0) {
-            long long s = warp_sums[lane];
+            long long w = warp_sums[lane];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const long long t = __shfl_up_sync(kFull, s, o);
-                if (lane >= o) s += t;
+                const long long t = __shfl_up_sync(kFull, w, o);
+                if (lane >= o) w += t;
             }
-            warp_sums[lane] = s;
+            warp_sums[lane] = w;
         }
         __syncthreads();
-        const long long incl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + v;
-        if (i < P) ptr[i + 1] = (int32_t)(incl > 0x7fffffffLL ? -1 : incl);
+        long long r = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + x - s;
+        for (int i = i0; i < i1; ++i) {
+            r += sv[i];
+            sv[i] = (int32_t)(r > 0x7fffffffLL ? -1 : r);
+        }
         carry += warp_sums[31];
         __syncthreads();
+#pragma unroll 11
+        for (int i = tid; i < n; i += 1024) ptr[c0 + i + 1] = sv[i];
+        __syncthreads();
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         ptr[0] = 0;
         if (carry > 0x7fffffffLL) ptr[P] = -1;
     }
 }
 
 // ---------------------------------------------------------------------------
-// a3: pack.  One block per 16-row stripe, one warp per row; each step covers
-// one 256-column group (4 tiles, 8 columns per lane).  Records are assembled
-// into the tile layout in shared memory and written out as whole tiles.  An
-// escape at (tile c4, row i, column j) goes to
-//   esc_ptr[t*G+g] + #escapes of the group before (c4,i) + rank inside (c4,i)
-// with the per-(c4,i) counts exchanged through shared memory.
+// a3: pack.  One warp per unit (16-row stripe t, 256-column group g), which
+// owns tiles 4u .. 4u+3 of the planes (4 KB of hi bytes, 2 KB of lo bytes,
+// contiguous) and the unit's escapes.  Lane (r = lane/4, q = lane%4) takes
+// columns 16q..16q+15 of rows r and r+8 of each tile: exactly one 16-byte slot
+// of the hi tile per row (the hi tile is row-major, byte 64*row + column) and
+// one 16-byte slot of the lo tile, so every store is a coalesced 512-byte
+// warp store and no shared memory or block barrier is needed.  Escapes go to
+// esc_ptr[u] + (their rank in (tile, row, column) order): rows r (all lanes,
+// lane order) then rows r+8, per tile, by a warp scan of per-lane counts.
 // ---------------------------------------------------------------------------
-__global__ __launch_bounds__(512) void k_pack(const uint16_t *__restrict__ W, int64_t ldw, int64_t N,
-                                              int64_t K, const uint8_t *__restrict__ base,
-                                              const int32_t *__restrict__ esc_ptr,
-                                              uint8_t *__restrict__ hi, uint8_t *__restrict__ lo,
-                                              uint32_t *__restrict__ esc, int64_t esc_cap) {
-    __shared__ __align__(16) uint8_t sh_hi[4 * kHiTileBytes];
-    __shared__ __align__(16) uint8_t sh_lo[4 * kLoTileBytes];
-    __shared__ int sh_cnt[2][64];  // [c4*16 + i]: counts, then exclusive prefix
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t = blockIdx.x;
-    const int64_t Kp = cols_padded(K), KT = Kp / 64, G = groups_of(K);
-    const int i = warp;  // row inside the stripe
-    const int64_t n = t * 16 + i;
-    const bool row_ok = n < N;
-    const int b = row_ok ? base[n] : 0;
-    const uint16_t *row = W + (row_ok ? n : 0) * ldw;
-    const bool vec = row_ok && (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-    const int c4 = lane >> 3;         // tile inside the group
-    const int jl = (lane & 7) * 8;    // first column inside the tile
-    const int L = (i & 7) * 4 + (jl >> 4);  // fragment slot
+constexpr int kPackWarps = 4;  // 126 registers (a whole unit in flight): four 4-warp blocks per SM
 
-    for (int64_t g = 0; g < G; ++g) {
-        const int buf = (int)(g & 1);
-        const int64_t k = g * 256 + lane * 8;
-        uint16_t v[8];
-        if (row_ok) {
-            load8(row, vec, k, K, v);
-        } else {
+// Sixteen weights of a row (columns k..k+15) as eight words; columns past K
+// read as `fill`.
+__device__ __forceinline__ void load16w(const uint16_t *row, bool vec, int64_t k, int64_t K, uint32_t fill,
+                                        uint32_t x[8]) {
+    const uint4 a = load8w(row, vec, k, K, fill), b = load8w(row, vec, k + 8, K, fill);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// Hi bytes of a word's two weights (bytes 0 and 2; 1 and 3 are don't-care):
+// sign << 7 | f >> 4, i.e. the 12-bit record s<<11 | f shifted right by 4.
+__device__ __forceinline__ uint32_t hi_pair(uint32_t d, uint32_t x) {
+    return ((d >> 4) & 0x007F007Fu) | ((x >> 8) & 0xFF80FF80u);
+}
+
+// The slot's 16 hi bytes, column c at byte c.
+__device__ __forceinline__ uint4 hi_slot(const uint32_t d[8], const uint32_t x[8]) {
+    return make_uint4(prmt(hi_pair(d[0], x[0]), hi_pair(d[1], x[1]), 0x6420),
+                      prmt(hi_pair(d[2], x[2]), hi_pair(d[3], x[3]), 0x6420),
+                      prmt(hi_pair(d[4], x[4]), hi_pair(d[5], x[5]), 0x6420),
+                      prmt(hi_pair(d[6], x[6]), hi_pair(d[7], x[7]), 0x6420));
+}
+
+// A lo word of eight columns c0..c0+7: byte u = lo(c0+u) << 4 | lo(c0+u+4),
+// the record's low nibble being f & 0xF.
+__device__ __forceinline__ uint32_t lo_word(uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3) {
+    const uint32_t a = prmt(d0, d1, 0x6420), b = prmt(d2, d3, 0x6420);
+    return ((a << 4) & 0xF0F0F0F0u) | (b & 0x0F0F0F0Fu);
+}
+
+// The escapes among this lane's 16 columns of tile row `row`: written in
+// (row, column) order after the `p` entries the unit already holds, in lane
+// order across the warp; their records become 0 (d = 0x8000, sign cleared).
+// Only the lanes that hold an escape (a few per tile) walk their set bits.
+__device__ __forceinline__ void pack_escapes(uint32_t d[8], uint32_t x[8], bool any, int c4, int row, int q,
+                                             int lane, int64_t &p, uint64_t esc_lim, uint32_t *__restrict__ esc) {
+    uint32_t m = 0;  // bit c: column 16q + c is an escape
+    if (any) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0;
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t e = escape_bits(d[i]);
+            m |= (uint32_t)((e & 0xFFFFu) != 0u) << (2 * i) | (uint32_t)((e >> 16) != 0u) << (2 * i + 1);
         }
-        uint32_t rec[8];
-        unsigned emask = 0;
+    }
+    if (!__any_sync(kFull, m != 0u)) return;
+    const int cnt = __popc(m);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int64_t pos = p + incl - cnt;
+    p += __shfl_sync(kFull, incl, 31);
+    if (m == 0u) return;
+    const uint32_t key0 = (uint32_t)(c4 << 10) | (uint32_t)(row << 6) | (uint32_t)(16 * q);
+    for (uint32_t mm = m; mm; mm &= mm - 1u, ++pos) {
+        const int c = __ffs(mm) - 1;
+        // the word of column c, picked by selects (no indexed array access)
+        const uint32_t w01 = (c & 2) ? x[1] : x[0], w23 = (c & 2) ? x[3] : x[2];
+        const uint32_t w45 = (c & 2) ? x[5] : x[4], w67 = (c & 2) ? x[7] : x[6];
+        const uint32_t w03 = (c & 4) ? w23 : w01, w47 = (c & 4) ? w67 : w45;
+        const uint32_t w = (c & 8) ? w47 : w03;
+        const uint32_t v = (c & 1) ? (w >> 16) : (w & 0xFFFFu);
+        if ((uint64_t)pos < esc_lim) esc[pos] = ((key0 + (uint32_t)c) << 16) | v;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t z = ((m >> (2 * i)) & 1u ? 0x0000FFFFu : 0u) | ((m >> (2 * i + 1)) & 1u ? 0xFFFF0000u : 0u);
+        d[i] = (d[i] & ~z) | (0x80008000u & z);
+        x[i] &= ~(z & 0x80008000u);
+    }
+}
+
+__global__ __launch_bounds__(kPackWarps * 32) void k_pack(const uint16_t *__restrict__ W, int64_t ldw, int64_t N,
+                                                          int64_t K, const uint8_t *__restrict__ base,
+                                                          const int32_t *__restrict__ esc_ptr,
+                                                          uint8_t *__restrict__ hi, uint8_t *__restrict__ lo,
+                                                          uint32_t *__restrict__ esc, int64_t esc_cap,
+                                                          int64_t units, int64_t G) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t u = (int64_t)blockIdx.x * kPackWarps + warp;
+    if (u >= units) return;  // warp-uniform
+    const int64_t t = u / G, g = u - t * G;
+    const int r = lane >> 2, q = lane & 3;
+    const int64_t nA = t * 16 + r, nB = nA + 8;
+    // a padding row (n >= N) reads nothing: base 0 and fill 0 give record 0
+    const bool okA = nA < N, okB = nB < N;
+    const uint32_t bA = okA ? base[nA] : 0u, bB = okB ? base[nB] : 0u;
+    const uint32_t c2A = window_c2(bA), c2B = window_c2(bB), fA = bA << 7, fB = bB << 7;
+    const uint16_t *rowA = W + (okA ? nA : 0) * ldw, *rowB = W + (okB ? nB : 0) * ldw;
+    const int64_t KA = okA ? K : 0, KB = okB ? K : 0;
+    const bool vecA = (reinterpret_cast<uintptr_t>(rowA) & 15) == 0, vecB = (reinterpret_cast<uintptr_t>(rowB) & 15) == 0;
+    uint4 *hu = reinterpret_cast<uint4 *>(hi + u * 4096);
+    uint4 *lu = reinterpret_cast<uint4 *>(lo + u * 2048);
+    int64_t p = esc_ptr[u];
+    // entries past esc_cap are not written, and none at all if the scan
+    // flagged an offset overflow (-1)
+    const uint64_t esc_lim = esc_ptr[units] >= 0 ? (uint64_t)esc_cap : 0u;
+    // a whole unit in range and aligned is loaded up front (8 KB per warp in
+    // flight) with plain 16-byte loads; a ragged or padding edge, or an
+    // unaligned row, takes bounds-checked loads per tile (warp-uniform choice)
+    const bool fast = okB && vecA && vecB && (g + 1) * 256 <= K;
+    uint4 A[8], B[8];
+    if (fast) {
+        const uint4 *pa = reinterpret_cast<const uint4 *>(rowA + g * 256 + 16 * q);
+        const uint4 *pb = reinterpret_cast<const uint4 *>(rowB + g * 256 + 16 * q);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const bool in = row_ok && (k + j < K);
-            const uint32_t f = window_field(v[j], b);
-            const bool esc_ = in && f > 0x7FFu;
-            if (esc_) emask |= 1u << j;
-            rec[j] = (in && !esc_) ? ((uint32_t)(v[j] >> 15) << 11) | f : 0u;  // s<<11 | (e-b)<<7 | m
+            A[j] = __ldg(pa + 8 * (j >> 1) + (j & 1));
+            B[j] = __ldg(pb + 8 * (j >> 1) + (j & 1));
         }
-        // per-(c4, i) count and this lane's exclusive prefix inside its 8 lanes
-        const int cnt = __popc(emask);
-        int incl = cnt;
+    }
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-            const int tmp = __shfl_up_sync(kFull, incl, o, 8);
-            if ((lane & 7) >= o) incl += tmp;
+    for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t xa[8], xb[8];
+        if (fast) {
+            const uint4 u0 = A[2 * c4], u1 = A[2 * c4 + 1], v0 = B[2 * c4], v1 = B[2 * c4 + 1];
+            xa[0] = u0.x, xa[1] = u0.y, xa[2] = u0.z, xa[3] = u0.w, xa[4] = u1.x, xa[5] = u1.y, xa[6] = u1.z, xa[7] = u1.w;
+            xb[0] = v0.x, xb[1] = v0.y, xb[2] = v0.z, xb[3] = v0.w, xb[4] = v1.x, xb[5] = v1.y, xb[6] = v1.z, xb[7] = v1.w;
+        } else {
+            const int64_t k = g * 256 + c4 * 64 + 16 * q;
+            load16w(rowA, vecA, k, KA, fA, xa);
+            load16w(rowB, vecB, k, KB, fB, xb);
         }
-        if ((lane & 7) == 7) sh_cnt[buf][c4 * 16 + i] = incl;
-        if (k < Kp) {
-            const uint32_t h0 = (rec[0] >> 4) | ((rec[1] >> 4) << 8) | ((rec[2] >> 4) << 16) | ((rec[3] >> 4) << 24);
-            const uint32_t h1 = (rec[4] >> 4) | ((rec[5] >> 4) << 8) | ((rec[6] >> 4) << 16) | ((rec[7] >> 4) << 24);
-            *reinterpret_cast<uint2 *>(sh_hi + c4 * kHiTileBytes + (i >> 3) * 512 + L * 16 + (jl & 15)) =
-                make_uint2(h0, h1);
-            uint32_t lw = 0;
+        uint32_t da[8], db[8], ea = 0, eb = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) lw |= (((rec[u] & 0xFu) << 4) | (rec[u + 4] & 0xFu)) << (8 * u);
-            *reinterpret_cast<uint32_t *>(sh_lo + c4 * kLoTileBytes + L * 16 + (i >> 3) * 8 + ((jl & 15) >> 3) * 4) = lw;
+        for (int i = 0; i < 8; ++i) {
+            da[i] = window_word(xa[i], c2A);
+            db[i] = window_word(xb[i], c2B);
+            ea |= escape_bits(da[i]);
+            eb |= escape_bits(db[i]);
         }
-        __syncthreads();
-        if (warp == 0) {  // exclusive scan of the 64 counts in (c4, i) order
-            const int a0 = sh_cnt[buf][2 * lane], a1 = sh_cnt[buf][2 * lane + 1];
-            int s = a0 + a1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int tmp = __shfl_up_sync(kFull, s, o);
-                if (lane >= o) s += tmp;
-            }
-            const int ex = s - a0 - a1;
-            sh_cnt[buf][2 * lane] = ex;
-            sh_cnt[buf][2 * lane + 1] = ex + a0;
+        if (__any_sync(kFull, (ea | eb) != 0u)) {
+            pack_escapes(da, xa, ea != 0u, c4, r, q, lane, p, esc_lim, esc);
+            pack_escapes(db, xb, eb != 0u, c4, r + 8, q, lane, p, esc_lim, esc);
         }
-        const int64_t c_first = g * 4;
-        const int ntiles = (int)((KT - c_first) < 4 ? (KT - c_first) : 4);
-        for (int x = threadIdx.x; x < ntiles * 96; x += blockDim.x) {
-            if (x < ntiles * 64) {
-                const int ct = x >> 6, o = x & 63;
-                reinterpret_cast<uint4 *>(hi + (t * KT + c_first + ct) * kHiTileBytes)[o] =
-                    reinterpret_cast<const uint4 *>(sh_hi + ct * kHiTileBytes)[o];
-            } else {
-                const int y = x - ntiles * 64;
-                const int ct = y >> 5, o = y & 31;
-                reinterpret_cast<uint4 *>(lo + (t * KT + c_first + ct) * kLoTileBytes)[o] =
-                    reinterpret_cast<const uint4 *>(sh_lo + ct * kLoTileBytes)[o];
-            }
-        }
-        __syncthreads();
-        if (emask) {
-            int64_t pos = (int64_t)esc_ptr[t * G + g] + sh_cnt[buf][c4 * 16 + i] + (incl - cnt);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if ((emask >> j) & 1u) {
-                    if (pos < esc_cap)
-                        esc[pos] = ((uint32_t)((c4 << 10) | (i << 6) | (jl + j)) << 16) | v[j];
-                    ++pos;
-                }
-            }
-        }
+        hu[c4 * 64 + lane] = hi_slot(da, xa);
+        hu[c4 * 64 + 32 + lane] = hi_slot(db, xb);
+        lu[c4 * 32 + lane] = make_uint4(lo_word(da[0], da[1], da[2], da[3]), lo_word(da[4], da[5], da[6], da[7]),
+                                        lo_word(db[0], db[1], db[2], db[3]), lo_word(db[4], db[5], db[6], db[7]));
     }
 }
 
@@ -371,22 +707,41 @@ __global__ void k_check_entries(TensorView t, unsigned long long *__restrict__ b
 cudaError_t launch_window_count(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base,
                                 int32_t *esc_ptr, cudaStream_t s) {
     if (N == 0) return cudaSuccess;
-    const int64_t blocks = (N + kWinWarps - 1) / kWinWarps;
-    k_window_count<<<(unsigned)blocks, kWinWarps * 32, 0, s>>>(W, ldw, N, K, base, esc_ptr);
+    if (K > kLongRow)
+        k_window_count_block<<<(unsigned)N, kRowWarps * 32, 0, s>>>(W, ldw, N, K, base, esc_ptr);
+    else
+        k_window_count_warp<<<(unsigned)N, 32, 0, s>>>(W, ldw, N, K, base, esc_ptr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_ptr_scan(int32_t *esc_ptr, int64_t P, cudaStream_t s) {
-    k_ptr_scan<<<1, 1024, 0, s>>>(esc_ptr, P);
+    // the kernel's shared-memory limit, raised once per device (several host
+    // threads may encode at once)
+    static std::mutex m;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(m);
+        if (dev < 0 || dev >= 64 || !configured[dev]) {
+            e = cudaFuncSetAttribute(k_ptr_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) configured[dev] = true;
+        }
+    }
+    const int64_t tile = P < kScanMaxTile ? P : kScanMaxTile;
+    k_ptr_scan<<<1, 1024, (size_t)tile * 4, s>>>(esc_ptr, P);
     return cudaGetLastError();
 }
 
 cudaError_t launch_pack(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const uint8_t *base,
                         const int32_t *esc_ptr, uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap,
                         cudaStream_t s) {
-    const int64_t stripes = rows_padded(N) / 16;
-    if (stripes == 0 || K == 0) return cudaSuccess;
-    k_pack<<<(unsigned)stripes, 512, 0, s>>>(W, ldw, N, K, base, esc_ptr, hi, lo, esc, esc_cap);
+    const int64_t G = groups_of(K), units = rows_padded(N) / 16 * G;
+    if (units == 0) return cudaSuccess;
+    const int64_t blocks = (units + kPackWarps - 1) / kPackWarps;
+    k_pack<<<(unsigned)blocks, kPackWarps * 32, 0, s>>>(W, ldw, N, K, base, esc_ptr, hi, lo, esc, esc_cap, units, G);
     return cudaGetLastError();
 }
 

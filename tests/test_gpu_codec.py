@@ -249,3 +249,25 @@ def test_full_size_encode_bytes_match_the_oracle_on_sampled_stripes(name, N, K, 
         assert np.array_equal(got["base"], ref.base), s
         assert np.array_equal(got["esc_ptr"], ref.esc_ptr), s
         assert np.array_equal(got["esc"], ref.esc[:ref.n_esc]), s
+
+
+def test_encode_into_preallocated_tensor(w12lib, oracle):
+    """w12_encode(W, out=t) reuses t's buffers: two different tensors of the
+    same shape encoded one after the other into the same buffers, each equal
+    to the oracle's bytes; a tensor that needs more escapes than t holds
+    raises W12_ERR_CAPACITY."""
+    N, K = 40, 520
+    pre = w12lib.empty_tensor(N, K, 4096, "cuda")
+    for seed in (21, 22):
+        W = synth.adversarial_weights(N, K, seed=seed)
+        st, ref = oracle.encode(W)
+        t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"), out=pre)
+        torch.cuda.synchronize()
+        assert t is pre and t.n_esc == ref.n_esc
+        g = host_view(t)
+        for key in ("hi", "lo", "base", "esc_ptr", "esc"):
+            assert np.array_equal(g[key], getattr(ref, key)), key
+    small = w12lib.empty_tensor(N, K, 8, "cuda")
+    with pytest.raises(w12lib.W12Error) as ei:
+        w12lib.w12_encode(synth.bits_to_tensor(synth.adversarial_weights(N, K, seed=23), "cuda"), out=small)
+    assert ei.value.status == w12lib.W12_ERR_CAPACITY
