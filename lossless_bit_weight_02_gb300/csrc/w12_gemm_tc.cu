@@ -225,6 +225,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Thread-block clusters (the split-K CTAs of one row tile): rank in the
+// cluster, a cluster-wide barrier (every thread of every CTA), and 16-byte
+// loads from another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_cluster4(uint32_t local_addr, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+
 // Byte offset of (row r, 16-byte chunk c) in a K-major 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
@@ -251,7 +273,7 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
 // before any of them decodes a tile of the next item, so no MMA of the next
 // item can overwrite it early.  The item, its chunk bounds and the order of
 // the split-K sum depend on (M, N, K) only, never on the grid.
-template <int D, bool SILU, bool PERSIST>
+template <int D, bool SILU, bool PERSIST, bool CLUSTER>
 __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_gemm_tc(
     TensorView t, GemmArgs g, TcParams tp, const __grid_constant__ CUtensorMap tmap,
     const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap lmap) {
@@ -295,20 +317,56 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
         g_end = ((s + 1) * t.G) / S;
     };
 
-    // the descriptors of the first copies load while the barriers are set up
-    if (lane == 0) {
-        if (warp == kWProdWarp) {
-            prefetch_tmap(&hmap);
-            if (!g.nested8) prefetch_tmap(&lmap);
-        } else if (warp == kBProdWarp) {
-            prefetch_tmap(&tmap);
+    // The first item starts at once, while the other barriers and TMEM are
+    // set up: the decoders load its bases and group offsets (kept raw until
+    // after the setup barrier, so no warp waits for them there; the escape
+    // entries, which need the offsets, follow in the item loop), and the
+    // weight producer initialises its own ring's barriers and issues the
+    // first ring-full of plane copies.  Both read only the W12 tensor.
+    int pre_ptrw = 0;
+    uint32_t pre_bA = 0, pre_bB = 0;
+    if (warp < kDecWarps && (int)blockIdx.x < items) {
+        int64_t tt0, gb0, ge0;
+        item_span((int)blockIdx.x, tt0, gb0, ge0);
+        const int64_t st0 = tt0 * 8 + (warp & 7);
+        if (st0 < T && ge0 > gb0) {
+            const int gi = (int)gb0 + lane;
+            if (gi <= (int)ge0) pre_ptrw = __ldg(t.esc_ptr + st0 * t.G + gi);
+            const int64_t nA = st0 * 16 + (lane >> 2), nB = nA + 8;
+            if (nA < t.N) pre_bA = __ldg(t.base + nA);
+            if (nB < t.N) pre_bB = __ldg(t.base + nB);
         }
     }
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < RW; ++i) {
-            mbar_init(&w_full[i], 1);                // the producer's expect_tx
-            mbar_init(&w_empty[i], 8);   // one arrival per stripe's decoder warp of the k-block
+    int pre_issued = 0;  // plane copies of the first item already in flight
+    if (warp == kWProdWarp) {
+        if (lane == 0) {
+            prefetch_tmap(&hmap);
+            if (!g.nested8) prefetch_tmap(&lmap);
+            for (int i = 0; i < RW; ++i) {
+                mbar_init(&w_full[i], 1);    // the producer's expect_tx
+                mbar_init(&w_empty[i], 8);   // one arrival per stripe's decoder warp of the k-block
+            }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
+        if ((int)blockIdx.x < items) {
+            int64_t tt0, gb0, ge0;
+            item_span((int)blockIdx.x, tt0, gb0, ge0);
+            const int nkb0 = (int)(4 * (ge0 - gb0));
+            pre_issued = nkb0 < RW ? nkb0 : RW;
+            if (lane == 0) {  // the ring is empty: no slot to wait for
+                for (int kb = 0; kb < pre_issued; ++kb) {
+                    mbar_expect_tx(&w_full[kb], g.nested8 ? 8192u : kWStageBytes);
+                    uint8_t *dst = w_st + kb * kWStageBytes;
+                    tma_load_4d(dst, &hmap, (int)(4 * gb0) + kb, (int)(tt0 * 8), &w_full[kb]);
+                    if (!g.nested8) tma_load_4d(dst + 8192, &lmap, (int)(4 * gb0) + kb, (int)(tt0 * 8), &w_full[kb]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kBProdWarp && lane == 0) {
+        prefetch_tmap(&tmap);
+    }
+    if (threadIdx.x == 0) {
         for (int i = 0; i < RA; ++i) {
             mbar_init(&a_full[i], 8);
             mbar_init(&a_empty[i], 1);               // tcgen05.commit
@@ -381,7 +439,7 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
                 }
                 return v;
             };
-            int ptrw = load_window(gw0);
+            int ptrw = it == 0 ? (pre_ptrw < 0 ? 0 : (pre_ptrw > n_esc ? n_esc : pre_ptrw)) : load_window(gw0);
             auto bounds = [&](int64_t gg64, int &p0, int &p1) {
                 const int gg = (int)gg64;
                 if (gg + 1 - gw0 >= 32) {  // slide the window (more than 30 groups per chunk)
@@ -393,9 +451,14 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
                 if (p1 < p0) p1 = p0;
             };
             if (live && nkb > 0) {
-                const int64_t nA = st * 16 + gid, nB = nA + 8;
-                base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
-                base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
+                if (it == 0) {
+                    base2A = pre_bA * 0x00800080u;
+                    base2B = pre_bB * 0x00800080u;
+                } else {
+                    const int64_t nA = st * 16 + gid, nB = nA + 8;
+                    base2A = (nA < t.N ? (uint32_t)__ldg(t.base + nA) : 0u) * 0x00800080u;
+                    base2B = (nB < t.N ? (uint32_t)__ldg(t.base + nB) : 0u) * 0x00800080u;
+                }
                 int p0, p1;
                 bounds(g_beg, p0, p1);
                 cur = load_group_escapes(t, p0, p1, lane);
@@ -504,6 +567,10 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
                                 if (m < g.M) g.Y[(int64_t)m * g.ldy + n] = f32_to_bf16_rn(v[j]);
                             }
                         }
+                    } else if (CLUSTER) {  // the CTA's partial [m][128 rows] in its own shared memory
+                        float *part = reinterpret_cast<float *>(base);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) part[(16 * c + j) * 128 + 32 * quarter + lane] = v[j];
                     } else if (n < t.Np) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
@@ -514,9 +581,9 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
             // every decoder warp is done reading the accumulator before any of
             // them hands the MMA warp a tile of the next item
             tc_fence_before();
-            if (S > 1) __threadfence();
+            if (S > 1 && !CLUSTER) __threadfence();
             asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
-            if (S > 1) {
+            if (S > 1 && !CLUSTER) {
                 // fixed-order combination by the last CTA of this row tile
                 if (threadIdx.x == 0) *last_flag = have ? (atomicAdd(&g.counters[tt], 1) == S - 1) : 0;
                 asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
@@ -601,6 +668,10 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
             item_span(item, tt, g_beg, g_end);
             const int nkb = (int)(4 * (g_end - g_beg));
             for (int kb = 0; kb < nkb; ++kb, wp.advance(1, RW)) {
+                if (item == (int)blockIdx.x && kb < pre_issued) {  // issued before the setup barrier
+                    ++issued;
+                    continue;
+                }
                 const int ws = wp.stage;
                 if (!__all_sync(kFull, mbar_wait(&w_empty[ws], wp.phase ^ 1u, abort_flag, g.error))) {
                     ok = false;
@@ -697,6 +768,67 @@ __global__ __launch_bounds__(Roles<D>::kThreads, Roles<D>::kCtasPerSm) void k_ge
 
     tc_fence_before();
     __syncthreads();
+    if (CLUSTER) {
+        // The S CTAs of row tile tt form one cluster (rank = chunk s).  Each
+        // has its FP32 partial [m][128] in its own shared memory; after the
+        // barrier the cluster combines them, CTA r taking the rows m = r,
+        // r + S, ...: every output is summed over s = 0..S-1 in that order,
+        // exactly as the global-memory path does.
+        cluster_sync();
+        if (warp < kDecWarps) {
+            const int r = (int)cluster_ctarank();
+            const int64_t tt = (int64_t)blockIdx.x / S;
+            const int qd = threadIdx.x & 31, rs = threadIdx.x >> 5;
+            const int64_t n0 = tt * 128 + 4 * qd;  // this thread's 4 weight rows
+            const uint32_t local = smem_addr(base) + (uint32_t)qd * 16u;
+            const int mmax = Mp < (int)g.M ? Mp : (int)g.M;
+            for (int m = r + S * rs; m < mmax; m += S * kDecWarps) {
+                const uint32_t row = local + (uint32_t)m * 512u;
+                if (!SILU) {
+                    if (n0 >= t.N) continue;
+                    float4 p[8];
+#pragma unroll
+                    for (int ss = 0; ss < 8; ++ss)
+                        if (ss < S) p[ss] = ld_cluster4(row, (uint32_t)ss);
+                    float4 acc = p[0];
+#pragma unroll
+                    for (int ss = 1; ss < 8; ++ss) {
+                        if (ss < S) {
+                            acc.x += p[ss].x;
+                            acc.y += p[ss].y;
+                            acc.z += p[ss].z;
+                            acc.w += p[ss].w;
+                        }
+                    }
+                    const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (n0 + i < t.N) g.Y[(int64_t)m * g.ldy + n0 + i] = f32_to_bf16_rn(a[i]);
+                } else {
+                    // gate rows 16h..16h+7, up rows 16h+8..16h+15: a gate quad
+                    // takes its up quad 8 rows on (N % 16 == 0)
+                    if ((qd & 2) || n0 >= t.N) continue;
+                    float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {  // gate rows, then up rows
+                        float4 pp[8];
+#pragma unroll
+                        for (int ss = 0; ss < 8; ++ss)
+                            if (ss < S) pp[ss] = ld_cluster4(row + 32u * h, (uint32_t)ss);
+                        float *a = h ? au : ag;
+#pragma unroll
+                        for (int ss = 0; ss < 8; ++ss)
+                            if (ss < S) a[0] += pp[ss].x, a[1] += pp[ss].y, a[2] += pp[ss].z, a[3] += pp[ss].w;
+                    }
+                    const int64_t col = (n0 >> 4) * 8 + (n0 & 15);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        g.Y[(int64_t)m * g.ldy + col + i] = f32_to_bf16_rn(silu_f32(ag[i]) * au[i]);
+                }
+            }
+        }
+        cluster_sync();  // no CTA leaves while another still reads its partial
+    }
     if (warp == kWProdWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tp.tmem_cols)
@@ -1306,38 +1438,44 @@ int64_t tc_split_for(int64_t T, int64_t G, int64_t Mp, int64_t K, int64_t slots)
 }
 
 // the kernel of a launch: K-chunks or balanced ranges, plain or with the
-// fused gate/up epilogue
-template <int D, bool Ranges, bool SILU, bool PERSIST>
+// fused gate/up epilogue; K-chunks with the split-K sum in global memory or
+// across a cluster
+template <int D, bool Ranges, bool SILU, bool PERSIST, bool CLUSTER>
 struct TcKernel {
-    static constexpr auto fn = k_gemm_tc<D, SILU, PERSIST>;
+    static constexpr auto fn = k_gemm_tc<D, SILU, PERSIST, CLUSTER>;
 };
-template <int D, bool SILU, bool PERSIST>
-struct TcKernel<D, true, SILU, PERSIST> {
+template <int D, bool SILU, bool PERSIST, bool CLUSTER>
+struct TcKernel<D, true, SILU, PERSIST, CLUSTER> {
     static constexpr auto fn = k_gemm_tc_ranges<D, SILU, PERSIST>;
 };
 
-template <int D, bool Ranges, bool SILU, bool PERSIST>
+// Raises the kernel's shared-memory limit, once per kernel and device
+// (several host threads may launch at once).
+template <auto kern>
+cudaError_t configure_smem(size_t budget, int dev) {
+    static std::mutex configured_mutex;
+    static int configured[64] = {0};
+    std::lock_guard<std::mutex> lock(configured_mutex);
+    if (dev < 0 || dev >= 64 || configured[dev] < (int)budget) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = (int)budget;
+    }
+    return cudaSuccess;
+}
+
+template <int D, bool Ranges, bool SILU, bool PERSIST, bool CLUSTER>
 cudaError_t launch_one(const TensorView &t, const GemmArgs &g, const TcParams &tp, const CUtensorMap &map,
                            const CUtensorMap &hmap, const CUtensorMap &lmap, cudaStream_t s) {
-    constexpr auto kern = TcKernel<D, Ranges, SILU, PERSIST>::fn;
+    constexpr auto kern = TcKernel<D, Ranges, SILU, PERSIST, CLUSTER>::fn;
     const size_t smem = tc_smem_bytes(tp);
     const size_t budget = tc_smem_budget(Roles<D>::kCtasPerSm);
     if (smem > budget) return cudaErrorInvalidConfiguration;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // the kernel's shared-memory limit, raised once per device (several host
-    // threads may launch at once)
-    static std::mutex configured_mutex;
-    static int configured[64] = {0};
-    {
-        std::lock_guard<std::mutex> lock(configured_mutex);
-        if (dev < 0 || dev >= 64 || configured[dev] < (int)smem) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
-            if (e != cudaSuccess) return e;
-            if (dev >= 0 && dev < 64) configured[dev] = (int)budget;
-        }
-    }
+    e = configure_smem<kern>(budget, dev);
+    if (e != cudaSuccess) return e;
     // one CTA per range, or per (row tile, K-chunk) item; a capped grid
     // walks the same items in the same cut (the result does not change)
     int64_t blocks = Ranges ? g.ranges : ((t.Np + 127) / 128) * (int64_t)g.split;
@@ -1348,23 +1486,81 @@ cudaError_t launch_one(const TensorView &t, const GemmArgs &g, const TcParams &t
     cfg.blockDim = dim3(Roles<D>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (g.overlap) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (CLUSTER) {  // the split's S CTAs of a row tile (consecutive items) form one cluster
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)g.split;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = g.overlap ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, t, g, tp, map, hmap, lmap);
 }
 
+// Whether the K-chunk build can sum its split across clusters: 2..8 chunks
+// (a portable cluster), the FP32 partial [Mpad][128] fits the dynamic shared
+// memory, and every cluster of the grid can be resident at once (a grid that
+// no longer fits in one wave would lose more than the sum saves).  The
+// answer depends on (device, build, split, Mpad) and is cached.
+template <int D, bool SILU>
+bool cluster_split_ok(const TensorView &t, const GemmArgs &g, const TcParams &tp) {
+    const int S = g.split;
+    if (S < 2 || S > 8) return false;
+    const size_t smem = tc_smem_bytes(tp);
+    if (smem < 1024 + 512 * (size_t)tp.Mp) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    const int64_t grid = ((t.Np + 127) / 128) * (int64_t)S;
+    static std::mutex m;
+    static int cached[64][9][17] = {};  // [device][split][Mpad / 16]: 0 unknown, else max resident clusters + 1
+    const int mi = (int)(tp.Mp / 16);
+    if (mi < 1 || mi > 16) return false;
+    std::lock_guard<std::mutex> lock(m);
+    int &c = cached[dev][S][mi];
+    if (c == 0) {
+        constexpr auto kern = TcKernel<D, false, SILU, false, true>::fn;
+        if (configure_smem<kern>(tc_smem_budget(Roles<D>::kCtasPerSm), dev) != cudaSuccess) return false;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)S);
+        cfg.blockDim = dim3(Roles<D>::kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        c = n + 1;
+    }
+    return (int64_t)(c - 1) * S >= grid;
+}
+
 // One CTA per item, or (max_ctas below the item count) a capped grid of
-// CTAs that walk several items each.
+// CTAs that walk several items each; an uncapped K-chunk split sums across
+// clusters where it can (bitwise the same result).
 template <int D, bool Ranges, bool SILU>
 cudaError_t launch_variant(const TensorView &t, const GemmArgs &g, const TcParams &tp, const CUtensorMap &map,
                            const CUtensorMap &hmap, const CUtensorMap &lmap, cudaStream_t s) {
     const int64_t items = Ranges ? g.ranges : ((t.Np + 127) / 128) * (int64_t)g.split;
     if (g.max_ctas > 0 && g.max_ctas < items)
-        return launch_one<D, Ranges, SILU, true>(t, g, tp, map, hmap, lmap, s);
-    return launch_one<D, Ranges, SILU, false>(t, g, tp, map, hmap, lmap, s);
+        return launch_one<D, Ranges, SILU, true, false>(t, g, tp, map, hmap, lmap, s);
+    if (!Ranges && cluster_split_ok<D, SILU>(t, g, tp))
+        return launch_one<D, false, SILU, false, true>(t, g, tp, map, hmap, lmap, s);
+    return launch_one<D, Ranges, SILU, false, false>(t, g, tp, map, hmap, lmap, s);
 }
 
 }  // namespace
