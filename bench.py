@@ -5,11 +5,13 @@ and the fraction of the HBM roofline, on the four GEMMs of a 27B-class dense
 decoder layer (QKV 5120->7168, O 5120->5120, gate/up 5120->34816,
 down 17408->5120).
 
-One step = the four layer GEMMs at each of M = 1, 2, 4, 8: 16 w12_gemm calls
-chained by programmatic dependent launch (STEP_FORM; the same GEMMs as one
-w12_gemm_list call, each reading its activations after the previous GEMM has
-completed, are timed beside it), weights resident in HBM as W12, synthetic
-BF16 activations.  The
+One step = the four layer GEMMs at each of M = 1, 2, 4, 8: four independent
+requests, each a chain of its four layer GEMMs (16 w12_gemm calls; a request's
+chain runs on its own stream, its GEMMs chained by programmatic dependent
+launch; STEP_FORM).  The same GEMMs as one chain on one stream, and as one
+w12_gemm_list call, each GEMM reading its activations after the previous one
+has completed, are timed beside it.  Weights resident in HBM as W12,
+synthetic BF16 activations.  The
 per-step working set (4 x 496 MB of W12) is larger than the 129 MB L2 and the
 layers are visited round-robin, so every weight tensor is re-read only after
 at least 228 MB of other weights have passed through L2.
@@ -35,8 +37,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 M_VALUES = (1, 2, 4, 8)
-# the form of the timed step: "calls" (16 w12_gemm calls chained by
-# programmatic dependent launch) or "list" (one w12_gemm_list call)
+# the form of the timed step: "calls" (16 w12_gemm calls, one stream per
+# request, each request's chain by programmatic dependent launch) or "list"
+# (one w12_gemm_list call)
 STEP_FORM = "calls"
 SWEEP_M = (16, 24, 32, 63, 64, 128, 256)  # tree / batch verification rows
 METRIC = "W12 GEMM weight-GB/s & % HBM roofline at M=1/16/64 (27B-class layers)"
@@ -223,7 +226,7 @@ def run_gpu(args):
              for M in Ms for name, t in layers}
 
     def calls_step(ev=None, m_values=M_VALUES):
-        """The step as 16 w12_gemm calls chained by programmatic dependent launch."""
+        """The 16 w12_gemm calls as one chain on one stream (programmatic dependent launch)."""
         j = 0
         for M in m_values:
             for name, t in layers:
@@ -234,22 +237,57 @@ def run_gpu(args):
                     ev[j][1].record(stream)
                 j += 1
 
+    # The step as four requests on four streams: request j's four layer GEMMs
+    # run as a chain on stream j (programmatic dependent launch inside it, a
+    # workspace of its own), so a GEMM of one request can take over the SMs
+    # another request's GEMM is draining.  The streams fork from and join back
+    # into `stream` every step, so events on `stream` bracket whole steps.
+    ws_bytes = max(w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in M_VALUES for _, t in layers)
+
+    class RequestStreams:
+        def __init__(self, main, a_of, o_of):
+            self.main = main
+            self.streams = [torch.cuda.Stream(dev) for _ in M_VALUES]
+            self.fork = torch.cuda.Event()
+            self.joins = [torch.cuda.Event() for _ in M_VALUES]
+            # one workspace per request: its chain's GEMMs run one after another
+            self.ws = [w12.Workspace(dev, ws_bytes) for _ in M_VALUES]
+            self.calls = [[w12.GemmCall(a_of[(M, name)], t, o_of[(M, name)], ws, stream=st, opts=overlap)
+                           for name, t in layers]
+                          for M, st, ws in zip(M_VALUES, self.streams, self.ws)]
+
+        def __call__(self):
+            self.fork.record(self.main)
+            for st in self.streams:
+                st.wait_event(self.fork)
+            for chain in self.calls:
+                for c in chain:
+                    c()
+            for st, ev in zip(self.streams, self.joins):
+                ev.record(st)
+                self.main.wait_event(ev)
+
+    streams_step = RequestStreams(stream, acts, outs)
+
     # The step as one w12_gemm_list call: the 16 GEMMs in one persistent
     # launch, each reading its activations only after the GEMM before it has
     # completed (the dependency a chain of layer GEMMs has).
     step_keys = [(M, name) for M in M_VALUES for name, _ in layers]
     tensor_of = dict(layers)
     wsl = w12.Workspace(dev)
-    list_call = w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], j - 1, 0) for j, k in enumerate(step_keys)],
+    # a request's first GEMM depends on nothing; each later one on the one before it
+    list_after = [j - 1 if j % len(layers) else -1 for j in range(len(step_keys))]
+    list_call = w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], list_after[j], 0) for j, k in enumerate(step_keys)],
                                  wsl, stream=stream)
 
     # Both forms of the step are timed over the same number of steps; the
     # headline `value` is STEP_FORM's, the other is reported beside it.
-    forms = {"calls": (calls_step, len(step_keys), "k_gemm_mma<1> (w12_gemm, M<=8)",
-                       "16 w12_gemm calls chained by programmatic dependent launch"),
+    forms = {"calls": (streams_step, len(step_keys), "k_gemm_mma<1> (w12_gemm, M<=8)",
+                       "16 w12_gemm calls: each request's (M's) four layer GEMMs chained by programmatic "
+                       "dependent launch on a stream of its own, the four requests' streams concurrent"),
              "list": (list_call, 1, "k_gemm_mma_list<1> (w12_gemm_list, M<=8)",
-                      "one w12_gemm_list call over the 16 GEMMs, each reading its activations after the "
-                      "GEMM before it has completed")}
+                      "one w12_gemm_list call over the 16 GEMMs, each of a request's later layers reading its "
+                      "activations after the request's GEMM before it has completed")}
     other_form = "list" if STEP_FORM == "calls" else "calls"
     one_step, launches_per_step, step_kernel, step_note = forms[STEP_FORM]
     other_step = forms[other_form][0]
@@ -292,6 +330,14 @@ def run_gpu(args):
     c1.record(stream)
     torch.cuda.synchronize()
     other_ms = c0.elapsed_time(c1) / args.steps
+    # ... and the 16 calls as one chain on one stream (every GEMM after the one
+    # before it, the four requests serialised)
+    c0.record(stream)
+    for k in range(args.steps):
+        calls_step()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    chain_ms = c0.elapsed_time(c1) / args.steps
 
     # Per-launch events of the 16-call step on 10 more steps: an event
     # between two launches keeps the second from overlapping the first, so
@@ -324,11 +370,10 @@ def run_gpu(args):
     # fixed sequence of GEMMs): 10 steps per graph, on a side stream
     gstream = torch.cuda.Stream(dev)
     if STEP_FORM == "list":
-        gcalls = [w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], j - 1, 0) for j, k in enumerate(step_keys)],
-                                   w12.Workspace(dev), stream=gstream)]
+        gcalls = [w12.GemmListCall([(acts[k], tensor_of[k[1]], outs[k], list_after[j], 0)
+                                    for j, k in enumerate(step_keys)], w12.Workspace(dev), stream=gstream)]
     else:
-        gcalls = [w12.GemmCall(acts[k], tensor_of[k[1]], outs[k], wsp, stream=gstream, opts=overlap)
-                  for k in step_keys]
+        gcalls = [RequestStreams(gstream, acts, outs)]  # the streams fork from and join the capture stream
     with torch.cuda.stream(gstream):
         for c in gcalls:
             c()
@@ -361,8 +406,9 @@ def run_gpu(args):
     kern_ms = sum(sum(v) for v in dur.values())
     kern_bytes = sum(alg_bytes[key] * len(v) for key, v in dur.items())
     achieved_serial = kern_bytes / (kern_ms * 1e-3) / 1e9
-    # The step's only kernel is k_gemm_mma<1> (16 launches that overlap by
-    # programmatic dependent launch) or k_gemm_mma_list<1> (one launch), so
+    # The step's only kernel is k_gemm_mma<1> (16 launches that overlap:
+    # programmatic dependent launch inside a request's chain, the requests'
+    # streams side by side) or k_gemm_mma_list<1> (one launch), so
     # the kernel's device time per step is the step's device time, and the
     # roofline's achieved rate is the step's algorithmic bytes over it.
     step_alg_bytes = sum(alg_bytes[(M, n)] for M in M_VALUES for n, _ in layers)
@@ -437,9 +483,8 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host buffers ----
     # Every step copies all of its activations host -> device in one copy (from
-    # pinned memory), runs the 16 GEMMs through the public call (one
-    # w12_gemm_list call, as in the device step), and reads all the outputs
-    # back in one copy.
+    # pinned memory), runs the 16 GEMMs through the public call (in the device
+    # step's form), and reads all the outputs back in one copy.
     keys = [(M, name) for M in M_VALUES for name, _ in layers]
     align = lambda n: (n + 7) // 8 * 8  # 16-byte aligned views
     in_off, out_off, n_in, n_out = {}, {}, 0, 0
@@ -458,11 +503,13 @@ def run_gpu(args):
         t = dict(layers)[key[1]]
         d_a = d_in_all[in_off[key]:in_off[key] + a.numel()].view(a.shape)
         d_o = d_out_all[out_off[key]:out_off[key] + o.numel()].view(o.shape)
-        e2e_entries.append((d_a, t, d_o, j - 1, 0))
+        e2e_entries.append((d_a, t, d_o, list_after[j], 0))
     if STEP_FORM == "list":
         e2e_calls = [w12.GemmListCall(e2e_entries, w12.Workspace(dev), stream=stream)]
     else:
-        e2e_calls = [w12.GemmCall(a, t, o, wsp, stream=stream, opts=overlap) for a, t, o, _, _ in e2e_entries]
+        e2e_a = {key: e[0] for key, e in zip(keys, e2e_entries)}
+        e2e_o = {key: e[2] for key, e in zip(keys, e2e_entries)}
+        e2e_calls = [RequestStreams(stream, e2e_a, e2e_o)]
     h2d = sum(acts[key].numel() * 2 for key in keys)
     d2h = sum(outs[key].numel() * 2 for key in keys)
 
@@ -757,6 +804,10 @@ def run_gpu(args):
         "step_form": {"headline": STEP_FORM, "note": step_note,
                       other_form: {"value": round(step_bytes / (other_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                                    "ms_per_step": round(other_ms, 4), "note": forms[other_form][3]},
+                      "one_stream_chain": {"value": round(step_bytes / (chain_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                                           "ms_per_step": round(chain_ms, 4),
+                                           "note": "the 16 w12_gemm calls as one chain on one stream (every GEMM "
+                                                   "after the one before it, the requests serialised)"},
                       "list_matches_calls_bitwise": list_matches_calls},
         "roofline_by_m": roofline_by_m,
         "value_graph": {"value": round(value_graph, 1), "unit": "GB/s",
