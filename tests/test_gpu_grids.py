@@ -91,3 +91,23 @@ def test_capped_grid_stall_reports_timeout(w12lib, oracle):
     Y = synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, workspace=ws, opts=w12lib.make_opts(max_ctas=3)))
     assert gemm_tolerance_failures(Y, Yr, Y64, mag).size == 0
     assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_OK
+
+
+@pytest.mark.parametrize("M,split", [(40, 3), (64, 5), (24, 2)])
+def test_tc_silu_split_across_grids(M, split, w12lib):
+    """The fused gate/up epilogue with a split: an uncapped grid (one CTA per
+    item; the split's partials summed across a thread-block cluster where the
+    clusters fit) and capped grids (partials summed in global memory by the
+    row tile's last CTA) add the chunks in the same order, so every output
+    bit is the same."""
+    N, K = 2 * 1536, 2048
+    W = synth.dense_weights(N, K, seed=970 + M)
+    A = synth.activations(M, K, seed=980 + M)
+    t = w12lib.w12_encode(synth.bits_to_tensor(W, "cuda"))
+    Ad = synth.bits_to_tensor(A, "cuda")
+    outs = []
+    for cap in (0, 5, 2, SMS, 3):
+        o = w12lib.make_opts(max_ctas=cap, split_k=split, flags=w12lib.W12_GEMM_SILU_MUL)
+        outs.append(synth.tensor_to_bits(w12lib.w12_gemm(Ad, t, opts=o)))
+    for y in outs[1:]:
+        assert np.array_equal(y, outs[0])
