@@ -271,3 +271,21 @@ def test_encode_into_preallocated_tensor(w12lib, oracle):
     with pytest.raises(w12lib.W12Error) as ei:
         w12lib.w12_encode(synth.bits_to_tensor(synth.adversarial_weights(N, K, seed=23), "cuda"), out=small)
     assert ei.value.status == w12lib.W12_ERR_CAPACITY
+
+
+@pytest.mark.parametrize("N,K,pad", [(37, 1000, 1), (21, 9000, 3), (16, 256, 5), (40, 8200, 0)])
+def test_encode_odd_row_strides(N, K, pad, w12lib, oracle):
+    """Rows that are not 16-byte aligned (an odd row stride) take the
+    bounds-checked loads in the window search and the pack; rows longer than
+    8192 columns take the 4-warp window kernel.  Bytes equal the oracle's."""
+    W = synth.adversarial_weights(N, K, seed=40 + N + pad)
+    big = np.zeros((N, K + pad), np.uint16)
+    big[:, :K] = W
+    Wd = synth.bits_to_tensor(big, "cuda")[:, :K]
+    t = w12lib.w12_encode(Wd)
+    torch.cuda.synchronize()
+    st, ref = oracle.encode(W)
+    g = host_view(t)
+    assert g["n_esc"] == ref.n_esc
+    for key in ("hi", "lo", "base", "esc_ptr", "esc"):
+        assert np.array_equal(g[key], getattr(ref, key)), key
