@@ -149,9 +149,15 @@ def status_string(status: int) -> str:
         return f"status {status}"
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:  # the current stream's handle without building a Stream object
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _check(status: int, what: str):
@@ -214,9 +220,22 @@ class W12Tensor:
     def esc_cap(self) -> int:
         return self.esc.numel()
 
+    def __setattr__(self, name, value):
+        if name != "n_esc":  # a new array or shape: the C view is rebuilt on next use
+            self.__dict__.pop("_cview", None)
+        object.__setattr__(self, name, value)
+
     def struct(self) -> _Tensor:
-        return _Tensor(self.N, self.K, self.hi.data_ptr(), self.lo.data_ptr(), self.base.data_ptr(),
-                       self.esc_ptr.data_ptr(), self.esc.data_ptr(), self.esc_cap, self.n_esc)
+        """The C view of the tensor (cached; n_esc refreshed on every call).
+        Assigning any field drops the cache; arrays must not be re-pointed in
+        place (Tensor.set_)."""
+        s = self.__dict__.get("_cview")
+        if s is None:
+            s = _Tensor(self.N, self.K, self.hi.data_ptr(), self.lo.data_ptr(), self.base.data_ptr(),
+                        self.esc_ptr.data_ptr(), self.esc.data_ptr(), self.esc_cap, self.n_esc)
+            self.__dict__["_cview"] = s
+        s.n_esc = self.n_esc
+        return s
 
     def nbytes(self) -> int:
         """Bytes the tensor stores (all of which the GEMM reads): both

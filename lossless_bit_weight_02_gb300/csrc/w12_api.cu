@@ -2,6 +2,8 @@
 // kernel launches.  Every public entry point is declared in include/w12.h.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "w12.h"
 #include "w12_device.cuh"
@@ -141,6 +143,44 @@ const char *w12_status_string(w12_status s) {
     return "W12_ERR_UNKNOWN";
 }
 
+// Host-mapped words that the pack kernel writes the escape total into, so an
+// encode reads it after the stream sync without a copy; one per encode in
+// flight (several host threads may encode at once), kept for reuse.
+namespace {
+class TotalSlots {
+  public:
+    int32_t *take() {
+        {
+            std::lock_guard<std::mutex> lock(m_);
+            if (!free_.empty()) {
+                int32_t *p = free_.back();
+                free_.pop_back();
+                return p;
+            }
+        }
+        void *p = nullptr;
+        if (cudaHostAlloc(&p, 64, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) return nullptr;
+        return static_cast<int32_t *>(p);
+    }
+    void give(int32_t *p) {
+        std::lock_guard<std::mutex> lock(m_);
+        free_.push_back(p);
+    }
+
+  private:
+    std::mutex m_;
+    std::vector<int32_t *> free_;
+};
+TotalSlots g_total_slots;
+
+struct SlotGuard {
+    int32_t *p;
+    ~SlotGuard() {
+        if (p) g_total_slots.give(p);
+    }
+};
+}  // namespace
+
 w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_stream_t stream) {
     w12_status st = check_tensor(out);
     if (st != W12_OK) return st;
@@ -149,18 +189,18 @@ w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_strea
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t N = out->N, K = out->K;
     const int64_t P = rows_padded(N) / 16 * groups_of(K);  // (stripe, group) count
-    if (cudaMemsetAsync(out->esc_ptr, 0, 4 * (size_t)(P + 1), s) != cudaSuccess) return W12_ERR_CUDA;
-    if (launch_window_count(W, ldw, N, K, out->base, out->esc_ptr, s) != cudaSuccess) return W12_ERR_CUDA;
-    if (launch_ptr_scan(out->esc_ptr, P, s) != cudaSuccess) return W12_ERR_CUDA;
-    // the pack kernel writes only the entries below esc_cap (none if the
-    // offsets overflowed), so the escape total is read once, at the end
-    if (launch_pack(W, ldw, N, K, out->base, out->esc_ptr, out->hi, out->lo, out->esc, out->esc_cap, s) !=
-        cudaSuccess)
+    // the kernel writes only the entries below esc_cap (none if the offsets
+    // overflowed), so the escape total is read once, at the end
+    SlotGuard slot{g_total_slots.take()};
+    int32_t *dslot = nullptr;
+    if (!slot.p || cudaHostGetDevicePointer(reinterpret_cast<void **>(&dslot), slot.p, 0) != cudaSuccess)
         return W12_ERR_CUDA;
-    int32_t total = 0;
-    if (cudaMemcpyAsync(&total, out->esc_ptr + P, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+    if (launch_encode(W, ldw, N, K, out->base, out->esc_ptr, out->hi, out->lo, out->esc, out->esc_cap, dslot,
+                      s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return W12_ERR_CUDA;
+    const int32_t total = P == 0 ? 0 : *reinterpret_cast<volatile int32_t *>(slot.p);
+    if (encode_timed_out(total)) return W12_ERR_TIMEOUT;
     if (total < 0) return W12_ERR_INVALID;  // more escapes than an int32 offset can index
     out->n_esc = total;
     return total > out->esc_cap ? W12_ERR_CAPACITY : W12_OK;

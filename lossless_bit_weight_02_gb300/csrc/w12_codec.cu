@@ -1,5 +1,5 @@
-// W12 codec kernels: encode (window search, escape count, offset scan,
-// pack), decode, load-time verify and escape-list structure check.
+// W12 codec kernels: encode (window search; pack with the escape offsets),
+// decode, load-time verify and escape-list structure check.
 //
 // All of them are HBM-bound integer work (SpecPilot, arXiv 2611.02501,
 // section 4.1: conversion to W12 and the bit-for-bit check of every decoded
@@ -43,12 +43,11 @@ __device__ __forceinline__ uint32_t escape_bits(uint32_t d) { return (d & 0xF800
 __device__ __forceinline__ int halves_set(uint32_t e) { return ((e & 0xFFFFu) != 0u) + ((e >> 16) != 0u); }
 
 // ---------------------------------------------------------------------------
-// a1 + a2: the window search and escape count, one of two kernels by row
-// length.  Both build the exact histogram of the row's exponent field, take
-// the window of 16 consecutive exponents holding the most counted weights
-// (exponents 0 and 255 are always escapes and not counted; ties go to the
-// largest base), and then re-read the row (mostly L2 hits) to add its escapes
-// per 256-column group into esc_ptr[t*G+g+1].
+// a1: the window search, one of two kernels by row length.  Both build the
+// exact histogram of the row's exponent field and take the window of 16
+// consecutive exponents holding the most counted weights (exponents 0 and 255
+// are always escapes and not counted; ties go to the largest base).  The grid
+// also sets esc_ptr[0..P] to -1 ("not yet") for the pack kernel's look-back.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
     asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
@@ -101,21 +100,13 @@ __device__ __forceinline__ int window_base(const uint32_t h[8], int lane) {
     return best_b;
 }
 
-// Adds the escapes of one lane's 8 weights of group g (a warp-wide call)
-// into cnt[g].
-__device__ __forceinline__ void count_group_escapes(int32_t *cnt, int g, const uint4 &x, uint32_t c2, int lane) {
-    const uint32_t e0 = escape_bits(window_word(x.x, c2)), e1 = escape_bits(window_word(x.y, c2));
-    const uint32_t e2 = escape_bits(window_word(x.z, c2)), e3 = escape_bits(window_word(x.w, c2));
-    const bool any = (e0 | e1 | e2 | e3) != 0u;
-    if (__any_sync(kFull, any)) {  // a third of a row's groups at the pages' escape rate
-        int k = any ? halves_set(e0) + halves_set(e1) + halves_set(e2) + halves_set(e3) : 0;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) k += __shfl_xor_sync(kFull, k, o);
-        if (lane == 0 && k) atomicAdd(&cnt[g], k);
-    }
-}
-
 constexpr int64_t kLongRow = 8192;  // columns: longer rows take the 4-warp kernel
+
+// Block n of an n_blocks grid sets its share of esc_ptr[0..P] to -1.
+__device__ __forceinline__ void mark_not_ready(int32_t *esc_ptr, int64_t P, int64_t n, int64_t n_blocks, int t,
+                                               int nt) {
+    for (int64_t i = n + n_blocks * t; i <= P; i += n_blocks * nt) esc_ptr[i] = -1;
+}
 
 // Rows of at most kLongRow columns: one warp (and block) per row, 24 rows in
 // flight per SM.  The histogram lives in shared memory as 8-bit counters
@@ -199,9 +190,9 @@ __device__ __forceinline__ void for_full_steps(const uint4 *__restrict__ p, int 
     for (; s < full; ++s) f(s, __ldg(p + 32 * s));
 }
 
-__global__ __launch_bounds__(32) void k_window_count_warp(const uint16_t *__restrict__ W, int64_t ldw, int64_t N,
-                                                     int64_t K, uint8_t *__restrict__ base,
-                                                     int32_t *__restrict__ esc_ptr) {
+__global__ __launch_bounds__(32) void k_window_warp(const uint16_t *__restrict__ W, int64_t ldw, int64_t N, int64_t K,
+                                                   uint8_t *__restrict__ base, int32_t *__restrict__ esc_ptr,
+                                                   int64_t P) {
     __shared__ __align__(16) uint32_t hist[64 * 32];  // [e % 64][lane], byte e / 64
     const int lane = threadIdx.x;
     const int64_t n = blockIdx.x;
@@ -241,20 +232,13 @@ __global__ __launch_bounds__(32) void k_window_count_warp(const uint16_t *__rest
     const uint32_t h[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
     const int best_b = window_base(h, lane);
     if (lane == 0) base[n] = (uint8_t)best_b;
-    // escapes per 256-column group (columns past K read as a weight at offset
-    // 0 of the window: never an escape)
-    const uint32_t c2 = window_c2((uint32_t)best_b), fill = (uint32_t)best_b << 7;
-    int32_t *cnt = esc_ptr + 1 + (n / 16) * G;
-    auto count_group = [&](int g, const uint4 &x) { count_group_escapes(cnt, g, x, c2, lane); };
-    for_full_steps(p, full, count_group);
-    for (int g = full; g < G; ++g) count_group(g, load8w(row, vec, (int64_t)g * 256 + lane * 8, K, fill));
+    mark_not_ready(esc_ptr, P, n, N, lane, 32);
 }
 
 // Longer rows: one block of 4 warps per row, warp w taking the row's
-// 256-column steps w, w+4, ...  Fewer rows are in flight (6 per SM), so the
-// second pass still finds its row in L2 (one warp per row re-read a third of
-// the 17408-column layer from HBM), and each row's fixed costs (clearing and
-// summing the table, the search) are spread over more columns.
+// 256-column steps w, w+4, ...  A row's fixed costs (clearing and summing the
+// table, the search) are spread over more columns, and a row's steps are
+// spread over more warps.
 //
 // The histogram is a shared-memory table of 32-bit counters with one column
 // per lane index: exponent e, lane L at byte 128*e + 4L, i.e. the counter of
@@ -307,12 +291,11 @@ __device__ __forceinline__ void for_warp_steps(const uint4 *__restrict__ p, int 
     for (; s < full; s += 4) f(s, __ldg(p + 32 * s));
 }
 
-__global__ __launch_bounds__(kRowWarps * 32) void k_window_count_block(const uint16_t *__restrict__ W, int64_t ldw,
-                                                                 int64_t N, int64_t K, uint8_t *__restrict__ base,
-                                                                 int32_t *__restrict__ esc_ptr) {
+__global__ __launch_bounds__(kRowWarps * 32) void k_window_block(const uint16_t *__restrict__ W, int64_t ldw,
+                                                               int64_t N, int64_t K, uint8_t *__restrict__ base,
+                                                               int32_t *__restrict__ esc_ptr, int64_t P) {
     __shared__ __align__(16) uint32_t hist[256 * 32];  // [exponent][lane]
     __shared__ uint32_t tot[256];
-    __shared__ int sh_base;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
 #pragma unroll
@@ -355,97 +338,52 @@ __global__ __launch_bounds__(kRowWarps * 32) void k_window_count_block(const uin
         const uint4 t0 = reinterpret_cast<const uint4 *>(tot)[2 * lane], t1 = reinterpret_cast<const uint4 *>(tot)[2 * lane + 1];
         const uint32_t h[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
         const int b = window_base(h, lane);
-        if (lane == 0) {
-            base[n] = (uint8_t)b;
-            sh_base = b;
-        }
+        if (lane == 0) base[n] = (uint8_t)b;
     }
-    __syncthreads();
-    // escapes per 256-column group (columns past K read as a weight at offset
-    // 0 of the window: never an escape)
-    const int best_b = sh_base;
-    const uint32_t c2 = window_c2((uint32_t)best_b), fill = (uint32_t)best_b << 7;
-    int32_t *cnt = esc_ptr + 1 + (n / 16) * G;
-    auto count_group = [&](int g, const uint4 &x) { count_group_escapes(cnt, g, x, c2, lane); };
-    for_warp_steps(p, warp, full, count_group);
-    for (int g = (full > warp ? full + ((warp - full) & 3) : warp); g < G; g += 4)
-        count_group(g, load8w(row, vec, (int64_t)g * 256 + lane * 8, K, fill));
+    mark_not_ready(esc_ptr, P, n, N, tid, kRowWarps * 32);
 }
 
 // ---------------------------------------------------------------------------
-// a2: inclusive scan of the per-group counts in esc_ptr[1..P] (one block).
-// Tiles of up to 1024 * 43 counts go through shared memory: coalesced loads,
-// each thread sums its `per` consecutive counts (per odd: no bank
-// conflicts), the block scans the 1024 sums, each thread rewrites its counts
-// as running totals, coalesced stores.  One tile covers every layer of a
-// 27B-class model.  esc_ptr[P] = -1 flags a total that does not fit an int32
-// offset.
+// a2 + a3: pack, with the escape offsets found on the way (k_pack, one
+// cooperative launch of resident blocks).
+//  1. Units (16-row stripe t, 256-column group g) are handed out one at a
+//     time from a counter in esc_ptr[0], so fast SMs take more.  A warp packs
+//     unit u into tiles 4u .. 4u+3 of the planes (4 KB of hi bytes, 2 KB of lo
+//     bytes, contiguous).  Lane (r = lane/4, q = lane%4) takes columns
+//     16q..16q+15 of rows r and r+8 of each tile: exactly one 16-byte slot of
+//     the hi tile per row (the hi tile is row-major, byte 64*row + column)
+//     and one 16-byte slot of the lo tile, so every store is a coalesced
+//     512-byte warp store.  The whole 8 KB unit is loaded before it is
+//     packed, and the block keeps little shared memory, so L1 can hold the
+//     loads of 16 warps in flight.  The unit's escapes, in (tile, row, column)
+//     order (rows r in lane order, then rows r+8, per tile, by a warp scan of
+//     per-lane counts), are staged in the warp's shared memory, and its
+//     esc_ptr slot gets its count as a code (below).
+//  2. A grid barrier (arrivals counted on the same counter).
+//  3. Block b scans the counts of units [b*SEG, (b+1)*SEG): it publishes the
+//     segment's total in the slot of its last unit (-2 - total), reads the
+//     slots of the segments before it until it meets an inclusive total
+//     (decoupled look-back, all threads reading at once), publishes its own
+//     inclusive total and writes the offsets of its units.
+//  4. A second grid barrier; then every warp copies its staged escapes to
+//     their offsets.  A unit whose escapes did not fit the staging area is
+//     re-derived from W by its scan block in step 3.
+// Slot codes while the kernel runs: -1 not yet (set by the window kernel), at
+// most kCountCode0 a unit's count from step 1, -2 .. kAggMin a segment total,
+// >= 0 an inclusive total, kEncTimeout / kEncOverflow an inclusive total that
+// carries an error.
 // ---------------------------------------------------------------------------
-constexpr int kScanMaxPer = 43;
-constexpr int kScanMaxTile = 1024 * kScanMaxPer;
-constexpr size_t kScanSmem = (size_t)kScanMaxTile * 4;
-
-__global__ __launch_bounds__(1024) void k_ptr_scan(int32_t *__restrict__ ptr, int64_t P) {
-    extern __shared__ int32_t sv[];
-    __shared__ long long warp_sums[32];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    long long carry = 0;
-    for (int64_t c0 = 0; c0 < P; c0 += kScanMaxTile) {
-        const int n = (int)((P - c0) < kScanMaxTile ? (P - c0) : kScanMaxTile);
-        const int per = ((n + 1023) / 1024) | 1;
-#pragma unroll 11
-        for (int i = tid; i < n; i += 1024) sv[i] = ptr[c0 + i + 1];  // loads in flight together
-        __syncthreads();
-        const int i0 = tid * per, i1 = (i0 + per < n) ? i0 + per : n;
-        long long s = 0;
-        for (int i = i0; i < i1; ++i) s += sv[i];
-        long long x = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long t = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += t;
-        }
-        if (lane == 31) warp_sums[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            long long w = warp_sums[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const long long t = __shfl_up_sync(kFull, w, o);
-                if (lane >= o) w += t;
-            }
-            warp_sums[lane] = w;
-        }
-        __syncthreads();
-        long long r = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + x - s;
-        for (int i = i0; i < i1; ++i) {
-            r += sv[i];
-            sv[i] = (int32_t)(r > 0x7fffffffLL ? -1 : r);
-        }
-        carry += warp_sums[31];
-        __syncthreads();
-#pragma unroll 11
-        for (int i = tid; i < n; i += 1024) ptr[c0 + i + 1] = sv[i];
-        __syncthreads();
-    }
-    if (tid == 0) {
-        ptr[0] = 0;
-        if (carry > 0x7fffffffLL) ptr[P] = -1;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// a3: pack.  One warp per unit (16-row stripe t, 256-column group g), which
-// owns tiles 4u .. 4u+3 of the planes (4 KB of hi bytes, 2 KB of lo bytes,
-// contiguous) and the unit's escapes.  Lane (r = lane/4, q = lane%4) takes
-// columns 16q..16q+15 of rows r and r+8 of each tile: exactly one 16-byte slot
-// of the hi tile per row (the hi tile is row-major, byte 64*row + column) and
-// one 16-byte slot of the lo tile, so every store is a coalesced 512-byte
-// warp store and no shared memory or block barrier is needed.  Escapes go to
-// esc_ptr[u] + (their rank in (tile, row, column) order): rows r (all lanes,
-// lane order) then rows r+8, per tile, by a warp scan of per-lane counts.
-// ---------------------------------------------------------------------------
-constexpr int kPackWarps = 4;  // 126 registers (a whole unit in flight): four 4-warp blocks per SM
+constexpr int kPackWarps = 4;     // 151 registers (a whole unit in flight): three 4-warp blocks per SM
+constexpr int kPackStage = 640;   // escape words a warp holds until the offsets are known
+constexpr int kPackList = 128;    // units a warp holds escapes for
+constexpr int kPackRedo = 256;    // unstaged units a scan block remembers (more: it redoes its segment)
+constexpr int32_t kEncNotReady = -1;
+constexpr int32_t kEncTimeout = INT32_MIN;  // inclusive totals that carry an error
+constexpr int32_t kEncOverflow = INT32_MIN + 1;
+constexpr int32_t kAggMin = -(1 << 30) + 1;        // segment totals: -2 - total, total <= 2^30 - 3
+constexpr int32_t kCountCode0 = -(1 << 30) - 1;    // a unit's count c: kCountCode0 - c (- kUnstaged)
+constexpr int32_t kUnstaged = 1 << 20;             // ... if its escapes are not in the staging area
+constexpr uint32_t kEncPollLimit = 1u << 21;       // polls of a wait (backoff to 256 ns): about 2 s
 
 // Sixteen weights of a row (columns k..k+15) as eight words; columns past K
 // read as `fill`.
@@ -477,32 +415,22 @@ __device__ __forceinline__ uint32_t lo_word(uint32_t d0, uint32_t d1, uint32_t d
     return ((a << 4) & 0xF0F0F0F0u) | (b & 0x0F0F0F0Fu);
 }
 
-// The escapes among this lane's 16 columns of tile row `row`: written in
-// (row, column) order after the `p` entries the unit already holds, in lane
-// order across the warp; their records become 0 (d = 0x8000, sign cleared).
-// Only the lanes that hold an escape (a few per tile) walk their set bits.
-__device__ __forceinline__ void pack_escapes(uint32_t d[8], uint32_t x[8], bool any, int c4, int row, int q,
-                                             int lane, int64_t &p, uint64_t esc_lim, uint32_t *__restrict__ esc) {
-    uint32_t m = 0;  // bit c: column 16q + c is an escape
-    if (any) {
+// The escape mask of a lane's 16 columns of one tile row: bit c is set when
+// column 16q + c is an escape.
+__device__ __forceinline__ uint32_t escape_mask(const uint32_t d[8]) {
+    uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t e = escape_bits(d[i]);
-            m |= (uint32_t)((e & 0xFFFFu) != 0u) << (2 * i) | (uint32_t)((e >> 16) != 0u) << (2 * i + 1);
-        }
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t e = escape_bits(d[i]);
+        m |= (uint32_t)((e & 0xFFFFu) != 0u) << (2 * i) | (uint32_t)((e >> 16) != 0u) << (2 * i + 1);
     }
-    if (!__any_sync(kFull, m != 0u)) return;
-    const int cnt = __popc(m);
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += v;
-    }
-    int64_t pos = p + incl - cnt;
-    p += __shfl_sync(kFull, incl, 31);
-    if (m == 0u) return;
-    const uint32_t key0 = (uint32_t)(c4 << 10) | (uint32_t)(row << 6) | (uint32_t)(16 * q);
+    return m;
+}
+
+// Writes the escapes of mask m (keys key0 + c, values from x) to esc[pos...]
+// below esc_lim and turns their records into 0 (d = 0x8000, sign cleared).
+__device__ __forceinline__ void put_escapes(uint32_t m, uint32_t d[8], uint32_t x[8], uint32_t key0, int64_t pos,
+                                            uint64_t esc_lim, uint32_t *__restrict__ esc) {
     for (uint32_t mm = m; mm; mm &= mm - 1u, ++pos) {
         const int c = __ffs(mm) - 1;
         // the word of column c, picked by selects (no indexed array access)
@@ -521,15 +449,37 @@ __device__ __forceinline__ void pack_escapes(uint32_t d[8], uint32_t x[8], bool 
     }
 }
 
-__global__ __launch_bounds__(kPackWarps * 32) void k_pack(const uint16_t *__restrict__ W, int64_t ldw, int64_t N,
-                                                          int64_t K, const uint8_t *__restrict__ base,
-                                                          const int32_t *__restrict__ esc_ptr,
-                                                          uint8_t *__restrict__ hi, uint8_t *__restrict__ lo,
-                                                          uint32_t *__restrict__ esc, int64_t esc_cap,
-                                                          int64_t units, int64_t G) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t u = (int64_t)blockIdx.x * kPackWarps + warp;
-    if (u >= units) return;  // warp-uniform
+// The escapes among this lane's columns 16q..16q+15 of tile rows r (d0, x0)
+// and r+8 (d1, x1) (a warp-wide call): written after the `p` entries the unit
+// already holds, in (row, column) order, i.e. row r of every lane in lane
+// order, then row r+8.  One warp scan ranks both rows (a 16-bit count each);
+// only the lanes that hold an escape (a few per tile) walk their set bits.
+__device__ __forceinline__ void pack_escapes(uint32_t d0[8], uint32_t x0[8], bool any0, uint32_t d1[8],
+                                             uint32_t x1[8], bool any1, int c4, int r, int q, int lane, int64_t &p,
+                                             uint64_t esc_lim, uint32_t *__restrict__ esc) {
+    const uint32_t m0 = any0 ? escape_mask(d0) : 0u, m1 = any1 ? escape_mask(d1) : 0u;
+    const uint32_t n0 = __popc(m0), n1 = __popc(m1);
+    uint32_t incl = n0 | (n1 << 16);  // at most 32 * 16 per half: no carry
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const uint32_t tot = __shfl_sync(kFull, incl, 31);
+    const int64_t pos0 = p + (int64_t)((incl & 0xFFFFu) - n0);
+    const int64_t pos1 = p + (int64_t)(tot & 0xFFFFu) + (int64_t)((incl >> 16) - n1);
+    p += (int64_t)(tot & 0xFFFFu) + (int64_t)(tot >> 16);
+    const uint32_t key = (uint32_t)(c4 << 10) | (uint32_t)(r << 6) | (uint32_t)(16 * q);
+    if (m0) put_escapes(m0, d0, x0, key, pos0, esc_lim, esc);
+    if (m1) put_escapes(m1, d1, x1, key + (8u << 6), pos1, esc_lim, esc);
+}
+
+// Packs unit u (a warp-wide call) into its planes and writes its escapes to
+// escd[p...] below lim, p advancing by their count.
+__device__ __forceinline__ void pack_unit(const uint16_t *__restrict__ W, int64_t ldw, int64_t N, int64_t K,
+                                          const uint8_t *__restrict__ base, uint8_t *__restrict__ hi,
+                                          uint8_t *__restrict__ lo, int64_t u, int64_t G, int lane, int64_t &p,
+                                          uint64_t lim, uint32_t *escd) {
     const int64_t t = u / G, g = u - t * G;
     const int r = lane >> 2, q = lane & 3;
     const int64_t nA = t * 16 + r, nB = nA + 8;
@@ -542,10 +492,6 @@ __global__ __launch_bounds__(kPackWarps * 32) void k_pack(const uint16_t *__rest
     const bool vecA = (reinterpret_cast<uintptr_t>(rowA) & 15) == 0, vecB = (reinterpret_cast<uintptr_t>(rowB) & 15) == 0;
     uint4 *hu = reinterpret_cast<uint4 *>(hi + u * 4096);
     uint4 *lu = reinterpret_cast<uint4 *>(lo + u * 2048);
-    int64_t p = esc_ptr[u];
-    // entries past esc_cap are not written, and none at all if the scan
-    // flagged an offset overflow (-1)
-    const uint64_t esc_lim = esc_ptr[units] >= 0 ? (uint64_t)esc_cap : 0u;
     // a whole unit in range and aligned is loaded up front (8 KB per warp in
     // flight) with plain 16-byte loads; a ragged or padding edge, or an
     // unaligned row, takes bounds-checked loads per tile (warp-uniform choice)
@@ -581,13 +527,327 @@ __global__ __launch_bounds__(kPackWarps * 32) void k_pack(const uint16_t *__rest
             eb |= escape_bits(db[i]);
         }
         if (__any_sync(kFull, (ea | eb) != 0u)) {
-            pack_escapes(da, xa, ea != 0u, c4, r, q, lane, p, esc_lim, esc);
-            pack_escapes(db, xb, eb != 0u, c4, r + 8, q, lane, p, esc_lim, esc);
+            pack_escapes(da, xa, ea != 0u, db, xb, eb != 0u, c4, r, q, lane, p, lim, escd);
         }
         hu[c4 * 64 + lane] = hi_slot(da, xa);
         hu[c4 * 64 + 32 + lane] = hi_slot(db, xb);
         lu[c4 * 32 + lane] = make_uint4(lo_word(da[0], da[1], da[2], da[3]), lo_word(da[4], da[5], da[6], da[7]),
                                         lo_word(db[0], db[1], db[2], db[3]), lo_word(db[4], db[5], db[6], db[7]));
+    }
+}
+
+__device__ __forceinline__ int32_t ld_status(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_status(int32_t *p, int32_t v) {
+    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// The escape offset of segment k (a block-wide call): the sum of the totals
+// of the segments before it, read from their status slots esc_ptr[(j+1)*SEG].
+// The block reads up to 512 slots per round trip: every segment is scanned at
+// once, so the nearest inclusive total can sit many segments back.  A
+// negative result is an error code taken over from a segment before, or
+// kEncTimeout if a segment before published nothing within the poll limit.
+struct LookbackSmem {
+    long long sum[kPackWarps];
+    long long jmax[kPackWarps];
+    int flags[kPackWarps];
+};
+__device__ __forceinline__ long long segment_offset(const int32_t *esc_ptr, int64_t k, int64_t SEG, LookbackSmem &sh) {
+    constexpr int NT = kPackWarps * 32, R = 4, WIN = NT * R;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    long long E = 0;
+    int64_t top = k - 1;  // the highest segment not yet summed
+    uint32_t polls = 0;
+    unsigned ns = 64;
+    while (top >= 0) {
+        int32_t v[R];
+        int64_t jj[R];
+        long long mine = -2;  // the highest of this thread's segments with an inclusive total
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            jj[r] = top - tid - (int64_t)NT * r;
+            v[r] = jj[r] >= 0 ? ld_status(esc_ptr + (jj[r] + 1) * SEG) : kEncNotReady;
+            if (jj[r] >= 0 && (v[r] >= 0 || v[r] <= kEncOverflow) && jj[r] > mine) mine = jj[r];
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const long long y = __shfl_xor_sync(kFull, mine, o);
+            mine = y > mine ? y : mine;
+        }
+        if (lane == 0) sh.jmax[warp] = mine;
+        __syncthreads();
+        long long J = sh.jmax[0];
+#pragma unroll
+        for (int w = 1; w < kPackWarps; ++w) J = sh.jmax[w] > J ? sh.jmax[w] : J;
+        if (J == -2 && top - WIN + 1 <= 0) J = -1;  // segment 0 starts at offset 0
+        // the segments above J must all have published a total
+        long long a = 0;
+        int notready = 0, poison = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (jj[r] < 0 || jj[r] < J) continue;
+            if (jj[r] == J) {
+                if (v[r] < 0) poison = v[r];
+                else a += v[r];
+            } else if (v[r] == kEncNotReady || v[r] < kAggMin) {  // no total yet
+                notready = 1;
+            } else {
+                a += (long long)(-2 - v[r]);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            a += __shfl_xor_sync(kFull, a, o);
+            notready |= __shfl_xor_sync(kFull, notready, o);
+            poison |= __shfl_xor_sync(kFull, poison, o);
+        }
+        __syncthreads();  // every thread has read jmax
+        if (lane == 0) {
+            sh.sum[warp] = a;
+            sh.flags[warp] = notready;
+            sh.jmax[warp] = poison;
+        }
+        __syncthreads();
+        a = 0;
+        notready = 0;
+        poison = 0;
+#pragma unroll
+        for (int w = 0; w < kPackWarps; ++w) {
+            a += sh.sum[w];
+            notready |= sh.flags[w];
+            poison |= (int)sh.jmax[w];
+        }
+        __syncthreads();  // before the next round writes the scratch
+        if (notready) {
+            if (++polls > kEncPollLimit) return kEncTimeout;
+            __nanosleep(ns);
+            if (ns < 256) ns *= 2;
+            continue;
+        }
+        if (poison) return poison;  // an error code (both are negative, ORs of one code)
+        E += a;
+        if (J >= -1) break;
+        top -= WIN;
+    }
+    return E > 0x7FFFFFFFLL ? (long long)kEncOverflow : E;
+}
+
+// Re-derives the escapes of unit u into esc[p...] below lim (a warp-wide
+// call, the slow path of a warp whose escapes outgrew its staging area).
+__device__ __noinline__ void unit_escapes(const uint16_t *__restrict__ W, int64_t ldw, int64_t N, int64_t K,
+                                          const uint8_t *__restrict__ base, int64_t u, int64_t G, int64_t p,
+                                          uint64_t lim, uint32_t *__restrict__ esc, int lane) {
+    const int64_t t = u / G, g = u - t * G;
+    const int r = lane >> 2, q = lane & 3;
+    const int64_t nA = t * 16 + r, nB = nA + 8;
+    const bool okA = nA < N, okB = nB < N;
+    const uint32_t bA = okA ? base[nA] : 0u, bB = okB ? base[nB] : 0u;
+    const uint32_t c2A = window_c2(bA), c2B = window_c2(bB), fA = bA << 7, fB = bB << 7;
+    const uint16_t *rowA = W + (okA ? nA : 0) * ldw, *rowB = W + (okB ? nB : 0) * ldw;
+    const int64_t KA = okA ? K : 0, KB = okB ? K : 0;
+    const bool vecA = (reinterpret_cast<uintptr_t>(rowA) & 15) == 0, vecB = (reinterpret_cast<uintptr_t>(rowB) & 15) == 0;
+    for (int c4 = 0; c4 < 4; ++c4) {
+        const int64_t k = g * 256 + c4 * 64 + 16 * q;
+        uint32_t xa[8], xb[8], da[8], db[8], ea = 0, eb = 0;
+        load16w(rowA, vecA, k, KA, fA, xa);
+        load16w(rowB, vecB, k, KB, fB, xb);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            da[i] = window_word(xa[i], c2A);
+            db[i] = window_word(xb[i], c2B);
+            ea |= escape_bits(da[i]);
+            eb |= escape_bits(db[i]);
+        }
+        if (__any_sync(kFull, (ea | eb) != 0u)) {
+            pack_escapes(da, xa, ea != 0u, db, xb, eb != 0u, c4, r, q, lane, p, lim, esc);
+        }
+    }
+}
+
+// Arrives at a grid barrier counted on *ctr and waits, within the poll
+// limit, until it reads at least `target` (or 0: the counter was reset after
+// the last barrier).  One thread per block.
+__device__ __forceinline__ bool grid_barrier(int32_t *ctr, int64_t target) {
+    __threadfence();
+    atomicAdd(ctr, 1);
+    unsigned ns = 32;
+    for (uint32_t i = 0; i < kEncPollLimit; ++i) {
+        const int32_t v = ld_status(ctr);
+        if (v >= target || v == 0) {
+            __threadfence();
+            return true;
+        }
+        __nanosleep(ns);
+        if (ns < 256) ns *= 2;
+    }
+    return false;
+}
+
+// The next unit for this warp: counter value + 1 (the counter starts at -1).
+__device__ __forceinline__ int64_t next_unit(int32_t *ctr, int lane) {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(ctr, 1);
+    return (int64_t)__shfl_sync(kFull, v, 0) + 1;
+}
+
+__global__ __launch_bounds__(kPackWarps * 32, 3) void k_pack(const uint16_t *__restrict__ W, int64_t ldw, int64_t N,
+                                                             int64_t K, const uint8_t *__restrict__ base,
+                                                             int32_t *__restrict__ esc_ptr, uint8_t *__restrict__ hi,
+                                                             uint8_t *__restrict__ lo, uint32_t *__restrict__ esc,
+                                                             int64_t esc_cap, int64_t P, int64_t G,
+                                                             int32_t *__restrict__ total) {
+    __shared__ uint32_t stage[kPackWarps][kPackStage];
+    __shared__ int32_t list_u[kPackWarps][kPackList];
+    __shared__ int32_t list_c[kPackWarps][kPackList];
+    __shared__ int32_t redo[kPackRedo];
+    __shared__ int n_redo;
+    __shared__ LookbackSmem lb;
+    __shared__ long long sE;
+    __shared__ int sync_ok;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int NT = kPackWarps * 32;
+    const int64_t B = gridDim.x;
+
+    // 1. pack units as they are handed out
+    int nl = 0;
+    {
+        int64_t p = 0;
+        int64_t u = next_unit(esc_ptr, lane);
+        while (u < P) {
+            // the next draw is in flight while this unit is packed
+            int vn = 0;
+            if (lane == 0) vn = atomicAdd(esc_ptr, 1);
+            const int64_t p0 = p;
+            pack_unit(W, ldw, N, K, base, hi, lo, u, G, lane, p, kPackStage, stage[warp]);
+            const int c = (int)(p - p0);
+            const bool staged = p <= kPackStage && nl < kPackList;
+            if (staged) {
+                if (lane == 0) {
+                    list_u[warp][nl] = (int32_t)u;
+                    list_c[warp][nl] = c;
+                }
+                ++nl;
+            } else {
+                p = p0;
+            }
+            if (lane == 0) esc_ptr[u + 1] = kCountCode0 - c - (staged ? 0 : kUnstaged);
+            u = (int64_t)__shfl_sync(kFull, vn, 0) + 1;
+        }
+    }
+    // 2. every count is in place: the counter has seen P + one failed draw
+    // per warp and one arrival per block
+    __syncthreads();
+    if (tid == 0) {
+        n_redo = 0;
+        sync_ok = grid_barrier(esc_ptr, P - 1 + (kPackWarps + 1) * B);
+    }
+    __syncthreads();
+    // 3. scan segment b: units [s0, s1), status slot esc_ptr[s1]
+    const int64_t SEG = (P + B - 1) / B, s0 = blockIdx.x * SEG, s1 = (s0 + SEG < P) ? s0 + SEG : P;
+    if (s0 < s1) {
+        // local inclusive totals replace the codes (all but the status slot,
+        // whose code is read first), in tiles of NT
+        long long run = 0;
+        for (int64_t c0 = s0; c0 < s1; c0 += NT) {
+            const int64_t u = c0 + tid;
+            int32_t cnt = 0;
+            if (u < s1) {
+                const int32_t code = __ldcg(esc_ptr + u + 1);
+                const int32_t x = kCountCode0 - code;
+                cnt = x & (kUnstaged - 1);
+                if (x & kUnstaged) {
+                    const int i = atomicAdd(&n_redo, 1);
+                    if (i < kPackRedo) redo[i] = (int32_t)(u - s0);
+                }
+            }
+            int x = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) lb.sum[warp] = x;
+            __syncthreads();
+            long long before = run;
+            for (int w = 0; w < warp; ++w) before += lb.sum[w];
+            long long tile = 0;
+            for (int w = 0; w < kPackWarps; ++w) tile += lb.sum[w];
+            if (u < s1 && u + 1 != s1) {
+                const long long v = before + x;
+                esc_ptr[u + 1] = (int32_t)(v < 0x7FFFFFFFLL ? v : 0x7FFFFFFFLL);
+            }
+            run += tile;
+            __syncthreads();
+        }
+        const long long agg = run;
+        const bool big = agg > -2LL - kAggMin;
+        if (tid == 0) st_status(esc_ptr + s1, big ? kEncOverflow : (int32_t)(-2 - agg));
+        long long E = kEncTimeout;
+        if (!sync_ok) {
+            if (tid == 0) st_status(esc_ptr + s1, kEncTimeout);
+        } else if (big) {
+            E = kEncOverflow;
+        } else {
+            E = segment_offset(esc_ptr, blockIdx.x, SEG, lb);
+            if (tid == 0) {
+                const long long incl = E < 0 ? E : (E + agg > 0x7FFFFFFFLL ? (long long)kEncOverflow : E + agg);
+                st_status(esc_ptr + s1, (int32_t)incl);
+            }
+        }
+        for (int64_t u = s0 + tid; u + 1 < s1; u += NT) {
+            const long long v = E + esc_ptr[u + 1];
+            esc_ptr[u + 1] = (E < 0 || v > 0x7FFFFFFFLL) ? -1 : (int32_t)v;
+        }
+        __syncthreads();  // the segment's offsets are in place
+        // units whose escapes were not staged: re-derived here (all of the
+        // segment's units if more than kPackRedo)
+        if (E >= 0) {
+            const uint64_t lim = (uint64_t)esc_cap;
+            const int nr = n_redo;
+            const int64_t m = nr <= kPackRedo ? nr : s1 - s0;
+            for (int64_t i = warp; i < m; i += kPackWarps) {
+                const int64_t u = s0 + (nr <= kPackRedo ? redo[i] : i);
+                unit_escapes(W, ldw, N, K, base, u, G, u == s0 ? E : (long long)esc_ptr[u], lim, esc, lane);
+            }
+        }
+    }
+    // 4. every offset is in place: staged escapes go out
+    __syncthreads();
+    if (tid == 0) {
+        const bool ok = grid_barrier(esc_ptr, P - 1 + (kPackWarps + 2) * B) && sync_ok;
+        sync_ok = ok;
+        if (!ok) {  // reported by the caller
+            st_status(esc_ptr + P, kEncTimeout);
+            *reinterpret_cast<volatile int32_t *>(total) = kEncTimeout;
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && tid == 0) {
+        esc_ptr[0] = 0;  // every block is past both barriers
+        if (sync_ok) *reinterpret_cast<volatile int32_t *>(total) = __ldcg(esc_ptr + P);
+    }
+    if (!sync_ok) return;
+    // the offsets of 32 listed units are fetched at once
+    int s = 0;
+    for (int i0 = 0; i0 < nl; i0 += 32) {
+        int offl = -1;
+        if (i0 + lane < nl) {
+            const int32_t u = list_u[warp][i0 + lane];
+            offl = u == 0 ? 0 : __ldcg(esc_ptr + u);
+        }
+        const int n = nl - i0 < 32 ? nl - i0 : 32;
+        for (int j = 0; j < n; ++j) {
+            const int off = __shfl_sync(kFull, offl, j);
+            const int c = list_c[warp][i0 + j];
+            if (off >= 0)
+                for (int k = lane; k < c; k += 32)
+                    if ((uint64_t)((int64_t)off + k) < (uint64_t)esc_cap) esc[(int64_t)off + k] = stage[warp][s + k];
+            s += c;
+        }
     }
 }
 
@@ -704,46 +964,53 @@ __global__ void k_check_entries(TensorView t, unsigned long long *__restrict__ b
 
 }  // namespace
 
-cudaError_t launch_window_count(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base,
-                                int32_t *esc_ptr, cudaStream_t s) {
-    if (N == 0) return cudaSuccess;
+cudaError_t launch_encode(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base, int32_t *esc_ptr,
+                          uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap, int32_t *total,
+                          cudaStream_t s) {
+    const int64_t G = groups_of(K), P = rows_padded(N) / 16 * G;
+    if (P == 0) {
+        // no columns: every window holds no weight, and ties go to the
+        // largest base, 239
+        cudaError_t e = N > 0 ? cudaMemsetAsync(base, 239, (size_t)N, s) : cudaSuccess;
+        return e != cudaSuccess ? e : cudaMemsetAsync(esc_ptr, 0, 4, s);
+    }
     if (K > kLongRow)
-        k_window_count_block<<<(unsigned)N, kRowWarps * 32, 0, s>>>(W, ldw, N, K, base, esc_ptr);
+        k_window_block<<<(unsigned)N, kRowWarps * 32, 0, s>>>(W, ldw, N, K, base, esc_ptr, P);
     else
-        k_window_count_warp<<<(unsigned)N, 32, 0, s>>>(W, ldw, N, K, base, esc_ptr);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_ptr_scan(int32_t *esc_ptr, int64_t P, cudaStream_t s) {
-    // the kernel's shared-memory limit, raised once per device (several host
-    // threads may encode at once)
-    static std::mutex m;
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+        k_window_warp<<<(unsigned)N, 32, 0, s>>>(W, ldw, N, K, base, esc_ptr, P);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // the resident pack blocks, once per device (several host threads may
+    // encode at once)
+    static std::mutex m;
+    static int slots[64] = {};
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    int sl = 0;
     {
         std::lock_guard<std::mutex> lock(m);
-        if (dev < 0 || dev >= 64 || !configured[dev]) {
-            e = cudaFuncSetAttribute(k_ptr_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+        if (dev >= 0 && dev < 64) sl = slots[dev];
+        if (sl == 0) {
+            int per_sm = 0, sms = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_pack, kPackWarps * 32, 0);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
-            if (dev >= 0 && dev < 64) configured[dev] = true;
+            sl = (per_sm > 0 ? per_sm : 1) * sms;
+            if (dev >= 0 && dev < 64) slots[dev] = sl;
         }
     }
-    const int64_t tile = P < kScanMaxTile ? P : kScanMaxTile;
-    k_ptr_scan<<<1, 1024, (size_t)tile * 4, s>>>(esc_ptr, P);
-    return cudaGetLastError();
+    // every block resident (the kernel has two grid barriers); the counter in
+    // esc_ptr[0] must reach P - 1 + 6 B as an int32
+    int64_t B = sl < P ? sl : P;
+    if (P - 1 + (kPackWarps + 2) * B > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const uint8_t *cbase = base;
+    void *args[] = {(void *)&W, (void *)&ldw, (void *)&N, (void *)&K, (void *)&cbase, (void *)&esc_ptr,
+                    (void *)&hi, (void *)&lo, (void *)&esc, (void *)&esc_cap, (void *)&P, (void *)&G,
+                    (void *)&total};
+    return cudaLaunchCooperativeKernel((const void *)k_pack, dim3((unsigned)B), dim3(kPackWarps * 32), args, 0, s);
 }
 
-cudaError_t launch_pack(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const uint8_t *base,
-                        const int32_t *esc_ptr, uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap,
-                        cudaStream_t s) {
-    const int64_t G = groups_of(K), units = rows_padded(N) / 16 * G;
-    if (units == 0) return cudaSuccess;
-    const int64_t blocks = (units + kPackWarps - 1) / kPackWarps;
-    k_pack<<<(unsigned)blocks, kPackWarps * 32, 0, s>>>(W, ldw, N, K, base, esc_ptr, hi, lo, esc, esc_cap, units, G);
-    return cudaGetLastError();
-}
+bool encode_timed_out(int32_t total) { return total == kEncTimeout; }
 
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s) {
     const int64_t blocks = (t.Np / 16) * t.G;

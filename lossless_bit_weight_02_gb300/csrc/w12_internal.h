@@ -46,17 +46,15 @@ static_assert(kWsPartialsOff + kMmaAutoPartialBytesM8 <= W12_NOALLOC_SCRATCH_BYT
 w12_status gemm_plan_bytes(int64_t M, int64_t N, int64_t K, const w12_gemm_opts *opts, size_t *bytes);
 
 // ---- codec (w12_codec.cu) ----
-// a1 + a2: base[n] and, added into esc_ptr[t*G+g+1] (zeroed by the caller),
-// the escape count of every (stripe, group).
-cudaError_t launch_window_count(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base,
-                                int32_t *esc_ptr, cudaStream_t s);
-// a2: in-place scan of esc_ptr[1..P] and esc_ptr[0] = 0; esc_ptr[P] = -1 on
-// int32 overflow.
-cudaError_t launch_ptr_scan(int32_t *esc_ptr, int64_t P, cudaStream_t s);
-// a3: planes + escapes (escape writes limited to esc_cap).
-cudaError_t launch_pack(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, const uint8_t *base,
-                        const int32_t *esc_ptr, uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap,
-                        cudaStream_t s);
+// a1 - a3: base, esc_ptr (inclusive offsets), planes and the escapes below
+// esc_cap; *total (device-visible, e.g. host-mapped) gets esc_ptr[P]: < 0 if
+// the total does not fit an int32 offset, or an error code that
+// encode_timed_out recognises if a bounded wait gave up.  Not written when
+// P == 0.  Two launches: the window search, then the pack.
+cudaError_t launch_encode(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base, int32_t *esc_ptr,
+                          uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap, int32_t *total,
+                          cudaStream_t s);
+bool encode_timed_out(int32_t total);
 // a4
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s);
 // escape-list structure violations added to *bad (device counter).

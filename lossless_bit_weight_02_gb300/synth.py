@@ -82,6 +82,15 @@ def dense_weights_device(N: int, K: int, seed: int, device="cuda", zero_frac=1e-
     return out
 
 
+def random_bits_device(N: int, K: int, seed: int, device="cuda") -> torch.Tensor:
+    """Uniformly random 16-bit patterns as torch.bfloat16 [N,K] on `device`
+    (every exponent equally likely: about 15 in 16 weights fall outside any
+    16-exponent window; zeros, subnormals, infinities and NaNs included)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randint(-32768, 32768, (N, K), dtype=torch.int16, device=device, generator=g).view(torch.bfloat16)
+
+
 def activations(M: int, K: int, seed: int) -> np.ndarray:
     """BF16 activations [M,K] ~ N(0,1).  Returns BF16 bits."""
     rng = np.random.default_rng(seed)

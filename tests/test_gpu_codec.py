@@ -251,6 +251,32 @@ def test_full_size_encode_bytes_match_the_oracle_on_sampled_stripes(name, N, K, 
         assert np.array_equal(got["esc"], ref.esc[:ref.n_esc]), s
 
 
+def test_encode_where_scan_blocks_redo_their_segments(w12lib, oracle):
+    """Random 16-bit patterns (about 15 escapes in 16 weights) over enough
+    16-row stripes that each block of the pack kernel's offset scan holds more
+    units whose escapes did not fit a warp's staging area than it can list, so
+    it re-derives every unit of its segment from W.  The GPU verifier checks
+    the whole tensor; sampled stripes equal the oracle's bytes."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 300 * 4 * sms  # > 256 units per scan block at up to 4 blocks per SM
+    N, K = 16 * T, 256
+    Wd = synth.random_bits_device(N, K, seed=31)
+    t = w12lib.w12_encode(Wd)
+    assert t.n_esc > N * K // 2
+    assert w12lib.w12_verify_roundtrip(Wd, t) == (w12lib.W12_OK, 0)
+    rng = np.random.default_rng(32)
+    for s in sorted({0, T - 1, T // 2, *rng.choice(T, size=3, replace=False).tolist()}):
+        n0, n1 = 16 * s, 16 * s + 16
+        got = host_view(t.rows(n0, n1))
+        st, ref = oracle.encode(synth.tensor_to_bits(Wd[n0:n1]))
+        assert st == oracle.OK and got["n_esc"] == ref.n_esc, s
+        for key in ("hi", "lo", "base", "esc_ptr"):
+            assert np.array_equal(got[key], getattr(ref, key)), (s, key)
+        assert np.array_equal(got["esc"], ref.esc[:ref.n_esc]), s
+    del Wd, t
+    torch.cuda.empty_cache()
+
+
 def test_encode_into_preallocated_tensor(w12lib, oracle):
     """w12_encode(W, out=t) reuses t's buffers: two different tensors of the
     same shape encoded one after the other into the same buffers, each equal
