@@ -506,11 +506,13 @@ __device__ __forceinline__ void pack_unit(const uint16_t *__restrict__ W, int64_
             B[j] = __ldg(pb + 8 * (j >> 1) + (j & 1));
         }
     }
-#pragma unroll
+    // one tile per pass, not unrolled (the loop then fits the instruction
+    // cache): the unit's registers move down by a tile after each pass
+#pragma unroll 1
     for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t xa[8], xb[8];
         if (fast) {
-            const uint4 u0 = A[2 * c4], u1 = A[2 * c4 + 1], v0 = B[2 * c4], v1 = B[2 * c4 + 1];
+            const uint4 u0 = A[0], u1 = A[1], v0 = B[0], v1 = B[1];
             xa[0] = u0.x, xa[1] = u0.y, xa[2] = u0.z, xa[3] = u0.w, xa[4] = u1.x, xa[5] = u1.y, xa[6] = u1.z, xa[7] = u1.w;
             xb[0] = v0.x, xb[1] = v0.y, xb[2] = v0.z, xb[3] = v0.w, xb[4] = v1.x, xb[5] = v1.y, xb[6] = v1.z, xb[7] = v1.w;
         } else {
@@ -533,6 +535,13 @@ __device__ __forceinline__ void pack_unit(const uint16_t *__restrict__ W, int64_
         hu[c4 * 64 + 32 + lane] = hi_slot(db, xb);
         lu[c4 * 32 + lane] = make_uint4(lo_word(da[0], da[1], da[2], da[3]), lo_word(da[4], da[5], da[6], da[7]),
                                         lo_word(db[0], db[1], db[2], db[3]), lo_word(db[4], db[5], db[6], db[7]));
+        if (fast) {
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+                A[j] = A[j + 2];
+                B[j] = B[j + 2];
+            }
+        }
     }
 }
 
