@@ -347,7 +347,9 @@ __global__ __launch_bounds__(kRowWarps * 32) void k_window_block(const uint16_t 
 // a2 + a3: pack, with the escape offsets found on the way (k_pack, one
 // cooperative launch of resident blocks).
 //  1. Units (16-row stripe t, 256-column group g) are handed out one at a
-//     time from a counter in esc_ptr[0], so fast SMs take more.  A warp packs
+//     time from a counter in esc_ptr[0], so fast SMs take more, last unit
+//     first: the window kernel read the last rows last, and part of them is
+//     still in L2.  A warp packs
 //     unit u into tiles 4u .. 4u+3 of the planes (4 KB of hi bytes, 2 KB of lo
 //     bytes, contiguous).  Lane (r = lane/4, q = lane%4) takes columns
 //     16q..16q+15 of rows r and r+8 of each tile: exactly one 16-byte slot of
@@ -725,8 +727,9 @@ __global__ __launch_bounds__(kPackWarps * 32, 3) void k_pack(const uint16_t *__r
     int nl = 0;
     {
         int64_t p = 0;
-        int64_t u = next_unit(esc_ptr, lane);
-        while (u < P) {
+        int64_t d = next_unit(esc_ptr, lane);
+        while (d < P) {
+            const int64_t u = P - 1 - d;
             // the next draw is in flight while this unit is packed
             int vn = 0;
             if (lane == 0) vn = atomicAdd(esc_ptr, 1);
@@ -744,7 +747,7 @@ __global__ __launch_bounds__(kPackWarps * 32, 3) void k_pack(const uint16_t *__r
                 p = p0;
             }
             if (lane == 0) esc_ptr[u + 1] = kCountCode0 - c - (staged ? 0 : kUnstaged);
-            u = (int64_t)__shfl_sync(kFull, vn, 0) + 1;
+            d = (int64_t)__shfl_sync(kFull, vn, 0) + 1;
         }
     }
     // 2. every count is in place: the counter has seen P + one failed draw
