@@ -220,20 +220,18 @@ class W12Tensor:
     def esc_cap(self) -> int:
         return self.esc.numel()
 
-    def __setattr__(self, name, value):
-        if name != "n_esc":  # a new array or shape: the C view is rebuilt on next use
-            self.__dict__.pop("_cview", None)
-        object.__setattr__(self, name, value)
-
     def struct(self) -> _Tensor:
-        """The C view of the tensor (cached; n_esc refreshed on every call).
-        Assigning any field drops the cache; arrays must not be re-pointed in
-        place (Tensor.set_)."""
-        s = self.__dict__.get("_cview")
-        if s is None:
+        """The C view of the tensor, cached while the same array objects and
+        shape are in place (n_esc is refreshed on every call); arrays must not
+        be re-pointed in place (Tensor.set_)."""
+        c = self.__dict__.get("_cview")
+        if (c is None or c[0] is not self.hi or c[1] is not self.lo or c[2] is not self.base
+                or c[3] is not self.esc_ptr or c[4] is not self.esc or c[5] != (self.N, self.K)):
             s = _Tensor(self.N, self.K, self.hi.data_ptr(), self.lo.data_ptr(), self.base.data_ptr(),
                         self.esc_ptr.data_ptr(), self.esc.data_ptr(), self.esc_cap, self.n_esc)
-            self.__dict__["_cview"] = s
+            c = (self.hi, self.lo, self.base, self.esc_ptr, self.esc, (self.N, self.K), s)
+            self.__dict__["_cview"] = c
+        s = c[6]
         s.n_esc = self.n_esc
         return s
 
@@ -273,15 +271,33 @@ def cols_padded(K: int) -> int:
     return int(load().w12_cols_padded(K))
 
 
+_array_sizes: dict = {}
+
+
+def _sizes_of(N: int, K: int):
+    """(hi bytes, lo bytes, esc_ptr entries) from the library's size queries,
+    kept per shape."""
+    key = (N, K)
+    v = _array_sizes.get(key)
+    if v is None:
+        lib = load()
+        v = (int(lib.w12_hi_bytes(N, K)), int(lib.w12_lo_bytes(N, K)), int(lib.w12_esc_ptr_len(N, K)))
+        _array_sizes[key] = v
+    return v
+
+
 def empty_tensor(N: int, K: int, esc_cap: int, device) -> W12Tensor:
-    lib = load()
-    hi = torch.empty(max(1, lib.w12_hi_bytes(N, K)), dtype=torch.uint8, device=device)
-    lo = torch.empty(max(1, lib.w12_lo_bytes(N, K)), dtype=torch.uint8, device=device)
-    base = torch.empty(max(1, N), dtype=torch.uint8, device=device)
-    esc_ptr = torch.empty(lib.w12_esc_ptr_len(N, K), dtype=torch.int32, device=device)
-    esc = torch.empty(max(1, esc_cap), dtype=torch.int32, device=device)
-    return W12Tensor(N, K, hi[:lib.w12_hi_bytes(N, K)], lo[:lib.w12_lo_bytes(N, K)], base[:N], esc_ptr,
-                     esc[:esc_cap], 0)
+    """An uninitialised W12 tensor: one device allocation, the five arrays
+    carved out of it at 256-byte aligned offsets."""
+    hb, lb, pl = _sizes_of(N, K)
+    a = lambda x: (x + 255) & ~255
+    o_lo = a(hb)
+    o_base = o_lo + a(lb)
+    o_ptr = o_base + a(N)
+    o_esc = o_ptr + a(4 * pl)
+    buf = torch.empty(max(1, o_esc + 4 * esc_cap), dtype=torch.uint8, device=device)
+    return W12Tensor(N, K, buf[:hb], buf[o_lo:o_lo + lb], buf[o_base:o_base + N],
+                     buf[o_ptr:o_ptr + 4 * pl].view(torch.int32), buf[o_esc:o_esc + 4 * esc_cap].view(torch.int32), 0)
 
 
 def w12_encode(W: torch.Tensor, esc_cap: int | None = None, stream=None, out: W12Tensor | None = None) -> W12Tensor:

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -257,3 +258,18 @@ def test_gdn_argument_checks(w12lib):
     assert call(*ok, ws=ctypes.c_size_t(need - 1)) == w12lib.W12_ERR_CAPACITY
     assert lib.w12_gdn_status(None, 256, None) == w12lib.W12_ERR_INVALID
     assert lib.w12_gdn_status(p, 255, None) == w12lib.W12_ERR_INVALID
+
+
+def test_empty_tensor_is_one_allocation_with_aligned_arrays(w12lib):
+    """empty_tensor carves the five arrays out of one buffer: sizes as the
+    library's size queries give them, every array at a 256-byte aligned offset
+    (the planes are read by TMA, which wants 16-byte aligned addresses)."""
+    lib = w12lib.load()
+    for N, K, cap in ((0, 64, 1024), (5, 0, 10), (17, 65, 3), (34816, 5120, 1000), (1, 1, 0)):
+        t = w12lib.empty_tensor(N, K, cap, "cpu")
+        assert t.hi.numel() == lib.w12_hi_bytes(N, K) and t.lo.numel() == lib.w12_lo_bytes(N, K)
+        assert t.base.numel() == N and t.esc_ptr.numel() == lib.w12_esc_ptr_len(N, K)
+        assert t.esc.numel() == cap and t.esc.dtype == torch.int32 and t.esc_ptr.dtype == torch.int32
+        arrays = (t.hi, t.lo, t.base, t.esc_ptr, t.esc)
+        assert all(x.storage_offset() * x.element_size() % 256 == 0 for x in arrays), (N, K)
+        assert len({x.untyped_storage().data_ptr() for x in arrays}) == 1
