@@ -167,12 +167,18 @@ int64_t w12_esc_ptr_len(int64_t N, int64_t K);  /* Np/16 * w12_groups(K) + 1 */
  * output channel, records, exact escape list).
  * W: device [N rows, stride ldw elements], ldw >= K.  out: N, K, all
  * pointers and esc_cap filled in by the caller; n_esc is written.
- * Synchronous: waits on `stream` once to read the escape count.
+ * Synchronous: two launches on `stream` (the window search, then one
+ * cooperative pack launch sized to the blocks the device holds at once, which
+ * counts, orders and writes the escapes), then one wait on `stream`; the
+ * escape count comes back through a host-mapped pinned word (the library
+ * keeps one per encode in flight, for reuse).
  * If the tensor needs more than esc_cap escapes the call returns
  * W12_ERR_CAPACITY with out->n_esc = the number needed; the planes, base and
  * esc_ptr are complete and the first esc_cap escapes are written, so the
  * caller can grow the escape array and call again.  Returns W12_ERR_INVALID
- * if the count would not fit an int32 offset. */
+ * if the count would not fit an int32 offset, and W12_ERR_TIMEOUT if a
+ * bounded wait inside the pack kernel gave up (about 2 s; the tensor is then
+ * unspecified). */
 w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_stream_t stream);
 
 /* ---- w12_decode ----  W12 -> BF16 [N,K] (paper section 4.1: decode is bit
