@@ -181,6 +181,12 @@ int64_t w12_esc_ptr_len(int64_t N, int64_t K);  /* Np/16 * w12_groups(K) + 1 */
  * unspecified). */
 w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_stream_t stream);
 
+/* ---- w12_encode_test_stall ----  Tests only: while `on` is nonzero, every
+ * w12_encode of this process makes the first block of its pack kernel skip
+ * the first grid barrier, so every block's bounded wait runs out (about 2 s
+ * per barrier) and the call returns W12_ERR_TIMEOUT.  Off by default. */
+void w12_encode_test_stall(int on);
+
 /* ---- w12_decode ----  W12 -> BF16 [N,K] (paper section 4.1: decode is bit
  * for bit).  W_out: device, stride ldw >= K.  Asynchronous.  For a tensor
  * whose escape list is malformed the output is unspecified (but no access

@@ -46,7 +46,7 @@ W12_LIST_MAX = 64  # GEMMs per launch of w12_gemm_list
 # Every symbol include/w12.h declares.
 EXPORTS = (
     "w12_rows_padded", "w12_cols_padded", "w12_hi_bytes", "w12_lo_bytes", "w12_groups",
-    "w12_esc_ptr_len", "w12_encode",
+    "w12_esc_ptr_len", "w12_encode", "w12_encode_test_stall",
     "w12_decode", "w12_verify_workspace_bytes", "w12_verify_roundtrip",
     "w12_gemm_workspace_bytes", "w12_gemm", "w12_gemm_noalloc", "w12_gemm_noalloc_status",
     "w12_gemm_workspace_status", "w12_gemm_list_workspace_bytes", "w12_gemm_list",
@@ -110,6 +110,7 @@ def load(path: str | None = None):
             "w12_groups": (i64, [i64]),
             "w12_esc_ptr_len": (i64, [i64, i64]),
             "w12_encode": (st, [vp, i64, ctypes.POINTER(_Tensor), vp]),
+            "w12_encode_test_stall": (None, [ctypes.c_int]),
             "w12_decode": (st, [ctypes.POINTER(_Tensor), vp, i64, vp]),
             "w12_verify_workspace_bytes": (sz, []),
             "w12_verify_roundtrip": (st, [vp, i64, ctypes.POINTER(_Tensor), ctypes.POINTER(i64), vp, sz, vp]),

@@ -2,6 +2,7 @@
 // kernel launches.  Every public entry point is declared in include/w12.h.
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -172,6 +173,7 @@ class TotalSlots {
     std::vector<int32_t *> free_;
 };
 TotalSlots g_total_slots;
+std::atomic<int> g_encode_test_stall{0};
 
 struct SlotGuard {
     int32_t *p;
@@ -196,7 +198,7 @@ w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_strea
     if (!slot.p || cudaHostGetDevicePointer(reinterpret_cast<void **>(&dslot), slot.p, 0) != cudaSuccess)
         return W12_ERR_CUDA;
     if (launch_encode(W, ldw, N, K, out->base, out->esc_ptr, out->hi, out->lo, out->esc, out->esc_cap, dslot,
-                      s) != cudaSuccess ||
+                      g_encode_test_stall.load() != 0, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return W12_ERR_CUDA;
     const int32_t total = P == 0 ? 0 : *reinterpret_cast<volatile int32_t *>(slot.p);
@@ -205,6 +207,8 @@ w12_status w12_encode(const uint16_t *W, int64_t ldw, w12_tensor *out, w12_strea
     out->n_esc = total;
     return total > out->esc_cap ? W12_ERR_CAPACITY : W12_OK;
 }
+
+void w12_encode_test_stall(int on) { g_encode_test_stall.store(on != 0 ? 1 : 0); }
 
 w12_status w12_decode(const w12_tensor *w, uint16_t *W_out, int64_t ldw, w12_stream_t stream) {
     w12_status st = check_tensor(w);

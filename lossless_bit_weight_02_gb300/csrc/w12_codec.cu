@@ -710,7 +710,7 @@ __global__ __launch_bounds__(kPackWarps * 32, 3) void k_pack(const uint16_t *__r
                                                              int32_t *__restrict__ esc_ptr, uint8_t *__restrict__ hi,
                                                              uint8_t *__restrict__ lo, uint32_t *__restrict__ esc,
                                                              int64_t esc_cap, int64_t P, int64_t G,
-                                                             int32_t *__restrict__ total) {
+                                                             int32_t *__restrict__ total, int test_stall) {
     __shared__ uint32_t stage[kPackWarps][kPackStage];
     __shared__ int32_t list_u[kPackWarps][kPackList];
     __shared__ int32_t list_c[kPackWarps][kPackList];
@@ -755,7 +755,9 @@ __global__ __launch_bounds__(kPackWarps * 32, 3) void k_pack(const uint16_t *__r
     __syncthreads();
     if (tid == 0) {
         n_redo = 0;
-        sync_ok = grid_barrier(esc_ptr, P - 1 + (kPackWarps + 1) * B);
+        // the test hook: block 0 never arrives, so every block's wait runs out
+        const bool arrive = !(test_stall && blockIdx.x == 0);
+        sync_ok = arrive && grid_barrier(esc_ptr, P - 1 + (kPackWarps + 1) * B);
     }
     __syncthreads();
     // 3. scan segment b: units [s0, s1), status slot esc_ptr[s1]
@@ -978,7 +980,7 @@ __global__ void k_check_entries(TensorView t, unsigned long long *__restrict__ b
 
 cudaError_t launch_encode(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base, int32_t *esc_ptr,
                           uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap, int32_t *total,
-                          cudaStream_t s) {
+                          bool test_stall, cudaStream_t s) {
     const int64_t G = groups_of(K), P = rows_padded(N) / 16 * G;
     if (P == 0) {
         // no columns: every window holds no weight, and ties go to the
@@ -1016,9 +1018,10 @@ cudaError_t launch_encode(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, 
     int64_t B = sl < P ? sl : P;
     if (P - 1 + (kPackWarps + 2) * B > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     const uint8_t *cbase = base;
+    int stall = test_stall ? 1 : 0;
     void *args[] = {(void *)&W, (void *)&ldw, (void *)&N, (void *)&K, (void *)&cbase, (void *)&esc_ptr,
                     (void *)&hi, (void *)&lo, (void *)&esc, (void *)&esc_cap, (void *)&P, (void *)&G,
-                    (void *)&total};
+                    (void *)&total, (void *)&stall};
     return cudaLaunchCooperativeKernel((const void *)k_pack, dim3((unsigned)B), dim3(kPackWarps * 32), args, 0, s);
 }
 

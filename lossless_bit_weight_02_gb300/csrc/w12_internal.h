@@ -50,10 +50,12 @@ w12_status gemm_plan_bytes(int64_t M, int64_t N, int64_t K, const w12_gemm_opts 
 // esc_cap; *total (device-visible, e.g. host-mapped) gets esc_ptr[P]: < 0 if
 // the total does not fit an int32 offset, or an error code that
 // encode_timed_out recognises if a bounded wait gave up.  Not written when
-// P == 0.  Two launches: the window search, then the pack.
+// P == 0.  Two launches: the window search, then the pack.  test_stall
+// (tests only): the pack's block 0 skips the first grid barrier, so every
+// bounded wait runs out and *total gets the timeout code.
 cudaError_t launch_encode(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, uint8_t *base, int32_t *esc_ptr,
                           uint8_t *hi, uint8_t *lo, uint32_t *esc, int64_t esc_cap, int32_t *total,
-                          cudaStream_t s);
+                          bool test_stall, cudaStream_t s);
 bool encode_timed_out(int32_t total);
 // a4
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s);

@@ -6,7 +6,8 @@ comes: it gives up, the CTA aborts, drains its own copies and MMAs, frees its
 TMEM and records the failure in the workspace error word.  The call returns,
 w12_gemm_workspace_status reports W12_ERR_TIMEOUT (and clears it), the
 workspace counters stay clean, and the next normal call on the same context
-gives the right result.  Nothing here traps or faults the GPU.
+gives the right result.  The encoder's waits are made to run out the same
+way (w12_encode_test_stall).  Nothing here traps or faults the GPU.
 """
 import numpy as np
 import pytest
@@ -41,3 +42,30 @@ def test_stalled_wait_reports_timeout_and_the_context_stays_usable(N, K, split, 
     torch.cuda.synchronize()
     assert gemm_tolerance_failures(Y, Yr, Y64, mag).size == 0
     assert w12lib.w12_gemm_workspace_status(ws) == w12lib.W12_OK
+
+
+@pytest.mark.parametrize("N,K", [(64, 1000), (2048, 5120)])
+def test_encode_stall_reports_timeout_and_the_next_encode_is_exact(N, K, w12lib, oracle):
+    """The encoder's bounded waits (the pack kernel's two grid barriers and its
+    look-back): with w12_encode_test_stall on, the pack's block 0 skips the
+    first barrier, every block's wait runs out and w12_encode reports
+    W12_ERR_TIMEOUT.  The next encode on the same context (hook off) gives the
+    oracle's bytes."""
+    W = synth.adversarial_weights(N, K, seed=51 + N)
+    Wd = synth.bits_to_tensor(W, "cuda")
+    lib = w12lib.load()
+    lib.w12_encode_test_stall(1)
+    try:
+        with pytest.raises(w12lib.W12Error) as ei:
+            w12lib.w12_encode(Wd)
+        assert ei.value.status == w12lib.W12_ERR_TIMEOUT
+    finally:
+        lib.w12_encode_test_stall(0)
+    t = w12lib.w12_encode(Wd)
+    torch.cuda.synchronize()
+    st, ref = oracle.encode(W)
+    assert t.n_esc == ref.n_esc
+    assert np.array_equal(t.hi.cpu().numpy(), ref.hi) and np.array_equal(t.lo.cpu().numpy(), ref.lo)
+    assert np.array_equal(t.base.cpu().numpy(), ref.base)
+    assert np.array_equal(t.esc_ptr.cpu().numpy(), ref.esc_ptr)
+    assert np.array_equal(t.esc[:t.n_esc].cpu().numpy().view(np.uint32), ref.esc[:ref.n_esc])
