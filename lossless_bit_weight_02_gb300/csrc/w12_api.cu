@@ -239,8 +239,11 @@ w12_status w12_verify_roundtrip(const uint16_t *W, int64_t ldw, const w12_tensor
     unsigned long long *cnt = static_cast<unsigned long long *>(workspace);
     const TensorView t = view_of(w);
     if (cudaMemsetAsync(cnt, 0, 16, s) != cudaSuccess) return W12_ERR_CUDA;
-    if (launch_check_structure(t, w->esc_cap, cnt, s) != cudaSuccess) return W12_ERR_CUDA;
-    if (w->K > 0 && launch_verify(t, W, ldw, cnt + 1, s) != cudaSuccess) return W12_ERR_CUDA;
+    // one launch checks the escape list's structure and compares every weight
+    // (a tensor without columns has only esc_ptr[0] to check)
+    if ((w->K > 0 ? launch_verify(t, W, ldw, cnt, cnt + 1, s) : launch_check_structure(t, w->esc_cap, cnt, s)) !=
+        cudaSuccess)
+        return W12_ERR_CUDA;
     unsigned long long host[2] = {0, 0};
     if (cudaMemcpyAsync(host, cnt, 16, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)

@@ -874,6 +874,7 @@ constexpr int kStageStride = 256 + 8;  // elements; 528 bytes keeps 16-byte alig
 
 __global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__restrict__ out, int64_t ldo,
                                                       const uint16_t *__restrict__ W_cmp, int64_t ldw,
+                                                      unsigned long long *__restrict__ structure_bad,
                                                       unsigned long long *__restrict__ mismatches) {
     __shared__ __align__(16) uint16_t stage[16 * kStageStride];
     const int64_t st = blockIdx.x / t.G, g = blockIdx.x % t.G, c0 = g * 4;
@@ -895,15 +896,25 @@ __global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__
         }
     }
     __syncthreads();
+    // verify also checks the escape list's structure for its group: the
+    // group's offsets (and the list's first and last), each entry's key in
+    // range, keys strictly increasing
+    int sbad = 0;
     {
+        const int64_t u = st * t.G + g;
         int64_t p0, p1;
-        escape_range(t.esc_ptr, st * t.G + g, t.n_esc, p0, p1);
+        escape_range(t.esc_ptr, u, t.n_esc, p0, p1);
         for (int64_t e = p0 + tid; e < p1; e += blockDim.x) {
             const uint32_t ent = t.esc[e];
             const int key = (int)(ent >> 16);
             const int r = (key >> 6) & 15, col = 64 * (key >> 10) + (key & 63);
-            if (key < 4096 && st * 16 + r < t.N && g * 256 + col < t.K)
-                stage[r * kStageStride + col] = (uint16_t)(ent & 0xFFFFu);
+            const bool in = key < 4096 && st * 16 + r < t.N && g * 256 + col < t.K;
+            if (in) stage[r * kStageStride + col] = (uint16_t)(ent & 0xFFFFu);
+            if (W_cmp != nullptr) sbad += (!in) + (e + 1 < p1 && (int)(t.esc[e + 1] >> 16) <= key);
+        }
+        if (W_cmp != nullptr && tid == 0) {
+            const int32_t a = t.esc_ptr[u], b = t.esc_ptr[u + 1];
+            sbad += (b < a) + (u == 0 && a != 0) + (u + 1 == (t.Np / 16) * t.G && (int64_t)b != t.n_esc);
         }
     }
     __syncthreads();
@@ -937,8 +948,12 @@ __global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__
     }
     if (W_cmp != nullptr) {
 #pragma unroll
-        for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(kFull, bad, o);
+        for (int o = 16; o; o >>= 1) {
+            bad += __shfl_xor_sync(kFull, bad, o);
+            sbad += __shfl_xor_sync(kFull, sbad, o);
+        }
         if ((tid & 31) == 0 && bad) atomicAdd(mismatches, (unsigned long long)bad);
+        if ((tid & 31) == 0 && sbad) atomicAdd(structure_bad, (unsigned long long)sbad);
     }
 }
 
@@ -954,26 +969,6 @@ __global__ void k_check_ptr(const int32_t *__restrict__ ptr, int64_t P, int64_t 
     if (i == P && (int64_t)ptr[P] != n_esc) ++v;
     if (i < P && ptr[i + 1] < ptr[i]) ++v;
     if (v) atomicAdd(bad, (unsigned long long)v);
-}
-
-// One warp per (stripe, group).
-__global__ void k_check_entries(TensorView t, unsigned long long *__restrict__ bad) {
-    const int lane = threadIdx.x & 31;
-    const int64_t grp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (grp >= (t.Np / 16) * t.G) return;
-    const int64_t st = grp / t.G, g = grp % t.G;
-    int64_t p0, p1;
-    escape_range(t.esc_ptr, grp, t.n_esc, p0, p1);
-    int v = 0;
-    for (int64_t e = p0 + lane; e < p1; e += 32) {
-        const uint32_t key = t.esc[e] >> 16;
-        const int64_t n = st * 16 + ((key >> 6) & 15), k = g * 256 + 64 * (key >> 10) + (key & 63);
-        if (key >= 4096 || n >= t.N || k >= t.K) ++v;
-        if (e + 1 < p1 && (t.esc[e + 1] >> 16) <= key) ++v;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    if (lane == 0 && v) atomicAdd(bad, (unsigned long long)v);
 }
 
 }  // namespace
@@ -1030,15 +1025,15 @@ bool encode_timed_out(int32_t total) { return total == kEncTimeout; }
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s) {
     const int64_t blocks = (t.Np / 16) * t.G;
     if (blocks == 0) return cudaSuccess;
-    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, out, ldo, nullptr, 0, nullptr);
+    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, out, ldo, nullptr, 0, nullptr, nullptr);
     return cudaGetLastError();
 }
 
-cudaError_t launch_verify(const TensorView &t, const uint16_t *W, int64_t ldw, unsigned long long *count,
-                          cudaStream_t s) {
+cudaError_t launch_verify(const TensorView &t, const uint16_t *W, int64_t ldw, unsigned long long *structure_bad,
+                          unsigned long long *count, cudaStream_t s) {
     const int64_t blocks = (t.Np / 16) * t.G;
     if (blocks == 0) return cudaSuccess;
-    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, nullptr, 0, W, ldw, count);
+    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, nullptr, 0, W, ldw, structure_bad, count);
     return cudaGetLastError();
 }
 
@@ -1047,9 +1042,6 @@ cudaError_t launch_check_structure(const TensorView &t, int64_t esc_cap, unsigne
     (void)esc_cap;
     const int64_t P = (t.Np / 16) * t.G;
     k_check_ptr<<<(unsigned)((P + 1 + 255) / 256), 256, 0, s>>>(t.esc_ptr, P, t.n_esc, bad);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || P == 0) return e;
-    k_check_entries<<<(unsigned)((P * 32 + 255) / 256), 256, 0, s>>>(t, bad);
     return cudaGetLastError();
 }
 

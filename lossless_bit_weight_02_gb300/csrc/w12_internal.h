@@ -59,11 +59,15 @@ cudaError_t launch_encode(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, 
 bool encode_timed_out(int32_t total);
 // a4
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s);
-// escape-list structure violations added to *bad (device counter).
+// escape-list structure violations of esc_ptr alone added to *bad (device
+// counter): for a tensor without groups, where launch_verify has nothing to
+// launch.
 cudaError_t launch_check_structure(const TensorView &t, int64_t esc_cap,
                                    unsigned long long *bad, cudaStream_t s);
-// a5: mismatches added to *count (device counter).
-cudaError_t launch_verify(const TensorView &t, const uint16_t *W, int64_t ldw,
+// a5: mismatches added to *count, escape-list structure violations (offsets
+// decreasing, esc_ptr[0] != 0, esc_ptr[P] != n_esc, a key out of range, keys
+// not increasing within a group) to *structure_bad (device counters).
+cudaError_t launch_verify(const TensorView &t, const uint16_t *W, int64_t ldw, unsigned long long *structure_bad,
                           unsigned long long *count, cudaStream_t s);
 
 // ---- GEMM ----
