@@ -122,10 +122,22 @@ __device__ __forceinline__ void mark_not_ready(int32_t *esc_ptr, int64_t P, int6
 // ---------------------------------------------------------------------------
 constexpr int kFoldSteps = 28;  // 28 * 8 = 224 < 256 adds per counter between folds
 
-// hl = the shared address of the counters + 4 * lane
+// 1 << 8 * (c & 3): byte c & 3 of the result is 1.  prmt's backward
+// 4-extract mode reads the selector's two low bits only and puts source byte
+// 0 (here the 1) at result byte c & 3, the others from source bytes 1..7 (0).
+__device__ __forceinline__ uint32_t byte_one(uint32_t c) {
+    uint32_t d;
+    asm("prmt.b32.b4e %0, %1, %2, %3;" : "=r"(d) : "r"(1u), "r"(0u), "r"(c));
+    return d;
+}
+
+// hl = the shared address of the counters + 4 * lane.  Exponent bits 6 and 7
+// of the low weight are bits 13 and 14 of x (bit 15, the sign, lands in the
+// selector's bit 2, which the extract ignores); of the high weight, 29 and 30.
 __device__ __forceinline__ void count_word(uint32_t hl, uint32_t x) {
-    red_add_shared(hl + (x & 0x1F80u), 1u << ((x >> 10) & 0x18u));
-    red_add_shared(hl + ((x >> 16) & 0x1F80u), 1u << ((x >> 26) & 0x18u));
+    red_add_shared(hl + (x & 0x1F80u), byte_one(x >> 13));
+    const uint32_t h = x >> 16;
+    red_add_shared(hl + (h & 0x1F80u), byte_one(h >> 13));
 }
 
 // Lane j adds counter words j and j+32 of all 32 copies (reading copy
