@@ -884,13 +884,27 @@ __global__ __launch_bounds__(kPackWarps * 32, 3) void k_pack(const uint16_t *__r
 // ---------------------------------------------------------------------------
 constexpr int kStageStride = 256 + 8;  // elements; 528 bytes keeps 16-byte alignment
 
-__global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__restrict__ out, int64_t ldo,
+// Two builds: kVerify compares with W_cmp (and counts structure violations),
+// else the group is stored to `out`.  The decode build fetches the group's
+// escape range and each thread's first entry before decoding the planes, so
+// those two dependent loads overlap the decode; it is held to 32 registers
+// (eight 256-thread blocks per SM: at 35 the prefetch lost a block and was
+// slower).  Verify does not prefetch (it was slower there).
+template <bool kVerify>
+__global__ __launch_bounds__(256, 8) void k_decode_group(TensorView t, uint16_t *__restrict__ out, int64_t ldo,
                                                       const uint16_t *__restrict__ W_cmp, int64_t ldw,
                                                       unsigned long long *__restrict__ structure_bad,
                                                       unsigned long long *__restrict__ mismatches) {
     __shared__ __align__(16) uint16_t stage[16 * kStageStride];
     const int64_t st = blockIdx.x / t.G, g = blockIdx.x % t.G, c0 = g * 4;
     const int tid = threadIdx.x;
+    const int64_t u = st * t.G + g;
+    int64_t p0 = 0, p1 = 0;
+    uint32_t ent0 = 0u;
+    if constexpr (!kVerify) {
+        escape_range(t.esc_ptr, u, t.n_esc, p0, p1);
+        if (p0 + tid < p1) ent0 = t.esc[p0 + tid];
+    }
     {
         const int ct = tid >> 6, h = (tid >> 5) & 1, L = tid & 31;
         const int64_t c = c0 + ct;
@@ -913,18 +927,16 @@ __global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__
     // range, keys strictly increasing
     int sbad = 0;
     {
-        const int64_t u = st * t.G + g;
-        int64_t p0, p1;
-        escape_range(t.esc_ptr, u, t.n_esc, p0, p1);
+        if constexpr (kVerify) escape_range(t.esc_ptr, u, t.n_esc, p0, p1);
         for (int64_t e = p0 + tid; e < p1; e += blockDim.x) {
-            const uint32_t ent = t.esc[e];
+            const uint32_t ent = (!kVerify && e == p0 + tid) ? ent0 : t.esc[e];
             const int key = (int)(ent >> 16);
             const int r = (key >> 6) & 15, col = 64 * (key >> 10) + (key & 63);
             const bool in = key < 4096 && st * 16 + r < t.N && g * 256 + col < t.K;
             if (in) stage[r * kStageStride + col] = (uint16_t)(ent & 0xFFFFu);
-            if (W_cmp != nullptr) sbad += (!in) + (e + 1 < p1 && (int)(t.esc[e + 1] >> 16) <= key);
+            if (kVerify) sbad += (!in) + (e + 1 < p1 && (int)(t.esc[e + 1] >> 16) <= key);
         }
-        if (W_cmp != nullptr && tid == 0) {
+        if (kVerify && tid == 0) {
             const int32_t a = t.esc_ptr[u], b = t.esc_ptr[u + 1];
             sbad += (b < a) + (u == 0 && a != 0) + (u + 1 == (t.Np / 16) * t.G && (int64_t)b != t.n_esc);
         }
@@ -936,7 +948,7 @@ __global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__
     if (n < t.N && k < t.K) {
         const uint16_t *src = stage + r * kStageStride + cc;
         const bool full = k + 16 <= t.K;
-        if (W_cmp == nullptr) {
+        if constexpr (!kVerify) {
             uint16_t *dst = out + n * ldo + k;
             if (full && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
                 reinterpret_cast<uint4 *>(dst)[0] = reinterpret_cast<const uint4 *>(src)[0];
@@ -958,7 +970,7 @@ __global__ __launch_bounds__(256) void k_decode_group(TensorView t, uint16_t *__
             }
         }
     }
-    if (W_cmp != nullptr) {
+    if constexpr (kVerify) {
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
             bad += __shfl_xor_sync(kFull, bad, o);
@@ -1037,7 +1049,7 @@ bool encode_timed_out(int32_t total) { return total == kEncTimeout; }
 cudaError_t launch_decode(const TensorView &t, uint16_t *out, int64_t ldo, cudaStream_t s) {
     const int64_t blocks = (t.Np / 16) * t.G;
     if (blocks == 0) return cudaSuccess;
-    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, out, ldo, nullptr, 0, nullptr, nullptr);
+    k_decode_group<false><<<(unsigned)blocks, 256, 0, s>>>(t, out, ldo, nullptr, 0, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -1045,7 +1057,7 @@ cudaError_t launch_verify(const TensorView &t, const uint16_t *W, int64_t ldw, u
                           unsigned long long *count, cudaStream_t s) {
     const int64_t blocks = (t.Np / 16) * t.G;
     if (blocks == 0) return cudaSuccess;
-    k_decode_group<<<(unsigned)blocks, 256, 0, s>>>(t, nullptr, 0, W, ldw, structure_bad, count);
+    k_decode_group<true><<<(unsigned)blocks, 256, 0, s>>>(t, nullptr, 0, W, ldw, structure_bad, count);
     return cudaGetLastError();
 }
 
