@@ -7,8 +7,8 @@ down 17408->5120).
 
 One step = the four layer GEMMs at each of M = 1, 2, 4, 8: four independent
 requests, each a chain of its four layer GEMMs (16 w12_gemm calls; a request's
-chain runs on its own stream, its GEMMs chained by programmatic dependent
-launch; STEP_FORM).  The same GEMMs as one chain on one stream, and as one
+chain runs in order on its own stream, every GEMM's grid capped at half the
+SMs so that two requests' GEMMs share the GPU; STEP_FORM).  The same GEMMs as one chain on one stream, and as one
 w12_gemm_list call, each GEMM reading its activations after the previous one
 has completed, are timed beside it.  Weights resident in HBM as W12,
 synthetic BF16 activations.  The per-step working set (4 x 496 MB of W12) is
@@ -245,17 +245,29 @@ def run_gpu(args):
     # workspace of its own), so a GEMM of one request can take over the SMs
     # another request's GEMM is draining.  The streams fork from and join back
     # into `stream` every step, so events on `stream` bracket whole steps.
+    # Each GEMM's grid is capped at half the SMs (max_ctas; the result is
+    # bitwise the same on every grid), so two requests' GEMMs run side by side
+    # and each one's start and tail overlap the other's work; these launches
+    # go without programmatic dependent launch, which let a request's next
+    # GEMM make its blocks resident early and hold SMs that another request's
+    # GEMM could use (4.78-4.95 TB/s, depending on what had run before).
+    # Measured on a GB300 (TB/s), caps without that overlap: 64: 4.73, 72: 4.85,
+    # 76: 5.05, 80: 5.07, 88: 5.03; the full grid with it: 4.81 (reported
+    # beside the headline as `calls_full_grid`).
     ws_bytes = max(w12.w12_gemm_workspace_bytes(M, t.N, t.K) for M in M_VALUES for _, t in layers)
+    half_grid = max(1, torch.cuda.get_device_properties(dev).multi_processor_count // 2)
 
     class RequestStreams:
-        def __init__(self, main, a_of, o_of):
+        def __init__(self, main, a_of, o_of, max_ctas=half_grid):
             self.main = main
             self.streams = [torch.cuda.Stream(dev) for _ in M_VALUES]
             self.fork = torch.cuda.Event()
             self.joins = [torch.cuda.Event() for _ in M_VALUES]
             # one workspace per request: its chain's GEMMs run one after another
             self.ws = [w12.Workspace(dev, ws_bytes) for _ in M_VALUES]
-            self.calls = [[w12.GemmCall(a_of[(M, name)], t, o_of[(M, name)], ws, stream=st, opts=overlap)
+            flags = 0 if max_ctas else w12.W12_GEMM_OVERLAP_PREVIOUS
+            opts = w12.make_opts(max_ctas=max_ctas, flags=flags)
+            self.calls = [[w12.GemmCall(a_of[(M, name)], t, o_of[(M, name)], ws, stream=st, opts=opts)
                            for name, t in layers]
                           for M, st, ws in zip(M_VALUES, self.streams, self.ws)]
 
@@ -271,6 +283,7 @@ def run_gpu(args):
                 self.main.wait_event(ev)
 
     streams_step = RequestStreams(stream, acts, outs)
+    full_grid_step = RequestStreams(stream, acts, outs, max_ctas=0)
 
     # The step as one w12_gemm_list call: the 16 GEMMs in one persistent
     # launch, each reading its activations only after the GEMM before it has
@@ -291,8 +304,9 @@ def run_gpu(args):
     # Both forms of the step are timed over the same number of steps; the
     # headline `value` is STEP_FORM's, the other is reported beside it.
     forms = {"calls": (streams_step, len(step_keys), "k_gemm_mma<1> (w12_gemm, M<=8)",
-                       "16 w12_gemm calls: each request's (M's) four layer GEMMs chained by programmatic "
-                       "dependent launch on a stream of its own, the four requests' streams concurrent"),
+                       "16 w12_gemm calls: each request's (M's) four layer GEMMs in order on a stream of its "
+                       f"own, the four requests' streams concurrent, every GEMM's grid capped at half the SMs "
+                       f"(max_ctas {half_grid}) so two requests' GEMMs share the GPU"),
              "list": (list_call, 1, "k_gemm_mma_list<1> (w12_gemm_list, M<=8)",
                       "one w12_gemm_list call over the 16 GEMMs, listed layer by layer with the four requests "
                       "side by side; each of a request's later layers reads its activations after the request's "
@@ -306,6 +320,7 @@ def run_gpu(args):
     for _ in range(args.warmup):
         one_step()
         other_step()
+        full_grid_step()
     torch.cuda.synchronize()
     # the list's outputs are bitwise those of the 16 separate calls
     list_out = {k: outs[k].clone() for k in step_keys}
@@ -347,6 +362,13 @@ def run_gpu(args):
     c1.record(stream)
     torch.cuda.synchronize()
     chain_ms = c0.elapsed_time(c1) / args.steps
+    # ... and the four streams with every GEMM on the full grid
+    c0.record(stream)
+    for k in range(args.steps):
+        full_grid_step()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    full_grid_ms = c0.elapsed_time(c1) / args.steps
 
     # Per-launch events of the 16-call step on 10 more steps: an event
     # between two launches keeps the second from overlapping the first, so
@@ -790,6 +812,8 @@ def run_gpu(args):
         "config": {"workload": "27B-class decoder layer GEMMs (QKV 7168x5120, O 5120x5120, gate/up "
                                "34816x5120, down 5120x17408), M in {1,2,4,8}, W12 weights resident",
                    "global_batch": list(M_VALUES), "parallelism": f"replica x{ws_n} (N-sharding not needed)",
+                   "grid": f"each GEMM of the step capped at {half_grid} CTAs (half the SMs; max_ctas), "
+                           "four request streams, no programmatic dependent launch",
                    "l2": "inputs larger than L2 (4 x 496 MB W12 per step; the requests share the layer tensors, "
                          "and distinct copies per request measured 0.2% slower: no reuse through L2)",
                    "bits_per_weight": round(sum(t.nbytes() for _, t in layers) * 8 /
@@ -815,6 +839,10 @@ def run_gpu(args):
                                            "ms_per_step": round(chain_ms, 4),
                                            "note": "the 16 w12_gemm calls as one chain on one stream (every GEMM "
                                                    "after the one before it, the requests serialised)"},
+                      "calls_full_grid": {"value": round(step_bytes / (full_grid_ms * 1e-3) / 1e9, 1),
+                                          "unit": "GB/s", "ms_per_step": round(full_grid_ms, 4),
+                                          "note": "the four request streams with every GEMM on the full grid, "
+                                                  "chained by programmatic dependent launch"},
                       "list_matches_calls_bitwise": list_matches_calls},
         "roofline_by_m": roofline_by_m,
         "value_graph": {"value": round(value_graph, 1), "unit": "GB/s",
