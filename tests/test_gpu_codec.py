@@ -226,8 +226,9 @@ def test_full_size_gate_up_encode_matches_oracle_on_sampled_stripes(w12lib, orac
                          [("stress", 5121, 17400, 4)])
 def test_full_size_encode_bytes_match_the_oracle_on_sampled_stripes(name, N, K, seed, w12lib, oracle):
     """The 27B-class layers (and the escape-stress shape) encoded on the GPU
-    at full size, so the window, scan and pack kernels run their multi-block
-    grids; then sampled 16-row stripes (first, last, and random ones) are
+    at full size, so the window kernel and the pack kernel (with its segmented
+    offset scan) run their multi-block grids; then sampled 16-row stripes
+    (first, last, and random ones) are
     compared byte for byte with the oracle's encoding of the same rows: hi and
     lo planes, bases, group offsets (rebased to the stripe) and escapes."""
     if name == "stress":
