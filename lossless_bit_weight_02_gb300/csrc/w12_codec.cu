@@ -40,7 +40,6 @@ __device__ __forceinline__ uint4 load8w(const uint16_t *row, bool vec, int64_t k
 __device__ __forceinline__ uint32_t window_c2(uint32_t b) { return 0x80008000u - b * 0x00800080u; }
 __device__ __forceinline__ uint32_t window_word(uint32_t x, uint32_t c2) { return (x & 0x7FFF7FFFu) + c2; }
 __device__ __forceinline__ uint32_t escape_bits(uint32_t d) { return (d & 0xF800F800u) ^ 0x80008000u; }
-__device__ __forceinline__ int halves_set(uint32_t e) { return ((e & 0xFFFFu) != 0u) + ((e >> 16) != 0u); }
 
 // ---------------------------------------------------------------------------
 // a1: the window search, one of two kernels by row length.  Both build the
@@ -729,7 +728,6 @@ __global__ __launch_bounds__(kPackWarps * 32, 3) void k_pack(const uint16_t *__r
     __shared__ int32_t redo[kPackRedo];
     __shared__ int n_redo;
     __shared__ LookbackSmem lb;
-    __shared__ long long sE;
     __shared__ int sync_ok;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int NT = kPackWarps * 32;
@@ -1041,7 +1039,15 @@ cudaError_t launch_encode(const uint16_t *W, int64_t ldw, int64_t N, int64_t K, 
     void *args[] = {(void *)&W, (void *)&ldw, (void *)&N, (void *)&K, (void *)&cbase, (void *)&esc_ptr,
                     (void *)&hi, (void *)&lo, (void *)&esc, (void *)&esc_cap, (void *)&P, (void *)&G,
                     (void *)&total, (void *)&stall};
-    return cudaLaunchCooperativeKernel((const void *)k_pack, dim3((unsigned)B), dim3(kPackWarps * 32), args, 0, s);
+    // every block must be resident at once: with fewer SMs free than the
+    // occupancy query saw (another context, a partitioned device), fewer
+    // blocks (longer segments) give the same result
+    for (;;) {
+        e = cudaLaunchCooperativeKernel((const void *)k_pack, dim3((unsigned)B), dim3(kPackWarps * 32), args, 0, s);
+        if (e != cudaErrorCooperativeLaunchTooLarge || B == 1) return e;
+        (void)cudaGetLastError();  // clear the launch error before the retry
+        B = (B + 1) / 2;
+    }
 }
 
 bool encode_timed_out(int32_t total) { return total == kEncTimeout; }
