@@ -316,3 +316,39 @@ def test_encode_odd_row_strides(N, K, pad, w12lib, oracle):
     assert g["n_esc"] == ref.n_esc
     for key in ("hi", "lo", "base", "esc_ptr", "esc"):
         assert np.array_equal(g[key], getattr(ref, key)), key
+
+
+def test_concurrent_encodes_from_two_threads(w12lib, oracle):
+    """Two host threads encode different tensors at once, each on a stream of
+    its own (the C call runs without the GIL): each gets its own escape-count
+    word and cached launch state, and both results equal the oracle's bytes."""
+    import threading
+    shapes = [(96, 1300, 61), (80, 2100, 62)]
+    Ws = [synth.adversarial_weights(N, K, seed=s) for N, K, s in shapes]
+    Wds = [synth.bits_to_tensor(W, "cuda") for W in Ws]
+    out = [None, None]
+    errors = []
+
+    def run(i):
+        try:
+            st = torch.cuda.Stream()
+            for _ in range(20):
+                t = w12lib.w12_encode(Wds[i], stream=st)
+            st.synchronize()
+            out[i] = t
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for i, W in enumerate(Ws):
+        st, ref = oracle.encode(W)
+        g = host_view(out[i])
+        assert g["n_esc"] == ref.n_esc
+        for key in ("hi", "lo", "base", "esc_ptr"):
+            assert np.array_equal(g[key], getattr(ref, key)), (i, key)
+        assert np.array_equal(g["esc"], ref.esc[:ref.n_esc]), i
