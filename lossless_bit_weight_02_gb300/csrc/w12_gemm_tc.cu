@@ -1398,15 +1398,18 @@ size_t tc_smem_bytes(const TcParams &tp) {
 // with two, half of the SM's 228 KB less the 1 KB each CTA reserves.
 size_t tc_smem_budget(int ctas_per_sm) { return ctas_per_sm > 1 ? 227 * 1024 / 2 - 1024 : 227 * 1024; }
 
-// Ring depths within the shared-memory budget: about 48 KB (24 KB with two
-// CTAs per SM) of activation stages (at least 2), 3 (2) decoded-A stages,
-// and the rest for weight stages: the weight ring is what keeps HBM busy (a
-// k-block's planes take a few microseconds to arrive under load).  Returns
-// false if not even two weight stages fit.
+// Ring depths within the shared-memory budget: about 96 KB (24 KB with two
+// CTAs per SM) of activation stages (2 to 6), 3 (2) decoded-A stages, and
+// the rest for weight stages: the weight ring is what keeps HBM busy (a
+// k-block's planes take a few microseconds to arrive under load).  An
+// activation stage is freed only when its k-block's MMAs complete, so at
+// Mp = 256 (32 KB a stage) two stages left the MMAs waiting on the refill
+// from L2: three ran the four layers 9% faster, six weight stages still
+// enough.  Returns false if not even two weight stages fit.
 bool tc_rings(TcParams &tp, int ctas_per_sm) {
     const size_t budget = tc_smem_budget(ctas_per_sm);
     const size_t bst = (size_t)tp.Mp * 128;
-    tp.b_st = (int)((ctas_per_sm > 1 ? 24 : 48) * 1024 / bst);
+    tp.b_st = (int)((ctas_per_sm > 1 ? 24 : 96) * 1024 / bst);
     tp.b_st = tp.b_st < 2 ? 2 : (tp.b_st > 6 ? 6 : tp.b_st);
     tp.a_st = ctas_per_sm > 1 ? 2 : 3;
     tp.w_st = 0;
@@ -1427,9 +1430,13 @@ bool tc_rings(TcParams &tp, int ctas_per_sm) {
 // about half the weight bytes (1.5*N*K); at these sizes they live in L2.
 // (A cap of 0.0375*K/Mpad left QKV and O at M = 128 with 40-56 CTAs; on
 // GB300 0.1 ran M = 128 and 256 13-17% faster and M <= 64 the same.)
+// Above Mpad = 128 a CTA's k-blocks are paced by its MMAs rather than by
+// its bytes, and the cap is 0.15*K/Mpad: O at M = 256 then runs 120 CTAs
+// instead of 80, 12% faster (0.15 for every Mpad made QKV at M = 128
+// slower).
 int64_t tc_split_for(int64_t T, int64_t G, int64_t Mp, int64_t K, int64_t slots) {
     int64_t S = slots / T;
-    const int64_t traffic_cap = (int64_t)(0.1 * (double)K / (double)Mp);
+    const int64_t traffic_cap = (int64_t)((Mp > 128 ? 0.15 : 0.1) * (double)K / (double)Mp);
     if (S > traffic_cap) S = traffic_cap;
     if (S > G) S = G;
     if (S > 16) S = 16;

@@ -94,7 +94,7 @@ def tc_split(w12lib, M, N, K, opts=None):
     (24, 7168, 5120, 5),    # 56 row tiles x 5 = 280 CTAs: two CTAs per SM
     (64, 7168, 5120, 5),
     (128, 7168, 5120, 2),   # 56 x 4 (partial-traffic cap 4) = 224 < 258: one CTA per SM, 152/56 = 2
-    (256, 5120, 5120, 2),   # Mpad > 128; the cap (2) binds: 152/40 = 3
+    (256, 5120, 5120, 3),   # Mpad > 128: 152/40 = 3 (cap 0.15*5120/256 = 3; 0.1 would give 2)
     (128, 5120, 2048, 1),   # cap 1.6
     (64, 34816, 5120, 1),   # 272 row tiles fill two CTAs per SM without a split
     (24, 5120, 17408, 7),   # 40 x 7 = 280
@@ -106,7 +106,8 @@ def tc_split(w12lib, M, N, K, opts=None):
 def test_tc_split_rule(M, N, K, S, w12lib):
     """The split (and with it the build) depends on (M, N, K) only: S chunks over 2 x 152
     slots when that grid has >= 258 CTAs and Mpad <= 128, else over 152 slots; each
-    capped by the column groups, 16, and the partial traffic 0.1*K/Mpad."""
+    capped by the column groups, 16, and the partial traffic 0.1*K/Mpad (0.15*K/Mpad above
+    Mpad = 128)."""
     assert tc_split(w12lib, M, N, K) == S
 
 
