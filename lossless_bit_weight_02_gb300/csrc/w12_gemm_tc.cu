@@ -1399,19 +1399,21 @@ size_t tc_smem_bytes(const TcParams &tp) {
 size_t tc_smem_budget(int ctas_per_sm) { return ctas_per_sm > 1 ? 227 * 1024 / 2 - 1024 : 227 * 1024; }
 
 // Ring depths within the shared-memory budget: about 96 KB (24 KB with two
-// CTAs per SM) of activation stages (2 to 6), 3 (2) decoded-A stages, and
-// the rest for weight stages: the weight ring is what keeps HBM busy (a
-// k-block's planes take a few microseconds to arrive under load).  An
-// activation stage is freed only when its k-block's MMAs complete, so at
-// Mp = 256 (32 KB a stage) two stages left the MMAs waiting on the refill
-// from L2: three ran the four layers 9% faster, six weight stages still
-// enough.  Returns false if not even two weight stages fit.
+// CTAs per SM) of activation stages (2 to 6); 3 decoded-A stages (4 above
+// Mp = 128, 2 with two CTAs per SM); and the rest for weight stages: the
+// weight ring is what keeps HBM busy (a k-block's planes take a few
+// microseconds to arrive under load).  An activation stage is freed only
+// when its k-block's MMAs complete, so at Mp = 256 (32 KB a stage) two
+// stages left the MMAs waiting on the refill from L2: three ran the four
+// layers 10% faster, and a fourth decoded-A stage another 2.5% (five weight
+// stages are still enough there).  Returns false if not even two weight
+// stages fit.
 bool tc_rings(TcParams &tp, int ctas_per_sm) {
     const size_t budget = tc_smem_budget(ctas_per_sm);
     const size_t bst = (size_t)tp.Mp * 128;
     tp.b_st = (int)((ctas_per_sm > 1 ? 24 : 96) * 1024 / bst);
     tp.b_st = tp.b_st < 2 ? 2 : (tp.b_st > 6 ? 6 : tp.b_st);
-    tp.a_st = ctas_per_sm > 1 ? 2 : 3;
+    tp.a_st = ctas_per_sm > 1 ? 2 : (tp.Mp > 128 ? 4 : 3);
     tp.w_st = 0;
     for (int w = kMaxStages; w >= 2; --w) {
         TcParams x = tp;
