@@ -275,9 +275,11 @@ def run_gpu(args):
             self.fork.record(self.main)
             for st in self.streams:
                 st.wait_event(self.fork)
-            for chain in self.calls:
-                for c in chain:
-                    c()
+            # enqueued layer by layer across the requests' streams (0.3% faster
+            # on a GB300 than request by request; stream priorities were slower)
+            for li in range(len(layers)):
+                for chain in self.calls:
+                    chain[li]()
             for st, ev in zip(self.streams, self.joins):
                 ev.record(st)
                 self.main.wait_event(ev)
