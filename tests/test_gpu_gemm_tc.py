@@ -31,7 +31,9 @@ def parity(w12lib, oracle, W, A, opts=None, reps=1):
     return outs[0]
 
 
-@pytest.mark.parametrize("M", [17, 24, 32, 33, 48, 63, 64, 128, 200, 256])
+# M > 128 spans the one-CTA build's ring depths (Mpad 144: 5 activation stages, 176-192: 4,
+# 208-256: 3; four decoded-A stages)
+@pytest.mark.parametrize("M", [17, 24, 32, 33, 48, 63, 64, 128, 136, 168, 184, 200, 232, 256])
 def test_tc_dense_1024(M, w12lib, oracle):
     W = synth.dense_weights(1024, 1024, seed=0)
     A = synth.activations(M, 1024, seed=3000 + M)
@@ -91,6 +93,15 @@ def test_tc_both_builds(M, split, kind, w12lib, oracle):
 def test_tc_balanced_ranges(N, K, M, kind, w12lib, oracle):
     W = (synth.dense_weights if kind == "dense" else synth.adversarial_weights)(N, K, seed=N + M)
     A = synth.activations(M, K, seed=3600 + M)
+    parity(w12lib, oracle, W, A, reps=2)
+
+
+@pytest.mark.parametrize("M", [200, 256])
+def test_tc_automatic_split_above_128(M, w12lib, oracle):
+    """8 row tiles, K = 8192: above Mpad = 128 the automatic split is capped at 0.15*K/Mpad
+    (5 chunks at M = 200, 4 at M = 256), summed in chunk order."""
+    W = synth.dense_weights(1024, 8192, seed=7)
+    A = synth.activations(M, 8192, seed=3700 + M)
     parity(w12lib, oracle, W, A, reps=2)
 
 
