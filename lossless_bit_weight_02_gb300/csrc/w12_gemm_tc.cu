@@ -1432,10 +1432,9 @@ bool tc_rings(TcParams &tp, int ctas_per_sm) {
 // about half the weight bytes (1.5*N*K); at these sizes they live in L2.
 // (A cap of 0.0375*K/Mpad left QKV and O at M = 128 with 40-56 CTAs; on
 // GB300 0.1 ran M = 128 and 256 13-17% faster and M <= 64 the same.)
-// Above Mpad = 128 a CTA's k-blocks are paced by its MMAs rather than by
-// its bytes, and the cap is 0.15*K/Mpad: O at M = 256 then runs 120 CTAs
-// instead of 80, 12% faster (0.15 for every Mpad made QKV at M = 128
-// slower).
+// Above Mpad = 128 the cap is 0.15*K/Mpad, as measured on GB300: O at
+// M = 256 then runs 120 CTAs instead of 80, 12% faster (0.15 for every Mpad
+// made QKV at M = 128 slower).
 int64_t tc_split_for(int64_t T, int64_t G, int64_t Mp, int64_t K, int64_t slots) {
     int64_t S = slots / T;
     const int64_t traffic_cap = (int64_t)((Mp > 128 ? 0.15 : 0.1) * (double)K / (double)Mp);
